@@ -1,0 +1,349 @@
+"""Throughput of the DP-SGD clipping path: per-example norms -> clip factors ->
+clipped sum -> Gaussian noise and 1/B, on synthetic inputs resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-cpu-baseline]
+
+Prints ONE JSON line on rank 0.  A step is one pass of the whole path over one
+batch.  N > 1 (under torchrun) runs independent replicas, one per GPU, each on
+its own batch: the path has no data exchange between replicas, so scaling is
+weak and there is no collective in the timed work (a barrier brackets it).
+`--impl reference` times the float64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "examples/sec through norm+clip+noisy-sum per config; % of TC/HBM roofline"
+DEFAULT_WORKLOAD = "seq_linear_b64_t128"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def layer_desc(dp, spec, B, dtype):
+    dt = dp.DP_BF16 if dtype == "bf16" else dp.DP_FP32
+    if spec.kind == "linear":
+        return dp.layer_desc(dp.DP_LINEAR, dt, B=B, p=spec.p, T=spec.T, d=spec.d, has_bias=spec.has_bias)
+    return dp.layer_desc(dp.DP_CONV2D, dt, B=B, p=spec.p, Cin=spec.Cin, H=spec.H, W=spec.W, k=spec.k,
+                         stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
+
+
+def step_work(wl, modes):
+    """Algorithmic FLOPs and bytes of one step, from the per-module complexity counts
+    of the mixed-ghost paper (Appendix C): ghost norm 2T^2(D+p) + 2T^2 per example,
+    instantiation 2TpD + 2pD, one-row norm 2(D+p), clipped sum 2TpD.  Bytes: the
+    inputs read once by the norm pass and once by the sum pass, the fp32 gradient
+    written once, and the noise pass reading and writing it."""
+    es = 2 if wl.dtype == "bf16" else 4
+    flop_norm = flop_sum = 0.0
+    in_bytes = 0
+    for spec, m in zip(wl.layers, modes):
+        T, D, p = spec.rows, spec.D, spec.p
+        if m == "ghost":
+            flop_norm += wl.B * (2.0 * T * T * (D + p) + 2.0 * T * T)
+        elif m == "instantiate":
+            flop_norm += wl.B * (2.0 * T * p * D + 2.0 * p * D)
+        else:
+            flop_norm += wl.B * 2.0 * (D + p)
+        flop_sum += wl.B * 2.0 * T * p * D
+        a_el = spec.T * spec.d if spec.kind == "linear" else spec.Cin * spec.H * spec.W
+        g_el = spec.T * spec.p if spec.kind == "linear" else spec.p * spec.Hout * spec.Wout
+        in_bytes += wl.B * (a_el + g_el) * es
+    n = wl.n_params
+    return dict(flop_norm=flop_norm, flop_sum=flop_sum, in_bytes=in_bytes,
+                bytes_total=2 * in_bytes + 4 * n + 8 * n, n_params=n)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(wl, inputs, budget_s: float = 12.0):
+    """Time the float64 CPU oracle (as it stands) on full batches of the workload."""
+    import oracle
+    t0 = time.perf_counter()
+    runs = 0
+    while True:
+        oracle.dp_step(wl, inputs, seed=wl.seed + runs)
+        runs += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return dict(value=wl.B * runs / dt, unit="examples/s", cores=_cores(), kind="oracle",
+                sample=f"{runs} full batch(es) of {wl.name} (B={wl.B}), float64 numpy, {dt:.1f} s")
+
+
+def _cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, wl):
+    import workloads
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    import oracle
+    inputs = [workloads.layer_inputs(wl, l) for l in range(len(wl.layers))]
+    for w in range(args.warmup):
+        oracle.dp_step(wl, inputs, seed=wl.seed + w)
+    times = []
+    for k in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.dp_step(wl, inputs, seed=wl.seed + 1000 + k)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = wl.B * args.steps / tot
+    cores = _cores()
+    line = dict(metric=METRIC, value=value, unit="examples/s", n_gpus=args.gpus, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * tot / args.steps, higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=_config(wl), e2e={"value": value, "unit": "examples/s", "h2d_bytes_per_step": 0,
+                                         "d2h_bytes_per_step": 0},
+                cpu_baseline=dict(value=value, unit="examples/s", cores=cores, kind="oracle",
+                                  sample=f"{args.steps} full batches of {wl.name} (B={wl.B}), float64 numpy"))
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl, extra=None):
+    c = dict(workload=wl.name, B=wl.B, dtype=wl.dtype, C=wl.C, sigma=wl.sigma,
+             clipping="per-layer" if wl.per_layer else "flat",
+             layers=[dict(kind=s.kind, T=s.rows, D=s.D, p=s.p) for s in wl.layers],
+             l2="flushed between timed steps (256 MiB write)", description=wl.description)
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_ours(args, wl):
+    import torch
+    import workloads
+    import example_gradient_clipping_gb300 as dp
+    world, rank, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    descs = [layer_desc(dp, s, wl.B, wl.dtype) for s in wl.layers]
+    step = dp.ClipStep(descs, C=wl.C, sigma=wl.sigma, per_layer=wl.per_layer, device=str(dev))
+    host_in = [workloads.layer_inputs(wl, l, threads=8) for l in range(len(wl.layers))]
+    dev_in = [(workloads.to_torch(A, wl.dtype, str(dev)), workloads.to_torch(G, wl.dtype, str(dev)))
+              for A, G in host_in]
+    modes = [dp.MODE_NAMES[m] for m, _, _ in step.plan]
+    work = step_work(wl, modes)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # events around each C-ABI call of the step, on the launching stream
+    names = ["norms", "factors", "sums", "noise"]
+
+    def one_step(k, evs=None):
+        seed = wl.seed + 1_000_003 * (rank + 1) + k
+        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
+        rec(0)
+        step.norms(dev_in)
+        rec(1)
+        step.factors_()
+        rec(2)
+        step.sums(dev_in)
+        rec(3)
+        step.noise(seed)
+        rec(4)
+
+    for w in range(max(args.warmup, 3)):
+        flush.zero_()
+        one_step(-1 - w)
+    torch.cuda.synchronize()
+
+    all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    launches0 = dp.dp_launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for k in range(args.steps):
+            flush.zero_()           # L2 flush outside the events
+            one_step(k, all_evs[k])
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = dp.dp_launch_count() - launches0
+    per_call = {n: [all_evs[k][i].elapsed_time(all_evs[k][i + 1]) for k in range(args.steps)]
+                for i, n in enumerate(names)}
+    step_ms = [all_evs[k][0].elapsed_time(all_evs[k][4]) for k in range(args.steps)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * wl.B * args.steps / (total_ms / 1e3)
+
+    # end to end through the public API: pinned host inputs copied in, result copied out
+    pinned = [(workloads.to_torch(A, wl.dtype).pin_memory(), workloads.to_torch(G, wl.dtype).pin_memory())
+              for A, G in host_in]
+    out_host = torch.empty(step.n_params, dtype=torch.float32).pin_memory()
+    h2d = sum(a.numel() * a.element_size() + g.numel() * g.element_size() for a, g in pinned)
+    d2h = out_host.numel() * 4
+    e2e_ms = []
+    for k in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for (ha, hg), (da, dg) in zip(pinned, dev_in):
+            da.copy_(ha, non_blocking=True)
+            dg.copy_(hg, non_blocking=True)
+        g = step.run(dev_in, seed=wl.seed + 7 * k)
+        out_host.copy_(g, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if k >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_tot = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_tot], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_tot = float(t.item())
+    e2e_value = world * wl.B * args.steps / (e2e_tot / 1e3)
+
+    # roofline of the dominant call
+    pk = _peaks()
+    means = {n: statistics.mean(v) for n, v in per_call.items()}
+    dom = max(means, key=means.get)
+    if dom == "sums":
+        roof = dict(bound="tensor", achieved=work["flop_sum"] / (means["sums"] * 1e-3) / 1e12,
+                    peak=pk["bf16"], unit="TFLOP/s")
+    elif dom == "norms":
+        roof = dict(bound="tensor", achieved=work["flop_norm"] / (means["norms"] * 1e-3) / 1e12,
+                    peak=pk["bf16"], unit="TFLOP/s")
+    else:
+        nb = 8 * work["n_params"]
+        roof = dict(bound="hbm", achieved=nb / (means[dom] * 1e-3) / 1e9, peak=pk["hbm"], unit="GB/s")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = {"sums": "dp_clipped_sum", "norms": "dp_layer_sqnorms", "noise": "dp_add_noise",
+                      "factors": "dp_clip_factors"}[dom]
+    roof["peak_source"] = f"{pk['src']} (burst)"
+
+    line = None
+    if rank == 0:
+        line = dict(metric=METRIC, value=value, unit="examples/s", n_gpus=world, steps=args.steps,
+                    warmup=max(args.warmup, 3), ms_per_step=total_ms / args.steps, higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype=wl.dtype, data="synthetic",
+                    config=_config(wl, dict(norm_modes=modes, parallelism=f"replicas x{world}")),
+                    e2e=dict(value=e2e_value, unit="examples/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+                    gpu_launches=int(launches), roofline=roof, clocks=clk.summary(),
+                    calls_ms={n: round(v, 5) for n, v in means.items()},
+                    step_flop=work["flop_norm"] + work["flop_sum"], step_bytes=work["bytes_total"])
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, host_in)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    import workloads
+    wl = workloads.get_workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

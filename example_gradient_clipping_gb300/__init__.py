@@ -1,0 +1,158 @@
+"""Python binding of libdpclip, DP-SGD per-example gradient clipping on GB300.
+
+Argument marshalling only: every function calls the C entry point of the same
+name (declared in include/dpclip.h) with raw device pointers and the current CUDA
+stream.  Tensors may be torch tensors (their data_ptr() is passed) or integer
+device addresses.  There is no fallback: importing this package fails if the
+compiled library is missing, and every non-DP_OK status raises DPError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdpclip.so")
+
+DP_OK, DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_CUDA, DP_ERR_NONFINITE, DP_ERR_TIMEOUT = range(6)
+DP_BF16, DP_FP32 = 0, 1
+DP_LINEAR, DP_CONV2D = 0, 1
+DP_NORM_AUTO, DP_NORM_GHOST, DP_NORM_INSTANTIATE, DP_NORM_T1 = 0, 1, 2, 3
+MODE_NAMES = {DP_NORM_GHOST: "ghost", DP_NORM_INSTANTIATE: "instantiate", DP_NORM_T1: "t1"}
+
+
+class DPError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"dpclip status {status}: {message}")
+        self.status = status
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("kind", "dtype", "B", "T", "d", "p", "Cin", "H", "W", "k", "stride", "pad", "dil",
+                 "has_bias")]
+
+
+def layer_desc(kind: int, dtype: int, B: int, p: int, T: int = 1, d: int = 0, Cin: int = 0,
+               H: int = 0, W: int = 0, k: int = 1, stride: int = 1, pad: int = 0, dil: int = 1,
+               has_bias: bool = True) -> LayerDesc:
+    return LayerDesc(kind, dtype, B, T, d, p, Cin, H, W, k, stride, pad, dil, int(bool(has_bias)))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built (run example_gradient_clipping_gb300.build.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    c_int, c_size, c_void, c_f, c_u64 = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float, ctypes.c_uint64
+    PD = ctypes.POINTER(LayerDesc)
+    PI = ctypes.POINTER(c_int)
+    sig = {
+        "dp_abi_version": (c_int, []),
+        "dp_launch_count": (ctypes.c_ulonglong, []),
+        "dp_last_error": (ctypes.c_char_p, []),
+        "dp_plan": (c_int, [PD, c_int, PI, PI, PI]),
+        "dp_workspace_size": (c_size, [PD, c_int]),
+        "dp_layer_sqnorms": (c_int, [PD, c_void, c_void, c_int, c_void, PI, c_void, c_size, c_void]),
+        "dp_clip_factors": (c_int, [c_void, c_int, c_int, c_int, ctypes.POINTER(c_f), c_void, c_void]),
+        "dp_clipped_sum": (c_int, [PD, c_void, c_void, c_void, c_void, c_void, c_int, c_void, c_size, c_void]),
+        "dp_add_noise": (c_int, [c_void, c_size, c_f, c_f, c_int, c_u64, c_u64, c_void]),
+        "dp_adaptive_bound": (c_int, [c_void, c_int, c_f, c_f, c_f, c_f, c_u64, c_int, c_void, c_void]),
+        "dp_check_status": (c_int, [c_void]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    return lib
+
+
+_lib = _load()
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _check(status: int) -> None:
+    if status != DP_OK:
+        raise DPError(status, _lib.dp_last_error().decode())
+
+
+def dp_abi_version() -> int:
+    return _lib.dp_abi_version()
+
+
+def dp_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return _lib.dp_launch_count()
+
+
+def dp_plan(desc: LayerDesc, requested: int = DP_NORM_AUTO):
+    """(chosen_mode, T, D) for a layer (host only)."""
+    m, T, D = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(_lib.dp_plan(ctypes.byref(desc), requested, ctypes.byref(m), ctypes.byref(T), ctypes.byref(D)))
+    return m.value, T.value, D.value
+
+
+def dp_workspace_size(desc: LayerDesc, mode: int = DP_NORM_AUTO) -> int:
+    return _lib.dp_workspace_size(ctypes.byref(desc), mode)
+
+
+def dp_layer_sqnorms(desc: LayerDesc, A, G, sqnorm_out, workspace=None, ws_bytes: Optional[int] = None,
+                     mode: int = DP_NORM_AUTO, stream=None) -> int:
+    chosen = ctypes.c_int(-1)
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None and not isinstance(workspace, int) else 0
+    _check(_lib.dp_layer_sqnorms(ctypes.byref(desc), _ptr(A), _ptr(G), mode, _ptr(sqnorm_out),
+                                 ctypes.byref(chosen), _ptr(workspace), ws_bytes, _stream(stream)))
+    return chosen.value
+
+
+def dp_clip_factors(sqnorms, B: int, L: int, per_layer: bool, C: Sequence[float], factors_out,
+                    stream=None) -> None:
+    Cs = list(C) if isinstance(C, (list, tuple)) else [float(C)]
+    arr = (ctypes.c_float * len(Cs))(*Cs)
+    _check(_lib.dp_clip_factors(_ptr(sqnorms), B, L, int(bool(per_layer)), arr, _ptr(factors_out),
+                                _stream(stream)))
+
+
+def dp_clipped_sum(desc: LayerDesc, A, G, factors, dW, db=None, workspace=None,
+                   ws_bytes: Optional[int] = None, accumulate: bool = False, stream=None) -> None:
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None and not isinstance(workspace, int) else 0
+    _check(_lib.dp_clipped_sum(ctypes.byref(desc), _ptr(A), _ptr(G), _ptr(factors), _ptr(dW), _ptr(db),
+                               int(bool(accumulate)), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def dp_add_noise(grad, sigma: float, C: float, B: int, seed: int, offset: int = 0,
+                 n: Optional[int] = None, stream=None) -> None:
+    if n is None:
+        n = grad.numel()
+    _check(_lib.dp_add_noise(_ptr(grad), n, sigma, C, B, seed, offset, _stream(stream)))
+
+
+def dp_adaptive_bound(sqnorms, B: int, C_l2: float, alpha: float, beta: float, sigma_l2: float,
+                      seed: int, layer: int, out, stream=None) -> None:
+    _check(_lib.dp_adaptive_bound(_ptr(sqnorms), B, C_l2, alpha, beta, sigma_l2, seed, layer, _ptr(out),
+                                  _stream(stream)))
+
+
+def dp_check_status(stream=None) -> int:
+    """Synchronizes and returns the device status (DP_OK or the raised code) without raising."""
+    return _lib.dp_check_status(_stream(stream))
+
+
+from .step import ClipStep  # noqa: E402,F401

@@ -1,0 +1,284 @@
+// C ABI of libdpclip: argument validation, the layerwise plan, workspace sizing and
+// launches.  No allocation happens on any of these paths.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+using dpk::Geom;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dp_status fail(dp_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+dp_status ok() { return DP_OK; }
+
+dp_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(DP_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Device status word, one per device (the address is looked up per device).
+__device__ unsigned int g_status_word;
+
+unsigned* status_ptr() {
+  static unsigned* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned*>(p);
+  }
+  return cache[dev];
+}
+
+// Validate a descriptor and resolve the per-example contraction geometry.
+dp_status make_geom(const dp_layer_desc* d, Geom* g) {
+  if (!d) return fail(DP_ERR_INVALID_ARG, "desc is NULL");
+  if (d->dtype != DP_BF16 && d->dtype != DP_FP32)
+    return fail(DP_ERR_INVALID_ARG, "dtype %d is not DP_BF16 or DP_FP32", d->dtype);
+  if (d->B <= 0 || d->p <= 0) return fail(DP_ERR_INVALID_ARG, "B=%d and p=%d must be > 0", d->B, d->p);
+  std::memset(g, 0, sizeof(*g));
+  g->B = d->B;
+  g->p = d->p;
+  g->has_bias = d->has_bias ? 1 : 0;
+  if (d->kind == DP_LINEAR) {
+    if (d->T <= 0 || d->d <= 0)
+      return fail(DP_ERR_INVALID_ARG, "linear layer needs T=%d > 0 and d=%d > 0", d->T, d->d);
+    g->conv = 0;
+    g->T = d->T;
+    g->d = g->D = d->d;
+  } else if (d->kind == DP_CONV2D) {
+    if (d->Cin <= 0 || d->H <= 0 || d->W <= 0 || d->k <= 0 || d->stride <= 0 || d->pad < 0 ||
+        d->dil <= 0)
+      return fail(DP_ERR_INVALID_ARG, "conv2d needs Cin, H, W, k, stride, dil > 0 and pad >= 0");
+    const long Ho = ((long)d->H + 2L * d->pad - (long)d->dil * (d->k - 1) - 1) / d->stride + 1;
+    const long Wo = ((long)d->W + 2L * d->pad - (long)d->dil * (d->k - 1) - 1) / d->stride + 1;
+    if (Ho <= 0 || Wo <= 0) return fail(DP_ERR_INVALID_ARG, "conv2d output is empty");
+    g->conv = 1;
+    g->Cin = d->Cin; g->H = d->H; g->W = d->W; g->k = d->k;
+    g->stride = d->stride; g->pad = d->pad; g->dil = d->dil;
+    g->Hout = (int)Ho; g->Wout = (int)Wo;
+    g->T = (int)(Ho * Wo);
+    g->D = d->Cin * d->k * d->k;
+    g->d = g->D;
+  } else {
+    return fail(DP_ERR_INVALID_ARG, "kind %d is not DP_LINEAR or DP_CONV2D", d->kind);
+  }
+  // element counts must fit the kernels' 32-bit per-example and 64-bit global indexing
+  if ((double)g->T * g->D > 2e9 || (double)g->T * g->p > 2e9 || (double)g->p * g->D > 2e9)
+    return fail(DP_ERR_UNSUPPORTED, "layer too large for one example's 32-bit indexing");
+  return DP_OK;
+}
+
+// Layerwise decision ([MixGhost] section 4, eq. 4.1): ghost norm iff its space 2T^2
+// is below the instantiation space p*D; ties instantiate; one row -> closed form.
+int resolve_mode(const Geom& g, int requested) {
+  if (requested == DP_NORM_T1) return DP_NORM_T1;
+  if (requested == DP_NORM_AUTO) {
+    if (g.T == 1 && !g.conv) return DP_NORM_T1;
+    const double ghost = 2.0 * (double)g.T * (double)g.T;
+    const double inst = (double)g.p * (double)g.D;
+    return ghost < inst ? DP_NORM_GHOST : DP_NORM_INSTANTIATE;
+  }
+  return requested;
+}
+
+size_t sum_ws_bytes(const Geom& g) {
+  if (dph::tc_sum_supported(g)) return dph::tc_sum_ws_bytes(g);
+  const size_t splits = dph::simt_sum_splits(g);
+  return splits * ((size_t)g.p * g.D + g.p) * sizeof(float);
+}
+
+size_t norm_ws_bytes(const Geom& g, int mode) {
+  switch (mode) {
+    case DP_NORM_T1: return 0;
+    case DP_NORM_GHOST:
+      if (dph::tc_ghost_supported(g)) return dph::tc_ghost_ws_bytes(g);
+      return dph::simt_ghost_ws_floats(g) * sizeof(float);
+    case DP_NORM_INSTANTIATE: return dph::simt_inst_ws_floats(g) * sizeof(float);
+  }
+  return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+std::atomic<unsigned long long> g_launches{0};
+
+}  // namespace
+
+namespace dph {
+void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace dph
+
+extern "C" {
+
+unsigned long long dp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+
+int dp_abi_version(void) { return DPCLIP_ABI_VERSION; }
+
+const char* dp_last_error(void) { return g_last_error.c_str(); }
+
+dp_status dp_plan(const dp_layer_desc* desc, int requested, int* chosen_mode, int* rows_T,
+                  int* width_D) {
+  Geom g;
+  dp_status st = make_geom(desc, &g);
+  if (st != DP_OK) return st;
+  if (requested < DP_NORM_AUTO || requested > DP_NORM_T1)
+    return fail(DP_ERR_INVALID_ARG, "norm mode %d unknown", requested);
+  if (requested == DP_NORM_T1 && (g.T != 1 || g.conv))
+    return fail(DP_ERR_INVALID_ARG, "DP_NORM_T1 needs a linear layer with T == 1 (T=%d)", g.T);
+  if (chosen_mode) *chosen_mode = resolve_mode(g, requested);
+  if (rows_T) *rows_T = g.T;
+  if (width_D) *width_D = g.D;
+  return ok();
+}
+
+size_t dp_workspace_size(const dp_layer_desc* desc, int mode) {
+  Geom g;
+  if (make_geom(desc, &g) != DP_OK) return 0;
+  if (mode < DP_NORM_AUTO || mode > DP_NORM_T1) return 0;
+  if (mode == DP_NORM_T1 && (g.T != 1 || g.conv)) return 0;
+  const int m = resolve_mode(g, mode);
+  return std::max(norm_ws_bytes(g, m), sum_ws_bytes(g));
+}
+
+dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void* G, int mode,
+                           float* sqnorm_out, int* chosen_mode_out, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream) {
+  int chosen = 0;
+  dp_status st = dp_plan(desc, mode, &chosen, nullptr, nullptr);
+  if (st != DP_OK) return st;
+  if (!A || !G || !sqnorm_out) return fail(DP_ERR_INVALID_ARG, "A, G and sqnorm_out must be non-NULL");
+  Geom g;
+  make_geom(desc, &g);
+  const size_t need = norm_ws_bytes(g, chosen);
+  if (need && (!workspace || ws_bytes < need))
+    return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  cudaError_t e = cudaSuccess;
+  float* ws = static_cast<float*>(workspace);
+  switch (chosen) {
+    case DP_NORM_T1:
+      e = dph::launch_t1_norm(g, desc->dtype, A, G, sqnorm_out, stream);
+      break;
+    case DP_NORM_GHOST:
+      if (dph::tc_ghost_supported(g) && desc->dtype == DP_BF16 && aligned16(A) && aligned16(G))
+        e = dph::launch_tc_ghost(g, A, G, sqnorm_out, ws, stream);
+      else
+        e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream);
+      break;
+    case DP_NORM_INSTANTIATE:
+      e = dph::launch_simt_inst(g, desc->dtype, A, G, sqnorm_out, ws, stream);
+      break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "dp_layer_sqnorms launch");
+  if (chosen_mode_out) *chosen_mode_out = chosen;
+  return ok();
+}
+
+dp_status dp_clip_factors(const float* sqnorms, int B, int L, int per_layer, const float* C,
+                          float* factors_out, cudaStream_t stream) {
+  if (!sqnorms || !factors_out || !C) return fail(DP_ERR_INVALID_ARG, "NULL pointer argument");
+  if (B <= 0 || L <= 0) return fail(DP_ERR_INVALID_ARG, "B=%d and L=%d must be > 0", B, L);
+  if (per_layer && L > 64)
+    return fail(DP_ERR_UNSUPPORTED, "per-layer clipping supports up to 64 layers per call (L=%d)", L);
+  const int nC = per_layer ? L : 1;
+  for (int l = 0; l < nC; ++l)
+    if (!(C[l] > 0.f) || !std::isfinite(C[l]))
+      return fail(DP_ERR_INVALID_ARG, "bound C[%d]=%g must be finite and > 0", l, (double)C[l]);
+  unsigned* st = status_ptr();
+  if (!st) return fail(DP_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = dph::launch_clip_factors(sqnorms, B, L, per_layer, C, factors_out, st, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_clip_factors launch");
+  return ok();
+}
+
+dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G,
+                         const float* factors, float* dW, float* db, int accumulate,
+                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  Geom g;
+  dp_status st = make_geom(desc, &g);
+  if (st != DP_OK) return st;
+  if (!A || !G || !factors || !dW) return fail(DP_ERR_INVALID_ARG, "A, G, factors and dW must be non-NULL");
+  if (db && !g.has_bias) return fail(DP_ERR_INVALID_ARG, "db given for a layer without bias");
+  const size_t need = sum_ws_bytes(g);
+  if (need && (!workspace || ws_bytes < need))
+    return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  cudaError_t e;
+  if (dph::tc_sum_supported(g) && desc->dtype == DP_BF16 && aligned16(A) && aligned16(G))
+    e = dph::launch_tc_sum(g, A, G, factors, dW, db, accumulate, static_cast<float*>(workspace),
+                           stream);
+  else
+    e = dph::launch_simt_clipped_sum(g, desc->dtype, A, G, factors, dW, db, accumulate,
+                                     static_cast<float*>(workspace), (int)dph::simt_sum_splits(g),
+                                     stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum launch");
+  return ok();
+}
+
+dp_status dp_add_noise(float* grad, size_t n, float sigma, float C, int B, uint64_t seed,
+                       uint64_t offset, cudaStream_t stream) {
+  if (n == 0) return ok();
+  if (!grad) return fail(DP_ERR_INVALID_ARG, "grad is NULL");
+  if (B <= 0) return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0", B);
+  if (!(sigma >= 0.f) || !std::isfinite(sigma) || !(C >= 0.f) || !std::isfinite(C))
+    return fail(DP_ERR_INVALID_ARG, "sigma=%g and C=%g must be finite and >= 0", (double)sigma, (double)C);
+  if (offset + n < offset) return fail(DP_ERR_INVALID_ARG, "offset + n overflows");
+  const float sc = (float)((double)sigma * (double)C);
+  const float invB = (float)(1.0 / (double)B);
+  cudaError_t e = dph::launch_add_noise(grad, n, sc, invB, seed, offset, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_add_noise launch");
+  return ok();
+}
+
+dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha, float beta,
+                            float sigma_l2, uint64_t seed, int layer, float* out,
+                            cudaStream_t stream) {
+  if (!sqnorms || !out) return fail(DP_ERR_INVALID_ARG, "sqnorms and out must be non-NULL");
+  if (B <= 0 || layer < 0) return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0 and layer=%d >= 0", B, layer);
+  if (!(C_l2 > 0.f) || !std::isfinite(alpha) || !std::isfinite(beta) || !(sigma_l2 >= 0.f))
+    return fail(DP_ERR_INVALID_ARG, "C_l2 > 0, finite alpha and beta, sigma_l2 >= 0 required");
+  cudaError_t e = dph::launch_adaptive_bound(sqnorms, B, C_l2, alpha, beta, sigma_l2, seed, layer,
+                                             out, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_adaptive_bound launch");
+  return ok();
+}
+
+dp_status dp_check_status(cudaStream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_check_status sync");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DP_ERR_CUDA, "cannot resolve the device status word");
+  unsigned v = 0;
+  e = cudaMemcpy(&v, st, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_check_status read");
+  if (v) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "dp_check_status clear");
+  }
+  if (v & dpk::kStatusTimeout) return fail(DP_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (v & dpk::kStatusNonfinite) return fail(DP_ERR_NONFINITE, "a per-example norm was not finite");
+  return ok();
+}
+
+}  // extern "C"

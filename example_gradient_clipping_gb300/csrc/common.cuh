@@ -1,0 +1,131 @@
+// Shared device/host helpers of libdpclip (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "dpclip.h"
+
+namespace dpk {
+
+// Device status bits (ORed into the status word; dp_check_status maps them).
+constexpr unsigned kStatusNonfinite = 1u;
+constexpr unsigned kStatusTimeout = 2u;
+
+// Geometry of one layer's per-example contraction, resolved on the host.
+// Linear: row t of example i is A[i, t, :] / G[i, t, :].
+// Conv2d: row t = (ho, wo) of the unfolded input U(a_i) and of F^{-1}(G_i).
+struct Geom {
+  int B, T, D, p;             // examples, rows, (unfolded) input width, outputs
+  int d;                      // linear input width (== D for linear)
+  int Cin, H, W, k, stride, pad, dil, Hout, Wout;
+  int conv;                   // 0 linear, 1 conv2d
+  int has_bias;
+};
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// Output-gradient element X(i, t, j), j < p.
+template <class E>
+__device__ __forceinline__ float ld_g(const E* __restrict__ G, const Geom& g, int i, int t, int j) {
+  if (!g.conv) return to_f(G[((size_t)i * g.T + t) * g.p + j]);
+  return to_f(G[((size_t)i * g.p + j) * g.T + t]);
+}
+
+// (Unfolded) input element Y(i, t, m), m < D; zero outside the image (padding).
+template <class E>
+__device__ __forceinline__ float ld_a(const E* __restrict__ A, const Geom& g, int i, int t, int m) {
+  if (!g.conv) return to_f(A[((size_t)i * g.T + t) * g.d + m]);
+  const int kk = g.k * g.k;
+  const int c = m / kk, r = m - c * kk;
+  const int kh = r / g.k, kw = r - kh * g.k;
+  const int ho = t / g.Wout, wo = t - ho * g.Wout;
+  const int h = ho * g.stride - g.pad + kh * g.dil;
+  const int w = wo * g.stride - g.pad + kw * g.dil;
+  if (h < 0 || h >= g.H || w < 0 || w >= g.W) return 0.f;
+  return to_f(A[(((size_t)i * g.Cin + c) * g.H + h) * g.W + w]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Philox4x32-10 block function (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 products,
+// XOR of the high halves into the other words and the round key, a word
+// permutation, and a Weyl-sequence key schedule.
+struct PhiloxOut { uint32_t x[4]; };
+
+__device__ __forceinline__ PhiloxOut philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                   uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = kM0 * c0, hi0 = __umulhi(kM0, c0);
+    const uint32_t lo1 = kM1 * c2, hi1 = __umulhi(kM1, c2);
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    k0 += kW0; k1 += kW1;
+  }
+  PhiloxOut o;
+  o.x[0] = c0; o.x[1] = c1; o.x[2] = c2; o.x[3] = c3;
+  return o;
+}
+
+// Uniform in (0, 1) from the top 23 bits of a word: (floor(x/2^9) + 1/2)/2^23, exact in fp32.
+__device__ __forceinline__ float u01_from_word(uint32_t x) {
+  return __uint2float_rn(x >> 9) * 0x1p-23f + 0x1p-24f;
+}
+
+// Four standard normals of Philox block q of stream `stream` under `seed`.
+__device__ __forceinline__ void normal4(uint64_t q, uint64_t seed, uint32_t stream, float z[4]) {
+  const PhiloxOut o = philox4x32_10((uint32_t)q, (uint32_t)(q >> 32), stream, 0u,
+                                    (uint32_t)seed, (uint32_t)(seed >> 32));
+  const float u0 = u01_from_word(o.x[0]), u1 = u01_from_word(o.x[1]);
+  const float u2 = u01_from_word(o.x[2]), u3 = u01_from_word(o.x[3]);
+  const float r01 = sqrtf(-2.f * logf(u0));
+  const float r23 = sqrtf(-2.f * logf(u2));
+  float s1, c1, s3, c3;
+  sincospif(2.f * u1, &s1, &c1);
+  sincospif(2.f * u3, &s3, &c3);
+  z[0] = r01 * c1; z[1] = r01 * s1; z[2] = r23 * c3; z[3] = r23 * s3;
+}
+
+}  // namespace dpk
+
+// Host-side launchers implemented by the kernel translation units.
+namespace dph {
+using dpk::Geom;
+// Counts kernels the library launched (reported by dp_launch_count).
+void count_launch(unsigned n = 1);
+cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* G, float* out,
+                           cudaStream_t s);
+cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, const float* C,
+                                float* out, unsigned* status, cudaStream_t s);
+cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,
+                             uint64_t offset, cudaStream_t s);
+cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
+                                  float sigma_l2, uint64_t seed, int layer, float* out,
+                                  cudaStream_t s);
+// SIMT (FFMA) paths: any dtype/shape.
+size_t simt_sum_splits(const Geom& g);
+cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, const void* G,
+                                    const float* factors, float* dW, float* db, int accumulate,
+                                    float* ws, int splits, cudaStream_t s);
+size_t simt_ghost_ws_floats(const Geom& g);
+cudaError_t launch_simt_ghost(const Geom& g, int dtype, const void* A, const void* G, float* out,
+                              float* ws, cudaStream_t s);
+size_t simt_inst_ws_floats(const Geom& g);
+cudaError_t launch_simt_inst(const Geom& g, int dtype, const void* A, const void* G, float* out,
+                             float* ws, cudaStream_t s);
+}  // namespace dph

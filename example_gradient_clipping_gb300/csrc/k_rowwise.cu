@@ -1,0 +1,190 @@
+// HBM-bound and tiny kernels: one-row norms, clip factors, Gaussian noise, adaptive bound.
+#include "common.cuh"
+
+namespace dpk {
+
+// ---------------------------------------------------------------------------
+// One-row norm ([FastClip] eq. 6: the per-example gradient of a one-row linear
+// layer is the outer product g a^T, so ||g a^T||_F^2 = ||a||^2 ||g||^2; the bias
+// gradient is g itself).  One warp per example, 16-byte vector loads when the
+// rows are 16-byte aligned, warp-shuffle reduction.
+template <class E>
+__device__ __forceinline__ float row_sqsum(const E* __restrict__ x, int n, int lane, bool vec) {
+  float acc = 0.f;
+  constexpr int kVec = 16 / sizeof(E);
+  int j0 = 0;
+  if (vec) {
+    const int nv = n / kVec;
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    for (int v = lane; v < nv; v += 32) {
+      uint4 w = __ldg(xv + v);
+      const E* e = reinterpret_cast<const E*>(&w);
+#pragma unroll
+      for (int q = 0; q < kVec; ++q) { const float f = to_f(e[q]); acc = fmaf(f, f, acc); }
+    }
+    j0 = nv * kVec;
+  }
+  for (int j = j0 + lane; j < n; j += 32) { const float f = to_f(x[j]); acc = fmaf(f, f, acc); }
+  return warp_sum(acc);
+}
+
+template <class E>
+__global__ void __launch_bounds__(256) t1_norm_kernel(Geom g, const E* __restrict__ A,
+                                                      const E* __restrict__ G, float* __restrict__ out,
+                                                      bool vec_a, bool vec_g) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < g.B; i += warps) {
+    const float sa = row_sqsum(A + (size_t)i * g.d, g.d, lane, vec_a);
+    const float sg = row_sqsum(G + (size_t)i * g.p, g.p, lane, vec_g);
+    if (lane == 0) out[i] = sa * sg + (g.has_bias ? sg : 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Clip factors: c = 1 if n <= C else C/n ([FastClip] section 2); flat sums the
+// layers' squared norms first, per-layer keeps them apart ([ThreeTools] section 2).
+struct Bounds { float C[64]; };
+
+__global__ void clip_factors_kernel(const float* __restrict__ sq, int B, int L, int per_layer,
+                                    Bounds bounds, const float* __restrict__ Cdev,
+                                    float* __restrict__ out, unsigned* status) {
+  const int n_out = per_layer ? B * L : B;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n_out; e += gridDim.x * blockDim.x) {
+    float s, C;
+    if (per_layer) {
+      const int l = e / B;
+      s = sq[e];
+      C = Cdev ? Cdev[l] : bounds.C[l];
+    } else {
+      s = 0.f;
+      for (int l = 0; l < L; ++l) s += sq[(size_t)l * B + e];
+      C = Cdev ? Cdev[0] : bounds.C[0];
+    }
+    const float n = sqrtf(s);
+    float c;
+    if (!isfinite(n)) {
+      c = 0.f;
+      atomicOr(status, kStatusNonfinite);
+    } else {
+      c = (n <= C) ? 1.f : C / n;
+    }
+    out[e] = c;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Gaussian mechanism + 1/B: grad[j] = (grad[j] + sc * z_{offset+j}) * invB.
+// One thread per Philox block of four consecutive elements of the global index;
+// float4 load/store when the four lie in range and are 16-byte aligned.
+__global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad, size_t n, float sc,
+                                                        float invB, uint64_t seed, uint64_t offset) {
+  const uint64_t q0 = offset >> 2;
+  const uint64_t q1 = (offset + n + 3) >> 2;  // one past the last block touched
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t q = q0 + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < q1; q += stride) {
+    float z[4];
+    normal4(q, seed, 0u, z);
+    const int64_t j0 = (int64_t)(q << 2) - (int64_t)offset;   // index of lane 0 in grad
+    float* p = grad + j0;
+    if (j0 >= 0 && j0 + 4 <= (int64_t)n && ((reinterpret_cast<uintptr_t>(p) & 15u) == 0)) {
+      float4 v = *reinterpret_cast<float4*>(p);
+      v.x = fmaf(sc, z[0], v.x) * invB;
+      v.y = fmaf(sc, z[1], v.y) * invB;
+      v.z = fmaf(sc, z[2], v.z) * invB;
+      v.w = fmaf(sc, z[3], v.w) * invB;
+      *reinterpret_cast<float4*>(p) = v;
+    } else {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int64_t j = j0 + r;
+        if (j >= 0 && j < (int64_t)n) grad[j] = fmaf(sc, z[r], grad[j]) * invB;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Adaptive bound ([ThreeTools] section 3): C_next = alpha/B (sum_i min(n_i, C_l2)
+// + sigma_l2 C_l2 z), C_l2_next = beta C_next.  One block; fp64 accumulation.
+__global__ void __launch_bounds__(256) adaptive_bound_kernel(const float* __restrict__ sq, int B,
+                                                             float C_l2, float alpha, float beta,
+                                                             float sigma_l2, uint64_t seed, int layer,
+                                                             float* __restrict__ out) {
+  __shared__ double part[8];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    const float n = sqrtf(sq[i]);
+    acc += (double)fminf(n, C_l2);
+  }
+  acc = warp_sum_d(acc);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += part[w];
+    float z[4];
+    const uint64_t e = (uint64_t)layer;
+    normal4(e >> 2, seed, 1u, z);
+    const double cn = (double)alpha / (double)B * (tot + (double)sigma_l2 * (double)C_l2 * (double)z[e & 3]);
+    out[0] = (float)cn;
+    out[1] = (float)((double)beta * cn);
+  }
+}
+
+}  // namespace dpk
+
+namespace dph {
+using namespace dpk;
+
+cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* G, float* out,
+                           cudaStream_t s) {
+  const int warps_per_block = 8;
+  const int blocks = (g.B + warps_per_block - 1) / warps_per_block;
+  const size_t es = dtype == DP_FP32 ? 4 : 2;
+  const bool va = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((g.d * es) % 16 == 0);
+  const bool vg = ((reinterpret_cast<uintptr_t>(G) & 15u) == 0) && ((g.p * es) % 16 == 0);
+  if (dtype == DP_FP32)
+    t1_norm_kernel<float><<<blocks, 256, 0, s>>>(g, (const float*)A, (const float*)G, out, va, vg);
+  else
+    t1_norm_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(g, (const __nv_bfloat16*)A,
+                                                         (const __nv_bfloat16*)G, out, va, vg);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, const float* C,
+                                float* out, unsigned* status, cudaStream_t s) {
+  Bounds b{};
+  const int nC = per_layer ? L : 1;
+  for (int l = 0; l < nC && l < 64; ++l) b.C[l] = C[l];
+  // more than 64 per-layer bounds are rejected by the caller
+  const int n_out = per_layer ? B * L : B;
+  const int blocks = (n_out + 255) / 256;
+  clip_factors_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(sq, B, L, per_layer, b, nullptr, out,
+                                                              status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,
+                             uint64_t offset, cudaStream_t s) {
+  const uint64_t blocks4 = ((offset + n + 3) >> 2) - (offset >> 2);
+  uint64_t grid = (blocks4 + 255) / 256;
+  const uint64_t cap = 152ull * 8ull;   // grid-stride beyond 8 resident blocks per SM
+  if (grid > cap) grid = cap;
+  if (grid == 0) grid = 1;
+  add_noise_kernel<<<(unsigned)grid, 256, 0, s>>>(grad, n, sc, invB, seed, offset);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
+                                  float sigma_l2, uint64_t seed, int layer, float* out,
+                                  cudaStream_t s) {
+  adaptive_bound_kernel<<<1, 256, 0, s>>>(sq, B, C_l2, alpha, beta, sigma_l2, seed, layer, out);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace dph

@@ -1,0 +1,17 @@
+// Tensor-core (tcgen05 / TMEM / TMA) kernels of libdpclip: declarations.
+#pragma once
+#include "common.cuh"
+
+namespace dph {
+using dpk::Geom;
+// Clipped sum as one reweighted GEMM over the batch rows (bf16 in, fp32 accumulate).
+bool tc_sum_supported(const Geom& g);
+size_t tc_sum_ws_bytes(const Geom& g);
+cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
+                          float* dW, float* db, int accumulate, float* ws, cudaStream_t s);
+// Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).
+bool tc_ghost_supported(const Geom& g);
+size_t tc_ghost_ws_bytes(const Geom& g);
+cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* ws,
+                            cudaStream_t s);
+}  // namespace dph

@@ -1,0 +1,85 @@
+"""One privatised-gradient step over a list of layers, through the C ABI.
+
+Per step: dp_layer_sqnorms for every layer (ghost norm, instantiation or the
+one-row form, layer by layer), dp_clip_factors (flat or per-layer), dp_clipped_sum
+for every layer into one flat fp32 gradient vector [W_0, b_0, W_1, b_1, ...], then
+dp_add_noise over it (per layer with its own bound when clipping per layer).
+Torch supplies device memory and the stream only.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence, Tuple
+
+from . import (DP_NORM_AUTO, LayerDesc, dp_add_noise, dp_clip_factors, dp_clipped_sum,
+               dp_layer_sqnorms, dp_plan, dp_workspace_size)
+
+
+class ClipStep:
+    def __init__(self, descs: Sequence[LayerDesc], C, sigma: float, per_layer: bool = False,
+                 norm_modes: Optional[Sequence[int]] = None, device: str = "cuda"):
+        import torch
+        self.descs = list(descs)
+        L = len(self.descs)
+        self.B = self.descs[0].B
+        if any(d.B != self.B for d in self.descs):
+            raise ValueError("all layers of a step share the batch size B")
+        self.per_layer = bool(per_layer)
+        self.C = [float(c) for c in (C if isinstance(C, (list, tuple)) else [C] * L)]
+        self.sigma = float(sigma)
+        self.modes = list(norm_modes) if norm_modes is not None else [DP_NORM_AUTO] * L
+        self.plan = [dp_plan(d, m) for d, m in zip(self.descs, self.modes)]
+        self.offsets, o = [], 0
+        self.shapes = []
+        for d, (_, T, D) in zip(self.descs, self.plan):
+            self.offsets.append(o)
+            self.shapes.append((d.p, D))
+            o += d.p * D + (d.p if d.has_bias else 0)
+        self.n_params = o
+        ws = max(dp_workspace_size(d, m) for d, m in zip(self.descs, self.modes))
+        dev = torch.device(device)
+        self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        self.sqnorms = torch.empty(L, self.B, dtype=torch.float32, device=dev)
+        self.factors = torch.empty((L if self.per_layer else 1), self.B, dtype=torch.float32, device=dev)
+        self.grad = torch.empty(self.n_params, dtype=torch.float32, device=dev)
+        self.chosen: List[int] = [m for m, _, _ in self.plan]
+
+    def layer_views(self, l: int) -> Tuple:
+        p, D = self.shapes[l]
+        o = self.offsets[l]
+        dW = self.grad[o:o + p * D]
+        db = self.grad[o + p * D:o + p * D + p] if self.descs[l].has_bias else None
+        return dW, db
+
+    def norms(self, inputs, stream=None) -> None:
+        for l, (d, (A, G)) in enumerate(zip(self.descs, inputs)):
+            self.chosen[l] = dp_layer_sqnorms(d, A, G, self.sqnorms[l], self.workspace, mode=self.modes[l],
+                                              stream=stream)
+
+    def factors_(self, stream=None) -> None:
+        L = len(self.descs)
+        dp_clip_factors(self.sqnorms, self.B, L, self.per_layer, self.C if self.per_layer else self.C[:1],
+                        self.factors, stream=stream)
+
+    def sums(self, inputs, stream=None) -> None:
+        for l, (d, (A, G)) in enumerate(zip(self.descs, inputs)):
+            dW, db = self.layer_views(l)
+            fac = self.factors[l] if self.per_layer else self.factors[0]
+            dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
+
+    def noise(self, seed: int, stream=None) -> None:
+        if not self.per_layer:
+            dp_add_noise(self.grad, self.sigma, self.C[0], self.B, seed, 0, stream=stream)
+            return
+        for l, d in enumerate(self.descs):
+            p, D = self.shapes[l]
+            n = p * D + (p if d.has_bias else 0)
+            o = self.offsets[l]
+            dp_add_noise(self.grad[o:o + n], self.sigma, self.C[l], self.B, seed, o, stream=stream)
+
+    def run(self, inputs, seed: int, stream=None):
+        """Norms -> factors -> clipped sums -> noise and 1/B; returns the flat gradient."""
+        self.norms(inputs, stream)
+        self.factors_(stream)
+        self.sums(inputs, stream)
+        self.noise(seed, stream)
+        return self.grad

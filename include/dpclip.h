@@ -1,0 +1,155 @@
+/*
+ * dpclip.h -- C ABI of libdpclip, DP-SGD per-example gradient clipping on GB300 (sm_103a).
+ *
+ * The library computes, for captured layer activations A and output gradients G,
+ * the per-example gradient norms (ghost norm or per-example instantiation, chosen
+ * layer by layer), the clip factors, the clipped sum sum_i c_i G_i^T A_i with its
+ * bias gradient, and the Gaussian noise with the 1/B scale.  Pages (by title):
+ *   [FastClip]   "Scaling up Differentially Private Deep Learning with Fast
+ *                Per-Example Gradient Clipping"
+ *   [ThreeTools] "Three Tools for Practical Differential Privacy"
+ *   [MixGhost]   "Scalable and Efficient Training of Large Convolutional Neural
+ *                Networks with Differential Privacy"
+ *
+ * Conventions for every call:
+ *  - Pointers named A, G, sqnorms, factors, dW, db, grad, workspace are DEVICE
+ *    pointers; the caller owns every buffer and the library never allocates on
+ *    these paths (workspace is caller-provided, sized by dp_workspace_size).
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream) unless noted.
+ *    Arguments are validated on the host before anything is launched; a bad
+ *    argument returns DP_ERR_INVALID_ARG (or DP_ERR_UNSUPPORTED) and launches
+ *    nothing.  dp_last_error() then holds a message (per calling thread).
+ *  - Device-side conditions (a non-finite norm) set a device status word that
+ *    dp_check_status() returns and clears.
+ *  - Layouts (row-major, contiguous, PyTorch conventions):
+ *      linear: A [B, T, d], G [B, T, p]; weight gradient [p, d]
+ *      conv2d: A [B, Cin, H, W] (NCHW), G [B, p, Hout, Wout]; weight gradient
+ *              [p, Cin, k, k]; T = Hout*Wout, D = Cin*k*k.
+ *    bf16 inputs are accumulated in fp32; every output is fp32.
+ */
+#ifndef DPCLIP_H
+#define DPCLIP_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DPCLIP_ABI_VERSION 1
+
+typedef enum {
+  DP_OK = 0,
+  DP_ERR_INVALID_ARG = 1,   /* bad pointer, size, mode or descriptor */
+  DP_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+  DP_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  DP_ERR_NONFINITE = 4,     /* a norm was inf/NaN: that example's factor was set to 0 */
+  DP_ERR_TIMEOUT = 5        /* a bounded device wait gave up */
+} dp_status;
+
+typedef enum { DP_BF16 = 0, DP_FP32 = 1 } dp_dtype;
+typedef enum { DP_LINEAR = 0, DP_CONV2D = 1 } dp_kind;
+
+/* How the per-example norm is formed ([MixGhost] section 4, the layerwise decision). */
+typedef enum {
+  DP_NORM_AUTO = 0,          /* ghost iff 2T^2 < p*D (ties instantiate); T == 1 -> closed form */
+  DP_NORM_GHOST = 1,         /* Gram identity: sum_{t,s} (a_t.a_s)(g_t.g_s) */
+  DP_NORM_INSTANTIATE = 2,   /* g_i = G_i^T U(A_i) formed on chip, squared and summed */
+  DP_NORM_T1 = 3             /* one row: ||a||^2 ||g||^2 (reported; also accepted when T == 1) */
+} dp_norm_mode;
+
+/* One layer.  Linear uses B, T, d, p; conv2d uses B, Cin, H, W, p, k, stride, pad, dil
+ * (square kernel; Hout = (H + 2 pad - dil (k-1) - 1)/stride + 1, likewise Wout). */
+typedef struct {
+  int kind;      /* dp_kind */
+  int dtype;     /* dp_dtype of A and G */
+  int B;         /* examples */
+  int T, d, p;   /* linear: rows per example, in features; p = out features / channels */
+  int Cin, H, W, k, stride, pad, dil;
+  int has_bias;  /* 1: the bias gradient joins the norm and the sum */
+} dp_layer_desc;
+
+/* ABI version (DPCLIP_ABI_VERSION).  Host only. */
+int dp_abi_version(void);
+
+/* Number of kernels this library has launched in the process so far (all devices and
+ * streams).  Host only; for accounting launches in a timed region. */
+unsigned long long dp_launch_count(void);
+
+/* Message for the last non-DP_OK status returned on this thread ("" if none). Host only. */
+const char* dp_last_error(void);
+
+/* Host-only planner: validates `desc`, resolves `requested` (DP_NORM_AUTO applies the
+ * layerwise rule of [MixGhost] eq. 4.1 -- the smaller of the ghost space 2T^2 and the
+ * instantiation space p*D, Appendix F) and reports the rows T and width D of the
+ * per-example contraction.  Any output pointer may be NULL.  Needs no GPU. */
+dp_status dp_plan(const dp_layer_desc* desc, int requested, int* chosen_mode, int* rows_T,
+                  int* width_D);
+
+/* Bytes of workspace dp_layer_sqnorms / dp_clipped_sum need for `desc` (0 if invalid).
+ * `mode` is the requested norm mode for dp_layer_sqnorms; the clipped sum's need is
+ * included.  Host only. */
+size_t dp_workspace_size(const dp_layer_desc* desc, int mode);
+
+/* Per-example squared gradient norm of one layer:
+ *   sqnorm_out[i] = ||dL_i/dW||_F^2 + has_bias * ||dL_i/db||^2,   i < B   (fp32, device)
+ * dL_i/dW = G_i^T A_i (linear, [MixGhost] eq. 2.4) or F^{-1}(G_i)^T U(A_i) (conv,
+ * eq. 2.6); formed by the ghost norm (eq. 2.7: sum_{t,s} (U U^T)_{ts} (G G^T)_{ts}),
+ * by instantiation on chip, or by the one-row closed form ||a||^2 ||g||^2
+ * ([FastClip] eq. 6), per `mode`.  chosen_mode_out (host int, may be NULL) receives
+ * the mode used.  workspace: device, >= dp_workspace_size(desc, mode) bytes. */
+dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void* G, int mode,
+                           float* sqnorm_out, int* chosen_mode_out, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/* Clip factors ([FastClip] section 2, clip_c; [MixGhost] Appendix C, min(R/||g||, 1)).
+ * sqnorms: device fp32 [L, B] (row l = one layer's sqnorm_out).
+ * per_layer = 0 (flat): n_i = sqrt(sum_l sqnorms[l,i]); factors_out[i] = 1 if n_i <= C[0]
+ *   else C[0]/n_i; factors_out is [B].
+ * per_layer = 1 ([ThreeTools] section 2): factors_out[l,i] from n_{l,i} and C[l]; [L, B].
+ * C: HOST array of 1 (flat) or L (per-layer) bounds, each > 0.
+ * A non-finite n gives factor 0 and sets DP_ERR_NONFINITE in the device status. */
+dp_status dp_clip_factors(const float* sqnorms, int B, int L, int per_layer, const float* C,
+                          float* factors_out, cudaStream_t stream);
+
+/* Clipped sum of one layer, as one reweighted contraction ([FastClip] section 5, the
+ * reweighted loss; [MixGhost] section 3.2, the second back-propagation):
+ *   dW[j, m] (+)= sum_i factors[i] * (dL_i/dW)[j, m]        fp32 [p, D], device
+ *   db[j]    (+)= sum_i factors[i] * sum_t G_i[t, j]        fp32 [p], device (NULL: skipped)
+ * factors: device fp32 [B] (a row of dp_clip_factors' output).  accumulate = 0 writes,
+ * 1 adds to the existing dW/db (gradient accumulation over micro-batches).
+ * workspace: device, >= dp_workspace_size(desc, 0) bytes. */
+dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G,
+                         const float* factors, float* dW, float* db, int accumulate,
+                         void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Gaussian mechanism and average ([FastClip] section 2; [MixGhost] eq. 2.1):
+ *   grad[j] = (grad[j] + sigma * C * z_{offset + j}) / B,   j < n   (fp32, device, in place)
+ * z_e is the standard normal of element e of Philox4x32-10 (Salmon et al., SC'11)
+ * stream 0 under `seed`, through Box-Muller:
+ *   counter (e/4 low, e/4 high, 0, 0), key (seed low, seed high); u_k = (x_k>>9 + 1/2)/2^23;
+ *   z0,z1 = sqrt(-2 ln u0)(cos, sin)(2 pi u1); z2,z3 likewise from u2,u3; e takes z_{e mod 4}.
+ * Use offset = the first index of this buffer in the flat parameter vector so that
+ * every parameter draws its own normal. */
+dp_status dp_add_noise(float* grad, size_t n, float sigma, float C, int B, uint64_t seed,
+                       uint64_t offset, cudaStream_t stream);
+
+/* Adaptive clipping bound of one layer ([ThreeTools] section 3):
+ *   C_next = alpha/B * (sum_i min(sqrt(sqnorms[i]), C_l2) + sigma_l2 * C_l2 * z),
+ *   C_l2_next = beta * C_next,
+ * z = element `layer` of noise stream 1 (counter word 2 = 1) under `seed`.
+ * sqnorms: device fp32 [B].  out: device fp32 [2] = {C_next, C_l2_next}. */
+dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha, float beta,
+                            float sigma_l2, uint64_t seed, int layer, float* out,
+                            cudaStream_t stream);
+
+/* Synchronizes `stream`, returns the device status word (DP_OK, DP_ERR_NONFINITE or
+ * DP_ERR_TIMEOUT) raised since the last check, and clears it. */
+dp_status dp_check_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DPCLIP_H */

@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 CPU oracle.
+
+Every workload's shapes are covered: in full where the oracle finishes in seconds,
+else on a smaller batch in full plus sampled examples at the full batch.  Edge
+cases: one example, ragged rows and widths, strides/dilation, no bias,
+accumulation, per-layer bounds, non-finite inputs, noise windows.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import TOL, Z_ATOL, Z_RTOL, desc_for, rel_elem, rel_vec, to_dev
+from workloads import LayerSpec, Workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_layer(dp, spec, wl, A, G, mode=None, factors=None):
+    """GPU sqnorms (and, with factors, the clipped sum) for one layer."""
+    import torch
+    B = A.shape[0]
+    desc = desc_for(dp, spec, B, wl.dtype)
+    mode = dp.DP_NORM_AUTO if mode is None else mode
+    ws = torch.empty(max(dp.dp_workspace_size(desc, mode), 16), dtype=torch.uint8, device="cuda")
+    Ad, Gd = to_dev(A, wl.dtype), to_dev(G, wl.dtype)
+    sq = torch.empty(B, dtype=torch.float32, device="cuda")
+    chosen = dp.dp_layer_sqnorms(desc, Ad, Gd, sq, ws, mode=mode)
+    out = dict(sq=sq, chosen=chosen)
+    if factors is not None:
+        f = torch.tensor(np.asarray(factors, dtype=np.float32), device="cuda")
+        dW = torch.empty(spec.p * spec.D, dtype=torch.float32, device="cuda")
+        db = torch.empty(spec.p, dtype=torch.float32, device="cuda") if spec.has_bias else None
+        dp.dp_clipped_sum(desc, Ad, Gd, f, dW, db, ws)
+        out.update(dW=dW, db=db)
+    torch.cuda.synchronize()
+    return out
+
+
+def _check_layer(dp, spec, wl, examples=None, mode=None, factor_range=(0.0, 1.0)):
+    A, G = workloads.layer_inputs(wl, list(wl.layers).index(spec), examples)
+    fac = workloads.factor_inputs(wl, A.shape[0], *factor_range)
+    got = _run_layer(dp, spec, wl, A, G, mode, fac)
+    s_ref = oracle.layer_sqnorms(spec, A, G)
+    tol = TOL[wl.dtype]
+    assert rel_elem(got["sq"].cpu().numpy(), s_ref) <= tol
+    S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
+    assert rel_vec(got["dW"].cpu().numpy(), S) <= tol
+    if spec.has_bias:
+        assert rel_vec(got["db"].cpu().numpy(), Sb) <= tol
+    return got
+
+
+# ----------------------------------------------------------------- workloads in full
+
+def test_t1_linear_full_step(lib):
+    """One-row fp32 layer: norms, factors, clipped sum, noise -- the whole step."""
+    import torch
+    dp = lib
+    wl = workloads.get_workload("t1_linear_b32")
+    inputs = [workloads.layer_inputs(wl, 0)]
+    ref = oracle.dp_step(wl, inputs)
+    desc = desc_for(dp, wl.layers[0], wl.B, wl.dtype)
+    step = dp.ClipStep([desc], C=wl.C, sigma=wl.sigma)
+    dev = [(to_dev(A, wl.dtype), to_dev(G, wl.dtype)) for A, G in inputs]
+    step.norms(dev)
+    step.factors_()
+    step.sums(dev)
+    torch.cuda.synchronize()
+    assert step.chosen == [dp.DP_NORM_T1]
+    assert rel_elem(step.sqnorms.cpu().numpy(), ref["sqnorms"]) <= TOL["fp32"]
+    assert rel_elem(step.factors.cpu().numpy()[0], ref["factors"]) <= TOL["fp32"]
+    S, Sb = ref["sums"][0]
+    pre = np.concatenate([S.ravel(), Sb])
+    assert rel_vec(step.grad.cpu().numpy(), pre) <= TOL["fp32"]
+    step.noise(wl.seed)
+    torch.cuda.synchronize()
+    assert rel_vec(step.grad.cpu().numpy(), ref["noisy"]) <= TOL["fp32"]
+
+
+def test_seq_linear_full_step(lib):
+    import torch
+    dp = lib
+    wl = workloads.get_workload("seq_linear_b64_t128")
+    inputs = [workloads.layer_inputs(wl, 0)]
+    ref = oracle.dp_step(wl, inputs)
+    desc = desc_for(dp, wl.layers[0], wl.B, wl.dtype)
+    step = dp.ClipStep([desc], C=wl.C, sigma=wl.sigma)
+    dev = [(to_dev(A, wl.dtype), to_dev(G, wl.dtype)) for A, G in inputs]
+    step.norms(dev)
+    step.factors_()
+    step.sums(dev)
+    torch.cuda.synchronize()
+    assert step.chosen == [dp.DP_NORM_GHOST]
+    tol = TOL["bf16"]
+    assert rel_elem(step.sqnorms.cpu().numpy(), ref["sqnorms"]) <= tol
+    assert rel_elem(step.factors.cpu().numpy()[0], ref["factors"]) <= tol
+    S, Sb = ref["sums"][0]
+    assert rel_vec(step.grad.cpu().numpy(), np.concatenate([S.ravel(), Sb])) <= tol
+    step.noise(wl.seed)
+    torch.cuda.synchronize()
+    assert rel_vec(step.grad.cpu().numpy(), ref["noisy"]) <= tol
+
+
+def test_conv3x3_full_batch(lib):
+    wl = workloads.get_workload("conv3x3_b256")
+    got = _check_layer(lib, wl.layers[0], wl)
+    assert got["chosen"] == lib.DP_NORM_INSTANTIATE
+
+
+def test_vgg11_stack_small_batch_flat_and_per_layer(lib):
+    """Every VGG-11 layer (mixed ghost/instantiate/one-row), whole step, flat and per-layer."""
+    import torch
+    dp = lib
+    wl = workloads.get_workload("vgg11_cifar_b1024").with_batch(12)
+    inputs = [workloads.layer_inputs(wl, l) for l in range(len(wl.layers))]
+    descs = [desc_for(dp, s, wl.B, wl.dtype) for s in wl.layers]
+    dev = [(to_dev(A, wl.dtype), to_dev(G, wl.dtype)) for A, G in inputs]
+    # scale so that some examples clip and some do not
+    for per_layer in (False, True):
+        ref = oracle.dp_step(wl, inputs, per_layer=per_layer)
+        step = dp.ClipStep(descs, C=wl.C, sigma=wl.sigma, per_layer=per_layer)
+        step.norms(dev)
+        step.factors_()
+        step.sums(dev)
+        torch.cuda.synchronize()
+        assert rel_elem(step.sqnorms.cpu().numpy(), ref["sqnorms"]) <= TOL["bf16"]
+        fac = step.factors.cpu().numpy()
+        assert rel_elem(fac if per_layer else fac[0], ref["factors"]) <= TOL["bf16"]
+        pre = np.concatenate([np.concatenate([S.ravel(), Sb]) for S, Sb in ref["sums"]])
+        g = step.grad.cpu().numpy()
+        for l in range(len(wl.layers)):
+            o, n = wl.param_offsets()[l], wl.layers[l].n_params
+            assert rel_vec(g[o:o + n], pre[o:o + n]) <= TOL["bf16"], wl.layers[l].name
+        step.noise(wl.seed)
+        torch.cuda.synchronize()
+        assert rel_vec(step.grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+
+
+def test_vit_mlp_small_batch(lib):
+    wl = workloads.get_workload("vit_mlp_b4096_t197").with_batch(6)
+    for spec in wl.layers:
+        got = _check_layer(lib, spec, wl)
+        assert got["chosen"] == lib.DP_NORM_GHOST
+
+
+# ----------------------------------------------------------------- forced modes agree
+
+@pytest.mark.parametrize("name,layer", [("seq_linear_b64_t128", 0), ("conv3x3_b256", 0),
+                                        ("vgg11_cifar_b1024", 2), ("vgg11_cifar_b1024", 1),
+                                        ("vgg11_cifar_b1024", 6)])
+def test_ghost_and_instantiation_agree(lib, name, layer):
+    wl = workloads.get_workload(name).with_batch(5)
+    spec = wl.layers[layer]
+    A, G = workloads.layer_inputs(wl, layer)
+    ref = oracle.layer_sqnorms(spec, A, G)
+    for mode in (lib.DP_NORM_GHOST, lib.DP_NORM_INSTANTIATE):
+        got = _run_layer(lib, spec, wl, A, G, mode)
+        assert got["chosen"] == mode
+        assert rel_elem(got["sq"].cpu().numpy(), ref) <= TOL[wl.dtype]
+
+
+# ----------------------------------------------------------------- edge shapes
+
+EDGE = [
+    ("lin_B1", LayerSpec("e", "linear", p=24, d=40, T=7), 1, "bf16"),
+    ("lin_ragged", LayerSpec("e", "linear", p=50, d=100, T=37), 5, "bf16"),
+    ("lin_ragged_fp32", LayerSpec("e", "linear", p=33, d=65, T=19), 4, "fp32"),
+    ("lin_nobias", LayerSpec("e", "linear", p=64, d=96, T=130, has_bias=False), 3, "bf16"),
+    ("lin_t1_odd", LayerSpec("e", "linear", p=10, d=13, T=1), 9, "bf16"),
+    ("lin_t1_fp32_odd", LayerSpec("e", "linear", p=7, d=5, T=1), 3, "fp32"),
+    ("conv_s2", LayerSpec("e", "conv2d", p=6, Cin=5, H=11, W=9, k=3, stride=2, pad=1), 3, "bf16"),
+    ("conv_dil", LayerSpec("e", "conv2d", p=4, Cin=3, H=10, W=10, k=3, stride=1, pad=2, dil=2), 2, "fp32"),
+    ("conv_k1", LayerSpec("e", "conv2d", p=8, Cin=16, H=6, W=6, k=1), 3, "bf16"),
+    ("conv_k5_nopad", LayerSpec("e", "conv2d", p=5, Cin=2, H=9, W=8, k=5, a_dist="abs_normal"), 2, "bf16"),
+]
+
+
+@pytest.mark.parametrize("tag,spec,B,dtype", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_shapes(lib, tag, spec, B, dtype):
+    wl = Workload(name=tag, B=B, layers=(spec,), dtype=dtype, C=1.0, sigma=1.0, seed=11)
+    for mode in (None, lib.DP_NORM_GHOST, lib.DP_NORM_INSTANTIATE):
+        if mode is not None and spec.rows == 1 and spec.kind == "linear" and mode == lib.DP_NORM_T1:
+            continue
+        _check_layer(lib, spec, wl, mode=mode)
+
+
+def test_accumulate_adds_to_existing_sum(lib):
+    import torch
+    dp = lib
+    spec = LayerSpec("e", "linear", p=40, d=72, T=9)
+    wl = Workload(name="acc", B=6, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=2)
+    A, G = workloads.layer_inputs(wl, 0)
+    fac = workloads.factor_inputs(wl, 6)
+    desc = desc_for(dp, spec, 6, "bf16")
+    ws = torch.empty(dp.dp_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    Ad, Gd = to_dev(A, "bf16"), to_dev(G, "bf16")
+    f = torch.tensor(fac, device="cuda")
+    dW = torch.full((spec.p * spec.D,), 0.25, device="cuda")
+    db = torch.full((spec.p,), -0.5, device="cuda")
+    dp.dp_clipped_sum(desc, Ad, Gd, f, dW, db, ws, accumulate=True)
+    dp.dp_clipped_sum(desc, Ad, Gd, f, dW, db, ws, accumulate=True)
+    S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
+    assert rel_vec(dW.cpu().numpy(), 0.25 + 2 * S.ravel()) <= TOL["bf16"]
+    assert rel_vec(db.cpu().numpy(), -0.5 + 2 * Sb) <= TOL["bf16"]
+
+
+def test_mixed_scale_factors_straddle_bound(lib):
+    """Some examples under C (factor exactly 1), some over; flat clipping over two layers."""
+    import torch
+    dp = lib
+    l1 = LayerSpec("a", "linear", p=32, d=48, T=16, g_std=0.05)
+    l2 = LayerSpec("b", "conv2d", p=8, Cin=4, H=6, W=6, k=3, pad=1, g_std=0.05)
+    wl = Workload(name="mixed", B=24, layers=(l1, l2), dtype="bf16", C=1.0, sigma=0.5, seed=5,
+                  g_scale="mixed")
+    inputs = [workloads.layer_inputs(wl, l) for l in range(2)]
+    ref = oracle.dp_step(wl, inputs)
+    n = np.sqrt(ref["sqnorms"].sum(0))
+    assert (n < 1).sum() >= 3 and (n > 1).sum() >= 3
+    step = dp.ClipStep([desc_for(dp, s, wl.B, "bf16") for s in wl.layers], C=1.0, sigma=0.5)
+    dev = [(to_dev(A, "bf16"), to_dev(G, "bf16")) for A, G in inputs]
+    grad = step.run(dev, seed=wl.seed)
+    torch.cuda.synchronize()
+    fac = step.factors.cpu().numpy()[0]
+    under = n < 1 - 1e-3
+    assert np.all(fac[under] == 1.0)
+    assert rel_elem(fac, ref["factors"]) <= TOL["bf16"]
+    assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+
+
+def test_nonfinite_norm_zeroes_factor_and_raises_status(lib):
+    import torch
+    dp = lib
+    spec = LayerSpec("e", "linear", p=16, d=16, T=4)
+    wl = Workload(name="nf", B=4, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=1)
+    A, G = workloads.layer_inputs(wl, 0)
+    G[2, 1, 3] = np.inf
+    assert dp.dp_check_status() == dp.DP_OK
+    got = _run_layer(dp, spec, wl, A, G)
+    sq = got["sq"]
+    fac = torch.empty(4, device="cuda")
+    dp.dp_clip_factors(sq.view(1, 4), 4, 1, False, [1.0], fac)
+    assert dp.dp_check_status() == dp.DP_ERR_NONFINITE
+    assert dp.dp_check_status() == dp.DP_OK      # cleared
+    f = fac.cpu().numpy()
+    assert f[2] == 0.0 and np.all(np.isfinite(f))
+
+
+# ----------------------------------------------------------------- noise and adaptive bound
+
+@pytest.mark.parametrize("n,offset", [(1, 0), (3, 5), (7, 2), (1000, 0), (1001, 13), (1 << 20, 3)])
+def test_noise_matches_oracle_definition(lib, n, offset):
+    import torch
+    seed = 0x1234_5678_9ABC
+    buf = torch.zeros(n + 1, device="cuda")[1:] if offset % 2 else torch.zeros(n, device="cuda")
+    lib.dp_add_noise(buf, 1.0, 1.0, 1, seed, offset)
+    z = buf.cpu().numpy().astype(np.float64)
+    ref = oracle.normal_noise(n, seed, offset)
+    assert np.all(np.abs(z - ref) <= Z_RTOL * np.abs(ref) + Z_ATOL)
+
+
+def test_noise_scale_and_moments(lib):
+    import torch
+    n = 1 << 22
+    x = torch.zeros(n, device="cuda")
+    lib.dp_add_noise(x, 0.7225, 2.0, 16, 99, 0)
+    y = x.double().cpu().numpy()
+    sd = 0.7225 * 2.0 / 16
+    assert abs(y.mean()) < 5 * sd / math.sqrt(n)
+    assert y.var() == pytest.approx(sd ** 2, rel=0.01)
+    base = torch.linspace(-1, 1, 1000, device="cuda")
+    b2 = base.clone()
+    lib.dp_add_noise(b2, 0.0, 1.0, 8, 1, 0)
+    assert torch.allclose(b2, base / 8, rtol=1e-7, atol=0)
+
+
+def test_adaptive_bound_matches_oracle(lib):
+    import torch
+    rng = np.random.default_rng(3)
+    s = (rng.random(1024) * 9.0).astype(np.float32)
+    sd = torch.tensor(s, device="cuda")
+    out = torch.empty(2, device="cuda")
+    for layer, C_l2 in ((0, 1.5), (5, 0.8), (8, 10.0)):
+        lib.dp_adaptive_bound(sd, 1024, C_l2, 1.1, 2.0, 2.5, 7, layer, out)
+        c, cl2 = out.cpu().numpy()
+        rc, rcl2 = oracle.adaptive_bound(s.astype(np.float64), C_l2, 1.1, 2.0, 2.5, 7, layer)
+        assert c == pytest.approx(rc, rel=1e-5, abs=1e-6)
+        assert cl2 == pytest.approx(rcl2, rel=1e-5, abs=1e-6)
