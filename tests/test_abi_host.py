@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def dp():
-    from example_gradient_clipping_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import example_gradient_clipping_gb300 as m
     return m
 

@@ -211,8 +211,8 @@ def test_mixed_scale_factors_straddle_bound(lib):
     """Some examples under C (factor exactly 1), some over; flat clipping over two layers."""
     import torch
     dp = lib
-    l1 = LayerSpec("a", "linear", p=32, d=48, T=16, g_std=0.05)
-    l2 = LayerSpec("b", "conv2d", p=8, Cin=4, H=6, W=6, k=3, pad=1, g_std=0.05)
+    l1 = LayerSpec("a", "linear", p=32, d=48, T=16, g_std=0.01)
+    l2 = LayerSpec("b", "conv2d", p=8, Cin=4, H=6, W=6, k=3, pad=1, g_std=0.01)
     wl = Workload(name="mixed", B=24, layers=(l1, l2), dtype="bf16", C=1.0, sigma=0.5, seed=5,
                   g_scale="mixed")
     inputs = [workloads.layer_inputs(wl, l) for l in range(2)]
