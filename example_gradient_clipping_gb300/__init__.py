@@ -54,6 +54,7 @@ def _load():
         "dp_plan": (c_int, [PD, c_int, PI, PI, PI]),
         "dp_workspace_size": (c_size, [PD, c_int]),
         "dp_layer_sqnorms": (c_int, [PD, c_void, c_void, c_int, c_void, PI, c_void, c_size, c_void]),
+        "dp_layer_sqnorms_noalloc": (c_int, [PD, c_void, c_void, c_int, c_void, PI, c_void]),
         "dp_clip_factors": (c_int, [c_void, c_int, c_int, c_int, ctypes.POINTER(c_f), c_void, c_void]),
         "dp_clipped_sum": (c_int, [PD, c_void, c_void, c_void, c_void, c_void, c_int, c_void, c_size, c_void]),
         "dp_add_noise": (c_int, [c_void, c_size, c_f, c_f, c_int, c_u64, c_u64, c_void]),
@@ -118,6 +119,15 @@ def dp_layer_sqnorms(desc: LayerDesc, A, G, sqnorm_out, workspace=None, ws_bytes
         ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None and not isinstance(workspace, int) else 0
     _check(_lib.dp_layer_sqnorms(ctypes.byref(desc), _ptr(A), _ptr(G), mode, _ptr(sqnorm_out),
                                  ctypes.byref(chosen), _ptr(workspace), ws_bytes, _stream(stream)))
+    return chosen.value
+
+
+def dp_layer_sqnorms_noalloc(desc: LayerDesc, A, G, sqnorm_out, mode: int = DP_NORM_AUTO,
+                             stream=None) -> int:
+    """dp_layer_sqnorms for callers that cannot allocate: the scratch is library-owned."""
+    chosen = ctypes.c_int(-1)
+    _check(_lib.dp_layer_sqnorms_noalloc(ctypes.byref(desc), _ptr(A), _ptr(G), mode, _ptr(sqnorm_out),
+                                         ctypes.byref(chosen), _stream(stream)))
     return chosen.value
 
 

@@ -125,6 +125,10 @@ std::atomic<unsigned long long> g_launches{0};
 
 namespace dph {
 void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// For entry points defined in other translation units.
+dp_status geom_from_desc(const dp_layer_desc* d, Geom* g) { return make_geom(d, g); }
+dp_status set_error(dp_status st, const char* msg) { return fail(st, "%s", msg); }
 }  // namespace dph
 
 extern "C" {

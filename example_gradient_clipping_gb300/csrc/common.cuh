@@ -108,6 +108,9 @@ namespace dph {
 using dpk::Geom;
 // Counts kernels the library launched (reported by dp_launch_count).
 void count_launch(unsigned n = 1);
+// Descriptor validation and the thread-local error message, shared by entry points.
+dp_status geom_from_desc(const dp_layer_desc* d, Geom* g);
+dp_status set_error(dp_status st, const char* msg);
 cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* G, float* out,
                            cudaStream_t s);
 cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, const float* C,

@@ -104,6 +104,25 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
                            float* sqnorm_out, int* chosen_mode_out, void* workspace,
                            size_t ws_bytes, cudaStream_t stream);
 
+/* dp_layer_sqnorms without a workspace argument, for callers that cannot allocate
+ * device memory: code that runs inside another framework's hook or callback and has
+ * no handle on that framework's allocator, so it must not call cudaMalloc behind its
+ * back (cudaMalloc and cudaFree synchronize the device and the memory escapes the
+ * framework's accounting), or a latency-bound loop that cannot afford that device-wide
+ * synchronization.  The pages have no counterpart: it changes where the scratch lives,
+ * not what is computed.
+ * Same arguments and results as dp_layer_sqnorms, minus the workspace.  The ghost and
+ * instantiation kernels keep their partial sums in a 4 MiB array the library owns
+ * (one per GPU that loads the library, held until the process exits); a layer whose
+ * partials need more returns DP_ERR_UNSUPPORTED and launches nothing.  Allocates
+ * nothing.  The first call on a device looks up that array's address with the device
+ * current (make it before any stream capture).  Every call shares the array: calls
+ * that overlap on the GPU (other streams, other threads) race and give wrong norms;
+ * serialize them. */
+dp_status dp_layer_sqnorms_noalloc(const dp_layer_desc* desc, const void* A, const void* G,
+                                   int mode, float* sqnorm_out, int* chosen_mode_out,
+                                   cudaStream_t stream);
+
 /* Clip factors ([FastClip] section 2, clip_c; [MixGhost] Appendix C, min(R/||g||, 1)).
  * sqnorms: device fp32 [L, B] (row l = one layer's sqnorm_out).
  * per_layer = 0 (flat): n_i = sqrt(sum_l sqnorms[l,i]); factors_out[i] = 1 if n_i <= C[0]
