@@ -100,24 +100,42 @@ int resolve_mode(const Geom& g, int requested) {
   return requested;
 }
 
-size_t sum_ws_bytes(const Geom& g) {
-  if (dph::tc_sum_supported(g)) return dph::tc_sum_ws_bytes(g);
-  const size_t splits = dph::simt_sum_splits(g);
-  return splits * ((size_t)g.p * g.D + g.p) * sizeof(float);
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Which kernel serves a call: the tensor-core kernels take bf16 inputs with 16-byte
+// aligned base pointers and the shapes they support; everything else runs SIMT.
+bool use_tc_sum(const Geom& g, int dtype, const void* A, const void* G) {
+  return dtype == DP_BF16 && dph::tc_sum_supported(g) && aligned16(A) && aligned16(G);
+}
+bool use_tc_ghost(const Geom& g, int dtype, const void* A, const void* G) {
+  return dtype == DP_BF16 && dph::tc_ghost_supported(g) && aligned16(A) && aligned16(G);
 }
 
-size_t norm_ws_bytes(const Geom& g, int mode) {
+size_t simt_sum_bytes(const Geom& g) {
+  return dph::simt_sum_splits(g) * ((size_t)g.p * g.D + g.p) * sizeof(float);
+}
+
+// Workspace a call needs on the path it takes.
+size_t sum_ws_bytes(const Geom& g, bool tc) { return tc ? dph::tc_sum_ws_bytes(g) : simt_sum_bytes(g); }
+
+size_t norm_ws_bytes(const Geom& g, int mode, bool tc) {
   switch (mode) {
     case DP_NORM_T1: return 0;
     case DP_NORM_GHOST:
-      if (dph::tc_ghost_supported(g)) return dph::tc_ghost_ws_bytes(g);
-      return dph::simt_ghost_ws_floats(g) * sizeof(float);
+      return tc ? dph::tc_ghost_ws_bytes(g) : dph::simt_ghost_ws_floats(g) * sizeof(float);
     case DP_NORM_INSTANTIATE: return dph::simt_inst_ws_floats(g) * sizeof(float);
   }
   return 0;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// The size dp_workspace_size reports covers every path a call with `desc` can take.
+size_t max_ws_bytes(const Geom& g, int mode) {
+  size_t n = std::max(norm_ws_bytes(g, mode, false), simt_sum_bytes(g));
+  if (dph::tc_ghost_supported(g)) n = std::max(n, norm_ws_bytes(g, mode, true));
+  if (dph::tc_sum_supported(g)) n = std::max(n, dph::tc_sum_ws_bytes(g));
+  return n;
+}
+
 
 std::atomic<unsigned long long> g_launches{0};
 
@@ -160,8 +178,7 @@ size_t dp_workspace_size(const dp_layer_desc* desc, int mode) {
   if (make_geom(desc, &g) != DP_OK) return 0;
   if (mode < DP_NORM_AUTO || mode > DP_NORM_T1) return 0;
   if (mode == DP_NORM_T1 && (g.T != 1 || g.conv)) return 0;
-  const int m = resolve_mode(g, mode);
-  return std::max(norm_ws_bytes(g, m), sum_ws_bytes(g));
+  return max_ws_bytes(g, resolve_mode(g, mode));
 }
 
 dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void* G, int mode,
@@ -173,7 +190,8 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
   if (!A || !G || !sqnorm_out) return fail(DP_ERR_INVALID_ARG, "A, G and sqnorm_out must be non-NULL");
   Geom g;
   make_geom(desc, &g);
-  const size_t need = norm_ws_bytes(g, chosen);
+  const bool tc = chosen == DP_NORM_GHOST && use_tc_ghost(g, desc->dtype, A, G);
+  const size_t need = norm_ws_bytes(g, chosen, tc);
   if (need && (!workspace || ws_bytes < need))
     return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? ws_bytes : (size_t)0);
@@ -184,8 +202,8 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
       e = dph::launch_t1_norm(g, desc->dtype, A, G, sqnorm_out, stream);
       break;
     case DP_NORM_GHOST:
-      if (dph::tc_ghost_supported(g) && desc->dtype == DP_BF16 && aligned16(A) && aligned16(G))
-        e = dph::launch_tc_ghost(g, A, G, sqnorm_out, ws, stream);
+      if (tc)
+        e = dph::launch_tc_ghost(g, A, G, sqnorm_out, ws, status_ptr(), stream);
       else
         e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream);
       break;
@@ -223,14 +241,15 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
   if (st != DP_OK) return st;
   if (!A || !G || !factors || !dW) return fail(DP_ERR_INVALID_ARG, "A, G, factors and dW must be non-NULL");
   if (db && !g.has_bias) return fail(DP_ERR_INVALID_ARG, "db given for a layer without bias");
-  const size_t need = sum_ws_bytes(g);
+  const bool tc = use_tc_sum(g, desc->dtype, A, G);
+  const size_t need = sum_ws_bytes(g, tc);
   if (need && (!workspace || ws_bytes < need))
     return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? ws_bytes : (size_t)0);
   cudaError_t e;
-  if (dph::tc_sum_supported(g) && desc->dtype == DP_BF16 && aligned16(A) && aligned16(G))
+  if (tc)
     e = dph::launch_tc_sum(g, A, G, factors, dW, db, accumulate, static_cast<float*>(workspace),
-                           stream);
+                           status_ptr(), stream);
   else
     e = dph::launch_simt_clipped_sum(g, desc->dtype, A, G, factors, dW, db, accumulate,
                                      static_cast<float*>(workspace), (int)dph::simt_sum_splits(g),

@@ -120,6 +120,9 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
 cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
                                   float sigma_l2, uint64_t seed, int layer, float* out,
                                   cudaStream_t s);
+// out[e] (+)= sum_k ws[k*n + e], fixed order.
+cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
+                                 cudaStream_t s);
 // SIMT (FFMA) paths: any dtype/shape.
 size_t simt_sum_splits(const Geom& g);
 cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, const void* G,

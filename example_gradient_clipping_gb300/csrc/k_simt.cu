@@ -299,6 +299,14 @@ cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, con
   return cudaGetLastError();
 }
 
+cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
+                                 cudaStream_t s) {
+  const size_t blocks = std::min<size_t>((n + 255) / 256, 152 * 8);
+  reduce_splits_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(ws, splits, n, out, accumulate);
+  count_launch();
+  return cudaGetLastError();
+}
+
 size_t simt_ghost_ws_floats(const Geom& g) {
   const long nb = cdiv(g.T, kGT);
   return (size_t)2 * g.B * (nb * (nb + 1) / 2);

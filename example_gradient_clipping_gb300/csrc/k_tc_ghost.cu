@@ -1,0 +1,238 @@
+// Ghost norm on the 5th-generation tensor cores ([MixGhost] eq. 2.7, Appendix C.3):
+//
+//   s_i = sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts} + has_bias * sum_{t,s} (G_i G_i^T)_{ts}
+//
+// The second term is ||sum_t g_t||^2, the bias gradient's squared norm.  One CTA per
+// example.  Rows are cut into 128-row blocks; for each block pair (tb <= sb) both
+// Gram tiles are accumulated in TMEM (two 128-column fp32 tiles), then read back
+// to form the Hadamard sum, weighted 2 off the diagonal (both Grams are symmetric).
+// TMEM holds two such pairs, so the epilogue of one pair overlaps the MMAs of the
+// next.  Operands are K-major (rows of A and G are contiguous), loaded by 3D TMA
+// boxes [1, 128 rows, 64 columns] whose rows past T read as zero.
+//   warp 0: TMA producer; warp 1: MMA issuer; warps 2-5: epilogue.
+#include <algorithm>
+
+#include "tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace dpk {
+namespace tcghost {
+
+constexpr int BT = 128, BK = 64, STAGES = 4;
+constexpr int TILE = BT * BK * 2;   // 16 KB
+constexpr int STAGE = 2 * TILE;     // t-block and s-block tiles
+constexpr int kThreads = 192;
+constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BT, BT, 0, 0);
+
+struct Params {
+  float* out;
+  unsigned* status;
+  int T, d, p, has_bias;
+};
+
+__device__ __forceinline__ void pair_of(int j, int nb, int& tb, int& sb) {
+  tb = 0;
+  while (j >= nb - tb) { j -= nb - tb; ++tb; }
+  sb = tb + j;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapG,
+                Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accum = empty + STAGES;       // [2]
+  uint64_t* tfree = accum + 2;            // [2]
+  uint64_t* drainb = tfree + 2;           // MMAs in flight at an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drainb + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(tmem_slot + 2);   // [8]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x;
+  const int nb = (P.T + BT - 1) / BT;
+  const int npairs = nb * (nb + 1) / 2;
+  const int kA = (P.d + BK - 1) / BK, kG = (P.p + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&accum[b], 1);
+      ptx::mbar_init(&tfree[b], 4);
+    }
+    ptx::mbar_init(drainb, 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&mapA);
+    ptx::prefetch_tensormap(&mapG);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int k = 0, issued = 0;
+      bool live = true;
+      for (int j = 0; j < npairs && live; ++j) {
+        int tb, sb;
+        pair_of(j, nb, tb, sb);
+        const bool diag = tb == sb;
+        for (int ph = 0; ph < 2 && live; ++ph) {
+          const CUtensorMap* map = ph == 0 ? &mapA : &mapG;
+          const int nk = ph == 0 ? kA : kG;
+          for (int kk = 0; kk < nk; ++kk, ++k) {
+            const int s = k % STAGES;
+            if (!ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status)) { live = false; break; }
+            uint8_t* st = smem + s * STAGE;
+            ptx::mbar_arrive_expect_tx(&full[s], diag ? TILE : STAGE);
+            ptx::tma_load_3d(map, &full[s], st, kk * BK, tb * BT, i);
+            if (!diag) ptx::tma_load_3d(map, &full[s], st + TILE, kk * BK, sb * BT, i);
+            ++issued;
+          }
+        }
+      }
+      if (*abort) {
+        for (int q = max(0, issued - STAGES); q < issued; ++q)
+          ptx::mbar_wait_drain(&full[q % STAGES], (q / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int k = 0;
+      bool live = true;
+      for (int j = 0; j < npairs && live; ++j) {
+        int tb, sb;
+        pair_of(j, nb, tb, sb);
+        const bool diag = tb == sb;
+        const int b = j & 1;
+        if (j >= 2 && !ptx::mbar_wait(&tfree[b], ((j >> 1) & 1) ^ 1, abort, P.status)) break;
+        ptx::tc_fence_after();
+        for (int ph = 0; ph < 2 && live; ++ph) {
+          const int nk = ph == 0 ? kA : kG;
+          const uint32_t d_tmem = tmem + b * 256 + ph * 128;
+          for (int kk = 0; kk < nk; ++kk, ++k) {
+            const int s = k % STAGES;
+            if (!ptx::mbar_wait(&full[s], (k / STAGES) & 1, abort, P.status)) { live = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t ta = ptx::smem_u32(smem + s * STAGE);
+            const uint32_t tbs = diag ? ta : ta + TILE;
+#pragma unroll
+            for (int u = 0; u < BK / 16; ++u) {
+              // K-major, 128-byte swizzle: 16 columns = 32 bytes along the swizzled row
+              const uint64_t da = ptx::sdesc_sw128(ta + u * 32, 16, 1024);
+              const uint64_t db = ptx::sdesc_sw128(tbs + u * 32, 16, 1024);
+              ptx::umma_bf16(d_tmem, da, db, kIdesc, (kk | u) != 0);
+            }
+            ptx::umma_commit(&empty[s]);
+          }
+        }
+        if (live) ptx::umma_commit(&accum[b]);
+      }
+    }
+  } else {
+    // ---- epilogue warps: lane quarter (warp & 3) of both Gram tiles ----
+    const int quarter = warp & 3;
+    float H = 0.f, S = 0.f;
+    bool ok = true;
+    for (int j = 0; j < npairs; ++j) {
+      int tb, sb;
+      pair_of(j, nb, tb, sb);
+      const int b = j & 1;
+      const bool w = ptx::mbar_wait(&accum[b], (j >> 1) & 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      ptx::tc_fence_after();
+      float h = 0.f, sg = 0.f;
+      const uint32_t base = tmem + b * 256 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BT / 32; ++c) {
+        float va[32], vg[32];
+        ptx::tmem_ld32(base + c * 32, va);
+        ptx::tmem_ld32(base + 128 + c * 32, vg);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          h = fmaf(va[e], vg[e], h);
+          sg += vg[e];
+        }
+      }
+      const float wgt = (tb == sb) ? 1.f : 2.f;
+      H = fmaf(wgt, h, H);
+      S = fmaf(wgt, sg, S);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tfree[b]);
+    }
+    H = warp_sum(H);
+    S = warp_sum(S);
+    if (lane == 0) {
+      red[(warp - 2) * 2] = H;
+      red[(warp - 2) * 2 + 1] = S;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps only
+    if (threadIdx.x == 64 && ok && !*abort) {
+      float h = 0.f, s = 0.f;
+      for (int q = 0; q < 4; ++q) { h += red[2 * q]; s += red[2 * q + 1]; }
+      P.out[i] = h + (P.has_bias ? s : 0.f);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort && threadIdx.x == 32) {
+    ptx::umma_commit(drainb);   // arrives once every MMA issued so far has completed
+    ptx::mbar_wait_drain(drainb, 0);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace tcghost
+}  // namespace dpk
+
+namespace dph {
+using namespace dpk;
+
+bool tc_ghost_supported(const Geom& g) {
+  return !g.conv && (g.d % 8 == 0) && (g.p % 8 == 0) && g.T >= 2 && g.T <= 512;
+}
+
+size_t tc_ghost_ws_bytes(const Geom&) { return 0; }
+
+cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* /*ws*/,
+                            unsigned* status, cudaStream_t s) {
+  CUtensorMap ma, mg;
+  const uint64_t da[3] = {(uint64_t)g.d, (uint64_t)g.T, (uint64_t)g.B};
+  const uint64_t sa[2] = {(uint64_t)g.d * 2, (uint64_t)g.T * g.d * 2};
+  const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
+  const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
+  const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
+  if (!encode_tmap_bf16(&ma, A, 3, da, sa, box) || !encode_tmap_bf16(&mg, G, 3, dg, sg, box))
+    return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcghost::tc_ghost_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tcghost::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias};
+  tcghost::tc_ghost_kernel<<<g.B, tcghost::kThreads, tcghost::SMEM, s>>>(ma, mg, P);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace dph

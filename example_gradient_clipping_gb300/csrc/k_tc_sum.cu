@@ -1,0 +1,326 @@
+// Clipped sum as one reweighted GEMM on the 5th-generation tensor cores.
+//
+//   dW[j, m] = sum_r c_{r/T} G[r, j] A[r, m],   db[j] = sum_r c_{r/T} G[r, j],   r < R = B*T
+//
+// ([FastClip] section 5: the gradient of the reweighted loss sum_i c_i l_i is the
+// clipped sum; [MixGhost] section 3.2: the second back-propagation's weight GEMM.)
+// MMA view: D[M = p-tile, N = d-tile] += G^T[M, K] A[K, N] over K = batch rows; both
+// operands are MN-major in memory (rows of G and A are contiguous along p and d).
+//
+// Per CTA: one 128 x 256 output tile over a contiguous range of rows (split-K).
+//   warp 0     TMA producer: per stage two 64x64 boxes of G and four of A (128B swizzle)
+//   warp 1     MMA issuer: four 128x256x16 tcgen05.mma per stage into TMEM (256 columns)
+//   warps 2-5  scale: multiply each row of the G tile in shared memory by its example's
+//              clip factor (zero outside the CTA's rows) and accumulate the bias sums;
+//              then the epilogue: TMEM -> registers -> fp32 partial tile.
+// Partials [split, p, d] are reduced in a fixed order (deterministic) by a second kernel.
+#include <algorithm>
+#include <cudaTypedefs.h>
+
+#include "tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace dpk {
+namespace tcsum {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int G_TILE = BM * BK * 2;            // 16 KB: two 64-column boxes
+constexpr int A_TILE = BN * BK * 2;            // 32 KB: four 64-column boxes
+constexpr int BOX = 64 * BK * 2;               // 8 KB
+constexpr int STAGE = G_TILE + A_TILE;
+constexpr int kThreads = 192;
+constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, BN, 1, 1);
+
+struct Params {
+  const float* factors;
+  float* ws;        // [splits, p, d]
+  float* ws_db;     // [splits, p] or null
+  unsigned* status;
+  long R, rows_per_split;
+  int T, p, d;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapA,
+              Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+  uint64_t* scaled = full + STAGES;
+  uint64_t* empty = scaled + STAGES;
+  uint64_t* accum = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN, split = blockIdx.z;
+  const long r0 = (long)split * P.rows_per_split;
+  const long r1 = min(P.R, r0 + P.rows_per_split);
+  const int nk = (int)((r1 - r0 + BK - 1) / BK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&scaled[s], 4);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(accum, 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&mapG);
+    ptx::prefetch_tensormap(&mapA);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, 256);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int k = 0; k < nk; ++k) {
+        const int s = k % STAGES;
+        if (!ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status)) break;
+        uint8_t* st = smem + s * STAGE;
+        ptx::mbar_arrive_expect_tx(&full[s], STAGE);
+        const int row = (int)(r0 + (long)k * BK);
+        ptx::tma_load_2d(&mapG, &full[s], st, m0, row);
+        ptx::tma_load_2d(&mapG, &full[s], st + BOX, m0 + 64, row);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ptx::tma_load_2d(&mapA, &full[s], st + G_TILE + j * BOX, n0 + 64 * j, row);
+        ++issued;
+      }
+      if (*abort) {   // let the copies already in flight land before the CTA exits
+        for (int k = max(0, issued - STAGES); k < issued; ++k)
+          ptx::mbar_wait_drain(&full[k % STAGES], (k / STAGES) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int k = 0; k < nk; ++k) {
+        const int s = k % STAGES;
+        if (!ptx::mbar_wait(&scaled[s], (k / STAGES) & 1, abort, P.status)) break;
+        ptx::tc_fence_after();
+        const uint32_t g = ptx::smem_u32(smem + s * STAGE);
+        const uint32_t a = g + G_TILE;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // 16 rows per MMA = two 8-row groups of 1024 B; MN chunks of 64 are 8 KB apart
+          const uint64_t da = ptx::sdesc_sw128(g + kk * 2048, BOX, 1024);
+          const uint64_t db = ptx::sdesc_sw128(a + kk * 2048, BOX, 1024);
+          ptx::umma_bf16(tmem, da, db, kIdesc, (k | kk) != 0);
+        }
+        ptx::umma_commit(&empty[s]);
+      }
+      ptx::umma_commit(accum);
+    }
+  } else {
+    // ---- scale warps (128 threads) ----
+    const int t = threadIdx.x - 64;
+    const int j = t & 7;            // row phase within each 8-row group
+    const int cg = t >> 3;          // 16 column groups of 8 elements: box (0/1) and 16-byte chunk
+    const int box = cg >> 3, q = cg & 7;
+    float dbacc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dbacc[e] = 0.f;
+    bool ok = true;
+    for (int k = 0; k < nk && ok; ++k) {
+      const int s = k % STAGES;
+      const bool w = ptx::mbar_wait(&full[s], (k / STAGES) & 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      uint8_t* gt = smem + s * STAGE + box * BOX;
+      const long rowbase = r0 + (long)k * BK;
+#pragma unroll
+      for (int rr = 0; rr < BK / 8; ++rr) {
+        const int r = rr * 8 + j;
+        const long row = rowbase + r;
+        const float c = (row < r1) ? __ldg(P.factors + (int)row / P.T) : 0.f;
+        // 128-byte swizzle: the 16-byte chunk q of row r sits at chunk q ^ (r % 8)
+        uint4* ptr = reinterpret_cast<uint4*>(gt + r * 128 + ((q ^ j) << 4));
+        uint4 v = *ptr;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(h[e]);
+          f.x *= c;
+          f.y *= c;
+          dbacc[2 * e] += f.x;
+          dbacc[2 * e + 1] += f.y;
+          h[e] = __floats2bfloat162_rn(f.x, f.y);
+        }
+        *ptr = v;
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&scaled[s]);
+    }
+    // bias partial sums: the 8 threads sharing a column group are lanes 8u..8u+7
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float v = dbacc[e];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      dbacc[e] = v;
+    }
+    if (ok && P.ws_db && blockIdx.y == 0 && j == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int col = m0 + box * 64 + q * 8 + e;
+        if (col < P.p) P.ws_db[(size_t)split * P.p + col] = dbacc[e];
+      }
+    }
+    // ---- epilogue: each thread owns one accumulator row (TMEM lane) ----
+    const bool w = ok && ptx::mbar_wait(accum, 0, abort, P.status);
+    if (__all_sync(0xffffffffu, w)) {
+      ptx::tc_fence_after();
+      const int quarter = warp & 3;
+      const int m = m0 + quarter * 32 + lane;
+      float* out = P.ws + ((size_t)split * P.p + m) * P.d;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
+        ptx::tmem_wait_ld();
+        const int n = n0 + c * 32;
+        if (m < P.p) {
+          if (n + 32 <= P.d && (P.d & 3) == 0) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(out + n + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (n + e < P.d) out[n + e] = v[e];
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort && threadIdx.x == 32) ptx::mbar_wait_drain(accum, 0);   // MMAs in flight
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace tcsum
+}  // namespace dpk
+
+namespace dph {
+using namespace dpk;
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides_bytes[i];
+  }
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int cdiv_i(long a, long b) { return (int)((a + b - 1) / b); }
+
+// Split of the batch rows over CTAs: enough splits to cover the SMs with output
+// tiles, each split a whole number of 64-row stages and every split non-empty.
+static void tc_sum_split(const Geom& g, int* splits_out, long* rows_per_split) {
+  const long tiles = (long)cdiv_i(g.p, tcsum::BM) * cdiv_i(g.D, tcsum::BN);
+  const long R = (long)g.B * g.T;
+  long splits = std::max<long>(1, 152 / tiles);
+  splits = std::min<long>(splits, std::max<long>(1, R / (4 * tcsum::BK)));
+  long rps = (R + splits - 1) / splits;
+  rps = (rps + tcsum::BK - 1) / tcsum::BK * tcsum::BK;
+  *splits_out = (int)((R + rps - 1) / rps);
+  *rows_per_split = rps;
+}
+
+static int tc_sum_splits(const Geom& g) {
+  int s;
+  long rps;
+  tc_sum_split(g, &s, &rps);
+  return s;
+}
+
+bool tc_sum_supported(const Geom& g) {
+  // linear layers whose rows are 16-byte multiples (TMA strides), wide enough for the tile
+  return !g.conv && (g.p % 8 == 0) && (g.D % 8 == 0) && g.p >= 64 && g.D >= 64 &&
+         (long)g.B * g.T < (1L << 31);
+}
+
+size_t tc_sum_ws_bytes(const Geom& g) {
+  return (size_t)tc_sum_splits(g) * ((size_t)g.p * g.D + g.p) * sizeof(float);
+}
+
+cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
+                          float* dW, float* db, int accumulate, float* ws, unsigned* status,
+                          cudaStream_t s) {
+  const long R = (long)g.B * g.T;
+  CUtensorMap mg, ma;
+  const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)R}, sg[1] = {(uint64_t)g.p * 2};
+  const uint64_t da[2] = {(uint64_t)g.D, (uint64_t)R}, sa[1] = {(uint64_t)g.D * 2};
+  const uint32_t box[2] = {64, tcsum::BK};
+  if (!encode_tmap_bf16(&mg, G, 2, dg, sg, box) || !encode_tmap_bf16(&ma, A, 2, da, sa, box))
+    return cudaErrorInvalidValue;
+  int splits;
+  long rps;
+  tc_sum_split(g, &splits, &rps);
+  tcsum::Params P;
+  P.factors = factors;
+  P.ws = ws;
+  P.ws_db = db ? ws + (size_t)splits * g.p * g.D : nullptr;
+  P.status = status;
+  P.R = R;
+  P.rows_per_split = rps;
+  P.T = g.T;
+  P.p = g.p;
+  P.d = g.D;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcsum::tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tcsum::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  dim3 grid(cdiv_i(g.p, tcsum::BM), cdiv_i(g.D, tcsum::BN), splits);
+  tcsum::tc_sum_kernel<<<grid, tcsum::kThreads, tcsum::SMEM, s>>>(mg, ma, P);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_reduce_splits(ws, splits, (size_t)g.p * g.D, dW, accumulate, s);
+  if (e != cudaSuccess) return e;
+  if (db) e = launch_reduce_splits(P.ws_db, splits, (size_t)g.p, db, accumulate, s);
+  return e;
+}
+
+}  // namespace dph

@@ -1,5 +1,7 @@
 // Tensor-core (tcgen05 / TMEM / TMA) kernels of libdpclip: declarations.
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace dph {
@@ -8,10 +10,14 @@ using dpk::Geom;
 bool tc_sum_supported(const Geom& g);
 size_t tc_sum_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
-                          float* dW, float* db, int accumulate, float* ws, cudaStream_t s);
+                          float* dW, float* db, int accumulate, float* ws, unsigned* status,
+                          cudaStream_t s);
 // Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).
 bool tc_ghost_supported(const Geom& g);
 size_t tc_ghost_ws_bytes(const Geom& g);
 cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* ws,
-                            cudaStream_t s);
+                            unsigned* status, cudaStream_t s);
+// 2D/3D bf16 tensor map with 128-byte swizzle (dims innermost first, strides in bytes).
+bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box);
 }  // namespace dph

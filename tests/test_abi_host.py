@@ -98,8 +98,9 @@ def test_invalid_calls_launch_nothing(dp):
     with pytest.raises(dp.DPError) as e:
         dp.dp_layer_sqnorms(d, 0, 0, 0, None, 0, stream=0)
     assert e.value.status == dp.DP_ERR_INVALID_ARG and "non-NULL" in str(e.value)
-    with pytest.raises(dp.DPError) as e:   # workspace too small
-        dp.dp_layer_sqnorms(d, 16, 16, 16, 16, 1, mode=dp.DP_NORM_GHOST, stream=0)
+    d32 = dp.layer_desc(dp.DP_LINEAR, dp.DP_FP32, B=4, p=8, T=3, d=8)
+    with pytest.raises(dp.DPError) as e:   # workspace too small (fp32 runs on the SIMT path)
+        dp.dp_layer_sqnorms(d32, 16, 16, 16, 16, 1, mode=dp.DP_NORM_GHOST, stream=0)
     assert e.value.status == dp.DP_ERR_INVALID_ARG and "workspace" in str(e.value)
     with pytest.raises(dp.DPError) as e:
         dp.dp_plan(d, dp.DP_NORM_T1)

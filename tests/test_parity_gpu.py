@@ -171,6 +171,10 @@ EDGE = [
     ("lin_nobias", LayerSpec("e", "linear", p=64, d=96, T=130, has_bias=False), 3, "bf16"),
     ("lin_t1_odd", LayerSpec("e", "linear", p=10, d=13, T=1), 9, "bf16"),
     ("lin_t1_fp32_odd", LayerSpec("e", "linear", p=7, d=5, T=1), 3, "fp32"),
+    ("lin_tc_ragged", LayerSpec("e", "linear", p=72, d=200, T=33), 5, "bf16"),
+    ("lin_tc_T256", LayerSpec("e", "linear", p=128, d=64, T=256), 3, "bf16"),
+    ("lin_tc_splits", LayerSpec("e", "linear", p=128, d=256, T=50), 37, "bf16"),
+    ("lin_tc_T300", LayerSpec("e", "linear", p=64, d=136, T=300, has_bias=False), 2, "bf16"),
     ("conv_s2", LayerSpec("e", "conv2d", p=6, Cin=5, H=11, W=9, k=3, stride=2, pad=1), 3, "bf16"),
     ("conv_dil", LayerSpec("e", "conv2d", p=4, Cin=3, H=10, W=10, k=3, stride=1, pad=2, dil=2), 2, "fp32"),
     ("conv_k1", LayerSpec("e", "conv2d", p=8, Cin=16, H=6, W=6, k=1), 3, "bf16"),
@@ -182,8 +186,6 @@ EDGE = [
 def test_edge_shapes(lib, tag, spec, B, dtype):
     wl = Workload(name=tag, B=B, layers=(spec,), dtype=dtype, C=1.0, sigma=1.0, seed=11)
     for mode in (None, lib.DP_NORM_GHOST, lib.DP_NORM_INSTANTIATE):
-        if mode is not None and spec.rows == 1 and spec.kind == "linear" and mode == lib.DP_NORM_T1:
-            continue
         _check_layer(lib, spec, wl, mode=mode)
 
 
