@@ -221,49 +221,48 @@ def run_ours(args, wl):
     work = step_work(wl, modes)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    # events around each C-ABI call of the step, on the launching stream
-    names = ["norms", "factors", "sums", "noise"]
+    # The whole step is one CUDA graph (norms -> factors -> clipped sums -> noise),
+    # replayed once per step; every kernel in it is a library kernel.
+    step.capture(dev_in)
+    # per-call graphs, timed separately for the per-kernel roofline
+    call_graphs = {}
+    for name, fn in (("norms", lambda: step.norms(dev_in)), ("factors", lambda: step.factors_()),
+                     ("sums", lambda: step.sums(dev_in)), ("noise", lambda: step.noise_devseed())):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        call_graphs[name] = g
 
-    def one_step(k, evs=None):
-        seed = wl.seed + 1_000_003 * (rank + 1) + k
-        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
-        rec(0)
-        step.norms(dev_in)
-        rec(1)
-        step.factors_()
-        rec(2)
-        step.sums(dev_in)
-        rec(3)
-        step.noise(seed)
-        rec(4)
+    def timed(replay, k_steps, seed_base):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(k_steps)]
+        for k in range(k_steps):
+            flush.zero_()                         # L2 flush, outside the events
+            step.seed_buf.fill_(seed_base + k)    # fresh noise seed, outside the events
+            evs[k][0].record(stream)
+            replay()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
 
-    for w in range(max(args.warmup, 3)):
-        flush.zero_()
-        one_step(-1 - w)
-    torch.cuda.synchronize()
-
-    all_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    launches0 = dp.dp_launch_count()
+    seed0 = wl.seed + 1_000_003 * (rank + 1)
+    timed(step.graph.replay, max(args.warmup, 3), seed0)      # warm-up
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
-        for k in range(args.steps):
-            flush.zero_()           # L2 flush outside the events
-            one_step(k, all_evs[k])
-        torch.cuda.synchronize()
+        step_ms = timed(step.graph.replay, args.steps, seed0)
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    launches = dp.dp_launch_count() - launches0
-    per_call = {n: [all_evs[k][i].elapsed_time(all_evs[k][i + 1]) for k in range(args.steps)]
-                for i, n in enumerate(names)}
-    step_ms = [all_evs[k][0].elapsed_time(all_evs[k][4]) for k in range(args.steps)]
+    launches = step.graph_kernels * args.steps
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     value = world * wl.B * args.steps / (total_ms / 1e3)
+    per_call = {n: timed(g.replay, args.steps, seed0) for n, g in call_graphs.items()}
 
     # end to end through the public API: pinned host inputs copied in, result copied out
     pinned = [(workloads.to_torch(A, wl.dtype).pin_memory(), workloads.to_torch(G, wl.dtype).pin_memory())
@@ -279,7 +278,7 @@ def run_ours(args, wl):
         for (ha, hg), (da, dg) in zip(pinned, dev_in):
             da.copy_(ha, non_blocking=True)
             dg.copy_(hg, non_blocking=True)
-        g = step.run(dev_in, seed=wl.seed + 7 * k)
+        g = step.replay(wl.seed + 7 * k)
         out_host.copy_(g, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -310,6 +309,7 @@ def run_ours(args, wl):
     roof["kernel"] = {"sums": "dp_clipped_sum", "norms": "dp_layer_sqnorms", "noise": "dp_add_noise",
                       "factors": "dp_clip_factors"}[dom]
     roof["peak_source"] = f"{pk['src']} (burst)"
+    roof["timing"] = "the call's own CUDA graph, replayed after an L2 flush, CUDA events"
 
     line = None
     if rank == 0:
@@ -320,6 +320,7 @@ def run_ours(args, wl):
                     e2e=dict(value=e2e_value, unit="examples/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
                     gpu_launches=int(launches), roofline=roof, clocks=clk.summary(),
                     calls_ms={n: round(v, 5) for n, v in means.items()},
+                    kernels_per_step=step.graph_kernels,
                     step_flop=work["flop_norm"] + work["flop_sum"], step_bytes=work["bytes_total"])
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, host_in)
@@ -336,9 +337,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (profiling and sweeps; not the bench line)")
     args = ap.parse_args()
     import workloads
     wl = workloads.get_workload(args.workload)
+    if args.batch:
+        wl = wl.with_batch(args.batch)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

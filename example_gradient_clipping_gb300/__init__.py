@@ -58,6 +58,7 @@ def _load():
         "dp_clip_factors": (c_int, [c_void, c_int, c_int, c_int, ctypes.POINTER(c_f), c_void, c_void]),
         "dp_clipped_sum": (c_int, [PD, c_void, c_void, c_void, c_void, c_void, c_int, c_void, c_size, c_void]),
         "dp_add_noise": (c_int, [c_void, c_size, c_f, c_f, c_int, c_u64, c_u64, c_void]),
+        "dp_add_noise_devseed": (c_int, [c_void, c_size, c_f, c_f, c_int, c_void, c_u64, c_void]),
         "dp_adaptive_bound": (c_int, [c_void, c_int, c_f, c_f, c_f, c_f, c_u64, c_int, c_void, c_void]),
         "dp_check_status": (c_int, [c_void]),
     }
@@ -152,6 +153,14 @@ def dp_add_noise(grad, sigma: float, C: float, B: int, seed: int, offset: int = 
     if n is None:
         n = grad.numel()
     _check(_lib.dp_add_noise(_ptr(grad), n, sigma, C, B, seed, offset, _stream(stream)))
+
+
+def dp_add_noise_devseed(grad, sigma: float, C: float, B: int, seed_dev, offset: int = 0,
+                         n: Optional[int] = None, stream=None) -> None:
+    """dp_add_noise reading the 64-bit seed from device memory (for CUDA-graph replays)."""
+    if n is None:
+        n = grad.numel()
+    _check(_lib.dp_add_noise_devseed(_ptr(grad), n, sigma, C, B, _ptr(seed_dev), offset, _stream(stream)))
 
 
 def dp_adaptive_bound(sqnorms, B: int, C_l2: float, alpha: float, beta: float, sigma_l2: float,

@@ -104,8 +104,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Which kernel serves a call: the tensor-core kernels take bf16 inputs with 16-byte
 // aligned base pointers and the shapes they support; everything else runs SIMT.
-bool use_tc_sum(const Geom& g, int dtype, const void* A, const void* G) {
-  return dtype == DP_BF16 && dph::tc_sum_supported(g) && aligned16(A) && aligned16(G);
+// 0: SIMT, 1: row-scaled tensor-core GEMM, 2: per-example tensor-core accumulation
+int sum_path(const Geom& g, int dtype, const void* A, const void* G) {
+  if (dtype != DP_BF16 || !aligned16(A) || !aligned16(G)) return 0;
+  if (dph::tc_sumx_supported(g)) return 2;
+  if (dph::tc_sum_supported(g)) return 1;
+  return 0;
 }
 bool use_tc_ghost(const Geom& g, int dtype, const void* A, const void* G) {
   return dtype == DP_BF16 && dph::tc_ghost_supported(g) && aligned16(A) && aligned16(G);
@@ -116,7 +120,9 @@ size_t simt_sum_bytes(const Geom& g) {
 }
 
 // Workspace a call needs on the path it takes.
-size_t sum_ws_bytes(const Geom& g, bool tc) { return tc ? dph::tc_sum_ws_bytes(g) : simt_sum_bytes(g); }
+size_t sum_ws_bytes(const Geom& g, int path) {
+  return path == 2 ? dph::tc_sumx_ws_bytes(g) : path == 1 ? dph::tc_sum_ws_bytes(g) : simt_sum_bytes(g);
+}
 
 size_t norm_ws_bytes(const Geom& g, int mode, bool tc) {
   switch (mode) {
@@ -133,6 +139,7 @@ size_t max_ws_bytes(const Geom& g, int mode) {
   size_t n = std::max(norm_ws_bytes(g, mode, false), simt_sum_bytes(g));
   if (dph::tc_ghost_supported(g)) n = std::max(n, norm_ws_bytes(g, mode, true));
   if (dph::tc_sum_supported(g)) n = std::max(n, dph::tc_sum_ws_bytes(g));
+  if (dph::tc_sumx_supported(g)) n = std::max(n, dph::tc_sumx_ws_bytes(g));
   return n;
 }
 
@@ -241,13 +248,15 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
   if (st != DP_OK) return st;
   if (!A || !G || !factors || !dW) return fail(DP_ERR_INVALID_ARG, "A, G, factors and dW must be non-NULL");
   if (db && !g.has_bias) return fail(DP_ERR_INVALID_ARG, "db given for a layer without bias");
-  const bool tc = use_tc_sum(g, desc->dtype, A, G);
-  const size_t need = sum_ws_bytes(g, tc);
+  const int path = sum_path(g, desc->dtype, A, G);
+  const size_t need = sum_ws_bytes(g, path);
   if (need && (!workspace || ws_bytes < need))
     return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? ws_bytes : (size_t)0);
   cudaError_t e;
-  if (tc)
+  if (path == 2)
+    e = dph::launch_tc_sumx(g, A, G, factors, dW, db, accumulate, workspace, status_ptr(), stream);
+  else if (path == 1)
     e = dph::launch_tc_sum(g, A, G, factors, dW, db, accumulate, static_cast<float*>(workspace),
                            status_ptr(), stream);
   else
@@ -258,8 +267,8 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
   return ok();
 }
 
-dp_status dp_add_noise(float* grad, size_t n, float sigma, float C, int B, uint64_t seed,
-                       uint64_t offset, cudaStream_t stream) {
+static dp_status add_noise_impl(float* grad, size_t n, float sigma, float C, int B, uint64_t seed,
+                                const unsigned long long* seed_dev, uint64_t offset, cudaStream_t stream) {
   if (n == 0) return ok();
   if (!grad) return fail(DP_ERR_INVALID_ARG, "grad is NULL");
   if (B <= 0) return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0", B);
@@ -268,9 +277,21 @@ dp_status dp_add_noise(float* grad, size_t n, float sigma, float C, int B, uint6
   if (offset + n < offset) return fail(DP_ERR_INVALID_ARG, "offset + n overflows");
   const float sc = (float)((double)sigma * (double)C);
   const float invB = (float)(1.0 / (double)B);
-  cudaError_t e = dph::launch_add_noise(grad, n, sc, invB, seed, offset, stream);
+  cudaError_t e = dph::launch_add_noise(grad, n, sc, invB, seed, offset, seed_dev, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_add_noise launch");
   return ok();
+}
+
+dp_status dp_add_noise(float* grad, size_t n, float sigma, float C, int B, uint64_t seed,
+                       uint64_t offset, cudaStream_t stream) {
+  return add_noise_impl(grad, n, sigma, C, B, seed, nullptr, offset, stream);
+}
+
+dp_status dp_add_noise_devseed(float* grad, size_t n, float sigma, float C, int B,
+                               const unsigned long long* seed_dev, uint64_t offset,
+                               cudaStream_t stream) {
+  if (!seed_dev && n) return fail(DP_ERR_INVALID_ARG, "seed_dev is NULL");
+  return add_noise_impl(grad, n, sigma, C, B, 0, seed_dev, offset, stream);
 }
 
 dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha, float beta,

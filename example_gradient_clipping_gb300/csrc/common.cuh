@@ -116,7 +116,7 @@ cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* 
 cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, const float* C,
                                 float* out, unsigned* status, cudaStream_t s);
 cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,
-                             uint64_t offset, cudaStream_t s);
+                             uint64_t offset, const unsigned long long* seed_dev, cudaStream_t s);
 cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
                                   float sigma_l2, uint64_t seed, int layer, float* out,
                                   cudaStream_t s);

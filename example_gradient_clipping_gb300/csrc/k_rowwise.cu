@@ -78,7 +78,9 @@ __global__ void clip_factors_kernel(const float* __restrict__ sq, int B, int L, 
 // One thread per Philox block of four consecutive elements of the global index;
 // float4 load/store when the four lie in range and are 16-byte aligned.
 __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad, size_t n, float sc,
-                                                        float invB, uint64_t seed, uint64_t offset) {
+                                                        float invB, uint64_t seed, uint64_t offset,
+                                                        const unsigned long long* __restrict__ seed_dev) {
+  if (seed_dev) seed = *seed_dev;
   const uint64_t q0 = offset >> 2;
   const uint64_t q1 = (offset + n + 3) >> 2;  // one past the last block touched
   const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -168,13 +170,13 @@ cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, co
 }
 
 cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,
-                             uint64_t offset, cudaStream_t s) {
+                             uint64_t offset, const unsigned long long* seed_dev, cudaStream_t s) {
   const uint64_t blocks4 = ((offset + n + 3) >> 2) - (offset >> 2);
   uint64_t grid = (blocks4 + 255) / 256;
   const uint64_t cap = 152ull * 8ull;   // grid-stride beyond 8 resident blocks per SM
   if (grid > cap) grid = cap;
   if (grid == 0) grid = 1;
-  add_noise_kernel<<<(unsigned)grid, 256, 0, s>>>(grad, n, sc, invB, seed, offset);
+  add_noise_kernel<<<(unsigned)grid, 256, 0, s>>>(grad, n, sc, invB, seed, offset, seed_dev);
   count_launch();
   return cudaGetLastError();
 }

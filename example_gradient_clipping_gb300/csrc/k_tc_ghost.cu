@@ -8,8 +8,11 @@
 // to form the Hadamard sum, weighted 2 off the diagonal (both Grams are symmetric).
 // TMEM holds two such pairs, so the epilogue of one pair overlaps the MMAs of the
 // next.  Operands are K-major (rows of A and G are contiguous), loaded by 3D TMA
-// boxes [1, 128 rows, 64 columns] whose rows past T read as zero.
-//   warp 0: TMA producer; warp 1: MMA issuer; warps 2-5: epilogue.
+// boxes [1, 128 rows, 64 columns] whose rows past T read as zero, into a ring of
+// eight 16 KB slots: a diagonal block pair takes one slot per K step (the tile is
+// both operands), an off-diagonal pair two.
+//   warps 0 and 6: TMA producers (alternate slots: one issuing thread streams only
+//   ~48 B/clk into an SM); warp 1: MMA issuer; warps 2-5: epilogue.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -18,10 +21,10 @@
 namespace dpk {
 namespace tcghost {
 
-constexpr int BT = 128, BK = 64, STAGES = 4;
+constexpr int BT = 128, BK = 64, STAGES = 8;
 constexpr int TILE = BT * BK * 2;   // 16 KB
-constexpr int STAGE = 2 * TILE;     // t-block and s-block tiles
-constexpr int kThreads = 192;
+constexpr int STAGE = TILE;         // one tile per slot
+constexpr int kThreads = 224;
 constexpr int SMEM = STAGES * STAGE + 1024 + 256;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BT, BT, 0, 0);
 
@@ -78,67 +81,84 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      int k = 0, issued = 0;
-      bool live = true;
-      for (int j = 0; j < npairs && live; ++j) {
-        int tb, sb;
-        pair_of(j, nb, tb, sb);
-        const bool diag = tb == sb;
-        for (int ph = 0; ph < 2 && live; ++ph) {
-          const CUtensorMap* map = ph == 0 ? &mapA : &mapG;
-          const int nk = ph == 0 ? kA : kG;
-          for (int kk = 0; kk < nk; ++kk, ++k) {
+  if (warp == 0 || warp == 6) {
+    // TMA producers (whole warp; the elected lane issues); producer pr loads slots k % 2 == pr
+    const int pr = warp == 6 ? 1 : 0;
+    int k = 0, issued = 0, last = -1;
+    bool live = true;
+    for (int j = 0; j < npairs && live; ++j) {
+      int tb, sb;
+      pair_of(j, nb, tb, sb);
+      const bool diag = tb == sb;
+      for (int ph = 0; ph < 2 && live; ++ph) {
+        const CUtensorMap* map = ph == 0 ? &mapA : &mapG;
+        const int nk = ph == 0 ? kA : kG;
+        for (int kk = 0; kk < nk; ++kk) {
+          for (int h = 0; h < (diag ? 1 : 2); ++h, ++k) {
+            if ((k & 1) != pr) continue;
             const int s = k % STAGES;
-            if (!ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status)) { live = false; break; }
-            uint8_t* st = smem + s * STAGE;
-            ptx::mbar_arrive_expect_tx(&full[s], diag ? TILE : STAGE);
-            ptx::tma_load_3d(map, &full[s], st, kk * BK, tb * BT, i);
-            if (!diag) ptx::tma_load_3d(map, &full[s], st + TILE, kk * BK, sb * BT, i);
-            ++issued;
-          }
-        }
-      }
-      if (*abort) {
-        for (int q = max(0, issued - STAGES); q < issued; ++q)
-          ptx::mbar_wait_drain(&full[q % STAGES], (q / STAGES) & 1);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      int k = 0;
-      bool live = true;
-      for (int j = 0; j < npairs && live; ++j) {
-        int tb, sb;
-        pair_of(j, nb, tb, sb);
-        const bool diag = tb == sb;
-        const int b = j & 1;
-        if (j >= 2 && !ptx::mbar_wait(&tfree[b], ((j >> 1) & 1) ^ 1, abort, P.status)) break;
-        ptx::tc_fence_after();
-        for (int ph = 0; ph < 2 && live; ++ph) {
-          const int nk = ph == 0 ? kA : kG;
-          const uint32_t d_tmem = tmem + b * 256 + ph * 128;
-          for (int kk = 0; kk < nk; ++kk, ++k) {
-            const int s = k % STAGES;
-            if (!ptx::mbar_wait(&full[s], (k / STAGES) & 1, abort, P.status)) { live = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t ta = ptx::smem_u32(smem + s * STAGE);
-            const uint32_t tbs = diag ? ta : ta + TILE;
-#pragma unroll
-            for (int u = 0; u < BK / 16; ++u) {
-              // K-major, 128-byte swizzle: 16 columns = 32 bytes along the swizzled row
-              const uint64_t da = ptx::sdesc_sw128(ta + u * 32, 16, 1024);
-              const uint64_t db = ptx::sdesc_sw128(tbs + u * 32, 16, 1024);
-              ptx::umma_bf16(d_tmem, da, db, kIdesc, (kk | u) != 0);
+            const bool w = ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
+            if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+            if (ptx::elect_one()) {
+              ptx::mbar_arrive_expect_tx(&full[s], TILE);
+              ptx::tma_load_3d(map, &full[s], smem + s * STAGE, kk * BK, (h ? sb : tb) * BT, i);
             }
-            ptx::umma_commit(&empty[s]);
+            __syncwarp();
+            ++issued;
+            last = k;
           }
+          if (!live) break;
         }
-        if (live) ptx::umma_commit(&accum[b]);
       }
     }
-  } else {
+    if (*abort && lane == 0) {   // let this producer's copies in flight land
+      for (int q = max(0, last - STAGES + 1); q <= last; ++q)
+        if ((q & 1) == pr) ptx::mbar_wait_drain(&full[q % STAGES], (q / STAGES) & 1);
+    }
+    (void)issued;
+  } else if (warp == 1) {
+    // MMA issuer (whole warp; the elected lane issues)
+    int k = 0;
+    bool live = true;
+    for (int j = 0; j < npairs && live; ++j) {
+      int tb, sb;
+      pair_of(j, nb, tb, sb);
+      const bool diag = tb == sb;
+      const int b = j & 1;
+      if (j >= 2) {
+        const bool w = ptx::mbar_wait(&tfree[b], ((j >> 1) & 1) ^ 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) break;
+      }
+      ptx::tc_fence_after();
+      for (int ph = 0; ph < 2 && live; ++ph) {
+        const int nk = ph == 0 ? kA : kG;
+        const uint32_t d_tmem = tmem + b * 256 + ph * 128;
+        for (int kk = 0; kk < nk; ++kk) {
+          const int s0 = k % STAGES, s1 = (k + 1) % STAGES;
+          bool w = ptx::mbar_wait(&full[s0], (k / STAGES) & 1, abort, P.status);
+          if (!diag) w = w && ptx::mbar_wait(&full[s1], ((k + 1) / STAGES) & 1, abort, P.status);
+          if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+          // (no tcgen05 fence per K step: the mbarrier orders the TMA data)
+          // K-major, 128-byte swizzle: 16 columns = 32 bytes along the swizzled row
+          const uint64_t da = ptx::sdesc_sw128(ptx::smem_u32(smem + s0 * STAGE), 16, 1024);
+          const uint64_t db = diag ? da : ptx::sdesc_sw128(ptx::smem_u32(smem + s1 * STAGE), 16, 1024);
+          if (ptx::elect_one()) {
+#pragma unroll
+            for (int u = 0; u < BK / 16; ++u)
+              ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, u * 32), ptx::sdesc_add(db, u * 32), kIdesc, (kk | u) != 0);
+            ptx::umma_commit(&empty[s0]);
+            if (!diag) ptx::umma_commit(&empty[s1]);
+          }
+          __syncwarp();
+          k += diag ? 1 : 2;
+        }
+      }
+      if (live) {
+        if (ptx::elect_one()) ptx::umma_commit(&accum[b]);
+        __syncwarp();
+      }
+    }
+  } else if (warp < 6) {
     // ---- epilogue warps: lane quarter (warp & 3) of both Gram tiles ----
     const int quarter = warp & 3;
     float H = 0.f, S = 0.f;

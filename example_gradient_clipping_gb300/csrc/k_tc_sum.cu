@@ -78,44 +78,49 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int k = 0; k < nk; ++k) {
-        const int s = k % STAGES;
-        if (!ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status)) break;
-        uint8_t* st = smem + s * STAGE;
+    // TMA producer (whole warp; the elected lane issues)
+    int issued = 0;
+    for (int k = 0; k < nk; ++k) {
+      const int s = k % STAGES;
+      const bool w = ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) break;
+      uint8_t* st = smem + s * STAGE;
+      const int row = (int)(r0 + (long)k * BK);
+      if (ptx::elect_one()) {
         ptx::mbar_arrive_expect_tx(&full[s], STAGE);
-        const int row = (int)(r0 + (long)k * BK);
         ptx::tma_load_2d(&mapG, &full[s], st, m0, row);
         ptx::tma_load_2d(&mapG, &full[s], st + BOX, m0 + 64, row);
 #pragma unroll
         for (int j = 0; j < 4; ++j) ptx::tma_load_2d(&mapA, &full[s], st + G_TILE + j * BOX, n0 + 64 * j, row);
-        ++issued;
       }
-      if (*abort) {   // let the copies already in flight land before the CTA exits
-        for (int k = max(0, issued - STAGES); k < issued; ++k)
-          ptx::mbar_wait_drain(&full[k % STAGES], (k / STAGES) & 1);
-      }
+      __syncwarp();
+      ++issued;
+    }
+    if (*abort && lane == 0) {   // let the copies already in flight land before the CTA exits
+      for (int k = max(0, issued - STAGES); k < issued; ++k)
+        ptx::mbar_wait_drain(&full[k % STAGES], (k / STAGES) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      for (int k = 0; k < nk; ++k) {
-        const int s = k % STAGES;
-        if (!ptx::mbar_wait(&scaled[s], (k / STAGES) & 1, abort, P.status)) break;
-        ptx::tc_fence_after();
-        const uint32_t g = ptx::smem_u32(smem + s * STAGE);
-        const uint32_t a = g + G_TILE;
+    // MMA issuer (whole warp; the elected lane issues)
+    for (int k = 0; k < nk; ++k) {
+      const int s = k % STAGES;
+      const bool w = ptx::mbar_wait(&scaled[s], (k / STAGES) & 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) break;
+      // the scale warps fenced their writes to the async proxy before arriving
+      const uint32_t g = ptx::smem_u32(smem + s * STAGE);
+      // 16 rows per MMA = two 8-row groups of 1024 B; MN chunks of 64 are 8 KB apart
+      const uint64_t da = ptx::sdesc_sw128(g, BOX, 1024);
+      const uint64_t db = ptx::sdesc_sw128(g + G_TILE, BOX, 1024);
+      if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // 16 rows per MMA = two 8-row groups of 1024 B; MN chunks of 64 are 8 KB apart
-          const uint64_t da = ptx::sdesc_sw128(g + kk * 2048, BOX, 1024);
-          const uint64_t db = ptx::sdesc_sw128(a + kk * 2048, BOX, 1024);
-          ptx::umma_bf16(tmem, da, db, kIdesc, (k | kk) != 0);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+          ptx::umma_bf16(tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(db, kk * 2048), kIdesc, (k | kk) != 0);
         ptx::umma_commit(&empty[s]);
       }
-      ptx::umma_commit(accum);
+      __syncwarp();
     }
+    if (ptx::elect_one()) ptx::umma_commit(accum);
+    __syncwarp();
   } else {
     // ---- scale warps (128 threads) ----
     const int t = threadIdx.x - 64;

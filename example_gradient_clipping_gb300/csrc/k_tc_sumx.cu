@@ -1,0 +1,565 @@
+// Clipped sum with the clip factor applied per example in fp32, on the tensor cores.
+//
+//   dW = sum_i c_i P_i,  P_i = G_i^T A_i  (the per-example gradient of [MixGhost] eq. 2.4),
+//   db = sum_i c_i sum_t G_i[t, :]
+//
+// The reweighted contraction of [FastClip] section 5 written per example: the tensor
+// cores form P_i for one 128 x 256 output tile in TMEM (one buffer per example,
+// double-buffered), and eight epilogue warps fold it into register accumulators
+// with D += c_i * P_i.  No operand is rescaled or re-rounded, and no CUDA-core work
+// sits between a TMA load and the MMA that consumes it.  Rows of example i are loaded
+// with 3D TMA boxes [1, rows, 64] (rows past T read as zero): full 64-row stages,
+// then 16-row stages for the remainder.  In CTAs of the first column tile two warps
+// also sum the G rows from shared memory for the bias.  Examples are split across
+// the CTAs of a thread-block cluster (up to 8, one output tile): after the main loop
+// each CTA stages its fp32 partial tile in its own shared memory, and after a
+// cluster barrier each CTA adds one slice of rows from every peer over distributed
+// shared memory, in a fixed order, so the result is deterministic and needs no
+// global workspace.
+//   warpgroup 0: warps 0 and 2 TMA producers (alternate stages: one issuing thread
+//                streams only ~48 B/clk into an SM, two reach ~96), warp 1 MMA
+//                issuer, warp 3 reduces the bias across the cluster (64 registers
+//                each after setmaxnreg.dec)
+//   warpgroups 1-2: eight epilogue warps, two per TMEM lane quarter, 128 columns
+//                each (216 registers after setmaxnreg.inc: 128 accumulators); in
+//                CTAs of the first column tile they also sum the G rows of every
+//                stage for the bias (they idle between examples otherwise)
+// Register budget: 128 x 64 + 256 x 216 = 63488 <= 64512 = 384 threads x 168 at launch.
+#include <algorithm>
+
+#include "tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace dpk {
+namespace tcsumx {
+
+constexpr int BM = 128, BN = 256, STAGES = 4;
+constexpr int BOX = 64 * 64 * 2;             // 64 rows x 128 B
+constexpr int STAGE = 6 * BOX;               // G: 2 boxes, A: 4 boxes
+constexpr int kEpiWarps = 8;
+constexpr int kBiasWarps = 1;                // warp 3: joins the workers' barriers
+constexpr int kThreads = 384;                // 3 warpgroups
+constexpr int kEpiFirst = 4;                 // first epilogue warp
+constexpr int kSyncThreads = 32 * (kBiasWarps + kEpiWarps);   // warps 3-11, named barrier 1
+constexpr int kLeader = 96;                  // first worker thread (warp 3, lane 0)
+constexpr int SMEM = STAGES * STAGE + 1024 + 512;
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, BN, 1, 1);
+
+constexpr int PSTR = BN + 4;                 // staged partial row stride (floats)
+constexpr int PART_BYTES = BM * PSTR * 4;    // staged weight partial, then 128 bias floats
+static_assert(PART_BYTES + BM * 4 <= STAGES * STAGE, "staging fits in the stage buffers");
+
+struct Params {
+  const float* factors;
+  float* dW;
+  float* db;          // null: no bias
+  unsigned* status;
+  int B, T, p, d;
+  int ex_per_split, splits, accumulate;   // splits = cluster size along z
+  int nfull, n16;     // per example: 64-row stages, then 16-row stages
+};
+
+// Shared-memory control block after the stages.
+struct Ctl {
+  uint64_t full[STAGES], empty[STAGES], accum[2], tfree[2], drain;
+  uint32_t tmem;
+  int abort;
+  int flags[2];       // [1] go / no-go after the main loops
+};
+
+__device__ __forceinline__ void sync_workers() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kSyncThreads) : "memory");
+}
+
+// One CTA-wide go/no-go after the main loops (the branches that follow hold barriers).
+__device__ __forceinline__ bool finish_decision(Ctl* c) {
+  sync_workers();
+  if (threadIdx.x == kLeader) c->flags[1] = *(volatile int*)&c->abort ? 0 : 1;
+  sync_workers();
+  return c->flags[1] != 0;
+}
+
+// Warps 0 and 2 (all lanes): TMA producers; producer `pr` loads the stages k with
+// k % 2 == pr.
+__device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG64, const CUtensorMap* mA64,
+                                         const CUtensorMap* mG16, const CUtensorMap* mA16, uint8_t* smem,
+                                         Ctl* c, int e0, int e1, int m0, int n0, int pr) {
+  volatile int* abort = &c->abort;
+  const int ns = P.nfull + P.n16;
+  int k = 0, issued = 0;
+  bool live = true;
+  int last = -1;
+  for (int e = e0; e < e1 && live; ++e) {
+    for (int u = 0; u < ns; ++u, ++k) {
+      if ((k & 1) != pr) continue;
+      const int s = k % STAGES;
+      const bool w = ptx::mbar_wait(&c->empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+      const bool big = u < P.nfull;
+      const int y = big ? u * 64 : P.nfull * 64 + (u - P.nfull) * 16;
+      const CUtensorMap* mg = big ? mG64 : mG16;
+      const CUtensorMap* ma = big ? mA64 : mA16;
+      uint8_t* st = smem + s * STAGE;
+      if (ptx::elect_one()) {
+        ptx::mbar_arrive_expect_tx(&c->full[s], (big ? 64 : 16) * 128 * 6);
+        ptx::tma_load_3d(mg, &c->full[s], st, m0, y, e);
+        ptx::tma_load_3d(mg, &c->full[s], st + BOX, m0 + 64, y, e);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ptx::tma_load_3d(ma, &c->full[s], st + (2 + j) * BOX, n0 + 64 * j, y, e);
+      }
+      __syncwarp();
+      ++issued;
+      last = k;
+    }
+  }
+  if (*abort && (threadIdx.x & 31) == 0) {   // let this producer's copies in flight land
+    for (int q = max(0, last - STAGES + 1); q <= last; ++q)
+      if ((q & 1) == pr) ptx::mbar_wait_drain(&c->full[q % STAGES], (q / STAGES) & 1);
+  }
+  (void)issued;
+}
+
+// Warp 1 (all lanes): MMA issuer.  Descriptors are built once per stage from the
+// stage base; the elected lane issues the MMAs and the commits.
+__device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0,
+                                           int e1) {
+  volatile int* abort = &c->abort;
+  const int ns = P.nfull + P.n16;
+  int k = 0;
+  bool live = true;
+  for (int e = e0; e < e1 && live; ++e) {
+    const int x = e - e0, b = x & 1;
+    if (x >= 2) {
+      const bool w = ptx::mbar_wait(&c->tfree[b], ((x >> 1) & 1) ^ 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) break;
+    }
+    ptx::tc_fence_after();
+    const uint32_t d_tmem = tmem + b * 256;
+    for (int u = 0; u < ns; ++u, ++k) {
+      const int s = k % STAGES;
+      const bool w = ptx::mbar_wait(&c->full[s], (k / STAGES) & 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+      // no tcgen05 fence here: the TMA data is ordered by the mbarrier (both async proxy),
+      // and a per-stage fence was measured to stall the MMA pipe
+      const uint32_t g = ptx::smem_u32(smem + s * STAGE);
+      // 16 rows per MMA = two 8-row groups of 1024 B; 64-column chunks are BOX apart
+      const uint64_t da = ptx::sdesc_sw128(g, BOX, 1024);
+      const uint64_t dbd = ptx::sdesc_sw128(g + 2 * BOX, BOX, 1024);
+      if (ptx::elect_one()) {
+        if (u < P.nfull) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(dbd, kk * 2048), kIdesc,
+                           (u | kk) != 0);
+        } else {
+          ptx::umma_bf16(d_tmem, da, dbd, kIdesc, u != 0);
+        }
+        ptx::umma_commit(&c->empty[s]);
+      }
+      __syncwarp();
+    }
+    if (live) {
+      if (ptx::elect_one()) ptx::umma_commit(&c->accum[b]);
+      __syncwarp();
+    }
+  }
+}
+
+// t[0..7] += the eight bf16 values of v.
+__device__ __forceinline__ void add_bf16x8(const uint4& v, float* t) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(h[q]);
+    t[2 * q] += f.x;
+    t[2 * q + 1] += f.y;
+  }
+}
+
+// Warps 4-11: drain P_e from TMEM into fp32 register accumulators, D += c_e * P_e.
+__device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0,
+                                         int e1, int m0, int n0, bool do_bias) {
+  volatile int* abort = &c->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
+  const int half = (warp - kEpiFirst) >> 2;      // columns 128*half .. +127
+  // bias: thread -> (box, 16-byte chunk, row phase); the 16 threads sharing a column
+  // group are the lanes of one half-warp
+  const int et = threadIdx.x - 32 * kEpiFirst;   // 0..255
+  const int bbox = et >> 7, bq = (et >> 4) & 7, bj = et & 15;
+  const int ns = P.nfull + P.n16;
+  float bacc[8], btmp[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) bacc[q] = btmp[q] = 0.f;
+  float acc[128];
+#pragma unroll
+  for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+  bool ok = true;
+  int k = 0;
+  for (int e = e0; e < e1 && ok; ++e) {
+    const int x = e - e0, b = x & 1;
+    if (do_bias) {
+      for (int u = 0; u < ns; ++u, ++k) {
+        const int s = k % STAGES;
+        const bool w = ptx::mbar_wait(&c->full[s], (k / STAGES) & 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        // 128-byte swizzle: chunk q of row r sits at chunk q ^ (r % 8)
+        const uint8_t* gt = smem + s * STAGE + bbox * BOX + bj * 128 + ((bq ^ (bj & 7)) << 4);
+        if (u < P.nfull) {
+          uint4 v[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) v[h] = *reinterpret_cast<const uint4*>(gt + h * 16 * 128);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) add_bf16x8(v[h], btmp);
+        } else {
+          add_bf16x8(*reinterpret_cast<const uint4*>(gt), btmp);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c->empty[s]);
+      }
+      if (!ok) break;
+    }
+    const bool w = ptx::mbar_wait(&c->accum[b], (x >> 1) & 1, abort, P.status);
+    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+    ptx::tc_fence_after();
+    const float cf = __ldg(P.factors + e);
+    const uint32_t base = tmem + b * 256 + half * 128 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+    for (int ch = 0; ch < 8; ch += 2) {
+      float v0[16], v1[16];
+      ptx::tmem_ld16(base + ch * 16, v0);          // two loads in flight per wait
+      ptx::tmem_ld16(base + ch * 16 + 16, v1);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        acc[ch * 16 + j] = fmaf(cf, v0[j], acc[ch * 16 + j]);
+        acc[ch * 16 + 16 + j] = fmaf(cf, v1[j], acc[ch * 16 + 16 + j]);
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&c->tfree[b]);
+    if (do_bias) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        bacc[q] = fmaf(cf, btmp[q], bacc[q]);
+        btmp[q] = 0.f;
+      }
+    }
+  }
+  if (do_bias) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float v = bacc[q];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      bacc[q] = v;
+    }
+  }
+  const bool good = finish_decision(c);
+  if (!good) return;
+  if (do_bias && bj == 0) {
+    float* partb = reinterpret_cast<float*>(smem + PART_BYTES);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = bbox * 64 + bq * 8 + q;
+      if (P.splits > 1) partb[j] = bacc[q];   // staged for the cluster reduction
+      else if (m0 + j < P.p) P.db[m0 + j] = bacc[q] + (P.accumulate ? P.db[m0 + j] : 0.f);
+    }
+  }
+  const int row = quarter * 32 + lane;
+  if (P.splits > 1) {            // stage the partial tile for the cluster reduction
+    float* part = reinterpret_cast<float*>(smem) + row * PSTR + half * 128;
+#pragma unroll
+    for (int j = 0; j < 128; j += 4)
+      *reinterpret_cast<float4*>(part + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+    return;
+  }
+  // single split: this CTA owns the tile
+  const int m = m0 + row;
+  if (m >= P.p) return;
+  const int nb = n0 + half * 128;
+  const bool vec = (P.d & 3) == 0;
+  float* out = P.dW + (size_t)m * P.d;
+#pragma unroll
+  for (int j = 0; j < 128; j += 4) {
+    const int n = nb + j;
+    if (vec && n + 4 <= P.d) {
+      float4 o = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+      if (P.accumulate) {
+        const float4 old = *reinterpret_cast<const float4*>(out + n);
+        o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+      }
+      *reinterpret_cast<float4*>(out + n) = o;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (n + q < P.d) out[n + q] = acc[j + q] + (P.accumulate ? out[n + q] : 0.f);
+    }
+  }
+}
+
+// After the cluster barrier: this CTA adds rows [r0, r1) of every peer's staged
+// partial (fixed peer order) and writes them; warps 2-3 do the same for the bias.
+__device__ __forceinline__ void cluster_reduce(const Params& P, uint8_t* smem, int m0, int n0, bool do_bias) {
+  const int S = P.splits;
+  const uint32_t rank = ptx::cluster_rank();
+  const int warp = threadIdx.x >> 5;
+  if (warp >= kEpiFirst) {
+    const int t = threadIdx.x - 32 * kEpiFirst;     // 0..255
+    const int rows_per = (BM + S - 1) / S;
+    const int r0 = min(BM, (int)rank * rows_per), r1 = min(BM, r0 + rows_per);
+    const uint32_t base = ptx::smem_u32(smem);
+    const bool vec = (P.d & 3) == 0;
+    const int items = (r1 - r0) * (BN / 4);
+    for (int it0 = t; it0 < items; it0 += 512) {
+      // two output float4s per pass, all peers' loads in flight together
+      float4 v[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int item = it0 + h * 256;
+        if (item >= items) continue;
+        const int row = r0 + item / (BN / 4), c4 = item % (BN / 4);
+        const uint32_t off = base + (uint32_t)(row * PSTR + c4 * 4) * 4u;
+#pragma unroll
+        for (int sp = 0; sp < 8; ++sp)
+          if (sp < S) v[h][sp] = ptx::ld_cluster_v4(ptx::map_rank(off, sp));
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int item = it0 + h * 256;
+        if (item >= items) continue;
+        const int row = r0 + item / (BN / 4), c4 = item % (BN / 4);
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sp = 0; sp < 8; ++sp)
+          if (sp < S) { sum.x += v[h][sp].x; sum.y += v[h][sp].y; sum.z += v[h][sp].z; sum.w += v[h][sp].w; }
+        const int m = m0 + row, n = n0 + c4 * 4;
+        if (m >= P.p) continue;
+        float* out = P.dW + (size_t)m * P.d + n;
+        if (vec && n + 4 <= P.d) {
+          if (P.accumulate) {
+            const float4 old = *reinterpret_cast<const float4*>(out);
+            sum.x += old.x; sum.y += old.y; sum.z += old.z; sum.w += old.w;
+          }
+          *reinterpret_cast<float4*>(out) = sum;
+        } else {
+          const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (n + q < P.d) out[q] = sv[q] + (P.accumulate ? out[q] : 0.f);
+        }
+      }
+    }
+  } else if (warp == 3 && do_bias) {
+    const int t = threadIdx.x - 96;                  // 0..31
+    const int cols_per = (BM + S - 1) / S;
+    const int c0 = min(BM, (int)rank * cols_per), c1 = min(BM, c0 + cols_per);
+    const uint32_t base = ptx::smem_u32(smem + PART_BYTES);
+    for (int j = c0 + t; j < c1; j += 32) {
+      float sum = 0.f;
+      for (int sp = 0; sp < S; ++sp) sum += ptx::ld_cluster_f32(ptx::map_rank(base + 4u * j, sp));
+      const int col = m0 + j;
+      if (col < P.p) P.db[col] = sum + (P.accumulate ? P.db[col] : 0.f);
+    }
+  }
+}
+
+// Common tail, executed by every warp inside its own role branch (so each runs under
+// its warpgroup's register budget): cluster reduction of the split partials, drain
+// after an abort, TMEM release.  Every thread of every CTA passes the same barriers.
+__device__ __forceinline__ void finish(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int m0, int n0,
+                                       bool do_bias) {
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (P.splits > 1) {
+    ptx::cluster_sync();                               // all partials staged
+    if (c->flags[1]) cluster_reduce(P, smem, m0, n0, do_bias);
+    ptx::cluster_sync();                               // peers are done reading
+  }
+  if (*(volatile int*)&c->abort && threadIdx.x == 32) {
+    ptx::umma_commit(&c->drain);   // arrives once every MMA issued so far has completed
+    ptx::mbar_wait_drain(&c->drain, 0);
+  }
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant__ CUtensorMap mapA64,
+               const __grid_constant__ CUtensorMap mapG16, const __grid_constant__ CUtensorMap mapA16,
+               Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl* c = reinterpret_cast<Ctl*>(smem + STAGES * STAGE);
+
+  const int warp = threadIdx.x >> 5;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int e0 = blockIdx.z * P.ex_per_split;
+  const int e1 = min(P.B, e0 + P.ex_per_split);
+  const bool do_bias = (P.db != nullptr) && blockIdx.y == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&c->full[s], 1);
+      ptx::mbar_init(&c->empty[s], do_bias ? 1 + kEpiWarps : 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&c->accum[b], 1);
+      ptx::mbar_init(&c->tfree[b], kEpiWarps);
+    }
+    ptx::mbar_init(&c->drain, 1);
+    c->abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&mapG64);
+    ptx::prefetch_tensormap(&mapA64);
+    ptx::prefetch_tensormap(&mapG16);
+    ptx::prefetch_tensormap(&mapA16);
+  }
+  if (warp == 1) ptx::tmem_alloc(&c->tmem, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = c->tmem;
+
+  if (warp >= kEpiFirst) {
+    ptx::regs_inc<216>();
+    epilogue(P, smem, c, tmem, e0, e1, m0, n0, do_bias);
+    finish(P, smem, c, tmem, m0, n0, do_bias);
+  } else {
+    ptx::regs_dec<64>();
+    if (warp == 0 || warp == 2) {
+      producer(P, &mapG64, &mapA64, &mapG16, &mapA16, smem, c, e0, e1, m0, n0, warp >> 1);
+    } else if (warp == 1) {
+      mma_issuer(P, smem, c, tmem, e0, e1);
+    } else {
+      finish_decision(c);        // warp 3 joins the workers' barrier
+    }
+    finish(P, smem, c, tmem, m0, n0, do_bias);
+  }
+}
+
+}  // namespace tcsumx
+}  // namespace dpk
+
+namespace dph {
+using namespace dpk;
+
+static int cdiv_x(long a, long b) { return (int)((a + b - 1) / b); }
+
+// Clusters of `size` CTAs of this kernel that the current device runs at once (one
+// CTA per SM; a cluster must fit in one GPC, so large clusters strand SMs).
+static int active_clusters(int size) {
+  static int cache[64][9] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || size < 1 || size > 8) return 0;
+  if (!cache[dev][size]) {
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, size);
+    cfg.blockDim = dim3(tcsumx::kThreads);
+    cfg.dynamicSmemBytes = tcsumx::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = size;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, tcsumx::tc_sumx_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152 / size;   // planning fallback: the full SM count
+    }
+    cache[dev][size] = n;
+  }
+  return cache[dev][size];
+}
+
+// Clusters larger than 4 CTAs were measured to start over ~20 us on GB300 (18
+// clusters of 8), against ~0.1 us for clusters of 2.
+constexpr long kMaxCluster = 4;
+
+// Examples are split over a cluster of S <= kMaxCluster CTAs per output tile: the
+// largest S whose clusters for every tile run in one wave (at least 1).  The planning-only
+// variant (no device) assumes 152 SMs in clusters of any size.
+static void tc_sumx_split(const Geom& g, int* splits, int* ex_per_split, bool query_device) {
+  const long tiles = (long)cdiv_x(g.p, tcsumx::BM) * cdiv_x(g.D, tcsumx::BN);
+  long s = 1;
+  for (long c = std::min<long>(kMaxCluster, g.B); c >= 2; --c) {
+    const long fit = query_device ? (long)active_clusters((int)c) : 152 / c;
+    if (tiles <= fit) { s = c; break; }
+  }
+  const int eps = cdiv_x(g.B, s);
+  *ex_per_split = eps;
+  *splits = cdiv_x(g.B, eps);
+}
+
+bool tc_sumx_supported(const Geom& g) {
+  return !g.conv && (g.p % 8 == 0) && (g.D % 8 == 0) && g.p >= 64 && g.D >= 64 && g.T >= 64;
+}
+
+size_t tc_sumx_ws_bytes(const Geom&) { return 0; }
+
+cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
+                           float* db, int accumulate, void* /*ws*/, unsigned* status, cudaStream_t s) {
+  CUtensorMap mg64, ma64, mg16, ma16;
+  const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
+  const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
+  const uint64_t da[3] = {(uint64_t)g.D, (uint64_t)g.T, (uint64_t)g.B};
+  const uint64_t sa[2] = {(uint64_t)g.D * 2, (uint64_t)g.T * g.D * 2};
+  const uint32_t box64[3] = {64, 64, 1}, box16[3] = {64, 16, 1};
+  if (!encode_tmap_bf16(&mg64, G, 3, dg, sg, box64) || !encode_tmap_bf16(&ma64, A, 3, da, sa, box64) ||
+      !encode_tmap_bf16(&mg16, G, 3, dg, sg, box16) || !encode_tmap_bf16(&ma16, A, 3, da, sa, box16))
+    return cudaErrorInvalidValue;
+  int splits, eps;
+  tc_sumx_split(g, &splits, &eps, true);
+  tcsumx::Params P;
+  P.factors = factors;
+  P.dW = dW;
+  P.db = db;
+  P.status = status;
+  P.B = g.B;
+  P.T = g.T;
+  P.p = g.p;
+  P.d = g.D;
+  P.ex_per_split = eps;
+  P.splits = splits;
+  P.accumulate = accumulate;
+  int nfull = g.T / 64, rem = g.T - 64 * nfull;
+  int n16 = (rem + 15) / 16;
+  if (n16 > 3) { nfull += 1; n16 = 0; }
+  P.nfull = nfull;
+  P.n16 = n16;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tcsumx::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cdiv_x(g.p, tcsumx::BM), cdiv_x(g.D, tcsumx::BN), splits);
+  cfg.blockDim = dim3(tcsumx::kThreads);
+  cfg.dynamicSmemBytes = tcsumx::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel, mg64, ma64, mg16, ma16, P);
+  count_launch();
+  return e;
+}
+
+}  // namespace dph

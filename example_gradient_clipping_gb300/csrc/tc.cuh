@@ -12,6 +12,11 @@ size_t tc_sum_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
                           float* dW, float* db, int accumulate, float* ws, unsigned* status,
                           cudaStream_t s);
+// Clipped sum with per-example TMEM accumulation and fp32 scaling (rows per example >= 64).
+bool tc_sumx_supported(const Geom& g);
+size_t tc_sumx_ws_bytes(const Geom& g);
+cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
+                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
 // Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).
 bool tc_ghost_supported(const Geom& g);
 size_t tc_ghost_ws_bytes(const Geom& g);

@@ -10,8 +10,8 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence, Tuple
 
-from . import (DP_NORM_AUTO, LayerDesc, dp_add_noise, dp_clip_factors, dp_clipped_sum,
-               dp_layer_sqnorms, dp_plan, dp_workspace_size)
+from . import (DP_NORM_AUTO, LayerDesc, dp_add_noise, dp_add_noise_devseed, dp_clip_factors,
+               dp_clipped_sum, dp_launch_count, dp_layer_sqnorms, dp_plan, dp_workspace_size)
 
 
 class ClipStep:
@@ -41,7 +41,10 @@ class ClipStep:
         self.sqnorms = torch.empty(L, self.B, dtype=torch.float32, device=dev)
         self.factors = torch.empty((L if self.per_layer else 1), self.B, dtype=torch.float32, device=dev)
         self.grad = torch.empty(self.n_params, dtype=torch.float32, device=dev)
+        self.seed_buf = torch.zeros(1, dtype=torch.int64, device=dev)
         self.chosen: List[int] = [m for m, _, _ in self.plan]
+        self.graph = None
+        self.graph_kernels = 0
 
     def layer_views(self, l: int) -> Tuple:
         p, D = self.shapes[l]
@@ -75,6 +78,42 @@ class ClipStep:
             n = p * D + (p if d.has_bias else 0)
             o = self.offsets[l]
             dp_add_noise(self.grad[o:o + n], self.sigma, self.C[l], self.B, seed, o, stream=stream)
+
+    def noise_devseed(self, stream=None) -> None:
+        """Noise with the seed read from self.seed_buf when the kernels run."""
+        if not self.per_layer:
+            dp_add_noise_devseed(self.grad, self.sigma, self.C[0], self.B, self.seed_buf, 0, stream=stream)
+            return
+        for l, d in enumerate(self.descs):
+            p, D = self.shapes[l]
+            n = p * D + (p if d.has_bias else 0)
+            o = self.offsets[l]
+            dp_add_noise_devseed(self.grad[o:o + n], self.sigma, self.C[l], self.B, self.seed_buf, o,
+                                 stream=stream)
+
+    def capture(self, inputs) -> None:
+        """Capture one whole step over the device buffers `inputs` in a CUDA graph.
+
+        replay(seed) reruns it (one launch for the step) with noise drawn from `seed`;
+        refill the same input buffers between replays to process new batches.
+        """
+        import torch
+        self.run(inputs, seed=0)           # first calls resolve per-device state outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        n0 = dp_launch_count()
+        with torch.cuda.graph(g):
+            self.norms(inputs)
+            self.factors_()
+            self.sums(inputs)
+            self.noise_devseed()
+        self.graph_kernels = dp_launch_count() - n0
+        self.graph = g
+
+    def replay(self, seed: int):
+        self.seed_buf.fill_(int(seed))
+        self.graph.replay()
+        return self.grad
 
     def run(self, inputs, seed: int, stream=None):
         """Norms -> factors -> clipped sums -> noise and 1/B; returns the flat gradient."""

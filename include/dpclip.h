@@ -155,6 +155,13 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
 dp_status dp_add_noise(float* grad, size_t n, float sigma, float C, int B, uint64_t seed,
                        uint64_t offset, cudaStream_t stream);
 
+/* dp_add_noise with the seed read from device memory (*seed_dev, a 64-bit value) when
+ * the kernel runs, so that a captured CUDA graph draws fresh noise on every replay
+ * after the caller updates *seed_dev.  Same noise definition as dp_add_noise. */
+dp_status dp_add_noise_devseed(float* grad, size_t n, float sigma, float C, int B,
+                               const unsigned long long* seed_dev, uint64_t offset,
+                               cudaStream_t stream);
+
 /* Adaptive clipping bound of one layer ([ThreeTools] section 3):
  *   C_next = alpha/B * (sum_i min(sqrt(sqnorms[i]), C_l2) + sigma_l2 * C_l2 * z),
  *   C_l2_next = beta * C_next,

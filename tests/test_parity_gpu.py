@@ -174,6 +174,7 @@ EDGE = [
     ("lin_tc_ragged", LayerSpec("e", "linear", p=72, d=200, T=33), 5, "bf16"),
     ("lin_tc_T256", LayerSpec("e", "linear", p=128, d=64, T=256), 3, "bf16"),
     ("lin_tc_splits", LayerSpec("e", "linear", p=128, d=256, T=50), 37, "bf16"),
+    ("lin_tc_B1", LayerSpec("e", "linear", p=64, d=64, T=64), 1, "bf16"),
     ("lin_tc_T300", LayerSpec("e", "linear", p=64, d=136, T=300, has_bias=False), 2, "bf16"),
     ("conv_s2", LayerSpec("e", "conv2d", p=6, Cin=5, H=11, W=9, k=3, stride=2, pad=1), 3, "bf16"),
     ("conv_dil", LayerSpec("e", "conv2d", p=4, Cin=3, H=10, W=10, k=3, stride=1, pad=2, dil=2), 2, "fp32"),
@@ -189,14 +190,20 @@ def test_edge_shapes(lib, tag, spec, B, dtype):
         _check_layer(lib, spec, wl, mode=mode)
 
 
-def test_accumulate_adds_to_existing_sum(lib):
+ACC = [(LayerSpec("e", "linear", p=40, d=72, T=9), 6),          # SIMT
+       (LayerSpec("e", "linear", p=128, d=64, T=40), 5),         # row-scaled tensor-core GEMM
+       (LayerSpec("e", "linear", p=128, d=128, T=64), 4),        # per-example, several splits
+       (LayerSpec("e", "linear", p=64, d=256, T=80), 1)]         # per-example, one split
+
+
+@pytest.mark.parametrize("spec,B", ACC, ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single"])
+def test_accumulate_adds_to_existing_sum(lib, spec, B):
     import torch
     dp = lib
-    spec = LayerSpec("e", "linear", p=40, d=72, T=9)
-    wl = Workload(name="acc", B=6, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=2)
+    wl = Workload(name="acc", B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=2)
     A, G = workloads.layer_inputs(wl, 0)
-    fac = workloads.factor_inputs(wl, 6)
-    desc = desc_for(dp, spec, 6, "bf16")
+    fac = workloads.factor_inputs(wl, B)
+    desc = desc_for(dp, spec, B, "bf16")
     ws = torch.empty(dp.dp_workspace_size(desc), dtype=torch.uint8, device="cuda")
     Ad, Gd = to_dev(A, "bf16"), to_dev(G, "bf16")
     f = torch.tensor(fac, device="cuda")
