@@ -1,0 +1,106 @@
+"""Full-size workloads on the GPU, checked on what the oracle can compute.
+
+Inputs are drawn on the device by a seeded generator (host generation of the
+multi-GB batches would take minutes); sampled examples are copied back for the
+oracle.  Norms: sampled examples against the oracle.  Clipped sum: the full-size
+launch with factors that are zero except for a sample of examples, against the
+oracle's sum over those examples, plus additivity in the factors over the whole
+batch.  Flat and per-layer factors of the whole step are checked against the
+factor rule applied to the GPU's own norms (the rule alone is what is checked
+there; the norms are checked against the oracle).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import TOL, desc_for, rel_elem, rel_vec
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE = [0, 1, 777, 2049, 4095]
+
+
+def _sample(B):
+    return sorted({i for i in SAMPLE if i < B} | {B - 1})
+
+
+def _host(x, i):
+    return x[i].float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("name", ["vit_mlp_b4096_t197", "vgg11_cifar_b1024", "conv3x3_b256",
+                                  "seq_linear_b64_t128"])
+def test_full_size_norms_and_sparse_sums(lib, name):
+    import torch
+    dp = lib
+    wl = workloads.get_workload(name)
+    idx = _sample(wl.B)
+    for l, spec in enumerate(wl.layers):
+        A, G = workloads.device_layer_inputs(wl, l)
+        desc = desc_for(dp, spec, wl.B, wl.dtype)
+        ws = torch.empty(max(dp.dp_workspace_size(desc), 16), dtype=torch.uint8, device="cuda")
+        sq = torch.empty(wl.B, device="cuda")
+        dp.dp_layer_sqnorms(desc, A, G, sq, ws)
+        # sparse factors: only the sampled examples contribute
+        fac = np.zeros(wl.B, dtype=np.float32)
+        fac[idx] = np.linspace(0.3, 1.0, len(idx), dtype=np.float32)
+        f = torch.tensor(fac, device="cuda")
+        dW = torch.empty(spec.p * spec.D, device="cuda")
+        db = torch.empty(spec.p, device="cuda")
+        dp.dp_clipped_sum(desc, A, G, f, dW, db, ws)
+        torch.cuda.synchronize()
+        a_s = np.stack([_host(A, i) for i in idx])
+        g_s = np.stack([_host(G, i) for i in idx])
+        ref_sq = oracle.layer_sqnorms(spec, a_s, g_s)
+        assert rel_elem(sq.cpu().numpy()[idx], ref_sq) <= TOL[wl.dtype], (name, spec.name)
+        S, Sb = oracle.clipped_sum(spec, a_s, g_s, fac[idx].astype(np.float64))
+        assert rel_vec(dW.cpu().numpy(), S) <= TOL[wl.dtype], (name, spec.name)
+        assert rel_vec(db.cpu().numpy(), Sb) <= TOL[wl.dtype], (name, spec.name)
+        assert np.all(np.isfinite(sq.cpu().numpy())) and np.all(sq.cpu().numpy() > 0)
+        del A, G
+
+
+@pytest.mark.parametrize("name", ["vit_mlp_b4096_t197", "conv3x3_b256"])
+def test_full_size_sum_is_additive_in_factors(lib, name):
+    """sum(c1) + sum(c2) = sum(c1 + c2) over the whole batch (the reweighting is linear)."""
+    import torch
+    dp = lib
+    wl = workloads.get_workload(name)
+    spec = wl.layers[0]
+    A, G = workloads.device_layer_inputs(wl, 0)
+    desc = desc_for(dp, spec, wl.B, wl.dtype)
+    ws = torch.empty(max(dp.dp_workspace_size(desc), 16), dtype=torch.uint8, device="cuda")
+    c1 = torch.tensor(workloads.factor_inputs(wl, wl.B, 0.0, 0.5), device="cuda")
+    c2 = torch.flip(c1, [0]) * 0.7
+    outs = []
+    for f in (c1, c2, c1 + c2):
+        dW = torch.empty(spec.p * spec.D, device="cuda")
+        db = torch.empty(spec.p, device="cuda")
+        dp.dp_clipped_sum(desc, A, G, f, dW, db, ws)
+        outs.append((dW.double(), db.double()))
+    torch.cuda.synchronize()
+    lhs = outs[0][0] + outs[1][0]
+    rhs = outs[2][0]
+    # fp32 accumulation of the same products in different groupings
+    assert (torch.linalg.norm(lhs - rhs) / torch.linalg.norm(rhs)).item() <= 1e-4
+    lhs_b = outs[0][1] + outs[1][1]
+    assert (torch.linalg.norm(lhs_b - outs[2][1]) / torch.linalg.norm(outs[2][1])).item() <= 1e-4
+
+
+def test_full_size_vgg_step_flat_and_per_layer_factors(lib):
+    """The whole VGG-11 step at B=1024: factors follow the rule on the GPU norms."""
+    import torch
+    dp = lib
+    wl = workloads.get_workload("vgg11_cifar_b1024")
+    descs = [desc_for(dp, s, wl.B, wl.dtype) for s in wl.layers]
+    inputs = [workloads.device_layer_inputs(wl, l) for l in range(len(wl.layers))]
+    for per_layer in (False, True):
+        step = dp.ClipStep(descs, C=wl.C, sigma=wl.sigma, per_layer=per_layer)
+        g = step.run(inputs, seed=3)
+        torch.cuda.synchronize()
+        sq = step.sqnorms.double().cpu().numpy()
+        want, _ = oracle.clip_factors(sq, wl.C if not per_layer else [wl.C] * len(wl.layers), per_layer)
+        got = step.factors.double().cpu().numpy()
+        assert rel_elem(got if per_layer else got[0], want) <= 1e-6
+        assert np.all(np.isfinite(g.cpu().numpy()))

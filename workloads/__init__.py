@@ -240,6 +240,31 @@ def layer_inputs(wl: Workload, layer: int, examples: Optional[Sequence[int]] = N
     return A, G
 
 
+def device_layer_inputs(wl: Workload, layer: int, device: str = "cuda"):
+    """(A, G) of the whole batch drawn on `device` by torch's seeded generator.
+
+    For the full-size workloads, whose host-side generation would take minutes.
+    Same shapes and distributions as layer_inputs (the values differ); the tests
+    copy sampled examples back to the host for the oracle, so both sides still read
+    the same numbers.  Returned in the workload dtype.
+    """
+    import torch
+    spec = wl.layers[layer]
+    gen = torch.Generator(device=device)
+    gen.manual_seed((wl.seed * 1_000_003 + 2 * layer + 1) & 0x7FFFFFFFFFFFFFFF)
+    A = torch.randn((wl.B,) + spec.a_example_shape(), generator=gen, device=device, dtype=torch.float32)
+    if spec.a_dist == "abs_normal":
+        A.abs_()
+    if spec.a_std != 1.0:
+        A.mul_(spec.a_std)
+    gen.manual_seed((wl.seed * 1_000_003 + 2 * layer + 2) & 0x7FFFFFFFFFFFFFFF)
+    G = torch.randn((wl.B,) + spec.g_example_shape(), generator=gen, device=device, dtype=torch.float32)
+    G.mul_(spec.g_std)
+    if wl.dtype == "bf16":
+        A, G = A.to(torch.bfloat16), G.to(torch.bfloat16)
+    return A, G
+
+
 def factor_inputs(wl: Workload, n: int, low: float = 0.0, high: float = 1.0) -> np.ndarray:
     """Externally supplied clip factors in [low, high) (for testing the clipped sum alone)."""
     return _gen(wl.seed, _TID_FACTORS, 0).uniform(low, high, size=n).astype(np.float32)
