@@ -225,6 +225,17 @@ def _config(wl, extra=None):
     return c
 
 
+def max_over_ranks(v: float, device) -> float:
+    """The slowest replica's time: MAX all-reduce of one float64 (identity on one process)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()) \
+            or torch.distributed.get_world_size() == 1:
+        return float(v)
+    t = torch.tensor([float(v)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args, wl):
     import torch
     import workloads
@@ -286,11 +297,7 @@ def run_ours(args, wl):
     if world > 1:
         torch.distributed.barrier()
     launches = step.graph_kernels * args.steps
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     value = world * wl.B * args.steps / (total_ms / 1e3)
     per_call = {n: [t / REPS for t in timed(g.replay, max(5, args.steps // 4), seed0)]
                 for n, g in call_graphs.items()}
@@ -315,11 +322,7 @@ def run_ours(args, wl):
         e1.synchronize()
         if k >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_tot = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_tot], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_tot = float(t.item())
+    e2e_tot = max_over_ranks(sum(e2e_ms), dev)
     e2e_value = world * wl.B * args.steps / (e2e_tot / 1e3)
 
     # roofline of the dominant call
