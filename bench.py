@@ -29,6 +29,10 @@ DEFAULT_WORKLOAD = "seq_linear_b64_t128"
 L2_FLUSH_BYTES = 256 << 20
 
 
+# inputs with more elements than this are drawn on the device rather than the host
+HOST_GEN_LIMIT = 1 << 27
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -159,19 +163,40 @@ def _dist_env():
     return world, rank, local
 
 
-def cpu_baseline(wl, inputs, budget_s: float = 12.0):
-    """Time the float64 CPU oracle (as it stands) on full batches of the workload."""
+def _oracle_batch_size(wl, sample_inputs, per_step_s: float) -> int:
+    """Largest sub-batch (doubling from 1, at most B) whose oracle step takes about per_step_s."""
     import oracle
+    b = 1
+    while b < wl.B:
+        t0 = time.perf_counter()
+        oracle.dp_step(wl.with_batch(b), sample_inputs(b), seed=wl.seed)
+        if time.perf_counter() - t0 >= per_step_s / 2:
+            break
+        b = min(2 * b, wl.B)
+    return b
+
+
+def cpu_baseline(wl, sample_inputs, budget_s: float = 12.0):
+    """Time the float64 CPU oracle (as it stands) on a bounded sample of the workload.
+
+    sample_inputs(b) returns the first b examples' (A, G) per layer as host arrays.
+    Full batches when one takes well under the budget, else a sub-batch of the
+    same layers; the value is examples per second either way.
+    """
+    import oracle
+    b = _oracle_batch_size(wl, sample_inputs, budget_s / 4)
+    sub, inputs = wl.with_batch(b), sample_inputs(b)
     t0 = time.perf_counter()
     runs = 0
     while True:
-        oracle.dp_step(wl, inputs, seed=wl.seed + runs)
+        oracle.dp_step(sub, inputs, seed=wl.seed + runs)
         runs += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return dict(value=wl.B * runs / dt, unit="examples/s", cores=_cores(), kind="oracle",
-                sample=f"{runs} full batch(es) of {wl.name} (B={wl.B}), float64 numpy, {dt:.1f} s")
+    what = "full batch(es)" if b == wl.B else f"sub-batches of the first {b} examples"
+    return dict(value=b * runs / dt, unit="examples/s", cores=_cores(), kind="oracle",
+                sample=f"{runs} {what} of {wl.name} (B={wl.B}), float64 numpy, {dt:.1f} s")
 
 
 def _cores():
@@ -194,16 +219,24 @@ def run_reference(args, wl):
     if rank != 0:
         return
     import oracle
-    inputs = [workloads.layer_inputs(wl, l) for l in range(len(wl.layers))]
+
+    def sample_inputs(b):
+        return [workloads.layer_inputs(wl.with_batch(b), l, threads=8) for l in range(len(wl.layers))]
+
+    # each step one bounded sample: the whole run stays within a few minutes
+    per_step_s = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    b = _oracle_batch_size(wl, sample_inputs, per_step_s)
+    sub, inputs = wl.with_batch(b), sample_inputs(b)
     for w in range(args.warmup):
-        oracle.dp_step(wl, inputs, seed=wl.seed + w)
+        oracle.dp_step(sub, inputs, seed=wl.seed + w)
     times = []
     for k in range(args.steps):
         t0 = time.perf_counter()
-        oracle.dp_step(wl, inputs, seed=wl.seed + 1000 + k)
+        oracle.dp_step(sub, inputs, seed=wl.seed + 1000 + k)
         times.append(time.perf_counter() - t0)
     tot = sum(times)
-    value = wl.B * args.steps / tot
+    value = b * args.steps / tot
+    what = "full batches" if b == wl.B else f"sub-batches of the first {b} examples"
     cores = _cores()
     line = dict(metric=METRIC, value=value, unit="examples/s", n_gpus=args.gpus, steps=args.steps,
                 warmup=args.warmup, ms_per_step=1e3 * tot / args.steps, higher_is_better=True,
@@ -211,7 +244,7 @@ def run_reference(args, wl):
                 config=_config(wl), e2e={"value": value, "unit": "examples/s", "h2d_bytes_per_step": 0,
                                          "d2h_bytes_per_step": 0},
                 cpu_baseline=dict(value=value, unit="examples/s", cores=cores, kind="oracle",
-                                  sample=f"{args.steps} full batches of {wl.name} (B={wl.B}), float64 numpy"))
+                                  sample=f"{args.steps} {what} of {wl.name} (B={wl.B}), float64 numpy"))
     print(json.dumps(line), flush=True)
 
 
@@ -251,9 +284,23 @@ def run_ours(args, wl):
 
     descs = [layer_desc(dp, s, wl.B, wl.dtype) for s in wl.layers]
     step = dp.ClipStep(descs, C=wl.C, sigma=wl.sigma, per_layer=wl.per_layer, device=str(dev))
-    host_in = [workloads.layer_inputs(wl, l, threads=8) for l in range(len(wl.layers))]
-    dev_in = [(workloads.to_torch(A, wl.dtype, str(dev)), workloads.to_torch(G, wl.dtype, str(dev)))
-              for A, G in host_in]
+    n_elem = wl.B * sum(math.prod(s.a_example_shape()) + math.prod(s.g_example_shape()) for s in wl.layers)
+    if n_elem <= HOST_GEN_LIMIT:
+        host_in = [workloads.layer_inputs(wl, l, threads=8) for l in range(len(wl.layers))]
+        dev_in = [(workloads.to_torch(A, wl.dtype, str(dev)), workloads.to_torch(G, wl.dtype, str(dev)))
+                  for A, G in host_in]
+        pinned = [(workloads.to_torch(A, wl.dtype).pin_memory(), workloads.to_torch(G, wl.dtype).pin_memory())
+                  for A, G in host_in]
+
+        def sample_inputs(b):
+            return [(A[:b], G[:b]) for A, G in host_in]
+    else:
+        # full-size inputs drawn on the device (host generation would take minutes)
+        dev_in = [workloads.device_layer_inputs(wl, l, str(dev)) for l in range(len(wl.layers))]
+        pinned = [(a.cpu().pin_memory(), g.cpu().pin_memory()) for a, g in dev_in]
+
+        def sample_inputs(b):
+            return [(a[:b].float().numpy(), g[:b].float().numpy()) for a, g in pinned]
     modes = [dp.MODE_NAMES[m] for m, _, _ in step.plan]
     work = step_work(wl, modes)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -303,8 +350,6 @@ def run_ours(args, wl):
                 for n, g in call_graphs.items()}
 
     # end to end through the public API: pinned host inputs copied in, result copied out
-    pinned = [(workloads.to_torch(A, wl.dtype).pin_memory(), workloads.to_torch(G, wl.dtype).pin_memory())
-              for A, G in host_in]
     out_host = torch.empty(step.n_params, dtype=torch.float32).pin_memory()
     h2d = sum(a.numel() * a.element_size() + g.numel() * g.element_size() for a, g in pinned)
     d2h = out_host.numel() * 4
@@ -358,7 +403,7 @@ def run_ours(args, wl):
                     kernels_per_step=step.graph_kernels,
                     step_flop=work["flop_norm"] + work["flop_sum"], step_bytes=work["bytes_total"])
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(wl, host_in)
+            line["cpu_baseline"] = cpu_baseline(wl, sample_inputs)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

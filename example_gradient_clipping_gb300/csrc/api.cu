@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 
@@ -101,46 +102,136 @@ int resolve_mode(const Geom& g, int requested) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Which kernel serves a call: the tensor-core kernels take bf16 inputs with 16-byte
-// aligned base pointers and the shapes they support; everything else runs SIMT.
-// 0: SIMT, 1: row-scaled tensor-core GEMM, 2: per-example tensor-core accumulation
-int sum_path(const Geom& g, int dtype, const void* A, const void* G) {
-  if (dtype != DP_BF16 || !aligned16(A) || !aligned16(G)) return 0;
-  if (dph::tc_sumx_supported(g)) return 2;
-  if (dph::tc_sum_supported(g)) return 1;
+// Conv layers in bf16 whose unfolded width D and output count p are multiples of 8
+// (16-byte TMA rows) run the linear tensor-core kernels on their row layout, written
+// into the front of the workspace: U [B, T, D] then Gt [B, T, p].
+Geom rows_geom(const Geom& g) {
+  Geom r = g;
+  r.conv = 0;
+  r.d = r.D;
+  return r;
+}
+bool rows_layout_ok(const Geom& g) { return !g.conv || (g.D % 8 == 0 && g.p % 8 == 0); }
+size_t rows_bytes(const Geom& g) {
+  return g.conv ? align256((size_t)g.B * g.T * g.D * 2) + align256((size_t)g.B * g.T * g.p * 2) : 0;
+}
+
+// Clipped-sum kernel: 0 SIMT, 1 row-scaled tensor-core GEMM, 2 per-example tensor-core
+// accumulation.  The per-example kernel splits the examples only over a cluster of <= 4
+// CTAs per output tile, so it serves layers with enough tiles to fill the GPU; the
+// row-scaled GEMM splits the batch rows over the whole grid.
+struct Plan {
+  int kernel;
+  bool rows;    // conv layer through its row layout
+  Geom lg;      // the geometry the kernel sees
+};
+
+bool tc_inputs(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
+  if (dtype != DP_BF16 || !aligned16(A) || !aligned16(G) || !rows_layout_ok(g)) return false;
+  return !g.conv || aligned16(ws);
+}
+
+// DPCLIP_SUM_KERNEL=rows|example pins the tensor-core clipped-sum kernel where the
+// shape allows it (both compute the same sum; used by the tests and for tuning).
+int pinned_sum_kernel() {
+  const char* v = std::getenv("DPCLIP_SUM_KERNEL");
+  if (!v) return 0;
+  if (!std::strcmp(v, "rows")) return 1;
+  if (!std::strcmp(v, "example")) return 2;
   return 0;
 }
-bool use_tc_ghost(const Geom& g, int dtype, const void* A, const void* G) {
-  return dtype == DP_BF16 && dph::tc_ghost_supported(g) && aligned16(A) && aligned16(G);
+
+int sum_kernel_for(const Geom& lg) {
+  const int pin = pinned_sum_kernel();
+  if (pin == 2 && dph::tc_sumx_supported(lg)) return 2;
+  if (pin == 1 && dph::tc_sum_supported(lg)) return 1;
+  const long tiles = (long)((lg.p + 127) / 128) * ((lg.D + 255) / 256);
+  if (dph::tc_sumx_supported(lg) && tiles * std::min(4, lg.B) >= 64) return 2;
+  if (dph::tc_sum_supported(lg)) return 1;
+  if (dph::tc_sumx_supported(lg)) return 2;
+  return 0;
+}
+
+Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
+  Plan pl{0, false, g};
+  if (!tc_inputs(g, dtype, A, G, ws)) return pl;
+  const Geom lg = g.conv ? rows_geom(g) : g;
+  const int k = sum_kernel_for(lg);
+  if (k) pl = Plan{k, g.conv != 0, lg};
+  return pl;
+}
+
+enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST };
+
+Plan norm_plan(const Geom& g, int mode, int dtype, const void* A, const void* G, const void* ws) {
+  if (mode == DP_NORM_T1) return Plan{NK_T1, false, g};
+  const Plan simt{mode == DP_NORM_GHOST ? NK_SIMT_GHOST : NK_SIMT_INST, false, g};
+  if (!tc_inputs(g, dtype, A, G, ws)) return simt;
+  const Geom lg = g.conv ? rows_geom(g) : g;
+  if (mode == DP_NORM_GHOST && dph::tc_ghost_supported(lg)) return Plan{NK_TC_GHOST, g.conv != 0, lg};
+  if (mode == DP_NORM_INSTANTIATE && dph::tc_sumx_supported(lg)) return Plan{NK_TC_INST, g.conv != 0, lg};
+  return simt;
 }
 
 size_t simt_sum_bytes(const Geom& g) {
   return dph::simt_sum_splits(g) * ((size_t)g.p * g.D + g.p) * sizeof(float);
 }
 
-// Workspace a call needs on the path it takes.
-size_t sum_ws_bytes(const Geom& g, int path) {
-  return path == 2 ? dph::tc_sumx_ws_bytes(g) : path == 1 ? dph::tc_sum_ws_bytes(g) : simt_sum_bytes(g);
+// Workspace a call needs on the path it takes (row layout first, then the kernel's own).
+size_t sum_ws_bytes(const Geom& g, const Plan& pl) {
+  const Geom& lg = pl.lg;
+  const size_t inner = pl.kernel == 2 ? dph::tc_sumx_ws_bytes(lg)
+                       : pl.kernel == 1 ? dph::tc_sum_ws_bytes(lg) : simt_sum_bytes(g);
+  return (pl.rows ? rows_bytes(g) : 0) + inner;
 }
 
-size_t norm_ws_bytes(const Geom& g, int mode, bool tc) {
-  switch (mode) {
-    case DP_NORM_T1: return 0;
-    case DP_NORM_GHOST:
-      return tc ? dph::tc_ghost_ws_bytes(g) : dph::simt_ghost_ws_floats(g) * sizeof(float);
-    case DP_NORM_INSTANTIATE: return dph::simt_inst_ws_floats(g) * sizeof(float);
+size_t norm_ws_bytes(const Geom& g, const Plan& pl) {
+  size_t inner = 0;
+  switch (pl.kernel) {
+    case NK_T1: inner = 0; break;
+    case NK_SIMT_GHOST: inner = dph::simt_ghost_ws_floats(g) * sizeof(float); break;
+    case NK_SIMT_INST: inner = dph::simt_inst_ws_floats(g) * sizeof(float); break;
+    case NK_TC_GHOST: inner = dph::tc_ghost_ws_bytes(pl.lg); break;
+    case NK_TC_INST: inner = dph::tc_inst_ws_bytes(pl.lg); break;
   }
-  return 0;
+  return (pl.rows ? rows_bytes(g) : 0) + inner;
 }
 
-// The size dp_workspace_size reports covers every path a call with `desc` can take.
+// The size dp_workspace_size reports covers every path a call with `desc` can take
+// (the choice also depends on the dtype and the alignment of the pointers).
 size_t max_ws_bytes(const Geom& g, int mode) {
-  size_t n = std::max(norm_ws_bytes(g, mode, false), simt_sum_bytes(g));
-  if (dph::tc_ghost_supported(g)) n = std::max(n, norm_ws_bytes(g, mode, true));
-  if (dph::tc_sum_supported(g)) n = std::max(n, dph::tc_sum_ws_bytes(g));
-  if (dph::tc_sumx_supported(g)) n = std::max(n, dph::tc_sumx_ws_bytes(g));
+  static const char kAligned[16] __attribute__((aligned(16))) = {};
+  const void* al = kAligned;
+  const void* mis = kAligned + 1;
+  size_t n = 0;
+  for (int dt : {DP_BF16, DP_FP32})
+    for (const void* ptr : {al, mis}) {
+      n = std::max(n, norm_ws_bytes(g, norm_plan(g, mode, dt, ptr, ptr, ptr)));
+      n = std::max(n, sum_ws_bytes(g, sum_plan(g, dt, ptr, ptr, ptr)));
+    }
+  // either tensor-core sum kernel may be pinned
+  if (rows_layout_ok(g)) {
+    const Geom lg = g.conv ? rows_geom(g) : g;
+    if (dph::tc_sum_supported(lg)) n = std::max(n, rows_bytes(g) + dph::tc_sum_ws_bytes(lg));
+    if (dph::tc_sumx_supported(lg)) n = std::max(n, rows_bytes(g) + dph::tc_sumx_ws_bytes(lg));
+  }
   return n;
+}
+
+// Launch the row layout of a conv layer into the workspace; returns the pointers.
+cudaError_t prepare_rows(const Geom& g, const Plan& pl, const void*& A, const void*& G, void*& ws,
+                         cudaStream_t stream) {
+  if (!pl.rows) return cudaSuccess;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* U = base;
+  void* Gt = base + align256((size_t)g.B * g.T * g.D * 2);
+  cudaError_t e = dph::launch_conv_rows(g, A, G, U, Gt, stream);
+  A = U;
+  G = Gt;
+  ws = base + rows_bytes(g);
+  return e;
 }
 
 
@@ -197,26 +288,21 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
   if (!A || !G || !sqnorm_out) return fail(DP_ERR_INVALID_ARG, "A, G and sqnorm_out must be non-NULL");
   Geom g;
   make_geom(desc, &g);
-  const bool tc = chosen == DP_NORM_GHOST && use_tc_ghost(g, desc->dtype, A, G);
-  const size_t need = norm_ws_bytes(g, chosen, tc);
+  const Plan pl = norm_plan(g, chosen, desc->dtype, A, G, workspace);
+  const size_t need = norm_ws_bytes(g, pl);
   if (need && (!workspace || ws_bytes < need))
     return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? ws_bytes : (size_t)0);
-  cudaError_t e = cudaSuccess;
-  float* ws = static_cast<float*>(workspace);
-  switch (chosen) {
-    case DP_NORM_T1:
-      e = dph::launch_t1_norm(g, desc->dtype, A, G, sqnorm_out, stream);
-      break;
-    case DP_NORM_GHOST:
-      if (tc)
-        e = dph::launch_tc_ghost(g, A, G, sqnorm_out, ws, status_ptr(), stream);
-      else
-        e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream);
-      break;
-    case DP_NORM_INSTANTIATE:
-      e = dph::launch_simt_inst(g, desc->dtype, A, G, sqnorm_out, ws, stream);
-      break;
+  void* wsp = workspace;
+  cudaError_t e = prepare_rows(g, pl, A, G, wsp, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_layer_sqnorms row layout");
+  float* ws = static_cast<float*>(wsp);
+  switch (pl.kernel) {
+    case NK_T1: e = dph::launch_t1_norm(g, desc->dtype, A, G, sqnorm_out, stream); break;
+    case NK_TC_GHOST: e = dph::launch_tc_ghost(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
+    case NK_TC_INST: e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
+    case NK_SIMT_GHOST: e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
+    case NK_SIMT_INST: e = dph::launch_simt_inst(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
   }
   if (e != cudaSuccess) return cuda_fail(e, "dp_layer_sqnorms launch");
   if (chosen_mode_out) *chosen_mode_out = chosen;
@@ -248,21 +334,22 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
   if (st != DP_OK) return st;
   if (!A || !G || !factors || !dW) return fail(DP_ERR_INVALID_ARG, "A, G, factors and dW must be non-NULL");
   if (db && !g.has_bias) return fail(DP_ERR_INVALID_ARG, "db given for a layer without bias");
-  const int path = sum_path(g, desc->dtype, A, G);
-  const size_t need = sum_ws_bytes(g, path);
+  const Plan pl = sum_plan(g, desc->dtype, A, G, workspace);
+  const size_t need = sum_ws_bytes(g, pl);
   if (need && (!workspace || ws_bytes < need))
     return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? ws_bytes : (size_t)0);
-  cudaError_t e;
-  if (path == 2)
-    e = dph::launch_tc_sumx(g, A, G, factors, dW, db, accumulate, workspace, status_ptr(), stream);
-  else if (path == 1)
-    e = dph::launch_tc_sum(g, A, G, factors, dW, db, accumulate, static_cast<float*>(workspace),
-                           status_ptr(), stream);
+  void* wsp = workspace;
+  cudaError_t e = prepare_rows(g, pl, A, G, wsp, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum row layout");
+  if (pl.kernel == 2)
+    e = dph::launch_tc_sumx(pl.lg, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
+  else if (pl.kernel == 1)
+    e = dph::launch_tc_sum(pl.lg, A, G, factors, dW, db, accumulate, static_cast<float*>(wsp), status_ptr(),
+                           stream);
   else
     e = dph::launch_simt_clipped_sum(g, desc->dtype, A, G, factors, dW, db, accumulate,
-                                     static_cast<float*>(workspace), (int)dph::simt_sum_splits(g),
-                                     stream);
+                                     static_cast<float*>(wsp), (int)dph::simt_sum_splits(g), stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum launch");
   return ok();
 }

@@ -25,6 +25,13 @@
 //                CTAs of the first column tile they also sum the G rows of every
 //                stage for the bias (they idle between examples otherwise)
 // Register budget: 128 x 64 + 256 x 216 = 63488 <= 64512 = 384 threads x 168 at launch.
+//
+// Norm mode (kNorm): the same per-example products serve the instantiated norm of
+// [MixGhost] section 3 (per-sample gradients formed, then their Frobenius norm):
+// the epilogue adds up P_i^2 over the tile instead of folding c_i P_i, plus the
+// squared bias gradient ||sum_t G_i[t, :]||^2 over the tile's outputs in the first
+// column tile, and writes one partial per (tile, example); a fixed-order reduction
+// over the tiles gives ||g_i||^2.  No cluster: the examples are split over the grid.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -57,6 +64,8 @@ struct Params {
   int B, T, p, d;
   int ex_per_split, splits, accumulate;   // splits = cluster size along z
   int nfull, n16;     // per example: 64-row stages, then 16-row stages
+  float* part;        // norm mode: [tiles, B] per-tile partial squared norms
+  int norm_bias;      // norm mode: the layer has a bias
 };
 
 // Shared-memory control block after the stages.
@@ -65,6 +74,7 @@ struct Ctl {
   uint32_t tmem;
   int abort;
   int flags[2];       // [1] go / no-go after the main loops
+  float red[2][8];    // norm mode: per-warp partials of the last two examples
 };
 
 __device__ __forceinline__ void sync_workers() {
@@ -174,6 +184,93 @@ __device__ __forceinline__ void add_bf16x8(const uint4& v, float* t) {
     t[2 * q] += f.x;
     t[2 * q + 1] += f.y;
   }
+}
+
+// Norm mode, warps 4-11: per example, sum of P_e^2 over the tile (plus the squared
+// bias sums in the first column tile) -> part[tile, e].  Every epilogue warp passes
+// one barrier per example, also after an abort, so none waits for a warp that left.
+__device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem,
+                                              int e0, int e1, bool do_bias) {
+  volatile int* abort = &c->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, half = (warp - kEpiFirst) >> 2;
+  const int et = threadIdx.x - 32 * kEpiFirst;
+  const int bbox = et >> 7, bq = (et >> 4) & 7, bj = et & 15;
+  const int ns = P.nfull + P.n16;
+  const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+  bool ok = true;
+  int k = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int x = e - e0, b = x & 1;
+    float ss = 0.f;
+    if (ok && do_bias) {
+      float bt[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) bt[q] = 0.f;
+      for (int u = 0; u < ns; ++u, ++k) {
+        const int s = k % STAGES;
+        const bool w = ptx::mbar_wait(&c->full[s], (k / STAGES) & 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        const uint8_t* gt = smem + s * STAGE + bbox * BOX + bj * 128 + ((bq ^ (bj & 7)) << 4);
+        if (u < P.nfull) {
+          uint4 v[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) v[h] = *reinterpret_cast<const uint4*>(gt + h * 16 * 128);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) add_bf16x8(v[h], bt);
+        } else {
+          add_bf16x8(*reinterpret_cast<const uint4*>(gt), bt);
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c->empty[s]);
+      }
+      // the 16 lanes of a half-warp share 8 output columns: total them, square them once
+      float bsq = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float v = bt[q];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        bsq = fmaf(v, v, bsq);
+      }
+      if (bj == 0) ss = bsq;
+    }
+    if (ok) {
+      const bool w = ptx::mbar_wait(&c->accum[b], (x >> 1) & 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) ok = false;
+    }
+    if (ok) {
+      ptx::tc_fence_after();
+      const uint32_t base = tmem + b * 256 + half * 128 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+      for (int ch = 0; ch < 8; ch += 2) {
+        float v0[16], v1[16];
+        ptx::tmem_ld16(base + ch * 16, v0);
+        ptx::tmem_ld16(base + ch * 16 + 16, v1);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          ss = fmaf(v0[j], v0[j], ss);
+          ss = fmaf(v1[j], v1[j], ss);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&c->tfree[b]);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) c->red[b][warp - kEpiFirst] = ss;
+    asm volatile("bar.sync 2, %0;" ::"r"(32 * kEpiWarps) : "memory");
+    if (threadIdx.x == 32 * kEpiFirst && !*abort) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kEpiWarps; ++w) t += c->red[b][w];
+      P.part[tile * P.B + e] = t;
+    }
+  }
+  finish_decision(c);
 }
 
 // Warps 4-11: drain P_e from TMEM into fp32 register accumulators, D += c_e * P_e.
@@ -390,6 +487,7 @@ __device__ __forceinline__ void finish(const Params& P, uint8_t* smem, Ctl* c, u
   }
 }
 
+template <bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant__ CUtensorMap mapA64,
                const __grid_constant__ CUtensorMap mapG16, const __grid_constant__ CUtensorMap mapA16,
@@ -402,7 +500,7 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
   const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
   const int e0 = blockIdx.z * P.ex_per_split;
   const int e1 = min(P.B, e0 + P.ex_per_split);
-  const bool do_bias = (P.db != nullptr) && blockIdx.y == 0;
+  const bool do_bias = (kNorm ? P.norm_bias != 0 : P.db != nullptr) && blockIdx.y == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -429,7 +527,10 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
 
   if (warp >= kEpiFirst) {
     ptx::regs_inc<216>();
-    epilogue(P, smem, c, tmem, e0, e1, m0, n0, do_bias);
+    if constexpr (kNorm)
+      epilogue_norm(P, smem, c, tmem, e0, e1, do_bias);
+    else
+      epilogue(P, smem, c, tmem, e0, e1, m0, n0, do_bias);
     finish(P, smem, c, tmem, m0, n0, do_bias);
   } else {
     ptx::regs_dec<64>();
@@ -472,7 +573,7 @@ static int active_clusters(int size) {
     attr[0].val.clusterDim.z = size;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, tcsumx::tc_sumx_kernel, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, tcsumx::tc_sumx_kernel<false>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = 152 / size;   // planning fallback: the full SM count
     }
@@ -540,8 +641,8 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tcsumx::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tcsumx::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -557,9 +658,65 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   attr[0].val.clusterDim.z = splits;
   cfg.attrs = attr;
   cfg.numAttrs = splits > 1 ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel, mg64, ma64, mg16, ma16, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false>, mg64, ma64, mg16, ma16, P);
   count_launch();
   return e;
+}
+
+// Instantiated norm on the tensor cores: per-tile partials [tiles, B] in the workspace,
+// then a fixed-order sum over the tiles.  The examples are split over the grid so the
+// CTAs cover the SMs about once.
+size_t tc_inst_ws_bytes(const Geom& g) {
+  const size_t tiles = (size_t)cdiv_x(g.p, tcsumx::BM) * cdiv_x(g.D, tcsumx::BN);
+  return tiles * (size_t)g.B * sizeof(float);
+}
+
+cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* out, float* ws,
+                           unsigned* status, cudaStream_t s) {
+  CUtensorMap mg64, ma64, mg16, ma16;
+  const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
+  const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
+  const uint64_t da[3] = {(uint64_t)g.D, (uint64_t)g.T, (uint64_t)g.B};
+  const uint64_t sa[2] = {(uint64_t)g.D * 2, (uint64_t)g.T * g.D * 2};
+  const uint32_t box64[3] = {64, 64, 1}, box16[3] = {64, 16, 1};
+  if (!encode_tmap_bf16(&mg64, G, 3, dg, sg, box64) || !encode_tmap_bf16(&ma64, A, 3, da, sa, box64) ||
+      !encode_tmap_bf16(&mg16, G, 3, dg, sg, box16) || !encode_tmap_bf16(&ma16, A, 3, da, sa, box16))
+    return cudaErrorInvalidValue;
+  const int tm = cdiv_x(g.p, tcsumx::BM), tn = cdiv_x(g.D, tcsumx::BN);
+  const long tiles = (long)tm * tn;
+  long chunks = std::max<long>(1, std::min<long>(g.B, 152 / tiles));
+  const int eps = cdiv_x(g.B, chunks);
+  chunks = cdiv_x(g.B, eps);
+  tcsumx::Params P = {};
+  P.status = status;
+  P.B = g.B;
+  P.T = g.T;
+  P.p = g.p;
+  P.d = g.D;
+  P.ex_per_split = eps;
+  P.splits = 1;
+  int nfull = g.T / 64, rem = g.T - 64 * nfull;
+  int n16 = (rem + 15) / 16;
+  if (n16 > 3) { nfull += 1; n16 = 0; }
+  P.nfull = nfull;
+  P.n16 = n16;
+  P.part = ws;
+  P.norm_bias = g.has_bias;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tcsumx::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  dim3 grid(tm, tn, (unsigned)chunks);
+  tcsumx::tc_sumx_kernel<true><<<grid, tcsumx::kThreads, tcsumx::SMEM, s>>>(mg64, ma64, mg16, ma16, P);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_reduce_splits(ws, (int)tiles, (size_t)g.B, out, 0, s);
 }
 
 }  // namespace dph

@@ -17,11 +17,19 @@ bool tc_sumx_supported(const Geom& g);
 size_t tc_sumx_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
                            float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
+// Instantiated norm ||G_i^T A_i||^2 (+ bias) from the same per-example TMEM products
+// (shapes as tc_sumx_supported).
+size_t tc_inst_ws_bytes(const Geom& g);
+cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* out, float* ws,
+                           unsigned* status, cudaStream_t s);
 // Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).
 bool tc_ghost_supported(const Geom& g);
 size_t tc_ghost_ws_bytes(const Geom& g);
 cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* ws,
                             unsigned* status, cudaStream_t s);
+// Conv layer -> row layout of a linear layer (bf16): unfolded input U [B, T, D] and the
+// output gradient transposed per example, Gt [B, T, p].
+cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s);
 // 2D/3D bf16 tensor map with 128-byte swizzle (dims innermost first, strides in bytes).
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);

@@ -61,11 +61,20 @@ def test_full_size_norms_and_sparse_sums(lib, name):
         del A, G
 
 
-@pytest.mark.parametrize("name", ["vit_mlp_b4096_t197", "conv3x3_b256"])
-def test_full_size_sum_is_additive_in_factors(lib, name):
+# The per-example kernel scales each example's fp32 product, so linearity holds to fp32
+# rounding; the row-scaled kernel rounds the scaled rows c_i G_i to bf16 before the
+# MMA (2^-9 relative per element), so it holds to that rounding.
+ADDITIVE = [("vit_mlp_b4096_t197", "", 1e-4), ("conv3x3_b256", "example", 1e-4),
+            ("conv3x3_b256", "rows", 1e-2)]
+
+
+@pytest.mark.parametrize("name,pin,tol", ADDITIVE, ids=["vit", "conv_example", "conv_rows"])
+def test_full_size_sum_is_additive_in_factors(lib, name, pin, tol, monkeypatch):
     """sum(c1) + sum(c2) = sum(c1 + c2) over the whole batch (the reweighting is linear)."""
     import torch
     dp = lib
+    if pin:
+        monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
     wl = workloads.get_workload(name)
     spec = wl.layers[0]
     A, G = workloads.device_layer_inputs(wl, 0)
@@ -82,10 +91,9 @@ def test_full_size_sum_is_additive_in_factors(lib, name):
     torch.cuda.synchronize()
     lhs = outs[0][0] + outs[1][0]
     rhs = outs[2][0]
-    # fp32 accumulation of the same products in different groupings
-    assert (torch.linalg.norm(lhs - rhs) / torch.linalg.norm(rhs)).item() <= 1e-4
+    assert (torch.linalg.norm(lhs - rhs) / torch.linalg.norm(rhs)).item() <= tol
     lhs_b = outs[0][1] + outs[1][1]
-    assert (torch.linalg.norm(lhs_b - outs[2][1]) / torch.linalg.norm(outs[2][1])).item() <= 1e-4
+    assert (torch.linalg.norm(lhs_b - outs[2][1]) / torch.linalg.norm(outs[2][1])).item() <= tol
 
 
 def test_full_size_vgg_step_flat_and_per_layer_factors(lib):

@@ -180,6 +180,14 @@ EDGE = [
     ("conv_dil", LayerSpec("e", "conv2d", p=4, Cin=3, H=10, W=10, k=3, stride=1, pad=2, dil=2), 2, "fp32"),
     ("conv_k1", LayerSpec("e", "conv2d", p=8, Cin=16, H=6, W=6, k=1), 3, "bf16"),
     ("conv_k5_nopad", LayerSpec("e", "conv2d", p=5, Cin=2, H=9, W=8, k=5, a_dist="abs_normal"), 2, "bf16"),
+    # conv layers through their row layout on the tensor cores (D and p multiples of 8)
+    ("conv_rows_3x3", LayerSpec("e", "conv2d", p=72, Cin=16, H=12, W=12, k=3, pad=1), 5, "bf16"),
+    ("conv_rows_s2_dil", LayerSpec("e", "conv2d", p=64, Cin=8, H=17, W=17, k=3, stride=2, pad=2, dil=2), 3,
+     "bf16"),
+    ("conv_rows_T16", LayerSpec("e", "conv2d", p=128, Cin=64, H=4, W=4, k=3, pad=1, a_dist="abs_normal"), 7,
+     "bf16"),
+    ("conv_rows_k1_nobias", LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=1, has_bias=False), 4, "bf16"),
+    ("conv_rows_p8", LayerSpec("e", "conv2d", p=8, Cin=8, H=5, W=7, k=3, pad=1), 3, "bf16"),
 ]
 
 
@@ -190,14 +198,29 @@ def test_edge_shapes(lib, tag, spec, B, dtype):
         _check_layer(lib, spec, wl, mode=mode)
 
 
+@pytest.mark.parametrize("pin", ["rows", "example"])
+def test_conv_rows_sum_kernels(lib, pin, monkeypatch):
+    """Both tensor-core clipped-sum kernels on a conv layer's row layout (ragged tiles)."""
+    monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
+    spec = LayerSpec("e", "conv2d", p=136, Cin=32, H=10, W=9, k=3, pad=1, a_dist="abs_normal")
+    wl = Workload(name="conv_pin", B=6, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=4)
+    _check_layer(lib, spec, wl)
+
+
 ACC = [(LayerSpec("e", "linear", p=40, d=72, T=9), 6),          # SIMT
        (LayerSpec("e", "linear", p=128, d=64, T=40), 5),         # row-scaled tensor-core GEMM
        (LayerSpec("e", "linear", p=128, d=128, T=64), 4),        # per-example, several splits
        (LayerSpec("e", "linear", p=64, d=256, T=80), 1)]         # per-example, one split
 
 
-@pytest.mark.parametrize("spec,B", ACC, ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single"])
-def test_accumulate_adds_to_existing_sum(lib, spec, B):
+ACC_PIN = ["", "rows", "example", "example"]
+
+
+@pytest.mark.parametrize("spec,B,pin", [(s, b, p) for (s, b), p in zip(ACC, ACC_PIN)],
+                         ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single"])
+def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
+    if pin:
+        monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
     import torch
     dp = lib
     wl = Workload(name="acc", B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=2)
