@@ -104,18 +104,27 @@ int resolve_mode(const Geom& g, int requested) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
-// Conv layers in bf16 whose unfolded width D and output count p are multiples of 8
-// (16-byte TMA rows) run the linear tensor-core kernels on their row layout, written
-// into the front of the workspace: U [B, T, D] then Gt [B, T, p].
+// Conv layers in bf16 whose output count p is a multiple of 8 (16-byte TMA rows) run
+// the linear tensor-core kernels on their row layout, written into the front of the
+// workspace: U [B, T, Dp] then Gt [B, T, p], Dp = D rounded up to 8 with zero
+// columns.  Zero columns leave the norms unchanged; a clipped sum over Dp columns
+// goes to a padded buffer in the workspace and its first D columns to dW.
 Geom rows_geom(const Geom& g) {
   Geom r = g;
   r.conv = 0;
-  r.d = r.D;
+  r.D = r.d = dph::conv_rows_width(g);
   return r;
 }
-bool rows_layout_ok(const Geom& g) { return !g.conv || (g.D % 8 == 0 && g.p % 8 == 0); }
+bool rows_layout_ok(const Geom& g) { return !g.conv || g.p % 8 == 0; }
 size_t rows_bytes(const Geom& g) {
-  return g.conv ? align256((size_t)g.B * g.T * g.D * 2) + align256((size_t)g.B * g.T * g.p * 2) : 0;
+  if (!g.conv) return 0;
+  const size_t Dp = dph::conv_rows_width(g);
+  return align256((size_t)g.B * g.T * Dp * 2) + align256((size_t)g.B * g.T * g.p * 2);
+}
+// Padded clipped-sum output (weights then bias) when Dp != D.
+size_t padded_out_bytes(const Geom& g) {
+  if (!g.conv || dph::conv_rows_width(g) == g.D) return 0;
+  return align256((size_t)g.p * dph::conv_rows_width(g) * 4) + align256((size_t)g.p * 4);
 }
 
 // Clipped-sum kernel: 0 SIMT, 1 row-scaled tensor-core GEMM, 2 per-example tensor-core
@@ -154,8 +163,21 @@ int sum_kernel_for(const Geom& lg) {
   return 0;
 }
 
+// DPCLIP_CONV=rows keeps conv layers on their written-out row layout (tests, tuning);
+// otherwise conv layers the im2col kernels take use them.
+bool conv_rows_pinned() {
+  const char* v = std::getenv("DPCLIP_CONV");
+  return v && !std::strcmp(v, "rows");
+}
+
+bool use_tc_conv(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
+  return g.conv && dtype == DP_BF16 && aligned16(A) && aligned16(G) && aligned16(ws) && !conv_rows_pinned() &&
+         dph::tc_conv_supported(g);
+}
+
 Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
   Plan pl{0, false, g};
+  if (!pinned_sum_kernel() && use_tc_conv(g, dtype, A, G, ws)) return Plan{3, false, g};
   if (!tc_inputs(g, dtype, A, G, ws)) return pl;
   const Geom lg = g.conv ? rows_geom(g) : g;
   const int k = sum_kernel_for(lg);
@@ -163,10 +185,11 @@ Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void
   return pl;
 }
 
-enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST };
+enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST, NK_TC_CONV };
 
 Plan norm_plan(const Geom& g, int mode, int dtype, const void* A, const void* G, const void* ws) {
   if (mode == DP_NORM_T1) return Plan{NK_T1, false, g};
+  if (mode == DP_NORM_INSTANTIATE && use_tc_conv(g, dtype, A, G, ws)) return Plan{NK_TC_CONV, false, g};
   const Plan simt{mode == DP_NORM_GHOST ? NK_SIMT_GHOST : NK_SIMT_INST, false, g};
   if (!tc_inputs(g, dtype, A, G, ws)) return simt;
   const Geom lg = g.conv ? rows_geom(g) : g;
@@ -182,9 +205,10 @@ size_t simt_sum_bytes(const Geom& g) {
 // Workspace a call needs on the path it takes (row layout first, then the kernel's own).
 size_t sum_ws_bytes(const Geom& g, const Plan& pl) {
   const Geom& lg = pl.lg;
-  const size_t inner = pl.kernel == 2 ? dph::tc_sumx_ws_bytes(lg)
+  const size_t inner = pl.kernel == 3   ? dph::tc_conv_ws_bytes(g, false)
+                       : pl.kernel == 2 ? dph::tc_sumx_ws_bytes(lg)
                        : pl.kernel == 1 ? dph::tc_sum_ws_bytes(lg) : simt_sum_bytes(g);
-  return (pl.rows ? rows_bytes(g) : 0) + inner;
+  return (pl.rows ? rows_bytes(g) + padded_out_bytes(g) : 0) + inner;
 }
 
 size_t norm_ws_bytes(const Geom& g, const Plan& pl) {
@@ -195,6 +219,7 @@ size_t norm_ws_bytes(const Geom& g, const Plan& pl) {
     case NK_SIMT_INST: inner = dph::simt_inst_ws_floats(g) * sizeof(float); break;
     case NK_TC_GHOST: inner = dph::tc_ghost_ws_bytes(pl.lg); break;
     case NK_TC_INST: inner = dph::tc_inst_ws_bytes(pl.lg); break;
+    case NK_TC_CONV: inner = dph::tc_conv_ws_bytes(g, true); break;
   }
   return (pl.rows ? rows_bytes(g) : 0) + inner;
 }
@@ -211,11 +236,19 @@ size_t max_ws_bytes(const Geom& g, int mode) {
       n = std::max(n, norm_ws_bytes(g, norm_plan(g, mode, dt, ptr, ptr, ptr)));
       n = std::max(n, sum_ws_bytes(g, sum_plan(g, dt, ptr, ptr, ptr)));
     }
-  // either tensor-core sum kernel may be pinned
+  // either tensor-core sum kernel may be pinned, and conv layers may be kept on rows
+  if (dph::tc_conv_supported(g))
+    n = std::max(n, std::max(dph::tc_conv_ws_bytes(g, true), dph::tc_conv_ws_bytes(g, false)));
   if (rows_layout_ok(g)) {
+    if (g.conv) {
+      const Geom lg = rows_geom(g);
+      if (mode == DP_NORM_INSTANTIATE && dph::tc_sumx_supported(lg))
+        n = std::max(n, rows_bytes(g) + dph::tc_inst_ws_bytes(lg));
+    }
     const Geom lg = g.conv ? rows_geom(g) : g;
-    if (dph::tc_sum_supported(lg)) n = std::max(n, rows_bytes(g) + dph::tc_sum_ws_bytes(lg));
-    if (dph::tc_sumx_supported(lg)) n = std::max(n, rows_bytes(g) + dph::tc_sumx_ws_bytes(lg));
+    const size_t pre = rows_bytes(g) + padded_out_bytes(g);
+    if (dph::tc_sum_supported(lg)) n = std::max(n, pre + dph::tc_sum_ws_bytes(lg));
+    if (dph::tc_sumx_supported(lg)) n = std::max(n, pre + dph::tc_sumx_ws_bytes(lg));
   }
   return n;
 }
@@ -226,7 +259,7 @@ cudaError_t prepare_rows(const Geom& g, const Plan& pl, const void*& A, const vo
   if (!pl.rows) return cudaSuccess;
   uint8_t* base = static_cast<uint8_t*>(ws);
   void* U = base;
-  void* Gt = base + align256((size_t)g.B * g.T * g.D * 2);
+  void* Gt = base + align256((size_t)g.B * g.T * dph::conv_rows_width(g) * 2);
   cudaError_t e = dph::launch_conv_rows(g, A, G, U, Gt, stream);
   A = U;
   G = Gt;
@@ -301,6 +334,7 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
     case NK_T1: e = dph::launch_t1_norm(g, desc->dtype, A, G, sqnorm_out, stream); break;
     case NK_TC_GHOST: e = dph::launch_tc_ghost(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_TC_INST: e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
+    case NK_TC_CONV: e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_SIMT_GHOST: e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
     case NK_SIMT_INST: e = dph::launch_simt_inst(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
   }
@@ -342,14 +376,31 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
   void* wsp = workspace;
   cudaError_t e = prepare_rows(g, pl, A, G, wsp, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum row layout");
-  if (pl.kernel == 2)
-    e = dph::launch_tc_sumx(pl.lg, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
+  // padded columns: the kernel writes a padded buffer, then its first D columns go out
+  const bool padded = pl.rows && padded_out_bytes(g) != 0;
+  float* kdW = dW;
+  float* kdb = db;
+  int kacc = accumulate;
+  if (padded) {
+    kdW = static_cast<float*>(wsp);
+    kdb = db ? kdW + align256((size_t)g.p * pl.lg.D * 4) / 4 : nullptr;
+    kacc = 0;
+    wsp = static_cast<uint8_t*>(wsp) + padded_out_bytes(g);
+  }
+  if (pl.kernel == 3)
+    e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
+  else if (pl.kernel == 2)
+    e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
   else if (pl.kernel == 1)
-    e = dph::launch_tc_sum(pl.lg, A, G, factors, dW, db, accumulate, static_cast<float*>(wsp), status_ptr(),
+    e = dph::launch_tc_sum(pl.lg, A, G, factors, kdW, kdb, kacc, static_cast<float*>(wsp), status_ptr(),
                            stream);
   else
     e = dph::launch_simt_clipped_sum(g, desc->dtype, A, G, factors, dW, db, accumulate,
                                      static_cast<float*>(wsp), (int)dph::simt_sum_splits(g), stream);
+  if (e == cudaSuccess && padded) {
+    e = dph::launch_compact_cols(kdW, g.p, g.D, pl.lg.D, dW, accumulate, stream);
+    if (e == cudaSuccess && db) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum launch");
   return ok();
 }

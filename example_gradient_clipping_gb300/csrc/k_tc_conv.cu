@@ -1,0 +1,518 @@
+// Convolution layers on the tensor cores with the unfold done by the TMA unit.
+//
+// The per-example gradient of a conv layer is P_i = F^{-1}(G_i)^T U(a_i) ([MixGhost]
+// section 3.1, eq. 3.1).  Here U(a_i) is never written out: a TMA im2col load brings
+// one [64 pixels x 64 channels] block of U for one filter tap straight from an NHWC
+// copy of the input (zero outside the image), and the NCHW output gradient G_i
+// [p, T] is the K-major A operand as it lies in memory.  Per CTA: one 128 x 256 tile
+// of P (128 outputs x four im2col blocks = 256 unfolded columns), per example in one
+// of two TMEM buffers.
+//   norm mode: the epilogue adds up P_i^2 over the tile -> part[tile, i]; the squared
+//              bias gradient comes from conv_bias_kernel; a fixed-order sum over the
+//              tiles gives ||g_i||^2 (the instantiated norm of [MixGhost] section 3).
+//   sum mode:  the epilogue folds c_i P_i into fp32 registers (the clip factor of
+//              [FastClip] section 5 applied in fp32) over the CTA's examples and
+//              writes a partial tile; a fixed-order reduction over the example splits
+//              maps the columns back to the weight layout [p, Cin, k, k].
+// Columns of the tile: block q = cc * k*k + tap (channel block cc of 64, filter tap
+// kh*k + kw), 64 channels each; the weight column is (64 cc + c) * k*k + tap.
+// Roles (384 threads): warps 0 and 2 TMA producers (alternate stages), warp 1 MMA
+// issuer, warp 3 idle, warps 4-11 epilogue (two per TMEM lane quarter, 128 columns).
+#include <algorithm>
+#include <cudaTypedefs.h>
+
+#include "tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace dpk {
+namespace tcconv {
+
+constexpr int BM = 128, BN = 256, STAGES = 4;
+constexpr int BOX = 64 * 64 * 2;             // 8 KB: 64 rows x 128 B
+constexpr int STAGE = 6 * BOX;               // G [128 outputs x 64 pixels], then 4 im2col blocks
+constexpr int kThreads = 384;
+constexpr int kEpiFirst = 4, kEpiWarps = 8;
+constexpr int SMEM = STAGES * STAGE + 1024 + 512;
+// A = G (K-major: pixels contiguous), B = im2col blocks (MN-major: channels contiguous)
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, BN, 0, 1);
+
+struct Params {
+  const float* factors;   // sum mode
+  float* part;            // norm: [tiles, B]; sum: [splits, p, ncols]
+  unsigned* status;
+  int B, T, p, Wout, k, stride, pad, dil;
+  int items;              // im2col blocks per pixel block: k*k*Cin/64
+  int nk;                 // 64-pixel stages per example
+  int ex_per_split;
+  int ncols;              // items * 64
+};
+
+struct Ctl {
+  uint64_t full[STAGES], empty[STAGES], accum[2], tfree[2], drain;
+  uint32_t tmem;
+  int abort;
+  float red[2][8];
+};
+
+__device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG, const CUtensorMap* mX,
+                                         uint8_t* smem, Ctl* c, int e0, int e1, int m0, int q0, int nitems,
+                                         int pr) {
+  volatile int* abort = &c->abort;
+  const int kk = P.k * P.k;
+  const uint32_t bytes = (uint32_t)(2 + nitems) * BOX;
+  int k = 0, last = -1;
+  bool live = true;
+  for (int e = e0; e < e1 && live; ++e) {
+    for (int u = 0; u < P.nk; ++u, ++k) {
+      if ((k & 1) != pr) continue;
+      const int s = k % STAGES;
+      const bool w = ptx::mbar_wait(&c->empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+      uint8_t* st = smem + s * STAGE;
+      if (ptx::elect_one()) {
+        ptx::mbar_arrive_expect_tx(&c->full[s], bytes);
+        const int t0 = u * 64;
+        ptx::tma_load_3d(mG, &c->full[s], st, t0, m0, e);
+        const int ho = t0 / P.Wout, wo = t0 - ho * P.Wout;
+        const int wb = wo * P.stride - P.pad, hb = ho * P.stride - P.pad;
+        for (int j = 0; j < nitems; ++j) {
+          const int q = q0 + j, cc = q / kk, tap = q - cc * kk;
+          const int kh = tap / P.k, kw = tap - kh * P.k;
+          ptx::tma_load_im2col_4d(mX, &c->full[s], st + (2 + j) * BOX, cc * 64, wb, hb, e,
+                                  (uint16_t)(kw * P.dil), (uint16_t)(kh * P.dil));
+        }
+      }
+      __syncwarp();
+      last = k;
+    }
+  }
+  if (*abort && (threadIdx.x & 31) == 0) {
+    for (int q = max(0, last - STAGES + 1); q <= last; ++q)
+      if ((q & 1) == pr) ptx::mbar_wait_drain(&c->full[q % STAGES], (q / STAGES) & 1);
+  }
+}
+
+__device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0,
+                                           int e1) {
+  volatile int* abort = &c->abort;
+  int k = 0;
+  bool live = true;
+  for (int e = e0; e < e1 && live; ++e) {
+    const int x = e - e0, b = x & 1;
+    if (x >= 2) {
+      const bool w = ptx::mbar_wait(&c->tfree[b], ((x >> 1) & 1) ^ 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) break;
+    }
+    ptx::tc_fence_after();
+    const uint32_t d_tmem = tmem + b * 256;
+    for (int u = 0; u < P.nk; ++u, ++k) {
+      const int s = k % STAGES;
+      const bool w = ptx::mbar_wait(&c->full[s], (k / STAGES) & 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+      const uint32_t g = ptx::smem_u32(smem + s * STAGE);
+      // A: 128 rows of 128 B (64 pixels), K step of 16 pixels = 32 B
+      const uint64_t da = ptx::sdesc_sw128(g, 16, 1024);
+      // B: 64-pixel rows of 128 B per block, blocks BOX apart, K step of 16 pixels = 2048 B
+      const uint64_t dbd = ptx::sdesc_sw128(g + 2 * BOX, BOX, 1024);
+      if (ptx::elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 32), ptx::sdesc_add(dbd, kk * 2048), kIdesc,
+                         (u | kk) != 0);
+        ptx::umma_commit(&c->empty[s]);
+      }
+      __syncwarp();
+    }
+    if (live) {
+      if (ptx::elect_one()) ptx::umma_commit(&c->accum[b]);
+      __syncwarp();
+    }
+  }
+}
+
+// Warps 4-11.  Every epilogue warp walks all of the CTA's examples (also after an
+// abort) so the per-example barrier of the norm mode is always complete.
+template <bool kNorm>
+__device__ __forceinline__ void epilogue(const Params& P, Ctl* c, uint32_t tmem, int e0, int e1, int m0,
+                                         int q0, int nitems) {
+  volatile int* abort = &c->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, half = (warp - kEpiFirst) >> 2;
+  // this thread's 128 columns are blocks 2*half and 2*half + 1 of the tile
+  const bool v0 = 2 * half < nitems, v1 = 2 * half + 1 < nitems;
+  const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+  float acc[kNorm ? 1 : 128];
+  if constexpr (!kNorm) {
+#pragma unroll
+    for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+  }
+  bool ok = true;
+  for (int e = e0; e < e1; ++e) {
+    const int x = e - e0, b = x & 1;
+    float ss = 0.f;
+    if (ok) {
+      const bool w = ptx::mbar_wait(&c->accum[b], (x >> 1) & 1, abort, P.status);
+      if (!__all_sync(0xffffffffu, w)) ok = false;
+    }
+    if (ok) {
+      ptx::tc_fence_after();
+      const float cf = kNorm ? 0.f : __ldg(P.factors + e);
+      const uint32_t base = tmem + b * 256 + half * 128 + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+      for (int ch = 0; ch < 8; ch += 2) {
+        float a0[16], a1[16];
+        ptx::tmem_ld16(base + ch * 16, a0);
+        ptx::tmem_ld16(base + ch * 16 + 16, a1);
+        ptx::tmem_wait_ld();
+        if constexpr (kNorm) {
+          if (ch < 4 ? v0 : v1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              ss = fmaf(a0[j], a0[j], ss);
+              ss = fmaf(a1[j], a1[j], ss);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            acc[ch * 16 + j] = fmaf(cf, a0[j], acc[ch * 16 + j]);
+            acc[ch * 16 + 16 + j] = fmaf(cf, a1[j], acc[ch * 16 + 16 + j]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&c->tfree[b]);
+    }
+    if constexpr (kNorm) {
+      ss = warp_sum(ss);
+      if (lane == 0) c->red[b][warp - kEpiFirst] = ss;
+      asm volatile("bar.sync 2, %0;" ::"r"(32 * kEpiWarps) : "memory");
+      if (threadIdx.x == 32 * kEpiFirst && !*abort) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kEpiWarps; ++w) t += c->red[b][w];
+        P.part[tile * P.B + e] = t;
+      }
+    }
+  }
+  if constexpr (!kNorm) {
+    const int m = m0 + quarter * 32 + lane;
+    if (!ok || *abort || m >= P.p) return;
+    float* out = P.part + ((size_t)blockIdx.z * P.p + m) * P.ncols + (size_t)(q0 + 2 * half) * 64;
+#pragma unroll
+    for (int j = 0; j < 128; j += 4) {
+      if (j < 64 ? v0 : v1)
+        *reinterpret_cast<float4*>(out + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void finish(Ctl* c, uint32_t tmem) {
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*(volatile int*)&c->abort && threadIdx.x == 32) {
+    ptx::umma_commit(&c->drain);   // arrives once every MMA issued so far has completed
+    ptx::mbar_wait_drain(&c->drain, 0);
+  }
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool kNorm>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapX, Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl* c = reinterpret_cast<Ctl*>(smem + STAGES * STAGE);
+  const int warp = threadIdx.x >> 5;
+  const int m0 = blockIdx.x * BM, q0 = blockIdx.y * 4;
+  const int nitems = min(4, P.items - q0);
+  const int e0 = blockIdx.z * P.ex_per_split;
+  const int e1 = min(P.B, e0 + P.ex_per_split);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&c->full[s], 1);
+      ptx::mbar_init(&c->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&c->accum[b], 1);
+      ptx::mbar_init(&c->tfree[b], kEpiWarps);
+    }
+    ptx::mbar_init(&c->drain, 1);
+    c->abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&mapG);
+    ptx::prefetch_tensormap(&mapX);
+  }
+  if (warp == 1) ptx::tmem_alloc(&c->tmem, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = c->tmem;
+
+  if (warp >= kEpiFirst) {
+    ptx::regs_inc<216>();
+    epilogue<kNorm>(P, c, tmem, e0, e1, m0, q0, nitems);
+    finish(c, tmem);
+  } else {
+    ptx::regs_dec<64>();
+    if (warp == 0 || warp == 2)
+      producer(P, &mapG, &mapX, smem, c, e0, e1, m0, q0, nitems, warp >> 1);
+    else if (warp == 1)
+      mma_issuer(P, smem, c, tmem, e0, e1);
+    finish(c, tmem);
+  }
+}
+
+// Bias part, from the NCHW output gradient (rows of T contiguous pixels, T % 8 == 0).
+//   norm: out[i] = sum_j (sum_t G[i, j, t])^2            (one block per example)
+//   sum:  part[split, j] = sum_{i in split} c_i sum_t G[i, j, t]   (one warp per row j)
+__global__ void conv_bias_norm_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
+                                      float* __restrict__ out) {
+  __shared__ float red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = blockIdx.x; i < B; i += gridDim.x) {
+    float acc = 0.f;
+    for (int j = warp; j < p; j += 8) {
+      const __nv_bfloat16* row = G + ((size_t)i * p + j) * T;
+      float s = 0.f;
+      for (int t = lane * 8; t < T; t += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + t);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(h[q]);
+          s += f.x + f.y;
+        }
+      }
+      s = warp_sum(s);
+      acc = fmaf(s, s, acc);
+    }
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+      for (int w = 0; w < 8; ++w) t += red[w];
+      out[i] = t;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void conv_bias_sum_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
+                                     const float* __restrict__ factors, int ex_per_split,
+                                     float* __restrict__ part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * 8 + warp;
+  if (j >= p) return;
+  const int i0 = blockIdx.y * ex_per_split, i1 = min(B, i0 + ex_per_split);
+  float acc = 0.f;
+  for (int i = i0; i < i1; ++i) {
+    const __nv_bfloat16* row = G + ((size_t)i * p + j) * T;
+    float s = 0.f;
+    for (int t = lane * 8; t < T; t += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + t);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        s += f.x + f.y;
+      }
+    }
+    s = warp_sum(s);
+    acc = fmaf(__ldg(factors + i), s, acc);
+  }
+  if (lane == 0) part[(size_t)blockIdx.y * p + j] = acc;
+}
+
+// dW[j, m] (+)= sum_s part[s, j, n(m)] in split order; n(m) maps the weight column
+// m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64).
+__global__ void conv_reduce_kernel(const float* __restrict__ part, int splits, int p, int ncols, int kk,
+                                   float* __restrict__ dW, int accumulate) {
+  const size_t n = (size_t)p * ncols;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
+    const int j = (int)(q / ncols), m = (int)(q - (size_t)j * ncols);
+    const int cch = m / kk, tap = m - cch * kk;
+    const int col = ((cch >> 6) * kk + tap) * 64 + (cch & 63);
+    float s = 0.f;
+    for (int sp = 0; sp < splits; ++sp) s += part[((size_t)sp * p + j) * ncols + col];
+    dW[q] = accumulate ? dW[q] + s : s;
+  }
+}
+
+}  // namespace tcconv
+}  // namespace dpk
+
+namespace dph {
+using namespace dpk;
+
+static int cdiv_c(long a, long b) { return (int)((a + b - 1) / b); }
+static size_t al256(size_t n) { return (n + 255) & ~size_t(255); }
+
+static PFN_cuTensorMapEncodeIm2col_v12000 im2col_fn() {
+  static PFN_cuTensorMapEncodeIm2col_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(p);
+  }
+  return fn;
+}
+
+bool tc_conv_supported(const Geom& g) {
+  if (!g.conv || g.Cin % 64 || g.T % 8 || g.T < 64 || g.p < 8) return false;
+  if (g.stride > 8 || g.pad > 127 || g.dil * (g.k - 1) - g.pad > 128 || g.dil * (g.k - 1) > 65535) return false;
+  return (double)g.B * g.H * g.W * g.Cin < 4e9;
+}
+
+struct ConvPlan {
+  int tm, tn, tiles, items, splits, eps;
+};
+
+static ConvPlan conv_plan(const Geom& g, bool norm) {
+  ConvPlan c;
+  c.items = g.k * g.k * (g.Cin / 64);
+  c.tm = cdiv_c(g.p, tcconv::BM);
+  c.tn = cdiv_c(c.items, 4);
+  c.tiles = c.tm * c.tn;
+  const long want = std::max<long>(1, std::min<long>(g.B, 152 / c.tiles));
+  c.eps = cdiv_c(g.B, want);
+  c.splits = cdiv_c(g.B, c.eps);
+  (void)norm;
+  return c;
+}
+
+// NHWC copy of the input, then the kernel's partials.
+static size_t nhwc_bytes(const Geom& g) { return al256((size_t)g.B * g.H * g.W * g.Cin * 2); }
+
+static constexpr int kBiasSplits = 64;
+
+size_t tc_conv_ws_bytes(const Geom& g, bool norm) {
+  const ConvPlan c = conv_plan(g, norm);
+  if (norm) return nhwc_bytes(g) + al256((size_t)(c.tiles + 1) * g.B * 4);
+  const int bsplits = std::min(g.B, kBiasSplits);
+  return nhwc_bytes(g) + al256((size_t)c.splits * g.p * c.items * 64 * 4) + al256((size_t)bsplits * g.p * 4);
+}
+
+static bool encode_maps(const Geom& g, const void* Xh, const void* G, CUtensorMap* mG, CUtensorMap* mX) {
+  const uint64_t dg[3] = {(uint64_t)g.T, (uint64_t)g.p, (uint64_t)g.B};
+  const uint64_t sg[2] = {(uint64_t)g.T * 2, (uint64_t)g.p * g.T * 2};
+  const uint32_t box[3] = {64, 128, 1};
+  if (!encode_tmap_bf16(mG, G, 3, dg, sg, box)) return false;
+  auto fn = im2col_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)g.Cin, (cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.B};
+  const cuuint64_t str[3] = {(cuuint64_t)g.Cin * 2, (cuuint64_t)g.W * g.Cin * 2, (cuuint64_t)g.H * g.W * g.Cin * 2};
+  const int lo[2] = {-g.pad, -g.pad};
+  const int hi[2] = {g.pad - g.dil * (g.k - 1), g.pad - g.dil * (g.k - 1)};
+  const cuuint32_t es[4] = {1, (cuuint32_t)g.stride, (cuuint32_t)g.stride, 1};
+  const CUresult r = fn(mX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(Xh), dims, str, lo, hi, 64, 64,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kNorm>
+static cudaError_t launch_kernel(const Geom& g, const ConvPlan& c, const CUtensorMap& mG, const CUtensorMap& mX,
+                                 const tcconv::Params& P, cudaStream_t s) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcconv::tc_conv_kernel<kNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tcconv::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  dim3 grid(c.tm, c.tn, c.splits);
+  tcconv::tc_conv_kernel<kNorm><<<grid, tcconv::kThreads, tcconv::SMEM, s>>>(mG, mX, P);
+  count_launch();
+  return cudaGetLastError();
+}
+
+static tcconv::Params base_params(const Geom& g, const ConvPlan& c, unsigned* status) {
+  tcconv::Params P = {};
+  P.status = status;
+  P.B = g.B;
+  P.T = g.T;
+  P.p = g.p;
+  P.Wout = g.Wout;
+  P.k = g.k;
+  P.stride = g.stride;
+  P.pad = g.pad;
+  P.dil = g.dil;
+  P.items = c.items;
+  P.nk = cdiv_c(g.T, 64);
+  P.ex_per_split = c.eps;
+  P.ncols = c.items * 64;
+  return P;
+}
+
+cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, float* out, void* ws,
+                                unsigned* status, cudaStream_t s) {
+  const ConvPlan c = conv_plan(g, true);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* Xh = w;
+  float* part = reinterpret_cast<float*>(w + nhwc_bytes(g));
+  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
+  if (e != cudaSuccess) return e;
+  CUtensorMap mG, mX;
+  if (!encode_maps(g, Xh, G, &mG, &mX)) return cudaErrorInvalidValue;
+  tcconv::Params P = base_params(g, c, status);
+  P.part = part;
+  e = launch_kernel<true>(g, c, mG, mX, P, s);
+  if (e != cudaSuccess) return e;
+  int rows = c.tiles;
+  if (g.has_bias) {
+    tcconv::conv_bias_norm_kernel<<<std::min(g.B, 152 * 8), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T, part + (size_t)c.tiles * g.B);
+    count_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    rows += 1;
+  }
+  return launch_reduce_splits(part, rows, (size_t)g.B, out, 0, s);
+}
+
+cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s) {
+  const ConvPlan c = conv_plan(g, false);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* Xh = w;
+  float* part = reinterpret_cast<float*>(w + nhwc_bytes(g));
+  float* part_db = reinterpret_cast<float*>(w + nhwc_bytes(g) + al256((size_t)c.splits * g.p * c.items * 64 * 4));
+  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mG, mX;
+  if (!encode_maps(g, Xh, G, &mG, &mX)) return cudaErrorInvalidValue;
+  tcconv::Params P = base_params(g, c, status);
+  P.factors = factors;
+  P.part = part;
+  e = launch_kernel<false>(g, c, mG, mX, P, s);
+  if (e != cudaSuccess) return e;
+  const size_t n = (size_t)g.p * c.items * 64;
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
+  tcconv::conv_reduce_kernel<<<blocks, 256, 0, s>>>(part, c.splits, g.p, c.items * 64, g.k * g.k, dW, accumulate);
+  count_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !db) return e;
+  const int bsplits = std::min(g.B, kBiasSplits);
+  const int beps = cdiv_c(g.B, bsplits);
+  dim3 bgrid(cdiv_c(g.p, 8), cdiv_c(g.B, beps));
+  tcconv::conv_bias_sum_kernel<<<bgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T, factors,
+                                                     beps, part_db);
+  count_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_reduce_splits(part_db, (int)bgrid.y, (size_t)g.p, db, accumulate, s);
+}
+
+}  // namespace dph

@@ -13,6 +13,10 @@
 // both operands), an off-diagonal pair two.
 //   warps 0 and 6: TMA producers (alternate slots: one issuing thread streams only
 //   ~48 B/clk into an SM); warp 1: MMA issuer; warps 2-5: epilogue.
+// Packed mode (2T <= 128): one CTA takes ept = 128 / T examples whose rows are
+// consecutive in memory (2D boxes over the flattened rows), so one Gram tile holds
+// every example's Gram as a diagonal block; the epilogue adds only entries (r, s) of
+// the same example, row by row, then sums each example's T rows in a fixed order.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -25,13 +29,14 @@ constexpr int BT = 128, BK = 64, STAGES = 8;
 constexpr int TILE = BT * BK * 2;   // 16 KB
 constexpr int STAGE = TILE;         // one tile per slot
 constexpr int kThreads = 224;
-constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+constexpr int SMEM = STAGES * STAGE + 1024 + 2048;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BT, BT, 0, 0);
 
 struct Params {
   float* out;
   unsigned* status;
   int T, d, p, has_bias;
+  int B, ept;          // packed mode: examples per CTA (0: one CTA per example)
 };
 
 __device__ __forceinline__ void pair_of(int j, int nb, int& tb, int& sb) {
@@ -53,10 +58,12 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drainb + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 2);   // [8]
+  float* rowbuf = red + 8;                                 // packed mode: [2][BT] per-row sums
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x;
-  const int nb = (P.T + BT - 1) / BT;
+  const bool packed = P.ept > 0;
+  const int nb = packed ? 1 : (P.T + BT - 1) / BT;
   const int npairs = nb * (nb + 1) / 2;
   const int kA = (P.d + BK - 1) / BK, kG = (P.p + BK - 1) / BK;
 
@@ -101,7 +108,10 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             if (!__all_sync(0xffffffffu, w)) { live = false; break; }
             if (ptx::elect_one()) {
               ptx::mbar_arrive_expect_tx(&full[s], TILE);
-              ptx::tma_load_3d(map, &full[s], smem + s * STAGE, kk * BK, (h ? sb : tb) * BT, i);
+              if (packed)
+                ptx::tma_load_2d(map, &full[s], smem + s * STAGE, kk * BK, i * P.ept * P.T);
+              else
+                ptx::tma_load_3d(map, &full[s], smem + s * STAGE, kk * BK, (h ? sb : tb) * BT, i);
             }
             __syncwarp();
             ++issued;
@@ -161,6 +171,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   } else if (warp < 6) {
     // ---- epilogue warps: lane quarter (warp & 3) of both Gram tiles ----
     const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;          // TMEM lane = tile row
+    // packed: columns [c_lo, c_hi) are this row's example block
+    const int c_lo = packed ? row / P.T * P.T : 0, c_hi = packed ? c_lo + P.T : BT;
     float H = 0.f, S = 0.f;
     bool ok = true;
     for (int j = 0; j < npairs; ++j) {
@@ -178,10 +191,20 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         ptx::tmem_ld32(base + c * 32, va);
         ptx::tmem_ld32(base + 128 + c * 32, vg);
         ptx::tmem_wait_ld();
+        if (packed) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          h = fmaf(va[e], vg[e], h);
-          sg += vg[e];
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            const bool in = col >= c_lo && col < c_hi;
+            h = fmaf(in ? va[e] : 0.f, vg[e], h);
+            sg += in ? vg[e] : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            h = fmaf(va[e], vg[e], h);
+            sg += vg[e];
+          }
         }
       }
       const float wgt = (tb == sb) ? 1.f : 2.f;
@@ -191,17 +214,29 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tfree[b]);
     }
-    H = warp_sum(H);
-    S = warp_sum(S);
-    if (lane == 0) {
-      red[(warp - 2) * 2] = H;
-      red[(warp - 2) * 2 + 1] = S;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps only
-    if (threadIdx.x == 64 && ok && !*abort) {
-      float h = 0.f, s = 0.f;
-      for (int q = 0; q < 4; ++q) { h += red[2 * q]; s += red[2 * q + 1]; }
-      P.out[i] = h + (P.has_bias ? s : 0.f);
+    if (packed) {
+      rowbuf[row] = H;
+      rowbuf[BT + row] = S;
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps only
+      const int e = threadIdx.x - 64, ex = i * P.ept + e;
+      if (e < P.ept && ex < P.B && ok && !*abort) {
+        float h = 0.f, sg = 0.f;
+        for (int r = e * P.T; r < (e + 1) * P.T; ++r) { h += rowbuf[r]; sg += rowbuf[BT + r]; }
+        P.out[ex] = h + (P.has_bias ? sg : 0.f);
+      }
+    } else {
+      H = warp_sum(H);
+      S = warp_sum(S);
+      if (lane == 0) {
+        red[(warp - 2) * 2] = H;
+        red[(warp - 2) * 2 + 1] = S;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps only
+      if (threadIdx.x == 64 && ok && !*abort) {
+        float h = 0.f, s = 0.f;
+        for (int q = 0; q < 4; ++q) { h += red[2 * q]; s += red[2 * q + 1]; }
+        P.out[i] = h + (P.has_bias ? s : 0.f);
+      }
     }
   }
 
@@ -233,13 +268,22 @@ size_t tc_ghost_ws_bytes(const Geom&) { return 0; }
 cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* /*ws*/,
                             unsigned* status, cudaStream_t s) {
   CUtensorMap ma, mg;
-  const uint64_t da[3] = {(uint64_t)g.d, (uint64_t)g.T, (uint64_t)g.B};
-  const uint64_t sa[2] = {(uint64_t)g.d * 2, (uint64_t)g.T * g.d * 2};
-  const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
-  const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
-  const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
-  if (!encode_tmap_bf16(&ma, A, 3, da, sa, box) || !encode_tmap_bf16(&mg, G, 3, dg, sg, box))
-    return cudaErrorInvalidValue;
+  const int ept = 2 * g.T <= tcghost::BT ? tcghost::BT / g.T : 0;
+  if (ept) {   // flattened rows [B*T, width]
+    const uint64_t da[2] = {(uint64_t)g.d, (uint64_t)g.B * g.T}, sa[1] = {(uint64_t)g.d * 2};
+    const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)g.B * g.T}, sg[1] = {(uint64_t)g.p * 2};
+    const uint32_t box[2] = {tcghost::BK, tcghost::BT};
+    if (!encode_tmap_bf16(&ma, A, 2, da, sa, box) || !encode_tmap_bf16(&mg, G, 2, dg, sg, box))
+      return cudaErrorInvalidValue;
+  } else {
+    const uint64_t da[3] = {(uint64_t)g.d, (uint64_t)g.T, (uint64_t)g.B};
+    const uint64_t sa[2] = {(uint64_t)g.d * 2, (uint64_t)g.T * g.d * 2};
+    const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
+    const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
+    const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
+    if (!encode_tmap_bf16(&ma, A, 3, da, sa, box) || !encode_tmap_bf16(&mg, G, 3, dg, sg, box))
+      return cudaErrorInvalidValue;
+  }
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
@@ -249,8 +293,9 @@ cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* 
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias};
-  tcghost::tc_ghost_kernel<<<g.B, tcghost::kThreads, tcghost::SMEM, s>>>(ma, mg, P);
+  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept};
+  const int grid = ept ? (g.B + ept - 1) / ept : g.B;
+  tcghost::tc_ghost_kernel<<<grid, tcghost::kThreads, tcghost::SMEM, s>>>(ma, mg, P);
   count_launch();
   return cudaGetLastError();
 }

@@ -602,7 +602,7 @@ static void tc_sumx_split(const Geom& g, int* splits, int* ex_per_split, bool qu
 }
 
 bool tc_sumx_supported(const Geom& g) {
-  return !g.conv && (g.p % 8 == 0) && (g.D % 8 == 0) && g.p >= 64 && g.D >= 64 && g.T >= 64;
+  return !g.conv && (g.p % 8 == 0) && (g.D % 8 == 0) && g.p >= 8 && g.D >= 8 && g.T >= 64;
 }
 
 size_t tc_sumx_ws_bytes(const Geom&) { return 0; }

@@ -2,21 +2,68 @@
 //
 // The per-example gradient of a conv layer is F^{-1}(G_i)^T U(a_i) ([MixGhost]
 // section 3.1, eq. 3.1: U is the unfold of the input, F^{-1} flattens the output
-// gradient over positions).  These two kernels write both factors in the row layout
-// of a linear layer, so the linear tensor-core kernels serve conv layers unchanged:
+// gradient over positions).  These kernels write both factors in the row layout of
+// a linear layer, so the linear tensor-core kernels serve conv layers unchanged:
 //   U[i, t, m]  = x_i[c, ho*s - pad + kh*dil, wo*s - pad + kw*dil]  (0 outside the image)
-//                 t = ho*Wout + wo,  m = c*k*k + kh*k + kw  (torch.nn.functional.unfold order)
+//                 t = ho*Wout + wo,  m = c*k*k + kh*k + kw  (torch.nn.functional.unfold order),
+//                 m < Dp: columns D <= m < Dp (Dp = D rounded up to 8) are zero
 //   Gt[i, t, j] = G_i[j, t]   (the NCHW output gradient, transposed per example)
 #include <algorithm>
 
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace dpk {
 
-// One thread writes 8 consecutive m of one row (16-byte store); D % 8 == 0.
-__global__ void unfold_rows_kernel(Geom g, const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ U,
-                                   size_t n_chunks) {
-  const int cpr = g.D >> 3;                           // chunks per row
+// One CTA per example: the example's whole input [Cin, H, W] (contiguous in NCHW) is
+// staged in shared memory with 16-byte loads, then its T output rows are written with
+// 16-byte stores, each gathered from shared memory (zero outside the image).
+__global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __restrict__ x,
+                                        __nv_bfloat16* __restrict__ U) {
+  extern __shared__ __align__(16) __nv_bfloat16 xs[];     // [Cin][H][W]
+  const int kk = g.k * g.k;
+  const int cpr = Dp >> 3;                                // 16-byte chunks per output row
+  const int HW = g.H * g.W;
+  const int n_in = g.Cin * HW;
+  for (int i = blockIdx.x; i < g.B; i += gridDim.x) {
+    const __nv_bfloat16* xi = x + (size_t)i * n_in;
+    if ((n_in & 7) == 0) {
+      for (int q = threadIdx.x; q < (n_in >> 3); q += blockDim.x)
+        reinterpret_cast<uint4*>(xs)[q] = reinterpret_cast<const uint4*>(xi)[q];
+    } else {
+      for (int q = threadIdx.x; q < n_in; q += blockDim.x) xs[q] = xi[q];
+    }
+    __syncthreads();
+    __nv_bfloat16* out = U + (size_t)i * g.T * Dp;
+    const int nch = g.T * cpr;
+    for (int q = threadIdx.x; q < nch; q += blockDim.x) {
+      const int t = q / cpr, m0 = (q - t * cpr) * 8;
+      const int ho = t / g.Wout, wo = t - ho * g.Wout;
+      const int hb = ho * g.stride - g.pad, wb = wo * g.stride - g.pad;
+      // (c, kh, kw) of m0 once, then stepped along the chunk (no per-element division)
+      int c = m0 / kk, r = m0 - c * kk;
+      int kh = r / g.k, kw = r - kh * g.k;
+      __align__(16) __nv_bfloat16 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int h = hb + kh * g.dil, w = wb + kw * g.dil;
+        v[j] = (m0 + j < g.D && h >= 0 && h < g.H && w >= 0 && w < g.W) ? xs[c * HW + h * g.W + w]
+                                                                         : __float2bfloat16_rn(0.f);
+        if (++kw == g.k) {
+          kw = 0;
+          if (++kh == g.k) { kh = 0; ++c; }
+        }
+      }
+      *reinterpret_cast<uint4*>(out + (size_t)q * 8) = *reinterpret_cast<const uint4*>(v);
+    }
+    __syncthreads();
+  }
+}
+
+// Fallback when the staged rows do not fit in shared memory: one thread per 16-byte
+// output chunk, gathered from global memory.
+__global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restrict__ x,
+                                   __nv_bfloat16* __restrict__ U, size_t n_chunks) {
+  const int cpr = Dp >> 3;
   const int kk = g.k * g.k;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n_chunks;
        q += (size_t)gridDim.x * blockDim.x) {
@@ -33,14 +80,53 @@ __global__ void unfold_rows_kernel(Geom g, const __nv_bfloat16* __restrict__ x, 
       const int kh = r / g.k, kw = r - kh * g.k;
       const int h = ho * g.stride - g.pad + kh * g.dil;
       const int w = wo * g.stride - g.pad + kw * g.dil;
-      v[j] = (h >= 0 && h < g.H && w >= 0 && w < g.W) ? xi[((size_t)c * g.H + h) * g.W + w]
-                                                      : __float2bfloat16_rn(0.f);
+      v[j] = (m < g.D && h >= 0 && h < g.H && w >= 0 && w < g.W) ? xi[((size_t)c * g.H + h) * g.W + w]
+                                                                 : __float2bfloat16_rn(0.f);
     }
     *reinterpret_cast<uint4*>(U + q * 8) = *reinterpret_cast<const uint4*>(v);
   }
 }
 
-// Per example [p, T] -> [T, p] through a 32 x 33 shared tile.
+// Per example [p, T] -> [T, p] in 64 x 64 tiles with 16-byte loads and stores
+// (T % 8 == 0 and p % 8 == 0).  Shared tile [j][t] in 8-element chunks, chunk
+// index XORed with (j / 8) % 8 so that both the row stores and the column gathers
+// spread over the banks.
+constexpr int kTT = 64;
+__global__ void transpose_rows_vec_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
+                                          __nv_bfloat16* __restrict__ Gt) {
+  __shared__ __align__(16) __nv_bfloat16 s[kTT][kTT];
+  const int tt = (T + kTT - 1) / kTT, tp = (p + kTT - 1) / kTT;
+  const long units = (long)B * tt * tp;
+  for (long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int i = (int)(u / ((long)tt * tp));
+    const int rem = (int)(u - (long)i * tt * tp);
+    const int t0 = (rem / tp) * kTT, j0 = (rem % tp) * kTT;
+    const __nv_bfloat16* gi = G + (size_t)i * T * p;
+    for (int q = threadIdx.x; q < kTT * (kTT / 8); q += blockDim.x) {
+      const int jr = q >> 3, tc = q & 7;                 // tile row (output j), t chunk
+      const int j = j0 + jr, t = t0 + tc * 8;
+      if (j < p && t < T)
+        *reinterpret_cast<uint4*>(&s[jr][(tc ^ ((jr >> 3) & 7)) * 8]) =
+            *reinterpret_cast<const uint4*>(gi + (size_t)j * T + t);
+    }
+    __syncthreads();
+    __nv_bfloat16* go = Gt + (size_t)i * T * p;
+    for (int q = threadIdx.x; q < kTT * (kTT / 8); q += blockDim.x) {
+      const int tr = q >> 3, jc = q & 7;                 // tile t, j chunk
+      const int t = t0 + tr, j = j0 + jc * 8;
+      if (t < T && j < p) {
+        __align__(16) __nv_bfloat16 v[8];
+        const int col = ((tr >> 3) ^ jc) * 8 + (tr & 7);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) v[r] = s[jc * 8 + r][col];
+        *reinterpret_cast<uint4*>(go + (size_t)t * p + j) = *reinterpret_cast<const uint4*>(v);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// General fallback: 32 x 33 tiles, 2-byte accesses.
 __global__ void transpose_rows_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
                                       __nv_bfloat16* __restrict__ Gt) {
   __shared__ __nv_bfloat16 tile[32][33];
@@ -60,22 +146,75 @@ __global__ void transpose_rows_kernel(int B, int T, int p, const __nv_bfloat16* 
   }
 }
 
+// dW[j, m] (+)= Wp[j, m] for m < D (the padded columns are dropped).
+__global__ void compact_cols_kernel(const float* __restrict__ Wp, int p, int D, int Dp, float* __restrict__ dW,
+                                    int accumulate) {
+  const size_t n = (size_t)p * D;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t j = q / D, m = q - j * D;
+    const float v = Wp[j * Dp + m];
+    dW[q] = accumulate ? dW[q] + v : v;
+  }
+}
+
+constexpr int kUnfoldSmemMax = 160 * 1024;
+
 }  // namespace dpk
 
 namespace dph {
 using namespace dpk;
 
+int conv_rows_width(const Geom& g) { return (g.D + 7) / 8 * 8; }
+
 cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s) {
-  const size_t n_chunks = (size_t)g.B * g.T * (g.D / 8);
-  const size_t blocks = std::min<size_t>((n_chunks + 255) / 256, (size_t)152 * 16);
-  unfold_rows_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(
-      g, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(U), n_chunks);
+  const int Dp = conv_rows_width(g);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  auto* Ub = static_cast<__nv_bfloat16*>(U);
+  const size_t stage = (size_t)g.Cin * g.H * g.W * sizeof(__nv_bfloat16);
+  if (stage <= (size_t)kUnfoldSmemMax) {
+    if (stage > 48 * 1024) {
+      int dev = 0;
+      cudaGetDevice(&dev);
+      static bool attr_set[64] = {};
+      if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(unfold_rows_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kUnfoldSmemMax);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+      }
+    }
+    const unsigned blocks = (unsigned)std::min<long>(g.B, 152L * 16);
+    unfold_rows_smem_kernel<<<blocks, 256, stage, s>>>(g, Dp, xb, Ub);
+  } else {
+    const size_t n_chunks = (size_t)g.B * g.T * (Dp / 8);
+    const size_t blocks = std::min<size_t>((n_chunks + 255) / 256, (size_t)152 * 16);
+    unfold_rows_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(g, Dp, xb, Ub, n_chunks);
+  }
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dim3 grid((g.T + 31) / 32, (g.p + 31) / 32, std::min(g.B, 65535));
-  transpose_rows_kernel<<<grid, dim3(32, 8), 0, s>>>(g.B, g.T, g.p, static_cast<const __nv_bfloat16*>(G),
-                                                      static_cast<__nv_bfloat16*>(Gt));
+  return launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);
+}
+
+cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s) {
+  const auto* Gb = static_cast<const __nv_bfloat16*>(src);
+  auto* Gtb = static_cast<__nv_bfloat16*>(dst);
+  if (T % 8 == 0 && p % 8 == 0) {
+    const long units = (long)B * ((T + kTT - 1) / kTT) * ((p + kTT - 1) / kTT);
+    const unsigned blocks = (unsigned)std::min<long>(units, 152L * 16);
+    transpose_rows_vec_kernel<<<blocks, 256, 0, s>>>(B, T, p, Gb, Gtb);
+  } else {
+    dim3 grid((T + 31) / 32, (p + 31) / 32, std::min(B, 65535));
+    transpose_rows_kernel<<<grid, dim3(32, 8), 0, s>>>(B, T, p, Gb, Gtb);
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact_cols(const float* Wp, int p, int D, int Dp, float* dW, int accumulate, cudaStream_t s) {
+  const size_t n = (size_t)p * D;
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
+  compact_cols_kernel<<<blocks ? blocks : 1, 256, 0, s>>>(Wp, p, D, Dp, dW, accumulate);
   count_launch();
   return cudaGetLastError();
 }

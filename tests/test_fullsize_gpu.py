@@ -64,11 +64,11 @@ def test_full_size_norms_and_sparse_sums(lib, name):
 # The per-example kernel scales each example's fp32 product, so linearity holds to fp32
 # rounding; the row-scaled kernel rounds the scaled rows c_i G_i to bf16 before the
 # MMA (2^-9 relative per element), so it holds to that rounding.
-ADDITIVE = [("vit_mlp_b4096_t197", "", 1e-4), ("conv3x3_b256", "example", 1e-4),
-            ("conv3x3_b256", "rows", 1e-2)]
+ADDITIVE = [("vit_mlp_b4096_t197", "", 1e-4), ("conv3x3_b256", "", 1e-4),
+            ("conv3x3_b256", "example", 1e-4), ("conv3x3_b256", "rows", 1e-2)]
 
 
-@pytest.mark.parametrize("name,pin,tol", ADDITIVE, ids=["vit", "conv_example", "conv_rows"])
+@pytest.mark.parametrize("name,pin,tol", ADDITIVE, ids=["vit", "conv_im2col", "conv_example", "conv_rows"])
 def test_full_size_sum_is_additive_in_factors(lib, name, pin, tol, monkeypatch):
     """sum(c1) + sum(c2) = sum(c1 + c2) over the whole batch (the reweighting is linear)."""
     import torch

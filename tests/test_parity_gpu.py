@@ -188,6 +188,15 @@ EDGE = [
      "bf16"),
     ("conv_rows_k1_nobias", LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=1, has_bias=False), 4, "bf16"),
     ("conv_rows_p8", LayerSpec("e", "conv2d", p=8, Cin=8, H=5, W=7, k=3, pad=1), 3, "bf16"),
+    # D = 27 padded to 32 columns in the row layout (the first VGG-11 layer's shape)
+    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16"),
+    ("conv_rows_padD_s2", LayerSpec("e", "conv2d", p=24, Cin=5, H=13, W=11, k=3, stride=2, pad=1), 3, "bf16"),
+    # conv layers whose unfold is done by TMA im2col loads (Cin % 64 == 0, T % 8 == 0, T >= 64)
+    ("conv_im2col_3x3", LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 3, "bf16"),
+    ("conv_im2col_s2_dil2", LayerSpec("e", "conv2d", p=136, Cin=128, H=23, W=23, k=3, stride=2, pad=2, dil=2),
+     2, "bf16"),
+    ("conv_im2col_k5_nobias", LayerSpec("e", "conv2d", p=64, Cin=64, H=12, W=12, k=5, has_bias=False,
+                                        a_dist="abs_normal"), 3, "bf16"),
 ]
 
 
@@ -195,6 +204,17 @@ EDGE = [
 def test_edge_shapes(lib, tag, spec, B, dtype):
     wl = Workload(name=tag, B=B, layers=(spec,), dtype=dtype, C=1.0, sigma=1.0, seed=11)
     for mode in (None, lib.DP_NORM_GHOST, lib.DP_NORM_INSTANTIATE):
+        _check_layer(lib, spec, wl, mode=mode)
+
+
+@pytest.mark.parametrize("conv_pin", ["", "rows"], ids=["im2col", "rows"])
+def test_conv3x3_im2col_and_row_layout(lib, conv_pin, monkeypatch):
+    """The 3x3 conv workload's layer (small batch): im2col kernels and the row layout."""
+    if conv_pin:
+        monkeypatch.setenv("DPCLIP_CONV", conv_pin)
+    wl = workloads.get_workload("conv3x3_b256").with_batch(5)
+    spec = wl.layers[0]
+    for mode in (None, lib.DP_NORM_INSTANTIATE, lib.DP_NORM_GHOST):
         _check_layer(lib, spec, wl, mode=mode)
 
 
@@ -207,17 +227,18 @@ def test_conv_rows_sum_kernels(lib, pin, monkeypatch):
     _check_layer(lib, spec, wl)
 
 
-ACC = [(LayerSpec("e", "linear", p=40, d=72, T=9), 6),          # SIMT
+ACC = [(LayerSpec("e", "linear", p=42, d=72, T=9), 6),          # SIMT (p not a multiple of 8)
        (LayerSpec("e", "linear", p=128, d=64, T=40), 5),         # row-scaled tensor-core GEMM
        (LayerSpec("e", "linear", p=128, d=128, T=64), 4),        # per-example, several splits
-       (LayerSpec("e", "linear", p=64, d=256, T=80), 1)]         # per-example, one split
+       (LayerSpec("e", "linear", p=64, d=256, T=80), 1),         # per-example, one split
+       (LayerSpec("e", "conv2d", p=16, Cin=3, H=8, W=8, k=3, pad=1), 3)]   # conv, padded columns
 
 
-ACC_PIN = ["", "rows", "example", "example"]
+ACC_PIN = ["", "rows", "example", "example", ""]
 
 
 @pytest.mark.parametrize("spec,B,pin", [(s, b, p) for (s, b), p in zip(ACC, ACC_PIN)],
-                         ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single"])
+                         ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single", "conv_padded"])
 def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
     if pin:
         monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
