@@ -170,14 +170,27 @@ bool conv_rows_pinned() {
   return v && !std::strcmp(v, "rows");
 }
 
+bool im2col_inputs(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
+  return g.conv && dtype == DP_BF16 && aligned16(A) && aligned16(G) && aligned16(ws) && !conv_rows_pinned();
+}
 bool use_tc_conv(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
-  return g.conv && dtype == DP_BF16 && aligned16(A) && aligned16(G) && aligned16(ws) && !conv_rows_pinned() &&
-         dph::tc_conv_supported(g);
+  return im2col_inputs(g, dtype, A, G, ws) && dph::tc_conv_supported(g);
+}
+
+// Conv clipped sums with im2col loads: per-example TMEM products (fp32 scaling) when an
+// example has at least 128 rows, else the row-scaled GEMM (many examples per stage).
+// One-row linear layers whose outer-product sum is small (or fp32) take the FFMA kernel.
+bool use_t1_sum(const Geom& g, int dtype) {
+  return !g.conv && g.T == 1 && (dtype == DP_FP32 || (double)g.p * g.d * g.B < (double)(1 << 28));
 }
 
 Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
   Plan pl{0, false, g};
-  if (!pinned_sum_kernel() && use_tc_conv(g, dtype, A, G, ws)) return Plan{3, false, g};
+  if (use_t1_sum(g, dtype)) return Plan{5, false, g};
+  if (!pinned_sum_kernel() && im2col_inputs(g, dtype, A, G, ws)) {
+    if (g.T >= 128 && dph::tc_conv_supported(g)) return Plan{3, false, g};
+    if (dph::tc_sum_conv_supported(g)) return Plan{4, false, g};
+  }
   if (!tc_inputs(g, dtype, A, G, ws)) return pl;
   const Geom lg = g.conv ? rows_geom(g) : g;
   const int k = sum_kernel_for(lg);
@@ -185,11 +198,13 @@ Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void
   return pl;
 }
 
-enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST, NK_TC_CONV };
+enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST, NK_TC_CONV, NK_TC_GHOST_CONV };
 
 Plan norm_plan(const Geom& g, int mode, int dtype, const void* A, const void* G, const void* ws) {
   if (mode == DP_NORM_T1) return Plan{NK_T1, false, g};
   if (mode == DP_NORM_INSTANTIATE && use_tc_conv(g, dtype, A, G, ws)) return Plan{NK_TC_CONV, false, g};
+  if (mode == DP_NORM_GHOST && im2col_inputs(g, dtype, A, G, ws) && dph::tc_ghost_conv_supported(g))
+    return Plan{NK_TC_GHOST_CONV, false, g};
   const Plan simt{mode == DP_NORM_GHOST ? NK_SIMT_GHOST : NK_SIMT_INST, false, g};
   if (!tc_inputs(g, dtype, A, G, ws)) return simt;
   const Geom lg = g.conv ? rows_geom(g) : g;
@@ -205,9 +220,14 @@ size_t simt_sum_bytes(const Geom& g) {
 // Workspace a call needs on the path it takes (row layout first, then the kernel's own).
 size_t sum_ws_bytes(const Geom& g, const Plan& pl) {
   const Geom& lg = pl.lg;
-  const size_t inner = pl.kernel == 3   ? dph::tc_conv_ws_bytes(g, false)
+  // a conv layer's row-scaled GEMM reads pre-scaled rows; its bias is summed separately
+  const size_t inner = pl.kernel == 5   ? dph::t1_sum_ws_bytes(g)
+                       : pl.kernel == 4 ? dph::tc_sum_conv_ws_bytes(g)
+                       : pl.kernel == 3 ? dph::tc_conv_ws_bytes(g, false)
                        : pl.kernel == 2 ? dph::tc_sumx_ws_bytes(lg)
-                       : pl.kernel == 1 ? dph::tc_sum_ws_bytes(lg) : simt_sum_bytes(g);
+                       : pl.kernel == 1 ? align256(dph::tc_sum_ws_bytes(lg)) +
+                                              (pl.rows ? dph::scaled_rows_bias_bytes(g.B, g.T, g.p) : 0)
+                                        : simt_sum_bytes(g);
   return (pl.rows ? rows_bytes(g) + padded_out_bytes(g) : 0) + inner;
 }
 
@@ -220,6 +240,7 @@ size_t norm_ws_bytes(const Geom& g, const Plan& pl) {
     case NK_TC_GHOST: inner = dph::tc_ghost_ws_bytes(pl.lg); break;
     case NK_TC_INST: inner = dph::tc_inst_ws_bytes(pl.lg); break;
     case NK_TC_CONV: inner = dph::tc_conv_ws_bytes(g, true); break;
+    case NK_TC_GHOST_CONV: inner = dph::tc_ghost_conv_ws_bytes(g); break;
   }
   return (pl.rows ? rows_bytes(g) : 0) + inner;
 }
@@ -239,6 +260,10 @@ size_t max_ws_bytes(const Geom& g, int mode) {
   // either tensor-core sum kernel may be pinned, and conv layers may be kept on rows
   if (dph::tc_conv_supported(g))
     n = std::max(n, std::max(dph::tc_conv_ws_bytes(g, true), dph::tc_conv_ws_bytes(g, false)));
+  if (dph::tc_sum_conv_supported(g)) n = std::max(n, dph::tc_sum_conv_ws_bytes(g));
+  if (mode == DP_NORM_GHOST && dph::tc_ghost_conv_supported(g)) n = std::max(n, dph::tc_ghost_conv_ws_bytes(g));
+  if (g.conv && rows_layout_ok(g) && mode == DP_NORM_GHOST && dph::tc_ghost_supported(rows_geom(g)))
+    n = std::max(n, rows_bytes(g) + dph::tc_ghost_ws_bytes(rows_geom(g)));
   if (rows_layout_ok(g)) {
     if (g.conv) {
       const Geom lg = rows_geom(g);
@@ -247,7 +272,9 @@ size_t max_ws_bytes(const Geom& g, int mode) {
     }
     const Geom lg = g.conv ? rows_geom(g) : g;
     const size_t pre = rows_bytes(g) + padded_out_bytes(g);
-    if (dph::tc_sum_supported(lg)) n = std::max(n, pre + dph::tc_sum_ws_bytes(lg));
+    if (dph::tc_sum_supported(lg))
+      n = std::max(n, pre + align256(dph::tc_sum_ws_bytes(lg)) +
+                          (g.conv ? dph::scaled_rows_bias_bytes(g.B, g.T, g.p) : 0));
     if (dph::tc_sumx_supported(lg)) n = std::max(n, pre + dph::tc_sumx_ws_bytes(lg));
   }
   return n;
@@ -255,12 +282,13 @@ size_t max_ws_bytes(const Geom& g, int mode) {
 
 // Launch the row layout of a conv layer into the workspace; returns the pointers.
 cudaError_t prepare_rows(const Geom& g, const Plan& pl, const void*& A, const void*& G, void*& ws,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const float* scale = nullptr, float* db = nullptr,
+                         int accumulate = 0, float* bias_part = nullptr) {
   if (!pl.rows) return cudaSuccess;
   uint8_t* base = static_cast<uint8_t*>(ws);
   void* U = base;
   void* Gt = base + align256((size_t)g.B * g.T * dph::conv_rows_width(g) * 2);
-  cudaError_t e = dph::launch_conv_rows(g, A, G, U, Gt, stream);
+  cudaError_t e = dph::launch_conv_rows(g, A, G, U, Gt, stream, scale, db, accumulate, bias_part);
   A = U;
   G = Gt;
   ws = base + rows_bytes(g);
@@ -335,6 +363,7 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
     case NK_TC_GHOST: e = dph::launch_tc_ghost(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_TC_INST: e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_TC_CONV: e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
+    case NK_TC_GHOST_CONV: e = dph::launch_tc_ghost_conv(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_SIMT_GHOST: e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
     case NK_SIMT_INST: e = dph::launch_simt_inst(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
   }
@@ -374,7 +403,15 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
     return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
                 workspace ? ws_bytes : (size_t)0);
   void* wsp = workspace;
-  cudaError_t e = prepare_rows(g, pl, A, G, wsp, stream);
+  // conv rows for the row-scaled GEMM: the transpose writes bf16(c_i G_i^T) directly and
+  // sums the bias on the way (its partials sit after the GEMM's in the workspace)
+  const bool prescale = pl.rows && pl.kernel == 1;
+  float* bias_part = prescale ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + rows_bytes(g) +
+                                                         padded_out_bytes(g) +
+                                                         align256(dph::tc_sum_ws_bytes(pl.lg)))
+                              : nullptr;
+  cudaError_t e = prepare_rows(g, pl, A, G, wsp, stream, prescale ? factors : nullptr, prescale ? db : nullptr,
+                               accumulate, bias_part);
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum row layout");
   // padded columns: the kernel writes a padded buffer, then its first D columns go out
   const bool padded = pl.rows && padded_out_bytes(g) != 0;
@@ -387,11 +424,18 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
     kacc = 0;
     wsp = static_cast<uint8_t*>(wsp) + padded_out_bytes(g);
   }
-  if (pl.kernel == 3)
+  if (pl.kernel == 5)
+    e = dph::launch_t1_sum(g, desc->dtype, A, G, factors, dW, db, accumulate, static_cast<float*>(wsp), stream);
+  else if (pl.kernel == 4)
+    e = dph::launch_tc_sum_conv(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
+  else if (pl.kernel == 3)
     e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
   else if (pl.kernel == 2)
     e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
-  else if (pl.kernel == 1)
+  else if (prescale) {
+    e = dph::launch_tc_sum_prescaled(pl.lg, A, G, kdW, kacc, static_cast<float*>(wsp), status_ptr(), stream);
+    kdb = nullptr;   // the bias went straight to db
+  } else if (pl.kernel == 1)
     e = dph::launch_tc_sum(pl.lg, A, G, factors, kdW, kdb, kacc, static_cast<float*>(wsp), status_ptr(),
                            stream);
   else
@@ -399,7 +443,7 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
                                      static_cast<float*>(wsp), (int)dph::simt_sum_splits(g), stream);
   if (e == cudaSuccess && padded) {
     e = dph::launch_compact_cols(kdW, g.p, g.D, pl.lg.D, dW, accumulate, stream);
-    if (e == cudaSuccess && db) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);
+    if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum launch");
   return ok();

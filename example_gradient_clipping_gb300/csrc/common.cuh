@@ -113,6 +113,11 @@ dp_status geom_from_desc(const dp_layer_desc* d, Geom* g);
 dp_status set_error(dp_status st, const char* msg);
 cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* G, float* out,
                            cudaStream_t s);
+// One-row (T = 1) linear clipped sum, FFMA, example splits reduced in a fixed order.
+int t1_sum_splits(const Geom& g);
+size_t t1_sum_ws_bytes(const Geom& g);
+cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G, const float* factors, float* dW,
+                          float* db, int accumulate, float* ws, cudaStream_t s);
 cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, const float* C,
                                 float* out, unsigned* status, cudaStream_t s);
 cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,

@@ -1,4 +1,6 @@
 // HBM-bound and tiny kernels: one-row norms, clip factors, Gaussian noise, adaptive bound.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dpk {
@@ -38,6 +40,37 @@ __global__ void __launch_bounds__(256) t1_norm_kernel(Geom g, const E* __restric
     const float sa = row_sqsum(A + (size_t)i * g.d, g.d, lane, vec_a);
     const float sg = row_sqsum(G + (size_t)i * g.p, g.p, lane, vec_g);
     if (lane == 0) out[i] = sa * sg + (g.has_bias ? sg : 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One-row clipped sum: dW[j, m] = sum_i c_i g_i[j] a_i[m], db[j] = sum_i c_i g_i[j]
+// (the reweighted sum of [FastClip] section 5 for T = 1: a sum of scaled outer
+// products).  Thread -> (j, four consecutive m); a warp reads a_i[m .. m+127]
+// coalesced and broadcasts g_i[j]; examples are split over blockIdx.y into partials.
+template <class E>
+__global__ void __launch_bounds__(256) t1_sum_kernel(Geom g, const E* __restrict__ A, const E* __restrict__ G,
+                                                     const float* __restrict__ factors, int ex_per_split,
+                                                     float* __restrict__ part_w, float* __restrict__ part_b) {
+  const int mq = (g.d + 3) / 4;                      // m quads per row
+  const long n_th = (long)g.p * mq;
+  const int i0 = blockIdx.y * ex_per_split, i1 = min(g.B, i0 + ex_per_split);
+  for (long q = blockIdx.x * (long)blockDim.x + threadIdx.x; q < n_th; q += (long)gridDim.x * blockDim.x) {
+    const int j = (int)(q / mq), m0 = (int)(q - (long)j * mq) * 4;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, bacc = 0.f;
+    for (int i = i0; i < i1; ++i) {
+      const float cg = __ldg(factors + i) * to_f(G[(size_t)i * g.p + j]);
+      const E* a = A + (size_t)i * g.d + m0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (m0 + r < g.d) acc[r] = fmaf(cg, to_f(a[r]), acc[r]);
+      bacc += cg;
+    }
+    float* out = part_w + ((size_t)blockIdx.y * g.p + j) * g.d + m0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      if (m0 + r < g.d) out[r] = acc[r];
+    if (part_b && m0 == 0) part_b[(size_t)blockIdx.y * g.p + j] = bacc;
   }
 }
 
@@ -187,6 +220,33 @@ cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alph
   adaptive_bound_kernel<<<1, 256, 0, s>>>(sq, B, C_l2, alpha, beta, sigma_l2, seed, layer, out);
   count_launch();
   return cudaGetLastError();
+}
+
+// Examples per split of the one-row clipped sum: about 128, at least one split.
+static int t1_sum_eps(const Geom& g) { return std::min(g.B, 128); }
+int t1_sum_splits(const Geom& g) { const int e = t1_sum_eps(g); return (g.B + e - 1) / e; }
+size_t t1_sum_ws_bytes(const Geom& g) {
+  return (size_t)t1_sum_splits(g) * ((size_t)g.p * g.d + g.p) * sizeof(float);
+}
+
+cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G, const float* factors, float* dW,
+                          float* db, int accumulate, float* ws, cudaStream_t s) {
+  const int eps = t1_sum_eps(g), splits = t1_sum_splits(g);
+  float* part_w = ws;
+  float* part_b = db ? ws + (size_t)splits * g.p * g.d : nullptr;
+  const long n_th = (long)g.p * ((g.d + 3) / 4);
+  dim3 grid((unsigned)std::min<long>((n_th + 255) / 256, 152L * 8), (unsigned)splits);
+  if (dtype == DP_FP32)
+    t1_sum_kernel<float><<<grid, 256, 0, s>>>(g, (const float*)A, (const float*)G, factors, eps, part_w, part_b);
+  else
+    t1_sum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(g, (const __nv_bfloat16*)A, (const __nv_bfloat16*)G,
+                                                      factors, eps, part_w, part_b);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_reduce_splits(part_w, splits, (size_t)g.p * g.d, dW, accumulate, s);
+  if (e != cudaSuccess || !db) return e;
+  return launch_reduce_splits(part_b, splits, (size_t)g.p, db, accumulate, s);
 }
 
 }  // namespace dph

@@ -132,6 +132,20 @@ __global__ void reduce_splits_kernel(const float* __restrict__ ws, int splits, s
   }
 }
 
+// Many splits of a short vector: one warp per element, lanes stride over the splits,
+// then a fixed butterfly (deterministic).
+__global__ void reduce_splits_warp_kernel(const float* __restrict__ ws, int splits, size_t n,
+                                          float* __restrict__ out, int accumulate) {
+  const int lane = threadIdx.x & 31;
+  const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
+  for (size_t e = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; e < n; e += nw) {
+    float s = 0.f;
+    for (int k = lane; k < splits; k += 32) s += ws[(size_t)k * n + e];
+    s = warp_sum(s);
+    if (lane == 0) out[e] = accumulate ? out[e] + s : s;
+  }
+}
+
 // Instantiated norm: CTA (bx, by, i) forms the 64x64 tile of g_i = G_i^T U(A_i)
 // over all T rows of example i, squares and sums it ([MixGhost] Appendix C.4).
 // CTAs with by == 0 also form the bias gradient sum_t G_i[t, :] of their rows.
@@ -301,6 +315,12 @@ cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, con
 
 cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
                                  cudaStream_t s) {
+  if (splits >= 16 && n <= ((size_t)1 << 16)) {
+    const size_t blocks = std::min<size_t>((n * 32 + 255) / 256, 152 * 8);
+    reduce_splits_warp_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(ws, splits, n, out, accumulate);
+    count_launch();
+    return cudaGetLastError();
+  }
   const size_t blocks = std::min<size_t>((n + 255) / 256, 152 * 8);
   reduce_splits_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(ws, splits, n, out, accumulate);
   count_launch();

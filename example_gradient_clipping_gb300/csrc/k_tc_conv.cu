@@ -312,18 +312,45 @@ __global__ void conv_bias_sum_kernel(const __nv_bfloat16* __restrict__ G, int B,
   if (j >= p) return;
   const int i0 = blockIdx.y * ex_per_split, i1 = min(B, i0 + ex_per_split);
   float acc = 0.f;
+  // four examples in flight per pass (independent loads), summed in example order
+  for (int ib = i0; ib < i1; ib += 4) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (ib + u >= i1) break;
+      const __nv_bfloat16* row = G + ((size_t)(ib + u) * p + j) * T;
+      for (int t = lane * 8; t < T; t += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + t);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(h[q]);
+          s[u] += f.x + f.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float su = warp_sum(s[u]);
+      if (ib + u < i1) acc = fmaf(__ldg(factors + ib + u), su, acc);
+    }
+  }
+  if (lane == 0) part[(size_t)blockIdx.y * p + j] = acc;
+}
+
+// As conv_bias_sum_kernel for rows whose length is not a multiple of 8 (scalar loads).
+__global__ void conv_bias_sum_scalar_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
+                                            const float* __restrict__ factors, int ex_per_split,
+                                            float* __restrict__ part) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * 8 + warp;
+  if (j >= p) return;
+  const int i0 = blockIdx.y * ex_per_split, i1 = min(B, i0 + ex_per_split);
+  float acc = 0.f;
   for (int i = i0; i < i1; ++i) {
     const __nv_bfloat16* row = G + ((size_t)i * p + j) * T;
     float s = 0.f;
-    for (int t = lane * 8; t < T; t += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(row + t);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(h[q]);
-        s += f.x + f.y;
-      }
-    }
+    for (int t = lane; t < T; t += 32) s += __bfloat162float(row[t]);
     s = warp_sum(s);
     acc = fmaf(__ldg(factors + i), s, acc);
   }
@@ -402,11 +429,11 @@ size_t tc_conv_ws_bytes(const Geom& g, bool norm) {
   return nhwc_bytes(g) + al256((size_t)c.splits * g.p * c.items * 64 * 4) + al256((size_t)bsplits * g.p * 4);
 }
 
-static bool encode_maps(const Geom& g, const void* Xh, const void* G, CUtensorMap* mG, CUtensorMap* mX) {
-  const uint64_t dg[3] = {(uint64_t)g.T, (uint64_t)g.p, (uint64_t)g.B};
-  const uint64_t sg[2] = {(uint64_t)g.T * 2, (uint64_t)g.p * g.T * 2};
-  const uint32_t box[3] = {64, 128, 1};
-  if (!encode_tmap_bf16(mG, G, 3, dg, sg, box)) return false;
+// im2col map over the NHWC copy [B, H, W, Cin]: the bounding box's corners are the
+// padding (lower -pad, upper pad - dil*(k-1)), so its positions are the output pixels'
+// top-left input positions; the element strides are the conv stride; 64 channels
+// (128 bytes, one swizzled row) per pixel and `pixels` pixels per load.
+bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pixels) {
   auto fn = im2col_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)g.Cin, (cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.B};
@@ -414,10 +441,27 @@ static bool encode_maps(const Geom& g, const void* Xh, const void* G, CUtensorMa
   const int lo[2] = {-g.pad, -g.pad};
   const int hi[2] = {g.pad - g.dil * (g.k - 1), g.pad - g.dil * (g.k - 1)};
   const cuuint32_t es[4] = {1, (cuuint32_t)g.stride, (cuuint32_t)g.stride, 1};
-  const CUresult r = fn(mX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(Xh), dims, str, lo, hi, 64, 64,
-                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(Xh), dims, str, lo, hi, 64,
+                        (cuuint32_t)pixels, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+static bool encode_maps(const Geom& g, const void* Xh, const void* G, CUtensorMap* mG, CUtensorMap* mX) {
+  const uint64_t dg[3] = {(uint64_t)g.T, (uint64_t)g.p, (uint64_t)g.B};
+  const uint64_t sg[2] = {(uint64_t)g.T * 2, (uint64_t)g.p * g.T * 2};
+  const uint32_t box[3] = {64, 128, 1};
+  if (!encode_tmap_bf16(mG, G, 3, dg, sg, box)) return false;
+  return encode_im2col_bf16(mX, Xh, g, 64);
+}
+
+cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
+                               cudaStream_t s) {
+  const size_t n = (size_t)p * ncols;
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
+  tcconv::conv_reduce_kernel<<<blocks ? blocks : 1, 256, 0, s>>>(part, splits, p, ncols, kk, dW, accumulate);
+  count_launch();
+  return cudaGetLastError();
 }
 
 template <bool kNorm>
@@ -498,21 +542,29 @@ cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, cons
   P.part = part;
   e = launch_kernel<false>(g, c, mG, mX, P, s);
   if (e != cudaSuccess) return e;
-  const size_t n = (size_t)g.p * c.items * 64;
-  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
-  tcconv::conv_reduce_kernel<<<blocks, 256, 0, s>>>(part, c.splits, g.p, c.items * 64, g.k * g.k, dW, accumulate);
-  count_launch();
-  e = cudaGetLastError();
+  e = launch_conv_reduce(part, c.splits, g.p, c.items * 64, g.k * g.k, dW, accumulate, s);
   if (e != cudaSuccess || !db) return e;
+  return launch_conv_bias_sum(g, G, factors, db, accumulate, part_db, s);
+}
+
+size_t conv_bias_sum_ws_bytes(const Geom& g) { return al256((size_t)std::min(g.B, kBiasSplits) * g.p * 4); }
+
+cudaError_t launch_conv_bias_sum(const Geom& g, const void* G, const float* factors, float* db, int accumulate,
+                                 float* part, cudaStream_t s) {
   const int bsplits = std::min(g.B, kBiasSplits);
   const int beps = cdiv_c(g.B, bsplits);
   dim3 bgrid(cdiv_c(g.p, 8), cdiv_c(g.B, beps));
-  tcconv::conv_bias_sum_kernel<<<bgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T, factors,
-                                                     beps, part_db);
+  if (g.T % 8 == 0) {
+    tcconv::conv_bias_sum_kernel<<<bgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
+                                                       factors, beps, part);
+  } else {
+    tcconv::conv_bias_sum_scalar_kernel<<<bgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
+                                                              factors, beps, part);
+  }
   count_launch();
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_reduce_splits(part_db, (int)bgrid.y, (size_t)g.p, db, accumulate, s);
+  return launch_reduce_splits(part, (int)bgrid.y, (size_t)g.p, db, accumulate, s);
 }
 
 }  // namespace dph

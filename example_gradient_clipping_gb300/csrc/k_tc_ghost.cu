@@ -37,7 +37,27 @@ struct Params {
   unsigned* status;
   int T, d, p, has_bias;
   int B, ept;          // packed mode: examples per CTA (0: one CTA per example)
+  // conv layers: mapA is a TMA im2col map over an NHWC copy of the input, and K
+  // chunk q of the unfolded rows is channel block q / (k*k), filter tap q % (k*k)
+  int conv, Wout, k, stride, pad, dil;
 };
+
+// Load K chunk kk (64 unfolded columns) of the 128 rows that start at row t0 of
+// example e: a tiled box, or for conv layers an im2col block of one filter tap.
+__device__ __forceinline__ void load_a_rows(const Params& P, const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int kk, int t0, int e, bool flat_rows) {
+  if (P.conv) {
+    const int taps = P.k * P.k, cc = kk / taps, tap = kk - cc * taps;
+    const int kh = tap / P.k, kw = tap - kh * P.k;
+    const int ho = t0 / P.Wout, wo = t0 - ho * P.Wout;
+    ptx::tma_load_im2col_4d(map, bar, dst, cc * 64, wo * P.stride - P.pad, ho * P.stride - P.pad, e,
+                            (uint16_t)(kw * P.dil), (uint16_t)(kh * P.dil));
+  } else if (flat_rows) {
+    ptx::tma_load_2d(map, bar, dst, kk * BK, e * P.T + t0);
+  } else {
+    ptx::tma_load_3d(map, bar, dst, kk * BK, t0, e);
+  }
+}
 
 __device__ __forceinline__ void pair_of(int j, int nb, int& tb, int& sb) {
   tb = 0;
@@ -108,10 +128,13 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
             if (!__all_sync(0xffffffffu, w)) { live = false; break; }
             if (ptx::elect_one()) {
               ptx::mbar_arrive_expect_tx(&full[s], TILE);
-              if (packed)
-                ptx::tma_load_2d(map, &full[s], smem + s * STAGE, kk * BK, i * P.ept * P.T);
+              const int e = packed ? i * P.ept : i, t0 = packed ? 0 : (h ? sb : tb) * BT;
+              if (ph == 0)
+                load_a_rows(P, map, &full[s], smem + s * STAGE, kk, t0, e, packed);
+              else if (packed)
+                ptx::tma_load_2d(map, &full[s], smem + s * STAGE, kk * BK, e * P.T);
               else
-                ptx::tma_load_3d(map, &full[s], smem + s * STAGE, kk * BK, (h ? sb : tb) * BT, i);
+                ptx::tma_load_3d(map, &full[s], smem + s * STAGE, kk * BK, t0, e);
             }
             __syncwarp();
             ++issued;
@@ -265,10 +288,70 @@ bool tc_ghost_supported(const Geom& g) {
 
 size_t tc_ghost_ws_bytes(const Geom&) { return 0; }
 
+static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtensorMap& mg, tcghost::Params P,
+                             cudaStream_t s) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(tcghost::tc_ghost_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tcghost::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int grid = P.ept ? (g.B + P.ept - 1) / P.ept : g.B;
+  tcghost::tc_ghost_kernel<<<grid, tcghost::kThreads, tcghost::SMEM, s>>>(ma, mg, P);
+  count_launch();
+  return cudaGetLastError();
+}
+
+static int ghost_ept(const Geom& g) { return 2 * g.T <= tcghost::BT ? tcghost::BT / g.T : 0; }
+
+// Conv layers with Cin % 64 == 0: the A-Gram reads the unfolded rows through TMA im2col
+// loads (128 pixels x 64 channels per filter tap) from an NHWC copy of the input; the
+// G-Gram reads the output gradient in its row layout [B, T, p].  Workspace: the NHWC
+// copy, then the row layout of G.
+bool tc_ghost_conv_supported(const Geom& g) {
+  return g.conv && g.Cin % 64 == 0 && g.p % 8 == 0 && g.T >= 2 && g.T <= 512 && g.stride <= 8 &&
+         g.pad <= 127 && g.dil * (g.k - 1) - g.pad <= 128 && (double)g.B * g.H * g.W * g.Cin < 4e9;
+}
+
+static size_t al256g(size_t n) { return (n + 255) & ~size_t(255); }
+
+size_t tc_ghost_conv_ws_bytes(const Geom& g) {
+  return al256g((size_t)g.B * g.H * g.W * g.Cin * 2) + al256g((size_t)g.B * g.T * g.p * 2);
+}
+
+cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, float* out, void* ws,
+                                 unsigned* status, cudaStream_t s) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* Xh = w;
+  void* Gt = w + al256g((size_t)g.B * g.H * g.W * g.Cin * 2);
+  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
+  if (e != cudaSuccess) return e;
+  e = launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);                        // [p, T] -> [T, p]
+  if (e != cudaSuccess) return e;
+  const int ept = ghost_ept(g);
+  CUtensorMap ma, mg;
+  if (!encode_im2col_bf16(&ma, Xh, g, tcghost::BT)) return cudaErrorInvalidValue;
+  if (ept) {
+    const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)g.B * g.T}, sg[1] = {(uint64_t)g.p * 2};
+    const uint32_t box[2] = {tcghost::BK, tcghost::BT};
+    if (!encode_tmap_bf16(&mg, Gt, 2, dg, sg, box)) return cudaErrorInvalidValue;
+  } else {
+    const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
+    const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
+    const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
+    if (!encode_tmap_bf16(&mg, Gt, 3, dg, sg, box)) return cudaErrorInvalidValue;
+  }
+  tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil};
+  return run_ghost(g, ma, mg, P, s);
+}
+
 cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* /*ws*/,
                             unsigned* status, cudaStream_t s) {
   CUtensorMap ma, mg;
-  const int ept = 2 * g.T <= tcghost::BT ? tcghost::BT / g.T : 0;
+  const int ept = ghost_ept(g);
   if (ept) {   // flattened rows [B*T, width]
     const uint64_t da[2] = {(uint64_t)g.d, (uint64_t)g.B * g.T}, sa[1] = {(uint64_t)g.d * 2};
     const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)g.B * g.T}, sg[1] = {(uint64_t)g.p * 2};
@@ -284,20 +367,8 @@ cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* 
     if (!encode_tmap_bf16(&ma, A, 3, da, sa, box) || !encode_tmap_bf16(&mg, G, 3, dg, sg, box))
       return cudaErrorInvalidValue;
   }
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static bool attr_set[64] = {};
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tcghost::tc_ghost_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, tcghost::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept};
-  const int grid = ept ? (g.B + ept - 1) / ept : g.B;
-  tcghost::tc_ghost_kernel<<<grid, tcghost::kThreads, tcghost::SMEM, s>>>(ma, mg, P);
-  count_launch();
-  return cudaGetLastError();
+  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0};
+  return run_ghost(g, ma, mg, P, s);
 }
 
 }  // namespace dph

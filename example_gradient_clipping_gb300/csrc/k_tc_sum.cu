@@ -8,8 +8,10 @@
 // operands are MN-major in memory (rows of G and A are contiguous along p and d).
 //
 // Per CTA: one 128 x 256 output tile over a contiguous range of rows (split-K).
-//   warp 0     TMA producer: per stage two 64x64 boxes of G and four of A (128B swizzle)
-//   warp 1     MMA issuer: four 128x256x16 tcgen05.mma per stage into TMEM (256 columns)
+//   warps 0, 6 TMA producers (alternate stages): per stage up to two 64x64 boxes of G and
+//              four of A (128B swizzle); boxes wholly past p or D are not loaded
+//   warp 1     MMA issuer: four 128xNx16 tcgen05.mma per stage into TMEM, N the tile's
+//              columns inside D rounded up to 16 (narrow layers issue narrow MMAs)
 //   warps 2-5  scale: multiply each row of the G tile in shared memory by its example's
 //              clip factor (zero outside the CTA's rows) and accumulate the bias sums;
 //              then the epilogue: TMEM -> registers -> fp32 partial tile.
@@ -28,9 +30,8 @@ constexpr int G_TILE = BM * BK * 2;            // 16 KB: two 64-column boxes
 constexpr int A_TILE = BN * BK * 2;            // 32 KB: four 64-column boxes
 constexpr int BOX = 64 * BK * 2;               // 8 KB
 constexpr int STAGE = G_TILE + A_TILE;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int SMEM = STAGES * STAGE + 1024 + 256;
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, BN, 1, 1);
 
 struct Params {
   const float* factors;
@@ -39,7 +40,28 @@ struct Params {
   unsigned* status;
   long R, rows_per_split;
   int T, p, d;
+  // conv layers (Cin % 64 == 0): mapA is a TMA im2col map over an NHWC copy of the
+  // input; unfolded column block q (64 wide) is channel block q / (k*k), tap q % (k*k)
+  int conv, Wout, k, stride, pad, dil;
+  // the G rows already hold bf16(c_i G) (written so by the transpose that made them):
+  // no scaling pass, the MMA takes each stage as it lands; the bias is summed elsewhere
+  int prescaled;
 };
+
+// Column block q of the unfolded rows starting at batch row `row` (64 rows).
+__device__ __forceinline__ void load_a_block(const Params& P, const CUtensorMap* map, uint64_t* bar, void* dst,
+                                             int q, int row) {
+  if (!P.conv) {
+    ptx::tma_load_2d(map, bar, dst, 64 * q, row);
+    return;
+  }
+  const int taps = P.k * P.k, cc = q / taps, tap = q - cc * taps;
+  const int kh = tap / P.k, kw = tap - kh * P.k;
+  const int e = row / P.T, t = row - e * P.T;
+  const int ho = t / P.Wout, wo = t - ho * P.Wout;
+  ptx::tma_load_im2col_4d(map, bar, dst, cc * 64, wo * P.stride - P.pad, ho * P.stride - P.pad, e,
+                          (uint16_t)(kw * P.dil), (uint16_t)(kh * P.dil));
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapA,
@@ -77,44 +99,47 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // TMA producer (whole warp; the elected lane issues)
-    int issued = 0;
-    for (int k = 0; k < nk; ++k) {
+  // boxes inside the layer: G boxes along p, A boxes along D; MMA width N along D
+  const int ng = min(2, (P.p - m0 + 63) / 64), na = min(4, (P.d - n0 + 63) / 64);
+  const int n_mma = min(BN, (P.d - n0 + 15) / 16 * 16);
+  if (warp == 0 || warp == 6) {
+    // TMA producers (whole warp; the elected lane issues); producer pr loads stages k % 2 == pr
+    const int pr = warp == 6 ? 1 : 0;
+    int last = -1;
+    for (int k = pr; k < nk; k += 2) {
       const int s = k % STAGES;
       const bool w = ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
       if (!__all_sync(0xffffffffu, w)) break;
       uint8_t* st = smem + s * STAGE;
       const int row = (int)(r0 + (long)k * BK);
       if (ptx::elect_one()) {
-        ptx::mbar_arrive_expect_tx(&full[s], STAGE);
-        ptx::tma_load_2d(&mapG, &full[s], st, m0, row);
-        ptx::tma_load_2d(&mapG, &full[s], st + BOX, m0 + 64, row);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) ptx::tma_load_2d(&mapA, &full[s], st + G_TILE + j * BOX, n0 + 64 * j, row);
+        ptx::mbar_arrive_expect_tx(&full[s], (uint32_t)(ng + na) * BOX);
+        for (int j = 0; j < ng; ++j) ptx::tma_load_2d(&mapG, &full[s], st + j * BOX, m0 + 64 * j, row);
+        for (int j = 0; j < na; ++j) load_a_block(P, &mapA, &full[s], st + G_TILE + j * BOX, n0 / 64 + j, row);
       }
       __syncwarp();
-      ++issued;
+      last = k;
     }
-    if (*abort && lane == 0) {   // let the copies already in flight land before the CTA exits
-      for (int k = max(0, issued - STAGES); k < issued; ++k)
-        ptx::mbar_wait_drain(&full[k % STAGES], (k / STAGES) & 1);
+    if (*abort && lane == 0) {   // let this producer's copies in flight land before the CTA exits
+      for (int k = max(pr, last - STAGES + 1); k <= last; ++k)
+        if ((k & 1) == pr) ptx::mbar_wait_drain(&full[k % STAGES], (k / STAGES) & 1);
     }
   } else if (warp == 1) {
     // MMA issuer (whole warp; the elected lane issues)
     for (int k = 0; k < nk; ++k) {
       const int s = k % STAGES;
-      const bool w = ptx::mbar_wait(&scaled[s], (k / STAGES) & 1, abort, P.status);
+      const bool w = ptx::mbar_wait(P.prescaled ? &full[s] : &scaled[s], (k / STAGES) & 1, abort, P.status);
       if (!__all_sync(0xffffffffu, w)) break;
       // the scale warps fenced their writes to the async proxy before arriving
       const uint32_t g = ptx::smem_u32(smem + s * STAGE);
       // 16 rows per MMA = two 8-row groups of 1024 B; MN chunks of 64 are 8 KB apart
       const uint64_t da = ptx::sdesc_sw128(g, BOX, 1024);
       const uint64_t db = ptx::sdesc_sw128(g + G_TILE, BOX, 1024);
+      const uint32_t idesc = ptx::idesc_bf16_f32(BM, n_mma, 1, 1);
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          ptx::umma_bf16(tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(db, kk * 2048), kIdesc, (k | kk) != 0);
+          ptx::umma_bf16(tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(db, kk * 2048), idesc, (k | kk) != 0);
         ptx::umma_commit(&empty[s]);
       }
       __syncwarp();
@@ -131,7 +156,7 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
 #pragma unroll
     for (int e = 0; e < 8; ++e) dbacc[e] = 0.f;
     bool ok = true;
-    for (int k = 0; k < nk && ok; ++k) {
+    for (int k = 0; k < nk && ok && !P.prescaled; ++k) {
       const int s = k % STAGES;
       const bool w = ptx::mbar_wait(&full[s], (k / STAGES) & 1, abort, P.status);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -139,6 +164,7 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
       const long rowbase = r0 + (long)k * BK;
 #pragma unroll
       for (int rr = 0; rr < BK / 8; ++rr) {
+        if (box >= ng) break;         // box not loaded (past p): nothing to scale
         const int r = rr * 8 + j;
         const long row = rowbase + r;
         const float c = (row < r1) ? __ldg(P.factors + (int)row / P.T) : 0.f;
@@ -170,7 +196,7 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       dbacc[e] = v;
     }
-    if (ok && P.ws_db && blockIdx.y == 0 && j == 0) {
+    if (ok && P.ws_db && !P.prescaled && blockIdx.y == 0 && j == 0) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int col = m0 + box * 64 + q * 8 + e;
@@ -185,7 +211,7 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
       const int m = m0 + quarter * 32 + lane;
       float* out = P.ws + ((size_t)split * P.p + m) * P.d;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < (n_mma + 31) / 32; ++c) {
         float v[32];
         ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
         ptx::tmem_wait_ld();
@@ -285,6 +311,13 @@ size_t tc_sum_ws_bytes(const Geom& g) {
   return (size_t)tc_sum_splits(g) * ((size_t)g.p * g.D + g.p) * sizeof(float);
 }
 
+// The row-scaled GEMM over maps already built (ma: tiled rows or im2col), partials
+// into ws, then the fixed-order reduction (conv: with the column map back to the
+// weight layout).
+static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtensorMap& ma, const float* factors,
+                              float* dW, float* db, int accumulate, float* ws, unsigned* status, cudaStream_t s,
+                              bool prescaled = false);
+
 cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
                           float* dW, float* db, int accumulate, float* ws, unsigned* status,
                           cudaStream_t s) {
@@ -295,19 +328,81 @@ cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const flo
   const uint32_t box[2] = {64, tcsum::BK};
   if (!encode_tmap_bf16(&mg, G, 2, dg, sg, box) || !encode_tmap_bf16(&ma, A, 2, da, sa, box))
     return cudaErrorInvalidValue;
+  return run_tc_sum(g, mg, ma, factors, dW, db, accumulate, ws, status, s);
+}
+
+cudaError_t launch_tc_sum_prescaled(const Geom& g, const void* A, const void* Gs, float* dW, int accumulate,
+                                    float* ws, unsigned* status, cudaStream_t s) {
+  const long R = (long)g.B * g.T;
+  CUtensorMap mg, ma;
+  const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)R}, sg[1] = {(uint64_t)g.p * 2};
+  const uint64_t da[2] = {(uint64_t)g.D, (uint64_t)R}, sa[1] = {(uint64_t)g.D * 2};
+  const uint32_t box[2] = {64, tcsum::BK};
+  if (!encode_tmap_bf16(&mg, Gs, 2, dg, sg, box) || !encode_tmap_bf16(&ma, A, 2, da, sa, box))
+    return cudaErrorInvalidValue;
+  return run_tc_sum(g, mg, ma, nullptr, dW, nullptr, accumulate, ws, status, s, true);
+}
+
+// Conv layers with Cin % 64 == 0: the unfolded rows come from TMA im2col loads over an
+// NHWC copy of the input, the output gradient from its row layout [B*T, p].  Workspace:
+// the NHWC copy, the row layout of G, then the split partials.
+bool tc_sum_conv_supported(const Geom& g) {
+  return g.conv && g.Cin % 64 == 0 && g.p % 8 == 0 && g.stride <= 8 && g.pad <= 127 &&
+         g.dil * (g.k - 1) - g.pad <= 128 && (double)g.B * g.H * g.W * g.Cin < 4e9 &&
+         (long)g.B * g.T < (1L << 31);
+}
+
+static size_t al256s(size_t n) { return (n + 255) & ~size_t(255); }
+
+size_t tc_sum_conv_ws_bytes(const Geom& g) {
+  return al256s((size_t)g.B * g.H * g.W * g.Cin * 2) + al256s((size_t)g.B * g.T * g.p * 2) +
+         al256s(tc_sum_ws_bytes(g)) + scaled_rows_bias_bytes(g.B, g.T, g.p);
+}
+
+cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  void* Xh = w;
+  void* Gt = w + al256s((size_t)g.B * g.H * g.W * g.Cin * 2);
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(Gt) + al256s((size_t)g.B * g.T * g.p * 2));
+  float* part_db = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part) + al256s(tc_sum_ws_bytes(g)));
+  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
+  if (e != cudaSuccess) return e;
+  e = launch_scaled_rows(g.B, g.T, g.p, G, Gt, factors, db, accumulate, part_db, s);   // bf16(c_i G_i^T), db
+  if (e != cudaSuccess) return e;
+  const long R = (long)g.B * g.T;
+  CUtensorMap mg, ma;
+  const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)R}, sg[1] = {(uint64_t)g.p * 2};
+  const uint32_t box[2] = {64, tcsum::BK};
+  if (!encode_tmap_bf16(&mg, Gt, 2, dg, sg, box) || !encode_im2col_bf16(&ma, Xh, g, tcsum::BK))
+    return cudaErrorInvalidValue;
+  return run_tc_sum(g, mg, ma, nullptr, dW, nullptr, accumulate, part, status, s, true);
+}
+
+static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtensorMap& ma, const float* factors,
+                              float* dW, float* db, int accumulate, float* ws, unsigned* status, cudaStream_t s,
+                              bool prescaled) {
+  const long R = (long)g.B * g.T;
   int splits;
   long rps;
   tc_sum_split(g, &splits, &rps);
   tcsum::Params P;
   P.factors = factors;
   P.ws = ws;
-  P.ws_db = db ? ws + (size_t)splits * g.p * g.D : nullptr;
+  P.ws_db = (db && !prescaled) ? ws + (size_t)splits * g.p * g.D : nullptr;
+  P.prescaled = prescaled ? 1 : 0;
   P.status = status;
   P.R = R;
   P.rows_per_split = rps;
   P.T = g.T;
   P.p = g.p;
   P.d = g.D;
+  P.conv = g.conv;
+  P.Wout = g.Wout;
+  P.k = g.k;
+  P.stride = g.stride;
+  P.pad = g.pad;
+  P.dil = g.dil;
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
@@ -322,9 +417,10 @@ cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const flo
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_reduce_splits(ws, splits, (size_t)g.p * g.D, dW, accumulate, s);
+  e = g.conv ? launch_conv_reduce(ws, splits, g.p, g.D, g.k * g.k, dW, accumulate, s)
+             : launch_reduce_splits(ws, splits, (size_t)g.p * g.D, dW, accumulate, s);
   if (e != cudaSuccess) return e;
-  if (db) e = launch_reduce_splits(P.ws_db, splits, (size_t)g.p, db, accumulate, s);
+  if (P.ws_db) e = launch_reduce_splits(P.ws_db, splits, (size_t)g.p, db, accumulate, s);
   return e;
 }
 

@@ -66,6 +66,8 @@ struct Params {
   int nfull, n16;     // per example: 64-row stages, then 16-row stages
   float* part;        // norm mode: [tiles, B] per-tile partial squared norms
   int norm_bias;      // norm mode: the layer has a bias
+  int gsplit;         // examples split over the grid (no cluster): CTA z writes its partial
+                      // tile to dW + z*p*d (db + z*p), reduced afterwards in z order
 };
 
 // Shared-memory control block after the stages.
@@ -363,6 +365,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     for (int q = 0; q < 8; ++q) {
       const int j = bbox * 64 + bq * 8 + q;
       if (P.splits > 1) partb[j] = bacc[q];   // staged for the cluster reduction
+      else if (P.gsplit && m0 + j < P.p) P.db[(size_t)blockIdx.z * P.p + m0 + j] = bacc[q];
       else if (m0 + j < P.p) P.db[m0 + j] = bacc[q] + (P.accumulate ? P.db[m0 + j] : 0.f);
     }
   }
@@ -374,18 +377,19 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
       *reinterpret_cast<float4*>(part + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
     return;
   }
-  // single split: this CTA owns the tile
+  // this CTA owns the tile (one split), or its grid split's partial of it
   const int m = m0 + row;
   if (m >= P.p) return;
   const int nb = n0 + half * 128;
   const bool vec = (P.d & 3) == 0;
-  float* out = P.dW + (size_t)m * P.d;
+  const int accum = P.gsplit ? 0 : P.accumulate;
+  float* out = P.dW + (P.gsplit ? (size_t)blockIdx.z * P.p * P.d : 0) + (size_t)m * P.d;
 #pragma unroll
   for (int j = 0; j < 128; j += 4) {
     const int n = nb + j;
     if (vec && n + 4 <= P.d) {
       float4 o = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-      if (P.accumulate) {
+      if (accum) {
         const float4 old = *reinterpret_cast<const float4*>(out + n);
         o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
       }
@@ -393,7 +397,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (n + q < P.d) out[n + q] = acc[j + q] + (P.accumulate ? out[n + q] : 0.f);
+        if (n + q < P.d) out[n + q] = acc[j + q] + (accum ? out[n + q] : 0.f);
     }
   }
 }
@@ -601,14 +605,29 @@ static void tc_sumx_split(const Geom& g, int* splits, int* ex_per_split, bool qu
   *splits = cdiv_x(g.B, eps);
 }
 
+// When clusters of <= 4 CTAs per tile cannot give the GPU ~120 CTAs, the examples are
+// split over the grid instead (no cluster): about one CTA per SM, each writing a
+// partial tile to the workspace, summed in split order by a second kernel.
+static int tc_sumx_grid_splits(const Geom& g) {
+  const long tiles = (long)cdiv_x(g.p, tcsumx::BM) * cdiv_x(g.D, tcsumx::BN);
+  if (tiles * kMaxCluster >= 120) return 0;
+  const long s = std::min<long>(g.B, 152 / tiles);
+  if (s <= kMaxCluster) return 0;
+  const int eps = cdiv_x(g.B, s);
+  return cdiv_x(g.B, eps);
+}
+
 bool tc_sumx_supported(const Geom& g) {
   return !g.conv && (g.p % 8 == 0) && (g.D % 8 == 0) && g.p >= 8 && g.D >= 8 && g.T >= 64;
 }
 
-size_t tc_sumx_ws_bytes(const Geom&) { return 0; }
+size_t tc_sumx_ws_bytes(const Geom& g) {
+  const int gs = tc_sumx_grid_splits(g);
+  return gs ? (size_t)gs * ((size_t)g.p * g.D + g.p) * sizeof(float) : 0;
+}
 
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                           float* db, int accumulate, void* /*ws*/, unsigned* status, cudaStream_t s) {
+                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s) {
   CUtensorMap mg64, ma64, mg16, ma16;
   const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
   const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
@@ -619,11 +638,20 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
       !encode_tmap_bf16(&mg16, G, 3, dg, sg, box16) || !encode_tmap_bf16(&ma16, A, 3, da, sa, box16))
     return cudaErrorInvalidValue;
   int splits, eps;
-  tc_sumx_split(g, &splits, &eps, true);
-  tcsumx::Params P;
+  const int gsplits = tc_sumx_grid_splits(g);
+  if (gsplits && !ws) return cudaErrorInvalidValue;
+  if (gsplits) {
+    eps = cdiv_x(g.B, gsplits);
+    splits = 1;
+  } else {
+    tc_sumx_split(g, &splits, &eps, true);
+  }
+  float* part_w = static_cast<float*>(ws);
+  float* part_b = (gsplits && db) ? part_w + (size_t)gsplits * g.p * g.D : nullptr;
+  tcsumx::Params P = {};
   P.factors = factors;
-  P.dW = dW;
-  P.db = db;
+  P.dW = gsplits ? part_w : dW;
+  P.db = gsplits ? part_b : db;
   P.status = status;
   P.B = g.B;
   P.T = g.T;
@@ -632,6 +660,7 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   P.ex_per_split = eps;
   P.splits = splits;
   P.accumulate = accumulate;
+  P.gsplit = gsplits ? 1 : 0;
   int nfull = g.T / 64, rem = g.T - 64 * nfull;
   int n16 = (rem + 15) / 16;
   if (n16 > 3) { nfull += 1; n16 = 0; }
@@ -647,7 +676,7 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
     attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cdiv_x(g.p, tcsumx::BM), cdiv_x(g.D, tcsumx::BN), splits);
+  cfg.gridDim = dim3(cdiv_x(g.p, tcsumx::BM), cdiv_x(g.D, tcsumx::BN), gsplits ? gsplits : splits);
   cfg.blockDim = dim3(tcsumx::kThreads);
   cfg.dynamicSmemBytes = tcsumx::SMEM;
   cfg.stream = s;
@@ -660,7 +689,10 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   cfg.numAttrs = splits > 1 ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false>, mg64, ma64, mg16, ma16, P);
   count_launch();
-  return e;
+  if (e != cudaSuccess || !gsplits) return e;
+  e = launch_reduce_splits(part_w, gsplits, (size_t)g.p * g.D, dW, accumulate, s);
+  if (e != cudaSuccess || !db) return e;
+  return launch_reduce_splits(part_b, gsplits, (size_t)g.p, db, accumulate, s);
 }
 
 // Instantiated norm on the tensor cores: per-tile partials [tiles, B] in the workspace,

@@ -87,23 +87,26 @@ __global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restri
   }
 }
 
-// Per example [p, T] -> [T, p] in 64 x 64 tiles with 16-byte loads and stores
-// (T % 8 == 0 and p % 8 == 0).  Shared tile [j][t] in 8-element chunks, chunk
-// index XORed with (j / 8) % 8 so that both the row stores and the column gathers
-// spread over the banks.
+// Per example [p, T] -> [T, p] with 16-byte loads and stores (T % 8 == 0, p % 8 == 0),
+// through a tile of 64 rows j by tt <= 64 pixels t (tt = T rounded up to 8 when T < 64).
+// Shared tile [j][t] in 8-element chunks, chunk index XORed with (j / 8) % 8 so that both
+// the row stores and the column gathers spread over the banks.  With `scale`, every
+// value of example i is multiplied by scale[i] in fp32 and rounded to bf16 once.
 constexpr int kTT = 64;
-__global__ void transpose_rows_vec_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
-                                          __nv_bfloat16* __restrict__ Gt) {
+__global__ void transpose_rows_vec_kernel(int B, int T, int p, int tt, const __nv_bfloat16* __restrict__ G,
+                                          __nv_bfloat16* __restrict__ Gt, const float* __restrict__ scale,
+                                          float* __restrict__ bias_part) {
   __shared__ __align__(16) __nv_bfloat16 s[kTT][kTT];
-  const int tt = (T + kTT - 1) / kTT, tp = (p + kTT - 1) / kTT;
-  const long units = (long)B * tt * tp;
+  const int nt = (T + tt - 1) / tt, tp = (p + kTT - 1) / kTT;
+  const int tch = tt / 8;                                 // t chunks per tile row
+  const long units = (long)B * nt * tp;
   for (long u = blockIdx.x; u < units; u += gridDim.x) {
-    const int i = (int)(u / ((long)tt * tp));
-    const int rem = (int)(u - (long)i * tt * tp);
-    const int t0 = (rem / tp) * kTT, j0 = (rem % tp) * kTT;
+    const int i = (int)(u / ((long)nt * tp));
+    const int rem = (int)(u - (long)i * nt * tp);
+    const int t0 = (rem / tp) * tt, j0 = (rem % tp) * kTT;
     const __nv_bfloat16* gi = G + (size_t)i * T * p;
-    for (int q = threadIdx.x; q < kTT * (kTT / 8); q += blockDim.x) {
-      const int jr = q >> 3, tc = q & 7;                 // tile row (output j), t chunk
+    for (int q = threadIdx.x; q < kTT * tch; q += blockDim.x) {
+      const int jr = q / tch, tc = q - jr * tch;          // tile row (output j), t chunk
       const int j = j0 + jr, t = t0 + tc * 8;
       if (j < p && t < T)
         *reinterpret_cast<uint4*>(&s[jr][(tc ^ ((jr >> 3) & 7)) * 8]) =
@@ -111,18 +114,63 @@ __global__ void transpose_rows_vec_kernel(int B, int T, int p, const __nv_bfloat
     }
     __syncthreads();
     __nv_bfloat16* go = Gt + (size_t)i * T * p;
-    for (int q = threadIdx.x; q < kTT * (kTT / 8); q += blockDim.x) {
+    const float sc = scale ? __ldg(scale + i) : 1.f;
+    for (int q = threadIdx.x; q < tt * (kTT / 8); q += blockDim.x) {
       const int tr = q >> 3, jc = q & 7;                 // tile t, j chunk
       const int t = t0 + tr, j = j0 + jc * 8;
       if (t < T && j < p) {
         __align__(16) __nv_bfloat16 v[8];
         const int col = ((tr >> 3) ^ jc) * 8 + (tr & 7);
 #pragma unroll
-        for (int r = 0; r < 8; ++r) v[r] = s[jc * 8 + r][col];
+        for (int r = 0; r < 8; ++r)
+          v[r] = scale ? __float2bfloat16_rn(sc * __bfloat162float(s[jc * 8 + r][col])) : s[jc * 8 + r][col];
         *reinterpret_cast<uint4*>(go + (size_t)t * p + j) = *reinterpret_cast<const uint4*>(v);
       }
     }
+    if (bias_part && threadIdx.x < kTT) {
+      // bias partial of this (example, pixel tile): scale[i] * sum_t G[i, j, t] in fp32
+      const int jr = threadIdx.x, j = j0 + jr;
+      if (j < p) {
+        float acc = 0.f;
+        for (int tc = 0; tc < tch && t0 + tc * 8 < T; ++tc) {
+          const __nv_bfloat16* c8 = &s[jr][(tc ^ ((jr >> 3) & 7)) * 8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) acc += __bfloat162float(c8[r]);
+        }
+        bias_part[((size_t)i * nt + rem / tp) * p + j] = sc * acc;
+      }
+    }
     __syncthreads();
+  }
+}
+
+// Rows with T % 8 != 0 (p % 8 == 0): one thread per (example, 8 outputs j0 .. j0+7),
+// over all T pixels: gathers eight rows of G_i per pixel, one 16-byte store each.
+__global__ void transpose_rows_short_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
+                                            __nv_bfloat16* __restrict__ Gt, const float* __restrict__ scale,
+                                            float* __restrict__ bias_part) {
+  const int cp = p >> 3;
+  const size_t n = (size_t)B * cp;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t i = q / cp;
+    const int j0 = (int)(q - i * cp) * 8;
+    const __nv_bfloat16* src = G + (i * p + j0) * T;
+    const float sc = scale ? __ldg(scale + i) : 1.f;
+    float bsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int t = 0; t < T; ++t) {
+      __align__(16) __nv_bfloat16 v[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const __nv_bfloat16 x = src[(size_t)r * T + t];
+        bsum[r] += __bfloat162float(x);
+        v[r] = scale ? __float2bfloat16_rn(sc * __bfloat162float(x)) : x;
+      }
+      *reinterpret_cast<uint4*>(Gt + (i * T + t) * p + j0) = *reinterpret_cast<const uint4*>(v);
+    }
+    if (bias_part) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) bias_part[i * p + j0 + r] = sc * bsum[r];
+    }
   }
 }
 
@@ -166,7 +214,8 @@ using namespace dpk;
 
 int conv_rows_width(const Geom& g) { return (g.D + 7) / 8 * 8; }
 
-cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s) {
+cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s,
+                             const float* scale, float* db, int accumulate, float* bias_part) {
   const int Dp = conv_rows_width(g);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   auto* Ub = static_cast<__nv_bfloat16*>(U);
@@ -193,22 +242,49 @@ cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* 
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (scale) return launch_scaled_rows(g.B, g.T, g.p, G, Gt, scale, db, accumulate, bias_part, s);
   return launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);
 }
 
-cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s) {
+int transpose_bias_parts(int B, int T) {
+  if (T % 8 == 0) {
+    const int tt = std::min(kTT, T);
+    return B * ((T + tt - 1) / tt);
+  }
+  return B;
+}
+
+cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s,
+                                  const float* scale, float* bias_part) {
   const auto* Gb = static_cast<const __nv_bfloat16*>(src);
   auto* Gtb = static_cast<__nv_bfloat16*>(dst);
   if (T % 8 == 0 && p % 8 == 0) {
-    const long units = (long)B * ((T + kTT - 1) / kTT) * ((p + kTT - 1) / kTT);
+    const int tt = std::min(kTT, T);
+    const long units = (long)B * ((T + tt - 1) / tt) * ((p + kTT - 1) / kTT);
     const unsigned blocks = (unsigned)std::min<long>(units, 152L * 16);
-    transpose_rows_vec_kernel<<<blocks, 256, 0, s>>>(B, T, p, Gb, Gtb);
+    transpose_rows_vec_kernel<<<blocks, 256, 0, s>>>(B, T, p, tt, Gb, Gtb, scale, bias_part);
+  } else if (p % 8 == 0) {
+    const size_t n = (size_t)B * (p / 8);
+    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 16);
+    transpose_rows_short_kernel<<<blocks ? blocks : 1, 256, 0, s>>>(B, T, p, Gb, Gtb, scale, bias_part);
   } else {
+    if (scale || bias_part) return cudaErrorInvalidValue;   // scaled copies need p % 8 == 0
     dim3 grid((T + 31) / 32, (p + 31) / 32, std::min(B, 65535));
     transpose_rows_kernel<<<grid, dim3(32, 8), 0, s>>>(B, T, p, Gb, Gtb);
   }
   count_launch();
   return cudaGetLastError();
+}
+
+cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
+                               int accumulate, float* bias_part, cudaStream_t s) {
+  cudaError_t e = launch_transpose_rows(B, T, p, G, Gt, s, factors, db ? bias_part : nullptr);
+  if (e != cudaSuccess || !db) return e;
+  return launch_reduce_splits(bias_part, transpose_bias_parts(B, T), (size_t)p, db, accumulate, s);
+}
+
+size_t scaled_rows_bias_bytes(int B, int T, int p) {
+  return ((size_t)transpose_bias_parts(B, T) * p * 4 + 255) & ~size_t(255);
 }
 
 cudaError_t launch_compact_cols(const float* Wp, int p, int D, int Dp, float* dW, int accumulate, cudaStream_t s) {

@@ -12,6 +12,9 @@ size_t tc_sum_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
                           float* dW, float* db, int accumulate, float* ws, unsigned* status,
                           cudaStream_t s);
+// The same GEMM over rows whose G part already holds bf16(c_i G) (no bias).
+cudaError_t launch_tc_sum_prescaled(const Geom& g, const void* A, const void* Gs, float* dW, int accumulate,
+                                    float* ws, unsigned* status, cudaStream_t s);
 // Clipped sum with per-example TMEM accumulation and fp32 scaling (rows per example >= 64).
 bool tc_sumx_supported(const Geom& g);
 size_t tc_sumx_ws_bytes(const Geom& g);
@@ -31,9 +34,24 @@ cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* 
 // output gradient transposed per example, Gt [B, T, p].
 // U has conv_rows_width(g) = D rounded up to 8 columns (the extra ones zero).
 int conv_rows_width(const Geom& g);
-cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s);
+// With `scale`, Gt holds bf16(scale[i] * G) (the clip factors applied once, for the
+// row-scaled clipped sum) and db (if given) receives the bias sum (see launch_scaled_rows).
+cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s,
+                             const float* scale = nullptr, float* db = nullptr, int accumulate = 0,
+                             float* bias_part = nullptr);
 // Per example [p, T] -> [T, p] (bf16): the output gradient's row layout, and NCHW -> NHWC.
-cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s);
+cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s,
+                                  const float* scale = nullptr, float* bias_part = nullptr);
+// Gt = bf16(c_i G_i^T) for the row-scaled clipped sum, and db (+)= sum_i c_i sum_t G[i, :, t]
+// from fp32 partial sums taken on the way (bias_part: scaled_rows_bias_bytes).
+cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
+                               int accumulate, float* bias_part, cudaStream_t s);
+size_t scaled_rows_bias_bytes(int B, int T, int p);
+// db (+)= sum_i c_i sum_t G[i, j, t] from the NCHW output gradient (fp32, fixed order);
+// part holds min(B, 64) * p floats.
+cudaError_t launch_conv_bias_sum(const Geom& g, const void* G, const float* factors, float* db, int accumulate,
+                                 float* part, cudaStream_t s);
+size_t conv_bias_sum_ws_bytes(const Geom& g);
 // Conv layers with the unfold done by TMA im2col loads (Cin % 64 == 0, T % 8 == 0, T >= 64):
 // instantiated norm and clipped sum; the workspace holds an NHWC copy of the input.
 bool tc_conv_supported(const Geom& g);
@@ -42,6 +60,22 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
                                 unsigned* status, cudaStream_t s);
 cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
                                float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
+// im2col map (bf16, 128-byte swizzle, 64 channels per pixel) over an NHWC copy of a conv input.
+bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pixels);
+// dW[j, m] (+)= sum over splits of part[s, j, col(m)], col mapping the weight column
+// m = c*kk + tap to the im2col tile column (c/64 * kk + tap) * 64 + c % 64.
+cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
+                               cudaStream_t s);
+// Row-scaled clipped sum of a conv layer (Cin % 64 == 0) with im2col loads for the input.
+bool tc_sum_conv_supported(const Geom& g);
+size_t tc_sum_conv_ws_bytes(const Geom& g);
+cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
+// Ghost norm of a conv layer (Cin % 64 == 0) with im2col loads for the input Gram.
+bool tc_ghost_conv_supported(const Geom& g);
+size_t tc_ghost_conv_ws_bytes(const Geom& g);
+cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, float* out, void* ws,
+                                 unsigned* status, cudaStream_t s);
 // dW[j, m] (+)= Wp[j, m] for j < p, m < D (Wp rows of Dp floats).
 cudaError_t launch_compact_cols(const float* Wp, int p, int D, int Dp, float* dW, int accumulate, cudaStream_t s);
 // 2D/3D bf16 tensor map with 128-byte swizzle (dims innermost first, strides in bytes).

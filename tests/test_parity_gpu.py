@@ -231,14 +231,19 @@ ACC = [(LayerSpec("e", "linear", p=42, d=72, T=9), 6),          # SIMT (p not a 
        (LayerSpec("e", "linear", p=128, d=64, T=40), 5),         # row-scaled tensor-core GEMM
        (LayerSpec("e", "linear", p=128, d=128, T=64), 4),        # per-example, several splits
        (LayerSpec("e", "linear", p=64, d=256, T=80), 1),         # per-example, one split
-       (LayerSpec("e", "conv2d", p=16, Cin=3, H=8, W=8, k=3, pad=1), 3)]   # conv, padded columns
+       (LayerSpec("e", "conv2d", p=16, Cin=3, H=8, W=8, k=3, pad=1), 3),   # conv, padded columns
+       (LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=3, pad=1), 3),  # conv, im2col row-scaled
+       (LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 2),  # conv, im2col per example
+       (LayerSpec("e", "linear", p=10, d=13, T=1), 300),                   # one row, 3 example splits
+       (LayerSpec("e", "linear", p=136, d=264, T=70), 11)]                 # per-example, grid splits
 
 
-ACC_PIN = ["", "rows", "example", "example", ""]
+ACC_PIN = ["", "rows", "example", "example", "", "", "", "", "example"]
 
 
 @pytest.mark.parametrize("spec,B,pin", [(s, b, p) for (s, b), p in zip(ACC, ACC_PIN)],
-                         ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single", "conv_padded"])
+                         ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single", "conv_padded",
+                              "conv_im2col_rows", "conv_im2col_example", "t1_splits", "tc_ex_grid"])
 def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
     if pin:
         monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
