@@ -33,6 +33,8 @@ constexpr int STAGE = 6 * BOX;               // G [128 outputs x 64 pixels], the
 constexpr int kThreads = 384;
 constexpr int kEpiFirst = 4, kEpiWarps = 8;
 constexpr int SMEM = STAGES * STAGE + 1024 + 512;
+constexpr int PSTR = BN + 4;                 // staged output row stride (floats)
+static_assert(BM * PSTR * 4 <= STAGES * STAGE, "staging fits in the stage buffers");
 // A = G (K-major: pixels contiguous), B = im2col blocks (MN-major: channels contiguous)
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, BN, 0, 1);
 
@@ -133,8 +135,8 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
 // Warps 4-11.  Every epilogue warp walks all of the CTA's examples (also after an
 // abort) so the per-example barrier of the norm mode is always complete.
 template <bool kNorm>
-__device__ __forceinline__ void epilogue(const Params& P, Ctl* c, uint32_t tmem, int e0, int e1, int m0,
-                                         int q0, int nitems) {
+__device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0, int e1,
+                                         int m0, int q0, int nitems) {
   volatile int* abort = &c->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, half = (warp - kEpiFirst) >> 2;
@@ -197,13 +199,26 @@ __device__ __forceinline__ void epilogue(const Params& P, Ctl* c, uint32_t tmem,
     }
   }
   if constexpr (!kNorm) {
-    const int m = m0 + quarter * 32 + lane;
-    if (!ok || *abort || m >= P.p) return;
-    float* out = P.part + ((size_t)blockIdx.z * P.p + m) * P.ncols + (size_t)(q0 + 2 * half) * 64;
+    // stage the partial tile in shared memory (the stage buffers are idle once the last
+    // MMA completed), then write whole rows so the stores coalesce; every epilogue warp
+    // passes the barrier
+    const int row = quarter * 32 + lane;
+    float* stg = reinterpret_cast<float*>(smem);
+    if (ok) {
 #pragma unroll
-    for (int j = 0; j < 128; j += 4) {
-      if (j < 64 ? v0 : v1)
-        *reinterpret_cast<float4*>(out + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+      for (int j = 0; j < 128; j += 4)
+        *reinterpret_cast<float4*>(stg + row * PSTR + half * 128 + j) =
+            make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+    }
+    asm volatile("bar.sync 2, %0;" ::"r"(32 * kEpiWarps) : "memory");
+    if (*abort) return;
+    const int nc4 = nitems * 16;                      // float4s per row of this tile
+    for (int item = threadIdx.x - 32 * kEpiFirst; item < BM * nc4; item += 32 * kEpiWarps) {
+      const int r = item / nc4, c4 = item - r * nc4;
+      const int m = m0 + r;
+      if (m >= P.p) continue;
+      *reinterpret_cast<float4*>(P.part + ((size_t)blockIdx.z * P.p + m) * P.ncols + (size_t)q0 * 64 + c4 * 4) =
+          *reinterpret_cast<const float4*>(stg + r * PSTR + c4 * 4);
     }
   }
 }
@@ -257,7 +272,7 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
 
   if (warp >= kEpiFirst) {
     ptx::regs_inc<216>();
-    epilogue<kNorm>(P, c, tmem, e0, e1, m0, q0, nitems);
+    epilogue<kNorm>(P, smem, c, tmem, e0, e1, m0, q0, nitems);
     finish(c, tmem);
   } else {
     ptx::regs_dec<64>();

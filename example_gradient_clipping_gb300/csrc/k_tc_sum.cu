@@ -31,6 +31,8 @@ constexpr int A_TILE = BN * BK * 2;            // 32 KB: four 64-column boxes
 constexpr int BOX = 64 * BK * 2;               // 8 KB
 constexpr int STAGE = G_TILE + A_TILE;
 constexpr int kThreads = 224;
+constexpr int PSTR = BN + 4;                   // staged output row stride (floats)
+static_assert(BM * PSTR * 4 <= STAGES * (BM * BK * 2 + BN * BK * 2), "staging fits in the stage buffers");
 constexpr int SMEM = STAGES * STAGE + 1024 + 256;
 
 struct Params {
@@ -203,29 +205,43 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
         if (col < P.p) P.ws_db[(size_t)split * P.p + col] = dbacc[e];
       }
     }
-    // ---- epilogue: each thread owns one accumulator row (TMEM lane) ----
+    // ---- epilogue: each thread drains one accumulator row (TMEM lane) into a shared
+    // staging tile (the stage buffers are idle once the last MMA completed), then the
+    // four warps write whole rows, so the stores coalesce.  All four warps pass the
+    // barrier, also after an abort.
     const bool w = ok && ptx::mbar_wait(accum, 0, abort, P.status);
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    float* stg = reinterpret_cast<float*>(smem);
     if (__all_sync(0xffffffffu, w)) {
       ptx::tc_fence_after();
-      const int quarter = warp & 3;
-      const int m = m0 + quarter * 32 + lane;
-      float* out = P.ws + ((size_t)split * P.p + m) * P.d;
 #pragma unroll 1
       for (int c = 0; c < (n_mma + 31) / 32; ++c) {
         float v[32];
         ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
         ptx::tmem_wait_ld();
-        const int n = n0 + c * 32;
-        if (m < P.p) {
-          if (n + 32 <= P.d && (P.d & 3) == 0) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(out + n + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-          } else {
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(stg + row * PSTR + c * 32 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+    if (!*abort) {
+      const int t = threadIdx.x - 64, nc4 = (n_mma + 3) / 4;
+      const bool vec = (P.d & 3) == 0;
+      for (int item = t; item < BM * nc4; item += 128) {
+        const int r = item / nc4, c4 = item - r * nc4;
+        const int m = m0 + r, n = n0 + c4 * 4;
+        if (m >= P.p) continue;
+        const float4 o = *reinterpret_cast<const float4*>(stg + r * PSTR + c4 * 4);
+        float* out = P.ws + ((size_t)split * P.p + m) * P.d + n;
+        if (vec && n + 4 <= P.d) {
+          *reinterpret_cast<float4*>(out) = o;
+        } else {
+          const float ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (n + e < P.d) out[n + e] = v[e];
-          }
+          for (int q = 0; q < 4; ++q)
+            if (n + q < P.d) out[q] = ov[q];
         }
       }
     }

@@ -324,16 +324,15 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     const float cf = __ldg(P.factors + e);
     const uint32_t base = tmem + b * 256 + half * 128 + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
-    for (int ch = 0; ch < 8; ch += 2) {
-      float v0[16], v1[16];
-      ptx::tmem_ld16(base + ch * 16, v0);          // two loads in flight per wait
-      ptx::tmem_ld16(base + ch * 16 + 16, v1);
+    for (int ch = 0; ch < 8; ch += 4) {
+      float v[4][16];                              // four loads in flight per wait
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ptx::tmem_ld16(base + (ch + u) * 16, v[u]);
       ptx::tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        acc[ch * 16 + j] = fmaf(cf, v0[j], acc[ch * 16 + j]);
-        acc[ch * 16 + 16 + j] = fmaf(cf, v1[j], acc[ch * 16 + 16 + j]);
-      }
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[(ch + u) * 16 + j] = fmaf(cf, v[u][j], acc[(ch + u) * 16 + j]);
     }
     ptx::tc_fence_before();
     __syncwarp();
@@ -369,35 +368,41 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
       else if (m0 + j < P.p) P.db[m0 + j] = bacc[q] + (P.accumulate ? P.db[m0 + j] : 0.f);
     }
   }
+  // stage the tile in shared memory (the stage buffers are idle: every load was consumed
+  // and every MMA completed before the last accum wait)
   const int row = quarter * 32 + lane;
-  if (P.splits > 1) {            // stage the partial tile for the cluster reduction
+  {
     float* part = reinterpret_cast<float*>(smem) + row * PSTR + half * 128;
 #pragma unroll
     for (int j = 0; j < 128; j += 4)
       *reinterpret_cast<float4*>(part + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-    return;
   }
-  // this CTA owns the tile (one split), or its grid split's partial of it
-  const int m = m0 + row;
-  if (m >= P.p) return;
-  const int nb = n0 + half * 128;
+  if (P.splits > 1) return;      // the cluster reduction reads the staged partials
+  // this CTA owns the tile (one split), or its grid split's partial of it: whole rows
+  // from shared memory, 64 threads per 1 KB row, so the stores coalesce
+  asm volatile("bar.sync 2, %0;" ::"r"(32 * kEpiWarps) : "memory");
+  const int et2 = threadIdx.x - 32 * kEpiFirst;
   const bool vec = (P.d & 3) == 0;
   const int accum = P.gsplit ? 0 : P.accumulate;
-  float* out = P.dW + (P.gsplit ? (size_t)blockIdx.z * P.p * P.d : 0) + (size_t)m * P.d;
-#pragma unroll
-  for (int j = 0; j < 128; j += 4) {
-    const int n = nb + j;
+  float* base_out = P.dW + (P.gsplit ? (size_t)blockIdx.z * P.p * P.d : 0);
+  const float* stg = reinterpret_cast<const float*>(smem);
+  for (int item = et2; item < BM * (BN / 4); item += 32 * kEpiWarps) {
+    const int r = item / (BN / 4), c4 = item % (BN / 4);
+    const int m = m0 + r, n = n0 + c4 * 4;
+    if (m >= P.p) continue;
+    float4 o = *reinterpret_cast<const float4*>(stg + r * PSTR + c4 * 4);
+    float* out = base_out + (size_t)m * P.d + n;
     if (vec && n + 4 <= P.d) {
-      float4 o = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
       if (accum) {
-        const float4 old = *reinterpret_cast<const float4*>(out + n);
+        const float4 old = *reinterpret_cast<const float4*>(out);
         o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
       }
-      *reinterpret_cast<float4*>(out + n) = o;
+      *reinterpret_cast<float4*>(out) = o;
     } else {
+      const float ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (n + q < P.d) out[n + q] = acc[j + q] + (accum ? out[n + q] : 0.f);
+        if (n + q < P.d) out[q] = ov[q] + (accum ? out[q] : 0.f);
     }
   }
 }
