@@ -47,6 +47,14 @@ __device__ __forceinline__ float ld_a(const E* __restrict__ A, const Geom& g, in
   return to_f(A[(((size_t)i * g.Cin + c) * g.H + h) * g.W + w]);
 }
 
+// Programmatic dependent launch: every library kernel is launched with programmatic
+// stream serialization, lets the next kernel in the stream start launching once all of
+// its CTAs are running (pdl_trigger), and waits for the previous kernel in the stream to
+// complete, with its memory visible, before its first global-memory access (pdl_wait).
+// Kernels that do not use these (another library's) keep ordinary stream order.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -108,6 +116,38 @@ namespace dph {
 using dpk::Geom;
 // Counts kernels the library launched (reported by dp_launch_count).
 void count_launch(unsigned n = 1);
+
+// Launch with programmatic stream serialization (see pdl_wait); counts the launch.
+// `pdl` false gives ordinary stream order (the kernel's pdl_wait is then a no-op): the
+// conv layout and im2col kernels, where overlapping launches measured slower.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+  count_launch();
+  return e;
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  return launch_k(true, kernel, grid, block, smem, s, static_cast<Args&&>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                         Args&&... args) {
+  return launch_k(false, kernel, grid, block, smem, s, static_cast<Args&&>(args)...);
+}
+// Counts kernels the library launched (reported by dp_launch_count).
 // Descriptor validation and the thread-local error message, shared by entry points.
 dp_status geom_from_desc(const dp_layer_desc* d, Geom* g);
 dp_status set_error(dp_status st, const char* msg);

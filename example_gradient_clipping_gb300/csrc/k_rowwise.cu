@@ -34,6 +34,8 @@ template <class E>
 __global__ void __launch_bounds__(256) t1_norm_kernel(Geom g, const E* __restrict__ A,
                                                       const E* __restrict__ G, float* __restrict__ out,
                                                       bool vec_a, bool vec_g) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < g.B; i += warps) {
@@ -52,6 +54,8 @@ template <class E>
 __global__ void __launch_bounds__(256) t1_sum_kernel(Geom g, const E* __restrict__ A, const E* __restrict__ G,
                                                      const float* __restrict__ factors, int ex_per_split,
                                                      float* __restrict__ part_w, float* __restrict__ part_b) {
+  pdl_trigger();
+  pdl_wait();
   const int mq = (g.d + 3) / 4;                      // m quads per row
   const long n_th = (long)g.p * mq;
   const int i0 = blockIdx.y * ex_per_split, i1 = min(g.B, i0 + ex_per_split);
@@ -82,6 +86,8 @@ struct Bounds { float C[64]; };
 __global__ void clip_factors_kernel(const float* __restrict__ sq, int B, int L, int per_layer,
                                     Bounds bounds, const float* __restrict__ Cdev,
                                     float* __restrict__ out, unsigned* status) {
+  pdl_trigger();
+  pdl_wait();
   const int n_out = per_layer ? B * L : B;
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < n_out; e += gridDim.x * blockDim.x) {
     float s, C;
@@ -113,6 +119,8 @@ __global__ void clip_factors_kernel(const float* __restrict__ sq, int B, int L, 
 __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad, size_t n, float sc,
                                                         float invB, uint64_t seed, uint64_t offset,
                                                         const unsigned long long* __restrict__ seed_dev) {
+  pdl_trigger();
+  pdl_wait();
   if (seed_dev) seed = *seed_dev;
   const uint64_t q0 = offset >> 2;
   const uint64_t q1 = (offset + n + 3) >> 2;  // one past the last block touched
@@ -146,6 +154,8 @@ __global__ void __launch_bounds__(256) adaptive_bound_kernel(const float* __rest
                                                              float C_l2, float alpha, float beta,
                                                              float sigma_l2, uint64_t seed, int layer,
                                                              float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ double part[8];
   double acc = 0.0;
   for (int i = threadIdx.x; i < B; i += blockDim.x) {
@@ -180,11 +190,10 @@ cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* 
   const bool va = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((g.d * es) % 16 == 0);
   const bool vg = ((reinterpret_cast<uintptr_t>(G) & 15u) == 0) && ((g.p * es) % 16 == 0);
   if (dtype == DP_FP32)
-    t1_norm_kernel<float><<<blocks, 256, 0, s>>>(g, (const float*)A, (const float*)G, out, va, vg);
+    launch_pdl(t1_norm_kernel<float>, blocks, 256, 0, s, g, (const float*)A, (const float*)G, out, va, vg);
   else
-    t1_norm_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(g, (const __nv_bfloat16*)A,
+    launch_pdl(t1_norm_kernel<__nv_bfloat16>, blocks, 256, 0, s, g, (const __nv_bfloat16*)A,
                                                          (const __nv_bfloat16*)G, out, va, vg);
-  count_launch();
   return cudaGetLastError();
 }
 
@@ -196,9 +205,8 @@ cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, co
   // more than 64 per-layer bounds are rejected by the caller
   const int n_out = per_layer ? B * L : B;
   const int blocks = (n_out + 255) / 256;
-  clip_factors_kernel<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(sq, B, L, per_layer, b, nullptr, out,
+  launch_pdl(clip_factors_kernel, blocks > 0 ? blocks : 1, 256, 0, s, sq, B, L, per_layer, b, nullptr, out,
                                                               status);
-  count_launch();
   return cudaGetLastError();
 }
 
@@ -209,16 +217,14 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
   const uint64_t cap = 152ull * 8ull;   // grid-stride beyond 8 resident blocks per SM
   if (grid > cap) grid = cap;
   if (grid == 0) grid = 1;
-  add_noise_kernel<<<(unsigned)grid, 256, 0, s>>>(grad, n, sc, invB, seed, offset, seed_dev);
-  count_launch();
+  launch_pdl(add_noise_kernel, (unsigned)grid, 256, 0, s, grad, n, sc, invB, seed, offset, seed_dev);
   return cudaGetLastError();
 }
 
 cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
                                   float sigma_l2, uint64_t seed, int layer, float* out,
                                   cudaStream_t s) {
-  adaptive_bound_kernel<<<1, 256, 0, s>>>(sq, B, C_l2, alpha, beta, sigma_l2, seed, layer, out);
-  count_launch();
+  launch_pdl(adaptive_bound_kernel, 1, 256, 0, s, sq, B, C_l2, alpha, beta, sigma_l2, seed, layer, out);
   return cudaGetLastError();
 }
 
@@ -237,11 +243,10 @@ cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G
   const long n_th = (long)g.p * ((g.d + 3) / 4);
   dim3 grid((unsigned)std::min<long>((n_th + 255) / 256, 152L * 8), (unsigned)splits);
   if (dtype == DP_FP32)
-    t1_sum_kernel<float><<<grid, 256, 0, s>>>(g, (const float*)A, (const float*)G, factors, eps, part_w, part_b);
+    launch_pdl(t1_sum_kernel<float>, grid, 256, 0, s, g, (const float*)A, (const float*)G, factors, eps, part_w, part_b);
   else
-    t1_sum_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(g, (const __nv_bfloat16*)A, (const __nv_bfloat16*)G,
+    launch_pdl(t1_sum_kernel<__nv_bfloat16>, grid, 256, 0, s, g, (const __nv_bfloat16*)A, (const __nv_bfloat16*)G,
                                                       factors, eps, part_w, part_b);
-  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_reduce_splits(part_w, splits, (size_t)g.p * g.d, dW, accumulate, s);

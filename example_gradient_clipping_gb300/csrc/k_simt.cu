@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kThreads) simt_clipped_sum_kernel(Geom g, cons
                                                                     float* __restrict__ ws,
                                                                     float* __restrict__ ws_db,
                                                                     long rows_per_split) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) float Xs[kBK][kBM + 4];
   __shared__ __align__(16) float Ys[kBK][kBN + 4];
   const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN, split = blockIdx.z;
@@ -124,6 +126,8 @@ __global__ void __launch_bounds__(kThreads) simt_clipped_sum_kernel(Geom g, cons
 // out[e] (+)= sum_s ws[s*n + e]  (fixed order: deterministic)
 __global__ void reduce_splits_kernel(const float* __restrict__ ws, int splits, size_t n,
                                      float* __restrict__ out, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
     float s = accumulate ? out[e] : 0.f;
@@ -136,6 +140,8 @@ __global__ void reduce_splits_kernel(const float* __restrict__ ws, int splits, s
 // then a fixed butterfly (deterministic).
 __global__ void reduce_splits_warp_kernel(const float* __restrict__ ws, int splits, size_t n,
                                           float* __restrict__ out, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
   for (size_t e = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; e < n; e += nw) {
@@ -154,6 +160,8 @@ __global__ void __launch_bounds__(kThreads) simt_inst_kernel(Geom g, const E* __
                                                              const E* __restrict__ G,
                                                              float* __restrict__ ws_w,
                                                              float* __restrict__ ws_b) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) float Xs[kBK][kBM + 4];
   __shared__ __align__(16) float Ys[kBK][kBN + 4];
   __shared__ float red[kThreads / 32];
@@ -229,6 +237,8 @@ __global__ void __launch_bounds__(kThreads) simt_ghost_kernel(Geom g, const E* _
                                                               const E* __restrict__ G,
                                                               float* __restrict__ ws_h,
                                                               float* __restrict__ ws_g) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float Ts[kGT][kGT + 1];
   __shared__ float Ss[kGT][kGT + 1];
   __shared__ float red[kThreads / 32];
@@ -257,6 +267,8 @@ __global__ void __launch_bounds__(kThreads) simt_ghost_kernel(Geom g, const E* _
 // out[i] = sum_j ws1[i*n1 + j] + bias * sum_j ws2[i*n2 + j]  (one warp per example)
 __global__ void reduce_norm_kernel(const float* __restrict__ ws1, int n1, const float* __restrict__ ws2,
                                    int n2, int B, int bias, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= B) return;
@@ -293,22 +305,17 @@ cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, con
   float* ws_db = db ? ws + (size_t)splits * g.p * g.D : nullptr;
   dim3 grid(cdiv(g.p, kBM), cdiv(g.D, kBN), splits);
   if (dtype == DP_FP32)
-    simt_clipped_sum_kernel<float><<<grid, kThreads, 0, s>>>(g, (const float*)A, (const float*)G,
+    launch_pdl(simt_clipped_sum_kernel<float>, grid, kThreads, 0, s, g, (const float*)A, (const float*)G,
                                                               factors, ws, ws_db, rps);
   else
-    simt_clipped_sum_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
-        g, (const __nv_bfloat16*)A, (const __nv_bfloat16*)G, factors, ws, ws_db, rps);
-  count_launch();
+    launch_pdl(simt_clipped_sum_kernel<__nv_bfloat16>, grid, kThreads, 0, s, g, (const __nv_bfloat16*)A, (const __nv_bfloat16*)G, factors, ws, ws_db, rps);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t n = (size_t)g.p * g.D;
-  reduce_splits_kernel<<<(unsigned)std::min<size_t>((n + 255) / 256, 152 * 8), 256, 0, s>>>(
-      ws, splits, n, dW, accumulate);
-  count_launch();
+  launch_pdl(reduce_splits_kernel, (unsigned)std::min<size_t>((n + 255) / 256, 152 * 8), 256, 0, s, ws, splits, n, dW, accumulate);
   if (db) {
-    reduce_splits_kernel<<<(unsigned)((g.p + 255) / 256), 256, 0, s>>>(ws_db, splits, (size_t)g.p, db,
+    launch_pdl(reduce_splits_kernel, (unsigned)((g.p + 255) / 256), 256, 0, s, ws_db, splits, (size_t)g.p, db,
                                                                        accumulate);
-    count_launch();
   }
   return cudaGetLastError();
 }
@@ -317,13 +324,11 @@ cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* o
                                  cudaStream_t s) {
   if (splits >= 16 && n <= ((size_t)1 << 16)) {
     const size_t blocks = std::min<size_t>((n * 32 + 255) / 256, 152 * 8);
-    reduce_splits_warp_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(ws, splits, n, out, accumulate);
-    count_launch();
+    launch_pdl(reduce_splits_warp_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate);
     return cudaGetLastError();
   }
   const size_t blocks = std::min<size_t>((n + 255) / 256, 152 * 8);
-  reduce_splits_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(ws, splits, n, out, accumulate);
-  count_launch();
+  launch_pdl(reduce_splits_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate);
   return cudaGetLastError();
 }
 
@@ -340,15 +345,13 @@ cudaError_t launch_simt_ghost(const Geom& g, int dtype, const void* A, const voi
   float* ws_g = ws + (size_t)g.B * npairs;
   dim3 grid(npairs, g.B);
   if (dtype == DP_FP32)
-    simt_ghost_kernel<float><<<grid, kThreads, 0, s>>>(g, (const float*)A, (const float*)G, ws_h, ws_g);
+    launch_pdl(simt_ghost_kernel<float>, grid, kThreads, 0, s, g, (const float*)A, (const float*)G, ws_h, ws_g);
   else
-    simt_ghost_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(g, (const __nv_bfloat16*)A,
+    launch_pdl(simt_ghost_kernel<__nv_bfloat16>, grid, kThreads, 0, s, g, (const __nv_bfloat16*)A,
                                                                (const __nv_bfloat16*)G, ws_h, ws_g);
-  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  reduce_norm_kernel<<<cdiv(g.B, 8), 256, 0, s>>>(ws_h, npairs, ws_g, npairs, g.B, g.has_bias, out);
-  count_launch();
+  launch_pdl(reduce_norm_kernel, cdiv(g.B, 8), 256, 0, s, ws_h, npairs, ws_g, npairs, g.B, g.has_bias, out);
   return cudaGetLastError();
 }
 
@@ -364,15 +367,13 @@ cudaError_t launch_simt_inst(const Geom& g, int dtype, const void* A, const void
   float* ws_b = ws + (size_t)g.B * tm * tn;
   dim3 grid(tm, tn, g.B);
   if (dtype == DP_FP32)
-    simt_inst_kernel<float><<<grid, kThreads, 0, s>>>(g, (const float*)A, (const float*)G, ws_w, ws_b);
+    launch_pdl(simt_inst_kernel<float>, grid, kThreads, 0, s, g, (const float*)A, (const float*)G, ws_w, ws_b);
   else
-    simt_inst_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(g, (const __nv_bfloat16*)A,
+    launch_pdl(simt_inst_kernel<__nv_bfloat16>, grid, kThreads, 0, s, g, (const __nv_bfloat16*)A,
                                                               (const __nv_bfloat16*)G, ws_w, ws_b);
-  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  reduce_norm_kernel<<<cdiv(g.B, 8), 256, 0, s>>>(ws_w, tm * tn, ws_b, tm, g.B, g.has_bias, out);
-  count_launch();
+  launch_pdl(reduce_norm_kernel, cdiv(g.B, 8), 256, 0, s, ws_w, tm * tn, ws_b, tm, g.B, g.has_bias, out);
   return cudaGetLastError();
 }
 

@@ -269,6 +269,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = c->tmem;
+  pdl_trigger();   // the next kernel in the stream may start launching
+  pdl_wait();      // the previous kernel has completed; its writes are visible
 
   if (warp >= kEpiFirst) {
     ptx::regs_inc<216>();
@@ -289,6 +291,8 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
 //   sum:  part[split, j] = sum_{i in split} c_i sum_t G[i, j, t]   (one warp per row j)
 __global__ void conv_bias_norm_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
                                       float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = blockIdx.x; i < B; i += gridDim.x) {
@@ -322,6 +326,8 @@ __global__ void conv_bias_norm_kernel(const __nv_bfloat16* __restrict__ G, int B
 __global__ void conv_bias_sum_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
                                      const float* __restrict__ factors, int ex_per_split,
                                      float* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * 8 + warp;
   if (j >= p) return;
@@ -357,6 +363,8 @@ __global__ void conv_bias_sum_kernel(const __nv_bfloat16* __restrict__ G, int B,
 __global__ void conv_bias_sum_scalar_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
                                             const float* __restrict__ factors, int ex_per_split,
                                             float* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * 8 + warp;
   if (j >= p) return;
@@ -376,6 +384,8 @@ __global__ void conv_bias_sum_scalar_kernel(const __nv_bfloat16* __restrict__ G,
 // m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64).
 __global__ void conv_reduce_kernel(const float* __restrict__ part, int splits, int p, int ncols, int kk,
                                    float* __restrict__ dW, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
   const size_t n = (size_t)p * ncols;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
     const int j = (int)(q / ncols), m = (int)(q - (size_t)j * ncols);
@@ -474,8 +484,7 @@ cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, 
                                cudaStream_t s) {
   const size_t n = (size_t)p * ncols;
   const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
-  tcconv::conv_reduce_kernel<<<blocks ? blocks : 1, 256, 0, s>>>(part, splits, p, ncols, kk, dW, accumulate);
-  count_launch();
+  launch_plain(tcconv::conv_reduce_kernel, blocks ? blocks : 1, 256, 0, s, part, splits, p, ncols, kk, dW, accumulate);
   return cudaGetLastError();
 }
 
@@ -492,8 +501,7 @@ static cudaError_t launch_kernel(const Geom& g, const ConvPlan& c, const CUtenso
     attr_set[dev] = true;
   }
   dim3 grid(c.tm, c.tn, c.splits);
-  tcconv::tc_conv_kernel<kNorm><<<grid, tcconv::kThreads, tcconv::SMEM, s>>>(mG, mX, P);
-  count_launch();
+  launch_plain(tcconv::tc_conv_kernel<kNorm>, grid, tcconv::kThreads, tcconv::SMEM, s, mG, mX, P);
   return cudaGetLastError();
 }
 
@@ -531,9 +539,7 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
   if (e != cudaSuccess) return e;
   int rows = c.tiles;
   if (g.has_bias) {
-    tcconv::conv_bias_norm_kernel<<<std::min(g.B, 152 * 8), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T, part + (size_t)c.tiles * g.B);
-    count_launch();
+    launch_plain(tcconv::conv_bias_norm_kernel, std::min(g.B, 152 * 8), 256, 0, s, static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T, part + (size_t)c.tiles * g.B);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     rows += 1;
@@ -570,13 +576,12 @@ cudaError_t launch_conv_bias_sum(const Geom& g, const void* G, const float* fact
   const int beps = cdiv_c(g.B, bsplits);
   dim3 bgrid(cdiv_c(g.p, 8), cdiv_c(g.B, beps));
   if (g.T % 8 == 0) {
-    tcconv::conv_bias_sum_kernel<<<bgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
+    launch_plain(tcconv::conv_bias_sum_kernel, bgrid, 256, 0, s, static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
                                                        factors, beps, part);
   } else {
-    tcconv::conv_bias_sum_scalar_kernel<<<bgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
+    launch_plain(tcconv::conv_bias_sum_scalar_kernel, bgrid, 256, 0, s, static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
                                                               factors, beps, part);
   }
-  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_reduce_splits(part, (int)bgrid.y, (size_t)g.p, db, accumulate, s);

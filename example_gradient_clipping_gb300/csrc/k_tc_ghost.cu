@@ -13,6 +13,11 @@
 // both operands), an off-diagonal pair two.
 //   warps 0 and 6: TMA producers (alternate slots: one issuing thread streams only
 //   ~48 B/clk into an SM); warp 1: MMA issuer; warps 2-5: epilogue.
+// Dual mode (two row blocks, 128 < T <= 256): the Grams of the wider operand X (A or G)
+// are formed first, all three block pairs at once from the two row blocks loaded per K
+// step (TMEM columns 0..383), then the narrower operand Y pair by pair into columns
+// 384..511; after each Y pair the epilogue forms that pair's Hadamard sum.  The wider
+// operand's rows are loaded once instead of once per pair.
 // Packed mode (2T <= 128): one CTA takes ept = 128 / T examples whose rows are
 // consecutive in memory (2D boxes over the flattened rows), so one Gram tile holds
 // every example's Gram as a diagonal block; the epilogue adds only entries (r, s) of
@@ -75,7 +80,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   uint64_t* accum = empty + STAGES;       // [2]
   uint64_t* tfree = accum + 2;            // [2]
   uint64_t* drainb = tfree + 2;           // MMAs in flight at an abort
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drainb + 1);
+  uint64_t* ydone = drainb + 1;           // dual mode: a Y pair's Gram (and all X Grams) complete
+  uint64_t* yfree = ydone + 1;            // dual mode: the epilogue has read the Y Gram
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(yfree + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 2);   // [8]
   float* rowbuf = red + 8;                                 // packed mode: [2][BT] per-row sums
@@ -86,6 +93,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   const int nb = packed ? 1 : (P.T + BT - 1) / BT;
   const int npairs = nb * (nb + 1) / 2;
   const int kA = (P.d + BK - 1) / BK, kG = (P.p + BK - 1) / BK;
+  const bool dual = !packed && nb == 2;
+  const bool x_is_g = kG >= kA;                 // dual: the wider operand goes first
+  const int kX = x_is_g ? kG : kA, kY = x_is_g ? kA : kG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -97,6 +107,8 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       ptx::mbar_init(&tfree[b], 4);
     }
     ptx::mbar_init(drainb, 1);
+    ptx::mbar_init(ydone, 1);
+    ptx::mbar_init(yfree, 4);
     *abort = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&mapA);
@@ -107,13 +119,48 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();   // the next kernel in the stream may start launching
+  pdl_wait();      // the previous kernel has completed; its writes are visible
 
   if (warp == 0 || warp == 6) {
     // TMA producers (whole warp; the elected lane issues); producer pr loads slots k % 2 == pr
     const int pr = warp == 6 ? 1 : 0;
     int k = 0, issued = 0, last = -1;
     bool live = true;
-    for (int j = 0; j < npairs && live; ++j) {
+    if (dual) {
+      // X: both row blocks per K step; then Y: pairs (0,0), (0,1), (1,1)
+      const int nunits = 2 * kX + 4 * kY;
+      for (int u = 0; u < nunits && live; ++u, ++k) {
+        if ((k & 1) != pr) continue;
+        const int s = k % STAGES;
+        const bool w = ptx::mbar_wait(&empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+        bool is_a;
+        int kk, blk;
+        if (u < 2 * kX) {
+          kk = u >> 1;
+          blk = u & 1;
+          is_a = !x_is_g;
+        } else {
+          const int v = u - 2 * kX;       // pair 0: kY units, pair 1: 2 kY, pair 2: kY
+          if (v < kY) { kk = v; blk = 0; }
+          else if (v < 3 * kY) { kk = (v - kY) >> 1; blk = (v - kY) & 1; }
+          else { kk = v - 3 * kY; blk = 1; }
+          is_a = x_is_g;
+        }
+        if (ptx::elect_one()) {
+          ptx::mbar_arrive_expect_tx(&full[s], TILE);
+          if (is_a)
+            load_a_rows(P, &mapA, &full[s], smem + s * STAGE, kk, blk * BT, i, false);
+          else
+            ptx::tma_load_3d(&mapG, &full[s], smem + s * STAGE, kk * BK, blk * BT, i);
+        }
+        __syncwarp();
+        ++issued;
+        last = k;
+      }
+    }
+    for (int j = 0; j < npairs && live && !dual; ++j) {
       int tb, sb;
       pair_of(j, nb, tb, sb);
       const bool diag = tb == sb;
@@ -153,7 +200,62 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     // MMA issuer (whole warp; the elected lane issues)
     int k = 0;
     bool live = true;
-    for (int j = 0; j < npairs && live; ++j) {
+    if (dual) {
+      ptx::tc_fence_after();
+      // X Grams: (X0,X0) -> cols 0, (X0,X1) -> 128, (X1,X1) -> 256
+      for (int kk = 0; kk < kX && live; ++kk, k += 2) {
+        const int s0 = k % STAGES, s1 = (k + 1) % STAGES;
+        bool w = ptx::mbar_wait(&full[s0], (k / STAGES) & 1, abort, P.status);
+        w = w && ptx::mbar_wait(&full[s1], ((k + 1) / STAGES) & 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+        const uint64_t d0 = ptx::sdesc_sw128(ptx::smem_u32(smem + s0 * STAGE), 16, 1024);
+        const uint64_t d1 = ptx::sdesc_sw128(ptx::smem_u32(smem + s1 * STAGE), 16, 1024);
+        if (ptx::elect_one()) {
+#pragma unroll
+          for (int u = 0; u < BK / 16; ++u) {
+            const uint64_t a0 = ptx::sdesc_add(d0, u * 32), a1 = ptx::sdesc_add(d1, u * 32);
+            ptx::umma_bf16(tmem, a0, a0, kIdesc, (kk | u) != 0);
+            ptx::umma_bf16(tmem + 128, a0, a1, kIdesc, (kk | u) != 0);
+            ptx::umma_bf16(tmem + 256, a1, a1, kIdesc, (kk | u) != 0);
+          }
+          ptx::umma_commit(&empty[s0]);
+          ptx::umma_commit(&empty[s1]);
+        }
+        __syncwarp();
+      }
+      // Y Gram of each pair into cols 384, after the epilogue read the previous one
+      for (int q = 0; q < 3 && live; ++q) {
+        if (q > 0) {
+          const bool w = ptx::mbar_wait(yfree, (q - 1) & 1, abort, P.status);
+          if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+          ptx::tc_fence_after();
+        }
+        const bool diag = q != 1;
+        for (int kk = 0; kk < kY; ++kk) {
+          const int s0 = k % STAGES, s1 = (k + 1) % STAGES;
+          bool w = ptx::mbar_wait(&full[s0], (k / STAGES) & 1, abort, P.status);
+          if (!diag) w = w && ptx::mbar_wait(&full[s1], ((k + 1) / STAGES) & 1, abort, P.status);
+          if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+          const uint64_t da = ptx::sdesc_sw128(ptx::smem_u32(smem + s0 * STAGE), 16, 1024);
+          const uint64_t db = diag ? da : ptx::sdesc_sw128(ptx::smem_u32(smem + s1 * STAGE), 16, 1024);
+          if (ptx::elect_one()) {
+#pragma unroll
+            for (int u = 0; u < BK / 16; ++u)
+              ptx::umma_bf16(tmem + 384, ptx::sdesc_add(da, u * 32), ptx::sdesc_add(db, u * 32), kIdesc,
+                             (kk | u) != 0);
+            ptx::umma_commit(&empty[s0]);
+            if (!diag) ptx::umma_commit(&empty[s1]);
+          }
+          __syncwarp();
+          k += diag ? 1 : 2;
+        }
+        if (live) {
+          if (ptx::elect_one()) ptx::umma_commit(ydone);
+          __syncwarp();
+        }
+      }
+    }
+    for (int j = 0; j < npairs && live && !dual; ++j) {
       int tb, sb;
       pair_of(j, nb, tb, sb);
       const bool diag = tb == sb;
@@ -199,7 +301,35 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     const int c_lo = packed ? row / P.T * P.T : 0, c_hi = packed ? c_lo + P.T : BT;
     float H = 0.f, S = 0.f;
     bool ok = true;
-    for (int j = 0; j < npairs; ++j) {
+    if (dual) {
+      for (int q = 0; q < 3; ++q) {
+        const bool w = ptx::mbar_wait(ydone, q & 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        ptx::tc_fence_after();
+        float h = 0.f, sg = 0.f;
+        const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
+        const uint32_t bx = tmem + q * 128 + lanes, by = tmem + 384 + lanes;
+#pragma unroll 1
+        for (int c = 0; c < BT / 32; ++c) {
+          float vx[32], vy[32];
+          ptx::tmem_ld32(bx + c * 32, vx);
+          ptx::tmem_ld32(by + c * 32, vy);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            h = fmaf(vx[e], vy[e], h);
+            sg += x_is_g ? vx[e] : vy[e];
+          }
+        }
+        const float wgt = q == 1 ? 2.f : 1.f;
+        H = fmaf(wgt, h, H);
+        S = fmaf(wgt, sg, S);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(yfree);
+      }
+    }
+    for (int j = 0; j < npairs && !dual; ++j) {
       int tb, sb;
       pair_of(j, nb, tb, sb);
       const int b = j & 1;
@@ -300,8 +430,7 @@ static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtenso
     attr_set[dev] = true;
   }
   const int grid = P.ept ? (g.B + P.ept - 1) / P.ept : g.B;
-  tcghost::tc_ghost_kernel<<<grid, tcghost::kThreads, tcghost::SMEM, s>>>(ma, mg, P);
-  count_launch();
+  launch_pdl(tcghost::tc_ghost_kernel, grid, tcghost::kThreads, tcghost::SMEM, s, ma, mg, P);
   return cudaGetLastError();
 }
 

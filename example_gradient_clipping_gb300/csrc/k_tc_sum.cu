@@ -100,6 +100,8 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();   // the next kernel in the stream may start launching
+  pdl_wait();      // the previous kernel has completed; its writes are visible
 
   // boxes inside the layer: G boxes along p, A boxes along D; MMA width N along D
   const int ng = min(2, (P.p - m0 + 63) / 64), na = min(4, (P.d - n0 + 63) / 64);
@@ -429,8 +431,7 @@ static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtens
     attr_set[dev] = true;
   }
   dim3 grid(cdiv_i(g.p, tcsum::BM), cdiv_i(g.D, tcsum::BN), splits);
-  tcsum::tc_sum_kernel<<<grid, tcsum::kThreads, tcsum::SMEM, s>>>(mg, ma, P);
-  count_launch();
+  launch_pdl(tcsum::tc_sum_kernel, grid, tcsum::kThreads, tcsum::SMEM, s, mg, ma, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = g.conv ? launch_conv_reduce(ws, splits, g.p, g.D, g.k * g.k, dW, accumulate, s)

@@ -533,6 +533,8 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = c->tmem;
+  pdl_trigger();   // the next kernel in the stream may start launching
+  pdl_wait();      // the previous kernel has completed; its writes are visible
 
   if (warp >= kEpiFirst) {
     ptx::regs_inc<216>();
@@ -685,13 +687,15 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   cfg.blockDim = dim3(tcsumx::kThreads);
   cfg.dynamicSmemBytes = tcsumx::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = splits;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = splits;
   cfg.attrs = attr;
-  cfg.numAttrs = splits > 1 ? 1 : 0;
+  cfg.numAttrs = splits > 1 ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false>, mg64, ma64, mg16, ma16, P);
   count_launch();
   if (e != cudaSuccess || !gsplits) return e;
@@ -749,8 +753,7 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
     attr_set[dev] = true;
   }
   dim3 grid(tm, tn, (unsigned)chunks);
-  tcsumx::tc_sumx_kernel<true><<<grid, tcsumx::kThreads, tcsumx::SMEM, s>>>(mg64, ma64, mg16, ma16, P);
-  count_launch();
+  launch_pdl(tcsumx::tc_sumx_kernel<true>, grid, tcsumx::kThreads, tcsumx::SMEM, s, mg64, ma64, mg16, ma16, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_reduce_splits(ws, (int)tiles, (size_t)g.B, out, 0, s);

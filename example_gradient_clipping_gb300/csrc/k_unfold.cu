@@ -19,6 +19,8 @@ namespace dpk {
 // 16-byte stores, each gathered from shared memory (zero outside the image).
 __global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __restrict__ x,
                                         __nv_bfloat16* __restrict__ U) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) __nv_bfloat16 xs[];     // [Cin][H][W]
   const int kk = g.k * g.k;
   const int cpr = Dp >> 3;                                // 16-byte chunks per output row
@@ -63,6 +65,8 @@ __global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __r
 // output chunk, gathered from global memory.
 __global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restrict__ x,
                                    __nv_bfloat16* __restrict__ U, size_t n_chunks) {
+  pdl_trigger();
+  pdl_wait();
   const int cpr = Dp >> 3;
   const int kk = g.k * g.k;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n_chunks;
@@ -96,6 +100,8 @@ constexpr int kTT = 64;
 __global__ void transpose_rows_vec_kernel(int B, int T, int p, int tt, const __nv_bfloat16* __restrict__ G,
                                           __nv_bfloat16* __restrict__ Gt, const float* __restrict__ scale,
                                           float* __restrict__ bias_part) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) __nv_bfloat16 s[kTT][kTT];
   const int nt = (T + tt - 1) / tt, tp = (p + kTT - 1) / kTT;
   const int tch = tt / 8;                                 // t chunks per tile row
@@ -149,6 +155,8 @@ __global__ void transpose_rows_vec_kernel(int B, int T, int p, int tt, const __n
 __global__ void transpose_rows_short_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
                                             __nv_bfloat16* __restrict__ Gt, const float* __restrict__ scale,
                                             float* __restrict__ bias_part) {
+  pdl_trigger();
+  pdl_wait();
   const int cp = p >> 3;
   const size_t n = (size_t)B * cp;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
@@ -177,6 +185,8 @@ __global__ void transpose_rows_short_kernel(int B, int T, int p, const __nv_bflo
 // General fallback: 32 x 33 tiles, 2-byte accesses.
 __global__ void transpose_rows_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
                                       __nv_bfloat16* __restrict__ Gt) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __nv_bfloat16 tile[32][33];
   const int t0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
   for (int i = blockIdx.z; i < B; i += gridDim.z) {
@@ -197,6 +207,8 @@ __global__ void transpose_rows_kernel(int B, int T, int p, const __nv_bfloat16* 
 // dW[j, m] (+)= Wp[j, m] for m < D (the padded columns are dropped).
 __global__ void compact_cols_kernel(const float* __restrict__ Wp, int p, int D, int Dp, float* __restrict__ dW,
                                     int accumulate) {
+  pdl_trigger();
+  pdl_wait();
   const size_t n = (size_t)p * D;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
     const size_t j = q / D, m = q - j * D;
@@ -233,13 +245,12 @@ cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* 
       }
     }
     const unsigned blocks = (unsigned)std::min<long>(g.B, 152L * 16);
-    unfold_rows_smem_kernel<<<blocks, 256, stage, s>>>(g, Dp, xb, Ub);
+    launch_plain(unfold_rows_smem_kernel, blocks, 256, stage, s, g, Dp, xb, Ub);
   } else {
     const size_t n_chunks = (size_t)g.B * g.T * (Dp / 8);
     const size_t blocks = std::min<size_t>((n_chunks + 255) / 256, (size_t)152 * 16);
-    unfold_rows_kernel<<<(unsigned)(blocks ? blocks : 1), 256, 0, s>>>(g, Dp, xb, Ub, n_chunks);
+    launch_plain(unfold_rows_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, g, Dp, xb, Ub, n_chunks);
   }
-  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (scale) return launch_scaled_rows(g.B, g.T, g.p, G, Gt, scale, db, accumulate, bias_part, s);
@@ -262,17 +273,16 @@ cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* ds
     const int tt = std::min(kTT, T);
     const long units = (long)B * ((T + tt - 1) / tt) * ((p + kTT - 1) / kTT);
     const unsigned blocks = (unsigned)std::min<long>(units, 152L * 16);
-    transpose_rows_vec_kernel<<<blocks, 256, 0, s>>>(B, T, p, tt, Gb, Gtb, scale, bias_part);
+    launch_plain(transpose_rows_vec_kernel, blocks, 256, 0, s, B, T, p, tt, Gb, Gtb, scale, bias_part);
   } else if (p % 8 == 0) {
     const size_t n = (size_t)B * (p / 8);
     const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 16);
-    transpose_rows_short_kernel<<<blocks ? blocks : 1, 256, 0, s>>>(B, T, p, Gb, Gtb, scale, bias_part);
+    launch_plain(transpose_rows_short_kernel, blocks ? blocks : 1, 256, 0, s, B, T, p, Gb, Gtb, scale, bias_part);
   } else {
     if (scale || bias_part) return cudaErrorInvalidValue;   // scaled copies need p % 8 == 0
     dim3 grid((T + 31) / 32, (p + 31) / 32, std::min(B, 65535));
-    transpose_rows_kernel<<<grid, dim3(32, 8), 0, s>>>(B, T, p, Gb, Gtb);
+    launch_plain(transpose_rows_kernel, grid, dim3(32, 8), 0, s, B, T, p, Gb, Gtb);
   }
-  count_launch();
   return cudaGetLastError();
 }
 
@@ -290,8 +300,7 @@ size_t scaled_rows_bias_bytes(int B, int T, int p) {
 cudaError_t launch_compact_cols(const float* Wp, int p, int D, int Dp, float* dW, int accumulate, cudaStream_t s) {
   const size_t n = (size_t)p * D;
   const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
-  compact_cols_kernel<<<blocks ? blocks : 1, 256, 0, s>>>(Wp, p, D, Dp, dW, accumulate);
-  count_launch();
+  launch_plain(compact_cols_kernel, blocks ? blocks : 1, 256, 0, s, Wp, p, D, Dp, dW, accumulate);
   return cudaGetLastError();
 }
 
