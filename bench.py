@@ -349,24 +349,29 @@ def run_ours(args, wl):
     per_call = {n: [t / REPS for t in timed(g.replay, max(5, args.steps // 4), seed0)]
                 for n, g in call_graphs.items()}
 
-    # end to end through the public API: pinned host inputs copied in, result copied out
-    out_host = torch.empty(step.n_params, dtype=torch.float32).pin_memory()
+    # end to end through the public API: every step copies a batch from pinned host memory
+    # and its gradient back (ClipPipeline: one graph per step, the copy of batch k+1 on a
+    # forked stream alongside the compute of batch k); events around K graph launches
+    pipe = dp.ClipPipeline(descs, [(tuple(a.shape), tuple(g.shape)) for a, g in pinned], wl.dtype, C=wl.C,
+                           sigma=wl.sigma, per_layer=wl.per_layer, device=str(dev))
+    for hset in (pipe.host_inputs(0), pipe.host_inputs(1)):     # the same batch every step
+        for (ha, hg), (sa, sg) in zip(hset, pinned):
+            ha.copy_(sa)
+            hg.copy_(sg)
     h2d = sum(a.numel() * a.element_size() + g.numel() * g.element_size() for a, g in pinned)
-    d2h = out_host.numel() * 4
-    e2e_ms = []
-    for k in range(args.warmup + args.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for (ha, hg), (da, dg) in zip(pinned, dev_in):
-            da.copy_(ha, non_blocking=True)
-            dg.copy_(hg, non_blocking=True)
-        g = step.replay(wl.seed + 7 * k)
-        out_host.copy_(g, non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        if k >= args.warmup:
-            e2e_ms.append(e0.elapsed_time(e1))
+    d2h = pipe.n_params * 4
+    pipe.start()
+    W = max(args.warmup, 3)
+    for k in range(W):
+        pipe.step(k, wl.seed + 7 * k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(W, W + args.steps):
+        pipe.step(k, wl.seed + 7 * k)
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = [e0.elapsed_time(e1)]
     e2e_tot = max_over_ranks(sum(e2e_ms), dev)
     e2e_value = world * wl.B * args.steps / (e2e_tot / 1e3)
 
@@ -397,7 +402,11 @@ def run_ours(args, wl):
                     warmup=max(args.warmup, 3), ms_per_step=total_ms / args.steps, higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype=wl.dtype, data="synthetic",
                     config=_config(wl, dict(norm_modes=modes, parallelism=f"replicas x{world}")),
-                    e2e=dict(value=e2e_value, unit="examples/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+                    e2e=dict(value=e2e_value, unit="examples/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                             pipeline="ClipPipeline: one CUDA graph per step runs the step on one of two "
+                                      "device buffer sets, copies its gradient to pinned host memory and, on a "
+                                      "forked stream, copies the next batch from pinned host memory into the other "
+                                      "set"),
                     gpu_launches=int(launches), roofline=roof, clocks=clk.summary(),
                     calls_ms={n: round(v, 5) for n, v in means.items()},
                     kernels_per_step=step.graph_kernels,
@@ -409,6 +418,55 @@ def run_ours(args, wl):
         torch.distributed.destroy_process_group()
 
 
+def run_hbm_sweep(args):
+    """Supplementary steady-state bandwidth of the HBM-bound kernels on large inputs (not
+    the bench line): the noise/scale pass over a >= 256 MB parameter vector and the one-row
+    norm over a >= 512 MB batch, each timed with CUDA events over back-to-back calls after
+    an L2 flush.  Bytes are algorithmic: noise reads and writes each fp32 element once;
+    the one-row norm reads A and G once."""
+    import torch
+    import example_gradient_clipping_gb300 as dp
+    pk = _peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    out = []
+
+    def timed(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    for n in (64 << 20, 256 << 20):                     # 256 MB and 1 GB of fp32
+        g = torch.randn(n, device="cuda")
+        sec = timed(lambda: dp.dp_add_noise(g, 1.0, 1.0, 64, 7, 0))
+        gbs = 8 * n / sec / 1e9
+        out.append(dict(kernel="add_noise_kernel", elements=n, bytes=8 * n, us=sec * 1e6, gbs=gbs,
+                        frac=gbs / pk["hbm"]))
+        del g
+    for B, d, p in ((262144, 512, 512), (65536, 4096, 4096)):   # 512 MB and 2 GB of bf16 rows
+        A = torch.randn(B, d, device="cuda").to(torch.bfloat16)
+        G = torch.randn(B, p, device="cuda").to(torch.bfloat16)
+        desc = dp.layer_desc(dp.DP_LINEAR, dp.DP_BF16, B=B, p=p, T=1, d=d, has_bias=True)
+        sq = torch.empty(B, device="cuda")
+        ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+        sec = timed(lambda: dp.dp_layer_sqnorms(desc, A, G, sq, ws, mode=dp.DP_NORM_T1))
+        nb = 2 * B * (d + p)
+        gbs = nb / sec / 1e9
+        out.append(dict(kernel="t1_norm_kernel", B=B, d=d, p=p, bytes=nb, us=sec * 1e6, gbs=gbs,
+                        frac=gbs / pk["hbm"]))
+        del A, G
+    print(json.dumps(dict(supplementary="hbm_sweep", peak_gbs=pk["hbm"], peak_source=pk["src"], results=out)),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -417,6 +475,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--hbm-sweep", action="store_true",
+                    help="supplementary steady-state bandwidth of the noise and one-row norm kernels")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling and sweeps; not the bench line)")
     args = ap.parse_args()
@@ -424,6 +484,9 @@ def main():
     wl = workloads.get_workload(args.workload)
     if args.batch:
         wl = wl.with_batch(args.batch)
+    if args.hbm_sweep:
+        run_hbm_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, wl)
     else:

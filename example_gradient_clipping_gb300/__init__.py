@@ -174,4 +174,4 @@ def dp_check_status(stream=None) -> int:
     return _lib.dp_check_status(_stream(stream))
 
 
-from .step import ClipStep  # noqa: E402,F401
+from .step import ClipPipeline, ClipStep  # noqa: E402,F401

@@ -39,8 +39,38 @@ __global__ void __launch_bounds__(256) t1_norm_kernel(Geom g, const E* __restric
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < g.B; i += warps) {
-    const float sa = row_sqsum(A + (size_t)i * g.d, g.d, lane, vec_a);
-    const float sg = row_sqsum(G + (size_t)i * g.p, g.p, lane, vec_g);
+    const E* a = A + (size_t)i * g.d;
+    const E* gg = G + (size_t)i * g.p;
+    float sa, sg;
+    if (vec_a && vec_g) {
+      // both rows at once: the loads of a and g are in flight together
+      constexpr int kVec = 16 / sizeof(E);
+      const int nva = g.d / kVec, nvg = g.p / kVec, nv = max(nva, nvg);
+      const uint4* av = reinterpret_cast<const uint4*>(a);
+      const uint4* gv = reinterpret_cast<const uint4*>(gg);
+      float xa = 0.f, xg = 0.f;
+#pragma unroll 2
+      for (int v = lane; v < nv; v += 32) {
+        uint4 wa = make_uint4(0u, 0u, 0u, 0u), wg = make_uint4(0u, 0u, 0u, 0u);
+        if (v < nva) wa = __ldg(av + v);
+        if (v < nvg) wg = __ldg(gv + v);
+        const E* ea = reinterpret_cast<const E*>(&wa);
+        const E* eg = reinterpret_cast<const E*>(&wg);
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) {
+          const float fa = to_f(ea[q]), fg = to_f(eg[q]);
+          xa = fmaf(fa, fa, xa);
+          xg = fmaf(fg, fg, xg);
+        }
+      }
+      for (int j = nva * kVec + lane; j < g.d; j += 32) { const float f = to_f(a[j]); xa = fmaf(f, f, xa); }
+      for (int j = nvg * kVec + lane; j < g.p; j += 32) { const float f = to_f(gg[j]); xg = fmaf(f, f, xg); }
+      sa = warp_sum(xa);
+      sg = warp_sum(xg);
+    } else {
+      sa = row_sqsum(a, g.d, lane, vec_a);
+      sg = row_sqsum(gg, g.p, lane, vec_g);
+    }
     if (lane == 0) out[i] = sa * sg + (g.has_bias ? sg : 0.f);
   }
 }
@@ -53,7 +83,8 @@ __global__ void __launch_bounds__(256) t1_norm_kernel(Geom g, const E* __restric
 template <class E>
 __global__ void __launch_bounds__(256) t1_sum_kernel(Geom g, const E* __restrict__ A, const E* __restrict__ G,
                                                      const float* __restrict__ factors, int ex_per_split,
-                                                     float* __restrict__ part_w, float* __restrict__ part_b) {
+                                                     float* __restrict__ part_w, float* __restrict__ part_b,
+                                                     int accumulate) {
   pdl_trigger();
   pdl_wait();
   const int mq = (g.d + 3) / 4;                      // m quads per row
@@ -62,19 +93,39 @@ __global__ void __launch_bounds__(256) t1_sum_kernel(Geom g, const E* __restrict
   for (long q = blockIdx.x * (long)blockDim.x + threadIdx.x; q < n_th; q += (long)gridDim.x * blockDim.x) {
     const int j = (int)(q / mq), m0 = (int)(q - (long)j * mq) * 4;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, bacc = 0.f;
-    for (int i = i0; i < i1; ++i) {
-      const float cg = __ldg(factors + i) * to_f(G[(size_t)i * g.p + j]);
-      const E* a = A + (size_t)i * g.d + m0;
+    // eight examples' loads in flight per pass, accumulated in example order
+    for (int ib = i0; ib < i1; ib += 8) {
+      float cg[8], av[8][4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (m0 + r < g.d) acc[r] = fmaf(cg, to_f(a[r]), acc[r]);
-      bacc += cg;
+      for (int u = 0; u < 8; ++u) {
+        const int i = ib + u;
+        cg[u] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) av[u][r] = 0.f;
+        if (i < i1) {
+          cg[u] = __ldg(factors + i) * to_f(G[(size_t)i * g.p + j]);
+          const E* a = A + (size_t)i * g.d + m0;
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (m0 + r < g.d) av[u][r] = to_f(a[r]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] = fmaf(cg[u], av[u][r], acc[r]);
+        bacc += cg[u];
+      }
     }
+    // partials of split blockIdx.y, or (one split, accumulate) the output itself
     float* out = part_w + ((size_t)blockIdx.y * g.p + j) * g.d + m0;
 #pragma unroll
     for (int r = 0; r < 4; ++r)
-      if (m0 + r < g.d) out[r] = acc[r];
-    if (part_b && m0 == 0) part_b[(size_t)blockIdx.y * g.p + j] = bacc;
+      if (m0 + r < g.d) out[r] = accumulate ? out[r] + acc[r] : acc[r];
+    if (part_b && m0 == 0) {
+      float* ob = part_b + (size_t)blockIdx.y * g.p + j;
+      *ob = accumulate ? *ob + bacc : bacc;
+    }
   }
 }
 
@@ -114,8 +165,28 @@ __global__ void clip_factors_kernel(const float* __restrict__ sq, int B, int L, 
 
 // ---------------------------------------------------------------------------
 // Gaussian mechanism + 1/B: grad[j] = (grad[j] + sc * z_{offset+j}) * invB.
-// One thread per Philox block of four consecutive elements of the global index;
-// float4 load/store when the four lie in range and are 16-byte aligned.
+// One thread per pair of Philox blocks (eight consecutive elements of the global index)
+// per pass: both loads are issued first, then the two generator chains run side by side
+// (the kernel is bound by the generator's arithmetic at large sizes); float4 load/store
+// when the four lie in range and are 16-byte aligned.
+__device__ __forceinline__ void noise_block_store(float* __restrict__ grad, size_t n, int64_t j0, bool vec, float4 v,
+                                                  const float (&z)[4], float sc, float invB) {
+  if (vec) {
+    v.x = fmaf(sc, z[0], v.x) * invB;
+    v.y = fmaf(sc, z[1], v.y) * invB;
+    v.z = fmaf(sc, z[2], v.z) * invB;
+    v.w = fmaf(sc, z[3], v.w) * invB;
+    __stcs(reinterpret_cast<float4*>(grad + j0), v);
+  } else {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int64_t j = j0 + r;
+      if (j >= 0 && j < (int64_t)n) grad[j] = fmaf(sc, z[r], grad[j]) * invB;
+    }
+  }
+}
+
+template <int NB>
 __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad, size_t n, float sc,
                                                         float invB, uint64_t seed, uint64_t offset,
                                                         const unsigned long long* __restrict__ seed_dev) {
@@ -124,26 +195,22 @@ __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad
   if (seed_dev) seed = *seed_dev;
   const uint64_t q0 = offset >> 2;
   const uint64_t q1 = (offset + n + 3) >> 2;  // one past the last block touched
-  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-  for (uint64_t q = q0 + (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; q < q1; q += stride) {
-    float z[4];
-    normal4(q, seed, 0u, z);
-    const int64_t j0 = (int64_t)(q << 2) - (int64_t)offset;   // index of lane 0 in grad
-    float* p = grad + j0;
-    if (j0 >= 0 && j0 + 4 <= (int64_t)n && ((reinterpret_cast<uintptr_t>(p) & 15u) == 0)) {
-      float4 v = *reinterpret_cast<float4*>(p);
-      v.x = fmaf(sc, z[0], v.x) * invB;
-      v.y = fmaf(sc, z[1], v.y) * invB;
-      v.z = fmaf(sc, z[2], v.z) * invB;
-      v.w = fmaf(sc, z[3], v.w) * invB;
-      *reinterpret_cast<float4*>(p) = v;
-    } else {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int64_t j = j0 + r;
-        if (j >= 0 && j < (int64_t)n) grad[j] = fmaf(sc, z[r], grad[j]) * invB;
-      }
-    }
+  const uint64_t stride = NB * (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t qa = q0 + NB * ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x); qa < q1; qa += stride) {
+    const uint64_t qb = qa + 1;
+    const bool has_b = NB == 2 && qb < q1;
+    const int64_t ja = (int64_t)(qa << 2) - (int64_t)offset, jb = ja + 4;   // index of lane 0 in grad
+    const bool va = ja >= 0 && ja + 4 <= (int64_t)n && ((reinterpret_cast<uintptr_t>(grad + ja) & 15u) == 0);
+    const bool vb = has_b && jb >= 0 && jb + 4 <= (int64_t)n &&
+                    ((reinterpret_cast<uintptr_t>(grad + jb) & 15u) == 0);
+    float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = xa;
+    if (va) xa = __ldcs(reinterpret_cast<const float4*>(grad + ja));
+    if (vb) xb = __ldcs(reinterpret_cast<const float4*>(grad + jb));
+    float za[4], zb[4];
+    normal4(qa, seed, 0u, za);
+    if (NB == 2) normal4(qb, seed, 0u, zb);
+    noise_block_store(grad, n, ja, va, xa, za, sc, invB);
+    if (has_b) noise_block_store(grad, n, jb, vb, xb, zb, sc, invB);
   }
 }
 
@@ -213,11 +280,16 @@ cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, co
 cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,
                              uint64_t offset, const unsigned long long* seed_dev, cudaStream_t s) {
   const uint64_t blocks4 = ((offset + n + 3) >> 2) - (offset >> 2);
-  uint64_t grid = (blocks4 + 255) / 256;
   const uint64_t cap = 152ull * 8ull;   // grid-stride beyond 8 resident blocks per SM
+  // two Philox blocks per thread and pass once the grid is full anyway, else one
+  const bool two = blocks4 >= 2 * cap * 256;
+  uint64_t grid = (blocks4 + (two ? 511 : 255)) / (two ? 512 : 256);
   if (grid > cap) grid = cap;
   if (grid == 0) grid = 1;
-  launch_pdl(add_noise_kernel, (unsigned)grid, 256, 0, s, grad, n, sc, invB, seed, offset, seed_dev);
+  if (two)
+    launch_pdl(add_noise_kernel<2>, (unsigned)grid, 256, 0, s, grad, n, sc, invB, seed, offset, seed_dev);
+  else
+    launch_pdl(add_noise_kernel<1>, (unsigned)grid, 256, 0, s, grad, n, sc, invB, seed, offset, seed_dev);
   return cudaGetLastError();
 }
 
@@ -228,8 +300,8 @@ cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alph
   return cudaGetLastError();
 }
 
-// Examples per split of the one-row clipped sum: about 128, at least one split.
-static int t1_sum_eps(const Geom& g) { return std::min(g.B, 128); }
+// Examples per split of the one-row clipped sum: about 32, at least one split.
+static int t1_sum_eps(const Geom& g) { return std::min(g.B, 32); }
 int t1_sum_splits(const Geom& g) { const int e = t1_sum_eps(g); return (g.B + e - 1) / e; }
 size_t t1_sum_ws_bytes(const Geom& g) {
   return (size_t)t1_sum_splits(g) * ((size_t)g.p * g.d + g.p) * sizeof(float);
@@ -238,17 +310,20 @@ size_t t1_sum_ws_bytes(const Geom& g) {
 cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G, const float* factors, float* dW,
                           float* db, int accumulate, float* ws, cudaStream_t s) {
   const int eps = t1_sum_eps(g), splits = t1_sum_splits(g);
-  float* part_w = ws;
-  float* part_b = db ? ws + (size_t)splits * g.p * g.d : nullptr;
+  const bool direct = splits == 1;           // one split writes dW and db itself
+  float* part_w = direct ? dW : ws;
+  float* part_b = db ? (direct ? db : ws + (size_t)splits * g.p * g.d) : nullptr;
+  const int acc = direct ? accumulate : 0;
   const long n_th = (long)g.p * ((g.d + 3) / 4);
   dim3 grid((unsigned)std::min<long>((n_th + 255) / 256, 152L * 8), (unsigned)splits);
   if (dtype == DP_FP32)
-    launch_pdl(t1_sum_kernel<float>, grid, 256, 0, s, g, (const float*)A, (const float*)G, factors, eps, part_w, part_b);
+    launch_pdl(t1_sum_kernel<float>, grid, 256, 0, s, g, (const float*)A, (const float*)G, factors, eps, part_w, part_b,
+               acc);
   else
     launch_pdl(t1_sum_kernel<__nv_bfloat16>, grid, 256, 0, s, g, (const __nv_bfloat16*)A, (const __nv_bfloat16*)G,
-                                                      factors, eps, part_w, part_b);
+                                                      factors, eps, part_w, part_b, acc);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || direct) return e;
   e = launch_reduce_splits(part_w, splits, (size_t)g.p * g.d, dW, accumulate, s);
   if (e != cudaSuccess || !db) return e;
   return launch_reduce_splits(part_b, splits, (size_t)g.p, db, accumulate, s);

@@ -152,6 +152,29 @@ __global__ void reduce_splits_warp_kernel(const float* __restrict__ ws, int spli
   }
 }
 
+// Very many splits of a short vector: one block per element, threads stride over the
+// splits, then a fixed tree over the block (deterministic).
+__global__ void reduce_splits_block_kernel(const float* __restrict__ ws, int splits, size_t n,
+                                           float* __restrict__ out, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (size_t e = blockIdx.x; e < n; e += gridDim.x) {
+    float s = 0.f;
+    for (int k = threadIdx.x; k < splits; k += blockDim.x) s += ws[(size_t)k * n + e];
+    s = warp_sum(s);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    if (warp == 0) {
+      float t = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
+      t = warp_sum(t);
+      if (lane == 0) out[e] = accumulate ? out[e] + t : t;
+    }
+    __syncthreads();
+  }
+}
+
 // Instantiated norm: CTA (bx, by, i) forms the 64x64 tile of g_i = G_i^T U(A_i)
 // over all T rows of example i, squares and sums it ([MixGhost] Appendix C.4).
 // CTAs with by == 0 also form the bias gradient sum_t G_i[t, :] of their rows.
@@ -322,6 +345,11 @@ cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, con
 
 cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
                                  cudaStream_t s) {
+  if (splits >= 512 && n <= ((size_t)1 << 14)) {
+    const unsigned blocks = (unsigned)std::min<size_t>(n, 152 * 8);
+    launch_pdl(reduce_splits_block_kernel, blocks ? blocks : 1, 256, 0, s, ws, splits, n, out, accumulate);
+    return cudaGetLastError();
+  }
   if (splits >= 16 && n <= ((size_t)1 << 16)) {
     const size_t blocks = std::min<size_t>((n * 32 + 255) / 256, 152 * 8);
     launch_pdl(reduce_splits_warp_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate);

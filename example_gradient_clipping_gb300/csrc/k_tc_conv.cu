@@ -7,13 +7,18 @@
 // [p, T] is the K-major A operand as it lies in memory.  Per CTA: one 128 x 256 tile
 // of P (128 outputs x four im2col blocks = 256 unfolded columns), per example in one
 // of two TMEM buffers.
-//   norm mode: the epilogue adds up P_i^2 over the tile -> part[tile, i]; the squared
-//              bias gradient comes from conv_bias_kernel; a fixed-order sum over the
-//              tiles gives ||g_i||^2 (the instantiated norm of [MixGhost] section 3).
+//   norm mode: the epilogue adds up P_i^2 over the tile -> part[tile, i]; a fixed-order
+//              sum over the tiles gives ||g_i||^2 (the instantiated norm of [MixGhost]
+//              section 3).
 //   sum mode:  the epilogue folds c_i P_i into fp32 registers (the clip factor of
 //              [FastClip] section 5 applied in fp32) over the CTA's examples and
 //              writes a partial tile; a fixed-order reduction over the example splits
 //              maps the columns back to the weight layout [p, Cin, k, k].
+//   bias:      the last column tile carries one more 64-column block of constant ones in
+//              every stage buffer (written once; the TMA never touches it), so the MMA
+//              also forms b_i = sum_t G_i[:, t] (every column of that block), accumulated
+//              in fp32 like the rest: its square joins the norm partial, c_i b_i the db
+//              partial of the CTA's split.
 // Columns of the tile: block q = cc * k*k + tap (channel block cc of 64, filter tap
 // kh*k + kw), 64 channels each; the weight column is (64 cc + c) * k*k + tap.
 // Roles (384 threads): warps 0 and 2 TMA producers (alternate stages), warp 1 MMA
@@ -35,12 +40,14 @@ constexpr int kEpiFirst = 4, kEpiWarps = 8;
 constexpr int SMEM = STAGES * STAGE + 1024 + 512;
 constexpr int PSTR = BN + 4;                 // staged output row stride (floats)
 static_assert(BM * PSTR * 4 <= STAGES * STAGE, "staging fits in the stage buffers");
-// A = G (K-major: pixels contiguous), B = im2col blocks (MN-major: channels contiguous)
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, BN, 0, 1);
+// A = G (K-major: pixels contiguous), B = im2col blocks (MN-major: channels contiguous);
+// the instruction's N is the tile's block count x 64
 
 struct Params {
   const float* factors;   // sum mode
   float* part;            // norm: [tiles, B]; sum: [splits, p, ncols]
+  float* part_db;         // sum mode with bias: [splits, p]
+  int bias;               // the layer has a bias
   unsigned* status;
   int B, T, p, Wout, k, stride, pad, dil;
   int items;              // im2col blocks per pixel block: k*k*Cin/64
@@ -95,8 +102,9 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG,
 }
 
 __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0,
-                                           int e1) {
+                                           int e1, int nblocks) {
   volatile int* abort = &c->abort;
+  const uint32_t idesc = ptx::idesc_bf16_f32(BM, 64 * nblocks, 0, 1);   // the tile's blocks only
   int k = 0;
   bool live = true;
   for (int e = e0; e < e1 && live; ++e) {
@@ -119,7 +127,7 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 32), ptx::sdesc_add(dbd, kk * 2048), kIdesc,
+          ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 32), ptx::sdesc_add(dbd, kk * 2048), idesc,
                          (u | kk) != 0);
         ptx::umma_commit(&c->empty[s]);
       }
@@ -136,10 +144,14 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
 // abort) so the per-example barrier of the norm mode is always complete.
 template <bool kNorm>
 __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0, int e1,
-                                         int m0, int q0, int nitems) {
+                                         int m0, int q0, int nitems, int ones_slot) {
   volatile int* abort = &c->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, half = (warp - kEpiFirst) >> 2;
+  // bias: the ones block (slot ones_slot of the tile, or -1) holds b_i in every column;
+  // this thread's rows take it from the first column when the slot is in its half
+  const bool my_ones = ones_slot >= 0 && (ones_slot >> 1) == half;
+  const int ones_ch = (ones_slot & 1) * 4;              // 16-column chunk of that column
   // this thread's 128 columns are blocks 2*half and 2*half + 1 of the tile
   const bool v0 = 2 * half < nitems, v1 = 2 * half + 1 < nitems;
   const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
@@ -174,6 +186,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
               ss = fmaf(a1[j], a1[j], ss);
             }
           }
+          if (my_ones && ch == ones_ch) ss = fmaf(a0[0], a0[0], ss);   // ||b_i||^2, once per row
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -203,6 +216,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     // MMA completed), then write whole rows so the stores coalesce; every epilogue warp
     // passes the barrier
     const int row = quarter * 32 + lane;
+    const int et = threadIdx.x - 32 * kEpiFirst;      // 0..255
     float* stg = reinterpret_cast<float*>(smem);
     if (ok) {
 #pragma unroll
@@ -212,6 +226,8 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     }
     asm volatile("bar.sync 2, %0;" ::"r"(32 * kEpiWarps) : "memory");
     if (*abort) return;
+    if (ones_slot >= 0 && P.part_db && et < BM && m0 + et < P.p)      // sum_i c_i b_i of row et
+      P.part_db[(size_t)blockIdx.z * P.p + m0 + et] = stg[et * PSTR + ones_slot * 64];
     const int nc4 = nitems * 16;                      // float4s per row of this tile
     for (int item = threadIdx.x - 32 * kEpiFirst; item < BM * nc4; item += 32 * kEpiWarps) {
       const int r = item / nc4, c4 = item - r * nc4;
@@ -245,10 +261,21 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
   Ctl* c = reinterpret_cast<Ctl*>(smem + STAGES * STAGE);
   const int warp = threadIdx.x >> 5;
   const int m0 = blockIdx.x * BM, q0 = blockIdx.y * 4;
-  const int nitems = min(4, P.items - q0);
+  const int nitems = max(0, min(4, P.items - q0));
+  // the ones block follows the last im2col block (a tile of its own when that tile is full)
+  const int ones_slot = (P.bias && P.items >= q0 && P.items < q0 + 4) ? P.items - q0 : -1;
+  const int nblocks = nitems + (ones_slot >= 0 ? 1 : 0);
   const int e0 = blockIdx.z * P.ex_per_split;
   const int e1 = min(P.B, e0 + P.ex_per_split);
 
+  if (ones_slot >= 0) {   // constant ones in that block of every stage buffer (bf16 1.0 = 0x3F80)
+    for (int q = threadIdx.x; q < STAGES * (BOX / 16); q += blockDim.x) {
+      const int s = q / (BOX / 16), o = q % (BOX / 16);
+      reinterpret_cast<uint4*>(smem + s * STAGE + (2 + ones_slot) * BOX)[o] =
+          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    }
+    ptx::fence_proxy_async_smem();         // visible to the tensor core
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&c->full[s], 1);
@@ -274,110 +301,16 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
 
   if (warp >= kEpiFirst) {
     ptx::regs_inc<216>();
-    epilogue<kNorm>(P, smem, c, tmem, e0, e1, m0, q0, nitems);
+    epilogue<kNorm>(P, smem, c, tmem, e0, e1, m0, q0, nitems, ones_slot);
     finish(c, tmem);
   } else {
     ptx::regs_dec<64>();
     if (warp == 0 || warp == 2)
       producer(P, &mapG, &mapX, smem, c, e0, e1, m0, q0, nitems, warp >> 1);
     else if (warp == 1)
-      mma_issuer(P, smem, c, tmem, e0, e1);
+      mma_issuer(P, smem, c, tmem, e0, e1, nblocks);
     finish(c, tmem);
   }
-}
-
-// Bias part, from the NCHW output gradient (rows of T contiguous pixels, T % 8 == 0).
-//   norm: out[i] = sum_j (sum_t G[i, j, t])^2            (one block per example)
-//   sum:  part[split, j] = sum_{i in split} c_i sum_t G[i, j, t]   (one warp per row j)
-__global__ void conv_bias_norm_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
-                                      float* __restrict__ out) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float red[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = blockIdx.x; i < B; i += gridDim.x) {
-    float acc = 0.f;
-    for (int j = warp; j < p; j += 8) {
-      const __nv_bfloat16* row = G + ((size_t)i * p + j) * T;
-      float s = 0.f;
-      for (int t = lane * 8; t < T; t += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + t);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(h[q]);
-          s += f.x + f.y;
-        }
-      }
-      s = warp_sum(s);
-      acc = fmaf(s, s, acc);
-    }
-    if (lane == 0) red[warp] = acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float t = 0.f;
-      for (int w = 0; w < 8; ++w) t += red[w];
-      out[i] = t;
-    }
-    __syncthreads();
-  }
-}
-
-__global__ void conv_bias_sum_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
-                                     const float* __restrict__ factors, int ex_per_split,
-                                     float* __restrict__ part) {
-  pdl_trigger();
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x * 8 + warp;
-  if (j >= p) return;
-  const int i0 = blockIdx.y * ex_per_split, i1 = min(B, i0 + ex_per_split);
-  float acc = 0.f;
-  // four examples in flight per pass (independent loads), summed in example order
-  for (int ib = i0; ib < i1; ib += 4) {
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (ib + u >= i1) break;
-      const __nv_bfloat16* row = G + ((size_t)(ib + u) * p + j) * T;
-      for (int t = lane * 8; t < T; t += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + t);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(h[q]);
-          s[u] += f.x + f.y;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float su = warp_sum(s[u]);
-      if (ib + u < i1) acc = fmaf(__ldg(factors + ib + u), su, acc);
-    }
-  }
-  if (lane == 0) part[(size_t)blockIdx.y * p + j] = acc;
-}
-
-// As conv_bias_sum_kernel for rows whose length is not a multiple of 8 (scalar loads).
-__global__ void conv_bias_sum_scalar_kernel(const __nv_bfloat16* __restrict__ G, int B, int p, int T,
-                                            const float* __restrict__ factors, int ex_per_split,
-                                            float* __restrict__ part) {
-  pdl_trigger();
-  pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x * 8 + warp;
-  if (j >= p) return;
-  const int i0 = blockIdx.y * ex_per_split, i1 = min(B, i0 + ex_per_split);
-  float acc = 0.f;
-  for (int i = i0; i < i1; ++i) {
-    const __nv_bfloat16* row = G + ((size_t)i * p + j) * T;
-    float s = 0.f;
-    for (int t = lane; t < T; t += 32) s += __bfloat162float(row[t]);
-    s = warp_sum(s);
-    acc = fmaf(__ldg(factors + i), s, acc);
-  }
-  if (lane == 0) part[(size_t)blockIdx.y * p + j] = acc;
 }
 
 // dW[j, m] (+)= sum_s part[s, j, n(m)] in split order; n(m) maps the weight column
@@ -433,7 +366,7 @@ static ConvPlan conv_plan(const Geom& g, bool norm) {
   ConvPlan c;
   c.items = g.k * g.k * (g.Cin / 64);
   c.tm = cdiv_c(g.p, tcconv::BM);
-  c.tn = cdiv_c(c.items, 4);
+  c.tn = cdiv_c(c.items + (g.has_bias ? 1 : 0), 4);   // + the ones block of the bias
   c.tiles = c.tm * c.tn;
   const long want = std::max<long>(1, std::min<long>(g.B, 152 / c.tiles));
   c.eps = cdiv_c(g.B, want);
@@ -445,13 +378,10 @@ static ConvPlan conv_plan(const Geom& g, bool norm) {
 // NHWC copy of the input, then the kernel's partials.
 static size_t nhwc_bytes(const Geom& g) { return al256((size_t)g.B * g.H * g.W * g.Cin * 2); }
 
-static constexpr int kBiasSplits = 64;
-
 size_t tc_conv_ws_bytes(const Geom& g, bool norm) {
   const ConvPlan c = conv_plan(g, norm);
-  if (norm) return nhwc_bytes(g) + al256((size_t)(c.tiles + 1) * g.B * 4);
-  const int bsplits = std::min(g.B, kBiasSplits);
-  return nhwc_bytes(g) + al256((size_t)c.splits * g.p * c.items * 64 * 4) + al256((size_t)bsplits * g.p * 4);
+  if (norm) return nhwc_bytes(g) + al256((size_t)c.tiles * g.B * 4);
+  return nhwc_bytes(g) + al256((size_t)c.splits * g.p * c.items * 64 * 4) + al256((size_t)c.splits * g.p * 4);
 }
 
 // im2col map over the NHWC copy [B, H, W, Cin]: the bounding box's corners are the
@@ -535,16 +465,10 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
   if (!encode_maps(g, Xh, G, &mG, &mX)) return cudaErrorInvalidValue;
   tcconv::Params P = base_params(g, c, status);
   P.part = part;
+  P.bias = g.has_bias;
   e = launch_kernel<true>(g, c, mG, mX, P, s);
   if (e != cudaSuccess) return e;
-  int rows = c.tiles;
-  if (g.has_bias) {
-    launch_plain(tcconv::conv_bias_norm_kernel, std::min(g.B, 152 * 8), 256, 0, s, static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T, part + (size_t)c.tiles * g.B);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    rows += 1;
-  }
-  return launch_reduce_splits(part, rows, (size_t)g.B, out, 0, s);
+  return launch_reduce_splits(part, c.tiles, (size_t)g.B, out, 0, s);
 }
 
 cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
@@ -561,30 +485,14 @@ cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, cons
   tcconv::Params P = base_params(g, c, status);
   P.factors = factors;
   P.part = part;
+  P.part_db = db ? part_db : nullptr;
+  P.bias = g.has_bias;                       // the plan's tiles include the ones block
   e = launch_kernel<false>(g, c, mG, mX, P, s);
   if (e != cudaSuccess) return e;
   e = launch_conv_reduce(part, c.splits, g.p, c.items * 64, g.k * g.k, dW, accumulate, s);
   if (e != cudaSuccess || !db) return e;
-  return launch_conv_bias_sum(g, G, factors, db, accumulate, part_db, s);
+  return launch_reduce_splits(part_db, c.splits, (size_t)g.p, db, accumulate, s);
 }
 
-size_t conv_bias_sum_ws_bytes(const Geom& g) { return al256((size_t)std::min(g.B, kBiasSplits) * g.p * 4); }
-
-cudaError_t launch_conv_bias_sum(const Geom& g, const void* G, const float* factors, float* db, int accumulate,
-                                 float* part, cudaStream_t s) {
-  const int bsplits = std::min(g.B, kBiasSplits);
-  const int beps = cdiv_c(g.B, bsplits);
-  dim3 bgrid(cdiv_c(g.p, 8), cdiv_c(g.B, beps));
-  if (g.T % 8 == 0) {
-    launch_plain(tcconv::conv_bias_sum_kernel, bgrid, 256, 0, s, static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
-                                                       factors, beps, part);
-  } else {
-    launch_plain(tcconv::conv_bias_sum_scalar_kernel, bgrid, 256, 0, s, static_cast<const __nv_bfloat16*>(G), g.B, g.p, g.T,
-                                                              factors, beps, part);
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_reduce_splits(part, (int)bgrid.y, (size_t)g.p, db, accumulate, s);
-}
 
 }  // namespace dph

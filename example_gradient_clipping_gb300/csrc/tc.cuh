@@ -47,11 +47,6 @@ cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* ds
 cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
                                int accumulate, float* bias_part, cudaStream_t s);
 size_t scaled_rows_bias_bytes(int B, int T, int p);
-// db (+)= sum_i c_i sum_t G[i, j, t] from the NCHW output gradient (fp32, fixed order);
-// part holds min(B, 64) * p floats.
-cudaError_t launch_conv_bias_sum(const Geom& g, const void* G, const float* factors, float* db, int accumulate,
-                                 float* part, cudaStream_t s);
-size_t conv_bias_sum_ws_bytes(const Geom& g);
 // Conv layers with the unfold done by TMA im2col loads (Cin % 64 == 0, T % 8 == 0, T >= 64):
 // instantiated norm and clipped sum; the workspace holds an NHWC copy of the input.
 bool tc_conv_supported(const Geom& g);

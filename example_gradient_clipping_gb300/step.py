@@ -122,3 +122,73 @@ class ClipStep:
         self.sums(inputs, stream)
         self.noise(seed, stream)
         return self.grad
+
+
+class ClipPipeline:
+    """Privatised-gradient steps over batches that arrive in pinned host memory.
+
+    Two ClipSteps with their own device input buffers alternate.  The step for batch k
+    is one CUDA graph: norms, factors, clipped sums and noise on buffer set k % 2, the
+    gradient copied back to pinned host memory, and, on a forked stream inside the same
+    graph, the copy of batch k+1 from host_inputs(k+1) into the other buffer set, which
+    overlaps the compute.  So one graph launch per step drives copies and kernels.
+
+    Use: fill host_inputs(0), call start(); then for each k fill host_inputs(k+1) and
+    call step(k, seed); the gradient of batch k is in the returned pinned tensor once
+    the stream reaches that point (it is reused by step k+2).  Results are exactly those
+    of ClipStep.run on the same batches and seeds.
+    """
+
+    def __init__(self, descs, shapes, dtype, C, sigma: float, per_layer: bool = False, device: str = "cuda"):
+        import torch
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        dev = torch.device(device)
+        self.steps = [ClipStep(descs, C=C, sigma=sigma, per_layer=per_layer, device=str(dev)) for _ in range(2)]
+        self.dev_in = [[(torch.zeros(a, dtype=tdt, device=dev), torch.zeros(g, dtype=tdt, device=dev))
+                        for a, g in shapes] for _ in range(2)]
+        self.host_in = [[(torch.zeros(a, dtype=tdt).pin_memory(), torch.zeros(g, dtype=tdt).pin_memory())
+                         for a, g in shapes] for _ in range(2)]
+        self.n_params = self.steps[0].n_params
+        self.out_host = [torch.empty(self.n_params, dtype=torch.float32).pin_memory() for _ in range(2)]
+        n0 = dp_launch_count()
+        for st, inp in zip(self.steps, self.dev_in):
+            st.run(inp, seed=0)                 # per-device state resolved outside capture
+        torch.cuda.synchronize()
+        self.side = torch.cuda.Stream(dev)
+        self.graphs = []
+        for b in range(2):
+            st, cur, nxt = self.steps[b], self.dev_in[b], 1 - b
+            g = torch.cuda.CUDAGraph()
+            n0 = dp_launch_count()
+            with torch.cuda.graph(g):
+                cap = torch.cuda.current_stream()
+                self.side.wait_stream(cap)
+                with torch.cuda.stream(self.side):      # the next batch's inputs, alongside
+                    for (ha, hg), (da, dg) in zip(self.host_in[nxt], self.dev_in[nxt]):
+                        da.copy_(ha, non_blocking=True)
+                        dg.copy_(hg, non_blocking=True)
+                st.norms(cur)
+                st.factors_()
+                st.sums(cur)
+                st.noise_devseed()
+                self.out_host[b].copy_(st.grad, non_blocking=True)
+                cap.wait_stream(self.side)
+            self.graph_kernels = dp_launch_count() - n0
+            self.graphs.append(g)
+
+    def host_inputs(self, k: int):
+        """The pinned (A, G) buffers per layer that batch k is read from."""
+        return self.host_in[k & 1]
+
+    def start(self) -> None:
+        """Copy batch 0 from host_inputs(0) to the device (the graphs copy every later one)."""
+        for (ha, hg), (da, dg) in zip(self.host_in[0], self.dev_in[0]):
+            da.copy_(ha, non_blocking=True)
+            dg.copy_(hg, non_blocking=True)
+
+    def step(self, k: int, seed: int):
+        """Batch k's step on the current stream; prefetches batch k+1 from host_inputs(k+1)."""
+        b = k & 1
+        self.steps[b].seed_buf.fill_(int(seed))
+        self.graphs[b].replay()
+        return self.out_host[b]

@@ -197,6 +197,9 @@ EDGE = [
      2, "bf16"),
     ("conv_im2col_k5_nobias", LayerSpec("e", "conv2d", p=64, Cin=64, H=12, W=12, k=5, has_bias=False,
                                         a_dist="abs_normal"), 3, "bf16"),
+    # one row block (64 < T <= 128): the ghost norm with single-block pairs
+    ("lin_ghost_split", LayerSpec("e", "linear", p=136, d=200, T=100), 3, "bf16"),
+    ("conv_im2col_ghost_split", LayerSpec("e", "conv2d", p=72, Cin=64, H=10, W=10, k=3, pad=1), 2, "bf16"),
 ]
 
 
@@ -346,3 +349,37 @@ def test_adaptive_bound_matches_oracle(lib):
         rc, rcl2 = oracle.adaptive_bound(s.astype(np.float64), C_l2, 1.1, 2.0, 2.5, 7, layer)
         assert c == pytest.approx(rc, rel=1e-5, abs=1e-6)
         assert cl2 == pytest.approx(rcl2, rel=1e-5, abs=1e-6)
+
+
+def test_pipeline_matches_step(lib):
+    """ClipPipeline (one graph per step, next batch copied alongside) gives ClipStep.run's result."""
+    import torch
+    dp = lib
+    spec = LayerSpec("e", "linear", p=96, d=80, T=70)
+    spec2 = LayerSpec("f", "linear", p=40, d=24, T=1)
+    wls = [Workload(name=f"pipe{k}", B=6, layers=(spec, spec2), dtype="bf16", C=1.0, sigma=0.8, seed=20 + k)
+           for k in range(4)]
+    descs = [desc_for(dp, s_, 6, "bf16") for s_ in (spec, spec2)]
+    host = []
+    for wl in wls:
+        host.append([tuple(workloads.to_torch(x, "bf16") for x in workloads.layer_inputs(wl, l)) for l in range(2)])
+    shapes = [(tuple(a.shape), tuple(g.shape)) for a, g in host[0]]
+    pipe = dp.ClipPipeline(descs, shapes, "bf16", C=1.0, sigma=0.8)
+
+    def fill(k):
+        for (ha, hg), (a, g) in zip(pipe.host_inputs(k), host[k]):
+            ha.copy_(a)
+            hg.copy_(g)
+    fill(0)
+    pipe.start()
+    got = []
+    for k in range(3):
+        fill(k + 1)                 # the step copies batch k+1 while it computes batch k
+        out = pipe.step(k, 1000 + k)
+        torch.cuda.synchronize()
+        got.append(out.clone())
+    ref = dp.ClipStep(descs, C=1.0, sigma=0.8)
+    for k in range(3):
+        want = ref.run([(a.cuda(), g.cuda()) for a, g in host[k]], seed=1000 + k).cpu()
+        torch.cuda.synchronize()
+        assert torch.equal(got[k], want), k
