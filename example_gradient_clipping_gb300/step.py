@@ -139,6 +139,8 @@ class ClipPipeline:
     of ClipStep.run on the same batches and seeds.
     """
 
+    kCopyLanes = 1
+
     def __init__(self, descs, shapes, dtype, C, sigma: float, per_layer: bool = False, device: str = "cuda"):
         import torch
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
@@ -154,7 +156,9 @@ class ClipPipeline:
         for st, inp in zip(self.steps, self.dev_in):
             st.run(inp, seed=0)                 # per-device state resolved outside capture
         torch.cuda.synchronize()
-        self.side = torch.cuda.Stream(dev)
+        # the next batch's copy runs on kCopyLanes forked streams, each taking a slice of
+        # every tensor (one lane measured fastest on GB300: four lanes lowered the rate)
+        self.side = [torch.cuda.Stream(dev) for _ in range(self.kCopyLanes)]
         self.graphs = []
         for b in range(2):
             st, cur, nxt = self.steps[b], self.dev_in[b], 1 - b
@@ -162,17 +166,22 @@ class ClipPipeline:
             n0 = dp_launch_count()
             with torch.cuda.graph(g):
                 cap = torch.cuda.current_stream()
-                self.side.wait_stream(cap)
-                with torch.cuda.stream(self.side):      # the next batch's inputs, alongside
-                    for (ha, hg), (da, dg) in zip(self.host_in[nxt], self.dev_in[nxt]):
-                        da.copy_(ha, non_blocking=True)
-                        dg.copy_(hg, non_blocking=True)
+                for lane, sd in enumerate(self.side):
+                    sd.wait_stream(cap)
+                    with torch.cuda.stream(sd):
+                        for (ha, hg), (da, dg) in zip(self.host_in[nxt], self.dev_in[nxt]):
+                            for h, d_ in ((ha, da), (hg, dg)):
+                                n = h.numel()
+                                lo, hi = n * lane // self.kCopyLanes, n * (lane + 1) // self.kCopyLanes
+                                if hi > lo:
+                                    d_.view(-1)[lo:hi].copy_(h.view(-1)[lo:hi], non_blocking=True)
                 st.norms(cur)
                 st.factors_()
                 st.sums(cur)
                 st.noise_devseed()
                 self.out_host[b].copy_(st.grad, non_blocking=True)
-                cap.wait_stream(self.side)
+                for sd in self.side:
+                    cap.wait_stream(sd)
             self.graph_kernels = dp_launch_count() - n0
             self.graphs.append(g)
 
