@@ -109,6 +109,13 @@ __device__ __forceinline__ void normal4(uint64_t q, uint64_t seed, uint32_t stre
   z[0] = r01 * c1; z[1] = r01 * s1; z[2] = r23 * c3; z[3] = r23 * s3;
 }
 
+// One vector of split partials: split k at ws + k*stride (n floats), summed into out.
+struct SplitSeg {
+  const float* ws;
+  size_t stride, n;
+  float* out;
+};
+
 }  // namespace dpk
 
 // Host-side launchers implemented by the kernel translation units.
@@ -168,6 +175,9 @@ cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alph
 // out[e] (+)= sum_k ws[k*n + e], fixed order.
 cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
                                  cudaStream_t s);
+// The weight and bias reductions of one clipped sum in one launch (segments: dpk::SplitSeg).
+using dpk::SplitSeg;
+cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumulate, cudaStream_t s);
 // SIMT (FFMA) paths: any dtype/shape.
 size_t simt_sum_splits(const Geom& g);
 cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, const void* G,

@@ -324,9 +324,9 @@ cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G
                                                       factors, eps, part_w, part_b, acc);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || direct) return e;
-  e = launch_reduce_splits(part_w, splits, (size_t)g.p * g.d, dW, accumulate, s);
-  if (e != cudaSuccess || !db) return e;
-  return launch_reduce_splits(part_b, splits, (size_t)g.p, db, accumulate, s);
+  const size_t nw = (size_t)g.p * g.d;
+  return launch_reduce_splits2(SplitSeg{part_w, nw, nw, dW}, SplitSeg{part_b, (size_t)g.p, db ? (size_t)g.p : 0, db},
+                               splits, accumulate, s);
 }
 
 }  // namespace dph

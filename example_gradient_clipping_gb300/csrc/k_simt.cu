@@ -136,6 +136,58 @@ __global__ void reduce_splits_kernel(const float* __restrict__ ws, int splits, s
   }
 }
 
+// Two segments (the weight and the bias of one layer) in one pass; V = 4: float4 items
+// (every base 16-byte aligned, strides and lengths multiples of 4), V = 1: floats.  Each
+// element adds its splits in ascending order, eight loads in flight.
+template <int V>
+__global__ void reduce_splits2_kernel(SplitSeg a, SplitSeg b, int splits, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
+  const size_t ia = a.n / V, items = ia + b.n / V;
+  for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+       it += (size_t)gridDim.x * blockDim.x) {
+    const bool first = it < ia;
+    const size_t off = (first ? it : it - ia) * V;
+    const float* src = (first ? a.ws : b.ws) + off;
+    const size_t stride = first ? a.stride : b.stride;
+    float* out = (first ? a.out : b.out) + off;
+    float acc[V];
+    if (accumulate) {
+      if constexpr (V == 4) {
+        const float4 o = *reinterpret_cast<const float4*>(out);
+        acc[0] = o.x; acc[1] = o.y; acc[2] = o.z; acc[3] = o.w;
+      } else {
+        acc[0] = out[0];
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] = 0.f;
+    }
+    for (int k0 = 0; k0 < splits; k0 += 8) {
+      float v[8][V];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (k0 + j >= splits) break;
+        const float* p = src + (size_t)(k0 + j) * stride;
+        if constexpr (V == 4) {
+          const float4 t = *reinterpret_cast<const float4*>(p);
+          v[j][0] = t.x; v[j][1] = t.y; v[j][2] = t.z; v[j][3] = t.w;
+        } else {
+          v[j][0] = p[0];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (k0 + j >= splits) break;
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] += v[j][q];
+      }
+    }
+    if constexpr (V == 4) *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    else out[0] = acc[0];
+  }
+}
+
 // Many splits of a short vector: one warp per element, lanes stride over the splits,
 // then a fixed butterfly (deterministic).
 __global__ void reduce_splits_warp_kernel(const float* __restrict__ ws, int splits, size_t n,
@@ -357,6 +409,26 @@ cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* o
   }
   const size_t blocks = std::min<size_t>((n + 255) / 256, 152 * 8);
   launch_pdl(reduce_splits_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumulate, cudaStream_t s) {
+  if (!b.out) b.n = 0;
+  if (splits >= 16 && std::max(a.n, b.n) <= ((size_t)1 << 16)) {
+    // many splits of short vectors: the warp- and block-per-element kernels (packed layouts)
+    cudaError_t e = launch_reduce_splits(a.ws, splits, a.n, a.out, accumulate, s);
+    if (e != cudaSuccess || !b.n) return e;
+    if (b.stride == b.n) return launch_reduce_splits(b.ws, splits, b.n, b.out, accumulate, s);
+    a.n = 0;   // a strided bias segment: the kernel below takes it alone
+  }
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  const bool v4 = al(a.ws) && al(a.out) && al(b.ws) && al(b.out) && a.stride % 4 == 0 && a.n % 4 == 0 &&
+                  b.stride % 4 == 0 && b.n % 4 == 0;
+  const size_t items = v4 ? (a.n + b.n) / 4 : a.n + b.n;
+  if (!items) return cudaSuccess;
+  const unsigned blocks = (unsigned)std::min<size_t>((items + 255) / 256, 152 * 8);
+  if (v4) launch_pdl(reduce_splits2_kernel<4>, blocks, 256, 0, s, a, b, splits, accumulate);
+  else launch_pdl(reduce_splits2_kernel<1>, blocks, 256, 0, s, a, b, splits, accumulate);
   return cudaGetLastError();
 }
 

@@ -434,8 +434,12 @@ static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtens
   launch_pdl(tcsum::tc_sum_kernel, grid, tcsum::kThreads, tcsum::SMEM, s, mg, ma, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = g.conv ? launch_conv_reduce(ws, splits, g.p, g.D, g.k * g.k, dW, accumulate, s)
-             : launch_reduce_splits(ws, splits, (size_t)g.p * g.D, dW, accumulate, s);
+  if (!g.conv) {
+    const size_t nw = (size_t)g.p * g.D;
+    return launch_reduce_splits2(SplitSeg{ws, nw, nw, dW},
+                                 SplitSeg{P.ws_db, (size_t)g.p, P.ws_db ? (size_t)g.p : 0, db}, splits, accumulate, s);
+  }
+  e = launch_conv_reduce(ws, splits, g.p, g.D, g.k * g.k, dW, accumulate, s);
   if (e != cudaSuccess) return e;
   if (P.ws_db) e = launch_reduce_splits(P.ws_db, splits, (size_t)g.p, db, accumulate, s);
   return e;

@@ -699,9 +699,9 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   cudaError_t e = cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false>, mg64, ma64, mg16, ma16, P);
   count_launch();
   if (e != cudaSuccess || !gsplits) return e;
-  e = launch_reduce_splits(part_w, gsplits, (size_t)g.p * g.D, dW, accumulate, s);
-  if (e != cudaSuccess || !db) return e;
-  return launch_reduce_splits(part_b, gsplits, (size_t)g.p, db, accumulate, s);
+  const size_t nw = (size_t)g.p * g.D;
+  return launch_reduce_splits2(SplitSeg{part_w, nw, nw, dW}, SplitSeg{part_b, (size_t)g.p, db ? (size_t)g.p : 0, db},
+                               gsplits, accumulate, s);
 }
 
 // Instantiated norm on the tensor cores: per-tile partials [tiles, B] in the workspace,
