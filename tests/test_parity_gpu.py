@@ -200,6 +200,10 @@ EDGE = [
     # one row block (64 < T <= 128): the ghost norm with single-block pairs
     ("lin_ghost_split", LayerSpec("e", "linear", p=136, d=200, T=100), 3, "bf16"),
     ("conv_im2col_ghost_split", LayerSpec("e", "conv2d", p=72, Cin=64, H=10, W=10, k=3, pad=1), 2, "bf16"),
+    # one row block: T just above the packed limit, batches of about half the SM count
+    ("lin_ghost_slab_T65", LayerSpec("e", "linear", p=40, d=48, T=65), 5, "bf16"),
+    ("lin_ghost_slab_B76", LayerSpec("e", "linear", p=64, d=72, T=128), 76, "bf16"),
+    ("lin_ghost_B77", LayerSpec("e", "linear", p=64, d=72, T=128, has_bias=False), 77, "bf16"),
 ]
 
 
