@@ -131,7 +131,7 @@ class ClockSampler:
 
 
 # Kernel that serves each call on the bench workload's tensor-core path.
-_DOMINANT_KERNELS = {"sums": ["tc_sumx_kernel", "tc_sum_kernel"], "norms": ["tc_ghost_kernel"],
+_DOMINANT_KERNELS = {"sums": ["tc_sum2_kernel", "tc_sumx_kernel", "tc_sum_kernel"], "norms": ["tc_ghost_kernel"],
                      "noise": ["add_noise_kernel"], "factors": ["clip_factors_kernel"]}
 
 

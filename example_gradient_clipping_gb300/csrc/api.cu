@@ -142,18 +142,22 @@ bool tc_inputs(const Geom& g, int dtype, const void* A, const void* G, const voi
   return !g.conv || aligned16(ws);
 }
 
-// DPCLIP_SUM_KERNEL=rows|example pins the tensor-core clipped-sum kernel where the
-// shape allows it (both compute the same sum; used by the tests and for tuning).
+// DPCLIP_SUM_KERNEL=rows|example|pair pins the tensor-core clipped-sum kernel where the
+// shape allows it (all compute the same sum; used by the tests and for tuning).  The
+// CTA-pair kernel is only taken when pinned: on the sequence and ViT MLP layers it ran
+// 1.4-1.5x slower than the per-example single-CTA kernel.
 int pinned_sum_kernel() {
   const char* v = std::getenv("DPCLIP_SUM_KERNEL");
   if (!v) return 0;
   if (!std::strcmp(v, "rows")) return 1;
   if (!std::strcmp(v, "example")) return 2;
+  if (!std::strcmp(v, "pair")) return 6;
   return 0;
 }
 
 int sum_kernel_for(const Geom& lg) {
   const int pin = pinned_sum_kernel();
+  if (pin == 6 && dph::tc_sum2_supported(lg)) return 6;
   if (pin == 2 && dph::tc_sumx_supported(lg)) return 2;
   if (pin == 1 && dph::tc_sum_supported(lg)) return 1;
   const long tiles = (long)((lg.p + 127) / 128) * ((lg.D + 255) / 256);
@@ -224,6 +228,7 @@ size_t sum_ws_bytes(const Geom& g, const Plan& pl) {
   const size_t inner = pl.kernel == 5   ? dph::t1_sum_ws_bytes(g)
                        : pl.kernel == 4 ? dph::tc_sum_conv_ws_bytes(g)
                        : pl.kernel == 3 ? dph::tc_conv_ws_bytes(g, false)
+                       : pl.kernel == 6 ? dph::tc_sum2_ws_bytes(lg)
                        : pl.kernel == 2 ? dph::tc_sumx_ws_bytes(lg)
                        : pl.kernel == 1 ? align256(dph::tc_sum_ws_bytes(lg)) +
                                               (pl.rows ? dph::scaled_rows_bias_bytes(g.B, g.T, g.p) : 0)
@@ -276,6 +281,7 @@ size_t max_ws_bytes(const Geom& g, int mode) {
       n = std::max(n, pre + align256(dph::tc_sum_ws_bytes(lg)) +
                           (g.conv ? dph::scaled_rows_bias_bytes(g.B, g.T, g.p) : 0));
     if (dph::tc_sumx_supported(lg)) n = std::max(n, pre + dph::tc_sumx_ws_bytes(lg));
+    if (dph::tc_sum2_supported(lg)) n = std::max(n, pre + dph::tc_sum2_ws_bytes(lg));
   }
   return n;
 }
@@ -430,6 +436,8 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
     e = dph::launch_tc_sum_conv(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
   else if (pl.kernel == 3)
     e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
+  else if (pl.kernel == 6)
+    e = dph::launch_tc_sum2(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
   else if (pl.kernel == 2)
     e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
   else if (prescale) {

@@ -153,6 +153,38 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
+// Arrive on the mbarrier at the same offset in CTA `rank` of the cluster (release).
+__device__ __forceinline__ void mbar_arrive_rank(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(map_rank(smem_u32(bar), rank))
+               : "memory");
+}
+
+// mbar_wait for a phase completed by an arrival from another CTA of the cluster (a
+// remote arrive or a multicast tcgen05.commit), acquire at cluster scope, the same time
+// limit and abort handling.  It polls with test_wait: a thread suspended in try_wait was
+// measured to notice such an arrival only ~0.8 us later.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  unsigned* status) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (*abort) return false;
+    if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      if (status) atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -235,6 +267,41 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---- CTA pairs (cta_group::2): a cluster of two CTAs on two SMs shares one MMA ------
+// Every tcgen05 allocation, MMA and commit of a pair kernel uses the pair form.  The
+// allocation is collective: one warp of each CTA executes it, and both receive the same
+// TMEM address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+// D (+)= A * B over the pair, issued by the even CTA: M = 256 with rows [128r, 128r+128)
+// from CTA r's shared memory (and into CTA r's TMEM), N split the same way (columns
+// [N/2 r, N/2 (r+1)) of B from CTA r); both descriptors address the same offsets in both.
+__device__ __forceinline__ void umma_pair_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// Arrive once on `bar` in every CTA of `mask` when the pair MMAs issued so far completed.
+__device__ __forceinline__ void umma_pair_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+// The same, on this CTA's `bar` only.
+__device__ __forceinline__ void umma_pair_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
 
 // Shared-memory matrix descriptor (tcgen05 format) for a 128-byte-swizzled operand:
 // start address, leading- and stride-dimension byte offsets (>> 4), descriptor

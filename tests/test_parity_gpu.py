@@ -242,15 +242,18 @@ ACC = [(LayerSpec("e", "linear", p=42, d=72, T=9), 6),          # SIMT (p not a 
        (LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=3, pad=1), 3),  # conv, im2col row-scaled
        (LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 2),  # conv, im2col per example
        (LayerSpec("e", "linear", p=10, d=13, T=1), 300),                   # one row, 3 example splits
-       (LayerSpec("e", "linear", p=136, d=264, T=70), 11)]                 # per-example, grid splits
+       (LayerSpec("e", "linear", p=136, d=264, T=70), 11),                 # per-example, grid splits
+       (LayerSpec("e", "linear", p=256, d=256, T=64), 1),                  # CTA pairs, one split
+       (LayerSpec("e", "linear", p=264, d=200, T=70), 11)]                 # CTA pairs, grid splits
 
 
-ACC_PIN = ["", "rows", "example", "example", "", "", "", "", "example"]
+ACC_PIN = ["", "rows", "example", "example", "", "", "", "", "example", "pair", "pair"]
 
 
 @pytest.mark.parametrize("spec,B,pin", [(s, b, p) for (s, b), p in zip(ACC, ACC_PIN)],
                          ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single", "conv_padded",
-                              "conv_im2col_rows", "conv_im2col_example", "t1_splits", "tc_ex_grid"])
+                              "conv_im2col_rows", "conv_im2col_example", "t1_splits", "tc_ex_grid",
+                              "pair_single", "pair_grid"])
 def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
     if pin:
         monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
@@ -270,6 +273,23 @@ def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
     S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
     assert rel_vec(dW.cpu().numpy(), 0.25 + 2 * S.ravel()) <= TOL["bf16"]
     assert rel_vec(db.cpu().numpy(), -0.5 + 2 * Sb) <= TOL["bf16"]
+
+
+# The per-example clipped sum on CTA pairs (256 x 256 tiles): ragged p (the second pair's
+# odd CTA entirely past p), ragged D, 16-row tail stages, no bias, many grid splits.
+PAIR = [
+    ("pair_B1", LayerSpec("e", "linear", p=256, d=256, T=64), 1),
+    ("pair_ragged", LayerSpec("e", "linear", p=264, d=200, T=70), 11),
+    ("pair_T130_nobias", LayerSpec("e", "linear", p=384, d=136, T=130, has_bias=False), 3),
+    ("pair_many_splits", LayerSpec("e", "linear", p=256, d=512, T=64), 40),
+]
+
+
+@pytest.mark.parametrize("tag,spec,B", PAIR, ids=[e[0] for e in PAIR])
+def test_pair_sum_kernel(lib, tag, spec, B, monkeypatch):
+    monkeypatch.setenv("DPCLIP_SUM_KERNEL", "pair")
+    wl = Workload(name=tag, B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=13)
+    _check_layer(lib, spec, wl)
 
 
 def test_mixed_scale_factors_straddle_bound(lib):
