@@ -92,10 +92,17 @@ dp_status make_geom(const dp_layer_desc* d, Geom* g) {
 // is below the instantiation space p*D; ties instantiate; one row -> closed form.
 int resolve_mode(const Geom& g, int requested) {
   if (requested == DP_NORM_T1) return DP_NORM_T1;
+  const double T = g.T, p = g.p, D = g.D;
   if (requested == DP_NORM_AUTO) {
     if (g.T == 1 && !g.conv) return DP_NORM_T1;
-    const double ghost = 2.0 * (double)g.T * (double)g.T;
-    const double inst = (double)g.p * (double)g.D;
+    // space priority: the ghost norm's 2T^2 against the instantiated gradient's p*D
+    return 2.0 * T * T < p * D ? DP_NORM_GHOST : DP_NORM_INSTANTIATE;
+  }
+  if (requested == DP_NORM_AUTO_TIME) {
+    if (g.T == 1 && !g.conv) return DP_NORM_T1;
+    // speed priority: Gram products and Hadamard sum against the gradient and its square
+    const double ghost = 2.0 * T * T * D + 2.0 * T * T * p + 2.0 * T * T;
+    const double inst = 2.0 * T * p * D + 2.0 * p * D;
     return ghost < inst ? DP_NORM_GHOST : DP_NORM_INSTANTIATE;
   }
   return requested;
@@ -328,7 +335,7 @@ dp_status dp_plan(const dp_layer_desc* desc, int requested, int* chosen_mode, in
   Geom g;
   dp_status st = make_geom(desc, &g);
   if (st != DP_OK) return st;
-  if (requested < DP_NORM_AUTO || requested > DP_NORM_T1)
+  if (requested < DP_NORM_AUTO || requested > DP_NORM_AUTO_TIME)
     return fail(DP_ERR_INVALID_ARG, "norm mode %d unknown", requested);
   if (requested == DP_NORM_T1 && (g.T != 1 || g.conv))
     return fail(DP_ERR_INVALID_ARG, "DP_NORM_T1 needs a linear layer with T == 1 (T=%d)", g.T);
@@ -341,7 +348,7 @@ dp_status dp_plan(const dp_layer_desc* desc, int requested, int* chosen_mode, in
 size_t dp_workspace_size(const dp_layer_desc* desc, int mode) {
   Geom g;
   if (make_geom(desc, &g) != DP_OK) return 0;
-  if (mode < DP_NORM_AUTO || mode > DP_NORM_T1) return 0;
+  if (mode < DP_NORM_AUTO || mode > DP_NORM_AUTO_TIME) return 0;
   if (mode == DP_NORM_T1 && (g.T != 1 || g.conv)) return 0;
   return max_ws_bytes(g, resolve_mode(g, mode));
 }

@@ -57,7 +57,10 @@ typedef enum {
   DP_NORM_AUTO = 0,          /* ghost iff 2T^2 < p*D (ties instantiate); T == 1 -> closed form */
   DP_NORM_GHOST = 1,         /* Gram identity: sum_{t,s} (a_t.a_s)(g_t.g_s) */
   DP_NORM_INSTANTIATE = 2,   /* g_i = G_i^T U(A_i) formed on chip, squared and summed */
-  DP_NORM_T1 = 3             /* one row: ||a||^2 ||g||^2 (reported; also accepted when T == 1) */
+  DP_NORM_T1 = 3,            /* one row: ||a||^2 ||g||^2 (reported; also accepted when T == 1) */
+  DP_NORM_AUTO_TIME = 4      /* speed priority ([MixGhost] section 4 with its Table 1 / Appendix C
+                                counts): ghost iff 2T^2 (D + p) + 2T^2 < 2TpD + 2pD (ties
+                                instantiate); T == 1 -> closed form.  Resolved, never reported. */
 } dp_norm_mode;
 
 /* One layer.  Linear uses B, T, d, p; conv2d uses B, Cin, H, W, p, k, stride, pad, dil
@@ -83,7 +86,8 @@ const char* dp_last_error(void);
 
 /* Host-only planner: validates `desc`, resolves `requested` (DP_NORM_AUTO applies the
  * layerwise rule of [MixGhost] eq. 4.1 -- the smaller of the ghost space 2T^2 and the
- * instantiation space p*D, Appendix F) and reports the rows T and width D of the
+ * instantiation space p*D, Appendix F; DP_NORM_AUTO_TIME compares the time counts
+ * instead) and reports the rows T and width D of the
  * per-example contraction.  Any output pointer may be NULL.  Needs no GPU. */
 dp_status dp_plan(const dp_layer_desc* desc, int requested, int* chosen_mode, int* rows_T,
                   int* width_D);

@@ -188,6 +188,23 @@ def norm_mode_plan(spec) -> str:
     return "ghost" if 2 * T * T < spec.p * spec.D else "instantiate"
 
 
+def norm_mode_plan_time(spec) -> str:
+    """Speed-priority variant of the layerwise choice ([MixGhost] section 4, the
+    version that compares time complexities; the counts are its Table 1 / Appendix C).
+
+    Per example: the ghost norm forms two T x T Grams (2T^2 D + 2T^2 p flop) and their
+    Hadamard sum (2T^2); instantiation forms the p x D gradient (2TpD) and squares
+    and sums it (2pD).  Ghost iff its count is strictly smaller; ties instantiate.
+    One row (T=1) uses the outer-product closed form.
+    """
+    T, p, D = spec.rows, spec.p, spec.D
+    if T == 1:
+        return "t1"
+    ghost = 2 * T * T * D + 2 * T * T * p + 2 * T * T
+    inst = 2 * T * p * D + 2 * p * D
+    return "ghost" if ghost < inst else "instantiate"
+
+
 def dp_step(wl, inputs: List, seed: Optional[int] = None, C: Optional[Sequence[float]] = None,
             per_layer: Optional[bool] = None) -> Dict:
     """One privatised gradient: norms -> factors -> clipped sums -> noise, 1/B.

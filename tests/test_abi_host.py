@@ -64,6 +64,25 @@ def test_planner_on_workloads(dp, name, mode):
         assert dp.dp_workspace_size(desc_for(dp, spec, wl.B, wl.dtype)) > 0
 
 
+@pytest.mark.parametrize("name", ["t1_linear_b32", "seq_linear_b64_t128", "conv3x3_b256", "vgg11_cifar_b1024",
+                                  "vit_mlp_b4096_t197"])
+def test_speed_priority_plan_matches_oracle(dp, name):
+    import oracle
+    import workloads
+    from helpers import desc_for
+    wl = workloads.get_workload(name)
+    for spec in wl.layers:
+        m, T, D = dp.dp_plan(desc_for(dp, spec, wl.B, wl.dtype), dp.DP_NORM_AUTO_TIME)
+        assert dp.MODE_NAMES[m] == oracle.dpsgd.norm_mode_plan_time(spec) and (T, D) == (spec.rows, spec.D)
+        assert dp.dp_workspace_size(desc_for(dp, spec, wl.B, wl.dtype), dp.DP_NORM_AUTO_TIME) > 0
+
+
+def test_speed_and_space_priority_part_ways(dp):
+    d = dp.layer_desc(dp.DP_LINEAR, dp.DP_BF16, B=2, p=256, T=150, d=256)
+    assert dp.dp_plan(d)[0] == dp.DP_NORM_GHOST
+    assert dp.dp_plan(d, dp.DP_NORM_AUTO_TIME)[0] == dp.DP_NORM_INSTANTIATE
+
+
 def test_ties_instantiate(dp):
     # 2T^2 == p*D: T=4 -> 32 = p*D with p=4, d=8
     d = dp.layer_desc(dp.DP_LINEAR, dp.DP_BF16, B=2, p=4, T=4, d=8)

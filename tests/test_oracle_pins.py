@@ -396,3 +396,29 @@ def test_layerwise_decision_golden():
         assert (spec.name, spec.rows, spec.D, spec.p) == (name, int(T), int(D), int(p))
         assert 2 * spec.rows ** 2 == int(ghost_space) and spec.p * spec.D == int(inst_space)
         assert dpsgd.norm_mode_plan(spec) == mode
+
+
+def test_speed_priority_counts_match_loop_nests():
+    """The speed-priority plan's per-example counts, pinned by counting the arithmetic of
+    the two algorithms as plain loop nests on tiny shapes (multiply and add = 2 flop)."""
+    T, p, D = 3, 2, 4
+    ghost = 0
+    for _ in range(T):
+        for _ in range(T):
+            ghost += 2 * D          # (U U^T)_{ts}: D multiply-adds
+            ghost += 2 * p          # (G G^T)_{ts}: p multiply-adds
+            ghost += 2              # Hadamard product term, accumulated
+    inst = 0
+    for _ in range(p):
+        for _ in range(D):
+            inst += 2 * T           # g[a, b] = sum_t G[t, a] U[t, b]
+            inst += 2               # g[a, b]^2, accumulated
+    spec = LayerSpec("x", "linear", p=p, d=D, T=T)
+    want = "ghost" if ghost < inst else "instantiate"
+    assert dpsgd.norm_mode_plan_time(spec) == want
+    # the space and speed rules part ways: T=150, p=D=256 -> space 2T^2 = 45000 < 65536
+    # (ghost); time 23,085,000 flop (ghost) > 19,791,872 flop (instantiate)
+    spec = LayerSpec("y", "linear", p=256, d=256, T=150)
+    assert dpsgd.norm_mode_plan(spec) == "ghost"
+    assert dpsgd.norm_mode_plan_time(spec) == "instantiate"
+    assert dpsgd.norm_mode_plan_time(LayerSpec("z", "linear", p=8, d=8, T=1)) == "t1"

@@ -292,6 +292,15 @@ def test_pair_sum_kernel(lib, tag, spec, B, monkeypatch):
     _check_layer(lib, spec, wl)
 
 
+def test_speed_priority_mode(lib):
+    """DP_NORM_AUTO_TIME resolves by the time counts (here: instantiate, where the space
+    rule would take the ghost norm) and gives the oracle's norms."""
+    spec = LayerSpec("e", "linear", p=256, d=256, T=150)
+    wl = Workload(name="speed", B=3, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=21)
+    got = _check_layer(lib, spec, wl, mode=lib.DP_NORM_AUTO_TIME)
+    assert got["chosen"] == lib.DP_NORM_INSTANTIATE
+
+
 def test_mixed_scale_factors_straddle_bound(lib):
     """Some examples under C (factor exactly 1), some over; flat clipping over two layers."""
     import torch
