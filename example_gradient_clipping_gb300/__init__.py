@@ -61,6 +61,7 @@ def _load():
         "dp_add_noise_devseed": (c_int, [c_void, c_size, c_f, c_f, c_int, c_void, c_u64, c_void]),
         "dp_adaptive_bound": (c_int, [c_void, c_int, c_f, c_f, c_f, c_f, c_u64, c_int, c_void, c_void]),
         "dp_check_status": (c_int, [c_void]),
+        "dp_selftest_wait_timeout": (c_int, [c_void, c_void]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -169,9 +170,15 @@ def dp_adaptive_bound(sqnorms, B: int, C_l2: float, alpha: float, beta: float, s
                                   _stream(stream)))
 
 
+def dp_selftest_wait_timeout(waited_ns=None, stream=None) -> None:
+    """Launch the diagnostic kernel whose bounded device wait runs out (see dpclip.h);
+    dp_check_status then returns DP_ERR_TIMEOUT."""
+    _check(_lib.dp_selftest_wait_timeout(_ptr(waited_ns), _stream(stream)))
+
+
 def dp_check_status(stream=None) -> int:
     """Synchronizes and returns the device status (DP_OK or the raised code) without raising."""
     return _lib.dp_check_status(_stream(stream))
 
 
-from .step import ClipPipeline, ClipStep  # noqa: E402,F401
+from .step import ClipPipeline, ClipStep, VirtualStep  # noqa: E402,F401

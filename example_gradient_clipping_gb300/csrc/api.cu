@@ -504,6 +504,14 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
   return ok();
 }
 
+dp_status dp_selftest_wait_timeout(unsigned long long* waited_ns, cudaStream_t stream) {
+  unsigned* st = status_ptr();
+  if (!st) return fail(DP_ERR_CUDA, "cannot resolve the device status word");
+  const cudaError_t e = dph::launch_selftest_wait(st, waited_ns, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_selftest_wait_timeout launch");
+  return ok();
+}
+
 dp_status dp_check_status(cudaStream_t stream) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_check_status sync");

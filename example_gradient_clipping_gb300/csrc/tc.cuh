@@ -31,6 +31,8 @@ cudaError_t launch_tc_sum2(const Geom& g, const void* A, const void* G, const fl
 size_t tc_inst_ws_bytes(const Geom& g);
 cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* out, float* ws,
                            unsigned* status, cudaStream_t s);
+// Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
+cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
 // Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).
 bool tc_ghost_supported(const Geom& g);
 size_t tc_ghost_ws_bytes(const Geom& g);

@@ -124,6 +124,75 @@ class ClipStep:
         return self.grad
 
 
+class VirtualStep:
+    """One logical batch processed as physical micro-batches (gradient accumulation, the
+    virtual step of [MixGhost] section 5 and Appendix E).
+
+    add(inputs, B) runs one micro-batch of B examples through the same calls as ClipStep
+    (norms, factors, clipped sums) and ADDS its clipped sums to the flat gradient; the clip
+    factor of an example depends on that example alone, so the split changes nothing.
+    finish(seed) then adds the noise N(0, sigma^2 C^2) once and scales by 1/B with B the
+    logical batch (every example added since zero()).  `descs` give the layer shapes; their
+    B is the largest micro-batch the step will see.
+    """
+
+    def __init__(self, descs: Sequence[LayerDesc], C, sigma: float, per_layer: bool = False,
+                 norm_modes: Optional[Sequence[int]] = None, device: str = "cuda"):
+        import torch
+        self.base = ClipStep(descs, C, sigma, per_layer=per_layer, norm_modes=norm_modes, device=device)
+        b = self.base
+        self.grad = b.grad
+        L = len(b.descs)
+        self.sq_flat = torch.empty(L * b.B, dtype=torch.float32, device=b.grad.device)
+        self.fac_flat = torch.empty((L if b.per_layer else 1) * b.B, dtype=torch.float32, device=b.grad.device)
+        self.examples = 0
+        self.zero()
+
+    def zero(self) -> None:
+        self.grad.zero_()
+        self.examples = 0
+
+    def add(self, inputs, B: int, stream=None) -> None:
+        import torch
+        b = self.base
+        if not 1 <= B <= b.B:
+            raise ValueError(f"micro-batch of {B} examples; this step takes 1..{b.B}")
+        L = len(b.descs)
+        descs = []
+        for d in b.descs:
+            dm = type(d).from_buffer_copy(d)
+            dm.B = B
+            descs.append(dm)
+        need = max(dp_workspace_size(d, m) for d, m in zip(descs, b.modes))
+        if need > b.workspace.numel():
+            b.workspace = torch.empty(need, dtype=torch.uint8, device=b.grad.device)
+        sq = self.sq_flat[:L * B].view(L, B)
+        fac = self.fac_flat[:(L if b.per_layer else 1) * B].view(-1, B)
+        for l, (d, (A, G)) in enumerate(zip(descs, inputs)):
+            b.chosen[l] = dp_layer_sqnorms(d, A, G, sq[l], b.workspace, mode=b.modes[l], stream=stream)
+        dp_clip_factors(sq, B, L, b.per_layer, b.C if b.per_layer else b.C[:1], fac, stream=stream)
+        for l, (d, (A, G)) in enumerate(zip(descs, inputs)):
+            dW, db = b.layer_views(l)
+            dp_clipped_sum(d, A, G, fac[l] if b.per_layer else fac[0], dW, db, b.workspace, accumulate=True,
+                           stream=stream)
+        self.examples += B
+
+    def finish(self, seed: int, stream=None):
+        """Noise once and 1/B over the logical batch; returns the flat gradient."""
+        if self.examples == 0:
+            raise ValueError("no micro-batch was added")
+        b = self.base
+        if not b.per_layer:
+            dp_add_noise(self.grad, b.sigma, b.C[0], self.examples, seed, 0, stream=stream)
+        else:
+            for l, d in enumerate(b.descs):
+                p, D = b.shapes[l]
+                n = p * D + (p if d.has_bias else 0)
+                o = b.offsets[l]
+                dp_add_noise(self.grad[o:o + n], b.sigma, b.C[l], self.examples, seed, o, stream=stream)
+        return self.grad
+
+
 class ClipPipeline:
     """Privatised-gradient steps over batches that arrive in pinned host memory.
 

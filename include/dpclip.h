@@ -179,6 +179,16 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
  * DP_ERR_TIMEOUT) raised since the last check, and clears it. */
 dp_status dp_check_status(cudaStream_t stream);
 
+/* Diagnostic of the device-side failure path.  Launches (asynchronously, on `stream`)
+ * one kernel that allocates tensor memory and waits on an mbarrier nothing arrives on:
+ * the bounded wait gives up after the device wait limit (2 s), raises DP_ERR_TIMEOUT in
+ * the device status word (read it with dp_check_status), and the kernel releases its
+ * tensor memory as the tensor-core kernels do after a timeout and returns; the context
+ * stays usable.  If `waited_ns` (device, one value) is non-NULL it receives the time the
+ * kernel spent from the start of the wait to the release, in ns.  Returns DP_ERR_CUDA if
+ * the launch fails. */
+dp_status dp_selftest_wait_timeout(unsigned long long* waited_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -422,3 +422,22 @@ def test_speed_priority_counts_match_loop_nests():
     assert dpsgd.norm_mode_plan(spec) == "ghost"
     assert dpsgd.norm_mode_plan_time(spec) == "instantiate"
     assert dpsgd.norm_mode_plan_time(LayerSpec("z", "linear", p=8, d=8, T=1)) == "t1"
+
+
+def test_micro_batch_sums_add_up():
+    """Gradient accumulation ([MixGhost] section 5, Appendix E): per-example clipping makes
+    the clipped sum additive over any split of the batch, and the noise and 1/B of the
+    logical batch are applied once to the total."""
+    wl = Workload(name="acc", B=7, layers=(LayerSpec("a", "linear", p=5, d=6, T=4),), dtype="fp32",
+                  C=0.5, sigma=0.0, seed=3)
+    spec = wl.layers[0]
+    A, G = layer_inputs(wl, 0)
+    sq = dpsgd.layer_sqnorms(spec, A, G)
+    fac, _ = dpsgd.clip_factors(sq[None, :], 0.5, False)
+    S, Sb = dpsgd.clipped_sum(spec, A, G, fac)
+    S1, Sb1 = dpsgd.clipped_sum(spec, A[:3], G[:3], fac[:3])
+    S2, Sb2 = dpsgd.clipped_sum(spec, A[3:], G[3:], fac[3:])
+    np.testing.assert_allclose(S1 + S2, S, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(Sb1 + Sb2, Sb, rtol=1e-12, atol=1e-15)
+    step = dpsgd.dp_step(wl, [(A, G)])
+    np.testing.assert_allclose(step["noisy"], np.concatenate([S.ravel(), Sb]) / 7, rtol=1e-12, atol=1e-15)

@@ -301,6 +301,50 @@ def test_speed_priority_mode(lib):
     assert got["chosen"] == lib.DP_NORM_INSTANTIATE
 
 
+@pytest.mark.parametrize("per_layer", [False, True], ids=["flat", "per_layer"])
+def test_virtual_step_matches_one_batch(lib, per_layer):
+    """Gradient accumulation: micro-batches of 3 and 5 examples added into one step, then
+    noise and 1/B once, equal the step over the logical batch of 8."""
+    l1 = LayerSpec("a", "linear", p=32, d=48, T=16)
+    l2 = LayerSpec("b", "conv2d", p=8, Cin=4, H=6, W=6, k=3, pad=1)
+    wl = Workload(name="virtual", B=8, layers=(l1, l2), dtype="bf16", C=1.0, sigma=0.5, seed=9,
+                  per_layer=per_layer)
+    Cs = [1.0, 0.5]
+    inputs = [workloads.layer_inputs(wl, l) for l in range(2)]
+    ref = oracle.dp_step(wl, inputs, C=Cs if per_layer else None)
+    vs = lib.VirtualStep([desc_for(lib, s, 5, "bf16") for s in wl.layers], C=Cs if per_layer else 1.0,
+                         sigma=0.5, per_layer=per_layer)
+    for _ in range(2):          # a second logical batch after zero() gives the same result
+        vs.zero()
+        for lo, hi in ((0, 3), (3, 8)):
+            dev = [(to_dev(A[lo:hi], "bf16"), to_dev(G[lo:hi], "bf16")) for A, G in inputs]
+            vs.add(dev, hi - lo)
+        grad = vs.finish(wl.seed)
+        assert vs.examples == 8
+        assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+
+
+def test_device_wait_timeout_reported_and_context_usable(lib):
+    """Failure detection without a fault: a kernel whose bounded mbarrier wait has nothing
+    to wait for gives up after the 2 s limit, the host reads DP_ERR_TIMEOUT, and the next
+    step on the same context still matches the oracle."""
+    import torch
+    assert lib.dp_check_status() == lib.DP_OK
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    lib.dp_selftest_wait_timeout(waited)
+    assert lib.dp_check_status() == lib.DP_ERR_TIMEOUT
+    assert 1.9e9 <= waited.item() <= 10e9
+    assert lib.dp_check_status() == lib.DP_OK            # cleared
+    spec = LayerSpec("a", "linear", p=32, d=48, T=16)
+    wl = Workload(name="after_timeout", B=6, layers=(spec,), dtype="bf16", C=1.0, sigma=0.5, seed=4)
+    inputs = [workloads.layer_inputs(wl, 0)]
+    ref = oracle.dp_step(wl, inputs)
+    step = lib.ClipStep([desc_for(lib, spec, wl.B, "bf16")], C=1.0, sigma=0.5)
+    grad = step.run([(to_dev(A, "bf16"), to_dev(G, "bf16")) for A, G in inputs], seed=wl.seed)
+    assert lib.dp_check_status() == lib.DP_OK
+    assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+
+
 def test_mixed_scale_factors_straddle_bound(lib):
     """Some examples under C (factor exactly 1), some over; flat clipping over two layers."""
     import torch
