@@ -52,16 +52,19 @@ def layer_desc(dp, spec, B, dtype):
                          stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
 
 
-def step_work(wl, modes):
+def step_work(wl, modes, kept=None):
     """Algorithmic FLOPs and bytes of one step, from the per-module complexity counts
     of the mixed-ghost paper (Appendix C): ghost norm 2T^2(D+p) + 2T^2 per example,
-    instantiation 2TpD + 2pD, one-row norm 2(D+p), clipped sum 2TpD.  Bytes: the
-    inputs read once by the norm pass and once by the sum pass, the fp32 gradient
-    written once, and the noise pass reading and writing it."""
+    instantiation 2TpD + 2pD, one-row norm 2(D+p), clipped sum 2TpD -- or, for a layer
+    that keeps its per-example gradients, the weighted sum 2pD of the kept gradients.
+    Bytes: the inputs read once by the norm pass and once by the sum pass (a kept layer:
+    its fp32 gradients written by the norm pass and read by the sum pass instead), the
+    fp32 gradient written once, and the noise pass reading and writing it."""
     es = 2 if wl.dtype == "bf16" else 4
+    kept = kept or [False] * len(wl.layers)
     flop_norm = flop_sum = 0.0
-    in_bytes = 0
-    for spec, m in zip(wl.layers, modes):
+    in_bytes = input_reads = kept_bytes = 0
+    for spec, m, kp in zip(wl.layers, modes, kept):
         T, D, p = spec.rows, spec.D, spec.p
         if m == "ghost":
             flop_norm += wl.B * (2.0 * T * T * (D + p) + 2.0 * T * T)
@@ -69,13 +72,20 @@ def step_work(wl, modes):
             flop_norm += wl.B * (2.0 * T * p * D + 2.0 * p * D)
         else:
             flop_norm += wl.B * 2.0 * (D + p)
-        flop_sum += wl.B * 2.0 * T * p * D
         a_el = spec.T * spec.d if spec.kind == "linear" else spec.Cin * spec.H * spec.W
         g_el = spec.T * spec.p if spec.kind == "linear" else spec.p * spec.Hout * spec.Wout
-        in_bytes += wl.B * (a_el + g_el) * es
+        layer_in = wl.B * (a_el + g_el) * es
+        in_bytes += layer_in
+        if kp:
+            flop_sum += wl.B * 2.0 * p * D
+            kept_bytes += wl.B * (p * D + p) * 4
+            input_reads += layer_in              # the norm pass only
+        else:
+            flop_sum += wl.B * 2.0 * T * p * D
+            input_reads += 2 * layer_in          # the norm pass and the sum pass
     n = wl.n_params
-    return dict(flop_norm=flop_norm, flop_sum=flop_sum, in_bytes=in_bytes,
-                bytes_total=2 * in_bytes + 4 * n + 8 * n, n_params=n)
+    return dict(flop_norm=flop_norm, flop_sum=flop_sum, in_bytes=in_bytes, kept_bytes=kept_bytes,
+                bytes_total=input_reads + 2 * kept_bytes + 4 * n + 8 * n, n_params=n)
 
 
 class ClockSampler:
@@ -302,7 +312,8 @@ def run_ours(args, wl):
         def sample_inputs(b):
             return [(a[:b].float().numpy(), g[:b].float().numpy()) for a, g in pinned]
     modes = [dp.MODE_NAMES[m] for m, _, _ in step.plan]
-    work = step_work(wl, modes)
+    kept = [k is not None for k in step.kept]
+    work = step_work(wl, modes, kept)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     # The whole step is one CUDA graph (norms -> factors -> clipped sums -> noise),
@@ -379,7 +390,11 @@ def run_ours(args, wl):
     pk = _peaks()
     means = {n: statistics.mean(v) for n, v in per_call.items()}
     dom = max(means, key=means.get)
-    if dom == "sums":
+    sum_bytes = work["kept_bytes"] + 4 * work["n_params"]     # kept gradients read, sums written
+    if dom == "sums" and sum_bytes / (pk["hbm"] * 1e9) > work["flop_sum"] / (pk["bf16"] * 1e12):
+        # mostly kept per-example gradients: a read-bound weighted sum
+        roof = dict(bound="hbm", achieved=sum_bytes / (means["sums"] * 1e-3) / 1e9, peak=pk["hbm"], unit="GB/s")
+    elif dom == "sums":
         roof = dict(bound="tensor", achieved=work["flop_sum"] / (means["sums"] * 1e-3) / 1e12,
                     peak=pk["bf16"], unit="TFLOP/s")
     elif dom == "norms":

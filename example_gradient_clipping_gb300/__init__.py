@@ -62,6 +62,9 @@ def _load():
         "dp_adaptive_bound": (c_int, [c_void, c_int, c_f, c_f, c_f, c_f, c_u64, c_int, c_void, c_void]),
         "dp_check_status": (c_int, [c_void]),
         "dp_selftest_wait_timeout": (c_int, [c_void, c_void]),
+        "dp_grads_size": (c_size, [PD]),
+        "dp_layer_sqnorms_keep": (c_int, [PD, c_void, c_void, c_void, c_void, c_void, c_size, c_void]),
+        "dp_clipped_sum_kept": (c_int, [PD, c_void, c_void, c_void, c_void, c_int, c_void, c_size, c_void]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -168,6 +171,29 @@ def dp_adaptive_bound(sqnorms, B: int, C_l2: float, alpha: float, beta: float, s
                       seed: int, layer: int, out, stream=None) -> None:
     _check(_lib.dp_adaptive_bound(_ptr(sqnorms), B, C_l2, alpha, beta, sigma_l2, seed, layer, _ptr(out),
                                   _stream(stream)))
+
+
+def dp_grads_size(desc: LayerDesc) -> int:
+    """Bytes of the kept per-example gradients of `desc` (0: the layer cannot keep them)."""
+    return int(_lib.dp_grads_size(ctypes.byref(desc)))
+
+
+def _ws_len(workspace) -> int:
+    return workspace.numel() * workspace.element_size() if workspace is not None and not isinstance(workspace, int) else 0
+
+
+def dp_layer_sqnorms_keep(desc: LayerDesc, A, G, sqnorm_out, grads, workspace=None, ws_bytes: Optional[int] = None,
+                          stream=None) -> None:
+    _check(_lib.dp_layer_sqnorms_keep(ctypes.byref(desc), _ptr(A), _ptr(G), _ptr(sqnorm_out), _ptr(grads),
+                                      _ptr(workspace), _ws_len(workspace) if ws_bytes is None else ws_bytes,
+                                      _stream(stream)))
+
+
+def dp_clipped_sum_kept(desc: LayerDesc, grads, factors, dW, db=None, workspace=None, ws_bytes: Optional[int] = None,
+                        accumulate: bool = False, stream=None) -> None:
+    _check(_lib.dp_clipped_sum_kept(ctypes.byref(desc), _ptr(grads), _ptr(factors), _ptr(dW), _ptr(db),
+                                    int(bool(accumulate)), _ptr(workspace),
+                                    _ws_len(workspace) if ws_bytes is None else ws_bytes, _stream(stream)))
 
 
 def dp_selftest_wait_timeout(waited_ns=None, stream=None) -> None:

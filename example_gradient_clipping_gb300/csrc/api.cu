@@ -257,6 +257,25 @@ size_t norm_ws_bytes(const Geom& g, const Plan& pl) {
   return (pl.rows ? rows_bytes(g) : 0) + inner;
 }
 
+// Kept per-example gradients: the instantiating tensor-core norm kernels store g_i and b_i;
+// the layout (conv tile column order, or [p, D] / [p, Dp] rows) follows from the plan, which
+// for aligned bf16 inputs depends on the geometry alone.
+static const char kAlignedProbe[16] __attribute__((aligned(16))) = {};
+
+bool keep_plan(int dtype, const Geom& g, const void* A, const void* G, const void* ws, Plan* pl) {
+  if (dtype != DP_BF16 || g.T == 1) return false;
+  *pl = norm_plan(g, DP_NORM_INSTANTIATE, dtype, A, G, ws);
+  return pl->kernel == NK_TC_CONV || pl->kernel == NK_TC_INST;
+}
+bool keep_plan(int dtype, const Geom& g, Plan* pl) {
+  return keep_plan(dtype, g, kAlignedProbe, kAlignedProbe, kAlignedProbe, pl);
+}
+// Columns of each kept gradient (conv tile columns = D; rows of a padded conv layer = Dp).
+int kept_width(const Geom& g, const Plan& pl) { return pl.kernel == NK_TC_CONV ? g.D : pl.lg.D; }
+size_t kept_sum_need(const Geom& g, const Plan& pl) {
+  return dph::kept_sum_ws_bytes(g.B, g.p, kept_width(g, pl)) + (pl.rows ? padded_out_bytes(g) : 0);
+}
+
 // The size dp_workspace_size reports covers every path a call with `desc` can take
 // (the choice also depends on the dtype and the alignment of the pointers).
 size_t max_ws_bytes(const Geom& g, int mode) {
@@ -290,6 +309,8 @@ size_t max_ws_bytes(const Geom& g, int mode) {
     if (dph::tc_sumx_supported(lg)) n = std::max(n, pre + dph::tc_sumx_ws_bytes(lg));
     if (dph::tc_sum2_supported(lg)) n = std::max(n, pre + dph::tc_sum2_ws_bytes(lg));
   }
+  Plan kp;
+  if (keep_plan(DP_BF16, g, &kp)) n = std::max(n, std::max(norm_ws_bytes(g, kp), kept_sum_need(g, kp)));
   return n;
 }
 
@@ -461,6 +482,80 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
     if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum launch");
+  return ok();
+}
+
+size_t dp_grads_size(const dp_layer_desc* desc) {
+  Geom g;
+  if (make_geom(desc, &g) != DP_OK) return 0;
+  Plan pl;
+  if (!keep_plan(desc->dtype, g, &pl)) return 0;
+  const size_t w = (size_t)g.B * g.p * kept_width(g, pl);
+  return (w + (g.has_bias ? (size_t)g.B * g.p : 0)) * sizeof(float);
+}
+
+dp_status dp_layer_sqnorms_keep(const dp_layer_desc* desc, const void* A, const void* G, float* sqnorm_out,
+                                float* grads, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  Geom g;
+  dp_status st = make_geom(desc, &g);
+  if (st != DP_OK) return st;
+  if (!A || !G || !sqnorm_out || !grads)
+    return fail(DP_ERR_INVALID_ARG, "A, G, sqnorm_out and grads must be non-NULL");
+  if (!aligned16(grads)) return fail(DP_ERR_INVALID_ARG, "grads must be 16-byte aligned");
+  Plan pl;
+  if (!keep_plan(desc->dtype, g, A, G, workspace, &pl))
+    return fail(DP_ERR_UNSUPPORTED,
+                "this layer's instantiated norm does not run on a kernel that keeps per-example gradients "
+                "(bf16 with 16-byte aligned A, G and workspace, tensor-core shapes)");
+  const size_t need = norm_ws_bytes(g, pl);
+  if (need && (!workspace || ws_bytes < need))
+    return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  void* wsp = workspace;
+  cudaError_t e = prepare_rows(g, pl, A, G, wsp, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_layer_sqnorms_keep row layout");
+  float* keep_b = g.has_bias ? grads + (size_t)g.B * g.p * kept_width(g, pl) : nullptr;
+  if (pl.kernel == NK_TC_CONV)
+    e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, wsp, status_ptr(), stream, grads, keep_b);
+  else
+    e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, static_cast<float*>(wsp), status_ptr(), stream, grads, keep_b);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_layer_sqnorms_keep launch");
+  return ok();
+}
+
+dp_status dp_clipped_sum_kept(const dp_layer_desc* desc, const float* grads, const float* factors, float* dW,
+                              float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  Geom g;
+  dp_status st = make_geom(desc, &g);
+  if (st != DP_OK) return st;
+  if (!grads || !factors || !dW) return fail(DP_ERR_INVALID_ARG, "grads, factors and dW must be non-NULL");
+  if (db && !g.has_bias) return fail(DP_ERR_INVALID_ARG, "db given for a layer without bias");
+  Plan pl;
+  if (!keep_plan(desc->dtype, g, &pl))
+    return fail(DP_ERR_UNSUPPORTED, "this layer keeps no per-example gradients (see dp_grads_size)");
+  const size_t need = kept_sum_need(g, pl);
+  if (!workspace || ws_bytes < need)
+    return fail(DP_ERR_INVALID_ARG, "workspace of %zu bytes needed, %zu given", need,
+                workspace ? ws_bytes : (size_t)0);
+  const int width = kept_width(g, pl);
+  const float* keep_b = g.has_bias ? grads + (size_t)g.B * g.p * width : nullptr;
+  const int conv_kk = pl.kernel == NK_TC_CONV ? g.k * g.k : 0;
+  const bool padded = pl.rows && padded_out_bytes(g) != 0;
+  float* kdW = dW;
+  float* kdb = db;
+  void* wsp = workspace;
+  if (padded) {     // rows of a conv layer whose unfolded width was padded: compact afterwards
+    kdW = static_cast<float*>(wsp);
+    kdb = db ? kdW + align256((size_t)g.p * width * 4) / 4 : nullptr;
+    wsp = static_cast<uint8_t*>(wsp) + padded_out_bytes(g);
+  }
+  cudaError_t e = dph::launch_kept_sum(g.B, g.p, width, conv_kk, grads, keep_b, factors, kdW, kdb,
+                                       padded ? 0 : accumulate, static_cast<float*>(wsp), stream);
+  if (e == cudaSuccess && padded) {
+    e = dph::launch_compact_cols(kdW, g.p, g.D, width, dW, accumulate, stream);
+    if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum_kept launch");
   return ok();
 }
 

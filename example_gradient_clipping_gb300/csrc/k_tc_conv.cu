@@ -54,6 +54,9 @@ struct Params {
   int nk;                 // 64-pixel stages per example
   int ex_per_split;
   int ncols;              // items * 64
+  float* keep;            // norm mode, or null: every example's gradient [B, p, ncols] in tile
+                          // column order ((cc * k*k + tap) * 64 + c), and its bias [B, p]
+  float* keep_b;
 };
 
 struct Ctl {
@@ -179,14 +182,27 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
         ptx::tmem_ld16(base + ch * 16 + 16, a1);
         ptx::tmem_wait_ld();
         if constexpr (kNorm) {
+          const int m = m0 + quarter * 32 + lane;
           if (ch < 4 ? v0 : v1) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               ss = fmaf(a0[j], a0[j], ss);
               ss = fmaf(a1[j], a1[j], ss);
             }
+            if (P.keep && m < P.p) {   // 32 consecutive tile columns of row m: one 128-byte line
+              float4* dst = reinterpret_cast<float4*>(P.keep + ((size_t)e * P.p + m) * P.ncols + (size_t)q0 * 64 +
+                                                      half * 128 + ch * 16);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                dst[j] = make_float4(a0[4 * j], a0[4 * j + 1], a0[4 * j + 2], a0[4 * j + 3]);
+                dst[4 + j] = make_float4(a1[4 * j], a1[4 * j + 1], a1[4 * j + 2], a1[4 * j + 3]);
+              }
+            }
           }
-          if (my_ones && ch == ones_ch) ss = fmaf(a0[0], a0[0], ss);   // ||b_i||^2, once per row
+          if (my_ones && ch == ones_ch) {
+            ss = fmaf(a0[0], a0[0], ss);   // ||b_i||^2, once per row
+            if (P.keep_b && m < P.p) P.keep_b[(size_t)e * P.p + m] = a0[0];
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -454,7 +470,7 @@ static tcconv::Params base_params(const Geom& g, const ConvPlan& c, unsigned* st
 }
 
 cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, float* out, void* ws,
-                                unsigned* status, cudaStream_t s) {
+                                unsigned* status, cudaStream_t s, float* keep, float* keep_b) {
   const ConvPlan c = conv_plan(g, true);
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* Xh = w;
@@ -466,6 +482,8 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
   tcconv::Params P = base_params(g, c, status);
   P.part = part;
   P.bias = g.has_bias;
+  P.keep = keep;
+  P.keep_b = g.has_bias ? keep_b : nullptr;
   e = launch_kernel<true>(g, c, mG, mX, P, s);
   if (e != cudaSuccess) return e;
   return launch_reduce_splits(part, c.tiles, (size_t)g.B, out, 0, s);

@@ -68,6 +68,8 @@ struct Params {
   int norm_bias;      // norm mode: the layer has a bias
   int gsplit;         // examples split over the grid (no cluster): CTA z writes its partial
                       // tile to dW + z*p*d (db + z*p), reduced afterwards in z order
+  float* keep;        // norm mode, or null: every example's gradient [B, p, d] and bias [B, p]
+  float* keep_b;
 };
 
 // Shared-memory control block after the stages.
@@ -228,6 +230,7 @@ __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ct
       }
       // the 16 lanes of a half-warp share 8 output columns: total them, square them once
       float bsq = 0.f;
+      const int mb = blockIdx.x * BM + bbox * 64 + bq * 8;   // this group's first output
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         float v = bt[q];
@@ -236,6 +239,7 @@ __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ct
         v += __shfl_xor_sync(0xffffffffu, v, 4);
         v += __shfl_xor_sync(0xffffffffu, v, 8);
         bsq = fmaf(v, v, bsq);
+        if (P.keep_b && bj == 0 && mb + q < P.p) P.keep_b[(size_t)e * P.p + mb + q] = v;
       }
       if (bj == 0) ss = bsq;
     }
@@ -256,6 +260,19 @@ __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ct
         for (int j = 0; j < 16; ++j) {
           ss = fmaf(v0[j], v0[j], ss);
           ss = fmaf(v1[j], v1[j], ss);
+        }
+        const int m = blockIdx.x * BM + quarter * 32 + lane;
+        const int n = blockIdx.y * BN + half * 128 + ch * 16;   // d % 8 == 0: whole float4s
+        if (P.keep && m < P.p) {
+          float* dst = P.keep + ((size_t)e * P.p + m) * P.d + n;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (n + 4 * j < P.d)
+              *reinterpret_cast<float4*>(dst + 4 * j) = make_float4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+            if (n + 16 + 4 * j < P.d)
+              *reinterpret_cast<float4*>(dst + 16 + 4 * j) =
+                  make_float4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
+          }
         }
       }
       ptx::tc_fence_before();
@@ -713,7 +730,7 @@ size_t tc_inst_ws_bytes(const Geom& g) {
 }
 
 cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* out, float* ws,
-                           unsigned* status, cudaStream_t s) {
+                           unsigned* status, cudaStream_t s, float* keep, float* keep_b) {
   CUtensorMap mg64, ma64, mg16, ma16;
   const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
   const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
@@ -743,6 +760,8 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
   P.n16 = n16;
   P.part = ws;
   P.norm_bias = g.has_bias;
+  P.keep = keep;
+  P.keep_b = g.has_bias ? keep_b : nullptr;
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};

@@ -29,8 +29,16 @@ cudaError_t launch_tc_sum2(const Geom& g, const void* A, const void* G, const fl
 // Instantiated norm ||G_i^T A_i||^2 (+ bias) from the same per-example TMEM products
 // (shapes as tc_sumx_supported).
 size_t tc_inst_ws_bytes(const Geom& g);
+// With `keep`, every example's gradient is also written to keep [B, p, D] and its bias to
+// keep_b [B, p] (fp32) for the kept-gradient clipped sum.
 cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* out, float* ws,
-                           unsigned* status, cudaStream_t s);
+                           unsigned* status, cudaStream_t s, float* keep = nullptr, float* keep_b = nullptr);
+// Clipped sum from kept per-example gradients: dW (+)= sum_i c_i g_i, db (+)= sum_i c_i b_i
+// (2pD flop per example, one read of the kept gradients).  conv_kk > 0: g_i in the conv
+// kernel's tile column order with that many filter taps (mapped back to [p, Cin, k, k]).
+size_t kept_sum_ws_bytes(int B, int p, int D);
+cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
+                            const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s);
 // Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
 // Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).
@@ -59,8 +67,10 @@ size_t scaled_rows_bias_bytes(int B, int T, int p);
 // instantiated norm and clipped sum; the workspace holds an NHWC copy of the input.
 bool tc_conv_supported(const Geom& g);
 size_t tc_conv_ws_bytes(const Geom& g, bool norm);
+// With `keep`, every example's gradient is also written to keep [B, p, D] in the kernel's
+// tile column order ((channel block * k*k + tap) * 64 + channel) and its bias to keep_b [B, p].
 cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, float* out, void* ws,
-                                unsigned* status, cudaStream_t s);
+                                unsigned* status, cudaStream_t s, float* keep = nullptr, float* keep_b = nullptr);
 cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
                                float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
 // im2col map (bf16, 128-byte swizzle, 64 channels per pixel) over an NHWC copy of a conv input.

@@ -10,13 +10,23 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence, Tuple
 
-from . import (DP_NORM_AUTO, LayerDesc, dp_add_noise, dp_add_noise_devseed, dp_clip_factors,
-               dp_clipped_sum, dp_launch_count, dp_layer_sqnorms, dp_plan, dp_workspace_size)
+from . import (DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_add_noise, dp_add_noise_devseed, dp_clip_factors,
+               dp_clipped_sum, dp_clipped_sum_kept, dp_grads_size, dp_launch_count, dp_layer_sqnorms,
+               dp_layer_sqnorms_keep, dp_plan, dp_workspace_size)
+
+# Instantiated layers with at least this many rows per example keep their per-example
+# gradients by default (the clipped sum then reads them once instead of recomputing a
+# contraction over the rows).
+KEEP_MIN_ROWS = 512
 
 
 class ClipStep:
+    """keep_grads: "auto" keeps the per-example gradients of instantiated layers with at
+    least KEEP_MIN_ROWS rows (where the library supports it), True keeps them wherever it
+    does, False never."""
+
     def __init__(self, descs: Sequence[LayerDesc], C, sigma: float, per_layer: bool = False,
-                 norm_modes: Optional[Sequence[int]] = None, device: str = "cuda"):
+                 norm_modes: Optional[Sequence[int]] = None, device: str = "cuda", keep_grads="auto"):
         import torch
         self.descs = list(descs)
         L = len(self.descs)
@@ -45,6 +55,11 @@ class ClipStep:
         self.chosen: List[int] = [m for m, _, _ in self.plan]
         self.graph = None
         self.graph_kernels = 0
+        self.kept = []
+        for d, (m, T, _) in zip(self.descs, self.plan):
+            want = keep_grads is True or (keep_grads == "auto" and T >= KEEP_MIN_ROWS)
+            nbytes = dp_grads_size(d) if (want and m == DP_NORM_INSTANTIATE) else 0
+            self.kept.append(torch.empty(nbytes // 4, dtype=torch.float32, device=dev) if nbytes else None)
 
     def layer_views(self, l: int) -> Tuple:
         p, D = self.shapes[l]
@@ -55,8 +70,12 @@ class ClipStep:
 
     def norms(self, inputs, stream=None) -> None:
         for l, (d, (A, G)) in enumerate(zip(self.descs, inputs)):
-            self.chosen[l] = dp_layer_sqnorms(d, A, G, self.sqnorms[l], self.workspace, mode=self.modes[l],
-                                              stream=stream)
+            if self.kept[l] is not None:
+                dp_layer_sqnorms_keep(d, A, G, self.sqnorms[l], self.kept[l], self.workspace, stream=stream)
+                self.chosen[l] = DP_NORM_INSTANTIATE
+            else:
+                self.chosen[l] = dp_layer_sqnorms(d, A, G, self.sqnorms[l], self.workspace, mode=self.modes[l],
+                                                  stream=stream)
 
     def factors_(self, stream=None) -> None:
         L = len(self.descs)
@@ -67,7 +86,10 @@ class ClipStep:
         for l, (d, (A, G)) in enumerate(zip(self.descs, inputs)):
             dW, db = self.layer_views(l)
             fac = self.factors[l] if self.per_layer else self.factors[0]
-            dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
+            if self.kept[l] is not None:
+                dp_clipped_sum_kept(d, self.kept[l], fac, dW, db, self.workspace, stream=stream)
+            else:
+                dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
 
     def noise(self, seed: int, stream=None) -> None:
         if not self.per_layer:
@@ -139,7 +161,8 @@ class VirtualStep:
     def __init__(self, descs: Sequence[LayerDesc], C, sigma: float, per_layer: bool = False,
                  norm_modes: Optional[Sequence[int]] = None, device: str = "cuda"):
         import torch
-        self.base = ClipStep(descs, C, sigma, per_layer=per_layer, norm_modes=norm_modes, device=device)
+        self.base = ClipStep(descs, C, sigma, per_layer=per_layer, norm_modes=norm_modes, device=device,
+                             keep_grads=False)
         b = self.base
         self.grad = b.grad
         L = len(b.descs)

@@ -175,6 +175,33 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
                             float sigma_l2, uint64_t seed, int layer, float* out,
                             cudaStream_t stream);
 
+/* ---- Kept per-example gradients (instantiated layers) --------------------------------
+ * Where a layer's norm is formed by instantiation ([MixGhost] section 3, the FastGradClip
+ * side of the mixed clipping), the instantiating kernel can also store every example's
+ * gradient g_i and bias gradient b_i; the clipped sum is then sum_i c_i g_i over the stored
+ * gradients (2pD flop per example, one read) instead of a second contraction over the T
+ * rows (2TpD).  It trades B*(p*D + p)*4 bytes of device memory for that time, and pays off
+ * when T is large (a few hundred rows and up).
+ *
+ * dp_grads_size: bytes of the `grads` buffer for `desc` (fp32, an internal layout), or 0
+ * when the layer's instantiated norm does not run on a kernel that keeps gradients (it
+ * needs bf16 inputs and the tensor-core shapes; T == 1 layers are excluded).  Host only.
+ *
+ * dp_layer_sqnorms_keep: the instantiated norm of dp_layer_sqnorms (sqnorm_out [B], as with
+ * DP_NORM_INSTANTIATE) that also writes every example's gradient into `grads` (device,
+ * 16-byte aligned, dp_grads_size bytes, caller-owned).  A, G and the workspace must be
+ * 16-byte aligned; otherwise DP_ERR_UNSUPPORTED and nothing is launched.  Workspace as
+ * dp_workspace_size(desc, DP_NORM_INSTANTIATE).
+ *
+ * dp_clipped_sum_kept: dW (+)= sum_i factors[i] g_i, db (+)= sum_i factors[i] b_i from a
+ * `grads` buffer that dp_layer_sqnorms_keep filled for the same `desc`; same output layout,
+ * accumulate flag and determinism as dp_clipped_sum.  Workspace as dp_workspace_size. */
+size_t dp_grads_size(const dp_layer_desc* desc);
+dp_status dp_layer_sqnorms_keep(const dp_layer_desc* desc, const void* A, const void* G, float* sqnorm_out,
+                                float* grads, void* workspace, size_t ws_bytes, cudaStream_t stream);
+dp_status dp_clipped_sum_kept(const dp_layer_desc* desc, const float* grads, const float* factors, float* dW,
+                              float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronizes `stream`, returns the device status word (DP_OK, DP_ERR_NONFINITE or
  * DP_ERR_TIMEOUT) raised since the last check, and clears it. */
 dp_status dp_check_status(cudaStream_t stream);

@@ -112,3 +112,34 @@ def test_full_size_vgg_step_flat_and_per_layer_factors(lib):
         got = step.factors.double().cpu().numpy()
         assert rel_elem(got if per_layer else got[0], want) <= 1e-6
         assert np.all(np.isfinite(g.cpu().numpy()))
+
+
+def test_full_size_conv3x3_kept_gradients_match_recomputed(lib):
+    """The 3x3 conv workload at B=256: norms and clipped sum from kept per-example gradients
+    equal the instantiated norms and the recomputing clipped sum (both fp32-accumulated)."""
+    import torch
+    dp = lib
+    wl = workloads.get_workload("conv3x3_b256")
+    spec = wl.layers[0]
+    desc = desc_for(dp, spec, wl.B, wl.dtype)
+    A, G = workloads.device_layer_inputs(wl, 0)
+    ws = torch.empty(dp.dp_workspace_size(desc, dp.DP_NORM_INSTANTIATE), dtype=torch.uint8, device="cuda")
+    grads = torch.empty(dp.dp_grads_size(desc) // 4, dtype=torch.float32, device="cuda")
+    sq_k = torch.empty(wl.B, device="cuda")
+    sq_r = torch.empty(wl.B, device="cuda")
+    dp.dp_layer_sqnorms_keep(desc, A, G, sq_k, grads, ws)
+    dp.dp_layer_sqnorms(desc, A, G, sq_r, ws, mode=dp.DP_NORM_INSTANTIATE)
+    f = torch.rand(wl.B, device="cuda", generator=torch.Generator("cuda").manual_seed(5))
+    outs = []
+    for kept in (True, False):
+        dW = torch.empty(spec.p * spec.D, device="cuda")
+        db = torch.empty(spec.p, device="cuda")
+        if kept:
+            dp.dp_clipped_sum_kept(desc, grads, f, dW, db, ws)
+        else:
+            dp.dp_clipped_sum(desc, A, G, f, dW, db, ws)
+        outs.append((dW, db))
+    torch.cuda.synchronize()
+    assert ((sq_k - sq_r).abs() / sq_r.abs()).max().item() <= 1e-5
+    for a, b in zip(outs[0], outs[1]):
+        assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() <= 1e-5

@@ -345,6 +345,71 @@ def test_device_wait_timeout_reported_and_context_usable(lib):
     assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
 
 
+# Kept per-example gradients: the instantiated norm stores g_i and b_i, the clipped sum
+# reads them back (conv through TMA im2col, linear per-example products, a conv layer on
+# its padded row layout).
+KEPT = [
+    ("conv_im2col", LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 3),
+    ("conv_im2col_s2_dil2_nobias", LayerSpec("e", "conv2d", p=136, Cin=128, H=23, W=23, k=3, stride=2, pad=2, dil=2,
+                                             has_bias=False), 2),
+    ("linear", LayerSpec("e", "linear", p=136, d=200, T=70), 5),
+    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4),
+]
+
+
+@pytest.mark.parametrize("tag,spec,B", KEPT, ids=[e[0] for e in KEPT])
+def test_kept_gradients_norm_and_sum(lib, tag, spec, B):
+    import torch
+    dp = lib
+    wl = Workload(name=tag, B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=17)
+    A, G = workloads.layer_inputs(wl, 0)
+    fac = workloads.factor_inputs(wl, B)
+    desc = desc_for(dp, spec, B, "bf16")
+    nbytes = dp.dp_grads_size(desc)
+    width = 32 if tag == "conv_rows_padD" else spec.D      # the padded row layout keeps 27 -> 32 columns
+    assert nbytes == 4 * B * spec.p * width + (4 * B * spec.p if spec.has_bias else 0)
+    grads = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    ws = torch.empty(dp.dp_workspace_size(desc, dp.DP_NORM_INSTANTIATE), dtype=torch.uint8, device="cuda")
+    Ad, Gd = to_dev(A, "bf16"), to_dev(G, "bf16")
+    sq = torch.empty(B, dtype=torch.float32, device="cuda")
+    dp.dp_layer_sqnorms_keep(desc, Ad, Gd, sq, grads, ws)
+    f = torch.tensor(fac, device="cuda")
+    dW = torch.empty(spec.p * spec.D, dtype=torch.float32, device="cuda")
+    db = torch.empty(spec.p, dtype=torch.float32, device="cuda") if spec.has_bias else None
+    dp.dp_clipped_sum_kept(desc, grads, f, dW, db, ws)
+    torch.cuda.synchronize()
+    assert rel_elem(sq.cpu().numpy(), oracle.layer_sqnorms(spec, A, G)) <= TOL["bf16"]
+    S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
+    assert rel_vec(dW.cpu().numpy(), S) <= TOL["bf16"]
+    if spec.has_bias:
+        assert rel_vec(db.cpu().numpy(), Sb) <= TOL["bf16"]
+    # accumulate: a second call adds the same sum
+    dp.dp_clipped_sum_kept(desc, grads, f, dW, db, ws, accumulate=True)
+    torch.cuda.synchronize()
+    assert rel_vec(dW.cpu().numpy(), 2 * S) <= TOL["bf16"]
+
+
+def test_kept_gradients_unsupported_layers(lib):
+    dp = lib
+    assert dp.dp_grads_size(dp.layer_desc(dp.DP_LINEAR, dp.DP_FP32, B=4, p=8, T=80, d=16)) == 0    # fp32
+    assert dp.dp_grads_size(dp.layer_desc(dp.DP_LINEAR, dp.DP_BF16, B=4, p=8, T=1, d=16)) == 0     # one row
+    assert dp.dp_grads_size(dp.layer_desc(dp.DP_LINEAR, dp.DP_BF16, B=4, p=12, T=80, d=16)) == 0   # p % 8
+
+
+def test_clip_step_with_kept_gradients(lib):
+    """A two-layer step with every instantiated layer keeping its gradients equals the oracle."""
+    l1 = LayerSpec("a", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1)
+    l2 = LayerSpec("b", "linear", p=136, d=200, T=70)
+    wl = Workload(name="kept_step", B=4, layers=(l1, l2), dtype="bf16", C=1.0, sigma=0.5, seed=23)
+    inputs = [workloads.layer_inputs(wl, l) for l in range(2)]
+    ref = oracle.dp_step(wl, inputs)
+    step = lib.ClipStep([desc_for(lib, s, wl.B, "bf16") for s in wl.layers], C=1.0, sigma=0.5,
+                        norm_modes=[lib.DP_NORM_INSTANTIATE] * 2, keep_grads=True)
+    assert all(k is not None for k in step.kept)
+    grad = step.run([(to_dev(A, "bf16"), to_dev(G, "bf16")) for A, G in inputs], seed=wl.seed)
+    assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+
+
 def test_mixed_scale_factors_straddle_bound(lib):
     """Some examples under C (factor exactly 1), some over; flat clipping over two layers."""
     import torch
