@@ -2,11 +2,10 @@
 //
 // When a layer's norm was formed by instantiating g_i ([MixGhost] section 3, the
 // FastGradClip side of the mixed clipping), the instantiating kernel can also store g_i
-// and b_i; the clipped sum is then dW = sum_i c_i g_i, db = sum_i c_i b_i ([FastClip]
-// section 2: clip each per-example gradient, then sum), 2pD flop per example read once,
-// instead of a second contraction over the T rows (2TpD).  The pages discuss this reuse
-// for instantiated layers in [MixGhost] sections 2-3 (storing the per-sample gradients
-// trades memory for time).
+// and b_i; the clipped sum is then the weighted gradient dW = sum_i c_i g_i, db =
+// sum_i c_i b_i formed from the stored per-sample gradients, as the Opacus approach of
+// [MixGhost] section 2 ("Previous arts") does -- fast but memory-costly -- at the 2BpD
+// time of its Appendix C.5, instead of a second contraction over the T rows (2BTpD).
 //
 // kept_wsum_kernel: examples split over blockIdx.y; thread = 4 consecutive elements of the
 // weight part (then of the bias part), summing c_i g_i over the split's examples in order;

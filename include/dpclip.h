@@ -178,10 +178,11 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
 /* ---- Kept per-example gradients (instantiated layers) --------------------------------
  * Where a layer's norm is formed by instantiation ([MixGhost] section 3, the FastGradClip
  * side of the mixed clipping), the instantiating kernel can also store every example's
- * gradient g_i and bias gradient b_i; the clipped sum is then sum_i c_i g_i over the stored
- * gradients (2pD flop per example, one read) instead of a second contraction over the T
- * rows (2TpD).  It trades B*(p*D + p)*4 bytes of device memory for that time, and pays off
- * when T is large (a few hundred rows and up).
+ * gradient g_i and bias gradient b_i; the clipped sum is then the weighted gradient
+ * sum_i c_i g_i of the stored gradients, as in the Opacus approach of [MixGhost] section 2
+ * (2pD flop per example, Appendix C.5; one read) instead of a second contraction over the
+ * T rows (2TpD).  It trades B*(p*D + p)*4 bytes of device memory for that time, and pays
+ * off when T is large (a few hundred rows and up).
  *
  * dp_grads_size: bytes of the `grads` buffer for `desc` (fp32, an internal layout), or 0
  * when the layer's instantiated norm does not run on a kernel that keeps gradients (it
