@@ -208,3 +208,4 @@ def dp_check_status(stream=None) -> int:
 
 
 from .step import ClipPipeline, ClipStep, VirtualStep  # noqa: E402,F401
+from .engine import PrivacyEngine  # noqa: E402,F401

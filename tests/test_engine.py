@@ -1,0 +1,101 @@
+"""PrivacyEngine: A and G captured by autograd hooks, the step through the C ABI.
+
+CPU: which models are accepted.  GPU: the privatised gradient equals the naive per-example
+loop of the pages (batch size 1, autograd per example) clipped and noised by the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+import torch.nn as nn
+
+import oracle
+
+
+def _model(dtype=torch.float32):
+    torch.manual_seed(0)
+    return nn.Sequential(nn.Conv2d(3, 8, 3, padding=1), nn.ReLU(), nn.Conv2d(8, 8, 3, stride=2, padding=1),
+                         nn.ReLU(), nn.Flatten(), nn.Linear(8 * 3 * 3, 16), nn.ReLU(), nn.Linear(16, 5)).to(dtype)
+
+
+def test_engine_accepts_linear_and_conv_only():
+    import example_gradient_clipping_gb300 as lib      # host only: hooks, no kernels
+    eng = lib.PrivacyEngine(_model())
+    assert len(eng.layers) == 4
+    eng.detach()
+    with pytest.raises(ValueError):
+        lib.PrivacyEngine(nn.Sequential(nn.Linear(4, 4), nn.LayerNorm(4)))
+    with pytest.raises(ValueError):
+        lib.PrivacyEngine(nn.Sequential(nn.Conv2d(4, 4, 3, groups=2)))
+    with pytest.raises(ValueError):
+        lib.PrivacyEngine(nn.Sequential(nn.Conv2d(4, 4, (3, 1))))
+    frozen = nn.Sequential(nn.Linear(4, 4), nn.LayerNorm(4))
+    for q in frozen[1].parameters():
+        q.requires_grad_(False)
+    lib.PrivacyEngine(frozen).detach()
+
+
+def _naive_reference(model, x, y, C, sigma, seed):
+    """The pages' naive method: one example at a time through autograd, then the oracle's
+    clip, sum and noise over the flat parameter vector [W_0, b_0, W_1, b_1, ...]."""
+    layers = [m for m in model.modules() if isinstance(m, (nn.Linear, nn.Conv2d))]
+    B = x.shape[0]
+    g = []
+    for i in range(B):
+        model.zero_grad()
+        loss = nn.functional.cross_entropy(model(x[i:i + 1]).float(), y[i:i + 1], reduction="sum")
+        loss.backward()
+        g.append(np.concatenate([np.concatenate([m.weight.grad.double().cpu().numpy().ravel(),
+                                                 m.bias.grad.double().cpu().numpy()]) for m in layers]))
+    g = np.stack(g)
+    n = np.sqrt((g * g).sum(1))
+    c = np.minimum(1.0, C / n)
+    return oracle.add_noise((c[:, None] * g).sum(0), sigma, C, B, seed)
+
+
+@pytest.fixture
+def no_tf32():
+    """fp32 convolutions and matmuls in full fp32 (cuDNN's TF32 default would round them)."""
+    saved = torch.backends.cudnn.allow_tf32, torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cudnn.allow_tf32 = torch.backends.cuda.matmul.allow_tf32 = False
+    yield
+    torch.backends.cudnn.allow_tf32, torch.backends.cuda.matmul.allow_tf32 = saved
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,tol", [(torch.float32, 1e-5), (torch.bfloat16, 2e-2)], ids=["fp32", "bf16"])
+def test_engine_matches_naive_per_example_loop(lib, no_tf32, dtype, tol):
+    model = _model(dtype).cuda()
+    gen = torch.Generator().manual_seed(1)
+    x = torch.randn(6, 3, 6, 6, generator=gen).to(dtype).cuda()
+    y = torch.randint(0, 5, (6,), generator=gen).cuda()
+    want = _naive_reference(model, x, y, C=0.5, sigma=0.3, seed=77)
+    eng = lib.PrivacyEngine(model, C=0.5, sigma=0.3)
+    model.zero_grad()
+    nn.functional.cross_entropy(model(x).float(), y, reduction="sum").backward()
+    flat = eng.privatise(seed=77)
+    got = flat.double().cpu().numpy()
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) <= tol
+    layers = [m for m in model.modules() if isinstance(m, (nn.Linear, nn.Conv2d))]
+    from_grads = np.concatenate([np.concatenate([m.weight.grad.double().cpu().numpy().ravel(),
+                                                 m.bias.grad.double().cpu().numpy()]) for m in layers])
+    if dtype == torch.float32:
+        np.testing.assert_array_equal(from_grads, got)       # .grad holds the privatised gradient
+    else:
+        assert np.linalg.norm(from_grads - got) / np.linalg.norm(got) <= 1e-2   # rounded to bf16
+    eng.detach()
+
+
+@pytest.mark.gpu
+def test_engine_mean_loss_equals_sum_loss(lib, no_tf32):
+    model = _model().cuda()
+    gen = torch.Generator().manual_seed(2)
+    x = torch.randn(5, 3, 6, 6, generator=gen).cuda()
+    y = torch.randint(0, 5, (5,), generator=gen).cuda()
+    outs = []
+    for red in ("sum", "mean"):
+        eng = lib.PrivacyEngine(model, C=0.5, sigma=0.3, loss_reduction=red)
+        model.zero_grad()
+        nn.functional.cross_entropy(model(x), y, reduction=red).backward()
+        outs.append(eng.privatise(seed=5).double().cpu().numpy())
+        eng.detach()
+    assert np.linalg.norm(outs[0] - outs[1]) / np.linalg.norm(outs[0]) <= 1e-5
