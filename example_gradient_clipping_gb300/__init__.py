@@ -63,6 +63,9 @@ def _load():
         "dp_check_status": (c_int, [c_void]),
         "dp_selftest_wait_timeout": (c_int, [c_void, c_void]),
         "dp_grads_size": (c_size, [PD]),
+        "dp_clipped_sum_reuse": (c_int, [PD, c_int, c_void, c_void, c_void, c_void, c_void, c_int, c_void, c_size,
+                                         c_void]),
+        "dp_layout_reused": (c_int, [PD, c_int]),
         "dp_layer_sqnorms_keep": (c_int, [PD, c_void, c_void, c_void, c_void, c_void, c_size, c_void]),
         "dp_clipped_sum_kept": (c_int, [PD, c_void, c_void, c_void, c_void, c_int, c_void, c_size, c_void]),
     }
@@ -171,6 +174,18 @@ def dp_adaptive_bound(sqnorms, B: int, C_l2: float, alpha: float, beta: float, s
                       seed: int, layer: int, out, stream=None) -> None:
     _check(_lib.dp_adaptive_bound(_ptr(sqnorms), B, C_l2, alpha, beta, sigma_l2, seed, layer, _ptr(out),
                                   _stream(stream)))
+
+
+def dp_clipped_sum_reuse(desc: LayerDesc, norm_mode: int, A, G, factors, dW, db=None, workspace=None,
+                         ws_bytes: Optional[int] = None, accumulate: bool = False, stream=None) -> None:
+    """dp_clipped_sum reading the layouts this layer's norm call left in `workspace`."""
+    _check(_lib.dp_clipped_sum_reuse(ctypes.byref(desc), norm_mode, _ptr(A), _ptr(G), _ptr(factors), _ptr(dW),
+                                     _ptr(db), int(bool(accumulate)), _ptr(workspace),
+                                     _ws_len(workspace) if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def dp_layout_reused(desc: LayerDesc, norm_mode: int = DP_NORM_AUTO) -> int:
+    return int(_lib.dp_layout_reused(ctypes.byref(desc), norm_mode))
 
 
 def dp_grads_size(desc: LayerDesc) -> int:

@@ -423,9 +423,17 @@ dp_status dp_clip_factors(const float* sqnorms, int B, int L, int per_layer, con
   return ok();
 }
 
-dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G,
-                         const float* factors, float* dW, float* db, int accumulate,
-                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+// Whether a dp_layer_sqnorms call in `norm_mode` leaves the NHWC copy of a conv layer's
+// input at the front of its workspace (the im2col ghost and instantiation kernels do).
+static bool norm_leaves_nhwc(const Geom& g, int norm_mode, int dtype, const void* A, const void* G, const void* ws) {
+  if (!g.conv || norm_mode < DP_NORM_AUTO || norm_mode > DP_NORM_AUTO_TIME || norm_mode == DP_NORM_T1) return false;
+  const Plan npl = norm_plan(g, resolve_mode(g, norm_mode), dtype, A, G, ws);
+  return npl.kernel == NK_TC_GHOST_CONV || npl.kernel == NK_TC_CONV;
+}
+
+static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, const void* G, const float* factors,
+                                  float* dW, float* db, int accumulate, void* workspace, size_t ws_bytes,
+                                  cudaStream_t stream, int reuse_norm_mode) {
   Geom g;
   dp_status st = make_geom(desc, &g);
   if (st != DP_OK) return st;
@@ -460,10 +468,13 @@ dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G
   }
   if (pl.kernel == 5)
     e = dph::launch_t1_sum(g, desc->dtype, A, G, factors, dW, db, accumulate, static_cast<float*>(wsp), stream);
-  else if (pl.kernel == 4)
-    e = dph::launch_tc_sum_conv(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
-  else if (pl.kernel == 3)
-    e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream);
+  else if (pl.kernel == 4 || pl.kernel == 3) {
+    const bool xh = reuse_norm_mode >= 0 && norm_leaves_nhwc(g, reuse_norm_mode, desc->dtype, A, G, workspace);
+    if (pl.kernel == 4)
+      e = dph::launch_tc_sum_conv(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, xh);
+    else
+      e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, xh);
+  }
   else if (pl.kernel == 6)
     e = dph::launch_tc_sum2(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
   else if (pl.kernel == 2)
@@ -557,6 +568,28 @@ dp_status dp_clipped_sum_kept(const dp_layer_desc* desc, const float* grads, con
   }
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum_kept launch");
   return ok();
+}
+
+dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G, const float* factors, float* dW,
+                         float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return clipped_sum_impl(desc, A, G, factors, dW, db, accumulate, workspace, ws_bytes, stream, -1);
+}
+
+dp_status dp_clipped_sum_reuse(const dp_layer_desc* desc, int norm_mode, const void* A, const void* G,
+                               const float* factors, float* dW, float* db, int accumulate, void* workspace,
+                               size_t ws_bytes, cudaStream_t stream) {
+  if (norm_mode < DP_NORM_AUTO || norm_mode > DP_NORM_AUTO_TIME)
+    return fail(DP_ERR_INVALID_ARG, "norm mode %d unknown", norm_mode);
+  return clipped_sum_impl(desc, A, G, factors, dW, db, accumulate, workspace, ws_bytes, stream, norm_mode);
+}
+
+int dp_layout_reused(const dp_layer_desc* desc, int norm_mode) {
+  Geom g;
+  if (make_geom(desc, &g) != DP_OK) return 0;
+  static const char al[16] __attribute__((aligned(16))) = {};
+  if (!norm_leaves_nhwc(g, norm_mode, desc->dtype, al, al, al)) return 0;
+  const Plan spl = sum_plan(g, desc->dtype, al, al, al);
+  return (spl.kernel == 4 || spl.kernel == 3) ? 1 : 0;
 }
 
 static dp_status add_noise_impl(float* grad, size_t n, float sigma, float C, int B, uint64_t seed,

@@ -490,13 +490,13 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
 }
 
 cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s) {
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, bool reuse_xh) {
   const ConvPlan c = conv_plan(g, false);
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* Xh = w;
   float* part = reinterpret_cast<float*>(w + nhwc_bytes(g));
   float* part_db = reinterpret_cast<float*>(w + nhwc_bytes(g) + al256((size_t)c.splits * g.p * c.items * 64 * 4));
-  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);
+  cudaError_t e = reuse_xh ? cudaSuccess : launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);
   if (e != cudaSuccess) return e;
   CUtensorMap mG, mX;
   if (!encode_maps(g, Xh, G, &mG, &mX)) return cudaErrorInvalidValue;

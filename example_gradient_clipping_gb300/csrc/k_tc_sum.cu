@@ -378,15 +378,17 @@ size_t tc_sum_conv_ws_bytes(const Geom& g) {
 }
 
 cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s) {
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, bool reuse_xh) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* Xh = w;
   void* Gt = w + al256s((size_t)g.B * g.H * g.W * g.Cin * 2);
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(Gt) + al256s((size_t)g.B * g.T * g.p * 2));
   float* part_db = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part) + al256s(tc_sum_ws_bytes(g)));
-  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
+  cudaError_t e = reuse_xh ? cudaSuccess : launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
   if (e != cudaSuccess) return e;
-  e = launch_scaled_rows(g.B, g.T, g.p, G, Gt, factors, db, accumulate, part_db, s);   // bf16(c_i G_i^T), db
+  // bf16(c_i G_i^T) and db in one pass, written right before the GEMM reads it (L2-hot);
+  // rereading a norm call's unscaled rows and scaling them in the GEMM measured slower
+  e = launch_scaled_rows(g.B, g.T, g.p, G, Gt, factors, db, accumulate, part_db, s);
   if (e != cudaSuccess) return e;
   const long R = (long)g.B * g.T;
   CUtensorMap mg, ma;

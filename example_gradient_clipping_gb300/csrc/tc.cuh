@@ -71,8 +71,10 @@ size_t tc_conv_ws_bytes(const Geom& g, bool norm);
 // tile column order ((channel block * k*k + tap) * 64 + channel) and its bias to keep_b [B, p].
 cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, float* out, void* ws,
                                 unsigned* status, cudaStream_t s, float* keep = nullptr, float* keep_b = nullptr);
+// reuse_xh: the workspace already holds the NHWC copy of the input (a norm call left it).
 cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
+                               bool reuse_xh = false);
 // im2col map (bf16, 128-byte swizzle, 64 channels per pixel) over an NHWC copy of a conv input.
 bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pixels);
 // dW[j, m] (+)= sum over splits of part[s, j, col(m)], col mapping the weight column
@@ -82,8 +84,10 @@ cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, 
 // Row-scaled clipped sum of a conv layer (Cin % 64 == 0) with im2col loads for the input.
 bool tc_sum_conv_supported(const Geom& g);
 size_t tc_sum_conv_ws_bytes(const Geom& g);
+// reuse_xh: the workspace already holds the NHWC copy of the input (a norm call left it).
 cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
+                               bool reuse_xh = false);
 // Ghost norm of a conv layer (Cin % 64 == 0) with im2col loads for the input Gram.
 bool tc_ghost_conv_supported(const Geom& g);
 size_t tc_ghost_conv_ws_bytes(const Geom& g);

@@ -11,8 +11,8 @@ from __future__ import annotations
 from typing import List, Optional, Sequence, Tuple
 
 from . import (DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_add_noise, dp_add_noise_devseed, dp_clip_factors,
-               dp_clipped_sum, dp_clipped_sum_kept, dp_grads_size, dp_launch_count, dp_layer_sqnorms,
-               dp_layer_sqnorms_keep, dp_plan, dp_workspace_size)
+               dp_clipped_sum, dp_clipped_sum_kept, dp_clipped_sum_reuse, dp_grads_size, dp_launch_count,
+               dp_layer_sqnorms, dp_layer_sqnorms_keep, dp_layout_reused, dp_plan, dp_workspace_size)
 
 # Instantiated layers with at least this many rows per example keep their per-example
 # gradients by default (the clipped sum then reads them once instead of recomputing a
@@ -60,6 +60,13 @@ class ClipStep:
             want = keep_grads is True or (keep_grads == "auto" and T >= KEEP_MIN_ROWS)
             nbytes = dp_grads_size(d) if (want and m == DP_NORM_INSTANTIATE) else 0
             self.kept.append(torch.empty(nbytes // 4, dtype=torch.float32, device=dev) if nbytes else None)
+        # conv layers whose clipped sum reuses the layouts their norm call wrote get a
+        # workspace of their own, so the layouts survive the other layers' calls
+        self.own_ws = []
+        for l, (d, m) in enumerate(zip(self.descs, self.modes)):
+            reuse = self.kept[l] is None and dp_layout_reused(d, m) > 0
+            self.own_ws.append(torch.empty(max(dp_workspace_size(d, m), 16), dtype=torch.uint8, device=dev)
+                               if reuse else None)
 
     def layer_views(self, l: int) -> Tuple:
         p, D = self.shapes[l]
@@ -74,8 +81,8 @@ class ClipStep:
                 dp_layer_sqnorms_keep(d, A, G, self.sqnorms[l], self.kept[l], self.workspace, stream=stream)
                 self.chosen[l] = DP_NORM_INSTANTIATE
             else:
-                self.chosen[l] = dp_layer_sqnorms(d, A, G, self.sqnorms[l], self.workspace, mode=self.modes[l],
-                                                  stream=stream)
+                ws = self.own_ws[l] if self.own_ws[l] is not None else self.workspace
+                self.chosen[l] = dp_layer_sqnorms(d, A, G, self.sqnorms[l], ws, mode=self.modes[l], stream=stream)
 
     def factors_(self, stream=None) -> None:
         L = len(self.descs)
@@ -88,6 +95,8 @@ class ClipStep:
             fac = self.factors[l] if self.per_layer else self.factors[0]
             if self.kept[l] is not None:
                 dp_clipped_sum_kept(d, self.kept[l], fac, dW, db, self.workspace, stream=stream)
+            elif self.own_ws[l] is not None:
+                dp_clipped_sum_reuse(d, self.modes[l], A, G, fac, dW, db, self.own_ws[l], stream=stream)
             else:
                 dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
 

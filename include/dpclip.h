@@ -175,6 +175,19 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
                             float sigma_l2, uint64_t seed, int layer, float* out,
                             cudaStream_t stream);
 
+/* ---- A layout shared by a layer's norm and sum calls ---------------------------------
+ * Conv layers on the im2col kernels work on an NHWC copy of the input, which both the norm
+ * and the sum call write at the front of the workspace.  dp_clipped_sum_reuse is
+ * dp_clipped_sum for a call whose `workspace` is the one this layer's dp_layer_sqnorms call
+ * (with `norm_mode`, the same desc, A and G) used, untouched since: it reads that copy
+ * instead of writing it again.  Results are undefined if anything else wrote the workspace
+ * in between.  dp_layout_reused reports, for aligned bf16 inputs, 1 when the copy is
+ * reused and 0 when the call is plain dp_clipped_sum.  Host only. */
+dp_status dp_clipped_sum_reuse(const dp_layer_desc* desc, int norm_mode, const void* A, const void* G,
+                               const float* factors, float* dW, float* db, int accumulate, void* workspace,
+                               size_t ws_bytes, cudaStream_t stream);
+int dp_layout_reused(const dp_layer_desc* desc, int norm_mode);
+
 /* ---- Kept per-example gradients (instantiated layers) --------------------------------
  * Where a layer's norm is formed by instantiation ([MixGhost] section 3, the FastGradClip
  * side of the mixed clipping), the instantiating kernel can also store every example's

@@ -410,6 +410,43 @@ def test_clip_step_with_kept_gradients(lib):
     assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
 
 
+# The clipped sum reading the NHWC input copy its layer's norm call left in the workspace:
+# after a ghost norm (the row-scaled GEMM) and after an instantiated norm (the per-example
+# conv kernel); a layer with no such copy (one-row fc) takes the plain path.
+REUSE = [
+    ("ghost_rows", LayerSpec("e", "conv2d", p=72, Cin=64, H=10, W=10, k=3, pad=1), 3, "GHOST", 1),
+    ("ghost_rows_s2_nobias", LayerSpec("e", "conv2d", p=136, Cin=128, H=15, W=15, k=3, stride=2, pad=1,
+                                       has_bias=False), 2, "GHOST", 1),
+    ("inst_nhwc", LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 3, "INSTANTIATE", 1),
+    ("linear_plain", LayerSpec("e", "linear", p=64, d=96, T=40), 3, "GHOST", 0),
+]
+
+
+@pytest.mark.parametrize("tag,spec,B,mode,level", REUSE, ids=[e[0] for e in REUSE])
+def test_clipped_sum_reuses_norm_layouts(lib, tag, spec, B, mode, level):
+    import torch
+    dp = lib
+    m = getattr(dp, "DP_NORM_" + mode)
+    wl = Workload(name=tag, B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=29)
+    A, G = workloads.layer_inputs(wl, 0)
+    fac = workloads.factor_inputs(wl, B)
+    desc = desc_for(dp, spec, B, "bf16")
+    assert dp.dp_layout_reused(desc, m) == level
+    ws = torch.empty(dp.dp_workspace_size(desc, m), dtype=torch.uint8, device="cuda")
+    Ad, Gd = to_dev(A, "bf16"), to_dev(G, "bf16")
+    sq = torch.empty(B, dtype=torch.float32, device="cuda")
+    dp.dp_layer_sqnorms(desc, Ad, Gd, sq, ws, mode=m)
+    f = torch.tensor(fac, device="cuda")
+    dW = torch.full((spec.p * spec.D,), 0.5, dtype=torch.float32, device="cuda")
+    db = torch.full((spec.p,), -1.0, dtype=torch.float32, device="cuda") if spec.has_bias else None
+    dp.dp_clipped_sum_reuse(desc, m, Ad, Gd, f, dW, db, ws, accumulate=True)
+    torch.cuda.synchronize()
+    S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
+    assert rel_vec(dW.cpu().numpy() - 0.5, S) <= TOL["bf16"]
+    if spec.has_bias:
+        assert rel_vec(db.cpu().numpy() + 1.0, Sb) <= TOL["bf16"]
+
+
 def test_mixed_scale_factors_straddle_bound(lib):
     """Some examples under C (factor exactly 1), some over; flat clipping over two layers."""
     import torch
