@@ -20,7 +20,8 @@ Layers: nn.Linear (inputs [B, ..., d]; the middle dimensions are the rows T) and
 nn.Conv2d (square kernel, equal stride / padding / dilation in both dimensions, groups 1,
 zero padding).  Every trainable parameter of the model must belong to such a layer.
 Activations right after them must not be in-place (the backward hook reads the layer's
-output gradient).
+output gradient).  PyTorch warns that the hook fires on output gradients when the model
+input needs no gradient; that gradient is the one wanted here.
 """
 from __future__ import annotations
 
