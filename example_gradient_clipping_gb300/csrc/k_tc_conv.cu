@@ -9,7 +9,8 @@
 // of two TMEM buffers.
 //   norm mode: the epilogue adds up P_i^2 over the tile -> part[tile, i]; a fixed-order
 //              sum over the tiles gives ||g_i||^2 (the instantiated norm of [MixGhost]
-//              section 3).
+//              section 3).  With `keep` it also stores P_i (tile column order) and b_i
+//              for the kept-gradient clipped sum.
 //   sum mode:  the epilogue folds c_i P_i into fp32 registers (the clip factor of
 //              [FastClip] section 5 applied in fp32) over the CTA's examples and
 //              writes a partial tile; a fixed-order reduction over the example splits

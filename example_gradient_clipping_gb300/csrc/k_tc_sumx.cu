@@ -9,13 +9,15 @@
 // with D += c_i * P_i.  No operand is rescaled or re-rounded, and no CUDA-core work
 // sits between a TMA load and the MMA that consumes it.  Rows of example i are loaded
 // with 3D TMA boxes [1, rows, 64] (rows past T read as zero): full 64-row stages,
-// then 16-row stages for the remainder.  In CTAs of the first column tile two warps
-// also sum the G rows from shared memory for the bias.  Examples are split across
-// the CTAs of a thread-block cluster (up to 8, one output tile): after the main loop
-// each CTA stages its fp32 partial tile in its own shared memory, and after a
-// cluster barrier each CTA adds one slice of rows from every peer over distributed
-// shared memory, in a fixed order, so the result is deterministic and needs no
-// global workspace.
+// then 16-row stages for the remainder.  In CTAs of the first column tile the
+// epilogue warps also sum the G rows from shared memory for the bias.  Examples are
+// split across the CTAs of a thread-block cluster (up to 4 per output tile): after
+// the main loop each CTA stages its fp32 partial tile in its own shared memory, and
+// after a cluster barrier each CTA adds one slice of rows from every peer over
+// distributed shared memory, in a fixed order, so the result is deterministic and
+// needs no global workspace.  When clusters of 4 cannot cover the GPU (few output
+// tiles), the examples are split over the grid instead: each CTA writes its partial
+// tile to the workspace and a second kernel sums the partials in split order.
 //   warpgroup 0: warps 0 and 2 TMA producers (alternate stages: one issuing thread
 //                streams only ~48 B/clk into an SM, two reach ~96), warp 1 MMA
 //                issuer, warp 3 reduces the bias across the cluster (64 registers
@@ -32,6 +34,8 @@
 // squared bias gradient ||sum_t G_i[t, :]||^2 over the tile's outputs in the first
 // column tile, and writes one partial per (tile, example); a fixed-order reduction
 // over the tiles gives ||g_i||^2.  No cluster: the examples are split over the grid.
+// With `keep`, the epilogue also stores P_i and the bias gradient of every example for
+// the kept-gradient clipped sum.
 #include <algorithm>
 
 #include "tc.cuh"
