@@ -135,9 +135,10 @@ size_t padded_out_bytes(const Geom& g) {
 }
 
 // Clipped-sum kernel: 0 SIMT, 1 row-scaled tensor-core GEMM, 2 per-example tensor-core
-// accumulation.  The per-example kernel splits the examples only over a cluster of <= 4
-// CTAs per output tile, so it serves layers with enough tiles to fill the GPU; the
-// row-scaled GEMM splits the batch rows over the whole grid.
+// accumulation (single CTA), 3 per-example conv kernel with TMA im2col loads, 4 the
+// row-scaled GEMM with im2col loads, 5 the one-row outer-product sum, 6 per-example on CTA
+// pairs (only when pinned).  The per-example kernels split the examples over clusters or
+// the grid; the row-scaled GEMM splits the batch rows over the whole grid.
 struct Plan {
   int kernel;
   bool rows;    // conv layer through its row layout
