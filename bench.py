@@ -48,6 +48,9 @@ def layer_desc(dp, spec, B, dtype):
     dt = dp.DP_BF16 if dtype == "bf16" else dp.DP_FP32
     if spec.kind == "linear":
         return dp.layer_desc(dp.DP_LINEAR, dt, B=B, p=spec.p, T=spec.T, d=spec.d, has_bias=spec.has_bias)
+    if spec.kind == "conv1d":
+        return dp.layer_desc(dp.DP_CONV1D, dt, B=B, p=spec.p, Cin=spec.Cin, H=1, W=spec.W, k=spec.k,
+                             stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
     return dp.layer_desc(dp.DP_CONV2D, dt, B=B, p=spec.p, Cin=spec.Cin, H=spec.H, W=spec.W, k=spec.k,
                          stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
 
@@ -72,8 +75,8 @@ def step_work(wl, modes, kept=None):
             flop_norm += wl.B * (2.0 * T * p * D + 2.0 * p * D)
         else:
             flop_norm += wl.B * 2.0 * (D + p)
-        a_el = spec.T * spec.d if spec.kind == "linear" else spec.Cin * spec.H * spec.W
-        g_el = spec.T * spec.p if spec.kind == "linear" else spec.p * spec.Hout * spec.Wout
+        a_el = int(np.prod(spec.a_example_shape()))
+        g_el = int(np.prod(spec.g_example_shape()))
         layer_in = wl.B * (a_el + g_el) * es
         in_bytes += layer_in
         if kp:

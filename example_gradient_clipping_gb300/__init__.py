@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libdpclip.so")
 
 DP_OK, DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_CUDA, DP_ERR_NONFINITE, DP_ERR_TIMEOUT = range(6)
 DP_BF16, DP_FP32 = 0, 1
-DP_LINEAR, DP_CONV2D = 0, 1
+DP_LINEAR, DP_CONV2D, DP_CONV1D = 0, 1, 2
 DP_NORM_AUTO, DP_NORM_GHOST, DP_NORM_INSTANTIATE, DP_NORM_T1, DP_NORM_AUTO_TIME = 0, 1, 2, 3, 4
 MODE_NAMES = {DP_NORM_GHOST: "ghost", DP_NORM_INSTANTIATE: "instantiate", DP_NORM_T1: "t1"}
 

@@ -19,7 +19,9 @@ struct Geom {
   int B, T, D, p;             // examples, rows, (unfolded) input width, outputs
   int d;                      // linear input width (== D for linear)
   int Cin, H, W, k, stride, pad, dil, Hout, Wout;
-  int conv;                   // 0 linear, 1 conv2d
+  int kh, padh;               // kernel height and vertical padding: k and pad (conv2d), 1 and 0
+                              // (conv1d: one input row, a 1 x k kernel)
+  int conv;                   // 0 linear, 1 conv2d or conv1d
   int has_bias;
 };
 
@@ -37,11 +39,11 @@ __device__ __forceinline__ float ld_g(const E* __restrict__ G, const Geom& g, in
 template <class E>
 __device__ __forceinline__ float ld_a(const E* __restrict__ A, const Geom& g, int i, int t, int m) {
   if (!g.conv) return to_f(A[((size_t)i * g.T + t) * g.d + m]);
-  const int kk = g.k * g.k;
+  const int kk = g.kh * g.k;
   const int c = m / kk, r = m - c * kk;
   const int kh = r / g.k, kw = r - kh * g.k;
   const int ho = t / g.Wout, wo = t - ho * g.Wout;
-  const int h = ho * g.stride - g.pad + kh * g.dil;
+  const int h = ho * g.stride - g.padh + kh * g.dil;
   const int w = wo * g.stride - g.pad + kw * g.dil;
   if (h < 0 || h >= g.H || w < 0 || w >= g.W) return 0.f;
   return to_f(A[(((size_t)i * g.Cin + c) * g.H + h) * g.W + w]);

@@ -4,8 +4,9 @@
 // section 3.1, eq. 3.1: U is the unfold of the input, F^{-1} flattens the output
 // gradient over positions).  These kernels write both factors in the row layout of
 // a linear layer, so the linear tensor-core kernels serve conv layers unchanged:
-//   U[i, t, m]  = x_i[c, ho*s - pad + kh*dil, wo*s - pad + kw*dil]  (0 outside the image)
-//                 t = ho*Wout + wo,  m = c*k*k + kh*k + kw  (torch.nn.functional.unfold order),
+//   U[i, t, m]  = x_i[c, ho*s - pad_h + kh*dil, wo*s - pad + kw*dil]  (0 outside the image)
+//                 t = ho*Wout + wo,  m = (c*k_h + kh)*k + kw  (torch.nn.functional.unfold order;
+//                 conv2d: k_h = k, pad_h = pad; conv1d: one input row, k_h = 1, pad_h = 0),
 //                 m < Dp: columns D <= m < Dp (Dp = D rounded up to 8) are zero
 //   Gt[i, t, j] = G_i[j, t]   (the NCHW output gradient, transposed per example)
 #include <algorithm>
@@ -22,7 +23,7 @@ __global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __r
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) __nv_bfloat16 xs[];     // [Cin][H][W]
-  const int kk = g.k * g.k;
+  const int kk = g.kh * g.k;
   const int cpr = Dp >> 3;                                // 16-byte chunks per output row
   const int HW = g.H * g.W;
   const int n_in = g.Cin * HW;
@@ -40,7 +41,7 @@ __global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __r
     for (int q = threadIdx.x; q < nch; q += blockDim.x) {
       const int t = q / cpr, m0 = (q - t * cpr) * 8;
       const int ho = t / g.Wout, wo = t - ho * g.Wout;
-      const int hb = ho * g.stride - g.pad, wb = wo * g.stride - g.pad;
+      const int hb = ho * g.stride - g.padh, wb = wo * g.stride - g.pad;
       // (c, kh, kw) of m0 once, then stepped along the chunk (no per-element division)
       int c = m0 / kk, r = m0 - c * kk;
       int kh = r / g.k, kw = r - kh * g.k;
@@ -52,7 +53,7 @@ __global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __r
                                                                          : __float2bfloat16_rn(0.f);
         if (++kw == g.k) {
           kw = 0;
-          if (++kh == g.k) { kh = 0; ++c; }
+          if (++kh == g.kh) { kh = 0; ++c; }
         }
       }
       *reinterpret_cast<uint4*>(out + (size_t)q * 8) = *reinterpret_cast<const uint4*>(v);
@@ -68,7 +69,7 @@ __global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restri
   pdl_trigger();
   pdl_wait();
   const int cpr = Dp >> 3;
-  const int kk = g.k * g.k;
+  const int kk = g.kh * g.k;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n_chunks;
        q += (size_t)gridDim.x * blockDim.x) {
     const size_t row = q / cpr;
@@ -82,7 +83,7 @@ __global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restri
       const int m = m0 + j;
       const int c = m / kk, r = m - c * kk;
       const int kh = r / g.k, kw = r - kh * g.k;
-      const int h = ho * g.stride - g.pad + kh * g.dil;
+      const int h = ho * g.stride - g.padh + kh * g.dil;
       const int w = wo * g.stride - g.pad + kw * g.dil;
       v[j] = (m < g.D && h >= 0 && h < g.H && w >= 0 && w < g.W) ? xi[((size_t)c * g.H + h) * g.W + w]
                                                                  : __float2bfloat16_rn(0.f);

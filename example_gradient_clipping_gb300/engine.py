@@ -16,9 +16,9 @@ Use (with a summed loss G_i is example i's own gradient; loss_reduction="mean" u
     engine.privatise(seed)                 # param.grad <- (sum_i c_i g_i + sigma C z) / B
     optimizer.step()
 
-Layers: nn.Linear (inputs [B, ..., d]; the middle dimensions are the rows T) and
-nn.Conv2d (square kernel, equal stride / padding / dilation in both dimensions, groups 1,
-zero padding).  Every trainable parameter of the model must belong to such a layer.
+Layers: nn.Linear (inputs [B, ..., d]; the middle dimensions are the rows T), nn.Conv2d
+(square kernel, equal stride / padding / dilation in both dimensions) and nn.Conv1d, both
+with groups 1 and zero padding.  Every trainable parameter of the model must belong to such a layer.
 Activations right after them must not be in-place (the backward hook reads the layer's
 output gradient).  PyTorch warns that the hook fires on output gradients when the model
 input needs no gradient; that gradient is the one wanted here.
@@ -27,7 +27,7 @@ from __future__ import annotations
 
 from typing import List, Optional
 
-from . import DP_BF16, DP_CONV2D, DP_FP32, DP_LINEAR, DP_NORM_AUTO, layer_desc
+from . import DP_BF16, DP_CONV1D, DP_CONV2D, DP_FP32, DP_LINEAR, DP_NORM_AUTO, layer_desc
 from .step import ClipStep
 
 
@@ -46,8 +46,8 @@ class PrivacyEngine:
         self.layers: List = []
         owned = set()
         for m in model.modules():
-            if isinstance(m, (nn.Linear, nn.Conv2d)) and m.weight.requires_grad:
-                if isinstance(m, nn.Conv2d):
+            if isinstance(m, (nn.Linear, nn.Conv2d, nn.Conv1d)) and m.weight.requires_grad:
+                if isinstance(m, (nn.Conv2d, nn.Conv1d)):
                     self._check_conv(m)
                 if m.bias is not None and not m.bias.requires_grad:
                     raise ValueError(f"{m}: a bias must be trainable with its weight")
@@ -57,10 +57,10 @@ class PrivacyEngine:
                     owned.add(id(m.bias))
         for name, prm in model.named_parameters():
             if prm.requires_grad and id(prm) not in owned:
-                raise ValueError(f"parameter {name}: only nn.Linear and nn.Conv2d layers have per-example "
+                raise ValueError(f"parameter {name}: only nn.Linear, nn.Conv2d and nn.Conv1d layers have per-example "
                                  "clipping here; freeze it or leave it out of the model")
         if not self.layers:
-            raise ValueError("the model has no trainable nn.Linear or nn.Conv2d layer")
+            raise ValueError("the model has no trainable nn.Linear, nn.Conv2d or nn.Conv1d layer")
         self._acts: List = [None] * len(self.layers)
         self._grads: List = [None] * len(self.layers)
         self._handles = []
@@ -73,9 +73,10 @@ class PrivacyEngine:
     @staticmethod
     def _check_conv(m) -> None:
         k, s, p, d = m.kernel_size, m.stride, m.padding, m.dilation
-        if (k[0] != k[1] or s[0] != s[1] or isinstance(p, str) or p[0] != p[1] or d[0] != d[1] or m.groups != 1
-                or m.padding_mode != "zeros"):
-            raise ValueError(f"{m}: square kernels, equal stride/padding/dilation, groups=1 and zero padding only")
+        if isinstance(p, str) or m.groups != 1 or m.padding_mode != "zeros":
+            raise ValueError(f"{m}: groups=1 and zero padding given as numbers only")
+        if len(k) == 2 and (k[0] != k[1] or s[0] != s[1] or p[0] != p[1] or d[0] != d[1]):
+            raise ValueError(f"{m}: square kernels with equal stride/padding/dilation in both dimensions only")
 
     def _fwd_hook(self, i):
         def hook(module, inputs, output):
@@ -101,6 +102,10 @@ class PrivacyEngine:
             if isinstance(m, nn.Linear):
                 T = a.numel() // (B * m.in_features)
                 out.append(layer_desc(DP_LINEAR, dtype, B=B, p=m.out_features, T=T, d=m.in_features, has_bias=hb))
+            elif isinstance(m, nn.Conv1d):
+                out.append(layer_desc(DP_CONV1D, dtype, B=B, p=m.out_channels, Cin=m.in_channels, H=1, W=a.shape[2],
+                                      k=m.kernel_size[0], stride=m.stride[0], pad=m.padding[0], dil=m.dilation[0],
+                                      has_bias=hb))
             else:
                 out.append(layer_desc(DP_CONV2D, dtype, B=B, p=m.out_channels, Cin=m.in_channels, H=a.shape[2],
                                       W=a.shape[3], k=m.kernel_size[0], stride=m.stride[0], pad=m.padding[0],

@@ -50,7 +50,7 @@ typedef enum {
 } dp_status;
 
 typedef enum { DP_BF16 = 0, DP_FP32 = 1 } dp_dtype;
-typedef enum { DP_LINEAR = 0, DP_CONV2D = 1 } dp_kind;
+typedef enum { DP_LINEAR = 0, DP_CONV2D = 1, DP_CONV1D = 2 } dp_kind;
 
 /* How the per-example norm is formed ([MixGhost] section 4, the layerwise decision). */
 typedef enum {
@@ -64,7 +64,9 @@ typedef enum {
 } dp_norm_mode;
 
 /* One layer.  Linear uses B, T, d, p; conv2d uses B, Cin, H, W, p, k, stride, pad, dil
- * (square kernel; Hout = (H + 2 pad - dil (k-1) - 1)/stride + 1, likewise Wout). */
+ * (square kernel; Hout = (H + 2 pad - dil (k-1) - 1)/stride + 1, likewise Wout); conv1d
+ * uses B, Cin, W (the length), p, k, stride, pad, dil (A [B, Cin, W], G [B, p, Wout],
+ * weight gradient [p, Cin, k]; H is ignored). */
 typedef struct {
   int kind;      /* dp_kind */
   int dtype;     /* dp_dtype of A and G */

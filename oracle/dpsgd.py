@@ -50,6 +50,26 @@ def unfold2d(x: np.ndarray, k: int, stride: int = 1, pad: int = 0, dil: int = 1)
     return U
 
 
+def unfold1d(x: np.ndarray, k: int, stride: int = 1, pad: int = 0, dil: int = 1) -> np.ndarray:
+    """U(a_i) of a 1-D convolution: one example x [Cin, L] -> [Lout, Cin*k].
+
+    The 1-D case of the unfold ([MixGhost] section 2.3 and Appendix B treat 1D to 3D
+    convolutions alike): row t = output position, column c*k + kw (the order of a
+    PyTorch Conv1d weight [p, Cin, k]); taps outside the input read the zero padding.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    Cin, L = x.shape
+    Lout = (L + 2 * pad - dil * (k - 1) - 1) // stride + 1
+    U = np.zeros((Lout, Cin * k))
+    for t in range(Lout):
+        for c in range(Cin):
+            for kw in range(k):
+                pos = t * stride - pad + kw * dil
+                if 0 <= pos < L:
+                    U[t, c * k + kw] = x[c, pos]
+    return U
+
+
 def per_example_grad(spec, a_i: np.ndarray, g_i: np.ndarray):
     """Materialised per-example gradient of one layer: (weight [p, D], bias [p]).
 
@@ -68,6 +88,11 @@ def per_example_grad(spec, a_i: np.ndarray, g_i: np.ndarray):
     elif spec.kind == "conv2d":
         U = unfold2d(a_i, spec.k, spec.stride, spec.pad, spec.dil)
         Gm = g.reshape(spec.p, spec.Hout * spec.Wout)      # F^{-1}: flatten the output map
+        gw = Gm @ U
+        gb = Gm.sum(axis=1)
+    elif spec.kind == "conv1d":
+        U = unfold1d(a_i, spec.k, spec.stride, spec.pad, spec.dil)
+        Gm = g.reshape(spec.p, spec.Wout)
         gw = Gm @ U
         gb = Gm.sum(axis=1)
     else:

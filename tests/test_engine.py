@@ -41,7 +41,7 @@ def test_engine_accepts_linear_and_conv_only():
 def _naive_reference(model, x, y, C, sigma, seed):
     """The pages' naive method: one example at a time through autograd, then the oracle's
     clip, sum and noise over the flat parameter vector [W_0, b_0, W_1, b_1, ...]."""
-    layers = [m for m in model.modules() if isinstance(m, (nn.Linear, nn.Conv2d))]
+    layers = [m for m in model.modules() if isinstance(m, (nn.Linear, nn.Conv2d, nn.Conv1d))]
     B = x.shape[0]
     g = []
     for i in range(B):
@@ -87,6 +87,23 @@ def test_engine_matches_naive_per_example_loop(lib, no_tf32, dtype, tol):
     else:
         assert np.linalg.norm(from_grads - got) / np.linalg.norm(got) <= 1e-2   # rounded to bf16
     eng.detach()
+
+
+@pytest.mark.gpu
+def test_engine_conv1d_model(lib, no_tf32):
+    torch.manual_seed(3)
+    model = nn.Sequential(nn.Conv1d(4, 8, 3, padding=1), nn.ReLU(), nn.Conv1d(8, 8, 5, stride=2, padding=2),
+                          nn.ReLU(), nn.Flatten(), nn.Linear(8 * 10, 5)).cuda()
+    gen = torch.Generator().manual_seed(4)
+    x = torch.randn(6, 4, 20, generator=gen).cuda()
+    y = torch.randint(0, 5, (6,), generator=gen).cuda()
+    want = _naive_reference(model, x, y, C=0.5, sigma=0.3, seed=8)
+    eng = lib.PrivacyEngine(model, C=0.5, sigma=0.3)
+    model.zero_grad()
+    nn.functional.cross_entropy(model(x), y, reduction="sum").backward()
+    got = eng.privatise(seed=8).double().cpu().numpy()
+    eng.detach()
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 1e-5
 
 
 @pytest.mark.gpu

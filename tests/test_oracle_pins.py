@@ -86,6 +86,29 @@ def test_conv_per_example_grad_matches_autograd(Cin, H, W, p, k, stride, pad, di
     np.testing.assert_allclose(gw, cw.reshape(p, -1).numpy(), rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("Cin,L,p,k,stride,pad,dil", [
+    (3, 20, 4, 3, 1, 1, 1), (2, 17, 3, 5, 2, 2, 1), (4, 9, 5, 1, 1, 0, 1), (2, 15, 3, 3, 1, 2, 2)])
+def test_conv1d_per_example_grad_matches_autograd(Cin, L, p, k, stride, pad, dil):
+    rng = np.random.default_rng(5)
+    spec = LayerSpec("c1", "conv1d", p=p, Cin=Cin, W=L, k=k, stride=stride, pad=pad, dil=dil)
+    a = _rand(rng, Cin, L)
+    g = _rand(rng, p, spec.Wout)
+    gw, gb = dpsgd.per_example_grad(spec, a, g)
+    x = torch.tensor(a)[None]
+    W = torch.zeros(p, Cin, k, dtype=torch.float64, requires_grad=True)
+    b = torch.zeros(p, dtype=torch.float64, requires_grad=True)
+    out = torch.nn.functional.conv1d(x, W, b, stride=stride, padding=pad, dilation=dil)
+    assert out.shape[1:] == g.shape
+    (out[0] * torch.tensor(g)).sum().backward()
+    np.testing.assert_allclose(gw, W.grad.reshape(p, -1).numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gb, b.grad.numpy(), rtol=1e-12, atol=1e-12)
+    # a conv1d is the conv2d of one input row with a 1 x k kernel
+    U1 = dpsgd.unfold1d(a, k, stride, pad, dil)
+    tu = torch.nn.functional.unfold(torch.tensor(a)[:, None, :][None], (1, k), dilation=(1, dil),
+                                    padding=(0, pad), stride=(1, stride))
+    np.testing.assert_array_equal(U1, tu[0].T.numpy())
+
+
 @pytest.mark.parametrize("k,stride,pad,dil", [(3, 1, 1, 1), (3, 2, 0, 1), (2, 1, 1, 2), (1, 1, 0, 1)])
 def test_unfold_matches_torch_unfold(k, stride, pad, dil):
     rng = np.random.default_rng(3)

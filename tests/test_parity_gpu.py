@@ -200,6 +200,12 @@ EDGE = [
     # one row block (64 < T <= 128): the ghost norm with single-block pairs
     ("lin_ghost_split", LayerSpec("e", "linear", p=136, d=200, T=100), 3, "bf16"),
     ("conv_im2col_ghost_split", LayerSpec("e", "conv2d", p=72, Cin=64, H=10, W=10, k=3, pad=1), 2, "bf16"),
+    # conv1d: the row layout on the tensor cores (p % 8 == 0), else the FFMA kernels
+    ("conv1d_rows", LayerSpec("e", "conv1d", p=16, Cin=8, W=50, k=5, stride=2, pad=2), 4, "bf16"),
+    ("conv1d_rows_dil_nobias", LayerSpec("e", "conv1d", p=24, Cin=3, W=70, k=3, dil=2, has_bias=False), 3, "bf16"),
+    ("conv1d_long", LayerSpec("e", "conv1d", p=64, Cin=32, W=300, k=3, pad=1), 2, "bf16"),
+    ("conv1d_fp32", LayerSpec("e", "conv1d", p=6, Cin=5, W=21, k=3, pad=1), 3, "fp32"),
+    ("conv1d_k1", LayerSpec("e", "conv1d", p=8, Cin=64, W=40, k=1), 3, "bf16"),
     # one row block: T just above the packed limit, batches of about half the SM count
     ("lin_ghost_slab_T65", LayerSpec("e", "linear", p=40, d=48, T=65), 5, "bf16"),
     ("lin_ghost_slab_B76", LayerSpec("e", "linear", p=64, d=72, T=128), 76, "bf16"),

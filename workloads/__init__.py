@@ -13,6 +13,7 @@ workloads that way) and the full batch is the concatenation of the examples.
 Layer layouts follow PyTorch conventions:
   linear  A [B, T, d]  (layer inputs a_{i,t}),  G [B, T, p]  (output grads)
   conv2d  A [B, Cin, H, W] (NCHW input),        G [B, p, Hout, Wout]
+  conv1d  A [B, Cin, W] (NCL input),              G [B, p, Wout]
 bf16 workloads draw fp32 values and round them to bf16 (round to nearest
 even); both sides read the rounded values.
 """
@@ -34,13 +35,13 @@ __all__ = [
 class LayerSpec:
     """One layer's shapes and the distribution of its captured tensors."""
     name: str
-    kind: str                 # "linear" or "conv2d"
+    kind: str                 # "linear", "conv2d" or "conv1d"
     p: int                    # output features / output channels
     d: int = 0                # linear: input features
     T: int = 1                # linear: rows (tokens) per example
-    Cin: int = 0              # conv2d: input channels
-    H: int = 0
-    W: int = 0
+    Cin: int = 0              # conv: input channels
+    H: int = 0                # conv2d only
+    W: int = 0                # conv2d width, conv1d length
     k: int = 1
     stride: int = 1
     pad: int = 0
@@ -58,7 +59,7 @@ class LayerSpec:
 
     @property
     def Wout(self) -> int:
-        if self.kind != "conv2d":
+        if self.kind == "linear":
             return 1
         return (self.W + 2 * self.pad - self.dil * (self.k - 1) - 1) // self.stride + 1
 
@@ -70,7 +71,9 @@ class LayerSpec:
     @property
     def D(self) -> int:
         """Width of the (unfolded) input: d, or Cin*k*k."""
-        return self.d if self.kind == "linear" else self.Cin * self.k * self.k
+        if self.kind == "linear":
+            return self.d
+        return self.Cin * self.k * (self.k if self.kind == "conv2d" else 1)
 
     @property
     def n_weight(self) -> int:
@@ -81,10 +84,14 @@ class LayerSpec:
         return self.n_weight + (self.p if self.has_bias else 0)
 
     def a_example_shape(self) -> Tuple[int, ...]:
-        return (self.T, self.d) if self.kind == "linear" else (self.Cin, self.H, self.W)
+        if self.kind == "linear":
+            return (self.T, self.d)
+        return (self.Cin, self.H, self.W) if self.kind == "conv2d" else (self.Cin, self.W)
 
     def g_example_shape(self) -> Tuple[int, ...]:
-        return (self.T, self.p) if self.kind == "linear" else (self.p, self.Hout, self.Wout)
+        if self.kind == "linear":
+            return (self.T, self.p)
+        return (self.p, self.Hout, self.Wout) if self.kind == "conv2d" else (self.p, self.Wout)
 
 
 @dataclass(frozen=True)
