@@ -48,6 +48,9 @@ def layer_desc(dp, spec, B, dtype):
     dt = dp.DP_BF16 if dtype == "bf16" else dp.DP_FP32
     if spec.kind == "linear":
         return dp.layer_desc(dp.DP_LINEAR, dt, B=B, p=spec.p, T=spec.T, d=spec.d, has_bias=spec.has_bias)
+    if spec.kind == "conv3d":
+        return dp.layer_desc(dp.DP_CONV3D, dt, B=B, p=spec.p, Cin=spec.Cin, Z=spec.Z, H=spec.H, W=spec.W, k=spec.k,
+                             stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
     if spec.kind == "conv1d":
         return dp.layer_desc(dp.DP_CONV1D, dt, B=B, p=spec.p, Cin=spec.Cin, H=1, W=spec.W, k=spec.k,
                              stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)

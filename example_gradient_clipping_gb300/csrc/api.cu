@@ -76,9 +76,28 @@ dp_status make_geom(const dp_layer_desc* d, Geom* g) {
     g->Cin = d->Cin; g->H = d->H; g->W = d->W; g->k = d->k;
     g->stride = d->stride; g->pad = d->pad; g->dil = d->dil;
     g->kh = d->k; g->padh = d->pad;
+    g->Z = 1; g->Zout = 1; g->kz = 1; g->padz = 0;
     g->Hout = (int)Ho; g->Wout = (int)Wo;
     g->T = (int)(Ho * Wo);
     g->D = d->Cin * d->k * d->k;
+    g->d = g->D;
+  } else if (d->kind == DP_CONV3D) {
+    if (d->Cin <= 0 || d->Z <= 0 || d->H <= 0 || d->W <= 0 || d->k <= 0 || d->stride <= 0 || d->pad < 0 ||
+        d->dil <= 0)
+      return fail(DP_ERR_INVALID_ARG, "conv3d needs Cin, Z, H, W, k, stride, dil > 0 and pad >= 0");
+    auto out = [&](int n) { return ((long)n + 2L * d->pad - (long)d->dil * (d->k - 1) - 1) / d->stride + 1; };
+    const long Zo = out(d->Z), Ho = out(d->H), Wo = out(d->W);
+    if (Zo <= 0 || Ho <= 0 || Wo <= 0) return fail(DP_ERR_INVALID_ARG, "conv3d output is empty");
+    if ((double)Zo * Ho * Wo > 2e9 || (double)d->Cin * d->k * d->k * d->k > 2e9)
+      return fail(DP_ERR_UNSUPPORTED, "conv3d layer too large for 32-bit indexing");
+    g->conv = 1;
+    g->Cin = d->Cin; g->H = d->H; g->W = d->W; g->k = d->k;
+    g->stride = d->stride; g->pad = d->pad; g->dil = d->dil;
+    g->kh = d->k; g->padh = d->pad;
+    g->Z = d->Z; g->Zout = (int)Zo; g->kz = d->k; g->padz = d->pad;
+    g->Hout = (int)Ho; g->Wout = (int)Wo;
+    g->T = (int)(Zo * Ho * Wo);
+    g->D = d->Cin * d->k * d->k * d->k;
     g->d = g->D;
   } else if (d->kind == DP_CONV1D) {
     // one input row [Cin, W], a 1 x k kernel: stride, padding and dilation along W only
@@ -90,12 +109,13 @@ dp_status make_geom(const dp_layer_desc* d, Geom* g) {
     g->Cin = d->Cin; g->H = 1; g->W = d->W; g->k = d->k;
     g->stride = d->stride; g->pad = d->pad; g->dil = d->dil;
     g->kh = 1; g->padh = 0;
+    g->Z = 1; g->Zout = 1; g->kz = 1; g->padz = 0;
     g->Hout = 1; g->Wout = (int)Wo;
     g->T = (int)Wo;
     g->D = d->Cin * d->k;
     g->d = g->D;
   } else {
-    return fail(DP_ERR_INVALID_ARG, "kind %d is not DP_LINEAR, DP_CONV2D or DP_CONV1D", d->kind);
+    return fail(DP_ERR_INVALID_ARG, "kind %d is not DP_LINEAR, DP_CONV2D, DP_CONV1D or DP_CONV3D", d->kind);
   }
   // element counts must fit the kernels' 32-bit per-example and 64-bit global indexing
   if ((double)g->T * g->D > 2e9 || (double)g->T * g->p > 2e9 || (double)g->p * g->D > 2e9)

@@ -19,9 +19,11 @@ struct Geom {
   int B, T, D, p;             // examples, rows, (unfolded) input width, outputs
   int d;                      // linear input width (== D for linear)
   int Cin, H, W, k, stride, pad, dil, Hout, Wout;
-  int kh, padh;               // kernel height and vertical padding: k and pad (conv2d), 1 and 0
-                              // (conv1d: one input row, a 1 x k kernel)
-  int conv;                   // 0 linear, 1 conv2d or conv1d
+  int kh, padh;               // kernel height and vertical padding: k and pad (conv2d, conv3d),
+                              // 1 and 0 (conv1d: one input row, a 1 x k kernel)
+  int Z, Zout, kz, padz;      // input depth, output depth, kernel depth, depth padding: conv3d,
+                              // else 1, 1, 1, 0
+  int conv;                   // 0 linear, 1 conv1d, conv2d or conv3d
   int has_bias;
 };
 
@@ -39,14 +41,20 @@ __device__ __forceinline__ float ld_g(const E* __restrict__ G, const Geom& g, in
 template <class E>
 __device__ __forceinline__ float ld_a(const E* __restrict__ A, const Geom& g, int i, int t, int m) {
   if (!g.conv) return to_f(A[((size_t)i * g.T + t) * g.d + m]);
-  const int kk = g.kh * g.k;
+  // m = ((c*kz + kd)*kh + kh_)*k + kw, t = (zo*Hout + ho)*Wout + wo (PyTorch unfold order)
+  const int kk = g.kz * g.kh * g.k;
   const int c = m / kk, r = m - c * kk;
-  const int kh = r / g.k, kw = r - kh * g.k;
-  const int ho = t / g.Wout, wo = t - ho * g.Wout;
+  const int khk = g.kh * g.k;
+  const int kd = r / khk, r2 = r - kd * khk;
+  const int kh = r2 / g.k, kw = r2 - kh * g.k;
+  const int hw = g.Hout * g.Wout;
+  const int zo = t / hw, t2 = t - zo * hw;
+  const int ho = t2 / g.Wout, wo = t2 - ho * g.Wout;
+  const int z = zo * g.stride - g.padz + kd * g.dil;
   const int h = ho * g.stride - g.padh + kh * g.dil;
   const int w = wo * g.stride - g.pad + kw * g.dil;
-  if (h < 0 || h >= g.H || w < 0 || w >= g.W) return 0.f;
-  return to_f(A[(((size_t)i * g.Cin + c) * g.H + h) * g.W + w]);
+  if (z < 0 || z >= g.Z || h < 0 || h >= g.H || w < 0 || w >= g.W) return 0.f;
+  return to_f(A[((((size_t)i * g.Cin + c) * g.Z + z) * g.H + h) * g.W + w]);
 }
 
 // Programmatic dependent launch: every library kernel is launched with programmatic

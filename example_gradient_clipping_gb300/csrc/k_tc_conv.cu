@@ -371,7 +371,7 @@ static PFN_cuTensorMapEncodeIm2col_v12000 im2col_fn() {
 
 bool tc_conv_supported(const Geom& g) {
   if (!g.conv || g.Cin % 64 || g.T % 8 || g.T < 64 || g.p < 8) return false;
-  if (g.kh != g.k || g.padh != g.pad) return false;   // square kernels (TMA im2col)
+  if (g.kh != g.k || g.padh != g.pad || g.Z != 1 || g.kz != 1) return false;   // square 2D kernels (TMA im2col)
   if (g.stride > 8 || g.pad > 127 || g.dil * (g.k - 1) - g.pad > 128 || g.dil * (g.k - 1) > 65535) return false;
   return (double)g.B * g.H * g.W * g.Cin < 4e9;
 }

@@ -441,7 +441,7 @@ static int ghost_ept(const Geom& g) { return 2 * g.T <= tcghost::BT ? tcghost::B
 // G-Gram reads the output gradient in its row layout [B, T, p].  Workspace: the NHWC
 // copy, then the row layout of G.
 bool tc_ghost_conv_supported(const Geom& g) {
-  if (g.kh != g.k || g.padh != g.pad) return false;   // square kernels (TMA im2col)
+  if (g.kh != g.k || g.padh != g.pad || g.Z != 1 || g.kz != 1) return false;   // square 2D kernels (TMA im2col)
   return g.conv && g.Cin % 64 == 0 && g.p % 8 == 0 && g.T >= 2 && g.T <= 512 && g.stride <= 8 &&
          g.pad <= 127 && g.dil * (g.k - 1) - g.pad <= 128 && (double)g.B * g.H * g.W * g.Cin < 4e9;
 }

@@ -365,7 +365,7 @@ cudaError_t launch_tc_sum_prescaled(const Geom& g, const void* A, const void* Gs
 // NHWC copy of the input, the output gradient from its row layout [B*T, p].  Workspace:
 // the NHWC copy, the row layout of G, then the split partials.
 bool tc_sum_conv_supported(const Geom& g) {
-  if (g.kh != g.k || g.padh != g.pad) return false;   // square kernels (TMA im2col)
+  if (g.kh != g.k || g.padh != g.pad || g.Z != 1 || g.kz != 1) return false;   // square 2D kernels (TMA im2col)
   return g.conv && g.Cin % 64 == 0 && g.p % 8 == 0 && g.stride <= 8 && g.pad <= 127 &&
          g.dil * (g.k - 1) - g.pad <= 128 && (double)g.B * g.H * g.W * g.Cin < 4e9 &&
          (long)g.B * g.T < (1L << 31);

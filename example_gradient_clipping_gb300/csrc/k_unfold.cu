@@ -4,9 +4,11 @@
 // section 3.1, eq. 3.1: U is the unfold of the input, F^{-1} flattens the output
 // gradient over positions).  These kernels write both factors in the row layout of
 // a linear layer, so the linear tensor-core kernels serve conv layers unchanged:
-//   U[i, t, m]  = x_i[c, ho*s - pad_h + kh*dil, wo*s - pad + kw*dil]  (0 outside the image)
-//                 t = ho*Wout + wo,  m = (c*k_h + kh)*k + kw  (torch.nn.functional.unfold order;
-//                 conv2d: k_h = k, pad_h = pad; conv1d: one input row, k_h = 1, pad_h = 0),
+//   U[i, t, m]  = x_i[c, zo*s - pad_z + kd*dil, ho*s - pad_h + kh*dil, wo*s - pad + kw*dil]
+//                 (0 outside the input), t = (zo*Hout + ho)*Wout + wo,
+//                 m = ((c*k_z + kd)*k_h + kh)*k + kw  (the order of a PyTorch weight;
+//                 conv2d: k_z = 1, k_h = k; conv1d: one input row, k_z = k_h = 1; conv3d:
+//                 a cubic kernel, the 2-D staging kernel does not take it),
 //                 m < Dp: columns D <= m < Dp (Dp = D rounded up to 8) are zero
 //   Gt[i, t, j] = G_i[j, t]   (the NCHW output gradient, transposed per example)
 #include <algorithm>
@@ -69,24 +71,29 @@ __global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restri
   pdl_trigger();
   pdl_wait();
   const int cpr = Dp >> 3;
-  const int kk = g.kh * g.k;
+  const int khk = g.kh * g.k, kk = g.kz * khk;
+  const int hw = g.Hout * g.Wout;
   for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n_chunks;
        q += (size_t)gridDim.x * blockDim.x) {
     const size_t row = q / cpr;
     const int m0 = (int)(q - row * cpr) * 8;
     const int i = (int)(row / g.T), t = (int)(row - (size_t)i * g.T);
-    const int ho = t / g.Wout, wo = t - ho * g.Wout;
-    const __nv_bfloat16* xi = x + (size_t)i * g.Cin * g.H * g.W;
+    const int zo = t / hw, t2 = t - zo * hw;
+    const int ho = t2 / g.Wout, wo = t2 - ho * g.Wout;
+    const __nv_bfloat16* xi = x + (size_t)i * g.Cin * g.Z * g.H * g.W;
     __align__(16) __nv_bfloat16 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int m = m0 + j;
       const int c = m / kk, r = m - c * kk;
-      const int kh = r / g.k, kw = r - kh * g.k;
+      const int kd = r / khk, r2 = r - kd * khk;
+      const int kh = r2 / g.k, kw = r2 - kh * g.k;
+      const int z = zo * g.stride - g.padz + kd * g.dil;
       const int h = ho * g.stride - g.padh + kh * g.dil;
       const int w = wo * g.stride - g.pad + kw * g.dil;
-      v[j] = (m < g.D && h >= 0 && h < g.H && w >= 0 && w < g.W) ? xi[((size_t)c * g.H + h) * g.W + w]
-                                                                 : __float2bfloat16_rn(0.f);
+      v[j] = (m < g.D && z >= 0 && z < g.Z && h >= 0 && h < g.H && w >= 0 && w < g.W)
+                 ? xi[(((size_t)c * g.Z + z) * g.H + h) * g.W + w]
+                 : __float2bfloat16_rn(0.f);
     }
     *reinterpret_cast<uint4*>(U + q * 8) = *reinterpret_cast<const uint4*>(v);
   }
@@ -233,7 +240,7 @@ cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* 
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   auto* Ub = static_cast<__nv_bfloat16*>(U);
   const size_t stage = (size_t)g.Cin * g.H * g.W * sizeof(__nv_bfloat16);
-  if (stage <= (size_t)kUnfoldSmemMax) {
+  if (g.Z == 1 && g.kz == 1 && stage <= (size_t)kUnfoldSmemMax) {     // 1-D and 2-D inputs staged whole
     if (stage > 48 * 1024) {
       int dev = 0;
       cudaGetDevice(&dev);

@@ -16,9 +16,9 @@ Use (with a summed loss G_i is example i's own gradient; loss_reduction="mean" u
     engine.privatise(seed)                 # param.grad <- (sum_i c_i g_i + sigma C z) / B
     optimizer.step()
 
-Layers: nn.Linear (inputs [B, ..., d]; the middle dimensions are the rows T), nn.Conv2d
-(square kernel, equal stride / padding / dilation in both dimensions) and nn.Conv1d, both
-with groups 1 and zero padding.  Every trainable parameter of the model must belong to such a layer.
+Layers: nn.Linear (inputs [B, ..., d]; the middle dimensions are the rows T), nn.Conv1d,
+nn.Conv2d and nn.Conv3d (square or cubic kernels, equal stride / padding / dilation in every
+dimension), the conv layers with groups 1 and zero padding.  Every trainable parameter of the model must belong to such a layer.
 Activations right after them must not be in-place (the backward hook reads the layer's
 output gradient).  PyTorch warns that the hook fires on output gradients when the model
 input needs no gradient; that gradient is the one wanted here.
@@ -27,7 +27,7 @@ from __future__ import annotations
 
 from typing import List, Optional
 
-from . import DP_BF16, DP_CONV1D, DP_CONV2D, DP_FP32, DP_LINEAR, DP_NORM_AUTO, layer_desc
+from . import DP_BF16, DP_CONV1D, DP_CONV2D, DP_CONV3D, DP_FP32, DP_LINEAR, DP_NORM_AUTO, layer_desc
 from .step import ClipStep
 
 
@@ -37,6 +37,7 @@ class PrivacyEngine:
         """loss_reduction: "sum" (G_i as captured) or "mean" (the captured output gradients
         carry a 1/B factor, undone before the norms)."""
         import torch.nn as nn
+        convs = (nn.Conv1d, nn.Conv2d, nn.Conv3d)
         if loss_reduction not in ("sum", "mean"):
             raise ValueError("loss_reduction is 'sum' or 'mean'")
         self.loss_reduction = loss_reduction
@@ -46,8 +47,8 @@ class PrivacyEngine:
         self.layers: List = []
         owned = set()
         for m in model.modules():
-            if isinstance(m, (nn.Linear, nn.Conv2d, nn.Conv1d)) and m.weight.requires_grad:
-                if isinstance(m, (nn.Conv2d, nn.Conv1d)):
+            if isinstance(m, (nn.Linear,) + convs) and m.weight.requires_grad:
+                if isinstance(m, convs):
                     self._check_conv(m)
                 if m.bias is not None and not m.bias.requires_grad:
                     raise ValueError(f"{m}: a bias must be trainable with its weight")
@@ -57,10 +58,10 @@ class PrivacyEngine:
                     owned.add(id(m.bias))
         for name, prm in model.named_parameters():
             if prm.requires_grad and id(prm) not in owned:
-                raise ValueError(f"parameter {name}: only nn.Linear, nn.Conv2d and nn.Conv1d layers have per-example "
+                raise ValueError(f"parameter {name}: only nn.Linear and nn.Conv1d/2d/3d layers have per-example "
                                  "clipping here; freeze it or leave it out of the model")
         if not self.layers:
-            raise ValueError("the model has no trainable nn.Linear, nn.Conv2d or nn.Conv1d layer")
+            raise ValueError("the model has no trainable nn.Linear or nn.Conv1d/2d/3d layer")
         self._acts: List = [None] * len(self.layers)
         self._grads: List = [None] * len(self.layers)
         self._handles = []
@@ -75,8 +76,8 @@ class PrivacyEngine:
         k, s, p, d = m.kernel_size, m.stride, m.padding, m.dilation
         if isinstance(p, str) or m.groups != 1 or m.padding_mode != "zeros":
             raise ValueError(f"{m}: groups=1 and zero padding given as numbers only")
-        if len(k) == 2 and (k[0] != k[1] or s[0] != s[1] or p[0] != p[1] or d[0] != d[1]):
-            raise ValueError(f"{m}: square kernels with equal stride/padding/dilation in both dimensions only")
+        if any(len(set(v)) != 1 for v in (k, s, p, d)):
+            raise ValueError(f"{m}: square or cubic kernels with equal stride/padding/dilation in every dimension only")
 
     def _fwd_hook(self, i):
         def hook(module, inputs, output):
@@ -106,6 +107,10 @@ class PrivacyEngine:
                 out.append(layer_desc(DP_CONV1D, dtype, B=B, p=m.out_channels, Cin=m.in_channels, H=1, W=a.shape[2],
                                       k=m.kernel_size[0], stride=m.stride[0], pad=m.padding[0], dil=m.dilation[0],
                                       has_bias=hb))
+            elif isinstance(m, nn.Conv3d):
+                out.append(layer_desc(DP_CONV3D, dtype, B=B, p=m.out_channels, Cin=m.in_channels, Z=a.shape[2],
+                                      H=a.shape[3], W=a.shape[4], k=m.kernel_size[0], stride=m.stride[0],
+                                      pad=m.padding[0], dil=m.dilation[0], has_bias=hb))
             else:
                 out.append(layer_desc(DP_CONV2D, dtype, B=B, p=m.out_channels, Cin=m.in_channels, H=a.shape[2],
                                       W=a.shape[3], k=m.kernel_size[0], stride=m.stride[0], pad=m.padding[0],

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define DPCLIP_ABI_VERSION 1
+#define DPCLIP_ABI_VERSION 2
 
 typedef enum {
   DP_OK = 0,
@@ -50,7 +50,7 @@ typedef enum {
 } dp_status;
 
 typedef enum { DP_BF16 = 0, DP_FP32 = 1 } dp_dtype;
-typedef enum { DP_LINEAR = 0, DP_CONV2D = 1, DP_CONV1D = 2 } dp_kind;
+typedef enum { DP_LINEAR = 0, DP_CONV2D = 1, DP_CONV1D = 2, DP_CONV3D = 3 } dp_kind;
 
 /* How the per-example norm is formed ([MixGhost] section 4, the layerwise decision). */
 typedef enum {
@@ -66,7 +66,8 @@ typedef enum {
 /* One layer.  Linear uses B, T, d, p; conv2d uses B, Cin, H, W, p, k, stride, pad, dil
  * (square kernel; Hout = (H + 2 pad - dil (k-1) - 1)/stride + 1, likewise Wout); conv1d
  * uses B, Cin, W (the length), p, k, stride, pad, dil (A [B, Cin, W], G [B, p, Wout],
- * weight gradient [p, Cin, k]; H is ignored). */
+ * weight gradient [p, Cin, k]; H is ignored); conv3d adds the input depth Z (A [B, Cin,
+ * Z, H, W], G [B, p, Zout, Hout, Wout], a cubic kernel, weight gradient [p, Cin, k, k, k]). */
 typedef struct {
   int kind;      /* dp_kind */
   int dtype;     /* dp_dtype of A and G */
@@ -74,6 +75,7 @@ typedef struct {
   int T, d, p;   /* linear: rows per example, in features; p = out features / channels */
   int Cin, H, W, k, stride, pad, dil;
   int has_bias;  /* 1: the bias gradient joins the norm and the sum */
+  int Z;         /* conv3d: input depth (ignored otherwise) */
 } dp_layer_desc;
 
 /* ABI version (DPCLIP_ABI_VERSION).  Host only. */

@@ -70,6 +70,31 @@ def unfold1d(x: np.ndarray, k: int, stride: int = 1, pad: int = 0, dil: int = 1)
     return U
 
 
+def unfold3d(x: np.ndarray, k: int, stride: int = 1, pad: int = 0, dil: int = 1) -> np.ndarray:
+    """U(a_i) of a 3-D convolution: one example x [Cin, Z, H, W] -> [Zout*Hout*Wout, Cin*k^3].
+
+    The 3-D case of the unfold ([MixGhost] section 2.3 and Appendix B): row
+    t = (zo*Hout + ho)*Wout + wo, column ((c*k + kd)*k + kh)*k + kw (the order of a
+    PyTorch Conv3d weight [p, Cin, k, k, k]); taps outside the input read the padding.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    Cin, Z, H, W = x.shape
+    o = lambda n: (n + 2 * pad - dil * (k - 1) - 1) // stride + 1
+    Zo, Ho, Wo = o(Z), o(H), o(W)
+    xp = np.zeros((Cin, Z + 2 * pad, H + 2 * pad, W + 2 * pad))
+    xp[:, pad:pad + Z, pad:pad + H, pad:pad + W] = x
+    U = np.empty((Zo * Ho * Wo, Cin * k ** 3))
+    for c in range(Cin):
+        for kd in range(k):
+            for kh in range(k):
+                for kw in range(k):
+                    z0, h0, w0 = kd * dil, kh * dil, kw * dil
+                    patch = xp[c, z0:z0 + stride * (Zo - 1) + 1:stride, h0:h0 + stride * (Ho - 1) + 1:stride,
+                               w0:w0 + stride * (Wo - 1) + 1:stride]
+                    U[:, ((c * k + kd) * k + kh) * k + kw] = patch.reshape(-1)
+    return U
+
+
 def per_example_grad(spec, a_i: np.ndarray, g_i: np.ndarray):
     """Materialised per-example gradient of one layer: (weight [p, D], bias [p]).
 
@@ -88,6 +113,11 @@ def per_example_grad(spec, a_i: np.ndarray, g_i: np.ndarray):
     elif spec.kind == "conv2d":
         U = unfold2d(a_i, spec.k, spec.stride, spec.pad, spec.dil)
         Gm = g.reshape(spec.p, spec.Hout * spec.Wout)      # F^{-1}: flatten the output map
+        gw = Gm @ U
+        gb = Gm.sum(axis=1)
+    elif spec.kind == "conv3d":
+        U = unfold3d(a_i, spec.k, spec.stride, spec.pad, spec.dil)
+        Gm = g.reshape(spec.p, spec.Zout * spec.Hout * spec.Wout)
         gw = Gm @ U
         gb = Gm.sum(axis=1)
     elif spec.kind == "conv1d":

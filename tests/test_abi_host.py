@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(dp):
             "dp_adaptive_bound"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
-    assert dp.dp_abi_version() == 1
+    assert dp.dp_abi_version() == 2
 
 
 def test_planner_matches_golden_vgg11_decisions(dp):

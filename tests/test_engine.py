@@ -32,6 +32,9 @@ def test_engine_accepts_linear_and_conv_only():
         lib.PrivacyEngine(nn.Sequential(nn.Conv2d(4, 4, 3, groups=2)))
     with pytest.raises(ValueError):
         lib.PrivacyEngine(nn.Sequential(nn.Conv2d(4, 4, (3, 1))))
+    with pytest.raises(ValueError):
+        lib.PrivacyEngine(nn.Sequential(nn.Conv3d(4, 4, 3, stride=(1, 2, 1))))
+    lib.PrivacyEngine(nn.Sequential(nn.Conv3d(4, 4, 3, padding=1))).detach()
     frozen = nn.Sequential(nn.Linear(4, 4), nn.LayerNorm(4))
     for q in frozen[1].parameters():
         q.requires_grad_(False)
@@ -41,7 +44,7 @@ def test_engine_accepts_linear_and_conv_only():
 def _naive_reference(model, x, y, C, sigma, seed):
     """The pages' naive method: one example at a time through autograd, then the oracle's
     clip, sum and noise over the flat parameter vector [W_0, b_0, W_1, b_1, ...]."""
-    layers = [m for m in model.modules() if isinstance(m, (nn.Linear, nn.Conv2d, nn.Conv1d))]
+    layers = [m for m in model.modules() if isinstance(m, (nn.Linear, nn.Conv1d, nn.Conv2d, nn.Conv3d))]
     B = x.shape[0]
     g = []
     for i in range(B):
@@ -102,6 +105,23 @@ def test_engine_conv1d_model(lib, no_tf32):
     model.zero_grad()
     nn.functional.cross_entropy(model(x), y, reduction="sum").backward()
     got = eng.privatise(seed=8).double().cpu().numpy()
+    eng.detach()
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 1e-5
+
+
+@pytest.mark.gpu
+def test_engine_conv3d_model(lib, no_tf32):
+    torch.manual_seed(5)
+    model = nn.Sequential(nn.Conv3d(2, 8, 3, padding=1), nn.ReLU(), nn.Conv3d(8, 8, 2, stride=2),
+                          nn.ReLU(), nn.Flatten(), nn.Linear(8 * 2 * 3 * 2, 4)).cuda()
+    gen = torch.Generator().manual_seed(6)
+    x = torch.randn(5, 2, 4, 6, 5, generator=gen).cuda()
+    y = torch.randint(0, 4, (5,), generator=gen).cuda()
+    want = _naive_reference(model, x, y, C=0.5, sigma=0.3, seed=9)
+    eng = lib.PrivacyEngine(model, C=0.5, sigma=0.3)
+    model.zero_grad()
+    nn.functional.cross_entropy(model(x), y, reduction="sum").backward()
+    got = eng.privatise(seed=9).double().cpu().numpy()
     eng.detach()
     assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 1e-5
 

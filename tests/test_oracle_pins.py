@@ -109,6 +109,33 @@ def test_conv1d_per_example_grad_matches_autograd(Cin, L, p, k, stride, pad, dil
     np.testing.assert_array_equal(U1, tu[0].T.numpy())
 
 
+@pytest.mark.parametrize("Cin,Z,H,W,p,k,stride,pad,dil", [
+    (2, 5, 6, 4, 3, 3, 1, 1, 1), (3, 7, 5, 6, 2, 3, 2, 1, 1), (2, 4, 4, 5, 3, 1, 1, 0, 1),
+    (1, 6, 7, 6, 2, 2, 1, 1, 2)])
+def test_conv3d_per_example_grad_matches_autograd(Cin, Z, H, W, p, k, stride, pad, dil):
+    rng = np.random.default_rng(6)
+    spec = LayerSpec("c3", "conv3d", p=p, Cin=Cin, Z=Z, H=H, W=W, k=k, stride=stride, pad=pad, dil=dil)
+    a = _rand(rng, Cin, Z, H, W)
+    g = _rand(rng, p, spec.Zout, spec.Hout, spec.Wout)
+    gw, gb = dpsgd.per_example_grad(spec, a, g)
+    x = torch.tensor(a)[None]
+    Wt = torch.zeros(p, Cin, k, k, k, dtype=torch.float64, requires_grad=True)
+    b = torch.zeros(p, dtype=torch.float64, requires_grad=True)
+    out = torch.nn.functional.conv3d(x, Wt, b, stride=stride, padding=pad, dilation=dil)
+    assert out.shape[1:] == g.shape
+    (out[0] * torch.tensor(g)).sum().backward()
+    np.testing.assert_allclose(gw, Wt.grad.reshape(p, -1).numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gb, b.grad.numpy(), rtol=1e-12, atol=1e-12)
+    # each depth tap kd of the 3-D unfold is the 2-D unfold of input slice zo*stride - pad + kd*dil
+    U3 = dpsgd.unfold3d(a, k, stride, pad, dil).reshape(spec.Zout, spec.Hout * spec.Wout, Cin, k, k * k)
+    for zo in range(spec.Zout):
+        for kd in range(k):
+            z = zo * stride - pad + kd * dil
+            sl = a[:, z] if 0 <= z < Z else np.zeros((Cin, H, W))
+            U2 = dpsgd.unfold2d(sl, k, stride, pad, dil).reshape(spec.Hout * spec.Wout, Cin, k * k)
+            np.testing.assert_array_equal(U3[zo, :, :, kd], U2)
+
+
 @pytest.mark.parametrize("k,stride,pad,dil", [(3, 1, 1, 1), (3, 2, 0, 1), (2, 1, 1, 2), (1, 1, 0, 1)])
 def test_unfold_matches_torch_unfold(k, stride, pad, dil):
     rng = np.random.default_rng(3)

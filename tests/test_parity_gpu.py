@@ -206,6 +206,16 @@ EDGE = [
     ("conv1d_long", LayerSpec("e", "conv1d", p=64, Cin=32, W=300, k=3, pad=1), 2, "bf16"),
     ("conv1d_fp32", LayerSpec("e", "conv1d", p=6, Cin=5, W=21, k=3, pad=1), 3, "fp32"),
     ("conv1d_k1", LayerSpec("e", "conv1d", p=8, Cin=64, W=40, k=1), 3, "bf16"),
+    # conv3d: cubic kernels through the gathered row layout (p % 8 == 0), else the FFMA kernels
+    ("conv3d_rows", LayerSpec("e", "conv3d", p=16, Cin=4, Z=6, H=7, W=8, k=3, pad=1), 3, "bf16"),
+    ("conv3d_s2_dil2", LayerSpec("e", "conv3d", p=24, Cin=2, Z=9, H=9, W=10, k=3, stride=2, pad=2, dil=2), 3,
+     "bf16"),
+    ("conv3d_k2_nobias", LayerSpec("e", "conv3d", p=16, Cin=8, Z=5, H=6, W=7, k=2, has_bias=False), 2, "bf16"),
+    ("conv3d_k1", LayerSpec("e", "conv3d", p=32, Cin=32, Z=4, H=4, W=4, k=1), 4, "bf16"),
+    # a shape the 2-D im2col kernels would take (Cin % 64 == 0, T % 8 == 0): depth must keep it off them
+    ("conv3d_k1_c64", LayerSpec("e", "conv3d", p=64, Cin=64, Z=3, H=8, W=8, k=1), 3, "bf16"),
+    ("conv3d_c64_pad", LayerSpec("e", "conv3d", p=64, Cin=64, Z=2, H=8, W=8, k=3, pad=1), 2, "bf16"),
+    ("conv3d_fp32", LayerSpec("e", "conv3d", p=6, Cin=3, Z=5, H=5, W=5, k=3, pad=1), 3, "fp32"),
     # one row block: T just above the packed limit, batches of about half the SM count
     ("lin_ghost_slab_T65", LayerSpec("e", "linear", p=40, d=48, T=65), 5, "bf16"),
     ("lin_ghost_slab_B76", LayerSpec("e", "linear", p=64, d=72, T=128), 76, "bf16"),

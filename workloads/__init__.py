@@ -14,6 +14,7 @@ Layer layouts follow PyTorch conventions:
   linear  A [B, T, d]  (layer inputs a_{i,t}),  G [B, T, p]  (output grads)
   conv2d  A [B, Cin, H, W] (NCHW input),        G [B, p, Hout, Wout]
   conv1d  A [B, Cin, W] (NCL input),              G [B, p, Wout]
+  conv3d  A [B, Cin, Z, H, W] (NCDHW input),       G [B, p, Zout, Hout, Wout]
 bf16 workloads draw fp32 values and round them to bf16 (round to nearest
 even); both sides read the rounded values.
 """
@@ -35,13 +36,13 @@ __all__ = [
 class LayerSpec:
     """One layer's shapes and the distribution of its captured tensors."""
     name: str
-    kind: str                 # "linear", "conv2d" or "conv1d"
+    kind: str                 # "linear", "conv1d", "conv2d" or "conv3d"
     p: int                    # output features / output channels
     d: int = 0                # linear: input features
     T: int = 1                # linear: rows (tokens) per example
     Cin: int = 0              # conv: input channels
-    H: int = 0                # conv2d only
-    W: int = 0                # conv2d width, conv1d length
+    H: int = 0                # conv2d / conv3d
+    W: int = 0                # conv2d / conv3d width, conv1d length
     k: int = 1
     stride: int = 1
     pad: int = 0
@@ -50,10 +51,17 @@ class LayerSpec:
     a_dist: str = "normal"    # "normal" (N(0, a_std^2)) or "abs_normal" (|N(0, a_std^2)|)
     a_std: float = 1.0
     g_std: float = 0.01       # output grads ~ N(0, g_std^2)
+    Z: int = 1                # conv3d: input depth
+
+    @property
+    def Zout(self) -> int:
+        if self.kind != "conv3d":
+            return 1
+        return (self.Z + 2 * self.pad - self.dil * (self.k - 1) - 1) // self.stride + 1
 
     @property
     def Hout(self) -> int:
-        if self.kind != "conv2d":
+        if self.kind not in ("conv2d", "conv3d"):
             return 1
         return (self.H + 2 * self.pad - self.dil * (self.k - 1) - 1) // self.stride + 1
 
@@ -66,14 +74,14 @@ class LayerSpec:
     @property
     def rows(self) -> int:
         """T: rows of the per-example contraction (tokens, or Hout*Wout)."""
-        return self.T if self.kind == "linear" else self.Hout * self.Wout
+        return self.T if self.kind == "linear" else self.Zout * self.Hout * self.Wout
 
     @property
     def D(self) -> int:
         """Width of the (unfolded) input: d, or Cin*k*k."""
         if self.kind == "linear":
             return self.d
-        return self.Cin * self.k * (self.k if self.kind == "conv2d" else 1)
+        return self.Cin * self.k ** {"conv1d": 1, "conv2d": 2, "conv3d": 3}[self.kind]
 
     @property
     def n_weight(self) -> int:
@@ -86,11 +94,15 @@ class LayerSpec:
     def a_example_shape(self) -> Tuple[int, ...]:
         if self.kind == "linear":
             return (self.T, self.d)
+        if self.kind == "conv3d":
+            return (self.Cin, self.Z, self.H, self.W)
         return (self.Cin, self.H, self.W) if self.kind == "conv2d" else (self.Cin, self.W)
 
     def g_example_shape(self) -> Tuple[int, ...]:
         if self.kind == "linear":
             return (self.T, self.p)
+        if self.kind == "conv3d":
+            return (self.p, self.Zout, self.Hout, self.Wout)
         return (self.p, self.Hout, self.Wout) if self.kind == "conv2d" else (self.p, self.Wout)
 
 
