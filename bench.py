@@ -78,8 +78,8 @@ def step_work(wl, modes, kept=None):
             flop_norm += wl.B * (2.0 * T * p * D + 2.0 * p * D)
         else:
             flop_norm += wl.B * 2.0 * (D + p)
-        a_el = int(np.prod(spec.a_example_shape()))
-        g_el = int(np.prod(spec.g_example_shape()))
+        a_el = math.prod(spec.a_example_shape())
+        g_el = math.prod(spec.g_example_shape())
         layer_in = wl.B * (a_el + g_el) * es
         in_bytes += layer_in
         if kp:

@@ -152,3 +152,20 @@ def test_package_refuses_to_import_without_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import example_gradient_clipping_gb300"], cwd=tmp_path,
                        capture_output=True, text=True)
     assert r.returncode != 0 and "not built" in r.stderr
+
+
+def test_bench_step_work_counts():
+    """bench.py's algorithmic counts (host only) for every workload and each conv kind."""
+    import bench
+    from workloads import WORKLOADS, LayerSpec, Workload
+    for wl in WORKLOADS.values():
+        for modes in (["ghost"] * len(wl.layers), ["instantiate"] * len(wl.layers)):
+            w = bench.step_work(wl, modes)
+            assert w["flop_sum"] == sum(wl.B * 2.0 * s.rows * s.p * s.D for s in wl.layers)
+            assert w["in_bytes"] > 0 and w["bytes_total"] > w["in_bytes"]
+    specs = (LayerSpec("c1", "conv1d", p=8, Cin=4, W=20, k=3, pad=1),
+             LayerSpec("c3", "conv3d", p=8, Cin=2, Z=4, H=5, W=6, k=3, pad=1))
+    wl = Workload(name="mixed", B=3, layers=specs, dtype="bf16", C=1.0, sigma=1.0)
+    w = bench.step_work(wl, ["instantiate", "ghost"], kept=[True, False])
+    assert w["in_bytes"] == 3 * 2 * (4 * 20 + 8 * 20 + 2 * 4 * 5 * 6 + 8 * 4 * 5 * 6)
+    assert w["kept_bytes"] == 3 * (8 * 12 + 8) * 4
