@@ -28,6 +28,12 @@ class DPError(RuntimeError):
         self.status = status
 
 
+class NoiseDesc(ctypes.Structure):
+    """dp_noise_desc: noise N(0, (sigma C)^2) and 1/B for a fused clipped sum."""
+    _fields_ = [("sigma", ctypes.c_float), ("C", ctypes.c_float), ("B", ctypes.c_int),
+                ("seed", ctypes.c_uint64), ("seed_dev", ctypes.c_void_p), ("offset", ctypes.c_uint64)]
+
+
 class LayerDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("kind", "dtype", "B", "T", "d", "p", "Cin", "H", "W", "k", "stride", "pad", "dil",
@@ -68,6 +74,10 @@ def _load():
         "dp_layout_reused": (c_int, [PD, c_int]),
         "dp_layer_sqnorms_keep": (c_int, [PD, c_void, c_void, c_void, c_void, c_void, c_size, c_void]),
         "dp_clipped_sum_kept": (c_int, [PD, c_void, c_void, c_void, c_void, c_int, c_void, c_size, c_void]),
+        "dp_clipped_sum_noised": (c_int, [PD, c_int, c_void, c_void, c_void, c_void, c_void, c_int,
+                                          ctypes.POINTER(NoiseDesc), c_void, c_size, c_void]),
+        "dp_clipped_sum_kept_noised": (c_int, [PD, c_void, c_void, c_void, c_void, c_int, ctypes.POINTER(NoiseDesc),
+                                               c_void, c_size, c_void]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -209,6 +219,27 @@ def dp_clipped_sum_kept(desc: LayerDesc, grads, factors, dW, db=None, workspace=
     _check(_lib.dp_clipped_sum_kept(ctypes.byref(desc), _ptr(grads), _ptr(factors), _ptr(dW), _ptr(db),
                                     int(bool(accumulate)), _ptr(workspace),
                                     _ws_len(workspace) if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def noise_desc(sigma: float, C: float, B: int, seed: int = 0, seed_dev=None, offset: int = 0) -> NoiseDesc:
+    return NoiseDesc(float(sigma), float(C), int(B), int(seed) & (2 ** 64 - 1), _ptr(seed_dev), int(offset))
+
+
+def dp_clipped_sum_noised(desc: LayerDesc, A, G, factors, dW, db, noise: NoiseDesc, workspace=None,
+                          ws_bytes: Optional[int] = None, norm_mode: int = -1, accumulate: bool = False,
+                          stream=None) -> None:
+    """The clipped sum (norm_mode -1: dp_clipped_sum; >= 0: dp_clipped_sum_reuse) and the
+    noise of dp_add_noise on this layer's blocks in one call."""
+    _check(_lib.dp_clipped_sum_noised(ctypes.byref(desc), norm_mode, _ptr(A), _ptr(G), _ptr(factors), _ptr(dW),
+                                      _ptr(db), int(bool(accumulate)), ctypes.byref(noise), _ptr(workspace),
+                                      _ws_len(workspace) if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def dp_clipped_sum_kept_noised(desc: LayerDesc, grads, factors, dW, db, noise: NoiseDesc, workspace=None,
+                               ws_bytes: Optional[int] = None, accumulate: bool = False, stream=None) -> None:
+    _check(_lib.dp_clipped_sum_kept_noised(ctypes.byref(desc), _ptr(grads), _ptr(factors), _ptr(dW), _ptr(db),
+                                           int(bool(accumulate)), ctypes.byref(noise), _ptr(workspace),
+                                           _ws_len(workspace) if ws_bytes is None else ws_bytes, _stream(stream)))
 
 
 def dp_selftest_wait_timeout(waited_ns=None, stream=None) -> None:

@@ -467,14 +467,50 @@ static bool norm_leaves_nhwc(const Geom& g, int norm_mode, int dtype, const void
   return npl.kernel == NK_TC_GHOST_CONV || npl.kernel == NK_TC_CONV;
 }
 
+// The noise of a fused call: the scale and divisor as dp_add_noise forms them.
+static dp_status noise_args(const dp_noise_desc* nd, const Geom& g, dph::NoiseArgs* nz) {
+  *nz = dph::NoiseArgs{};
+  if (!nd) return fail(DP_ERR_INVALID_ARG, "noise descriptor is NULL");
+  if (nd->B <= 0) return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0", nd->B);
+  if (!(nd->sigma >= 0.f) || !std::isfinite(nd->sigma) || !(nd->C >= 0.f) || !std::isfinite(nd->C))
+    return fail(DP_ERR_INVALID_ARG, "sigma=%g and C=%g must be finite and >= 0", (double)nd->sigma, (double)nd->C);
+  const uint64_t n = (uint64_t)g.p * g.D + (uint64_t)g.p;
+  if (nd->offset + n < nd->offset) return fail(DP_ERR_INVALID_ARG, "offset + p*D + p overflows");
+  nz->on = 1;
+  nz->sc = (float)((double)nd->sigma * (double)nd->C);
+  nz->invB = (float)(1.0 / (double)nd->B);
+  nz->seed = nd->seed;
+  nz->seed_dev = nd->seed_dev;
+  nz->off_a = nd->offset;
+  nz->off_b = nd->offset + (uint64_t)g.p * g.D;
+  return DP_OK;
+}
+
+// The noise pass over dW and db when no kernel of the sum fused it.
+static cudaError_t finish_noise(const Geom& g, float* dW, float* db, const dph::NoiseArgs* nz, cudaStream_t s) {
+  if (!nz || !nz->on || nz->applied) return cudaSuccess;
+  const size_t nw = (size_t)g.p * g.D;
+  if (db && db == dW + nw)
+    return dph::launch_add_noise(dW, nw + g.p, nz->sc, nz->invB, nz->seed, nz->off_a, nz->seed_dev, s);
+  cudaError_t e = dph::launch_add_noise(dW, nw, nz->sc, nz->invB, nz->seed, nz->off_a, nz->seed_dev, s);
+  if (e == cudaSuccess && db) e = dph::launch_add_noise(db, g.p, nz->sc, nz->invB, nz->seed, nz->off_b, nz->seed_dev, s);
+  return e;
+}
+
 static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, const void* G, const float* factors,
                                   float* dW, float* db, int accumulate, void* workspace, size_t ws_bytes,
-                                  cudaStream_t stream, int reuse_norm_mode) {
+                                  cudaStream_t stream, int reuse_norm_mode, const dp_noise_desc* noise) {
   Geom g;
   dp_status st = make_geom(desc, &g);
   if (st != DP_OK) return st;
   if (!A || !G || !factors || !dW) return fail(DP_ERR_INVALID_ARG, "A, G, factors and dW must be non-NULL");
   if (db && !g.has_bias) return fail(DP_ERR_INVALID_ARG, "db given for a layer without bias");
+  dph::NoiseArgs nzv;
+  dph::NoiseArgs* nz = nullptr;
+  if (noise) {
+    if ((st = noise_args(noise, g, &nzv)) != DP_OK) return st;
+    nz = &nzv;
+  }
   const Plan pl = sum_plan(g, desc->dtype, A, G, workspace);
   const size_t need = sum_ws_bytes(g, pl);
   if (need && (!workspace || ws_bytes < need))
@@ -503,7 +539,7 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
     wsp = static_cast<uint8_t*>(wsp) + padded_out_bytes(g);
   }
   if (pl.kernel == 5)
-    e = dph::launch_t1_sum(g, desc->dtype, A, G, factors, dW, db, accumulate, static_cast<float*>(wsp), stream);
+    e = dph::launch_t1_sum(g, desc->dtype, A, G, factors, dW, db, accumulate, static_cast<float*>(wsp), stream, nz);
   else if (pl.kernel == 4 || pl.kernel == 3) {
     const bool xh = reuse_norm_mode >= 0 && norm_leaves_nhwc(g, reuse_norm_mode, desc->dtype, A, G, workspace);
     if (pl.kernel == 4)
@@ -513,8 +549,8 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
   }
   else if (pl.kernel == 6)
     e = dph::launch_tc_sum2(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
-  else if (pl.kernel == 2)
-    e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
+  else if (pl.kernel == 2)   // (a padded output gets its noise after the compaction below)
+    e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream, padded ? nullptr : nz);
   else if (prescale) {
     e = dph::launch_tc_sum_prescaled(pl.lg, A, G, kdW, kacc, static_cast<float*>(wsp), status_ptr(), stream);
     kdb = nullptr;   // the bias went straight to db
@@ -528,6 +564,7 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
     e = dph::launch_compact_cols(kdW, g.p, g.D, pl.lg.D, dW, accumulate, stream);
     if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);
   }
+  if (e == cudaSuccess) e = finish_noise(g, dW, db, nz, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum launch");
   return ok();
 }
@@ -570,13 +607,20 @@ dp_status dp_layer_sqnorms_keep(const dp_layer_desc* desc, const void* A, const 
   return ok();
 }
 
-dp_status dp_clipped_sum_kept(const dp_layer_desc* desc, const float* grads, const float* factors, float* dW,
-                              float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+static dp_status kept_sum_impl(const dp_layer_desc* desc, const float* grads, const float* factors, float* dW,
+                               float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                               const dp_noise_desc* noise) {
   Geom g;
   dp_status st = make_geom(desc, &g);
   if (st != DP_OK) return st;
   if (!grads || !factors || !dW) return fail(DP_ERR_INVALID_ARG, "grads, factors and dW must be non-NULL");
   if (db && !g.has_bias) return fail(DP_ERR_INVALID_ARG, "db given for a layer without bias");
+  dph::NoiseArgs nzv;
+  dph::NoiseArgs* nz = nullptr;
+  if (noise) {
+    if ((st = noise_args(noise, g, &nzv)) != DP_OK) return st;
+    nz = &nzv;
+  }
   Plan pl;
   if (!keep_plan(desc->dtype, g, &pl))
     return fail(DP_ERR_UNSUPPORTED, "this layer keeps no per-example gradients (see dp_grads_size)");
@@ -597,18 +641,40 @@ dp_status dp_clipped_sum_kept(const dp_layer_desc* desc, const float* grads, con
     wsp = static_cast<uint8_t*>(wsp) + padded_out_bytes(g);
   }
   cudaError_t e = dph::launch_kept_sum(g.B, g.p, width, conv_kk, grads, keep_b, factors, kdW, kdb,
-                                       padded ? 0 : accumulate, static_cast<float*>(wsp), stream);
+                                       padded ? 0 : accumulate, static_cast<float*>(wsp), stream,
+                                       padded ? nullptr : nz);
   if (e == cudaSuccess && padded) {
     e = dph::launch_compact_cols(kdW, g.p, g.D, width, dW, accumulate, stream);
     if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);
   }
+  if (e == cudaSuccess) e = finish_noise(g, dW, db, nz, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum_kept launch");
   return ok();
 }
 
+dp_status dp_clipped_sum_kept(const dp_layer_desc* desc, const float* grads, const float* factors, float* dW,
+                              float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  return kept_sum_impl(desc, grads, factors, dW, db, accumulate, workspace, ws_bytes, stream, nullptr);
+}
+
+dp_status dp_clipped_sum_kept_noised(const dp_layer_desc* desc, const float* grads, const float* factors, float* dW,
+                                     float* db, int accumulate, const dp_noise_desc* noise, void* workspace,
+                                     size_t ws_bytes, cudaStream_t stream) {
+  if (!noise) return fail(DP_ERR_INVALID_ARG, "noise descriptor is NULL");
+  return kept_sum_impl(desc, grads, factors, dW, db, accumulate, workspace, ws_bytes, stream, noise);
+}
+
 dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G, const float* factors, float* dW,
                          float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  return clipped_sum_impl(desc, A, G, factors, dW, db, accumulate, workspace, ws_bytes, stream, -1);
+  return clipped_sum_impl(desc, A, G, factors, dW, db, accumulate, workspace, ws_bytes, stream, -1, nullptr);
+}
+
+dp_status dp_clipped_sum_noised(const dp_layer_desc* desc, int norm_mode, const void* A, const void* G,
+                                const float* factors, float* dW, float* db, int accumulate,
+                                const dp_noise_desc* noise, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (norm_mode < -1 || norm_mode > DP_NORM_AUTO_TIME) return fail(DP_ERR_INVALID_ARG, "norm mode %d unknown", norm_mode);
+  if (!noise) return fail(DP_ERR_INVALID_ARG, "noise descriptor is NULL");
+  return clipped_sum_impl(desc, A, G, factors, dW, db, accumulate, workspace, ws_bytes, stream, norm_mode, noise);
 }
 
 dp_status dp_clipped_sum_reuse(const dp_layer_desc* desc, int norm_mode, const void* A, const void* G,
@@ -616,7 +682,7 @@ dp_status dp_clipped_sum_reuse(const dp_layer_desc* desc, int norm_mode, const v
                                size_t ws_bytes, cudaStream_t stream) {
   if (norm_mode < DP_NORM_AUTO || norm_mode > DP_NORM_AUTO_TIME)
     return fail(DP_ERR_INVALID_ARG, "norm mode %d unknown", norm_mode);
-  return clipped_sum_impl(desc, A, G, factors, dW, db, accumulate, workspace, ws_bytes, stream, norm_mode);
+  return clipped_sum_impl(desc, A, G, factors, dW, db, accumulate, workspace, ws_bytes, stream, norm_mode, nullptr);
 }
 
 int dp_layout_reused(const dp_layer_desc* desc, int norm_mode) {

@@ -126,6 +126,43 @@ struct SplitSeg {
   float* out;
 };
 
+// The Gaussian mechanism and the 1/B average applied by a clipped sum's final pass, with
+// the arithmetic of the separate noise pass: x <- (x + sc z_e) * invB, z_e lane e % 4 of
+// normal4(e / 4) in stream 0, e the element's index in the flat parameter vector.
+struct NoiseArgs {
+  int on;
+  float sc, invB;
+  uint64_t seed;
+  const unsigned long long* seed_dev;   // non-null: the seed is read here when the kernel runs
+  uint64_t off_a, off_b;                // flat index of the first element of segment a / b
+  int applied;                          // host: set by the launcher that fused it
+};
+
+// z_e for the four consecutive flat indices e0 .. e0+3 (one or two Philox blocks).
+__device__ __forceinline__ void noise_z4(uint64_t e0, uint64_t seed, float z[4]) {
+  const int m = (int)(e0 & 3);
+  float a[4];
+  normal4(e0 >> 2, seed, 0u, a);
+  if (m == 0) {
+    z[0] = a[0]; z[1] = a[1]; z[2] = a[2]; z[3] = a[3];
+    return;
+  }
+  float b[4];
+  normal4((e0 >> 2) + 1, seed, 0u, b);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int k = m + r;   // 1 .. 6: lane k of a, then of b
+    z[r] = k == 1 ? a[1] : k == 2 ? a[2] : k == 3 ? a[3] : k == 4 ? b[0] : k == 5 ? b[1] : b[2];
+  }
+}
+
+__device__ __forceinline__ float noise_z1(uint64_t e, uint64_t seed) {
+  float a[4];
+  normal4(e >> 2, seed, 0u, a);
+  const int m = (int)(e & 3);
+  return m == 0 ? a[0] : m == 1 ? a[1] : m == 2 ? a[2] : a[3];
+}
+
 }  // namespace dpk
 
 // Host-side launchers implemented by the kernel translation units.
@@ -174,7 +211,7 @@ cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* 
 int t1_sum_splits(const Geom& g);
 size_t t1_sum_ws_bytes(const Geom& g);
 cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G, const float* factors, float* dW,
-                          float* db, int accumulate, float* ws, cudaStream_t s);
+                          float* db, int accumulate, float* ws, cudaStream_t s, dpk::NoiseArgs* nz = nullptr);
 cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, const float* C,
                                 float* out, unsigned* status, cudaStream_t s);
 cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,
@@ -186,8 +223,12 @@ cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alph
 cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
                                  cudaStream_t s);
 // The weight and bias reductions of one clipped sum in one launch (segments: dpk::SplitSeg).
+// With nz->on the same pass adds the noise and the 1/B scale (nz->applied is then set;
+// with the short-vector kernels it is left for a separate noise pass).
 using dpk::SplitSeg;
-cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumulate, cudaStream_t s);
+using dpk::NoiseArgs;
+cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumulate, cudaStream_t s,
+                                  NoiseArgs* nz = nullptr);
 // SIMT (FFMA) paths: any dtype/shape.
 size_t simt_sum_splits(const Geom& g);
 cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, const void* G,

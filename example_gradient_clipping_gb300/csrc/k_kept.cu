@@ -79,7 +79,8 @@ size_t kept_sum_ws_bytes(int B, int p, int D) {
 }
 
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
-                            const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s) {
+                            const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s,
+                            NoiseArgs* nz) {
   if (((size_t)p * D) % 4 || p % 4) return cudaErrorInvalidValue;
   const int splits = kept_splits(B, p, D);
   const int eps = (B + splits - 1) / splits;
@@ -99,7 +100,7 @@ cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep,
     return launch_reduce_splits(part_b, splits, (size_t)p, db, accumulate, s);
   }
   return launch_reduce_splits2(SplitSeg{part, nw, nw, dW}, SplitSeg{part_b, (size_t)p, bias ? (size_t)p : 0, db},
-                               splits, accumulate, s);
+                               splits, accumulate, s, nz);
 }
 
 }  // namespace dph

@@ -308,7 +308,7 @@ size_t t1_sum_ws_bytes(const Geom& g) {
 }
 
 cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G, const float* factors, float* dW,
-                          float* db, int accumulate, float* ws, cudaStream_t s) {
+                          float* db, int accumulate, float* ws, cudaStream_t s, NoiseArgs* nz) {
   const int eps = t1_sum_eps(g), splits = t1_sum_splits(g);
   const bool direct = splits == 1;           // one split writes dW and db itself
   float* part_w = direct ? dW : ws;
@@ -326,7 +326,7 @@ cudaError_t launch_t1_sum(const Geom& g, int dtype, const void* A, const void* G
   if (e != cudaSuccess || direct) return e;
   const size_t nw = (size_t)g.p * g.d;
   return launch_reduce_splits2(SplitSeg{part_w, nw, nw, dW}, SplitSeg{part_b, (size_t)g.p, db ? (size_t)g.p : 0, db},
-                               splits, accumulate, s);
+                               splits, accumulate, s, nz);
 }
 
 }  // namespace dph

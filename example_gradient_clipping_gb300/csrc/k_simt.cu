@@ -140,9 +140,10 @@ __global__ void reduce_splits_kernel(const float* __restrict__ ws, int splits, s
 // (every base 16-byte aligned, strides and lengths multiples of 4), V = 1: floats.  Each
 // element adds its splits in ascending order, eight loads in flight.
 template <int V>
-__global__ void reduce_splits2_kernel(SplitSeg a, SplitSeg b, int splits, int accumulate) {
+__global__ void reduce_splits2_kernel(SplitSeg a, SplitSeg b, int splits, int accumulate, NoiseArgs nz) {
   pdl_trigger();
   pdl_wait();
+  const uint64_t seed = nz.on && nz.seed_dev ? (uint64_t)*nz.seed_dev : nz.seed;
   const size_t ia = a.n / V, items = ia + b.n / V;
   for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < items;
        it += (size_t)gridDim.x * blockDim.x) {
@@ -182,6 +183,14 @@ __global__ void reduce_splits2_kernel(SplitSeg a, SplitSeg b, int splits, int ac
 #pragma unroll
         for (int q = 0; q < V; ++q) acc[q] += v[j][q];
       }
+    }
+    if (nz.on) {
+      const uint64_t e0 = (first ? nz.off_a : nz.off_b) + off;
+      float z[V];
+      if constexpr (V == 4) noise_z4(e0, seed, z);
+      else z[0] = noise_z1(e0, seed);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] = fmaf(nz.sc, z[q], acc[q]) * nz.invB;
     }
     if constexpr (V == 4) *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     else out[0] = acc[0];
@@ -412,9 +421,11 @@ cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* o
   return cudaGetLastError();
 }
 
-cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumulate, cudaStream_t s) {
+cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumulate, cudaStream_t s,
+                                  NoiseArgs* nz) {
   if (!b.out) b.n = 0;
-  if (splits >= 16 && std::max(a.n, b.n) <= ((size_t)1 << 16)) {
+  const bool noise = nz && nz->on;
+  if (!noise && splits >= 16 && std::max(a.n, b.n) <= ((size_t)1 << 16)) {
     // many splits of short vectors: the warp- and block-per-element kernels (packed layouts)
     cudaError_t e = launch_reduce_splits(a.ws, splits, a.n, a.out, accumulate, s);
     if (e != cudaSuccess || !b.n) return e;
@@ -426,9 +437,12 @@ cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumu
                   b.stride % 4 == 0 && b.n % 4 == 0;
   const size_t items = v4 ? (a.n + b.n) / 4 : a.n + b.n;
   if (!items) return cudaSuccess;
+  NoiseArgs off = {};
+  const NoiseArgs& na = noise ? *nz : off;
   const unsigned blocks = (unsigned)std::min<size_t>((items + 255) / 256, 152 * 8);
-  if (v4) launch_pdl(reduce_splits2_kernel<4>, blocks, 256, 0, s, a, b, splits, accumulate);
-  else launch_pdl(reduce_splits2_kernel<1>, blocks, 256, 0, s, a, b, splits, accumulate);
+  if (v4) launch_pdl(reduce_splits2_kernel<4>, blocks, 256, 0, s, a, b, splits, accumulate, na);
+  else launch_pdl(reduce_splits2_kernel<1>, blocks, 256, 0, s, a, b, splits, accumulate, na);
+  if (noise) nz->applied = 1;
   return cudaGetLastError();
 }
 

@@ -655,7 +655,7 @@ size_t tc_sumx_ws_bytes(const Geom& g) {
 }
 
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s) {
+                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, NoiseArgs* nz) {
   CUtensorMap mg64, ma64, mg16, ma16;
   const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
   const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
@@ -722,7 +722,7 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   if (e != cudaSuccess || !gsplits) return e;
   const size_t nw = (size_t)g.p * g.D;
   return launch_reduce_splits2(SplitSeg{part_w, nw, nw, dW}, SplitSeg{part_b, (size_t)g.p, db ? (size_t)g.p : 0, db},
-                               gsplits, accumulate, s);
+                               gsplits, accumulate, s, nz);
 }
 
 // Instantiated norm on the tensor cores: per-tile partials [tiles, B] in the workspace,

@@ -19,7 +19,8 @@ cudaError_t launch_tc_sum_prescaled(const Geom& g, const void* A, const void* Gs
 bool tc_sumx_supported(const Geom& g);
 size_t tc_sumx_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
+                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
+                           dpk::NoiseArgs* nz = nullptr);
 // The same per-example clipped sum on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2);
 // p and D above 128 (neither half of a pair tile empty).
 bool tc_sum2_supported(const Geom& g);
@@ -38,7 +39,8 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
 // kernel's tile column order with that many filter taps (mapped back to [p, Cin, k, k]).
 size_t kept_sum_ws_bytes(int B, int p, int D);
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
-                            const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s);
+                            const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s,
+                            dpk::NoiseArgs* nz = nullptr);
 // Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
 // Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).

@@ -1,18 +1,21 @@
 """One privatised-gradient step over a list of layers, through the C ABI.
 
 Per step: dp_layer_sqnorms for every layer (ghost norm, instantiation or the
-one-row form, layer by layer), dp_clip_factors (flat or per-layer), dp_clipped_sum
-for every layer into one flat fp32 gradient vector [W_0, b_0, W_1, b_1, ...], then
-dp_add_noise over it (per layer with its own bound when clipping per layer).
-Torch supplies device memory and the stream only.
+one-row form, layer by layer), dp_clip_factors (flat or per-layer), then for every
+layer the clipped sum into one flat fp32 gradient vector [W_0, b_0, W_1, b_1, ...]
+with the layer's noise and 1/B added by the same call (dp_clipped_sum_noised, each
+layer's noise drawn at its flat offset, with its own bound when clipping per layer).
+fuse_noise=False runs dp_clipped_sum per layer and dp_add_noise over the vector
+instead; the result is bit-identical.  Torch supplies device memory and the stream only.
 """
 from __future__ import annotations
 
 from typing import List, Optional, Sequence, Tuple
 
 from . import (DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_add_noise, dp_add_noise_devseed, dp_clip_factors,
-               dp_clipped_sum, dp_clipped_sum_kept, dp_clipped_sum_reuse, dp_grads_size, dp_launch_count,
-               dp_layer_sqnorms, dp_layer_sqnorms_keep, dp_layout_reused, dp_plan, dp_workspace_size)
+               dp_clipped_sum, dp_clipped_sum_kept, dp_clipped_sum_kept_noised, dp_clipped_sum_noised,
+               dp_clipped_sum_reuse, dp_grads_size, dp_launch_count, dp_layer_sqnorms, dp_layer_sqnorms_keep,
+               dp_layout_reused, dp_plan, dp_workspace_size, noise_desc)
 
 # Instantiated layers with at least this many rows per example keep their per-example
 # gradients by default (the clipped sum then reads them once instead of recomputing a
@@ -26,8 +29,10 @@ class ClipStep:
     does, False never."""
 
     def __init__(self, descs: Sequence[LayerDesc], C, sigma: float, per_layer: bool = False,
-                 norm_modes: Optional[Sequence[int]] = None, device: str = "cuda", keep_grads="auto"):
+                 norm_modes: Optional[Sequence[int]] = None, device: str = "cuda", keep_grads="auto",
+                 fuse_noise: bool = True):
         import torch
+        self.fuse_noise = bool(fuse_noise)
         self.descs = list(descs)
         L = len(self.descs)
         self.B = self.descs[0].B
@@ -100,6 +105,22 @@ class ClipStep:
             else:
                 dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
 
+    def sums_noised(self, inputs, seed: int = 0, seed_dev=None, stream=None) -> None:
+        """sums() and noise() together: every layer's clipped sum call also adds its blocks'
+        noise and the 1/B scale (in the sum's final reduction where it has one)."""
+        for l, (d, (A, G)) in enumerate(zip(self.descs, inputs)):
+            dW, db = self.layer_views(l)
+            fac = self.factors[l] if self.per_layer else self.factors[0]
+            nd = noise_desc(self.sigma, self.C[l] if self.per_layer else self.C[0], self.B, seed, seed_dev,
+                            self.offsets[l])
+            if self.kept[l] is not None:
+                dp_clipped_sum_kept_noised(d, self.kept[l], fac, dW, db, nd, self.workspace, stream=stream)
+            elif self.own_ws[l] is not None:
+                dp_clipped_sum_noised(d, A, G, fac, dW, db, nd, self.own_ws[l], norm_mode=self.modes[l],
+                                      stream=stream)
+            else:
+                dp_clipped_sum_noised(d, A, G, fac, dW, db, nd, self.workspace, stream=stream)
+
     def noise(self, seed: int, stream=None) -> None:
         if not self.per_layer:
             dp_add_noise(self.grad, self.sigma, self.C[0], self.B, seed, 0, stream=stream)
@@ -122,6 +143,15 @@ class ClipStep:
             dp_add_noise_devseed(self.grad[o:o + n], self.sigma, self.C[l], self.B, self.seed_buf, o,
                                  stream=stream)
 
+    def sums_and_noise_devseed(self, inputs, stream=None) -> None:
+        """The clipped sums and the noise with the seed read from self.seed_buf when the
+        kernels run (fused unless fuse_noise is False)."""
+        if self.fuse_noise:
+            self.sums_noised(inputs, seed_dev=self.seed_buf, stream=stream)
+        else:
+            self.sums(inputs, stream)
+            self.noise_devseed(stream)
+
     def capture(self, inputs) -> None:
         """Capture one whole step over the device buffers `inputs` in a CUDA graph.
 
@@ -136,8 +166,7 @@ class ClipStep:
         with torch.cuda.graph(g):
             self.norms(inputs)
             self.factors_()
-            self.sums(inputs)
-            self.noise_devseed()
+            self.sums_and_noise_devseed(inputs)
         self.graph_kernels = dp_launch_count() - n0
         self.graph = g
 
@@ -150,8 +179,11 @@ class ClipStep:
         """Norms -> factors -> clipped sums -> noise and 1/B; returns the flat gradient."""
         self.norms(inputs, stream)
         self.factors_(stream)
-        self.sums(inputs, stream)
-        self.noise(seed, stream)
+        if self.fuse_noise:
+            self.sums_noised(inputs, seed=seed, stream=stream)
+        else:
+            self.sums(inputs, stream)
+            self.noise(seed, stream)
         return self.grad
 
 
@@ -278,8 +310,7 @@ class ClipPipeline:
                                     d_.view(-1)[lo:hi].copy_(h.view(-1)[lo:hi], non_blocking=True)
                 st.norms(cur)
                 st.factors_()
-                st.sums(cur)
-                st.noise_devseed()
+                st.sums_and_noise_devseed(cur)
                 self.out_host[b].copy_(st.grad, non_blocking=True)
                 for sd in self.side:
                     cap.wait_stream(sd)

@@ -220,6 +220,36 @@ dp_status dp_layer_sqnorms_keep(const dp_layer_desc* desc, const void* A, const 
 dp_status dp_clipped_sum_kept(const dp_layer_desc* desc, const float* grads, const float* factors, float* dW,
                               float* db, int accumulate, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* ---- The clipped sum and the noise in one call ---------------------------------------
+ * The Gaussian mechanism and average of dp_add_noise applied to this layer's blocks of the
+ * flat gradient right after its clipped sum:
+ *   dW[j] = (S_W[j] + sigma * C * z_{offset + j}) / B,       j < p*D
+ *   db[j] = (S_b[j] + sigma * C * z_{offset + p*D + j}) / B, j < p
+ * S = the clipped sum of dp_clipped_sum (norm_mode = -1), of dp_clipped_sum_reuse
+ * (norm_mode >= 0: the layout reuse described above) or of dp_clipped_sum_kept, plus the
+ * old contents of dW/db when accumulate = 1; z as dp_add_noise defines it, `offset` = the
+ * index of dW[0] in the flat parameter vector (db[0] follows at offset + p*D).  Where the sum
+ * ends in a reduction of example splits, that pass adds the noise (one pass over the
+ * gradient less); otherwise the noise pass follows in the same call.  Either way the
+ * result is bit-identical to the sum call followed by dp_add_noise on the same blocks.
+ * seed_dev non-NULL: the seed is read from device memory when the kernels run (as
+ * dp_add_noise_devseed), seed is then ignored.  Arguments, workspace and errors otherwise
+ * as the sum call; DP_ERR_INVALID_ARG for B <= 0 or a negative or non-finite sigma or C. */
+typedef struct {
+  float sigma, C;                       /* the noise standard deviation is sigma * C */
+  int B;                                /* the divisor (the logical batch size) */
+  uint64_t seed;                        /* Philox key */
+  const unsigned long long* seed_dev;   /* device, or NULL */
+  uint64_t offset;                      /* flat index of dW[0] */
+} dp_noise_desc;
+dp_status dp_clipped_sum_noised(const dp_layer_desc* desc, int norm_mode, const void* A, const void* G,
+                                const float* factors, float* dW, float* db, int accumulate,
+                                const dp_noise_desc* noise, void* workspace, size_t ws_bytes,
+                                cudaStream_t stream);
+dp_status dp_clipped_sum_kept_noised(const dp_layer_desc* desc, const float* grads, const float* factors,
+                                     float* dW, float* db, int accumulate, const dp_noise_desc* noise,
+                                     void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* Synchronizes `stream`, returns the device status word (DP_OK, DP_ERR_NONFINITE or
  * DP_ERR_TIMEOUT) raised since the last check, and clears it. */
 dp_status dp_check_status(cudaStream_t stream);
