@@ -141,6 +141,26 @@ def test_invalid_calls_launch_nothing(dp):
         dp.dp_adaptive_bound(16, 4, 0.0, 1.1, 2.0, 2.5, 0, 0, 16, stream=0)
 
 
+def test_invalid_noise_of_fused_sums_launches_nothing(dp):
+    """The fused sum+noise calls check the noise descriptor before anything launches."""
+    import ctypes
+    d = dp.layer_desc(dp.DP_LINEAR, dp.DP_BF16, B=4, p=8, T=3, d=8)
+    for nd in (dp.noise_desc(1.0, 1.0, 0), dp.noise_desc(-1.0, 1.0, 4), dp.noise_desc(1.0, float("nan"), 4),
+               dp.noise_desc(float("inf"), 1.0, 4), dp.noise_desc(1.0, 1.0, 4, offset=2 ** 64 - 8)):
+        with pytest.raises(dp.DPError) as e:
+            dp.dp_clipped_sum_noised(d, 16, 16, 16, 16, 16, nd, workspace=16, ws_bytes=1 << 30, stream=0)
+        assert e.value.status == dp.DP_ERR_INVALID_ARG
+        with pytest.raises(dp.DPError) as e:
+            dp.dp_clipped_sum_kept_noised(d, 16, 16, 16, 16, nd, workspace=16, ws_bytes=1 << 30, stream=0)
+        assert e.value.status in (dp.DP_ERR_INVALID_ARG, dp.DP_ERR_UNSUPPORTED)
+    ok = dp.noise_desc(1.0, 1.0, 4)
+    with pytest.raises(dp.DPError) as e:
+        dp.dp_clipped_sum_noised(d, 16, 16, 16, 16, 16, ok, workspace=16, ws_bytes=1 << 30, norm_mode=9, stream=0)
+    assert e.value.status == dp.DP_ERR_INVALID_ARG
+    st = dp._lib.dp_clipped_sum_noised(ctypes.byref(d), -1, 16, 16, 16, 16, 16, 0, None, 16, 1 << 30, None)
+    assert st == dp.DP_ERR_INVALID_ARG and b"noise" in dp._lib.dp_last_error()
+
+
 def test_package_refuses_to_import_without_library(tmp_path):
     """The binding fails loudly when the compiled library is absent (no fallback)."""
     import shutil
