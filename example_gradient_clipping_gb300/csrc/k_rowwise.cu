@@ -300,8 +300,16 @@ cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alph
   return cudaGetLastError();
 }
 
-// Examples per split of the one-row clipped sum: about 32, at least one split.
-static int t1_sum_eps(const Geom& g) { return std::min(g.B, 32); }
+// Examples per split of the one-row clipped sum: enough splits to give the SMs about two
+// blocks each, 8 to 32 examples per split (one to four passes of eight loads in flight; the
+// cap also bounds each thread's fp32 accumulation chain).
+static int t1_sum_eps(const Geom& g) {
+  const long n_th = (long)g.p * ((g.d + 3) / 4);
+  const long bx = std::min<long>((n_th + 255) / 256, 152L * 8);
+  const long want = std::max<long>(1, (2L * 152 + bx - 1) / bx);
+  const long eps = std::min<long>(32, std::max<long>(8, (g.B + want - 1) / want));
+  return (int)std::min<long>(g.B, eps);
+}
 int t1_sum_splits(const Geom& g) { const int e = t1_sum_eps(g); return (g.B + e - 1) / e; }
 size_t t1_sum_ws_bytes(const Geom& g) {
   return (size_t)t1_sum_splits(g) * ((size_t)g.p * g.d + g.p) * sizeof(float);
