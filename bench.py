@@ -325,18 +325,23 @@ def run_ours(args, wl):
     # The whole step is one CUDA graph (norms -> factors -> clipped sums -> noise),
     # replayed once per step; every kernel in it is a library kernel.
     step.capture(dev_in)
-    # per-call graphs for the per-kernel roofline: each holds REPS back-to-back calls,
-    # so graph launch latency is amortised (the first call finds a flushed L2; in the
-    # step the clipped sum likewise runs right after the norm pass read the inputs)
+    # per-call graphs for the per-kernel roofline: each holds REPS calls, so graph launch
+    # latency is amortised (the first call finds a flushed L2; in the step the clipped sum
+    # likewise runs right after the norm pass read the inputs).  Each call is followed by
+    # a one-element PyTorch kernel, which takes no part in programmatic launch, so no call
+    # overlaps the next; a graph of REPS such separators is timed too and subtracted.
     REPS = 20
+    sep_buf = torch.zeros(1, dtype=torch.float32, device=dev)
     call_graphs = {}
     for name, fn in (("norms", lambda: step.norms(dev_in)), ("factors", lambda: step.factors_()),
                      ("sums", lambda: step.sums(dev_in)), ("noise", lambda: step.noise_devseed()),
-                     ("sums_noised", lambda: step.sums_and_noise_devseed(dev_in))):
+                     ("sums_noised", lambda: step.sums_and_noise_devseed(dev_in)), ("_sep", None)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for _ in range(REPS):
-                fn()
+                if fn is not None:
+                    fn()
+                sep_buf.add_(1.0)
         call_graphs[name] = g
 
     def timed(replay, k_steps, seed_base):
@@ -364,8 +369,10 @@ def run_ours(args, wl):
     launches = step.graph_kernels * args.steps
     total_ms = max_over_ranks(sum(step_ms), dev)
     value = world * wl.B * args.steps / (total_ms / 1e3)
-    per_call = {n: [t / REPS for t in timed(g.replay, max(5, args.steps // 4), seed0)]
-                for n, g in call_graphs.items()}
+    n_rep = max(5, args.steps // 4)
+    sep_ms = statistics.mean(timed(call_graphs["_sep"].replay, n_rep, seed0))
+    per_call = {n: [max(t - sep_ms, 0.0) / REPS for t in timed(g.replay, n_rep, seed0)]
+                for n, g in call_graphs.items() if n != "_sep"}
 
     # end to end through the public API: every step copies a batch from pinned host memory
     # and its gradient back (ClipPipeline: one graph per step, the copy of batch k+1 on a
@@ -415,8 +422,9 @@ def run_ours(args, wl):
     roof["kernel"] = {"sums": "dp_clipped_sum", "norms": "dp_layer_sqnorms", "noise": "dp_add_noise",
                       "factors": "dp_clip_factors"}[dom]
     roof["peak_source"] = f"{pk['src']} (burst)"
-    roof["timing"] = (f"CUDA events around a graph of {REPS} back-to-back calls after an L2 flush; "
-                      "per-launch mean")
+    roof["timing"] = (f"CUDA events around a graph of {REPS} calls after an L2 flush, each call followed by a "
+                      "one-element PyTorch kernel (no overlap between calls; the separators' own graph time "
+                      "subtracted); per-call mean")
 
     line = None
     if rank == 0:

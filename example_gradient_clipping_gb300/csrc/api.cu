@@ -430,8 +430,13 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
   float* ws = static_cast<float*>(wsp);
   switch (pl.kernel) {
     case NK_T1: e = dph::launch_t1_norm(g, desc->dtype, A, G, sqnorm_out, stream); break;
-    case NK_TC_GHOST: e = dph::launch_tc_ghost(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
-    case NK_TC_INST: e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream); break;
+    // linear layers read the caller's A and G, which may start before the previous kernel ends
+    case NK_TC_GHOST:
+      e = dph::launch_tc_ghost(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream, !pl.rows);
+      break;
+    case NK_TC_INST:
+      e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, ws, status_ptr(), stream, nullptr, nullptr, !pl.rows);
+      break;
     case NK_TC_CONV: e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_TC_GHOST_CONV: e = dph::launch_tc_ghost_conv(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_SIMT_GHOST: e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
@@ -550,7 +555,8 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
   else if (pl.kernel == 6)
     e = dph::launch_tc_sum2(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
   else if (pl.kernel == 2)   // (a padded output gets its noise after the compaction below)
-    e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream, padded ? nullptr : nz);
+    e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream, padded ? nullptr : nz,
+                            !pl.rows);
   else if (prescale) {
     e = dph::launch_tc_sum_prescaled(pl.lg, A, G, kdW, kacc, static_cast<float*>(wsp), status_ptr(), stream);
     kdb = nullptr;   // the bias went straight to db
@@ -602,7 +608,8 @@ dp_status dp_layer_sqnorms_keep(const dp_layer_desc* desc, const void* A, const 
   if (pl.kernel == NK_TC_CONV)
     e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, wsp, status_ptr(), stream, grads, keep_b);
   else
-    e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, static_cast<float*>(wsp), status_ptr(), stream, grads, keep_b);
+    e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, static_cast<float*>(wsp), status_ptr(), stream, grads, keep_b,
+                            !pl.rows);
   if (e != cudaSuccess) return cuda_fail(e, "dp_layer_sqnorms_keep launch");
   return ok();
 }

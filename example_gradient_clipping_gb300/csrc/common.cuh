@@ -60,8 +60,10 @@ __device__ __forceinline__ float ld_a(const E* __restrict__ A, const Geom& g, in
 // Programmatic dependent launch: every library kernel is launched with programmatic
 // stream serialization, lets the next kernel in the stream start launching once all of
 // its CTAs are running (pdl_trigger), and waits for the previous kernel in the stream to
-// complete, with its memory visible, before its first global-memory access (pdl_wait).
-// Kernels that do not use these (another library's) keep ordinary stream order.
+// complete, with its memory visible, before its first global-memory access (pdl_wait) --
+// except the tensor-core kernels of linear layers, whose loads of the caller's A and G
+// (which no library kernel writes) may precede the wait.  Kernels that do not use these
+// (another library's) keep ordinary stream order.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -45,6 +45,7 @@ struct Params {
   // conv layers: mapA is a TMA im2col map over an NHWC copy of the input, and K
   // chunk q of the unfolded rows is channel block q / (k*k), filter tap q % (k*k)
   int conv, Wout, k, stride, pad, dil;
+  int early;           // A and G are the caller's inputs: loads may start before pdl_wait
 };
 
 // Load K chunk kk (64 unfolded columns) of the 128 rows that start at row t0 of
@@ -120,7 +121,10 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();   // the next kernel in the stream may start launching
-  pdl_wait();      // the previous kernel has completed; its writes are visible
+  // With P.early, A and G (the caller's inputs, which no library kernel writes) are loaded
+  // and multiplied before the previous kernel in the stream has completed; the epilogue
+  // warps pass pdl_wait before they write.  Otherwise every warp waits here.
+  if (!P.early) pdl_wait();
 
   if (warp == 0 || warp == 6) {
     // TMA producers (whole warp; the elected lane issues); producer pr loads slots k % 2 == pr
@@ -295,6 +299,7 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     }
   } else if (warp < 6) {
     // ---- epilogue warps: lane quarter (warp & 3) of both Gram tiles ----
+    pdl_wait();
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;          // TMEM lane = tile row
     // packed: columns [c_lo, c_hi) are this row's example block
@@ -474,12 +479,12 @@ cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, fl
     const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
     if (!encode_tmap_bf16(&mg, Gt, 3, dg, sg, box)) return cudaErrorInvalidValue;
   }
-  tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil};
+  tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil, 0};
   return run_ghost(g, ma, mg, P, s);
 }
 
 cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* /*ws*/,
-                            unsigned* status, cudaStream_t s) {
+                            unsigned* status, cudaStream_t s, bool early) {
   CUtensorMap ma, mg;
   const int ept = ghost_ept(g);
   if (ept) {   // flattened rows [B*T, width]
@@ -497,7 +502,7 @@ cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* 
     if (!encode_tmap_bf16(&ma, A, 3, da, sa, box) || !encode_tmap_bf16(&mg, G, 3, dg, sg, box))
       return cudaErrorInvalidValue;
   }
-  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0};
+  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0, early ? 1 : 0};
   return run_ghost(g, ma, mg, P, s);
 }
 

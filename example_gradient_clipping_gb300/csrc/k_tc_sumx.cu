@@ -74,6 +74,7 @@ struct Params {
                       // tile to dW + z*p*d (db + z*p), reduced afterwards in z order
   float* keep;        // norm mode, or null: every example's gradient [B, p, d] and bias [B, p]
   float* keep_b;
+  int early;          // A and G are the caller's inputs: loads may start before pdl_wait
 };
 
 // Shared-memory control block after the stages.
@@ -555,9 +556,14 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
   ptx::tc_fence_after();
   const uint32_t tmem = c->tmem;
   pdl_trigger();   // the next kernel in the stream may start launching
-  pdl_wait();      // the previous kernel has completed; its writes are visible
+  // With P.early, A and G (the caller's inputs, which no library kernel writes) are loaded
+  // and multiplied before the previous kernel in the stream has completed: the factors,
+  // the outputs and the workspace are touched after pdl_wait, which every warp passes
+  // before its first such access.  Otherwise every warp waits here.
+  if (!P.early) pdl_wait();
 
   if (warp >= kEpiFirst) {
+    pdl_wait();
     ptx::regs_inc<216>();
     if constexpr (kNorm)
       epilogue_norm(P, smem, c, tmem, e0, e1, do_bias);
@@ -571,8 +577,10 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
     } else if (warp == 1) {
       mma_issuer(P, smem, c, tmem, e0, e1);
     } else {
+      pdl_wait();
       finish_decision(c);        // warp 3 joins the workers' barrier
     }
+    pdl_wait();
     finish(P, smem, c, tmem, m0, n0, do_bias);
   }
 }
@@ -655,7 +663,8 @@ size_t tc_sumx_ws_bytes(const Geom& g) {
 }
 
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, NoiseArgs* nz) {
+                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, NoiseArgs* nz,
+                           bool early) {
   CUtensorMap mg64, ma64, mg16, ma16;
   const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
   const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
@@ -689,6 +698,7 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   P.splits = splits;
   P.accumulate = accumulate;
   P.gsplit = gsplits ? 1 : 0;
+  P.early = early ? 1 : 0;
   int nfull = g.T / 64, rem = g.T - 64 * nfull;
   int n16 = (rem + 15) / 16;
   if (n16 > 3) { nfull += 1; n16 = 0; }
@@ -734,7 +744,7 @@ size_t tc_inst_ws_bytes(const Geom& g) {
 }
 
 cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* out, float* ws,
-                           unsigned* status, cudaStream_t s, float* keep, float* keep_b) {
+                           unsigned* status, cudaStream_t s, float* keep, float* keep_b, bool early) {
   CUtensorMap mg64, ma64, mg16, ma16;
   const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
   const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
@@ -750,6 +760,7 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
   const int eps = cdiv_x(g.B, chunks);
   chunks = cdiv_x(g.B, eps);
   tcsumx::Params P = {};
+  P.early = early ? 1 : 0;
   P.status = status;
   P.B = g.B;
   P.T = g.T;

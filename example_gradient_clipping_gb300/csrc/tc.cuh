@@ -20,7 +20,7 @@ bool tc_sumx_supported(const Geom& g);
 size_t tc_sumx_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
                            float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
-                           dpk::NoiseArgs* nz = nullptr);
+                           dpk::NoiseArgs* nz = nullptr, bool early = false);
 // The same per-example clipped sum on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2);
 // p and D above 128 (neither half of a pair tile empty).
 bool tc_sum2_supported(const Geom& g);
@@ -33,7 +33,8 @@ size_t tc_inst_ws_bytes(const Geom& g);
 // With `keep`, every example's gradient is also written to keep [B, p, D] and its bias to
 // keep_b [B, p] (fp32) for the kept-gradient clipped sum.
 cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* out, float* ws,
-                           unsigned* status, cudaStream_t s, float* keep = nullptr, float* keep_b = nullptr);
+                           unsigned* status, cudaStream_t s, float* keep = nullptr, float* keep_b = nullptr,
+                           bool early = false);
 // Clipped sum from kept per-example gradients: dW (+)= sum_i c_i g_i, db (+)= sum_i c_i b_i
 // (2pD flop per example, one read of the kept gradients).  conv_kk > 0: g_i in the conv
 // kernel's tile column order with that many filter taps (mapped back to [p, Cin, k, k]).
@@ -47,7 +48,7 @@ cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns
 bool tc_ghost_supported(const Geom& g);
 size_t tc_ghost_ws_bytes(const Geom& g);
 cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* ws,
-                            unsigned* status, cudaStream_t s);
+                            unsigned* status, cudaStream_t s, bool early = false);
 // Conv layer -> row layout of a linear layer (bf16): unfolded input U [B, T, D] and the
 // output gradient transposed per example, Gt [B, T, p].
 // U has conv_rows_width(g) = D rounded up to 8 columns (the extra ones zero).

@@ -21,6 +21,15 @@
  *    nothing.  dp_last_error() then holds a message (per calling thread).
  *  - Device-side conditions (a non-finite norm) set a device status word that
  *    dp_check_status() returns and clears.
+ *  - Stream order: the library's kernels use programmatic dependent launch.  Each
+ *    waits for the previous kernel in the stream before it reads what that kernel
+ *    wrote, except that the tensor-core kernels of linear layers may start loading
+ *    A and G while the previous kernel still runs, if that kernel lets its dependents
+ *    launch early (the library's own kernels do; kernels that do not use programmatic
+ *    launch, such as PyTorch's and cuBLAS's, complete first).  So A and G must be
+ *    complete before the previous such kernel in the stream starts: never written by
+ *    a kernel that itself triggers programmatic launch right before the call.  The
+ *    library never writes A or G.
  *  - Layouts (row-major, contiguous, PyTorch conventions):
  *      linear: A [B, T, d], G [B, T, p]; weight gradient [p, d]
  *      conv2d: A [B, Cin, H, W] (NCHW), G [B, p, Hout, Wout]; weight gradient
