@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libdpclip.so")
 DP_OK, DP_ERR_INVALID_ARG, DP_ERR_UNSUPPORTED, DP_ERR_CUDA, DP_ERR_NONFINITE, DP_ERR_TIMEOUT = range(6)
 DP_BF16, DP_FP32 = 0, 1
 DP_LINEAR, DP_CONV2D, DP_CONV1D, DP_CONV3D = 0, 1, 2, 3
+DP_NCHW, DP_NHWC = 0, 1
 DP_NORM_AUTO, DP_NORM_GHOST, DP_NORM_INSTANTIATE, DP_NORM_T1, DP_NORM_AUTO_TIME = 0, 1, 2, 3, 4
 MODE_NAMES = {DP_NORM_GHOST: "ghost", DP_NORM_INSTANTIATE: "instantiate", DP_NORM_T1: "t1"}
 
@@ -37,13 +38,15 @@ class NoiseDesc(ctypes.Structure):
 class LayerDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("kind", "dtype", "B", "T", "d", "p", "Cin", "H", "W", "k", "stride", "pad", "dil",
-                 "has_bias", "Z")]
+                 "has_bias", "Z", "layout")]
 
 
 def layer_desc(kind: int, dtype: int, B: int, p: int, T: int = 1, d: int = 0, Cin: int = 0,
                H: int = 0, W: int = 0, k: int = 1, stride: int = 1, pad: int = 0, dil: int = 1,
-               has_bias: bool = True, Z: int = 0) -> LayerDesc:
-    return LayerDesc(kind, dtype, B, T, d, p, Cin, H, W, k, stride, pad, dil, int(bool(has_bias)), Z)
+               has_bias: bool = True, Z: int = 0, layout: int = 0) -> LayerDesc:
+    """layout: DP_NCHW (channels first, PyTorch's default) or DP_NHWC (channels last) for
+    the A and G of conv layers."""
+    return LayerDesc(kind, dtype, B, T, d, p, Cin, H, W, k, stride, pad, dil, int(bool(has_bias)), Z, layout)
 
 
 def _load():

@@ -59,6 +59,9 @@ dp_status make_geom(const dp_layer_desc* d, Geom* g) {
   g->B = d->B;
   g->p = d->p;
   g->has_bias = d->has_bias ? 1 : 0;
+  if (d->kind != DP_LINEAR && d->layout != DP_NCHW && d->layout != DP_NHWC)
+    return fail(DP_ERR_INVALID_ARG, "layout %d is not DP_NCHW or DP_NHWC", d->layout);
+  g->nhwc = d->kind != DP_LINEAR && d->layout == DP_NHWC;
   if (d->kind == DP_LINEAR) {
     if (d->T <= 0 || d->d <= 0)
       return fail(DP_ERR_INVALID_ARG, "linear layer needs T=%d > 0 and d=%d > 0", d->T, d->d);
@@ -154,6 +157,7 @@ size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 Geom rows_geom(const Geom& g) {
   Geom r = g;
   r.conv = 0;
+  r.nhwc = 0;
   r.D = r.d = dph::conv_rows_width(g);
   return r;
 }
@@ -360,7 +364,7 @@ cudaError_t prepare_rows(const Geom& g, const Plan& pl, const void*& A, const vo
   void* Gt = base + align256((size_t)g.B * g.T * dph::conv_rows_width(g) * 2);
   cudaError_t e = dph::launch_conv_rows(g, A, G, U, Gt, stream, scale, db, accumulate, bias_part);
   A = U;
-  G = Gt;
+  if (!g.nhwc || scale) G = Gt;     // channels-last output gradients are the rows already
   ws = base + rows_bytes(g);
   return e;
 }
@@ -467,7 +471,8 @@ dp_status dp_clip_factors(const float* sqnorms, int B, int L, int per_layer, con
 // Whether a dp_layer_sqnorms call in `norm_mode` leaves the NHWC copy of a conv layer's
 // input at the front of its workspace (the im2col ghost and instantiation kernels do).
 static bool norm_leaves_nhwc(const Geom& g, int norm_mode, int dtype, const void* A, const void* G, const void* ws) {
-  if (!g.conv || norm_mode < DP_NORM_AUTO || norm_mode > DP_NORM_AUTO_TIME || norm_mode == DP_NORM_T1) return false;
+  if (!g.conv || g.nhwc || norm_mode < DP_NORM_AUTO || norm_mode > DP_NORM_AUTO_TIME || norm_mode == DP_NORM_T1)
+    return false;   // (channels-last inputs need no copy to share)
   const Plan npl = norm_plan(g, resolve_mode(g, norm_mode), dtype, A, G, ws);
   return npl.kernel == NK_TC_GHOST_CONV || npl.kernel == NK_TC_CONV;
 }

@@ -24,6 +24,7 @@ struct Geom {
   int Z, Zout, kz, padz;      // input depth, output depth, kernel depth, depth padding: conv3d,
                               // else 1, 1, 1, 0
   int conv;                   // 0 linear, 1 conv1d, conv2d or conv3d
+  int nhwc;                   // conv: A and G channels last ([.., H, W, C]), else channels first
   int has_bias;
 };
 
@@ -33,7 +34,7 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float
 // Output-gradient element X(i, t, j), j < p.
 template <class E>
 __device__ __forceinline__ float ld_g(const E* __restrict__ G, const Geom& g, int i, int t, int j) {
-  if (!g.conv) return to_f(G[((size_t)i * g.T + t) * g.p + j]);
+  if (!g.conv || g.nhwc) return to_f(G[((size_t)i * g.T + t) * g.p + j]);
   return to_f(G[((size_t)i * g.p + j) * g.T + t]);
 }
 
@@ -54,6 +55,7 @@ __device__ __forceinline__ float ld_a(const E* __restrict__ A, const Geom& g, in
   const int h = ho * g.stride - g.padh + kh * g.dil;
   const int w = wo * g.stride - g.pad + kw * g.dil;
   if (z < 0 || z >= g.Z || h < 0 || h >= g.H || w < 0 || w >= g.W) return 0.f;
+  if (g.nhwc) return to_f(A[((((size_t)i * g.Z + z) * g.H + h) * g.W + w) * g.Cin + c]);
   return to_f(A[((((size_t)i * g.Cin + c) * g.Z + z) * g.H + h) * g.W + w]);
 }
 

@@ -393,8 +393,26 @@ static ConvPlan conv_plan(const Geom& g, bool norm) {
   return c;
 }
 
-// NHWC copy of the input, then the kernel's partials.
-static size_t nhwc_bytes(const Geom& g) { return al256((size_t)g.B * g.H * g.W * g.Cin * 2); }
+// The layout copy (NCHW inputs: an NHWC copy of the input for the im2col loads; channels-
+// last inputs: the output gradient per example as [p, T], the kernel's K-major operand),
+// then the kernel's partials.
+static size_t nhwc_bytes(const Geom& g) {
+  return al256(g.nhwc ? (size_t)g.B * g.T * g.p * 2 : (size_t)g.B * g.H * g.W * g.Cin * 2);
+}
+
+// The im2col source and the [p, T] output gradient of a call: channels-last inputs are
+// their own im2col source and have their output gradient transposed into the workspace.
+static cudaError_t conv_layouts(const Geom& g, const void* A, const void* G, void* ws, bool reuse_xh,
+                                const void** Xh, const void** Gc, cudaStream_t s) {
+  if (g.nhwc) {
+    *Xh = A;
+    *Gc = ws;
+    return launch_transpose_rows(g.B, g.p, g.T, G, ws, s);     // [T, p] -> [p, T]
+  }
+  *Xh = ws;
+  *Gc = G;
+  return reuse_xh ? cudaSuccess : launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, ws, s);   // NCHW -> NHWC
+}
 
 size_t tc_conv_ws_bytes(const Geom& g, bool norm) {
   const ConvPlan c = conv_plan(g, norm);
@@ -475,12 +493,12 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
                                 unsigned* status, cudaStream_t s, float* keep, float* keep_b) {
   const ConvPlan c = conv_plan(g, true);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  void* Xh = w;
   float* part = reinterpret_cast<float*>(w + nhwc_bytes(g));
-  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
+  const void *Xh, *Gc;
+  cudaError_t e = conv_layouts(g, A, G, w, false, &Xh, &Gc, s);
   if (e != cudaSuccess) return e;
   CUtensorMap mG, mX;
-  if (!encode_maps(g, Xh, G, &mG, &mX)) return cudaErrorInvalidValue;
+  if (!encode_maps(g, Xh, Gc, &mG, &mX)) return cudaErrorInvalidValue;
   tcconv::Params P = base_params(g, c, status);
   P.part = part;
   P.bias = g.has_bias;
@@ -495,13 +513,13 @@ cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, cons
                                float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, bool reuse_xh) {
   const ConvPlan c = conv_plan(g, false);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  void* Xh = w;
   float* part = reinterpret_cast<float*>(w + nhwc_bytes(g));
   float* part_db = reinterpret_cast<float*>(w + nhwc_bytes(g) + al256((size_t)c.splits * g.p * c.items * 64 * 4));
-  cudaError_t e = reuse_xh ? cudaSuccess : launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);
+  const void *Xh, *Gc;
+  cudaError_t e = conv_layouts(g, A, G, w, reuse_xh, &Xh, &Gc, s);
   if (e != cudaSuccess) return e;
   CUtensorMap mG, mX;
-  if (!encode_maps(g, Xh, G, &mG, &mX)) return cudaErrorInvalidValue;
+  if (!encode_maps(g, Xh, Gc, &mG, &mX)) return cudaErrorInvalidValue;
   tcconv::Params P = base_params(g, c, status);
   P.factors = factors;
   P.part = part;

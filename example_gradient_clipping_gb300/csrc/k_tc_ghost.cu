@@ -462,10 +462,15 @@ cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, fl
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* Xh = w;
   void* Gt = w + al256g((size_t)g.B * g.H * g.W * g.Cin * 2);
-  cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
-  if (e != cudaSuccess) return e;
-  e = launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);                        // [p, T] -> [T, p]
-  if (e != cudaSuccess) return e;
+  if (g.nhwc) {          // channels last: the inputs are the NHWC source and the rows already
+    Xh = const_cast<void*>(A);
+    Gt = const_cast<void*>(G);
+  } else {
+    cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
+    if (e != cudaSuccess) return e;
+    e = launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);                        // [p, T] -> [T, p]
+    if (e != cudaSuccess) return e;
+  }
   const int ept = ghost_ept(g);
   CUtensorMap ma, mg;
   if (!encode_im2col_bf16(&ma, Xh, g, tcghost::BT)) return cudaErrorInvalidValue;

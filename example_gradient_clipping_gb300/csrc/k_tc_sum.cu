@@ -385,11 +385,14 @@ cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, cons
   void* Gt = w + al256s((size_t)g.B * g.H * g.W * g.Cin * 2);
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(Gt) + al256s((size_t)g.B * g.T * g.p * 2));
   float* part_db = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(part) + al256s(tc_sum_ws_bytes(g)));
-  cudaError_t e = reuse_xh ? cudaSuccess : launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
+  // channels-last inputs are the im2col source themselves; else an NHWC copy (or the one a
+  // norm call left in the workspace)
+  cudaError_t e = (reuse_xh || g.nhwc) ? cudaSuccess : launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);
   if (e != cudaSuccess) return e;
+  if (g.nhwc) Xh = const_cast<void*>(A);
   // bf16(c_i G_i^T) and db in one pass, written right before the GEMM reads it (L2-hot);
   // rereading a norm call's unscaled rows and scaling them in the GEMM measured slower
-  e = launch_scaled_rows(g.B, g.T, g.p, G, Gt, factors, db, accumulate, part_db, s);
+  e = launch_scaled_rows(g.B, g.T, g.p, G, Gt, factors, db, accumulate, part_db, s, g.nhwc != 0);
   if (e != cudaSuccess) return e;
   const long R = (long)g.B * g.T;
   CUtensorMap mg, ma;

@@ -10,25 +10,29 @@
 //                 conv2d: k_z = 1, k_h = k; conv1d: one input row, k_z = k_h = 1; conv3d:
 //                 a cubic kernel, the 2-D staging kernel does not take it),
 //                 m < Dp: columns D <= m < Dp (Dp = D rounded up to 8) are zero
-//   Gt[i, t, j] = G_i[j, t]   (the NCHW output gradient, transposed per example)
+//   Gt[i, t, j] = G_i[j, t]   (the NCHW output gradient, transposed per example; a
+//                 channels-last output gradient is already in this layout)
+// Channels-last inputs (x_i stored [Z, H, W, Cin]) are read with their own strides.
 #include <algorithm>
 
 #include "tc.cuh"
 
 namespace dpk {
 
-// One CTA per example: the example's whole input [Cin, H, W] (contiguous in NCHW) is
-// staged in shared memory with 16-byte loads, then its T output rows are written with
-// 16-byte stores, each gathered from shared memory (zero outside the image).
+// One CTA per example: the example's whole input ([Cin, H, W] or, channels last,
+// [H, W, Cin]: contiguous either way) is staged in shared memory with 16-byte loads, then
+// its T output rows are written with 16-byte stores, each gathered from shared memory
+// (zero outside the image).
 __global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __restrict__ x,
                                         __nv_bfloat16* __restrict__ U) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ __align__(16) __nv_bfloat16 xs[];     // [Cin][H][W]
+  extern __shared__ __align__(16) __nv_bfloat16 xs[];     // [Cin][H][W] or [H][W][Cin]
   const int kk = g.kh * g.k;
   const int cpr = Dp >> 3;                                // 16-byte chunks per output row
   const int HW = g.H * g.W;
   const int n_in = g.Cin * HW;
+  const int cs = g.nhwc ? 1 : HW, ps = g.nhwc ? g.Cin : 1;   // channel and pixel strides
   for (int i = blockIdx.x; i < g.B; i += gridDim.x) {
     const __nv_bfloat16* xi = x + (size_t)i * n_in;
     if ((n_in & 7) == 0) {
@@ -51,7 +55,7 @@ __global__ void unfold_rows_smem_kernel(Geom g, int Dp, const __nv_bfloat16* __r
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int h = hb + kh * g.dil, w = wb + kw * g.dil;
-        v[j] = (m0 + j < g.D && h >= 0 && h < g.H && w >= 0 && w < g.W) ? xs[c * HW + h * g.W + w]
+        v[j] = (m0 + j < g.D && h >= 0 && h < g.H && w >= 0 && w < g.W) ? xs[c * cs + (h * g.W + w) * ps]
                                                                          : __float2bfloat16_rn(0.f);
         if (++kw == g.k) {
           kw = 0;
@@ -91,9 +95,9 @@ __global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restri
       const int z = zo * g.stride - g.padz + kd * g.dil;
       const int h = ho * g.stride - g.padh + kh * g.dil;
       const int w = wo * g.stride - g.pad + kw * g.dil;
-      v[j] = (m < g.D && z >= 0 && z < g.Z && h >= 0 && h < g.H && w >= 0 && w < g.W)
-                 ? xi[(((size_t)c * g.Z + z) * g.H + h) * g.W + w]
-                 : __float2bfloat16_rn(0.f);
+      const bool in = m < g.D && z >= 0 && z < g.Z && h >= 0 && h < g.H && w >= 0 && w < g.W;
+      const size_t pix = ((size_t)z * g.H + h) * g.W + w;
+      v[j] = in ? xi[g.nhwc ? pix * g.Cin + c : (size_t)c * g.Z * g.H * g.W + pix] : __float2bfloat16_rn(0.f);
     }
     *reinterpret_cast<uint4*>(U + q * 8) = *reinterpret_cast<const uint4*>(v);
   }
@@ -190,6 +194,48 @@ __global__ void transpose_rows_short_kernel(int B, int T, int p, const __nv_bflo
   }
 }
 
+// Channels-last output gradients are rows [B, T, p] already: bf16(c_i G) in place of the
+// scaled transpose, with the bias partial c_i sum_t G[i, t, j] of each example (p % 8 == 0).
+// Thread = (example, 8 channels); consecutive threads read consecutive 16-byte chunks of a
+// row, four rows in flight.
+__global__ void scale_rows_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
+                                  __nv_bfloat16* __restrict__ Gs, const float* __restrict__ scale,
+                                  float* __restrict__ bias_part) {
+  pdl_trigger();
+  pdl_wait();
+  const int cp = p >> 3;
+  const size_t n = (size_t)B * cp;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t i = q / cp;
+    const int j0 = (int)(q - i * cp) * 8;
+    const float sc = __ldg(scale + i);
+    float bsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int t0 = 0; t0 < T; t0 += 4) {
+      uint4 raw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (t0 + u < T) raw[u] = __ldcs(reinterpret_cast<const uint4*>(G + (i * T + t0 + u) * p + j0));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (t0 + u >= T) break;
+        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw[u]);
+        __align__(16) __nv_bfloat16 v[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float f = __bfloat162float(x[r]);
+          bsum[r] += f;
+          v[r] = __float2bfloat16_rn(sc * f);
+        }
+        *reinterpret_cast<uint4*>(Gs + (i * T + t0 + u) * p + j0) = *reinterpret_cast<const uint4*>(v);
+      }
+    }
+    if (bias_part) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) bias_part[i * p + j0 + r] = sc * bsum[r];
+    }
+  }
+}
+
 // General fallback: 32 x 33 tiles, 2-byte accesses.
 __global__ void transpose_rows_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
                                       __nv_bfloat16* __restrict__ Gt) {
@@ -261,7 +307,8 @@ cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* 
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (scale) return launch_scaled_rows(g.B, g.T, g.p, G, Gt, scale, db, accumulate, bias_part, s);
+  if (scale) return launch_scaled_rows(g.B, g.T, g.p, G, Gt, scale, db, accumulate, bias_part, s, g.nhwc != 0);
+  if (g.nhwc) return cudaSuccess;        // channels last: G is already the rows the kernels read
   return launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);
 }
 
@@ -295,7 +342,18 @@ cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* ds
 }
 
 cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
-                               int accumulate, float* bias_part, cudaStream_t s) {
+                               int accumulate, float* bias_part, cudaStream_t s, bool rows_in) {
+  if (rows_in) {   // channels last: scale in place of the transpose, one bias partial per example
+    if (p % 8) return cudaErrorInvalidValue;
+    const size_t n = (size_t)B * (p / 8);
+    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 16);
+    launch_plain(scale_rows_kernel, blocks ? blocks : 1, 256, 0, s, B, T, p,
+                 static_cast<const __nv_bfloat16*>(G), static_cast<__nv_bfloat16*>(Gt), factors,
+                 db ? bias_part : nullptr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !db) return e;
+    return launch_reduce_splits(bias_part, B, (size_t)p, db, accumulate, s);
+  }
   cudaError_t e = launch_transpose_rows(B, T, p, G, Gt, s, factors, db ? bias_part : nullptr);
   if (e != cudaSuccess || !db) return e;
   return launch_reduce_splits(bias_part, transpose_bias_parts(B, T), (size_t)p, db, accumulate, s);

@@ -64,7 +64,7 @@ cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* ds
 // Gt = bf16(c_i G_i^T) for the row-scaled clipped sum, and db (+)= sum_i c_i sum_t G[i, :, t]
 // from fp32 partial sums taken on the way (bias_part: scaled_rows_bias_bytes).
 cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
-                               int accumulate, float* bias_part, cudaStream_t s);
+                               int accumulate, float* bias_part, cudaStream_t s, bool rows_in = false);
 size_t scaled_rows_bias_bytes(int B, int T, int p);
 // Conv layers with the unfold done by TMA im2col loads (Cin % 64 == 0, T % 8 == 0, T >= 64):
 // instantiated norm and clipped sum; the workspace holds an NHWC copy of the input.

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DPCLIP_ABI_VERSION 2
+#define DPCLIP_ABI_VERSION 3
 
 typedef enum {
   DP_OK = 0,
@@ -60,6 +60,11 @@ typedef enum {
 
 typedef enum { DP_BF16 = 0, DP_FP32 = 1 } dp_dtype;
 typedef enum { DP_LINEAR = 0, DP_CONV2D = 1, DP_CONV1D = 2, DP_CONV3D = 3 } dp_kind;
+/* Memory layout of a conv layer's A and G: channels first (PyTorch's default, NCHW) or
+ * channels last (NHWC: A [B, H, W, Cin], G [B, Hout, Wout, p]; conv1d [B, L, C], conv3d
+ * [B, Z, H, W, C]; PyTorch's channels_last memory format).  Channels-last inputs feed the
+ * TMA im2col loads and the row layout directly, without the layout copies. */
+typedef enum { DP_NCHW = 0, DP_NHWC = 1 } dp_layout;
 
 /* How the per-example norm is formed ([MixGhost] section 4, the layerwise decision). */
 typedef enum {
@@ -85,6 +90,7 @@ typedef struct {
   int Cin, H, W, k, stride, pad, dil;
   int has_bias;  /* 1: the bias gradient joins the norm and the sum */
   int Z;         /* conv3d: input depth (ignored otherwise) */
+  int layout;    /* conv layers: dp_layout of A and G (ignored for linear layers) */
 } dp_layer_desc;
 
 /* ABI version (DPCLIP_ABI_VERSION).  Host only. */

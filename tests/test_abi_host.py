@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(dp):
             "dp_adaptive_bound"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
-    assert dp.dp_abi_version() == 2
+    assert dp.dp_abi_version() == 3
 
 
 def test_planner_matches_golden_vgg11_decisions(dp):
@@ -103,7 +103,8 @@ def test_conv_output_size(dp):
     dict(kind=0, dtype=0, B=0, p=4, T=2, d=3), dict(kind=0, dtype=0, B=2, p=0, T=2, d=3),
     dict(kind=0, dtype=7, B=2, p=4, T=2, d=3), dict(kind=5, dtype=0, B=2, p=4, T=2, d=3),
     dict(kind=0, dtype=0, B=2, p=4, T=0, d=3), dict(kind=1, dtype=0, B=2, p=4, Cin=2, H=2, W=2, k=5),
-    dict(kind=1, dtype=0, B=2, p=4, Cin=2, H=8, W=8, k=3, stride=0)])
+    dict(kind=1, dtype=0, B=2, p=4, Cin=2, H=8, W=8, k=3, stride=0),
+    dict(kind=1, dtype=0, B=2, p=4, Cin=2, H=8, W=8, k=3, layout=2)])
 def test_invalid_descriptors_rejected(dp, kw):
     d = dp.layer_desc(**kw)
     with pytest.raises(dp.DPError) as e:
