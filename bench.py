@@ -44,18 +44,18 @@ def _peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
-def layer_desc(dp, spec, B, dtype):
+def layer_desc(dp, spec, B, dtype, layout=0):
     dt = dp.DP_BF16 if dtype == "bf16" else dp.DP_FP32
     if spec.kind == "linear":
         return dp.layer_desc(dp.DP_LINEAR, dt, B=B, p=spec.p, T=spec.T, d=spec.d, has_bias=spec.has_bias)
     if spec.kind == "conv3d":
         return dp.layer_desc(dp.DP_CONV3D, dt, B=B, p=spec.p, Cin=spec.Cin, Z=spec.Z, H=spec.H, W=spec.W, k=spec.k,
-                             stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
+                             stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias, layout=layout)
     if spec.kind == "conv1d":
         return dp.layer_desc(dp.DP_CONV1D, dt, B=B, p=spec.p, Cin=spec.Cin, H=1, W=spec.W, k=spec.k,
-                             stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
+                             stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias, layout=layout)
     return dp.layer_desc(dp.DP_CONV2D, dt, B=B, p=spec.p, Cin=spec.Cin, H=spec.H, W=spec.W, k=spec.k,
-                         stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias)
+                         stride=spec.stride, pad=spec.pad, dil=spec.dil, has_bias=spec.has_bias, layout=layout)
 
 
 def step_work(wl, modes, kept=None):
@@ -298,25 +298,33 @@ def run_ours(args, wl):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
 
-    descs = [layer_desc(dp, s, wl.B, wl.dtype) for s in wl.layers]
+    # --channels-last: conv layers' A and G handed over channels last (same values)
+    cl = [bool(args.channels_last) and s.kind != "linear" for s in wl.layers]
+    descs = [layer_desc(dp, s, wl.B, wl.dtype, layout=int(c)) for s, c in zip(wl.layers, cl)]
+
+    def to_layout(pair, c):
+        return tuple(x.movedim(1, -1).contiguous() for x in pair) if c else pair
+
     step = dp.ClipStep(descs, C=wl.C, sigma=wl.sigma, per_layer=wl.per_layer, device=str(dev))
     n_elem = wl.B * sum(math.prod(s.a_example_shape()) + math.prod(s.g_example_shape()) for s in wl.layers)
     if n_elem <= HOST_GEN_LIMIT:
         host_in = [workloads.layer_inputs(wl, l, threads=8) for l in range(len(wl.layers))]
-        dev_in = [(workloads.to_torch(A, wl.dtype, str(dev)), workloads.to_torch(G, wl.dtype, str(dev)))
-                  for A, G in host_in]
-        pinned = [(workloads.to_torch(A, wl.dtype).pin_memory(), workloads.to_torch(G, wl.dtype).pin_memory())
-                  for A, G in host_in]
+        dev_in = [to_layout((workloads.to_torch(A, wl.dtype, str(dev)), workloads.to_torch(G, wl.dtype, str(dev))), c)
+                  for (A, G), c in zip(host_in, cl)]
+        pinned = [tuple(x.pin_memory() for x in to_layout((workloads.to_torch(A, wl.dtype),
+                                                             workloads.to_torch(G, wl.dtype)), c))
+                  for (A, G), c in zip(host_in, cl)]
 
         def sample_inputs(b):
             return [(A[:b], G[:b]) for A, G in host_in]
     else:
         # full-size inputs drawn on the device (host generation would take minutes)
-        dev_in = [workloads.device_layer_inputs(wl, l, str(dev)) for l in range(len(wl.layers))]
+        dev_in = [to_layout(workloads.device_layer_inputs(wl, l, str(dev)), c) for l, c in enumerate(cl)]
         pinned = [(a.cpu().pin_memory(), g.cpu().pin_memory()) for a, g in dev_in]
 
-        def sample_inputs(b):
-            return [(a[:b].float().numpy(), g[:b].float().numpy()) for a, g in pinned]
+        def sample_inputs(b):     # channels first for the oracle
+            return [tuple((x[:b].movedim(-1, 1) if c else x[:b]).float().numpy() for x in pair)
+                    for pair, c in zip(pinned, cl)]
     modes = [dp.MODE_NAMES[m] for m, _, _ in step.plan]
     kept = [k is not None for k in step.kept]
     work = step_work(wl, modes, kept)
@@ -431,7 +439,8 @@ def run_ours(args, wl):
         line = dict(metric=METRIC, value=value, unit="examples/s", n_gpus=world, steps=args.steps,
                     warmup=max(args.warmup, 3), ms_per_step=total_ms / args.steps, higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype=wl.dtype, data="synthetic",
-                    config=_config(wl, dict(norm_modes=modes, parallelism=f"replicas x{world}")),
+                    config=_config(wl, dict(norm_modes=modes, parallelism=f"replicas x{world}",
+                                            conv_layout="channels last" if any(cl) else "channels first")),
                     e2e=dict(value=e2e_value, unit="examples/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                              pipeline="ClipPipeline: one CUDA graph per step runs the step on one of two "
                                       "device buffer sets, copies its gradient to pinned host memory and, on a "
@@ -507,6 +516,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--hbm-sweep", action="store_true",
                     help="supplementary steady-state bandwidth of the noise and one-row norm kernels")
+    ap.add_argument("--channels-last", action="store_true",
+                    help="hand conv layers' A and G over channels last (DP_NHWC); same values")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling and sweeps; not the bench line)")
     args = ap.parse_args()

@@ -41,7 +41,8 @@ constexpr int kEpiFirst = 4, kEpiWarps = 8;
 constexpr int SMEM = STAGES * STAGE + 1024 + 512;
 constexpr int PSTR = BN + 4;                 // staged output row stride (floats)
 static_assert(BM * PSTR * 4 <= STAGES * STAGE, "staging fits in the stage buffers");
-// A = G (K-major: pixels contiguous), B = im2col blocks (MN-major: channels contiguous);
+// A = G (K-major: pixels contiguous; channels-last output gradients: MN-major, outputs
+// contiguous, two 64-output boxes), B = im2col blocks (MN-major: channels contiguous);
 // the instruction's N is the tile's block count x 64
 
 struct Params {
@@ -58,6 +59,7 @@ struct Params {
   float* keep;            // norm mode, or null: every example's gradient [B, p, ncols] in tile
                           // column order ((cc * k*k + tap) * 64 + c), and its bias [B, p]
   float* keep_b;
+  int g_mn;               // G channels last ([B, T, p]): the A operand is MN-major
 };
 
 struct Ctl {
@@ -85,7 +87,12 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG,
       if (ptx::elect_one()) {
         ptx::mbar_arrive_expect_tx(&c->full[s], bytes);
         const int t0 = u * 64;
-        ptx::tma_load_3d(mG, &c->full[s], st, t0, m0, e);
+        if (P.g_mn) {             // [64 pixels x 64 outputs] twice: outputs m0.. and m0+64..
+          ptx::tma_load_3d(mG, &c->full[s], st, m0, t0, e);
+          ptx::tma_load_3d(mG, &c->full[s], st + BOX, m0 + 64, t0, e);
+        } else {
+          ptx::tma_load_3d(mG, &c->full[s], st, t0, m0, e);
+        }
         const int ho = t0 / P.Wout, wo = t0 - ho * P.Wout;
         const int wb = wo * P.stride - P.pad, hb = ho * P.stride - P.pad;
         for (int j = 0; j < nitems; ++j) {
@@ -108,7 +115,8 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG,
 __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0,
                                            int e1, int nblocks) {
   volatile int* abort = &c->abort;
-  const uint32_t idesc = ptx::idesc_bf16_f32(BM, 64 * nblocks, 0, 1);   // the tile's blocks only
+  const uint32_t idesc = ptx::idesc_bf16_f32(BM, 64 * nblocks, P.g_mn ? 1 : 0, 1);   // the tile's blocks only
+  const int a_kstep = P.g_mn ? 2048 : 32;           // bytes per 16 pixels of the A operand
   int k = 0;
   bool live = true;
   for (int e = e0; e < e1 && live; ++e) {
@@ -124,14 +132,15 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
       const bool w = ptx::mbar_wait(&c->full[s], (k / STAGES) & 1, abort, P.status);
       if (!__all_sync(0xffffffffu, w)) { live = false; break; }
       const uint32_t g = ptx::smem_u32(smem + s * STAGE);
-      // A: 128 rows of 128 B (64 pixels), K step of 16 pixels = 32 B
-      const uint64_t da = ptx::sdesc_sw128(g, 16, 1024);
+      // A: 128 rows of 128 B (64 pixels), K step of 16 pixels = 32 B; MN-major: two boxes of
+      // 64 pixel rows x 128 B (64 outputs), BOX apart, K step of 16 pixels = 2048 B
+      const uint64_t da = P.g_mn ? ptx::sdesc_sw128(g, BOX, 1024) : ptx::sdesc_sw128(g, 16, 1024);
       // B: 64-pixel rows of 128 B per block, blocks BOX apart, K step of 16 pixels = 2048 B
       const uint64_t dbd = ptx::sdesc_sw128(g + 2 * BOX, BOX, 1024);
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 32), ptx::sdesc_add(dbd, kk * 2048), idesc,
+          ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * a_kstep), ptx::sdesc_add(dbd, kk * 2048), idesc,
                          (u | kk) != 0);
         ptx::umma_commit(&c->empty[s]);
       }
@@ -371,6 +380,7 @@ static PFN_cuTensorMapEncodeIm2col_v12000 im2col_fn() {
 
 bool tc_conv_supported(const Geom& g) {
   if (!g.conv || g.Cin % 64 || g.T % 8 || g.T < 64 || g.p < 8) return false;
+  if (g.nhwc && g.p % 8) return false;     // channels-last G rows: 16-byte TMA strides
   if (g.kh != g.k || g.padh != g.pad || g.Z != 1 || g.kz != 1) return false;   // square 2D kernels (TMA im2col)
   if (g.stride > 8 || g.pad > 127 || g.dil * (g.k - 1) - g.pad > 128 || g.dil * (g.k - 1) > 65535) return false;
   return (double)g.B * g.H * g.W * g.Cin < 4e9;
@@ -393,24 +403,21 @@ static ConvPlan conv_plan(const Geom& g, bool norm) {
   return c;
 }
 
-// The layout copy (NCHW inputs: an NHWC copy of the input for the im2col loads; channels-
-// last inputs: the output gradient per example as [p, T], the kernel's K-major operand),
+// The NHWC copy of an NCHW input for the im2col loads (channels-last inputs need none),
 // then the kernel's partials.
-static size_t nhwc_bytes(const Geom& g) {
-  return al256(g.nhwc ? (size_t)g.B * g.T * g.p * 2 : (size_t)g.B * g.H * g.W * g.Cin * 2);
-}
+static size_t nhwc_bytes(const Geom& g) { return g.nhwc ? 0 : al256((size_t)g.B * g.H * g.W * g.Cin * 2); }
 
-// The im2col source and the [p, T] output gradient of a call: channels-last inputs are
-// their own im2col source and have their output gradient transposed into the workspace.
+// The im2col source of a call: channels-last inputs are their own; else an NHWC copy in
+// the workspace (or the one a norm call left there).  The output gradient is read as it
+// lies either way ([p, T] K-major, or channels last [T, p] MN-major).
 static cudaError_t conv_layouts(const Geom& g, const void* A, const void* G, void* ws, bool reuse_xh,
                                 const void** Xh, const void** Gc, cudaStream_t s) {
+  *Gc = G;
   if (g.nhwc) {
     *Xh = A;
-    *Gc = ws;
-    return launch_transpose_rows(g.B, g.p, g.T, G, ws, s);     // [T, p] -> [p, T]
+    return cudaSuccess;
   }
   *Xh = ws;
-  *Gc = G;
   return reuse_xh ? cudaSuccess : launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, ws, s);   // NCHW -> NHWC
 }
 
@@ -439,10 +446,17 @@ bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pix
 }
 
 static bool encode_maps(const Geom& g, const void* Xh, const void* G, CUtensorMap* mG, CUtensorMap* mX) {
-  const uint64_t dg[3] = {(uint64_t)g.T, (uint64_t)g.p, (uint64_t)g.B};
-  const uint64_t sg[2] = {(uint64_t)g.T * 2, (uint64_t)g.p * g.T * 2};
-  const uint32_t box[3] = {64, 128, 1};
-  if (!encode_tmap_bf16(mG, G, 3, dg, sg, box)) return false;
+  if (g.nhwc) {     // [B, T, p]: boxes of 64 outputs x 64 pixels
+    const uint64_t dg[3] = {(uint64_t)g.p, (uint64_t)g.T, (uint64_t)g.B};
+    const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
+    const uint32_t box[3] = {64, 64, 1};
+    if (!encode_tmap_bf16(mG, G, 3, dg, sg, box)) return false;
+  } else {
+    const uint64_t dg[3] = {(uint64_t)g.T, (uint64_t)g.p, (uint64_t)g.B};
+    const uint64_t sg[2] = {(uint64_t)g.T * 2, (uint64_t)g.p * g.T * 2};
+    const uint32_t box[3] = {64, 128, 1};
+    if (!encode_tmap_bf16(mG, G, 3, dg, sg, box)) return false;
+  }
   return encode_im2col_bf16(mX, Xh, g, 64);
 }
 
@@ -473,6 +487,7 @@ static cudaError_t launch_kernel(const Geom& g, const ConvPlan& c, const CUtenso
 
 static tcconv::Params base_params(const Geom& g, const ConvPlan& c, unsigned* status) {
   tcconv::Params P = {};
+  P.g_mn = g.nhwc;
   P.status = status;
   P.B = g.B;
   P.T = g.T;

@@ -18,7 +18,9 @@ Use (with a summed loss G_i is example i's own gradient; loss_reduction="mean" u
 
 Layers: nn.Linear (inputs [B, ..., d]; the middle dimensions are the rows T), nn.Conv1d,
 nn.Conv2d and nn.Conv3d (square or cubic kernels, equal stride / padding / dilation in every
-dimension), the conv layers with groups 1 and zero padding.  Every trainable parameter of the model must belong to such a layer.
+dimension), the conv layers with groups 1 and zero padding.  Conv2d/Conv3d layers whose input
+arrives in PyTorch's channels_last memory format are handed over channels last (no layout
+copy); their output gradients are brought to the same format.  Every trainable parameter of the model must belong to such a layer.
 Activations right after them must not be in-place (the backward hook reads the layer's
 output gradient).  PyTorch warns that the hook fires on output gradients when the model
 input needs no gradient; that gradient is the one wanted here.
@@ -27,7 +29,7 @@ from __future__ import annotations
 
 from typing import List, Optional
 
-from . import DP_BF16, DP_CONV1D, DP_CONV2D, DP_CONV3D, DP_FP32, DP_LINEAR, DP_NORM_AUTO, layer_desc
+from . import DP_BF16, DP_CONV1D, DP_CONV2D, DP_CONV3D, DP_FP32, DP_LINEAR, DP_NCHW, DP_NHWC, DP_NORM_AUTO, layer_desc
 from .step import ClipStep
 
 
@@ -95,10 +97,30 @@ class PrivacyEngine:
             h.remove()
         self._handles = []
 
-    def _descs(self, B: int, dtype: int):
+    @staticmethod
+    def _layout(m, a) -> int:
+        import torch
+        import torch.nn as nn
+        if isinstance(m, nn.Conv2d) and a.dim() == 4 and not a.is_contiguous() and \
+                a.is_contiguous(memory_format=torch.channels_last):
+            return DP_NHWC
+        if isinstance(m, nn.Conv3d) and a.dim() == 5 and not a.is_contiguous() and \
+                a.is_contiguous(memory_format=torch.channels_last_3d):
+            return DP_NHWC
+        return DP_NCHW
+
+    @staticmethod
+    def _as_layout(x, layout: int, dtype):
+        import torch
+        x = x.to(dtype)
+        if layout == DP_NHWC:
+            return x.contiguous(memory_format=torch.channels_last if x.dim() == 4 else torch.channels_last_3d)
+        return x.contiguous()
+
+    def _descs(self, B: int, dtype: int, layouts):
         import torch.nn as nn
         out = []
-        for m, a in zip(self.layers, self._acts):
+        for m, a, lay in zip(self.layers, self._acts, layouts):
             hb = m.bias is not None
             if isinstance(m, nn.Linear):
                 T = a.numel() // (B * m.in_features)
@@ -110,11 +132,11 @@ class PrivacyEngine:
             elif isinstance(m, nn.Conv3d):
                 out.append(layer_desc(DP_CONV3D, dtype, B=B, p=m.out_channels, Cin=m.in_channels, Z=a.shape[2],
                                       H=a.shape[3], W=a.shape[4], k=m.kernel_size[0], stride=m.stride[0],
-                                      pad=m.padding[0], dil=m.dilation[0], has_bias=hb))
+                                      pad=m.padding[0], dil=m.dilation[0], has_bias=hb, layout=lay))
             else:
                 out.append(layer_desc(DP_CONV2D, dtype, B=B, p=m.out_channels, Cin=m.in_channels, H=a.shape[2],
                                       W=a.shape[3], k=m.kernel_size[0], stride=m.stride[0], pad=m.padding[0],
-                                      dil=m.dilation[0], has_bias=hb))
+                                      dil=m.dilation[0], has_bias=hb, layout=lay))
         return out
 
     def privatise(self, seed: int, stream=None):
@@ -127,15 +149,16 @@ class PrivacyEngine:
         if dt not in (torch.bfloat16, torch.float32):
             raise ValueError(f"inputs of dtype {dt}: bf16 or fp32 only")
         dtype = DP_BF16 if dt == torch.bfloat16 else DP_FP32
-        key = (B, dtype, tuple(tuple(a.shape) for a in self._acts))
+        layouts = [self._layout(m, a) for m, a in zip(self.layers, self._acts)]
+        key = (B, dtype, tuple(tuple(a.shape) for a in self._acts), tuple(layouts))
         if self._key != key:
-            self._step = ClipStep(self._descs(B, dtype), C=self.C, sigma=self.sigma, per_layer=self.per_layer,
+            self._step = ClipStep(self._descs(B, dtype, layouts), C=self.C, sigma=self.sigma, per_layer=self.per_layer,
                                   norm_modes=[self.norm_mode] * len(self.layers), device=str(self._acts[0].device),
                                   keep_grads=self.keep_grads)
             self._key = key
         scale = float(B) if self.loss_reduction == "mean" else 1.0
-        inputs = [(a.to(dt).contiguous(), (g * scale if scale != 1.0 else g).to(dt).contiguous())
-                  for a, g in zip(self._acts, self._grads)]
+        inputs = [(self._as_layout(a, lay, dt), self._as_layout(g * scale if scale != 1.0 else g, lay, dt))
+                  for a, g, lay in zip(self._acts, self._grads, layouts)]
         flat = self._step.run(inputs, seed=seed, stream=stream)
         for l, m in enumerate(self.layers):
             dW, db = self._step.layer_views(l)

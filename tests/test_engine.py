@@ -93,6 +93,26 @@ def test_engine_matches_naive_per_example_loop(lib, no_tf32, dtype, tol):
 
 
 @pytest.mark.gpu
+def test_engine_channels_last_model(lib):
+    """A channels_last model: its conv layers are handed over channels last (no layout copy)
+    and give the naive per-example loop's result."""
+    model = _model(torch.bfloat16).cuda().to(memory_format=torch.channels_last)
+    gen = torch.Generator().manual_seed(9)
+    x = torch.randn(6, 3, 6, 6, generator=gen).to(torch.bfloat16).cuda().to(memory_format=torch.channels_last)
+    y = torch.randint(0, 5, (6,), generator=gen).cuda()
+    want = _naive_reference(model, x, y, C=0.5, sigma=0.3, seed=21)
+    eng = lib.PrivacyEngine(model, C=0.5, sigma=0.3)
+    model.zero_grad()
+    nn.functional.cross_entropy(model(x).float(), y, reduction="sum").backward()
+    got = eng.privatise(seed=21).double().cpu().numpy()
+    convs = [m for m in eng.layers if isinstance(m, nn.Conv2d)]
+    assert [d.layout for d, m in zip(eng._step.descs, eng.layers) if isinstance(m, nn.Conv2d)] == \
+        [lib.DP_NHWC] * len(convs)
+    eng.detach()
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) <= 2e-2
+
+
+@pytest.mark.gpu
 def test_engine_conv1d_model(lib, no_tf32):
     torch.manual_seed(3)
     model = nn.Sequential(nn.Conv1d(4, 8, 3, padding=1), nn.ReLU(), nn.Conv1d(8, 8, 5, stride=2, padding=2),
