@@ -357,12 +357,12 @@ size_t max_ws_bytes(const Geom& g, int mode) {
 // Launch the row layout of a conv layer into the workspace; returns the pointers.
 cudaError_t prepare_rows(const Geom& g, const Plan& pl, const void*& A, const void*& G, void*& ws,
                          cudaStream_t stream, const float* scale = nullptr, float* db = nullptr,
-                         int accumulate = 0, float* bias_part = nullptr) {
+                         int accumulate = 0, float* bias_part = nullptr, dph::NoiseArgs* nz = nullptr) {
   if (!pl.rows) return cudaSuccess;
   uint8_t* base = static_cast<uint8_t*>(ws);
   void* U = base;
   void* Gt = base + align256((size_t)g.B * g.T * dph::conv_rows_width(g) * 2);
-  cudaError_t e = dph::launch_conv_rows(g, A, G, U, Gt, stream, scale, db, accumulate, bias_part);
+  cudaError_t e = dph::launch_conv_rows(g, A, G, U, Gt, stream, scale, db, accumulate, bias_part, nz);
   A = U;
   if (!g.nhwc || scale) G = Gt;     // channels-last output gradients are the rows already
   ws = base + rows_bytes(g);
@@ -498,12 +498,14 @@ static dp_status noise_args(const dp_noise_desc* nd, const Geom& g, dph::NoiseAr
 
 // The noise pass over dW and db when no kernel of the sum fused it.
 static cudaError_t finish_noise(const Geom& g, float* dW, float* db, const dph::NoiseArgs* nz, cudaStream_t s) {
-  if (!nz || !nz->on || nz->applied) return cudaSuccess;
+  if (!nz || !nz->on) return cudaSuccess;
   const size_t nw = (size_t)g.p * g.D;
-  if (db && db == dW + nw)
+  const bool w = !nz->applied_a, b = db && !nz->applied_b;
+  if (w && b && db == dW + nw)
     return dph::launch_add_noise(dW, nw + g.p, nz->sc, nz->invB, nz->seed, nz->off_a, nz->seed_dev, s);
-  cudaError_t e = dph::launch_add_noise(dW, nw, nz->sc, nz->invB, nz->seed, nz->off_a, nz->seed_dev, s);
-  if (e == cudaSuccess && db) e = dph::launch_add_noise(db, g.p, nz->sc, nz->invB, nz->seed, nz->off_b, nz->seed_dev, s);
+  cudaError_t e = w ? dph::launch_add_noise(dW, nw, nz->sc, nz->invB, nz->seed, nz->off_a, nz->seed_dev, s)
+                    : cudaSuccess;
+  if (e == cudaSuccess && b) e = dph::launch_add_noise(db, g.p, nz->sc, nz->invB, nz->seed, nz->off_b, nz->seed_dev, s);
   return e;
 }
 
@@ -535,7 +537,7 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
                                                          align256(dph::tc_sum_ws_bytes(pl.lg)))
                               : nullptr;
   cudaError_t e = prepare_rows(g, pl, A, G, wsp, stream, prescale ? factors : nullptr, prescale ? db : nullptr,
-                               accumulate, bias_part);
+                               accumulate, bias_part, prescale ? nz : nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "dp_clipped_sum row layout");
   // padded columns: the kernel writes a padded buffer, then its first D columns go out
   const bool padded = pl.rows && padded_out_bytes(g) != 0;
@@ -553,9 +555,9 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
   else if (pl.kernel == 4 || pl.kernel == 3) {
     const bool xh = reuse_norm_mode >= 0 && norm_leaves_nhwc(g, reuse_norm_mode, desc->dtype, A, G, workspace);
     if (pl.kernel == 4)
-      e = dph::launch_tc_sum_conv(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, xh);
+      e = dph::launch_tc_sum_conv(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, xh, nz);
     else
-      e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, xh);
+      e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, xh, nz);
   }
   else if (pl.kernel == 6)
     e = dph::launch_tc_sum2(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
@@ -563,11 +565,12 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
     e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream, padded ? nullptr : nz,
                             !pl.rows);
   else if (prescale) {
-    e = dph::launch_tc_sum_prescaled(pl.lg, A, G, kdW, kacc, static_cast<float*>(wsp), status_ptr(), stream);
+    e = dph::launch_tc_sum_prescaled(pl.lg, A, G, kdW, kacc, static_cast<float*>(wsp), status_ptr(), stream,
+                                     padded ? nullptr : nz);
     kdb = nullptr;   // the bias went straight to db
   } else if (pl.kernel == 1)
     e = dph::launch_tc_sum(pl.lg, A, G, factors, kdW, kdb, kacc, static_cast<float*>(wsp), status_ptr(),
-                           stream);
+                           stream, padded ? nullptr : nz);
   else
     e = dph::launch_simt_clipped_sum(g, desc->dtype, A, G, factors, dW, db, accumulate,
                                      static_cast<float*>(wsp), (int)dph::simt_sum_splits(g), stream);

@@ -139,7 +139,7 @@ struct NoiseArgs {
   uint64_t seed;
   const unsigned long long* seed_dev;   // non-null: the seed is read here when the kernel runs
   uint64_t off_a, off_b;                // flat index of the first element of segment a / b
-  int applied;                          // host: set by the launcher that fused it
+  int applied_a, applied_b;             // host: set by the launcher that fused it (dW, db)
 };
 
 // z_e for the four consecutive flat indices e0 .. e0+3 (one or two Philox blocks).
@@ -223,12 +223,13 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
 cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
                                   float sigma_l2, uint64_t seed, int layer, float* out,
                                   cudaStream_t s);
-// out[e] (+)= sum_k ws[k*n + e], fixed order.
+// out[e] (+)= sum_k ws[k*n + e], fixed order; with nz->on also the noise of flat index
+// noff + e and the 1/B scale.
 cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
-                                 cudaStream_t s);
+                                 cudaStream_t s, const dpk::NoiseArgs* nz = nullptr, uint64_t noff = 0);
 // The weight and bias reductions of one clipped sum in one launch (segments: dpk::SplitSeg).
-// With nz->on the same pass adds the noise and the 1/B scale (nz->applied is then set;
-// with the short-vector kernels it is left for a separate noise pass).
+// With nz->on the same pass adds the noise and the 1/B scale to both segments (nz->applied_a
+// and applied_b are then set; with the short-vector kernels it is left for a noise pass).
 using dpk::SplitSeg;
 using dpk::NoiseArgs;
 cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumulate, cudaStream_t s,

@@ -97,7 +97,7 @@ cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep,
   if (conv_kk > 0) {
     e = launch_conv_reduce(part, splits, p, D, conv_kk, dW, accumulate, s);
     if (e != cudaSuccess || !bias) return e;
-    return launch_reduce_splits(part_b, splits, (size_t)p, db, accumulate, s);
+    return conv_bias_reduce(part_b, splits, p, db, accumulate, s, nz);
   }
   return launch_reduce_splits2(SplitSeg{part, nw, nw, dW}, SplitSeg{part_b, (size_t)p, bias ? (size_t)p : 0, db},
                                splits, accumulate, s, nz);

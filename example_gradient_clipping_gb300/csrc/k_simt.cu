@@ -124,15 +124,22 @@ __global__ void __launch_bounds__(kThreads) simt_clipped_sum_kernel(Geom g, cons
 }
 
 // out[e] (+)= sum_s ws[s*n + e]  (fixed order: deterministic)
+// With nz.on, the reductions below also add the Gaussian noise of element e (flat index
+// noff + e) and the 1/B scale on the way out, as the separate noise pass does.
+__device__ __forceinline__ float with_noise(const NoiseArgs& nz, uint64_t seed, uint64_t e, float v) {
+  return nz.on ? fmaf(nz.sc, noise_z1(e, seed), v) * nz.invB : v;
+}
+
 __global__ void reduce_splits_kernel(const float* __restrict__ ws, int splits, size_t n,
-                                     float* __restrict__ out, int accumulate) {
+                                     float* __restrict__ out, int accumulate, NoiseArgs nz, uint64_t noff) {
   pdl_trigger();
   pdl_wait();
+  const uint64_t seed = nz.on && nz.seed_dev ? (uint64_t)*nz.seed_dev : nz.seed;
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
     float s = accumulate ? out[e] : 0.f;
     for (int k = 0; k < splits; ++k) s += ws[(size_t)k * n + e];
-    out[e] = s;
+    out[e] = with_noise(nz, seed, noff + e, s);
   }
 }
 
@@ -200,25 +207,27 @@ __global__ void reduce_splits2_kernel(SplitSeg a, SplitSeg b, int splits, int ac
 // Many splits of a short vector: one warp per element, lanes stride over the splits,
 // then a fixed butterfly (deterministic).
 __global__ void reduce_splits_warp_kernel(const float* __restrict__ ws, int splits, size_t n,
-                                          float* __restrict__ out, int accumulate) {
+                                          float* __restrict__ out, int accumulate, NoiseArgs nz, uint64_t noff) {
   pdl_trigger();
   pdl_wait();
+  const uint64_t seed = nz.on && nz.seed_dev ? (uint64_t)*nz.seed_dev : nz.seed;
   const int lane = threadIdx.x & 31;
   const size_t nw = ((size_t)gridDim.x * blockDim.x) >> 5;
   for (size_t e = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; e < n; e += nw) {
     float s = 0.f;
     for (int k = lane; k < splits; k += 32) s += ws[(size_t)k * n + e];
     s = warp_sum(s);
-    if (lane == 0) out[e] = accumulate ? out[e] + s : s;
+    if (lane == 0) out[e] = with_noise(nz, seed, noff + e, accumulate ? out[e] + s : s);
   }
 }
 
 // Very many splits of a short vector: one block per element, threads stride over the
 // splits, then a fixed tree over the block (deterministic).
 __global__ void reduce_splits_block_kernel(const float* __restrict__ ws, int splits, size_t n,
-                                           float* __restrict__ out, int accumulate) {
+                                           float* __restrict__ out, int accumulate, NoiseArgs nz, uint64_t noff) {
   pdl_trigger();
   pdl_wait();
+  const uint64_t seed = nz.on && nz.seed_dev ? (uint64_t)*nz.seed_dev : nz.seed;
   __shared__ float red[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (size_t e = blockIdx.x; e < n; e += gridDim.x) {
@@ -230,7 +239,7 @@ __global__ void reduce_splits_block_kernel(const float* __restrict__ ws, int spl
     if (warp == 0) {
       float t = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.f;
       t = warp_sum(t);
-      if (lane == 0) out[e] = accumulate ? out[e] + t : t;
+      if (lane == 0) out[e] = with_noise(nz, seed, noff + e, accumulate ? out[e] + t : t);
     }
     __syncthreads();
   }
@@ -396,28 +405,34 @@ cudaError_t launch_simt_clipped_sum(const Geom& g, int dtype, const void* A, con
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t n = (size_t)g.p * g.D;
-  launch_pdl(reduce_splits_kernel, (unsigned)std::min<size_t>((n + 255) / 256, 152 * 8), 256, 0, s, ws, splits, n, dW, accumulate);
+  const NoiseArgs none = {};
+  launch_pdl(reduce_splits_kernel, (unsigned)std::min<size_t>((n + 255) / 256, 152 * 8), 256, 0, s, ws, splits, n, dW,
+             accumulate, none, (uint64_t)0);
   if (db) {
     launch_pdl(reduce_splits_kernel, (unsigned)((g.p + 255) / 256), 256, 0, s, ws_db, splits, (size_t)g.p, db,
-                                                                       accumulate);
+               accumulate, none, (uint64_t)0);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, const NoiseArgs* nz, uint64_t noff) {
+  const NoiseArgs none = {};
+  const NoiseArgs& na = (nz && nz->on) ? *nz : none;
   if (splits >= 512 && n <= ((size_t)1 << 14)) {
     const unsigned blocks = (unsigned)std::min<size_t>(n, 152 * 8);
-    launch_pdl(reduce_splits_block_kernel, blocks ? blocks : 1, 256, 0, s, ws, splits, n, out, accumulate);
+    launch_pdl(reduce_splits_block_kernel, blocks ? blocks : 1, 256, 0, s, ws, splits, n, out, accumulate, na, noff);
     return cudaGetLastError();
   }
   if (splits >= 16 && n <= ((size_t)1 << 16)) {
     const size_t blocks = std::min<size_t>((n * 32 + 255) / 256, 152 * 8);
-    launch_pdl(reduce_splits_warp_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate);
+    launch_pdl(reduce_splits_warp_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate,
+               na, noff);
     return cudaGetLastError();
   }
   const size_t blocks = std::min<size_t>((n + 255) / 256, 152 * 8);
-  launch_pdl(reduce_splits_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate);
+  launch_pdl(reduce_splits_kernel, (unsigned)(blocks ? blocks : 1), 256, 0, s, ws, splits, n, out, accumulate, na,
+             noff);
   return cudaGetLastError();
 }
 
@@ -442,7 +457,7 @@ cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumu
   const unsigned blocks = (unsigned)std::min<size_t>((items + 255) / 256, 152 * 8);
   if (v4) launch_pdl(reduce_splits2_kernel<4>, blocks, 256, 0, s, a, b, splits, accumulate, na);
   else launch_pdl(reduce_splits2_kernel<1>, blocks, 256, 0, s, a, b, splits, accumulate, na);
-  if (noise) nz->applied = 1;
+  if (noise) nz->applied_a = nz->applied_b = 1;
   return cudaGetLastError();
 }
 

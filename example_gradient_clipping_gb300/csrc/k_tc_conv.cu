@@ -340,7 +340,10 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
 }
 
 // dW[j, m] (+)= sum_s part[s, j, n(m)] in split order; n(m) maps the weight column
-// m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64).
+// m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64).  (The noise of a fused
+// call is not drawn here: one output per thread would draw a whole Philox block per output,
+// which measured slower than the separate four-outputs-per-block noise pass on the large
+// layers; grouping four outputs per thread instead starved the small layers of threads.)
 __global__ void conv_reduce_kernel(const float* __restrict__ part, int splits, int p, int ncols, int kk,
                                    float* __restrict__ dW, int accumulate) {
   pdl_trigger();
@@ -468,6 +471,13 @@ cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, 
   return cudaGetLastError();
 }
 
+cudaError_t conv_bias_reduce(const float* part_db, int splits, int p, float* db, int accumulate, cudaStream_t s,
+                             NoiseArgs* nz) {
+  const cudaError_t e = launch_reduce_splits(part_db, splits, (size_t)p, db, accumulate, s, nz, nz ? nz->off_b : 0);
+  if (nz && nz->on) nz->applied_b = 1;
+  return e;
+}
+
 template <bool kNorm>
 static cudaError_t launch_kernel(const Geom& g, const ConvPlan& c, const CUtensorMap& mG, const CUtensorMap& mX,
                                  const tcconv::Params& P, cudaStream_t s) {
@@ -525,7 +535,8 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
 }
 
 cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, bool reuse_xh) {
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, bool reuse_xh,
+                               NoiseArgs* nz) {
   const ConvPlan c = conv_plan(g, false);
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* part = reinterpret_cast<float*>(w + nhwc_bytes(g));
@@ -544,7 +555,7 @@ cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, cons
   if (e != cudaSuccess) return e;
   e = launch_conv_reduce(part, c.splits, g.p, c.items * 64, g.k * g.k, dW, accumulate, s);
   if (e != cudaSuccess || !db) return e;
-  return launch_reduce_splits(part_db, c.splits, (size_t)g.p, db, accumulate, s);
+  return conv_bias_reduce(part_db, c.splits, g.p, db, accumulate, s, nz);
 }
 
 

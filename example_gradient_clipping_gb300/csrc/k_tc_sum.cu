@@ -334,11 +334,11 @@ size_t tc_sum_ws_bytes(const Geom& g) {
 // weight layout).
 static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtensorMap& ma, const float* factors,
                               float* dW, float* db, int accumulate, float* ws, unsigned* status, cudaStream_t s,
-                              bool prescaled = false);
+                              bool prescaled = false, NoiseArgs* nz = nullptr);
 
 cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
                           float* dW, float* db, int accumulate, float* ws, unsigned* status,
-                          cudaStream_t s) {
+                          cudaStream_t s, NoiseArgs* nz) {
   const long R = (long)g.B * g.T;
   CUtensorMap mg, ma;
   const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)R}, sg[1] = {(uint64_t)g.p * 2};
@@ -346,11 +346,11 @@ cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const flo
   const uint32_t box[2] = {64, tcsum::BK};
   if (!encode_tmap_bf16(&mg, G, 2, dg, sg, box) || !encode_tmap_bf16(&ma, A, 2, da, sa, box))
     return cudaErrorInvalidValue;
-  return run_tc_sum(g, mg, ma, factors, dW, db, accumulate, ws, status, s);
+  return run_tc_sum(g, mg, ma, factors, dW, db, accumulate, ws, status, s, false, nz);
 }
 
 cudaError_t launch_tc_sum_prescaled(const Geom& g, const void* A, const void* Gs, float* dW, int accumulate,
-                                    float* ws, unsigned* status, cudaStream_t s) {
+                                    float* ws, unsigned* status, cudaStream_t s, NoiseArgs* nz) {
   const long R = (long)g.B * g.T;
   CUtensorMap mg, ma;
   const uint64_t dg[2] = {(uint64_t)g.p, (uint64_t)R}, sg[1] = {(uint64_t)g.p * 2};
@@ -358,7 +358,7 @@ cudaError_t launch_tc_sum_prescaled(const Geom& g, const void* A, const void* Gs
   const uint32_t box[2] = {64, tcsum::BK};
   if (!encode_tmap_bf16(&mg, Gs, 2, dg, sg, box) || !encode_tmap_bf16(&ma, A, 2, da, sa, box))
     return cudaErrorInvalidValue;
-  return run_tc_sum(g, mg, ma, nullptr, dW, nullptr, accumulate, ws, status, s, true);
+  return run_tc_sum(g, mg, ma, nullptr, dW, nullptr, accumulate, ws, status, s, true, nz);
 }
 
 // Conv layers with Cin % 64 == 0: the unfolded rows come from TMA im2col loads over an
@@ -379,7 +379,8 @@ size_t tc_sum_conv_ws_bytes(const Geom& g) {
 }
 
 cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, bool reuse_xh) {
+                               float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s, bool reuse_xh,
+                               NoiseArgs* nz) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   void* Xh = w;
   void* Gt = w + al256s((size_t)g.B * g.H * g.W * g.Cin * 2);
@@ -392,7 +393,7 @@ cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, cons
   if (g.nhwc) Xh = const_cast<void*>(A);
   // bf16(c_i G_i^T) and db in one pass, written right before the GEMM reads it (L2-hot);
   // rereading a norm call's unscaled rows and scaling them in the GEMM measured slower
-  e = launch_scaled_rows(g.B, g.T, g.p, G, Gt, factors, db, accumulate, part_db, s, g.nhwc != 0);
+  e = launch_scaled_rows(g.B, g.T, g.p, G, Gt, factors, db, accumulate, part_db, s, g.nhwc != 0, nz);
   if (e != cudaSuccess) return e;
   const long R = (long)g.B * g.T;
   CUtensorMap mg, ma;
@@ -400,12 +401,12 @@ cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, cons
   const uint32_t box[2] = {64, tcsum::BK};
   if (!encode_tmap_bf16(&mg, Gt, 2, dg, sg, box) || !encode_im2col_bf16(&ma, Xh, g, tcsum::BK))
     return cudaErrorInvalidValue;
-  return run_tc_sum(g, mg, ma, nullptr, dW, nullptr, accumulate, part, status, s, true);
+  return run_tc_sum(g, mg, ma, nullptr, dW, nullptr, accumulate, part, status, s, true, nz);
 }
 
 static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtensorMap& ma, const float* factors,
                               float* dW, float* db, int accumulate, float* ws, unsigned* status, cudaStream_t s,
-                              bool prescaled) {
+                              bool prescaled, NoiseArgs* nz) {
   const long R = (long)g.B * g.T;
   int splits;
   long rps;
@@ -443,11 +444,12 @@ static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtens
   if (!g.conv) {
     const size_t nw = (size_t)g.p * g.D;
     return launch_reduce_splits2(SplitSeg{ws, nw, nw, dW},
-                                 SplitSeg{P.ws_db, (size_t)g.p, P.ws_db ? (size_t)g.p : 0, db}, splits, accumulate, s);
+                                 SplitSeg{P.ws_db, (size_t)g.p, P.ws_db ? (size_t)g.p : 0, db}, splits, accumulate, s,
+                                 nz);
   }
   e = launch_conv_reduce(ws, splits, g.p, g.D, g.k * g.k, dW, accumulate, s);
   if (e != cudaSuccess) return e;
-  if (P.ws_db) e = launch_reduce_splits(P.ws_db, splits, (size_t)g.p, db, accumulate, s);
+  if (P.ws_db) e = conv_bias_reduce(P.ws_db, splits, g.p, db, accumulate, s, nz);
   return e;
 }
 

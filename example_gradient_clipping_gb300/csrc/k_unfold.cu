@@ -281,7 +281,7 @@ using namespace dpk;
 int conv_rows_width(const Geom& g) { return (g.D + 7) / 8 * 8; }
 
 cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s,
-                             const float* scale, float* db, int accumulate, float* bias_part) {
+                             const float* scale, float* db, int accumulate, float* bias_part, NoiseArgs* nz) {
   const int Dp = conv_rows_width(g);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   auto* Ub = static_cast<__nv_bfloat16*>(U);
@@ -307,7 +307,7 @@ cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* 
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (scale) return launch_scaled_rows(g.B, g.T, g.p, G, Gt, scale, db, accumulate, bias_part, s, g.nhwc != 0);
+  if (scale) return launch_scaled_rows(g.B, g.T, g.p, G, Gt, scale, db, accumulate, bias_part, s, g.nhwc != 0, nz);
   if (g.nhwc) return cudaSuccess;        // channels last: G is already the rows the kernels read
   return launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);
 }
@@ -342,7 +342,7 @@ cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* ds
 }
 
 cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
-                               int accumulate, float* bias_part, cudaStream_t s, bool rows_in) {
+                               int accumulate, float* bias_part, cudaStream_t s, bool rows_in, NoiseArgs* nz) {
   if (rows_in) {   // channels last: scale in place of the transpose, one bias partial per example
     if (p % 8) return cudaErrorInvalidValue;
     const size_t n = (size_t)B * (p / 8);
@@ -352,11 +352,11 @@ cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, con
                  db ? bias_part : nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !db) return e;
-    return launch_reduce_splits(bias_part, B, (size_t)p, db, accumulate, s);
+    return conv_bias_reduce(bias_part, B, p, db, accumulate, s, nz);
   }
   cudaError_t e = launch_transpose_rows(B, T, p, G, Gt, s, factors, db ? bias_part : nullptr);
   if (e != cudaSuccess || !db) return e;
-  return launch_reduce_splits(bias_part, transpose_bias_parts(B, T), (size_t)p, db, accumulate, s);
+  return conv_bias_reduce(bias_part, transpose_bias_parts(B, T), p, db, accumulate, s, nz);
 }
 
 size_t scaled_rows_bias_bytes(int B, int T, int p) {

@@ -11,10 +11,10 @@ bool tc_sum_supported(const Geom& g);
 size_t tc_sum_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sum(const Geom& g, const void* A, const void* G, const float* factors,
                           float* dW, float* db, int accumulate, float* ws, unsigned* status,
-                          cudaStream_t s);
+                          cudaStream_t s, dpk::NoiseArgs* nz = nullptr);
 // The same GEMM over rows whose G part already holds bf16(c_i G) (no bias).
 cudaError_t launch_tc_sum_prescaled(const Geom& g, const void* A, const void* Gs, float* dW, int accumulate,
-                                    float* ws, unsigned* status, cudaStream_t s);
+                                    float* ws, unsigned* status, cudaStream_t s, dpk::NoiseArgs* nz = nullptr);
 // Clipped sum with per-example TMEM accumulation and fp32 scaling (rows per example >= 64).
 bool tc_sumx_supported(const Geom& g);
 size_t tc_sumx_ws_bytes(const Geom& g);
@@ -57,14 +57,15 @@ int conv_rows_width(const Geom& g);
 // row-scaled clipped sum) and db (if given) receives the bias sum (see launch_scaled_rows).
 cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* U, void* Gt, cudaStream_t s,
                              const float* scale = nullptr, float* db = nullptr, int accumulate = 0,
-                             float* bias_part = nullptr);
+                             float* bias_part = nullptr, dpk::NoiseArgs* nz = nullptr);
 // Per example [p, T] -> [T, p] (bf16): the output gradient's row layout, and NCHW -> NHWC.
 cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s,
                                   const float* scale = nullptr, float* bias_part = nullptr);
 // Gt = bf16(c_i G_i^T) for the row-scaled clipped sum, and db (+)= sum_i c_i sum_t G[i, :, t]
 // from fp32 partial sums taken on the way (bias_part: scaled_rows_bias_bytes).
 cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
-                               int accumulate, float* bias_part, cudaStream_t s, bool rows_in = false);
+                               int accumulate, float* bias_part, cudaStream_t s, bool rows_in = false,
+                               dpk::NoiseArgs* nz = nullptr);
 size_t scaled_rows_bias_bytes(int B, int T, int p);
 // Conv layers with the unfold done by TMA im2col loads (Cin % 64 == 0, T % 8 == 0, T >= 64):
 // instantiated norm and clipped sum; the workspace holds an NHWC copy of the input.
@@ -77,20 +78,24 @@ cudaError_t launch_tc_conv_norm(const Geom& g, const void* A, const void* G, flo
 // reuse_xh: the workspace already holds the NHWC copy of the input (a norm call left it).
 cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
                                float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
-                               bool reuse_xh = false);
+                               bool reuse_xh = false, dpk::NoiseArgs* nz = nullptr);
 // im2col map (bf16, 128-byte swizzle, 64 channels per pixel) over an NHWC copy of a conv input.
 bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pixels);
 // dW[j, m] (+)= sum over splits of part[s, j, col(m)], col mapping the weight column
 // m = c*kk + tap to the im2col tile column (c/64 * kk + tap) * 64 + c % 64.
 cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
                                cudaStream_t s);
+// A conv sum's bias: db (+)= the splits of part_db [splits, p] in order, with nz's noise
+// (nz->applied_b is then set).
+cudaError_t conv_bias_reduce(const float* part_db, int splits, int p, float* db, int accumulate, cudaStream_t s,
+                             dpk::NoiseArgs* nz = nullptr);
 // Row-scaled clipped sum of a conv layer (Cin % 64 == 0) with im2col loads for the input.
 bool tc_sum_conv_supported(const Geom& g);
 size_t tc_sum_conv_ws_bytes(const Geom& g);
 // reuse_xh: the workspace already holds the NHWC copy of the input (a norm call left it).
 cudaError_t launch_tc_sum_conv(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
                                float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
-                               bool reuse_xh = false);
+                               bool reuse_xh = false, dpk::NoiseArgs* nz = nullptr);
 // Ghost norm of a conv layer (Cin % 64 == 0) with im2col loads for the input Gram.
 bool tc_ghost_conv_supported(const Geom& g);
 size_t tc_ghost_conv_ws_bytes(const Geom& g);

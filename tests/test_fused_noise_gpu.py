@@ -12,18 +12,25 @@ import pytest
 
 import oracle
 import workloads
-from helpers import TOL, desc_for, rel_vec, to_dev
+from helpers import TOL, desc_for, rel_vec, to_dev, to_dev_channels_last
 from workloads import LayerSpec, Workload
 
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (name, spec, B, dtype, fused into the split reduction)
-    ("seq_linear_b64_t128", None, 64, "bf16", True),
-    ("t1_fp32_splits", LayerSpec("e", "linear", p=40, d=36, T=1), 100, "fp32", True),
-    ("conv_rows", LayerSpec("e", "conv2d", p=64, Cin=16, H=12, W=12, k=3, pad=1), 5, "bf16", False),
-    ("conv_im2col", LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 3, "bf16", False),
-    ("ffma_small", LayerSpec("e", "linear", p=6, d=10, T=5), 4, "fp32", False),
+    # (name, spec, B, dtype, channels last, fused into the sum's final reductions)
+    ("seq_linear_b64_t128", None, 64, "bf16", False, True),
+    ("t1_fp32_splits", LayerSpec("e", "linear", p=40, d=36, T=1), 100, "fp32", False, True),
+    ("lin_rowscaled", LayerSpec("e", "linear", p=128, d=64, T=40), 5, "bf16", False, True),
+    ("conv_rows", LayerSpec("e", "conv2d", p=64, Cin=16, H=12, W=12, k=3, pad=1), 5, "bf16", False, True),
+    # im2col conv sums: the bias gets its noise in its reduction, the weights in a noise pass
+    ("conv_im2col", LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 3, "bf16", False, False),
+    ("conv_im2col_rowscaled", LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=3, pad=1), 4, "bf16", False, False),
+    ("conv_im2col_rowscaled_cl", LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=3, pad=1), 4, "bf16", True,
+     False),
+    # padded unfolded width: the weights get their noise after the compaction
+    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16", False, False),
+    ("ffma_small", LayerSpec("e", "linear", p=6, d=10, T=5), 4, "fp32", False, False),
 ]
 
 
@@ -38,15 +45,16 @@ def _case(name, spec, B, dtype):
     return wl, spec, A, G, fac
 
 
-@pytest.mark.parametrize("name,spec,B,dtype,fused", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("name,spec,B,dtype,cl,fused", CASES, ids=[c[0] for c in CASES])
 @pytest.mark.parametrize("offset,accumulate,with_db", [(0, 0, True), (3, 1, True), (6, 0, False)])
-def test_fused_equals_sum_then_noise(lib, name, spec, B, dtype, fused, offset, accumulate, with_db):
+def test_fused_equals_sum_then_noise(lib, name, spec, B, dtype, cl, fused, offset, accumulate, with_db):
     import torch
     dp = lib
     wl, spec, A, G, fac = _case(name, spec, B, dtype)
-    desc = desc_for(dp, spec, wl.B, wl.dtype)
+    desc = desc_for(dp, spec, wl.B, wl.dtype, layout=dp.DP_NHWC if cl else dp.DP_NCHW)
     p, D = spec.p, spec.D
-    dA, dG = to_dev(A, wl.dtype), to_dev(G, wl.dtype)
+    conv = to_dev_channels_last if cl else to_dev
+    dA, dG = conv(A, wl.dtype), conv(G, wl.dtype)
     f = torch.tensor(fac, dtype=torch.float32, device="cuda")
     ws = torch.empty(max(dp.dp_workspace_size(desc, dp.DP_NORM_AUTO), 16), dtype=torch.uint8, device="cuda")
     gen = torch.Generator(device="cuda").manual_seed(5)
@@ -71,7 +79,7 @@ def test_fused_equals_sum_then_noise(lib, name, spec, B, dtype, fused, offset, a
         outs.append(flat[:p * D + (p if db is not None else 0)].cpu())
     assert torch.equal(outs[0], outs[1])
     if fused:
-        assert n_fused == n_sum          # the noise rode in the split reduction
+        assert n_fused == n_sum          # the noise rode in the sum's final reductions
     else:
         assert n_fused > n_sum
 
