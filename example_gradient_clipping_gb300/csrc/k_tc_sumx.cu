@@ -9,7 +9,9 @@
 // with D += c_i * P_i.  No operand is rescaled or re-rounded, and no CUDA-core work
 // sits between a TMA load and the MMA that consumes it.  Rows of example i are loaded
 // with 3D TMA boxes [1, rows, 64] (rows past T read as zero): full 64-row stages,
-// then 16-row stages for the remainder.  In CTAs of the first column tile the
+// then 16-row stages for the remainder.  A column tile narrower than 256 (the layer's
+// last, or a narrow layer) loads only the boxes it needs and runs its MMAs at that width
+// (a multiple of 16).  In CTAs of the first column tile the
 // epilogue warps also sum the G rows from shared memory for the bias.  Examples are
 // split across the CTAs of a thread-block cluster (up to 4 per output tile): after
 // the main loop each CTA stages its fp32 partial tile in its own shared memory, and
@@ -54,7 +56,6 @@ constexpr int kEpiFirst = 4;                 // first epilogue warp
 constexpr int kSyncThreads = 32 * (kBiasWarps + kEpiWarps);   // warps 3-11, named barrier 1
 constexpr int kLeader = 96;                  // first worker thread (warp 3, lane 0)
 constexpr int SMEM = STAGES * STAGE + 1024 + 512;
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BM, BN, 1, 1);
 
 constexpr int PSTR = BN + 4;                 // staged partial row stride (floats)
 constexpr int PART_BYTES = BM * PSTR * 4;    // staged weight partial, then 128 bias floats
@@ -98,13 +99,24 @@ __device__ __forceinline__ bool finish_decision(Ctl* c) {
   return c->flags[1] != 0;
 }
 
+// The MMA width of column tile n0: the layer's remaining columns rounded up to 16 (at most
+// BN), so narrow layers load and multiply only their own columns.
+// kTrim false (every column tile full: D % 256 == 0) keeps the full-width code paths.
+template <bool kTrim>
+__device__ __forceinline__ int tile_n(const Params& P, int n0) {
+  if constexpr (!kTrim) return BN;
+  else return min(BN, (P.d - n0 + 15) & ~15);
+}
+
 // Warps 0 and 2 (all lanes): TMA producers; producer `pr` loads the stages k with
-// k % 2 == pr.
+// k % 2 == pr (the two G boxes and the A boxes the tile's width needs).
+template <bool kTrim>
 __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG64, const CUtensorMap* mA64,
                                          const CUtensorMap* mG16, const CUtensorMap* mA16, uint8_t* smem,
                                          Ctl* c, int e0, int e1, int m0, int n0, int pr) {
   volatile int* abort = &c->abort;
   const int ns = P.nfull + P.n16;
+  const int na = (tile_n<kTrim>(P, n0) + 63) / 64;      // A boxes per stage
   int k = 0, issued = 0;
   bool live = true;
   int last = -1;
@@ -120,11 +132,12 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG6
       const CUtensorMap* ma = big ? mA64 : mA16;
       uint8_t* st = smem + s * STAGE;
       if (ptx::elect_one()) {
-        ptx::mbar_arrive_expect_tx(&c->full[s], (big ? 64 : 16) * 128 * 6);
+        ptx::mbar_arrive_expect_tx(&c->full[s], (big ? 64 : 16) * 128 * (2 + na));
         ptx::tma_load_3d(mg, &c->full[s], st, m0, y, e);
         ptx::tma_load_3d(mg, &c->full[s], st + BOX, m0 + 64, y, e);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ptx::tma_load_3d(ma, &c->full[s], st + (2 + j) * BOX, n0 + 64 * j, y, e);
+        for (int j = 0; j < 4; ++j)
+          if (j < na) ptx::tma_load_3d(ma, &c->full[s], st + (2 + j) * BOX, n0 + 64 * j, y, e);
       }
       __syncwarp();
       ++issued;
@@ -140,10 +153,12 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG6
 
 // Warp 1 (all lanes): MMA issuer.  Descriptors are built once per stage from the
 // stage base; the elected lane issues the MMAs and the commits.
+template <bool kTrim>
 __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0,
                                            int e1) {
   volatile int* abort = &c->abort;
   const int ns = P.nfull + P.n16;
+  const uint32_t idesc = ptx::idesc_bf16_f32(BM, tile_n<kTrim>(P, blockIdx.y * BN), 1, 1);
   int k = 0;
   bool live = true;
   for (int e = e0; e < e1 && live; ++e) {
@@ -168,10 +183,10 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
         if (u < P.nfull) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(dbd, kk * 2048), kIdesc,
+            ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(dbd, kk * 2048), idesc,
                            (u | kk) != 0);
         } else {
-          ptx::umma_bf16(d_tmem, da, dbd, kIdesc, u != 0);
+          ptx::umma_bf16(d_tmem, da, dbd, idesc, u != 0);
         }
         ptx::umma_commit(&c->empty[s]);
       }
@@ -198,6 +213,7 @@ __device__ __forceinline__ void add_bf16x8(const uint4& v, float* t) {
 // Norm mode, warps 4-11: per example, sum of P_e^2 over the tile (plus the squared
 // bias sums in the first column tile) -> part[tile, e].  Every epilogue warp passes
 // one barrier per example, also after an abort, so none waits for a warp that left.
+template <bool kTrim>
 __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem,
                                               int e0, int e1, bool do_bias) {
   volatile int* abort = &c->abort;
@@ -207,6 +223,7 @@ __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ct
   const int bbox = et >> 7, bq = (et >> 4) & 7, bj = et & 15;
   const int ns = P.nfull + P.n16;
   const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+  const int ncol = tile_n<kTrim>(P, blockIdx.y * BN) - half * 128;   // this warp's columns with products
   bool ok = true;
   int k = 0;
   for (int e = e0; e < e1; ++e) {
@@ -257,14 +274,16 @@ __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ct
       const uint32_t base = tmem + b * 256 + half * 128 + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
       for (int ch = 0; ch < 8; ch += 2) {
+        if (kTrim && ch * 16 >= ncol) break;       // (warp-uniform; widths are multiples of 16)
         float v0[16], v1[16];
         ptx::tmem_ld16(base + ch * 16, v0);
         ptx::tmem_ld16(base + ch * 16 + 16, v1);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          ss = fmaf(v0[j], v0[j], ss);
-          ss = fmaf(v1[j], v1[j], ss);
+        for (int j = 0; j < 16; ++j) ss = fmaf(v0[j], v0[j], ss);
+        if (!kTrim || (ch + 1) * 16 < ncol) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ss = fmaf(v1[j], v1[j], ss);
         }
         const int m = blockIdx.x * BM + quarter * 32 + lane;
         const int n = blockIdx.y * BN + half * 128 + ch * 16;   // d % 8 == 0: whole float4s
@@ -298,6 +317,7 @@ __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ct
 }
 
 // Warps 4-11: drain P_e from TMEM into fp32 register accumulators, D += c_e * P_e.
+template <bool kTrim>
 __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0,
                                          int e1, int m0, int n0, bool do_bias) {
   volatile int* abort = &c->abort;
@@ -309,6 +329,8 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
   const int et = threadIdx.x - 32 * kEpiFirst;   // 0..255
   const int bbox = et >> 7, bq = (et >> 4) & 7, bj = et & 15;
   const int ns = P.nfull + P.n16;
+  const int ncol = tile_n<kTrim>(P, n0) - half * 128;   // this warp's columns with products (past them:
+                                                  // stale TMEM, accumulated but never stored)
   float bacc[8], btmp[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) bacc[q] = btmp[q] = 0.f;
@@ -347,6 +369,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     const uint32_t base = tmem + b * 256 + half * 128 + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
     for (int ch = 0; ch < 8; ch += 4) {
+      if (kTrim && ch * 16 >= ncol) break;         // (warp-uniform)
       float v[4][16];                              // four loads in flight per wait
 #pragma unroll
       for (int u = 0; u < 4; ++u) ptx::tmem_ld16(base + (ch + u) * 16, v[u]);
@@ -518,7 +541,7 @@ __device__ __forceinline__ void finish(const Params& P, uint8_t* smem, Ctl* c, u
   }
 }
 
-template <bool kNorm>
+template <bool kNorm, bool kTrim>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant__ CUtensorMap mapA64,
                const __grid_constant__ CUtensorMap mapG16, const __grid_constant__ CUtensorMap mapA16,
@@ -566,16 +589,16 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
     pdl_wait();
     ptx::regs_inc<216>();
     if constexpr (kNorm)
-      epilogue_norm(P, smem, c, tmem, e0, e1, do_bias);
+      epilogue_norm<kTrim>(P, smem, c, tmem, e0, e1, do_bias);
     else
-      epilogue(P, smem, c, tmem, e0, e1, m0, n0, do_bias);
+      epilogue<kTrim>(P, smem, c, tmem, e0, e1, m0, n0, do_bias);
     finish(P, smem, c, tmem, m0, n0, do_bias);
   } else {
     ptx::regs_dec<64>();
     if (warp == 0 || warp == 2) {
-      producer(P, &mapG64, &mapA64, &mapG16, &mapA16, smem, c, e0, e1, m0, n0, warp >> 1);
+      producer<kTrim>(P, &mapG64, &mapA64, &mapG16, &mapA16, smem, c, e0, e1, m0, n0, warp >> 1);
     } else if (warp == 1) {
-      mma_issuer(P, smem, c, tmem, e0, e1);
+      mma_issuer<kTrim>(P, smem, c, tmem, e0, e1);
     } else {
       pdl_wait();
       finish_decision(c);        // warp 3 joins the workers' barrier
@@ -613,7 +636,7 @@ static int active_clusters(int size) {
     attr[0].val.clusterDim.z = size;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, tcsumx::tc_sumx_kernel<false>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, tcsumx::tc_sumx_kernel<false, false>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = 152 / size;   // planning fallback: the full SM count
     }
@@ -708,8 +731,11 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<false>,
+    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<false, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, tcsumx::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tcsumx::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -727,7 +753,9 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   attr[1].val.clusterDim.z = splits;
   cfg.attrs = attr;
   cfg.numAttrs = splits > 1 ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false>, mg64, ma64, mg16, ma16, P);
+  cudaError_t e = g.D % tcsumx::BN
+                      ? cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false, true>, mg64, ma64, mg16, ma16, P)
+                      : cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false, false>, mg64, ma64, mg16, ma16, P);
   count_launch();
   if (e != cudaSuccess || !gsplits) return e;
   const size_t nw = (size_t)g.p * g.D;
@@ -781,13 +809,20 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<true>,
+    cudaError_t e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<true, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, tcsumx::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tcsumx::tc_sumx_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               tcsumx::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   dim3 grid(tm, tn, (unsigned)chunks);
-  launch_pdl(tcsumx::tc_sumx_kernel<true>, grid, tcsumx::kThreads, tcsumx::SMEM, s, mg64, ma64, mg16, ma16, P);
+  if (g.D % tcsumx::BN)
+    launch_pdl(tcsumx::tc_sumx_kernel<true, true>, grid, tcsumx::kThreads, tcsumx::SMEM, s, mg64, ma64, mg16, ma16, P);
+  else
+    launch_pdl(tcsumx::tc_sumx_kernel<true, false>, grid, tcsumx::kThreads, tcsumx::SMEM, s, mg64, ma64, mg16, ma16,
+               P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_reduce_splits(ws, (int)tiles, (size_t)g.B, out, 0, s);
