@@ -178,6 +178,11 @@ WORKLOADS: Dict[str, Workload] = {
         per_layer=True, alpha=1.1, beta=2.0, sigma_l2=2.5, layers=_vgg11_cifar_layers(),
         description="VGG-11 CIFAR stack (8 conv + fc): B=1024, bf16, per-layer C=2, "
                     "sigma=0.7225, adaptive alpha=1.1 beta=2 sigma_l2=2.5"),
+    # The same stack clipped flat (one bound over all layers).
+    "vgg11_cifar_b1024_flat": Workload(
+        name="vgg11_cifar_b1024_flat", B=1024, dtype="bf16", C=2.0, sigma=0.7225, seed=0,
+        per_layer=False, layers=_vgg11_cifar_layers(),
+        description="VGG-11 CIFAR stack (8 conv + fc): B=1024, bf16, flat C=2, sigma=0.7225"),
     # ViT-Base MLP pair at large batch.
     "vit_mlp_b4096_t197": Workload(
         name="vit_mlp_b4096_t197", B=4096, dtype="bf16", C=1.0, sigma=1.0, seed=0,
