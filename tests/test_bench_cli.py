@@ -1,0 +1,49 @@
+"""bench.py as the driver runs it: one JSON line with the keys the measurement contract names.
+
+The reference arm (the float64 oracle on the host cores) runs here without a GPU; our arm
+runs on the GPU with a short step count.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+             "scaling", "vs_baseline", "dtype", "data", "config", "e2e"}
+
+
+def _run(args, timeout):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, capture_output=True,
+                         text=True, timeout=timeout)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line():
+    d = _run(["--impl", "reference", "--steps", "1", "--warmup", "3", "--workload", "t1_linear_b32"], 300)
+    assert BASE_KEYS <= set(d) and d["impl"] == "reference"
+    assert d["value"] > 0 and d["unit"] == "examples/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "t1_linear_b32" and d["warmup"] >= 3
+    assert d["e2e"] == {"value": d["value"], "unit": "examples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+
+
+@pytest.mark.gpu
+def test_bench_line_keys():
+    d = _run(["--steps", "3", "--warmup", "3", "--no-cpu-baseline"], 600)
+    assert BASE_KEYS <= set(d) and {"roofline", "clocks", "gpu_launches"} <= set(d)
+    assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] >= 3
+    assert d["config"]["workload"] == "seq_linear_b64_t128" and d["data"] == "synthetic"
+    r = d["roofline"]
+    assert r["bound"] in ("tensor", "hbm") and 0 < r["frac"] < 1.5 and r["peak"] > 0
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] == 2 * 64 * 128 * 768 * 2 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 3 * d["kernels_per_step"] > 0
+    assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}

@@ -29,16 +29,21 @@ def _host(x, i):
     return x[i].float().cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("name", ["vit_mlp_b4096_t197", "vgg11_cifar_b1024", "conv3x3_b256",
-                                  "seq_linear_b64_t128"])
-def test_full_size_norms_and_sparse_sums(lib, name):
+@pytest.mark.parametrize("name,cl", [("vit_mlp_b4096_t197", False), ("vgg11_cifar_b1024", False),
+                                     ("conv3x3_b256", False), ("seq_linear_b64_t128", False),
+                                     ("vgg11_cifar_b1024", True), ("conv3x3_b256", True)],
+                         ids=["vit", "vgg", "conv3x3", "seq", "vgg_channels_last", "conv3x3_channels_last"])
+def test_full_size_norms_and_sparse_sums(lib, name, cl):
     import torch
     dp = lib
     wl = workloads.get_workload(name)
     idx = _sample(wl.B)
     for l, spec in enumerate(wl.layers):
         A, G = workloads.device_layer_inputs(wl, l)
-        desc = desc_for(dp, spec, wl.B, wl.dtype)
+        lay = dp.DP_NHWC if (cl and spec.kind != "linear") else dp.DP_NCHW
+        desc = desc_for(dp, spec, wl.B, wl.dtype, layout=lay)
+        if lay == dp.DP_NHWC:       # the same values channels last; the oracle reads channels first
+            A, G = A.movedim(1, -1).contiguous(), G.movedim(1, -1).contiguous()
         ws = torch.empty(max(dp.dp_workspace_size(desc), 16), dtype=torch.uint8, device="cuda")
         sq = torch.empty(wl.B, device="cuda")
         dp.dp_layer_sqnorms(desc, A, G, sq, ws)
@@ -52,6 +57,8 @@ def test_full_size_norms_and_sparse_sums(lib, name):
         torch.cuda.synchronize()
         a_s = np.stack([_host(A, i) for i in idx])
         g_s = np.stack([_host(G, i) for i in idx])
+        if lay == dp.DP_NHWC:
+            a_s, g_s = np.moveaxis(a_s, -1, 1), np.moveaxis(g_s, -1, 1)
         ref_sq = oracle.layer_sqnorms(spec, a_s, g_s)
         assert rel_elem(sq.cpu().numpy()[idx], ref_sq) <= TOL[wl.dtype], (name, spec.name)
         S, Sb = oracle.clipped_sum(spec, a_s, g_s, fac[idx].astype(np.float64))
