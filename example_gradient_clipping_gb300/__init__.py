@@ -35,6 +35,11 @@ class NoiseDesc(ctypes.Structure):
                 ("seed", ctypes.c_uint64), ("seed_dev", ctypes.c_void_p), ("offset", ctypes.c_uint64)]
 
 
+class NoiseBlock(ctypes.Structure):
+    """dp_noise_block: one block of the flat gradient with its bound."""
+    _fields_ = [("offset", ctypes.c_uint64), ("n", ctypes.c_uint64), ("C", ctypes.c_float)]
+
+
 class LayerDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("kind", "dtype", "B", "T", "d", "p", "Cin", "H", "W", "k", "stride", "pad", "dil",
@@ -81,6 +86,8 @@ def _load():
                                           ctypes.POINTER(NoiseDesc), c_void, c_size, c_void]),
         "dp_clipped_sum_kept_noised": (c_int, [PD, c_void, c_void, c_void, c_void, c_int, ctypes.POINTER(NoiseDesc),
                                                c_void, c_size, c_void]),
+        "dp_add_noise_blocks": (c_int, [c_void, ctypes.POINTER(NoiseBlock), c_int, c_f, c_int, c_u64, c_void,
+                                        c_void]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -243,6 +250,13 @@ def dp_clipped_sum_kept_noised(desc: LayerDesc, grads, factors, dW, db, noise: N
     _check(_lib.dp_clipped_sum_kept_noised(ctypes.byref(desc), _ptr(grads), _ptr(factors), _ptr(dW), _ptr(db),
                                            int(bool(accumulate)), ctypes.byref(noise), _ptr(workspace),
                                            _ws_len(workspace) if ws_bytes is None else ws_bytes, _stream(stream)))
+
+
+def dp_add_noise_blocks(grad, blocks, sigma: float, B: int, seed: int = 0, seed_dev=None, stream=None) -> None:
+    """dp_add_noise over several (offset, n, C) blocks of the flat gradient `grad` in one launch."""
+    arr = (NoiseBlock * len(blocks))(*[NoiseBlock(int(o), int(n), float(c)) for o, n, c in blocks])
+    _check(_lib.dp_add_noise_blocks(_ptr(grad), arr, len(blocks), float(sigma), int(B), int(seed) & (2 ** 64 - 1),
+                                    _ptr(seed_dev), _stream(stream)))
 
 
 def dp_selftest_wait_timeout(waited_ns=None, stream=None) -> None:

@@ -736,6 +736,33 @@ dp_status dp_add_noise_devseed(float* grad, size_t n, float sigma, float C, int 
   return add_noise_impl(grad, n, sigma, C, B, 0, seed_dev, offset, stream);
 }
 
+dp_status dp_add_noise_blocks(float* grad, const dp_noise_block* blocks, int nblocks, float sigma, int B,
+                              uint64_t seed, const unsigned long long* seed_dev, cudaStream_t stream) {
+  if (!grad || !blocks) return fail(DP_ERR_INVALID_ARG, "grad and blocks must be non-NULL");
+  if (nblocks < 1 || nblocks > dpk::kMaxNoiseBlocks)
+    return fail(DP_ERR_INVALID_ARG, "nblocks=%d must be in 1..%d", nblocks, dpk::kMaxNoiseBlocks);
+  if (B <= 0) return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0", B);
+  if (!(sigma >= 0.f) || !std::isfinite(sigma)) return fail(DP_ERR_INVALID_ARG, "sigma=%g must be finite and >= 0", (double)sigma);
+  dpk::NoiseBlocks nb{};
+  nb.count = nblocks;
+  uint64_t end = 0;
+  for (int b = 0; b < nblocks; ++b) {
+    const dp_noise_block& k = blocks[b];
+    if (!(k.C >= 0.f) || !std::isfinite(k.C)) return fail(DP_ERR_INVALID_ARG, "block %d: C=%g", b, (double)k.C);
+    if (k.offset + k.n < k.offset) return fail(DP_ERR_INVALID_ARG, "block %d: offset + n overflows", b);
+    if (b && k.offset < end) return fail(DP_ERR_INVALID_ARG, "block %d overlaps or precedes block %d", b, b - 1);
+    end = k.offset + k.n;
+    nb.off[b] = k.offset;
+    nb.n[b] = k.n;
+    nb.sc[b] = (float)((double)sigma * (double)k.C);
+    nb.qcum[b + 1] = nb.qcum[b] + (k.n ? ((k.offset + k.n + 3) >> 2) - (k.offset >> 2) : 0);
+  }
+  const float invB = (float)(1.0 / (double)B);
+  cudaError_t e = dph::launch_add_noise_blocks(grad, nb, invB, seed, seed_dev, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_add_noise_blocks launch");
+  return ok();
+}
+
 dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha, float beta,
                             float sigma_l2, uint64_t seed, int layer, float* out,
                             cudaStream_t stream) {

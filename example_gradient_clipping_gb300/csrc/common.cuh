@@ -142,6 +142,16 @@ struct NoiseArgs {
   int applied_a, applied_b;             // host: set by the launcher that fused it (dW, db)
 };
 
+// Up to 64 blocks of a flat gradient with their noise scales (sigma * C_b), in increasing
+// offset order, not overlapping; qcum[b] = Philox blocks touched by blocks 0 .. b-1.
+constexpr int kMaxNoiseBlocks = 64;
+struct NoiseBlocks {
+  int count;
+  uint64_t off[kMaxNoiseBlocks], n[kMaxNoiseBlocks];
+  float sc[kMaxNoiseBlocks];
+  uint64_t qcum[kMaxNoiseBlocks + 1];
+};
+
 // z_e for the four consecutive flat indices e0 .. e0+3 (one or two Philox blocks).
 __device__ __forceinline__ void noise_z4(uint64_t e0, uint64_t seed, float z[4]) {
   const int m = (int)(e0 & 3);
@@ -220,6 +230,8 @@ cudaError_t launch_clip_factors(const float* sq, int B, int L, int per_layer, co
                                 float* out, unsigned* status, cudaStream_t s);
 cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64_t seed,
                              uint64_t offset, const unsigned long long* seed_dev, cudaStream_t s);
+cudaError_t launch_add_noise_blocks(float* grad, const dpk::NoiseBlocks& nb, float invB, uint64_t seed,
+                                    const unsigned long long* seed_dev, cudaStream_t s);
 cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
                                   float sigma_l2, uint64_t seed, int layer, float* out,
                                   cudaStream_t s);

@@ -3,8 +3,9 @@
 Per step: dp_layer_sqnorms for every layer (ghost norm, instantiation or the
 one-row form, layer by layer), dp_clip_factors (flat or per-layer), then for every
 layer the clipped sum into one flat fp32 gradient vector [W_0, b_0, W_1, b_1, ...]
-with the layer's noise and 1/B added by the same call (dp_clipped_sum_noised, each
-layer's noise drawn at its flat offset, with its own bound when clipping per layer).
+with the noise and 1/B added by the same call for linear layers (dp_clipped_sum_noised)
+and by one multi-block pass after the sums for conv layers (dp_add_noise_blocks); each
+layer's noise is drawn at its flat offset, with its own bound when clipping per layer.
 fuse_noise=False runs dp_clipped_sum per layer and dp_add_noise over the vector
 instead; the result is bit-identical.  Torch supplies device memory and the stream only.
 """
@@ -12,7 +13,8 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence, Tuple
 
-from . import (DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_add_noise, dp_add_noise_devseed, dp_clip_factors,
+from . import (DP_LINEAR, DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_add_noise, dp_add_noise_blocks,
+               dp_add_noise_devseed, dp_clip_factors,
                dp_clipped_sum, dp_clipped_sum_kept, dp_clipped_sum_kept_noised, dp_clipped_sum_noised,
                dp_clipped_sum_reuse, dp_grads_size, dp_launch_count, dp_layer_sqnorms, dp_layer_sqnorms_keep,
                dp_layout_reused, dp_plan, dp_workspace_size, noise_desc)
@@ -106,20 +108,33 @@ class ClipStep:
                 dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
 
     def sums_noised(self, inputs, seed: int = 0, seed_dev=None, stream=None) -> None:
-        """sums() and noise() together: every layer's clipped sum call also adds its blocks'
-        noise and the 1/B scale (in the sum's final reduction where it has one)."""
+        """sums() and noise() together.  Linear layers' clipped sum calls add their blocks'
+        noise and the 1/B scale in the sum's final reduction (dp_clipped_sum_noised); the
+        conv layers' weight sums end in a column-mapping pass that does not draw noise, so
+        their blocks get theirs from one multi-block noise launch after the sums
+        (dp_add_noise_blocks) instead of one noise pass per layer."""
+        blocks = []
         for l, (d, (A, G)) in enumerate(zip(self.descs, inputs)):
             dW, db = self.layer_views(l)
             fac = self.factors[l] if self.per_layer else self.factors[0]
-            nd = noise_desc(self.sigma, self.C[l] if self.per_layer else self.C[0], self.B, seed, seed_dev,
-                            self.offsets[l])
+            C = self.C[l] if self.per_layer else self.C[0]
+            if d.kind != DP_LINEAR:
+                p, D = self.shapes[l]
+                blocks.append((self.offsets[l], p * D + (p if d.has_bias else 0), C))
+                if self.kept[l] is not None:
+                    dp_clipped_sum_kept(d, self.kept[l], fac, dW, db, self.workspace, stream=stream)
+                elif self.own_ws[l] is not None:
+                    dp_clipped_sum_reuse(d, self.modes[l], A, G, fac, dW, db, self.own_ws[l], stream=stream)
+                else:
+                    dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
+                continue
+            nd = noise_desc(self.sigma, C, self.B, seed, seed_dev, self.offsets[l])
             if self.kept[l] is not None:
                 dp_clipped_sum_kept_noised(d, self.kept[l], fac, dW, db, nd, self.workspace, stream=stream)
-            elif self.own_ws[l] is not None:
-                dp_clipped_sum_noised(d, A, G, fac, dW, db, nd, self.own_ws[l], norm_mode=self.modes[l],
-                                      stream=stream)
             else:
                 dp_clipped_sum_noised(d, A, G, fac, dW, db, nd, self.workspace, stream=stream)
+        if blocks:
+            dp_add_noise_blocks(self.grad, blocks, self.sigma, self.B, seed=seed, seed_dev=seed_dev, stream=stream)
 
     def noise(self, seed: int, stream=None) -> None:
         if not self.per_layer:

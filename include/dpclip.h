@@ -185,6 +185,22 @@ dp_status dp_add_noise_devseed(float* grad, size_t n, float sigma, float C, int 
                                const unsigned long long* seed_dev, uint64_t offset,
                                cudaStream_t stream);
 
+/* The noise pass of dp_add_noise over several blocks of one flat gradient in one launch,
+ * each block with its own bound (per-layer clipping, [ThreeTools] section 2):
+ *   grad[o_b + j] = (grad[o_b + j] + sigma * C_b * z_{o_b + j}) / B,   j < n_b,
+ * with z as dp_add_noise defines it and o_b the block's flat index (grad points to the flat
+ * vector's element 0).  Bit-identical to one dp_add_noise call per block.  blocks: host
+ * array of 1..64 blocks in increasing offset order, not overlapping (DP_ERR_INVALID_ARG
+ * otherwise, or for B <= 0 or a negative or non-finite sigma or C_b).  seed_dev non-NULL: the
+ * seed is read from device memory when the kernel runs, seed is then ignored. */
+typedef struct {
+  uint64_t offset;   /* flat index of the block's first element */
+  uint64_t n;        /* elements */
+  float C;           /* the block's bound */
+} dp_noise_block;
+dp_status dp_add_noise_blocks(float* grad, const dp_noise_block* blocks, int nblocks, float sigma, int B,
+                              uint64_t seed, const unsigned long long* seed_dev, cudaStream_t stream);
+
 /* Adaptive clipping bound of one layer ([ThreeTools] section 3):
  *   C_next = alpha/B * (sum_i min(sqrt(sqnorms[i]), C_l2) + sigma_l2 * C_l2 * z),
  *   C_l2_next = beta * C_next,

@@ -162,6 +162,18 @@ def test_invalid_noise_of_fused_sums_launches_nothing(dp):
     assert st == dp.DP_ERR_INVALID_ARG and b"noise" in dp._lib.dp_last_error()
 
 
+def test_invalid_noise_blocks_launch_nothing(dp):
+    for blocks in ([], [(0, 10, 1.0)] * 65, [(0, 10, 1.0), (5, 10, 1.0)], [(0, 10, -1.0)],
+                   [(0, 10, float("nan"))], [(2 ** 64 - 4, 8, 1.0)]):
+        with pytest.raises(dp.DPError) as e:
+            dp.dp_add_noise_blocks(16, blocks, 1.0, 4, stream=0)
+        assert e.value.status == dp.DP_ERR_INVALID_ARG
+    with pytest.raises(dp.DPError):
+        dp.dp_add_noise_blocks(16, [(0, 10, 1.0)], 1.0, 0, stream=0)
+    with pytest.raises(dp.DPError):
+        dp.dp_add_noise_blocks(16, [(0, 10, 1.0)], -1.0, 4, stream=0)
+
+
 def test_package_refuses_to_import_without_library(tmp_path):
     """The binding fails loudly when the compiled library is absent (no fallback)."""
     import shutil

@@ -142,3 +142,27 @@ def test_clip_step_fused_matches_unfused_and_oracle(lib, per_layer):
     assert torch.equal(got[0], got[1])
     ref = oracle.dp_step(wl, inputs, seed=99, C=C)
     assert rel_vec(got[1].numpy(), ref["noisy"]) <= TOL["bf16"]
+
+
+def test_noise_blocks_equal_one_pass_per_block(lib):
+    """dp_add_noise_blocks over blocks with their own bounds (misaligned offsets, neighbours
+    sharing a Philox block, an empty block, a gap) equals one dp_add_noise per block, bit for
+    bit; with the device-side seed too."""
+    import torch
+    dp = lib
+    n = 5000
+    blocks = [(0, 1001, 0.5), (1001, 3, 2.0), (1004, 0, 1.0), (1004, 998, 1.0), (2100, 2900, 0.25)]
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    base = torch.randn(n, generator=gen, device="cuda")
+    for use_dev in (False, True):
+        a, b = base.clone(), base.clone()
+        seed = 0xDEADBEEF12
+        for o, m, C in blocks:
+            if m:
+                dp.dp_add_noise(a[o:o + m], 0.8, C, 7, seed, o)
+        sd = torch.tensor([seed], dtype=torch.int64, device="cuda") if use_dev else None
+        dp.dp_add_noise_blocks(b, blocks, 0.8, 7, seed=0 if use_dev else seed, seed_dev=sd)
+        torch.cuda.synchronize()
+        assert torch.equal(a.cpu(), b.cpu())
+        assert torch.equal(b[2002:2100].cpu(), base[2002:2100].cpu())     # the gap is untouched
+
