@@ -119,20 +119,24 @@ def test_fused_devseed_and_kept(lib):
 
 @pytest.mark.parametrize("per_layer", [False, True])
 def test_clip_step_fused_matches_unfused_and_oracle(lib, per_layer):
-    """A two-layer step: fused and unfused ClipStep agree bit for bit, eagerly and as a
+    """A three-layer step: fused and unfused ClipStep agree bit for bit, eagerly and as a
     captured graph; both match the oracle's step."""
     import torch
     dp = lib
-    specs = (LayerSpec("a", "linear", p=136, d=200, T=100), LayerSpec("b", "conv2d", p=64, Cin=16, H=10, W=10, k=3,
-                                                                        pad=1))
-    wl = Workload(name="two", B=12, layers=specs, dtype="bf16", C=1.0, sigma=0.6, seed=21, per_layer=per_layer)
-    inputs = [workloads.layer_inputs(wl, l) for l in range(2)]
+    # a linear layer (noise fused into its sum), a conv layer on the row layout and a conv layer
+    # that keeps its per-example gradients (T = 576): the conv layers' noise is one launch
+    specs = (LayerSpec("a", "linear", p=136, d=200, T=100),
+             LayerSpec("b", "conv2d", p=64, Cin=16, H=10, W=10, k=3, pad=1),
+             LayerSpec("c", "conv2d", p=64, Cin=64, H=24, W=24, k=3, pad=1))
+    wl = Workload(name="three", B=12, layers=specs, dtype="bf16", C=1.0, sigma=0.6, seed=21, per_layer=per_layer)
+    inputs = [workloads.layer_inputs(wl, l) for l in range(3)]
     dev = [(to_dev(A, "bf16"), to_dev(G, "bf16")) for A, G in inputs]
     descs = [desc_for(dp, s, wl.B, "bf16") for s in specs]
-    C = [0.5, 0.8] if per_layer else 1.0
+    C = [0.5, 0.8, 0.3] if per_layer else 1.0
     got = []
     for fuse in (False, True):
         st = dp.ClipStep(descs, C=C, sigma=wl.sigma, per_layer=per_layer, fuse_noise=fuse)
+        assert [k is not None for k in st.kept] == [False, False, True]
         eager = st.run(dev, seed=99).clone()
         st.capture(dev)
         replayed = st.replay(99).clone()
