@@ -742,7 +742,8 @@ dp_status dp_add_noise_blocks(float* grad, const dp_noise_block* blocks, int nbl
   if (nblocks < 1 || nblocks > dpk::kMaxNoiseBlocks)
     return fail(DP_ERR_INVALID_ARG, "nblocks=%d must be in 1..%d", nblocks, dpk::kMaxNoiseBlocks);
   if (B <= 0) return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0", B);
-  if (!(sigma >= 0.f) || !std::isfinite(sigma)) return fail(DP_ERR_INVALID_ARG, "sigma=%g must be finite and >= 0", (double)sigma);
+  if (!(sigma >= 0.f) || !std::isfinite(sigma))
+    return fail(DP_ERR_INVALID_ARG, "sigma=%g must be finite and >= 0", (double)sigma);
   dpk::NoiseBlocks nb{};
   nb.count = nblocks;
   uint64_t end = 0;

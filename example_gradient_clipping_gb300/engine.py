@@ -20,7 +20,8 @@ Layers: nn.Linear (inputs [B, ..., d]; the middle dimensions are the rows T), nn
 nn.Conv2d and nn.Conv3d (square or cubic kernels, equal stride / padding / dilation in every
 dimension), the conv layers with groups 1 and zero padding.  Conv2d/Conv3d layers whose input
 arrives in PyTorch's channels_last memory format are handed over channels last (no layout
-copy); their output gradients are brought to the same format.  Every trainable parameter of the model must belong to such a layer.
+copy); their output gradients are brought to the same format.  Every trainable parameter of
+the model must belong to such a layer.
 Activations right after them must not be in-place (the backward hook reads the layer's
 output gradient).  PyTorch warns that the hook fires on output gradients when the model
 input needs no gradient; that gradient is the one wanted here.
