@@ -20,6 +20,7 @@ clip rule); see tests/test_oracle_pins.py.
 """
 from .dpsgd import (  # noqa: F401
     unfold2d, unfold1d, unfold3d, per_example_grad, layer_sqnorms, clip_factors, clipped_sum,
+    clipped_sum_elements,
     add_noise, adaptive_bound, norm_mode_plan, norm_mode_plan_time, dp_step, NONFINITE,
 )
 from .philox import philox4, normal_noise, noise_words, uniform_from_word  # noqa: F401

@@ -199,6 +199,42 @@ def clipped_sum(spec, A: np.ndarray, G: np.ndarray, factors: np.ndarray):
     return S, (Sb if spec.has_bias else None)
 
 
+def clipped_sum_elements(spec, A: np.ndarray, G: np.ndarray, factors: np.ndarray, rows, cols):
+    """Selected entries of the clipped sum: S[j, m] for j in rows, m in cols, and Sb[j].
+
+    The quantity of clipped_sum (sum_i c_i g_i: [FastClip] section 2, [MixGhost] eq. 2.1
+    and Appendix C.5) written entry by entry from the per-example gradient's definition
+    g_i[j, m] = sum_t G_i[t, j] U(A_i)[t, m] and b_i[j] = sum_t G_i[t, j] ([MixGhost]
+    eq. 2.4 for linear layers, eq. 2.6 for convolutions), so that a few entries of a large
+    layer cost O(B T) each.  Column m of a convolution's unfold, m = c*k^n + (tap), reads
+    input channel c alone (Appendix B), so each example is unfolded over just the channels
+    the requested columns read.  Examples with factor 0 are skipped, as in clipped_sum.
+    Returns (S_sel [len(rows), len(cols)], Sb_sel [len(rows)] or None without a bias).
+    """
+    rows = np.asarray(rows, dtype=np.int64).ravel()
+    cols = np.asarray(cols, dtype=np.int64).ravel()
+    S = np.zeros((rows.size, cols.size))
+    Sb = np.zeros(rows.size)
+    if spec.kind != "linear":
+        taps = spec.k ** {"conv1d": 1, "conv2d": 2, "conv3d": 3}[spec.kind]
+        chans = np.unique(cols // taps)                       # input channels the columns read
+        sub_col = np.searchsorted(chans, cols // taps) * taps + cols % taps
+        unfold = {"conv1d": unfold1d, "conv2d": unfold2d, "conv3d": unfold3d}[spec.kind]
+    for i in range(A.shape[0]):
+        c = float(factors[i])
+        if c == 0.0:
+            continue
+        if spec.kind == "linear":
+            U = np.asarray(np.asarray(A[i]).reshape(spec.T, spec.d)[:, cols], dtype=np.float64)
+            Gt = np.asarray(np.asarray(G[i]).reshape(spec.T, spec.p)[:, rows], dtype=np.float64)
+        else:
+            U = unfold(np.asarray(A[i])[chans], spec.k, spec.stride, spec.pad, spec.dil)[:, sub_col]
+            Gt = np.asarray(np.asarray(G[i]).reshape(spec.p, -1)[rows], dtype=np.float64).T
+        S += c * (Gt.T @ U)
+        Sb += c * Gt.sum(axis=0)
+    return S, (Sb if spec.has_bias else None)
+
+
 def add_noise(x: np.ndarray, sigma: float, C: float, B: int, seed: int, offset: int = 0,
               stream: int = 0) -> np.ndarray:
     """(x + sigma*C*z) / B with z the seeded standard normals of elements offset.. .

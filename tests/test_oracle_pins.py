@@ -312,6 +312,48 @@ def test_clipped_sum_linear_in_factors_and_additive_over_batch():
     np.testing.assert_allclose(S, 0.3 * tw, rtol=1e-12, atol=1e-14)
 
 
+@pytest.mark.parametrize("spec", [
+    _lin(7, 19, 11), _lin(1, 9, 6, bias=False),
+    _conv(5, 9, 7, 6, 3, 2, 1, 1), _conv(3, 8, 8, 4, 3, 1, 2, 2, bias=False),
+    LayerSpec(name="c1", kind="conv1d", p=5, Cin=4, W=17, k=3, stride=2, pad=1),
+    LayerSpec(name="c3", kind="conv3d", p=3, Cin=3, Z=5, H=4, W=6, k=2, stride=1, pad=1, dil=2)],
+    ids=["linear", "linear_t1_nobias", "conv2d_s2", "conv2d_dil_nobias", "conv1d", "conv3d"])
+def test_clipped_sum_elements_match_the_full_sum(spec):
+    """Entry-wise clipped sum = the selected entries of the materialised sum, for every
+    entry and for scattered, repeated and unordered index lists."""
+    rng = np.random.default_rng(31)
+    B = 4
+    A = _rand(rng, B, *spec.a_example_shape())
+    G = _rand(rng, B, *spec.g_example_shape())
+    c = rng.random(B)
+    c[1] = 0.0
+    S, Sb = dpsgd.clipped_sum(spec, A, G, c)
+    Se, Sbe = dpsgd.clipped_sum_elements(spec, A, G, c, np.arange(spec.p), np.arange(spec.D))
+    np.testing.assert_allclose(Se, S, rtol=1e-12, atol=1e-12)
+    if spec.has_bias:
+        np.testing.assert_allclose(Sbe, Sb, rtol=1e-12, atol=1e-12)
+    else:
+        assert Sbe is None
+    rows = [spec.p - 1, 0, spec.p // 2, spec.p - 1]
+    cols = [spec.D - 1, 3, 0, spec.D // 2, 3]
+    Se, Sbe = dpsgd.clipped_sum_elements(spec, A, G, c, rows, cols)
+    np.testing.assert_allclose(Se, S[np.ix_(rows, cols)], rtol=1e-12, atol=1e-12)
+    if spec.has_bias:
+        np.testing.assert_allclose(Sbe, Sb[rows], rtol=1e-12, atol=1e-12)
+
+
+def test_clipped_sum_elements_linear_entry_by_brute_force():
+    """One entry of a linear layer's clipped sum by plain loops over examples and rows."""
+    rng = np.random.default_rng(32)
+    spec = _lin(5, 4, 3)
+    A, G, c = _rand(rng, 3, 5, 4), _rand(rng, 3, 5, 3), rng.random(3)
+    j, m = 2, 1
+    want = sum(c[i] * sum(G[i, t, j] * A[i, t, m] for t in range(5)) for i in range(3))
+    Se, Sbe = dpsgd.clipped_sum_elements(spec, A, G, c, [j], [m])
+    assert Se[0, 0] == pytest.approx(want, rel=1e-13)
+    assert Sbe[0] == pytest.approx(sum(c[i] * G[i, :, j].sum() for i in range(3)), rel=1e-13)
+
+
 # ---------------------------------------------------------------- noise
 
 def test_philox4x64_matches_numpy():
