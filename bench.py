@@ -25,7 +25,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "examples/sec through norm+clip+noisy-sum per config; % of TC/HBM roofline"
-DEFAULT_WORKLOAD = "seq_linear_b64_t128"
+DEFAULT_WORKLOAD = "vit_mlp_b4096_t197"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -146,29 +146,32 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# Kernel that serves each call on the bench workload's tensor-core path.
-_DOMINANT_KERNELS = {"sums": ["tc_sum2_kernel", "tc_sumx_kernel", "tc_sum_kernel"], "norms": ["tc_ghost_kernel"],
+# Kernels that serve each call on the tensor-core paths (for the DRAM traffic record).
+_DOMINANT_KERNELS = {"sums": ["tc_sumx_kernel", "tc_sum_kernel", "tc_conv_kernel", "kept_wsum_kernel"],
+                     "norms": ["tc_ghost_kernel", "tc_conv_kernel", "tc_sumx_kernel"],
                      "noise": ["add_noise_kernel"], "factors": ["clip_factors_kernel"]}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def _profiled_traffic(workload, kernels):
-    """DRAM bytes per launch from the committed ncu summary (profiles/dram_traffic_*.md),
-    or None when no capture exists or the kernel's source has changed since."""
-    import glob
+    """DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture,
+    recorded in profiles/dram_traffic.json with the hash of the kernel's source file at
+    capture time; None when there is no record or the source has changed since."""
     import hashlib
-    import re
-    for path in glob.glob(os.path.join(ROOT, "profiles", "dram_traffic_*.md")):
-        for line in open(path):
-            m = re.match(r"traffic: workload=(\S+) kernel=(\S+) dram_bytes_per_launch=(\d+) "
-                         r"source=(\S+) source_sha256_16=(\w+)", line.strip())
-            if not m or m.group(1) != workload or m.group(2) not in kernels:
-                continue
-            src = os.path.join(ROOT, "example_gradient_clipping_gb300", "csrc", m.group(4))
-            try:
-                cur = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-            except OSError:
-                return None
-            return int(m.group(3)) if cur == m.group(5) else None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            recs = json.load(f)["records"]
+    except (OSError, ValueError, KeyError):
+        return None
+    for r in recs:
+        if r.get("workload") != workload or r.get("kernel") not in kernels:
+            continue
+        src = os.path.join(ROOT, "example_gradient_clipping_gb300", "csrc", r["source"])
+        try:
+            cur = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        except OSError:
+            return None
+        return int(r["dram_bytes_per_launch"]) if cur == r["source_sha256_16"] else None
     return None
 
 
@@ -285,9 +288,140 @@ def max_over_ranks(v: float, device) -> float:
     return float(t.item())
 
 
+# The smaller workloads of the metric, each timed on the device after the headline one
+# (step time, examples/s and the dominant call's roofline fraction): the one-row layer,
+# the sequence layer, the 3x3 conv layer, and the VGG-11 stack clipped per layer (with
+# the adaptive bound) and flat.
+PER_CONFIG = ("t1_linear_b32", "seq_linear_b64_t128", "conv3x3_b256", "vgg11_cifar_b1024",
+              "vgg11_cifar_b1024_flat")
+# FP32 FFMA peak for the fp32 one-row layer's FFMA kernels: 152 SMs x 128 FP32 lanes x
+# 2 flop x 2.07 GHz.
+FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def roofline(wl, work, means, pk, peak_kind="burst"):
+    """Roofline object of the step's dominant call (largest per-call mean)."""
+    dom = max(("norms", "factors", "sums", "noise"), key=means.get)   # sums_noised: the step's fused form
+    tc_peak = pk["bf16"] if peak_kind == "burst" else pk["bf16_sus"]
+    sum_bytes = work["kept_bytes"] + 4 * work["n_params"]     # kept gradients read, sums written
+    if dom in ("sums", "norms") and wl.dtype == "fp32":
+        flop = work["flop_sum"] if dom == "sums" else work["flop_norm"]
+        roof = dict(bound="alu", achieved=flop / (means[dom] * 1e-3) / 1e12, peak=FP32_FFMA_TFLOPS,
+                    unit="TFLOP/s")
+    elif dom == "sums" and sum_bytes / (pk["hbm"] * 1e9) > work["flop_sum"] / (tc_peak * 1e12):
+        # mostly kept per-example gradients: a read-bound weighted sum
+        roof = dict(bound="hbm", achieved=sum_bytes / (means["sums"] * 1e-3) / 1e9, peak=pk["hbm"], unit="GB/s")
+    elif dom == "sums":
+        roof = dict(bound="tensor", achieved=work["flop_sum"] / (means["sums"] * 1e-3) / 1e12,
+                    peak=tc_peak, unit="TFLOP/s")
+    elif dom == "norms":
+        roof = dict(bound="tensor", achieved=work["flop_norm"] / (means["norms"] * 1e-3) / 1e12,
+                    peak=tc_peak, unit="TFLOP/s")
+    else:
+        nb = 8 * work["n_params"]
+        roof = dict(bound="hbm", achieved=nb / (means[dom] * 1e-3) / 1e9, peak=pk["hbm"], unit="GB/s")
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = _profiled_traffic(wl.name, _DOMINANT_KERNELS[dom])
+    roof["kernel"] = {"sums": "dp_clipped_sum", "norms": "dp_layer_sqnorms", "noise": "dp_add_noise",
+                      "factors": "dp_clip_factors"}[dom]
+    roof["peak_source"] = (f"{pk['src']} ({peak_kind})" if roof["bound"] == "tensor" else
+                           pk["src"] if roof["bound"] == "hbm" else "derived: 152 SMs x 128 lanes x 2 x 2.07 GHz")
+    return roof
+
+
+class StepBench:
+    """One workload's step on the device: inputs, the captured step graph, per-call graphs."""
+
+    REPS = 20
+
+    def __init__(self, dp, wl, dev, channels_last=False, host_inputs=False):
+        import torch
+        import workloads
+        self.wl, self.dev = wl, dev
+        cl = [bool(channels_last) and s.kind != "linear" for s in wl.layers]
+        self.cl = cl
+        self.descs = [layer_desc(dp, s, wl.B, wl.dtype, layout=int(c)) for s, c in zip(wl.layers, cl)]
+
+        def to_layout(pair, c):
+            return tuple(x.movedim(1, -1).contiguous() for x in pair) if c else pair
+
+        n_elem = wl.B * sum(math.prod(s.a_example_shape()) + math.prod(s.g_example_shape()) for s in wl.layers)
+        self.host_in = None
+        if host_inputs and n_elem <= HOST_GEN_LIMIT:
+            self.host_in = [workloads.layer_inputs(wl, l, threads=8) for l in range(len(wl.layers))]
+            self.dev_in = [to_layout((workloads.to_torch(A, wl.dtype, str(dev)),
+                                      workloads.to_torch(G, wl.dtype, str(dev))), c)
+                           for (A, G), c in zip(self.host_in, cl)]
+        else:
+            # full-size inputs drawn on the device (host generation would take minutes)
+            self.dev_in = [to_layout(workloads.device_layer_inputs(wl, l, str(dev)), c) for l, c in enumerate(cl)]
+        adaptive = None
+        if wl.per_layer and wl.alpha is not None:
+            # C_l2 of the first step: the mean unclipped per-layer norm of a batch of random
+            # noise ([ThreeTools] section 3), which the synthetic batch is
+            probe = dp.ClipStep(self.descs, C=wl.C, sigma=wl.sigma, per_layer=True, device=str(dev))
+            probe.norms(self.dev_in)
+            c_l2 = probe.sqnorms.double().sqrt().mean(dim=1).tolist()
+            del probe
+            adaptive = dict(alpha=wl.alpha, beta=wl.beta, sigma_l2=wl.sigma_l2, C_l2=c_l2)
+        self.step = dp.ClipStep(self.descs, C=wl.C, sigma=wl.sigma, per_layer=wl.per_layer, device=str(dev),
+                                adaptive=adaptive)
+        step = self.step
+        self.modes = [dp.MODE_NAMES[m] for m, _, _ in step.plan]
+        self.kept = [k is not None for k in step.kept]
+        self.work = step_work(wl, self.modes, self.kept)
+        # The whole step is one CUDA graph (norms -> [adaptive bound] -> factors -> clipped
+        # sums -> noise), replayed once per step; every kernel in it is a library kernel.
+        step.capture(self.dev_in)
+        # per-call graphs for the per-kernel roofline: each holds REPS calls, so graph launch
+        # latency is amortised (the first call finds a flushed L2; in the step the clipped sum
+        # likewise runs right after the norm pass read the inputs).  Each call is followed by
+        # a one-element PyTorch kernel, which takes no part in programmatic launch, so no call
+        # overlaps the next; a graph of REPS such separators is timed too and subtracted.
+        self.sep_buf = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.call_graphs = {}
+        dev_in = self.dev_in
+        for name, fn in (("norms", lambda: step.norms(dev_in)), ("factors", lambda: step.factors_()),
+                         ("sums", lambda: step.sums(dev_in)), ("noise", lambda: step.noise_devseed()),
+                         ("sums_noised", lambda: step.sums_and_noise_devseed(dev_in)), ("_sep", None)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(self.REPS):
+                    if fn is not None:
+                        fn()
+                    self.sep_buf.add_(1.0)
+            self.call_graphs[name] = g
+
+    def timed(self, replay, k_steps, seed_base, flush, stream):
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(k_steps)]
+        for k in range(k_steps):
+            flush.zero_()                              # L2 flush, outside the events
+            self.step.seed_buf.fill_(seed_base + k)    # fresh noise seed, outside the events
+            evs[k][0].record(stream)
+            replay()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def per_call_means(self, n_rep, seed0, flush, stream):
+        sep_ms = statistics.mean(self.timed(self.call_graphs["_sep"].replay, n_rep, seed0, flush, stream))
+        per_call = {n: [max(t - sep_ms, 0.0) / self.REPS for t in self.timed(g.replay, n_rep, seed0, flush, stream)]
+                    for n, g in self.call_graphs.items() if n != "_sep"}
+        return {n: statistics.mean(v) for n, v in per_call.items()}
+
+    def free(self):
+        import torch
+        self.call_graphs = {}
+        self.step = None
+        self.dev_in = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
 def run_ours(args, wl):
     import torch
-    import workloads
     import example_gradient_clipping_gb300 as dp
     world, rank, local = _dist_env()
     if world > 1:
@@ -297,104 +431,59 @@ def run_ours(args, wl):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-
-    # --channels-last: conv layers' A and G handed over channels last (same values)
-    cl = [bool(args.channels_last) and s.kind != "linear" for s in wl.layers]
-    descs = [layer_desc(dp, s, wl.B, wl.dtype, layout=int(c)) for s, c in zip(wl.layers, cl)]
-
-    def to_layout(pair, c):
-        return tuple(x.movedim(1, -1).contiguous() for x in pair) if c else pair
-
-    step = dp.ClipStep(descs, C=wl.C, sigma=wl.sigma, per_layer=wl.per_layer, device=str(dev))
-    n_elem = wl.B * sum(math.prod(s.a_example_shape()) + math.prod(s.g_example_shape()) for s in wl.layers)
-    if n_elem <= HOST_GEN_LIMIT:
-        host_in = [workloads.layer_inputs(wl, l, threads=8) for l in range(len(wl.layers))]
-        dev_in = [to_layout((workloads.to_torch(A, wl.dtype, str(dev)), workloads.to_torch(G, wl.dtype, str(dev))), c)
-                  for (A, G), c in zip(host_in, cl)]
-        pinned = [tuple(x.pin_memory() for x in to_layout((workloads.to_torch(A, wl.dtype),
-                                                             workloads.to_torch(G, wl.dtype)), c))
-                  for (A, G), c in zip(host_in, cl)]
-
-        def sample_inputs(b):
-            return [(A[:b], G[:b]) for A, G in host_in]
-    else:
-        # full-size inputs drawn on the device (host generation would take minutes)
-        dev_in = [to_layout(workloads.device_layer_inputs(wl, l, str(dev)), c) for l, c in enumerate(cl)]
-        pinned = [(a.cpu().pin_memory(), g.cpu().pin_memory()) for a, g in dev_in]
-
-        def sample_inputs(b):     # channels first for the oracle
-            return [tuple((x[:b].movedim(-1, 1) if c else x[:b]).float().numpy() for x in pair)
-                    for pair, c in zip(pinned, cl)]
-    modes = [dp.MODE_NAMES[m] for m, _, _ in step.plan]
-    kept = [k is not None for k in step.kept]
-    work = step_work(wl, modes, kept)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    pk = _peaks()
 
-    # The whole step is one CUDA graph (norms -> factors -> clipped sums -> noise),
-    # replayed once per step; every kernel in it is a library kernel.
-    step.capture(dev_in)
-    # per-call graphs for the per-kernel roofline: each holds REPS calls, so graph launch
-    # latency is amortised (the first call finds a flushed L2; in the step the clipped sum
-    # likewise runs right after the norm pass read the inputs).  Each call is followed by
-    # a one-element PyTorch kernel, which takes no part in programmatic launch, so no call
-    # overlaps the next; a graph of REPS such separators is timed too and subtracted.
-    REPS = 20
-    sep_buf = torch.zeros(1, dtype=torch.float32, device=dev)
-    call_graphs = {}
-    for name, fn in (("norms", lambda: step.norms(dev_in)), ("factors", lambda: step.factors_()),
-                     ("sums", lambda: step.sums(dev_in)), ("noise", lambda: step.noise_devseed()),
-                     ("sums_noised", lambda: step.sums_and_noise_devseed(dev_in)), ("_sep", None)):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(REPS):
-                if fn is not None:
-                    fn()
-                sep_buf.add_(1.0)
-        call_graphs[name] = g
-
-    def timed(replay, k_steps, seed_base):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(k_steps)]
-        for k in range(k_steps):
-            flush.zero_()                         # L2 flush, outside the events
-            step.seed_buf.fill_(seed_base + k)    # fresh noise seed, outside the events
-            evs[k][0].record(stream)
-            replay()
-            evs[k][1].record(stream)
-        torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in evs]
-
+    sb = StepBench(dp, wl, dev, channels_last=args.channels_last, host_inputs=True)
+    step = sb.step
+    W = max(args.warmup, 3)
     seed0 = wl.seed + 1_000_003 * (rank + 1)
-    timed(step.graph.replay, max(args.warmup, 3), seed0)      # warm-up
+    sb.timed(step.graph.replay, W, seed0, flush, stream)      # warm-up
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
-        step_ms = timed(step.graph.replay, args.steps, seed0)
+        step_ms = sb.timed(step.graph.replay, args.steps, seed0, flush, stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     launches = step.graph_kernels * args.steps
     total_ms = max_over_ranks(sum(step_ms), dev)
     value = world * wl.B * args.steps / (total_ms / 1e3)
-    n_rep = max(5, args.steps // 4)
-    sep_ms = statistics.mean(timed(call_graphs["_sep"].replay, n_rep, seed0))
-    per_call = {n: [max(t - sep_ms, 0.0) / REPS for t in timed(g.replay, n_rep, seed0)]
-                for n, g in call_graphs.items() if n != "_sep"}
+    means = sb.per_call_means(max(5, min(args.steps // 4, 12)), seed0, flush, stream)
+    clocks = clk.summary()
+    # the tensor-core peak for the dominant kernel: the burst figure, and the sustained one
+    # beside it when the timed region ran under the power cap
+    roof = roofline(wl, sb.work, means, pk, "burst")
+    if roof["bound"] == "tensor":
+        roof["frac_of_sustained"] = roof["achieved"] / pk["bf16_sus"]
+    roof["timing"] = (f"CUDA events around a graph of {StepBench.REPS} calls after an L2 flush, each call followed "
+                      "by a one-element PyTorch kernel (no overlap between calls; the separators' own graph time "
+                      "subtracted); per-call mean")
 
     # end to end through the public API: every step copies a batch from pinned host memory
     # and its gradient back (ClipPipeline: one graph per step, the copy of batch k+1 on a
     # forked stream alongside the compute of batch k); events around K graph launches
-    pipe = dp.ClipPipeline(descs, [(tuple(a.shape), tuple(g.shape)) for a, g in pinned], wl.dtype, C=wl.C,
-                           sigma=wl.sigma, per_layer=wl.per_layer, device=str(dev))
+    shapes = [(tuple(a.shape), tuple(g.shape)) for a, g in sb.dev_in]
+    pipe = dp.ClipPipeline(sb.descs, shapes, wl.dtype, C=wl.C, sigma=wl.sigma, per_layer=wl.per_layer,
+                           device=str(dev))
     for hset in (pipe.host_inputs(0), pipe.host_inputs(1)):     # the same batch every step
-        for (ha, hg), (sa, sg) in zip(hset, pinned):
-            ha.copy_(sa)
-            hg.copy_(sg)
-    h2d = sum(a.numel() * a.element_size() + g.numel() * g.element_size() for a, g in pinned)
+        for (ha, hg), (da, dg) in zip(hset, sb.dev_in):
+            ha.copy_(da)
+            hg.copy_(dg)
+    h2d = sum(a.numel() * a.element_size() + g.numel() * g.element_size() for a, g in pipe.host_inputs(0))
     d2h = pipe.n_params * 4
+    host_in, cl = sb.host_in, sb.cl
+    hin0 = pipe.host_inputs(0)
+
+    def sample_inputs(b):
+        if host_in is not None:
+            return [(A[:b], G[:b]) for A, G in host_in]
+        return [tuple((x[:b].movedim(-1, 1) if c else x[:b]).float().numpy() for x in pair)   # channels first
+                for pair, c in zip(hin0, cl)]
+
+    sb.free()
     pipe.start()
-    W = max(args.warmup, 3)
     for k in range(W):
         pipe.step(k, wl.seed + 7 * k)
     torch.cuda.synchronize()
@@ -404,54 +493,59 @@ def run_ours(args, wl):
         pipe.step(k, wl.seed + 7 * k)
     e1.record(stream)
     e1.synchronize()
-    e2e_ms = [e0.elapsed_time(e1)]
-    e2e_tot = max_over_ranks(sum(e2e_ms), dev)
+    e2e_tot = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = world * wl.B * args.steps / (e2e_tot / 1e3)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, sample_inputs)
+    del pipe
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
-    # roofline of the dominant call
-    pk = _peaks()
-    means = {n: statistics.mean(v) for n, v in per_call.items()}
-    dom = max(("norms", "factors", "sums", "noise"), key=means.get)   # sums_noised: the step's fused form
-    sum_bytes = work["kept_bytes"] + 4 * work["n_params"]     # kept gradients read, sums written
-    if dom == "sums" and sum_bytes / (pk["hbm"] * 1e9) > work["flop_sum"] / (pk["bf16"] * 1e12):
-        # mostly kept per-example gradients: a read-bound weighted sum
-        roof = dict(bound="hbm", achieved=sum_bytes / (means["sums"] * 1e-3) / 1e9, peak=pk["hbm"], unit="GB/s")
-    elif dom == "sums":
-        roof = dict(bound="tensor", achieved=work["flop_sum"] / (means["sums"] * 1e-3) / 1e12,
-                    peak=pk["bf16"], unit="TFLOP/s")
-    elif dom == "norms":
-        roof = dict(bound="tensor", achieved=work["flop_norm"] / (means["norms"] * 1e-3) / 1e12,
-                    peak=pk["bf16"], unit="TFLOP/s")
-    else:
-        nb = 8 * work["n_params"]
-        roof = dict(bound="hbm", achieved=nb / (means[dom] * 1e-3) / 1e9, peak=pk["hbm"], unit="GB/s")
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = _profiled_traffic(wl.name, _DOMINANT_KERNELS[dom])
-    roof["kernel"] = {"sums": "dp_clipped_sum", "norms": "dp_layer_sqnorms", "noise": "dp_add_noise",
-                      "factors": "dp_clip_factors"}[dom]
-    roof["peak_source"] = f"{pk['src']} (burst)"
-    roof["timing"] = (f"CUDA events around a graph of {REPS} calls after an L2 flush, each call followed by a "
-                      "one-element PyTorch kernel (no overlap between calls; the separators' own graph time "
-                      "subtracted); per-call mean")
+    # the other workloads of the metric, device step time only
+    per_config = {}
+    if not args.no_per_config and wl.name == DEFAULT_WORKLOAD:
+        k_steps = max(3, min(args.steps, 20))
+        for name in PER_CONFIG:
+            import workloads
+            w2 = workloads.get_workload(name)
+            b2 = StepBench(dp, w2, dev)
+            b2.timed(b2.step.graph.replay, W, seed0, flush, stream)
+            ms = b2.timed(b2.step.graph.replay, k_steps, seed0, flush, stream)
+            m2 = b2.per_call_means(5, seed0, flush, stream)
+            r2 = roofline(w2, b2.work, m2, pk, "burst")
+            tot = max_over_ranks(sum(ms), dev)
+            per_config[name] = dict(
+                value=world * w2.B * k_steps / (tot / 1e3), unit="examples/s", ms_per_step=tot / k_steps,
+                steps=k_steps, dtype=w2.dtype, norm_modes=b2.modes, kernels_per_step=b2.step.graph_kernels,
+                step_flop=b2.work["flop_norm"] + b2.work["flop_sum"], step_bytes=b2.work["bytes_total"],
+                calls_ms={n: round(v, 5) for n, v in m2.items()},
+                roofline={k: r2[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic")},
+                description=w2.description)
+            b2.free()
+            del b2
 
     line = None
     if rank == 0:
         line = dict(metric=METRIC, value=value, unit="examples/s", n_gpus=world, steps=args.steps,
-                    warmup=max(args.warmup, 3), ms_per_step=total_ms / args.steps, higher_is_better=True,
+                    warmup=W, ms_per_step=total_ms / args.steps, higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype=wl.dtype, data="synthetic",
-                    config=_config(wl, dict(norm_modes=modes, parallelism=f"replicas x{world}",
-                                            conv_layout="channels last" if any(cl) else "channels first")),
+                    config=_config(wl),
                     e2e=dict(value=e2e_value, unit="examples/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                              pipeline="ClipPipeline: one CUDA graph per step runs the step on one of two "
                                       "device buffer sets, copies its gradient to pinned host memory and, on a "
                                       "forked stream, copies the next batch from pinned host memory into the other "
                                       "set"),
-                    gpu_launches=int(launches), roofline=roof, clocks=clk.summary(),
+                    gpu_launches=int(launches), roofline=roof, clocks=clocks,
                     calls_ms={n: round(v, 5) for n, v in means.items()},
-                    kernels_per_step=step.graph_kernels,
-                    step_flop=work["flop_norm"] + work["flop_sum"], step_bytes=work["bytes_total"])
-        if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(wl, sample_inputs)
+                    kernels_per_step=step.graph_kernels, norm_modes=sb.modes,
+                    parallelism=f"replicas x{world}",
+                    conv_layout="channels last" if any(cl) else "channels first",
+                    step_flop=sb.work["flop_norm"] + sb.work["flop_sum"], step_bytes=sb.work["bytes_total"])
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        if per_config:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -514,6 +608,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the smaller workloads' device timings after the headline workload")
     ap.add_argument("--hbm-sweep", action="store_true",
                     help="supplementary steady-state bandwidth of the noise and one-row norm kernels")
     ap.add_argument("--channels-last", action="store_true",

@@ -13,8 +13,8 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence, Tuple
 
-from . import (DP_LINEAR, DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_add_noise, dp_add_noise_blocks,
-               dp_add_noise_devseed, dp_clip_factors,
+from . import (DP_LINEAR, DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_adaptive_bound, dp_add_noise,
+               dp_add_noise_blocks, dp_add_noise_devseed, dp_clip_factors,
                dp_clipped_sum, dp_clipped_sum_kept, dp_clipped_sum_kept_noised, dp_clipped_sum_noised,
                dp_clipped_sum_reuse, dp_grads_size, dp_launch_count, dp_layer_sqnorms, dp_layer_sqnorms_keep,
                dp_layout_reused, dp_plan, dp_workspace_size, noise_desc)
@@ -28,11 +28,17 @@ KEEP_MIN_ROWS = 512
 class ClipStep:
     """keep_grads: "auto" keeps the per-example gradients of instantiated layers with at
     least KEEP_MIN_ROWS rows (where the library supports it), True keeps them wherever it
-    does, False never."""
+    does, False never.
+
+    adaptive: None, or dict(alpha, beta, sigma_l2, C_l2) -- the noisy-mean adaptive bound
+    of [ThreeTools] section 3, run per layer on the step's norms right after they are
+    formed (dp_adaptive_bound; C_l2 one value or one per layer).  Layer l's next bound
+    and next norm bound land in bounds_next[l] = (C_next, C_l2_next) on the device; the
+    step's own factors use the bounds it was built with."""
 
     def __init__(self, descs: Sequence[LayerDesc], C, sigma: float, per_layer: bool = False,
                  norm_modes: Optional[Sequence[int]] = None, device: str = "cuda", keep_grads="auto",
-                 fuse_noise: bool = True):
+                 fuse_noise: bool = True, adaptive: Optional[dict] = None):
         import torch
         self.fuse_noise = bool(fuse_noise)
         self.descs = list(descs)
@@ -59,6 +65,13 @@ class ClipStep:
         self.factors = torch.empty((L if self.per_layer else 1), self.B, dtype=torch.float32, device=dev)
         self.grad = torch.empty(self.n_params, dtype=torch.float32, device=dev)
         self.seed_buf = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.adaptive = None
+        if adaptive is not None:
+            cl2 = adaptive["C_l2"]
+            cl2 = [float(c) for c in (cl2 if isinstance(cl2, (list, tuple)) else [cl2] * L)]
+            self.adaptive = dict(alpha=float(adaptive["alpha"]), beta=float(adaptive["beta"]),
+                                 sigma_l2=float(adaptive["sigma_l2"]), C_l2=cl2)
+            self.bounds_next = torch.empty(L, 2, dtype=torch.float32, device=dev)
         self.chosen: List[int] = [m for m, _, _ in self.plan]
         self.graph = None
         self.graph_kernels = 0
@@ -90,6 +103,15 @@ class ClipStep:
             else:
                 ws = self.own_ws[l] if self.own_ws[l] is not None else self.workspace
                 self.chosen[l] = dp_layer_sqnorms(d, A, G, self.sqnorms[l], ws, mode=self.modes[l], stream=stream)
+
+    def adaptive_(self, seed: int = 0, stream=None) -> None:
+        """The adaptive bound of every layer from the norms just formed (no-op without one)."""
+        a = self.adaptive
+        if a is None:
+            return
+        for l in range(len(self.descs)):
+            dp_adaptive_bound(self.sqnorms[l], self.B, a["C_l2"][l], a["alpha"], a["beta"], a["sigma_l2"], seed, l,
+                              self.bounds_next[l], stream=stream)
 
     def factors_(self, stream=None) -> None:
         L = len(self.descs)
@@ -180,6 +202,7 @@ class ClipStep:
         n0 = dp_launch_count()
         with torch.cuda.graph(g):
             self.norms(inputs)
+            self.adaptive_()
             self.factors_()
             self.sums_and_noise_devseed(inputs)
         self.graph_kernels = dp_launch_count() - n0
@@ -191,8 +214,10 @@ class ClipStep:
         return self.grad
 
     def run(self, inputs, seed: int, stream=None):
-        """Norms -> factors -> clipped sums -> noise and 1/B; returns the flat gradient."""
+        """Norms (and the adaptive bound) -> factors -> clipped sums -> noise and 1/B; returns
+        the flat gradient."""
         self.norms(inputs, stream)
+        self.adaptive_(seed, stream)
         self.factors_(stream)
         if self.fuse_noise:
             self.sums_noised(inputs, seed=seed, stream=stream)

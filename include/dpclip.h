@@ -139,9 +139,12 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
  * (one per GPU that loads the library, held until the process exits); a layer whose
  * partials need more returns DP_ERR_UNSUPPORTED and launches nothing.  Allocates
  * nothing.  The first call on a device looks up that array's address with the device
- * current (make it before any stream capture).  Every call shares the array: calls
- * that overlap on the GPU (other streams, other threads) race and give wrong norms;
- * serialize them. */
+ * current (make it before any stream capture) and keeps it for the life of the process:
+ * after a cudaDeviceReset (or any reset of the device's primary context) the kept
+ * address is stale, so do not call this entry point again in a process that reset the
+ * device.  Every call shares the array: calls that overlap on the GPU (other streams,
+ * other threads) race and give wrong norms; serialize them.  Each call writes every
+ * partial it reads, so what an earlier call left in the array does not matter. */
 dp_status dp_layer_sqnorms_noalloc(const dp_layer_desc* desc, const void* A, const void* G,
                                    int mode, float* sqnorm_out, int* chosen_mode_out,
                                    cudaStream_t stream);

@@ -4,7 +4,10 @@ import numpy as np
 import workloads
 
 # Tolerances stated for this path: relative 1e-5 for fp32 inputs, 2e-2 for bf16
-# inputs with fp32 accumulation (norms and factors per element; sums per vector).
+# inputs with fp32 accumulation.  Norms and factors: per element, relative to the
+# element.  Sums: per element, relative to |ref| + rms of the reference over the
+# element's row (a row of the weight gradient, or the whole bias vector), so that an
+# entry near zero is held to the row's scale rather than to its own.
 TOL = {"fp32": 1e-5, "bf16": 2e-2}
 # Normal draws: libm/CUDA transcendentals differ in the last bits.
 Z_RTOL, Z_ATOL = 1e-5, 1e-6
@@ -33,11 +36,41 @@ def to_dev_channels_last(x, dtype):
     return to_dev(x, dtype).movedim(1, -1).contiguous()
 
 
-def rel_vec(x, ref):
+def rel_rows(x, ref, row_len=None):
+    """Largest element-wise error max_k |x_k - ref_k| / (|ref_k| + rms_k), rms_k the root
+    mean square of ref over the row (row_len consecutive elements) holding k, or over the
+    whole vector when row_len is None."""
     x = np.asarray(x, dtype=np.float64).ravel()
     ref = np.asarray(ref, dtype=np.float64).ravel()
-    den = np.linalg.norm(ref)
-    return float(np.linalg.norm(x - ref) / (den if den > 0 else 1.0))
+    assert x.shape == ref.shape, (x.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0
+    if not np.all(np.isfinite(x)):
+        return float("inf")
+    n = row_len if row_len else ref.size
+    X, R = x.reshape(-1, n), ref.reshape(-1, n)
+    rms = np.sqrt(np.mean(R * R, axis=1, keepdims=True))
+    den = np.abs(R) + rms
+    den = np.where(den > 0, den, 1.0)
+    return float(np.max(np.abs(X - R) / den))
+
+
+def rel_flat(g, ref, specs):
+    """rel_rows over a flat gradient [W_0, b_0, W_1, b_1, ...] of layers `specs`: the rows of
+    each weight block ([p, D]) and each bias block, each against its own rms."""
+    g = np.asarray(g, dtype=np.float64).ravel()
+    ref = np.asarray(ref, dtype=np.float64).ravel()
+    assert g.shape == ref.shape
+    worst, o = 0.0, 0
+    for s in specs:
+        n = s.p * s.D
+        worst = max(worst, rel_rows(g[o:o + n], ref[o:o + n], s.D))
+        o += n
+        if s.has_bias:
+            worst = max(worst, rel_rows(g[o:o + s.p], ref[o:o + s.p]))
+            o += s.p
+    assert o == g.size
+    return worst
 
 
 def rel_elem(x, ref):

@@ -36,14 +36,34 @@ def test_reference_arm_line():
 
 @pytest.mark.gpu
 def test_bench_line_keys():
-    d = _run(["--steps", "3", "--warmup", "3", "--no-cpu-baseline"], 600)
-    assert BASE_KEYS <= set(d) and {"roofline", "clocks", "gpu_launches"} <= set(d)
+    """The default run: the ViT-Base MLP pair at B=4096 as the headline, the other
+    workloads under per_config."""
+    d = _run(["--steps", "3", "--warmup", "3", "--no-cpu-baseline"], 1200)
+    assert BASE_KEYS <= set(d) and {"roofline", "clocks", "gpu_launches", "per_config"} <= set(d)
     assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] >= 3
-    assert d["config"]["workload"] == "seq_linear_b64_t128" and d["data"] == "synthetic"
+    assert d["config"]["workload"] == "vit_mlp_b4096_t197" and d["data"] == "synthetic"
     r = d["roofline"]
-    assert r["bound"] in ("tensor", "hbm") and 0 < r["frac"] < 1.5 and r["peak"] > 0
+    assert r["bound"] == "tensor" and 0 < r["frac"] < 1.5 and r["peak"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    # the dominant call's achieved rate recomputes from its FLOP count and its mean time
+    flop = {"dp_clipped_sum": 2 * 4096 * 197 * 3072 * 768 * 2}.get(r["kernel"])
+    if flop is not None:
+        assert abs(flop / (d["calls_ms"]["sums"] * 1e-3) / 1e12 - r["achieved"]) <= 1e-3 * r["achieved"]
     e = d["e2e"]
-    assert e["value"] > 0 and e["h2d_bytes_per_step"] == 2 * 64 * 128 * 768 * 2 and e["d2h_bytes_per_step"] > 0
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4096 * 197 * (768 + 3072) * 2 * 2
+    assert e["d2h_bytes_per_step"] == 4 * (3072 * 768 + 3072 + 768 * 3072 + 768)
     assert d["gpu_launches"] == 3 * d["kernels_per_step"] > 0
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    pc = d["per_config"]
+    assert set(pc) == {"t1_linear_b32", "seq_linear_b64_t128", "conv3x3_b256", "vgg11_cifar_b1024",
+                       "vgg11_cifar_b1024_flat"}
+    for name, c in pc.items():
+        assert c["value"] > 0 and c["ms_per_step"] > 0 and c["roofline"]["frac"] > 0, name
+    assert pc["vgg11_cifar_b1024"]["kernels_per_step"] > pc["vgg11_cifar_b1024_flat"]["kernels_per_step"]
+
+
+@pytest.mark.gpu
+def test_bench_line_small_workload():
+    d = _run(["--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--workload", "seq_linear_b64_t128"], 600)
+    assert d["config"]["workload"] == "seq_linear_b64_t128" and "per_config" not in d
+    assert d["e2e"]["h2d_bytes_per_step"] == 2 * 64 * 128 * 768 * 2

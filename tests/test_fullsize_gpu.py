@@ -3,9 +3,11 @@
 Inputs are drawn on the device by a seeded generator (host generation of the
 multi-GB batches would take minutes); sampled examples are copied back for the
 oracle.  Norms: sampled examples against the oracle.  Clipped sum: the full-size
-launch with factors that are zero except for a sample of examples, against the
-oracle's sum over those examples, plus additivity in the factors over the whole
-batch.  Flat and per-layer factors of the whole step are checked against the
+launch with dense factors (every example contributes) against the oracle's
+entry-wise sum on sampled entries, among them every tile edge of the output and its
+ragged last rows and columns; the full-size launch with factors that are zero except
+for a sample of examples, against the oracle's whole sum over those examples; and
+additivity in the factors over the whole batch.  Flat and per-layer factors of the whole step are checked against the
 factor rule applied to the GPU's own norms (the rule alone is what is checked
 there; the norms are checked against the oracle).
 """
@@ -14,7 +16,7 @@ import pytest
 
 import oracle
 import workloads
-from helpers import TOL, desc_for, rel_elem, rel_vec
+from helpers import TOL, desc_for, rel_elem, rel_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -62,9 +64,70 @@ def test_full_size_norms_and_sparse_sums(lib, name, cl):
         ref_sq = oracle.layer_sqnorms(spec, a_s, g_s)
         assert rel_elem(sq.cpu().numpy()[idx], ref_sq) <= TOL[wl.dtype], (name, spec.name)
         S, Sb = oracle.clipped_sum(spec, a_s, g_s, fac[idx].astype(np.float64))
-        assert rel_vec(dW.cpu().numpy(), S) <= TOL[wl.dtype], (name, spec.name)
-        assert rel_vec(db.cpu().numpy(), Sb) <= TOL[wl.dtype], (name, spec.name)
+        assert rel_rows(dW.cpu().numpy(), S, spec.D) <= TOL[wl.dtype], (name, spec.name)
+        assert rel_rows(db.cpu().numpy(), Sb) <= TOL[wl.dtype], (name, spec.name)
         assert np.all(np.isfinite(sq.cpu().numpy())) and np.all(sq.cpu().numpy() > 0)
+        del A, G
+
+
+def _edge_indices(n, rng, k=12):
+    """Indices of one output dimension: both ends, both sides of every 64-wide tile edge
+    (the kernels' tiles are 64, 128 or 256 wide), the ragged tail, and k random ones."""
+    idx = {0, 1, n - 2, n - 1}
+    for e in range(64, n, 64):
+        idx |= {e - 1, e}
+    idx = sorted(i for i in idx if 0 <= i < n)
+    if len(idx) > 40:           # wide layers: keep every 256-edge, sample the rest
+        keep = [i for i in idx if i < 2 or i >= n - 2 or (i + 1) % 256 in (0, 1)]
+        rest = sorted(set(idx) - set(keep))
+        idx = sorted(set(keep) | set(rng.choice(rest, 40 - min(len(keep), 40), replace=False).tolist()))
+    extra = rng.choice(n, min(k, n), replace=False)
+    return np.array(sorted(set(idx) | set(extra.tolist())), dtype=np.int64)
+
+
+DENSE = [("vit_mlp_b4096_t197", False), ("seq_linear_b64_t128", False), ("conv3x3_b256", False),
+         ("conv3x3_b256", True), ("vgg11_cifar_b1024", False)]
+
+
+@pytest.mark.parametrize("name,cl", DENSE, ids=["vit", "seq", "conv3x3", "conv3x3_channels_last", "vgg"])
+def test_full_size_dense_sum_entries(lib, name, cl):
+    """Every example contributes (dense factors in [0, 1)): sampled entries of dW and db of
+    every layer against the oracle's entry-wise sum, element by element."""
+    import torch
+    dp = lib
+    wl = workloads.get_workload(name)
+    rng = np.random.default_rng(7)
+    fac = workloads.factor_inputs(wl, wl.B, 0.0, 1.0)
+    f = torch.tensor(fac, device="cuda")
+    for l, spec in enumerate(wl.layers):
+        A, G = workloads.device_layer_inputs(wl, l)
+        lay = dp.DP_NHWC if (cl and spec.kind != "linear") else dp.DP_NCHW
+        desc = desc_for(dp, spec, wl.B, wl.dtype, layout=lay)
+        Ad, Gd = (A.movedim(1, -1).contiguous(), G.movedim(1, -1).contiguous()) if lay == dp.DP_NHWC else (A, G)
+        ws = torch.empty(max(dp.dp_workspace_size(desc), 16), dtype=torch.uint8, device="cuda")
+        dW = torch.full((spec.p * spec.D,), float("nan"), device="cuda")
+        db = torch.full((spec.p,), float("nan"), device="cuda")
+        dp.dp_clipped_sum(desc, Ad, Gd, f, dW, db, ws)
+        torch.cuda.synchronize()
+        del Ad, Gd
+        rows, cols = _edge_indices(spec.p, rng), _edge_indices(spec.D, rng)
+        if spec.kind == "linear":
+            # entry (j, m) of a linear layer's sum reads G's column j and A's column m only:
+            # the oracle gets those columns (a layer of width len(cols) -> len(rows))
+            sub = workloads.LayerSpec("sub", "linear", p=rows.size, d=cols.size, T=spec.T)
+            a_h = A[:, :, torch.tensor(cols, device="cuda")].float().cpu().numpy()
+            g_h = G[:, :, torch.tensor(rows, device="cuda")].float().cpu().numpy()
+            S, Sb = oracle.clipped_sum_elements(sub, a_h, g_h, fac.astype(np.float64),
+                                                np.arange(rows.size), np.arange(cols.size))
+        else:
+            S, Sb = oracle.clipped_sum_elements(spec, A.float().cpu().numpy(), G.float().cpu().numpy(),
+                                                fac.astype(np.float64), rows, cols)
+        got = dW.view(spec.p, spec.D).cpu().numpy()[np.ix_(rows, cols)]
+        tol = TOL[wl.dtype]
+        assert rel_rows(got, S, cols.size) <= tol, (name, spec.name)
+        assert rel_rows(db.cpu().numpy()[rows], Sb) <= tol, (name, spec.name)
+        # the whole output was written (no entry left at the NaN fill)
+        assert bool(torch.isfinite(dW).all()) and bool(torch.isfinite(db).all()), (name, spec.name)
         del A, G
 
 
@@ -96,11 +159,10 @@ def test_full_size_sum_is_additive_in_factors(lib, name, pin, tol, monkeypatch):
         dp.dp_clipped_sum(desc, A, G, f, dW, db, ws)
         outs.append((dW.double(), db.double()))
     torch.cuda.synchronize()
-    lhs = outs[0][0] + outs[1][0]
-    rhs = outs[2][0]
-    assert (torch.linalg.norm(lhs - rhs) / torch.linalg.norm(rhs)).item() <= tol
-    lhs_b = outs[0][1] + outs[1][1]
-    assert (torch.linalg.norm(lhs_b - outs[2][1]) / torch.linalg.norm(outs[2][1])).item() <= tol
+    lhs = (outs[0][0] + outs[1][0]).cpu().numpy()
+    assert rel_rows(lhs, outs[2][0].cpu().numpy(), spec.D) <= tol
+    lhs_b = (outs[0][1] + outs[1][1]).cpu().numpy()
+    assert rel_rows(lhs_b, outs[2][1].cpu().numpy()) <= tol
 
 
 def test_full_size_vgg_step_flat_and_per_layer_factors(lib):
@@ -148,5 +210,5 @@ def test_full_size_conv3x3_kept_gradients_match_recomputed(lib):
         outs.append((dW, db))
     torch.cuda.synchronize()
     assert ((sq_k - sq_r).abs() / sq_r.abs()).max().item() <= 1e-5
-    for a, b in zip(outs[0], outs[1]):
-        assert (torch.linalg.norm(a - b) / torch.linalg.norm(b)).item() <= 1e-5
+    assert rel_rows(outs[0][0].cpu().numpy(), outs[1][0].cpu().numpy(), spec.D) <= 1e-5
+    assert rel_rows(outs[0][1].cpu().numpy(), outs[1][1].cpu().numpy()) <= 1e-5

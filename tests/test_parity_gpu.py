@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 import workloads
-from helpers import TOL, Z_ATOL, Z_RTOL, desc_for, rel_elem, rel_vec, to_dev
+from helpers import TOL, Z_ATOL, Z_RTOL, desc_for, rel_elem, rel_flat, rel_rows, to_dev
 from workloads import LayerSpec, Workload
 
 pytestmark = pytest.mark.gpu
@@ -47,9 +47,9 @@ def _check_layer(dp, spec, wl, examples=None, mode=None, factor_range=(0.0, 1.0)
     tol = TOL[wl.dtype]
     assert rel_elem(got["sq"].cpu().numpy(), s_ref) <= tol
     S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
-    assert rel_vec(got["dW"].cpu().numpy(), S) <= tol
+    assert rel_rows(got["dW"].cpu().numpy(), S, spec.D) <= tol
     if spec.has_bias:
-        assert rel_vec(got["db"].cpu().numpy(), Sb) <= tol
+        assert rel_rows(got["db"].cpu().numpy(), Sb) <= tol
     return got
 
 
@@ -74,10 +74,10 @@ def test_t1_linear_full_step(lib):
     assert rel_elem(step.factors.cpu().numpy()[0], ref["factors"]) <= TOL["fp32"]
     S, Sb = ref["sums"][0]
     pre = np.concatenate([S.ravel(), Sb])
-    assert rel_vec(step.grad.cpu().numpy(), pre) <= TOL["fp32"]
+    assert rel_flat(step.grad.cpu().numpy(), pre, wl.layers) <= TOL["fp32"]
     step.noise(wl.seed)
     torch.cuda.synchronize()
-    assert rel_vec(step.grad.cpu().numpy(), ref["noisy"]) <= TOL["fp32"]
+    assert rel_flat(step.grad.cpu().numpy(), ref["noisy"], wl.layers) <= TOL["fp32"]
 
 
 def test_seq_linear_full_step(lib):
@@ -98,10 +98,10 @@ def test_seq_linear_full_step(lib):
     assert rel_elem(step.sqnorms.cpu().numpy(), ref["sqnorms"]) <= tol
     assert rel_elem(step.factors.cpu().numpy()[0], ref["factors"]) <= tol
     S, Sb = ref["sums"][0]
-    assert rel_vec(step.grad.cpu().numpy(), np.concatenate([S.ravel(), Sb])) <= tol
+    assert rel_flat(step.grad.cpu().numpy(), np.concatenate([S.ravel(), Sb]), wl.layers) <= tol
     step.noise(wl.seed)
     torch.cuda.synchronize()
-    assert rel_vec(step.grad.cpu().numpy(), ref["noisy"]) <= tol
+    assert rel_flat(step.grad.cpu().numpy(), ref["noisy"], wl.layers) <= tol
 
 
 def test_conv3x3_full_batch(lib):
@@ -133,10 +133,10 @@ def test_vgg11_stack_small_batch_flat_and_per_layer(lib):
         g = step.grad.cpu().numpy()
         for l in range(len(wl.layers)):
             o, n = wl.param_offsets()[l], wl.layers[l].n_params
-            assert rel_vec(g[o:o + n], pre[o:o + n]) <= TOL["bf16"], wl.layers[l].name
+            assert rel_flat(g[o:o + n], pre[o:o + n], [wl.layers[l]]) <= TOL["bf16"], wl.layers[l].name
         step.noise(wl.seed)
         torch.cuda.synchronize()
-        assert rel_vec(step.grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+        assert rel_flat(step.grad.cpu().numpy(), ref["noisy"], wl.layers) <= TOL["bf16"]
 
 
 def test_vit_mlp_small_batch(lib):
@@ -291,8 +291,8 @@ def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
     dp.dp_clipped_sum(desc, Ad, Gd, f, dW, db, ws, accumulate=True)
     dp.dp_clipped_sum(desc, Ad, Gd, f, dW, db, ws, accumulate=True)
     S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
-    assert rel_vec(dW.cpu().numpy(), 0.25 + 2 * S.ravel()) <= TOL["bf16"]
-    assert rel_vec(db.cpu().numpy(), -0.5 + 2 * Sb) <= TOL["bf16"]
+    assert rel_rows(dW.cpu().numpy() - 0.25, 2 * S.ravel(), spec.D) <= TOL["bf16"]
+    assert rel_rows(db.cpu().numpy() + 0.5, 2 * Sb) <= TOL["bf16"]
 
 
 # The per-example clipped sum on CTA pairs (256 x 256 tiles): ragged p (the second pair's
@@ -341,7 +341,7 @@ def test_virtual_step_matches_one_batch(lib, per_layer):
             vs.add(dev, hi - lo)
         grad = vs.finish(wl.seed)
         assert vs.examples == 8
-        assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+        assert rel_flat(grad.cpu().numpy(), ref["noisy"], wl.layers) <= TOL["bf16"]
 
 
 def test_device_wait_timeout_reported_and_context_usable(lib):
@@ -362,7 +362,7 @@ def test_device_wait_timeout_reported_and_context_usable(lib):
     step = lib.ClipStep([desc_for(lib, spec, wl.B, "bf16")], C=1.0, sigma=0.5)
     grad = step.run([(to_dev(A, "bf16"), to_dev(G, "bf16")) for A, G in inputs], seed=wl.seed)
     assert lib.dp_check_status() == lib.DP_OK
-    assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+    assert rel_flat(grad.cpu().numpy(), ref["noisy"], wl.layers) <= TOL["bf16"]
 
 
 # Kept per-example gradients: the instantiated norm stores g_i and b_i, the clipped sum
@@ -400,13 +400,13 @@ def test_kept_gradients_norm_and_sum(lib, tag, spec, B):
     torch.cuda.synchronize()
     assert rel_elem(sq.cpu().numpy(), oracle.layer_sqnorms(spec, A, G)) <= TOL["bf16"]
     S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
-    assert rel_vec(dW.cpu().numpy(), S) <= TOL["bf16"]
+    assert rel_rows(dW.cpu().numpy(), S, spec.D) <= TOL["bf16"]
     if spec.has_bias:
-        assert rel_vec(db.cpu().numpy(), Sb) <= TOL["bf16"]
+        assert rel_rows(db.cpu().numpy(), Sb) <= TOL["bf16"]
     # accumulate: a second call adds the same sum
     dp.dp_clipped_sum_kept(desc, grads, f, dW, db, ws, accumulate=True)
     torch.cuda.synchronize()
-    assert rel_vec(dW.cpu().numpy(), 2 * S) <= TOL["bf16"]
+    assert rel_rows(dW.cpu().numpy(), 2 * S, spec.D) <= TOL["bf16"]
 
 
 def test_kept_gradients_unsupported_layers(lib):
@@ -427,7 +427,7 @@ def test_clip_step_with_kept_gradients(lib):
                         norm_modes=[lib.DP_NORM_INSTANTIATE] * 2, keep_grads=True)
     assert all(k is not None for k in step.kept)
     grad = step.run([(to_dev(A, "bf16"), to_dev(G, "bf16")) for A, G in inputs], seed=wl.seed)
-    assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+    assert rel_flat(grad.cpu().numpy(), ref["noisy"], wl.layers) <= TOL["bf16"]
 
 
 # The clipped sum reading the NHWC input copy its layer's norm call left in the workspace:
@@ -462,9 +462,9 @@ def test_clipped_sum_reuses_norm_layouts(lib, tag, spec, B, mode, level):
     dp.dp_clipped_sum_reuse(desc, m, Ad, Gd, f, dW, db, ws, accumulate=True)
     torch.cuda.synchronize()
     S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
-    assert rel_vec(dW.cpu().numpy() - 0.5, S) <= TOL["bf16"]
+    assert rel_rows(dW.cpu().numpy() - 0.5, S, spec.D) <= TOL["bf16"]
     if spec.has_bias:
-        assert rel_vec(db.cpu().numpy() + 1.0, Sb) <= TOL["bf16"]
+        assert rel_rows(db.cpu().numpy() + 1.0, Sb) <= TOL["bf16"]
 
 
 def test_mixed_scale_factors_straddle_bound(lib):
@@ -487,7 +487,7 @@ def test_mixed_scale_factors_straddle_bound(lib):
     under = n < 1 - 1e-3
     assert np.all(fac[under] == 1.0)
     assert rel_elem(fac, ref["factors"]) <= TOL["bf16"]
-    assert rel_vec(grad.cpu().numpy(), ref["noisy"]) <= TOL["bf16"]
+    assert rel_flat(grad.cpu().numpy(), ref["noisy"], wl.layers) <= TOL["bf16"]
 
 
 def test_nonfinite_norm_zeroes_factor_and_raises_status(lib):
