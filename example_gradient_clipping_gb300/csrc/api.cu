@@ -771,8 +771,10 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
   if (B <= 0 || layer < 0) return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0 and layer=%d >= 0", B, layer);
   if (!(C_l2 > 0.f) || !std::isfinite(alpha) || !std::isfinite(beta) || !(sigma_l2 >= 0.f))
     return fail(DP_ERR_INVALID_ARG, "C_l2 > 0, finite alpha and beta, sigma_l2 >= 0 required");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DP_ERR_CUDA, "dp_adaptive_bound: no device status word on the current device");
   cudaError_t e = dph::launch_adaptive_bound(sqnorms, B, C_l2, alpha, beta, sigma_l2, seed, layer,
-                                             out, stream);
+                                             out, st, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_adaptive_bound launch");
   return ok();
 }

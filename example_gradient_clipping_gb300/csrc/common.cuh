@@ -233,7 +233,7 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
 cudaError_t launch_add_noise_blocks(float* grad, const dpk::NoiseBlocks& nb, float invB, uint64_t seed,
                                     const unsigned long long* seed_dev, cudaStream_t s);
 cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
-                                  float sigma_l2, uint64_t seed, int layer, float* out,
+                                  float sigma_l2, uint64_t seed, int layer, float* out, unsigned* status,
                                   cudaStream_t s);
 // out[e] (+)= sum_k ws[k*n + e], fixed order; with nz->on also the noise of flat index
 // noff + e and the 1/B scale.

@@ -220,14 +220,17 @@ __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad
 __global__ void __launch_bounds__(256) adaptive_bound_kernel(const float* __restrict__ sq, int B,
                                                              float C_l2, float alpha, float beta,
                                                              float sigma_l2, uint64_t seed, int layer,
-                                                             float* __restrict__ out) {
+                                                             float* __restrict__ out, unsigned* status) {
   pdl_trigger();
   pdl_wait();
   __shared__ double part[8];
   double acc = 0.0;
   for (int i = threadIdx.x; i < B; i += blockDim.x) {
     const float n = sqrtf(sq[i]);
-    acc += (double)fminf(n, C_l2);
+    // a non-finite norm raises the status (as the clip factors do) and counts as a norm
+    // at the bound, min(inf, C_l2) = C_l2
+    if (!isfinite(n)) atomicOr(status, kStatusNonfinite);
+    acc += isfinite(n) ? (double)fminf(n, C_l2) : (double)C_l2;
   }
   acc = warp_sum_d(acc);
   if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
@@ -294,9 +297,9 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
 }
 
 cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
-                                  float sigma_l2, uint64_t seed, int layer, float* out,
+                                  float sigma_l2, uint64_t seed, int layer, float* out, unsigned* status,
                                   cudaStream_t s) {
-  launch_pdl(adaptive_bound_kernel, 1, 256, 0, s, sq, B, C_l2, alpha, beta, sigma_l2, seed, layer, out);
+  launch_pdl(adaptive_bound_kernel, 1, 256, 0, s, sq, B, C_l2, alpha, beta, sigma_l2, seed, layer, out, status);
   return cudaGetLastError();
 }
 

@@ -46,8 +46,15 @@
 namespace dpk {
 namespace tcsumx {
 
-constexpr int BM = 128, BN = 256, STAGES = 4;
-constexpr int BOX = 64 * 64 * 2;             // 64 rows x 128 B
+#ifndef DPCLIP_SUMX_FR
+#define DPCLIP_SUMX_FR 64
+#endif
+#ifndef DPCLIP_SUMX_STAGES
+#define DPCLIP_SUMX_STAGES 4
+#endif
+constexpr int BM = 128, BN = 256, STAGES = DPCLIP_SUMX_STAGES;
+constexpr int FR = DPCLIP_SUMX_FR;           // rows of a full stage (a multiple of 16)
+constexpr int BOX = FR * 64 * 2;             // FR rows x 128 B
 constexpr int STAGE = 6 * BOX;               // G: 2 boxes, A: 4 boxes
 constexpr int kEpiWarps = 8;
 constexpr int kBiasWarps = 1;                // warp 3: joins the workers' barriers
@@ -127,12 +134,12 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG6
       const bool w = ptx::mbar_wait(&c->empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
       if (!__all_sync(0xffffffffu, w)) { live = false; break; }
       const bool big = u < P.nfull;
-      const int y = big ? u * 64 : P.nfull * 64 + (u - P.nfull) * 16;
+      const int y = big ? u * FR : P.nfull * FR + (u - P.nfull) * 16;
       const CUtensorMap* mg = big ? mG64 : mG16;
       const CUtensorMap* ma = big ? mA64 : mA16;
       uint8_t* st = smem + s * STAGE;
       if (ptx::elect_one()) {
-        ptx::mbar_arrive_expect_tx(&c->full[s], (big ? 64 : 16) * 128 * (2 + na));
+        ptx::mbar_arrive_expect_tx(&c->full[s], (big ? FR : 16) * 128 * (2 + na));
         ptx::tma_load_3d(mg, &c->full[s], st, m0, y, e);
         ptx::tma_load_3d(mg, &c->full[s], st + BOX, m0 + 64, y, e);
 #pragma unroll
@@ -182,7 +189,7 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
       if (ptx::elect_one()) {
         if (u < P.nfull) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < FR / 16; ++kk)
             ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(dbd, kk * 2048), idesc,
                            (u | kk) != 0);
         } else {
@@ -239,11 +246,11 @@ __device__ __forceinline__ void epilogue_norm(const Params& P, uint8_t* smem, Ct
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         const uint8_t* gt = smem + s * STAGE + bbox * BOX + bj * 128 + ((bq ^ (bj & 7)) << 4);
         if (u < P.nfull) {
-          uint4 v[4];
+          uint4 v[FR / 16];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) v[h] = *reinterpret_cast<const uint4*>(gt + h * 16 * 128);
+          for (int h = 0; h < FR / 16; ++h) v[h] = *reinterpret_cast<const uint4*>(gt + h * 16 * 128);
 #pragma unroll
-          for (int h = 0; h < 4; ++h) add_bf16x8(v[h], bt);
+          for (int h = 0; h < FR / 16; ++h) add_bf16x8(v[h], bt);
         } else {
           add_bf16x8(*reinterpret_cast<const uint4*>(gt), bt);
         }
@@ -349,11 +356,11 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
         // 128-byte swizzle: chunk q of row r sits at chunk q ^ (r % 8)
         const uint8_t* gt = smem + s * STAGE + bbox * BOX + bj * 128 + ((bq ^ (bj & 7)) << 4);
         if (u < P.nfull) {
-          uint4 v[4];
+          uint4 v[FR / 16];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) v[h] = *reinterpret_cast<const uint4*>(gt + h * 16 * 128);
+          for (int h = 0; h < FR / 16; ++h) v[h] = *reinterpret_cast<const uint4*>(gt + h * 16 * 128);
 #pragma unroll
-          for (int h = 0; h < 4; ++h) add_bf16x8(v[h], btmp);
+          for (int h = 0; h < FR / 16; ++h) add_bf16x8(v[h], btmp);
         } else {
           add_bf16x8(*reinterpret_cast<const uint4*>(gt), btmp);
         }
@@ -693,7 +700,7 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
   const uint64_t da[3] = {(uint64_t)g.D, (uint64_t)g.T, (uint64_t)g.B};
   const uint64_t sa[2] = {(uint64_t)g.D * 2, (uint64_t)g.T * g.D * 2};
-  const uint32_t box64[3] = {64, 64, 1}, box16[3] = {64, 16, 1};
+  const uint32_t box64[3] = {64, (uint32_t)tcsumx::FR, 1}, box16[3] = {64, 16, 1};
   if (!encode_tmap_bf16(&mg64, G, 3, dg, sg, box64) || !encode_tmap_bf16(&ma64, A, 3, da, sa, box64) ||
       !encode_tmap_bf16(&mg16, G, 3, dg, sg, box16) || !encode_tmap_bf16(&ma16, A, 3, da, sa, box16))
     return cudaErrorInvalidValue;
@@ -722,9 +729,9 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   P.accumulate = accumulate;
   P.gsplit = gsplits ? 1 : 0;
   P.early = early ? 1 : 0;
-  int nfull = g.T / 64, rem = g.T - 64 * nfull;
+  int nfull = g.T / tcsumx::FR, rem = g.T - tcsumx::FR * nfull;
   int n16 = (rem + 15) / 16;
-  if (n16 > 3) { nfull += 1; n16 = 0; }
+  if (n16 > tcsumx::FR / 16 - 1) { nfull += 1; n16 = 0; }
   P.nfull = nfull;
   P.n16 = n16;
   int dev = 0;
@@ -778,7 +785,7 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
   const uint64_t sg[2] = {(uint64_t)g.p * 2, (uint64_t)g.T * g.p * 2};
   const uint64_t da[3] = {(uint64_t)g.D, (uint64_t)g.T, (uint64_t)g.B};
   const uint64_t sa[2] = {(uint64_t)g.D * 2, (uint64_t)g.T * g.D * 2};
-  const uint32_t box64[3] = {64, 64, 1}, box16[3] = {64, 16, 1};
+  const uint32_t box64[3] = {64, (uint32_t)tcsumx::FR, 1}, box16[3] = {64, 16, 1};
   if (!encode_tmap_bf16(&mg64, G, 3, dg, sg, box64) || !encode_tmap_bf16(&ma64, A, 3, da, sa, box64) ||
       !encode_tmap_bf16(&mg16, G, 3, dg, sg, box16) || !encode_tmap_bf16(&ma16, A, 3, da, sa, box16))
     return cudaErrorInvalidValue;
@@ -796,9 +803,9 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
   P.d = g.D;
   P.ex_per_split = eps;
   P.splits = 1;
-  int nfull = g.T / 64, rem = g.T - 64 * nfull;
+  int nfull = g.T / tcsumx::FR, rem = g.T - tcsumx::FR * nfull;
   int n16 = (rem + 15) / 16;
-  if (n16 > 3) { nfull += 1; n16 = 0; }
+  if (n16 > tcsumx::FR / 16 - 1) { nfull += 1; n16 = 0; }
   P.nfull = nfull;
   P.n16 = n16;
   P.part = ws;

@@ -165,6 +165,10 @@ dp_status dp_clip_factors(const float* sqnorms, int B, int L, int per_layer, con
  *   db[j]    (+)= sum_i factors[i] * sum_t G_i[t, j]        fp32 [p], device (NULL: skipped)
  * factors: device fp32 [B] (a row of dp_clip_factors' output).  accumulate = 0 writes,
  * 1 adds to the existing dW/db (gradient accumulation over micro-batches).
+ * An example whose norm overflowed but whose inputs are finite gets factor 0 from
+ * dp_clip_factors and adds nothing; an example whose A or G hold inf or NaN can still
+ * turn entries of the sum into NaN (0 * inf), and dp_clip_factors has raised
+ * DP_ERR_NONFINITE for it: a caller that sees that status discards the step.
  * workspace: device, >= dp_workspace_size(desc, 0) bytes. */
 dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G,
                          const float* factors, float* dW, float* db, int accumulate,
@@ -208,7 +212,9 @@ dp_status dp_add_noise_blocks(float* grad, const dp_noise_block* blocks, int nbl
  *   C_next = alpha/B * (sum_i min(sqrt(sqnorms[i]), C_l2) + sigma_l2 * C_l2 * z),
  *   C_l2_next = beta * C_next,
  * z = element `layer` of noise stream 1 (counter word 2 = 1) under `seed`.
- * sqnorms: device fp32 [B].  out: device fp32 [2] = {C_next, C_l2_next}. */
+ * sqnorms: device fp32 [B].  out: device fp32 [2] = {C_next, C_l2_next}.
+ * A non-finite norm sets DP_ERR_NONFINITE in the device status word (read it with
+ * dp_check_status) and enters the sum as the bound C_l2 (min(inf, C_l2)). */
 dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha, float beta,
                             float sigma_l2, uint64_t seed, int layer, float* out,
                             cudaStream_t stream);

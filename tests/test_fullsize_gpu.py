@@ -133,9 +133,11 @@ def test_full_size_dense_sum_entries(lib, name, cl):
 
 # The per-example kernel scales each example's fp32 product, so linearity holds to fp32
 # rounding; the row-scaled kernel rounds the scaled rows c_i G_i to bf16 before the
-# MMA (2^-9 relative per element), so it holds to that rounding.
+# MMA (2^-9 relative per element, which over 262,144 terms leaves a few 1e-3 of the
+# row's scale on a typical entry and about 1e-2 on the worst of 36,864), so it holds
+# to the bf16 path's tolerance.
 ADDITIVE = [("vit_mlp_b4096_t197", "", 1e-4), ("conv3x3_b256", "", 1e-4),
-            ("conv3x3_b256", "example", 1e-4), ("conv3x3_b256", "rows", 1e-2)]
+            ("conv3x3_b256", "example", 1e-4), ("conv3x3_b256", "rows", 2e-2)]
 
 
 @pytest.mark.parametrize("name,pin,tol", ADDITIVE, ids=["vit", "conv_im2col", "conv_example", "conv_rows"])

@@ -550,6 +550,27 @@ def test_adaptive_bound_matches_oracle(lib):
         assert cl2 == pytest.approx(rcl2, rel=1e-5, abs=1e-6)
 
 
+def test_adaptive_bound_nonfinite_norm_raises_status(lib):
+    """A non-finite norm raises DP_ERR_NONFINITE and enters the noisy mean at the bound
+    (min(inf, C_l2) = C_l2): the oracle's value with that norm set to the bound."""
+    import torch
+    rng = np.random.default_rng(4)
+    s = (rng.random(300) * 4.0).astype(np.float32)
+    C_l2 = 1.2
+    for bad in (np.inf, np.nan):
+        t = s.copy()
+        t[17] = bad
+        assert lib.dp_check_status() == lib.DP_OK
+        out = torch.empty(2, device="cuda")
+        lib.dp_adaptive_bound(torch.tensor(t, device="cuda"), 300, C_l2, 1.1, 2.0, 2.5, 5, 3, out)
+        assert lib.dp_check_status() == lib.DP_ERR_NONFINITE
+        ref = s.astype(np.float64)
+        ref[17] = C_l2 * C_l2
+        rc, rcl2 = oracle.adaptive_bound(ref, C_l2, 1.1, 2.0, 2.5, 5, 3)
+        c, cl2 = out.cpu().numpy()
+        assert c == pytest.approx(rc, rel=1e-5, abs=1e-6) and cl2 == pytest.approx(rcl2, rel=1e-5, abs=1e-6)
+
+
 def test_pipeline_matches_step(lib):
     """ClipPipeline (one graph per step, next batch copied alongside) gives ClipStep.run's result."""
     import torch
