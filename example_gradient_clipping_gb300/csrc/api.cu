@@ -175,9 +175,9 @@ size_t padded_out_bytes(const Geom& g) {
 
 // Clipped-sum kernel: 0 SIMT, 1 row-scaled tensor-core GEMM, 2 per-example tensor-core
 // accumulation (single CTA), 3 per-example conv kernel with TMA im2col loads, 4 the
-// row-scaled GEMM with im2col loads, 5 the one-row outer-product sum, 6 per-example on CTA
-// pairs (only when pinned).  The per-example kernels split the examples over clusters or
-// the grid; the row-scaled GEMM splits the batch rows over the whole grid.
+// row-scaled GEMM with im2col loads, 5 the one-row outer-product sum.  The per-example
+// kernels split the examples over clusters or the grid; the row-scaled GEMM splits the
+// batch rows over the whole grid.
 struct Plan {
   int kernel;
   bool rows;    // conv layer through its row layout
@@ -189,22 +189,18 @@ bool tc_inputs(const Geom& g, int dtype, const void* A, const void* G, const voi
   return !g.conv || aligned16(ws);
 }
 
-// DPCLIP_SUM_KERNEL=rows|example|pair pins the tensor-core clipped-sum kernel where the
-// shape allows it (all compute the same sum; used by the tests and for tuning).  The
-// CTA-pair kernel is only taken when pinned: on the sequence and ViT MLP layers it ran
-// 1.4-1.5x slower than the per-example single-CTA kernel.
+// DPCLIP_SUM_KERNEL=rows|example pins the tensor-core clipped-sum kernel where the
+// shape allows it (all compute the same sum; used by the tests and for tuning).
 int pinned_sum_kernel() {
   const char* v = std::getenv("DPCLIP_SUM_KERNEL");
   if (!v) return 0;
   if (!std::strcmp(v, "rows")) return 1;
   if (!std::strcmp(v, "example")) return 2;
-  if (!std::strcmp(v, "pair")) return 6;
   return 0;
 }
 
 int sum_kernel_for(const Geom& lg) {
   const int pin = pinned_sum_kernel();
-  if (pin == 6 && dph::tc_sum2_supported(lg)) return 6;
   if (pin == 2 && dph::tc_sumx_supported(lg)) return 2;
   if (pin == 1 && dph::tc_sum_supported(lg)) return 1;
   const long tiles = (long)((lg.p + 127) / 128) * ((lg.D + 255) / 256);
@@ -275,7 +271,6 @@ size_t sum_ws_bytes(const Geom& g, const Plan& pl) {
   const size_t inner = pl.kernel == 5   ? dph::t1_sum_ws_bytes(g)
                        : pl.kernel == 4 ? dph::tc_sum_conv_ws_bytes(g)
                        : pl.kernel == 3 ? dph::tc_conv_ws_bytes(g, false)
-                       : pl.kernel == 6 ? dph::tc_sum2_ws_bytes(lg)
                        : pl.kernel == 2 ? dph::tc_sumx_ws_bytes(lg)
                        : pl.kernel == 1 ? align256(dph::tc_sum_ws_bytes(lg)) +
                                               (pl.rows ? dph::scaled_rows_bias_bytes(g.B, g.T, g.p) : 0)
@@ -347,7 +342,6 @@ size_t max_ws_bytes(const Geom& g, int mode) {
       n = std::max(n, pre + align256(dph::tc_sum_ws_bytes(lg)) +
                           (g.conv ? dph::scaled_rows_bias_bytes(g.B, g.T, g.p) : 0));
     if (dph::tc_sumx_supported(lg)) n = std::max(n, pre + dph::tc_sumx_ws_bytes(lg));
-    if (dph::tc_sum2_supported(lg)) n = std::max(n, pre + dph::tc_sum2_ws_bytes(lg));
   }
   Plan kp;
   if (keep_plan(DP_BF16, g, &kp)) n = std::max(n, std::max(norm_ws_bytes(g, kp), kept_sum_need(g, kp)));
@@ -559,8 +553,6 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
     else
       e = dph::launch_tc_conv_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, xh, nz);
   }
-  else if (pl.kernel == 6)
-    e = dph::launch_tc_sum2(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream);
   else if (pl.kernel == 2)   // (a padded output gets its noise after the compaction below)
     e = dph::launch_tc_sumx(pl.lg, A, G, factors, kdW, kdb, kacc, wsp, status_ptr(), stream, padded ? nullptr : nz,
                             !pl.rows);

@@ -67,6 +67,7 @@ constexpr int SMEM = STAGES * STAGE + 1024 + 512;
 constexpr int PSTR = BN + 4;                 // staged partial row stride (floats)
 constexpr int PART_BYTES = BM * PSTR * 4;    // staged weight partial, then 128 bias floats
 static_assert(PART_BYTES + BM * 4 <= STAGES * STAGE, "staging fits in the stage buffers");
+static_assert(STAGES % 2 == 0, "each slot is filled by one of the two producers");
 
 struct Params {
   const float* factors;
@@ -83,11 +84,23 @@ struct Params {
   float* keep;        // norm mode, or null: every example's gradient [B, p, d] and bias [B, p]
   float* keep_b;
   int early;          // A and G are the caller's inputs: loads may start before pdl_wait
+  // Sum mode, bias: with bias_nt == 1 the CTAs of the first column tile sum the G rows of
+  // every example; with bias_nt > 1 column tile j < bias_nt sums those of the examples x
+  // (counted from the split's first) with x % bias_nt == j, and writes its partial bias to
+  // bias_part [bias_nt, p] (summed over the tiles afterwards, in order)
+  int bias_nt;
+  float* bias_part;
 };
+
+// Does this CTA sum the G rows of example x (counted from its split's first) for the bias?
+__device__ __forceinline__ bool bias_example(const Params& P, int x) {
+  if (!P.db) return false;
+  return P.bias_nt == 1 ? blockIdx.y == 0 : (int)blockIdx.y == x % P.bias_nt;
+}
 
 // Shared-memory control block after the stages.
 struct Ctl {
-  uint64_t full[STAGES], empty[STAGES], accum[2], tfree[2], drain;
+  uint64_t full[STAGES], empty[STAGES], bfree[STAGES], accum[2], tfree[2], drain;
   uint32_t tmem;
   int abort;
   int flags[2];       // [1] go / no-go after the main loops
@@ -117,7 +130,7 @@ __device__ __forceinline__ int tile_n(const Params& P, int n0) {
 
 // Warps 0 and 2 (all lanes): TMA producers; producer `pr` loads the stages k with
 // k % 2 == pr (the two G boxes and the A boxes the tile's width needs).
-template <bool kTrim>
+template <bool kNorm, bool kTrim>
 __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG64, const CUtensorMap* mA64,
                                          const CUtensorMap* mG16, const CUtensorMap* mA16, uint8_t* smem,
                                          Ctl* c, int e0, int e1, int m0, int n0, int pr) {
@@ -127,11 +140,22 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG6
   int k = 0, issued = 0;
   bool live = true;
   int last = -1;
+  // sum mode: per slot, whether its last stage had its G rows summed for the bias (the
+  // slot is then also released by the epilogue warps, on bfree) and the parity of the
+  // slot's such rounds so far
+  uint32_t pend = 0, par = 0;
   for (int e = e0; e < e1 && live; ++e) {
+    const bool bias_e = !kNorm && bias_example(P, e - e0);
     for (int u = 0; u < ns; ++u, ++k) {
       if ((k & 1) != pr) continue;
       const int s = k % STAGES;
-      const bool w = ptx::mbar_wait(&c->empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
+      bool w = ptx::mbar_wait(&c->empty[s], ((k / STAGES) & 1) ^ 1, abort, P.status);
+      if (!kNorm && ((pend >> s) & 1u)) {
+        w = w && ptx::mbar_wait(&c->bfree[s], (par >> s) & 1u, abort, P.status);
+        par ^= 1u << s;
+        pend &= ~(1u << s);
+      }
+      if (bias_e) pend |= 1u << s;
       if (!__all_sync(0xffffffffu, w)) { live = false; break; }
       const bool big = u < P.nfull;
       const int y = big ? u * FR : P.nfull * FR + (u - P.nfull) * 16;
@@ -156,6 +180,58 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mG6
       if ((q & 1) == pr) ptx::mbar_wait_drain(&c->full[q % STAGES], (q / STAGES) & 1);
   }
   (void)issued;
+}
+
+#ifndef DPCLIP_SUMX_PREFETCH
+#define DPCLIP_SUMX_PREFETCH 2
+#endif
+// Examples ahead of the producers whose rows warp 3 prefetches into L2.
+constexpr int kPrefetch = DPCLIP_SUMX_PREFETCH;
+
+// TMA prefetch of one box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+               "r"(z)
+               : "memory");
+}
+
+// Warp 3 (sum mode): L2 prefetch of the rows kPrefetch examples ahead of the producers,
+// so that their loads find the rows in L2 instead of waiting for HBM (the CTAs that share
+// a box request it at about the same time, and each waited for the first one's miss).
+// The CTAs of the first column tile prefetch their G columns, those of the first row tile
+// their A columns, so every byte is prefetched once.  Warp 3 follows the producers by
+// waiting for the first stage of each example to land.
+template <bool kTrim>
+__device__ __forceinline__ void prefetcher(const Params& P, const CUtensorMap* mG64, const CUtensorMap* mA64,
+                                           const CUtensorMap* mG16, const CUtensorMap* mA16, Ctl* c, int e0,
+                                           int e1, int m0, int n0) {
+  const bool pg = blockIdx.y == 0, pa = blockIdx.x == 0;
+  if (!pg && !pa) return;
+  volatile int* abort = &c->abort;
+  const int ns = P.nfull + P.n16;
+  const int na = (tile_n<kTrim>(P, n0) + 63) / 64;
+  auto fetch = [&](int e) {
+    if (ptx::elect_one()) {
+      for (int u = 0; u < ns; ++u) {
+        const bool big = u < P.nfull;
+        const int y = big ? u * FR : P.nfull * FR + (u - P.nfull) * 16;
+        if (pg) {
+          tma_prefetch_3d(big ? mG64 : mG16, m0, y, e);
+          tma_prefetch_3d(big ? mG64 : mG16, m0 + 64, y, e);
+        }
+        if (pa)
+          for (int j = 0; j < na; ++j) tma_prefetch_3d(big ? mA64 : mA16, n0 + 64 * j, y, e);
+      }
+    }
+    __syncwarp();
+  };
+  for (int e = e0; e < min(e1, e0 + kPrefetch); ++e) fetch(e);
+  for (int e = e0; e + kPrefetch < e1; ++e) {
+    const int k = (e - e0) * ns;
+    const bool w = ptx::mbar_wait(&c->full[k % STAGES], (k / STAGES) & 1, abort, P.status);
+    if (!__all_sync(0xffffffffu, w)) return;
+    fetch(e + kPrefetch);
+  }
 }
 
 // Warp 1 (all lanes): MMA issuer.  Descriptors are built once per stage from the
@@ -345,12 +421,12 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
 #pragma unroll
   for (int j = 0; j < 128; ++j) acc[j] = 0.f;
   bool ok = true;
-  int k = 0;
   for (int e = e0; e < e1 && ok; ++e) {
     const int x = e - e0, b = x & 1;
-    if (do_bias) {
-      for (int u = 0; u < ns; ++u, ++k) {
-        const int s = k % STAGES;
+    const bool bias_e = bias_example(P, x);
+    if (bias_e) {
+      for (int u = 0; u < ns; ++u) {
+        const int k = x * ns + u, s = k % STAGES;
         const bool w = ptx::mbar_wait(&c->full[s], (k / STAGES) & 1, abort, P.status);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         // 128-byte swizzle: chunk q of row r sits at chunk q ^ (r % 8)
@@ -365,7 +441,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
           add_bf16x8(*reinterpret_cast<const uint4*>(gt), btmp);
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&c->empty[s]);
+        if (lane == 0) ptx::mbar_arrive(&c->bfree[s]);
       }
       if (!ok) break;
     }
@@ -389,7 +465,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&c->tfree[b]);
-    if (do_bias) {
+    if (bias_e) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         bacc[q] = fmaf(cf, btmp[q], bacc[q]);
@@ -416,6 +492,7 @@ __device__ __forceinline__ void epilogue(const Params& P, uint8_t* smem, Ctl* c,
     for (int q = 0; q < 8; ++q) {
       const int j = bbox * 64 + bq * 8 + q;
       if (P.splits > 1) partb[j] = bacc[q];   // staged for the cluster reduction
+      else if (P.bias_nt > 1 && m0 + j < P.p) P.bias_part[(size_t)blockIdx.y * P.p + m0 + j] = bacc[q];
       else if (P.gsplit && m0 + j < P.p) P.db[(size_t)blockIdx.z * P.p + m0 + j] = bacc[q];
       else if (m0 + j < P.p) P.db[m0 + j] = bacc[q] + (P.accumulate ? P.db[m0 + j] : 0.f);
     }
@@ -520,7 +597,9 @@ __device__ __forceinline__ void cluster_reduce(const Params& P, uint8_t* smem, i
       float sum = 0.f;
       for (int sp = 0; sp < S; ++sp) sum += ptx::ld_cluster_f32(ptx::map_rank(base + 4u * j, sp));
       const int col = m0 + j;
-      if (col < P.p) P.db[col] = sum + (P.accumulate ? P.db[col] : 0.f);
+      if (col >= P.p) continue;
+      if (P.bias_nt > 1) P.bias_part[(size_t)blockIdx.y * P.p + col] = sum;
+      else P.db[col] = sum + (P.accumulate ? P.db[col] : 0.f);
     }
   }
 }
@@ -561,12 +640,18 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
   const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
   const int e0 = blockIdx.z * P.ex_per_split;
   const int e1 = min(P.B, e0 + P.ex_per_split);
-  const bool do_bias = (kNorm ? P.norm_bias != 0 : P.db != nullptr) && blockIdx.y == 0;
+  // this CTA sums G rows for the bias (norm mode: the first column tile, every example;
+  // sum mode: see bias_example)
+  const bool do_bias = kNorm ? (P.norm_bias != 0 && blockIdx.y == 0)
+                             : (P.db != nullptr && (int)blockIdx.y < P.bias_nt);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&c->full[s], 1);
-      ptx::mbar_init(&c->empty[s], do_bias ? 1 + kEpiWarps : 1);
+      // norm mode: the MMA commit plus the eight epilogue warps when they sum G rows;
+      // sum mode: the MMA commit, and bfree the eight warps for the stages they sum
+      ptx::mbar_init(&c->empty[s], kNorm && do_bias ? 1 + kEpiWarps : 1);
+      ptx::mbar_init(&c->bfree[s], kEpiWarps);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&c->accum[b], 1);
@@ -603,10 +688,11 @@ tc_sumx_kernel(const __grid_constant__ CUtensorMap mapG64, const __grid_constant
   } else {
     ptx::regs_dec<64>();
     if (warp == 0 || warp == 2) {
-      producer<kTrim>(P, &mapG64, &mapA64, &mapG16, &mapA16, smem, c, e0, e1, m0, n0, warp >> 1);
+      producer<kNorm, kTrim>(P, &mapG64, &mapA64, &mapG16, &mapA16, smem, c, e0, e1, m0, n0, warp >> 1);
     } else if (warp == 1) {
       mma_issuer<kTrim>(P, smem, c, tmem, e0, e1);
     } else {
+      if (!kNorm && kPrefetch > 0) prefetcher<kTrim>(P, &mapG64, &mapA64, &mapG16, &mapA16, c, e0, e1, m0, n0);
       pdl_wait();
       finish_decision(c);        // warp 3 joins the workers' barrier
     }
@@ -687,9 +773,22 @@ bool tc_sumx_supported(const Geom& g) {
   return !g.conv && (g.p % 8 == 0) && (g.D % 8 == 0) && g.p >= 8 && g.D >= 8 && g.T >= 64;
 }
 
+// Column tiles that share the bias (Params::bias_nt).  The CTAs that sum G rows for the
+// bias read 16 KB more of shared memory per stage than the others, and shared-memory
+// bandwidth is what bounds this kernel (about a quarter more time on the ViT-Base MLP
+// layers when one column tile summed every example), so with examples split over
+// clusters and enough of them (B >= 256: at least 64 per CTA) every column tile sums its
+// share, at the cost of a reduction of bias_nt partial vectors after the kernel.
+static int tc_sumx_bias_nt(const Geom& g) {
+  const int ntn = cdiv_x(g.D, tcsumx::BN);
+  return (g.has_bias && !tc_sumx_grid_splits(g) && ntn > 1 && g.B >= 256) ? ntn : 1;
+}
+
 size_t tc_sumx_ws_bytes(const Geom& g) {
   const int gs = tc_sumx_grid_splits(g);
-  return gs ? (size_t)gs * ((size_t)g.p * g.D + g.p) * sizeof(float) : 0;
+  if (gs) return (size_t)gs * ((size_t)g.p * g.D + g.p) * sizeof(float);
+  const int bnt = tc_sumx_bias_nt(g);
+  return bnt > 1 ? (size_t)bnt * g.p * sizeof(float) : 0;
 }
 
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
@@ -728,6 +827,10 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
   P.splits = splits;
   P.accumulate = accumulate;
   P.gsplit = gsplits ? 1 : 0;
+  const int bias_nt = db ? tc_sumx_bias_nt(g) : 1;
+  if (bias_nt > 1 && !ws) return cudaErrorInvalidValue;
+  P.bias_nt = bias_nt;
+  P.bias_part = bias_nt > 1 ? static_cast<float*>(ws) : nullptr;
   P.early = early ? 1 : 0;
   int nfull = g.T / tcsumx::FR, rem = g.T - tcsumx::FR * nfull;
   int n16 = (rem + 15) / 16;
@@ -764,6 +867,10 @@ cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const fl
                       ? cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false, true>, mg64, ma64, mg16, ma16, P)
                       : cudaLaunchKernelEx(&cfg, tcsumx::tc_sumx_kernel<false, false>, mg64, ma64, mg16, ma16, P);
   count_launch();
+  if (e == cudaSuccess && bias_nt > 1) {   // the column tiles' partial biases, in order
+    e = launch_reduce_splits(P.bias_part, bias_nt, (size_t)g.p, db, accumulate, s, nz, nz ? nz->off_b : 0);
+    if (nz && nz->on) nz->applied_b = 1;
+  }
   if (e != cudaSuccess || !gsplits) return e;
   const size_t nw = (size_t)g.p * g.D;
   return launch_reduce_splits2(SplitSeg{part_w, nw, nw, dW}, SplitSeg{part_b, (size_t)g.p, db ? (size_t)g.p : 0, db},

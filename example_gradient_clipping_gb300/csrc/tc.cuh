@@ -21,12 +21,6 @@ size_t tc_sumx_ws_bytes(const Geom& g);
 cudaError_t launch_tc_sumx(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
                            float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
                            dpk::NoiseArgs* nz = nullptr, bool early = false);
-// The same per-example clipped sum on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2);
-// p and D above 128 (neither half of a pair tile empty).
-bool tc_sum2_supported(const Geom& g);
-size_t tc_sum2_ws_bytes(const Geom& g);
-cudaError_t launch_tc_sum2(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
-                           float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s);
 // Instantiated norm ||G_i^T A_i||^2 (+ bias) from the same per-example TMEM products
 // (shapes as tc_sumx_supported).
 size_t tc_inst_ws_bytes(const Geom& g);

@@ -234,6 +234,35 @@ def test_edge_shapes(lib, tag, spec, B, dtype):
         _check_layer(lib, spec, wl, mode=mode)
 
 
+@pytest.mark.parametrize("B,accumulate", [(300, False), (257, True)], ids=["B300", "B257_accumulate"])
+def test_bias_shared_across_column_tiles(lib, B, accumulate):
+    """A layer whose examples split over clusters with B >= 256: every column tile sums the
+    bias over its share of the examples and the partial biases are added after the kernel.
+    The whole bias and sampled weight entries against the oracle's entry-wise sum."""
+    import torch
+    dp = lib
+    spec = LayerSpec("e", "linear", p=768, d=1280, T=64)
+    wl = Workload(name="bias_shared", B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=37)
+    A, G = workloads.layer_inputs(wl, 0)
+    fac = workloads.factor_inputs(wl, B)
+    desc = desc_for(dp, spec, B, "bf16")
+    ws = torch.empty(dp.dp_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    dW = torch.full((spec.p * spec.D,), 0.5, device="cuda")
+    db = torch.full((spec.p,), -0.25, device="cuda")
+    dp.dp_clipped_sum(desc, to_dev(A, "bf16"), to_dev(G, "bf16"), torch.tensor(fac, device="cuda"), dW, db, ws,
+                      accumulate=accumulate)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.r_[0, 127, 128, 255, 256, 767, rng.choice(spec.p, 20, replace=False)])
+    cols = np.unique(np.r_[0, 255, 256, 511, 512, 1023, 1024, 1279, rng.choice(spec.D, 20, replace=False)])
+    S, _ = oracle.clipped_sum_elements(spec, A, G, fac.astype(np.float64), rows, cols)
+    _, Sb = oracle.clipped_sum_elements(spec, A, G, fac.astype(np.float64), np.arange(spec.p), [0])
+    base_w, base_b = (0.5, -0.25) if accumulate else (0.0, 0.0)
+    got = dW.view(spec.p, spec.D).cpu().numpy()[np.ix_(rows, cols)] - base_w
+    assert rel_rows(got, S, cols.size) <= TOL["bf16"]
+    assert rel_rows(db.cpu().numpy() - base_b, Sb) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("conv_pin", ["", "rows"], ids=["im2col", "rows"])
 def test_conv3x3_im2col_and_row_layout(lib, conv_pin, monkeypatch):
     """The 3x3 conv workload's layer (small batch): im2col kernels and the row layout."""
@@ -263,17 +292,17 @@ ACC = [(LayerSpec("e", "linear", p=42, d=72, T=9), 6),          # SIMT (p not a 
        (LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 2),  # conv, im2col per example
        (LayerSpec("e", "linear", p=10, d=13, T=1), 300),                   # one row, 3 example splits
        (LayerSpec("e", "linear", p=136, d=264, T=70), 11),                 # per-example, grid splits
-       (LayerSpec("e", "linear", p=256, d=256, T=64), 1),                  # CTA pairs, one split
-       (LayerSpec("e", "linear", p=264, d=200, T=70), 11)]                 # CTA pairs, grid splits
+       (LayerSpec("e", "linear", p=256, d=256, T=64), 1),                  # per-example, bias, one split
+       (LayerSpec("e", "linear", p=512, d=256, T=70), 11)]                 # per-example, bias, splits
 
 
-ACC_PIN = ["", "rows", "example", "example", "", "", "", "", "example", "pair", "pair"]
+ACC_PIN = ["", "rows", "example", "example", "", "", "", "", "example", "example", "example"]
 
 
 @pytest.mark.parametrize("spec,B,pin", [(s, b, p) for (s, b), p in zip(ACC, ACC_PIN)],
                          ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single", "conv_padded",
                               "conv_im2col_rows", "conv_im2col_example", "t1_splits", "tc_ex_grid",
-                              "pair_single", "pair_grid"])
+                              "tc_ex_256_single", "tc_ex_tail_splits"])
 def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
     if pin:
         monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
@@ -293,23 +322,6 @@ def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
     S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
     assert rel_rows(dW.cpu().numpy() - 0.25, 2 * S.ravel(), spec.D) <= TOL["bf16"]
     assert rel_rows(db.cpu().numpy() + 0.5, 2 * Sb) <= TOL["bf16"]
-
-
-# The per-example clipped sum on CTA pairs (256 x 256 tiles): ragged p (the second pair's
-# odd CTA entirely past p), ragged D, 16-row tail stages, no bias, many grid splits.
-PAIR = [
-    ("pair_B1", LayerSpec("e", "linear", p=256, d=256, T=64), 1),
-    ("pair_ragged", LayerSpec("e", "linear", p=264, d=200, T=70), 11),
-    ("pair_T130_nobias", LayerSpec("e", "linear", p=384, d=136, T=130, has_bias=False), 3),
-    ("pair_many_splits", LayerSpec("e", "linear", p=256, d=512, T=64), 40),
-]
-
-
-@pytest.mark.parametrize("tag,spec,B", PAIR, ids=[e[0] for e in PAIR])
-def test_pair_sum_kernel(lib, tag, spec, B, monkeypatch):
-    monkeypatch.setenv("DPCLIP_SUM_KERNEL", "pair")
-    wl = Workload(name=tag, B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=13)
-    _check_layer(lib, spec, wl)
 
 
 def test_speed_priority_mode(lib):
