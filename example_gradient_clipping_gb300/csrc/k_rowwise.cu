@@ -38,39 +38,62 @@ __global__ void __launch_bounds__(256) t1_norm_kernel(Geom g, const E* __restric
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < g.B; i += warps) {
-    const E* a = A + (size_t)i * g.d;
-    const E* gg = G + (size_t)i * g.p;
-    float sa, sg;
-    if (vec_a && vec_g) {
-      // both rows at once: the loads of a and g are in flight together
-      constexpr int kVec = 16 / sizeof(E);
-      const int nva = g.d / kVec, nvg = g.p / kVec, nv = max(nva, nvg);
-      const uint4* av = reinterpret_cast<const uint4*>(a);
-      const uint4* gv = reinterpret_cast<const uint4*>(gg);
-      float xa = 0.f, xg = 0.f;
+  const int w0 = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (vec_a && vec_g) {
+    // Vector path: each warp takes two examples per pass (i and i + warps) and has the loads
+    // of both rows of both examples in flight together; the grid is capped, so warps pass
+    // over many examples instead of retiring after one.
+    constexpr int kVec = 16 / sizeof(E);
+    const int nva = g.d / kVec, nvg = g.p / kVec, nv = max(nva, nvg);
+    for (int i = w0; i < g.B; i += 2 * warps) {
+      const int i2 = i + warps;
+      const bool two = i2 < g.B;
+      const uint4* av = reinterpret_cast<const uint4*>(A + (size_t)i * g.d);
+      const uint4* gv = reinterpret_cast<const uint4*>(G + (size_t)i * g.p);
+      const uint4* av2 = reinterpret_cast<const uint4*>(A + (size_t)(two ? i2 : i) * g.d);
+      const uint4* gv2 = reinterpret_cast<const uint4*>(G + (size_t)(two ? i2 : i) * g.p);
+      float xa = 0.f, xg = 0.f, ya = 0.f, yg = 0.f;
 #pragma unroll 2
       for (int v = lane; v < nv; v += 32) {
-        uint4 wa = make_uint4(0u, 0u, 0u, 0u), wg = make_uint4(0u, 0u, 0u, 0u);
-        if (v < nva) wa = __ldg(av + v);
-        if (v < nvg) wg = __ldg(gv + v);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 wa = v < nva ? __ldg(av + v) : z, wg = v < nvg ? __ldg(gv + v) : z;
+        const uint4 wa2 = (two && v < nva) ? __ldg(av2 + v) : z, wg2 = (two && v < nvg) ? __ldg(gv2 + v) : z;
         const E* ea = reinterpret_cast<const E*>(&wa);
         const E* eg = reinterpret_cast<const E*>(&wg);
+        const E* ea2 = reinterpret_cast<const E*>(&wa2);
+        const E* eg2 = reinterpret_cast<const E*>(&wg2);
 #pragma unroll
         for (int q = 0; q < kVec; ++q) {
-          const float fa = to_f(ea[q]), fg = to_f(eg[q]);
+          const float fa = to_f(ea[q]), fg = to_f(eg[q]), fa2 = to_f(ea2[q]), fg2 = to_f(eg2[q]);
           xa = fmaf(fa, fa, xa);
           xg = fmaf(fg, fg, xg);
+          ya = fmaf(fa2, fa2, ya);
+          yg = fmaf(fg2, fg2, yg);
         }
       }
+      const E* a = A + (size_t)i * g.d;
+      const E* gg = G + (size_t)i * g.p;
       for (int j = nva * kVec + lane; j < g.d; j += 32) { const float f = to_f(a[j]); xa = fmaf(f, f, xa); }
       for (int j = nvg * kVec + lane; j < g.p; j += 32) { const float f = to_f(gg[j]); xg = fmaf(f, f, xg); }
-      sa = warp_sum(xa);
-      sg = warp_sum(xg);
-    } else {
-      sa = row_sqsum(a, g.d, lane, vec_a);
-      sg = row_sqsum(gg, g.p, lane, vec_g);
+      if (two) {
+        const E* a2 = A + (size_t)i2 * g.d;
+        const E* g2 = G + (size_t)i2 * g.p;
+        for (int j = nva * kVec + lane; j < g.d; j += 32) { const float f = to_f(a2[j]); ya = fmaf(f, f, ya); }
+        for (int j = nvg * kVec + lane; j < g.p; j += 32) { const float f = to_f(g2[j]); yg = fmaf(f, f, yg); }
+      }
+      const float sa = warp_sum(xa), sg = warp_sum(xg), ta = warp_sum(ya), tg = warp_sum(yg);
+      if (lane == 0) {
+        out[i] = sa * sg + (g.has_bias ? sg : 0.f);
+        if (two) out[i2] = ta * tg + (g.has_bias ? tg : 0.f);
+      }
     }
+    return;
+  }
+  for (int i = w0; i < g.B; i += warps) {
+    const E* a = A + (size_t)i * g.d;
+    const E* gg = G + (size_t)i * g.p;
+    const float sa = row_sqsum(a, g.d, lane, vec_a);
+    const float sg = row_sqsum(gg, g.p, lane, vec_g);
     if (lane == 0) out[i] = sa * sg + (g.has_bias ? sg : 0.f);
   }
 }
@@ -186,6 +209,33 @@ __device__ __forceinline__ void noise_block_store(float* __restrict__ grad, size
   }
 }
 
+// The common case, flat offset % 4 == 0 and grad 16-byte aligned, with fewer than 2^31
+// Philox blocks: block b covers grad[4b .. 4b+3], every block full but possibly the last;
+// 32-bit indices and no alignment tests per block (the pass is bound by its arithmetic).
+template <int NB>
+__global__ void __launch_bounds__(256) add_noise_aligned_kernel(float* __restrict__ grad, uint32_t n4, uint32_t tail,
+                                                                float sc, float invB, uint64_t seed, uint64_t q0,
+                                                                const unsigned long long* __restrict__ seed_dev) {
+  pdl_trigger();
+  pdl_wait();
+  if (seed_dev) seed = *seed_dev;
+  const PhiloxKey key = philox_key(seed);
+  const uint32_t nb = n4 + (tail ? 1u : 0u);          // blocks touched
+  const uint32_t stride = NB * gridDim.x * blockDim.x;
+  for (uint32_t b = NB * (blockIdx.x * blockDim.x + threadIdx.x); b < nb; b += stride) {
+    float4* g4 = reinterpret_cast<float4*>(grad) + b;
+    float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = xa;
+    if (b < n4) xa = __ldcs(g4);
+    if (NB == 2 && b + 1 < n4) xb = __ldcs(g4 + 1);
+    float za[4], zb[4];
+    normal4(q0 + b, key, 0u, za);
+    if (NB == 2) normal4(q0 + b + 1, key, 0u, zb);
+    const size_t n = (size_t)n4 * 4 + tail;
+    noise_block_store(grad, n, (int64_t)b * 4, b < n4, xa, za, sc, invB);
+    if (NB == 2 && b + 1 < nb) noise_block_store(grad, n, (int64_t)(b + 1) * 4, b + 1 < n4, xb, zb, sc, invB);
+  }
+}
+
 template <int NB>
 __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad, size_t n, float sc,
                                                         float invB, uint64_t seed, uint64_t offset,
@@ -193,6 +243,7 @@ __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad
   pdl_trigger();
   pdl_wait();
   if (seed_dev) seed = *seed_dev;
+  const PhiloxKey key = philox_key(seed);
   const uint64_t q0 = offset >> 2;
   const uint64_t q1 = (offset + n + 3) >> 2;  // one past the last block touched
   const uint64_t stride = NB * (uint64_t)gridDim.x * blockDim.x;
@@ -207,8 +258,8 @@ __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad
     if (va) xa = __ldcs(reinterpret_cast<const float4*>(grad + ja));
     if (vb) xb = __ldcs(reinterpret_cast<const float4*>(grad + jb));
     float za[4], zb[4];
-    normal4(qa, seed, 0u, za);
-    if (NB == 2) normal4(qb, seed, 0u, zb);
+    normal4(qa, key, 0u, za);
+    if (NB == 2) normal4(qb, key, 0u, zb);
     noise_block_store(grad, n, ja, va, xa, za, sc, invB);
     if (has_b) noise_block_store(grad, n, jb, vb, xb, zb, sc, invB);
   }
@@ -255,7 +306,8 @@ using namespace dpk;
 cudaError_t launch_t1_norm(const Geom& g, int dtype, const void* A, const void* G, float* out,
                            cudaStream_t s) {
   const int warps_per_block = 8;
-  const int blocks = (g.B + warps_per_block - 1) / warps_per_block;
+  // about eight resident blocks per SM; warps then pass over many examples
+  const int blocks = std::min((g.B + warps_per_block - 1) / warps_per_block, 152 * 8);
   const size_t es = dtype == DP_FP32 ? 4 : 2;
   const bool va = ((reinterpret_cast<uintptr_t>(A) & 15u) == 0) && ((g.d * es) % 16 == 0);
   const bool vg = ((reinterpret_cast<uintptr_t>(G) & 15u) == 0) && ((g.p * es) % 16 == 0);
@@ -289,10 +341,21 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
   uint64_t grid = (blocks4 + (two ? 511 : 255)) / (two ? 512 : 256);
   if (grid > cap) grid = cap;
   if (grid == 0) grid = 1;
-  if (two)
+  const bool aligned = (offset & 3) == 0 && (reinterpret_cast<uintptr_t>(grad) & 15u) == 0 &&
+                       blocks4 < ((uint64_t)1 << 31) - 2;
+  if (aligned) {
+    const uint32_t n4 = (uint32_t)(n >> 2), tail = (uint32_t)(n & 3);
+    if (two)
+      launch_pdl(add_noise_aligned_kernel<2>, (unsigned)grid, 256, 0, s, grad, n4, tail, sc, invB, seed, offset >> 2,
+                 seed_dev);
+    else
+      launch_pdl(add_noise_aligned_kernel<1>, (unsigned)grid, 256, 0, s, grad, n4, tail, sc, invB, seed, offset >> 2,
+                 seed_dev);
+  } else if (two) {
     launch_pdl(add_noise_kernel<2>, (unsigned)grid, 256, 0, s, grad, n, sc, invB, seed, offset, seed_dev);
-  else
+  } else {
     launch_pdl(add_noise_kernel<1>, (unsigned)grid, 256, 0, s, grad, n, sc, invB, seed, offset, seed_dev);
+  }
   return cudaGetLastError();
 }
 

@@ -234,6 +234,22 @@ def test_edge_shapes(lib, tag, spec, B, dtype):
         _check_layer(lib, spec, wl, mode=mode)
 
 
+@pytest.mark.parametrize("B,d,p", [(25001, 64, 48), (19457, 40, 24)], ids=["B25001", "B19457_short_rows"])
+def test_t1_norm_many_examples(lib, B, d, p):
+    """One-row norms over more examples than the capped grid has warps (each warp takes two
+    examples per pass; an odd count leaves the last pass with one)."""
+    import torch
+    spec = LayerSpec("e", "linear", p=p, d=d, T=1)
+    wl = Workload(name="t1_many", B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=43)
+    A, G = workloads.layer_inputs(wl, 0, threads=8)
+    desc = desc_for(lib, spec, B, "bf16")
+    sq = torch.full((B,), float("nan"), device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    assert lib.dp_layer_sqnorms(desc, to_dev(A, "bf16"), to_dev(G, "bf16"), sq, ws) == lib.DP_NORM_T1
+    torch.cuda.synchronize()
+    assert rel_elem(sq.cpu().numpy(), oracle.layer_sqnorms(spec, A, G)) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("B,accumulate", [(300, False), (257, True)], ids=["B300", "B257_accumulate"])
 def test_bias_shared_across_column_tiles(lib, B, accumulate):
     """A layer whose examples split over clusters with B >= 256: every column tile sums the
@@ -522,7 +538,8 @@ def test_nonfinite_norm_zeroes_factor_and_raises_status(lib):
 
 # ----------------------------------------------------------------- noise and adaptive bound
 
-@pytest.mark.parametrize("n,offset", [(1, 0), (3, 5), (7, 2), (1000, 0), (1001, 13), (1 << 20, 3)])
+@pytest.mark.parametrize("n,offset", [(1, 0), (3, 5), (7, 2), (1000, 0), (1001, 13), (1 << 20, 3), (1002, 8),
+                                      (3 << 20, 4), ((3 << 20) + 3, 12)])
 def test_noise_matches_oracle_definition(lib, n, offset):
     import torch
     seed = 0x1234_5678_9ABC
