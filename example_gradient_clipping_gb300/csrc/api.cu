@@ -175,7 +175,8 @@ size_t padded_out_bytes(const Geom& g) {
 
 // Clipped-sum kernel: 0 SIMT, 1 row-scaled tensor-core GEMM, 2 per-example tensor-core
 // accumulation (single CTA), 3 per-example conv kernel with TMA im2col loads, 4 the
-// row-scaled GEMM with im2col loads, 5 the one-row outer-product sum.  The per-example
+// row-scaled GEMM with im2col loads, 5 the one-row outer-product sum, 7 the on-chip unfold
+// kernel of narrow conv layers.  The per-example
 // kernels split the examples over clusters or the grid; the row-scaled GEMM splits the
 // batch rows over the whole grid.
 struct Plan {
@@ -223,6 +224,11 @@ bool im2col_inputs(const Geom& g, int dtype, const void* A, const void* G, const
 bool use_tc_conv(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
   return im2col_inputs(g, dtype, A, G, ws) && dph::tc_conv_supported(g);
 }
+// Conv layers with at most 64 unfolded columns (plus bias) form their unfold on chip and
+// read G as it lies (DPCLIP_CONV=rows keeps them on the written-out row layout).
+bool use_tc_unfold(const Geom& g, int dtype, const void* G) {
+  return g.conv && dtype == DP_BF16 && aligned16(G) && !conv_rows_pinned() && dph::tc_unfold_supported(g);
+}
 
 // Conv clipped sums with im2col loads: per-example TMEM products (fp32 scaling) when an
 // example has at least 128 rows, else the row-scaled GEMM (many examples per stage).
@@ -234,6 +240,7 @@ bool use_t1_sum(const Geom& g, int dtype) {
 Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
   Plan pl{0, false, g};
   if (use_t1_sum(g, dtype)) return Plan{5, false, g};
+  if (!pinned_sum_kernel() && use_tc_unfold(g, dtype, G)) return Plan{7, false, g};
   if (!pinned_sum_kernel() && im2col_inputs(g, dtype, A, G, ws)) {
     if (g.T >= 128 && dph::tc_conv_supported(g)) return Plan{3, false, g};
     if (dph::tc_sum_conv_supported(g)) return Plan{4, false, g};
@@ -245,10 +252,11 @@ Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void
   return pl;
 }
 
-enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST, NK_TC_CONV, NK_TC_GHOST_CONV };
+enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST, NK_TC_CONV, NK_TC_GHOST_CONV, NK_TC_UNFOLD };
 
 Plan norm_plan(const Geom& g, int mode, int dtype, const void* A, const void* G, const void* ws) {
   if (mode == DP_NORM_T1) return Plan{NK_T1, false, g};
+  if (mode == DP_NORM_INSTANTIATE && use_tc_unfold(g, dtype, G)) return Plan{NK_TC_UNFOLD, false, g};
   if (mode == DP_NORM_INSTANTIATE && use_tc_conv(g, dtype, A, G, ws)) return Plan{NK_TC_CONV, false, g};
   if (mode == DP_NORM_GHOST && im2col_inputs(g, dtype, A, G, ws) && dph::tc_ghost_conv_supported(g))
     return Plan{NK_TC_GHOST_CONV, false, g};
@@ -268,7 +276,8 @@ size_t simt_sum_bytes(const Geom& g) {
 size_t sum_ws_bytes(const Geom& g, const Plan& pl) {
   const Geom& lg = pl.lg;
   // a conv layer's row-scaled GEMM reads pre-scaled rows; its bias is summed separately
-  const size_t inner = pl.kernel == 5   ? dph::t1_sum_ws_bytes(g)
+  const size_t inner = pl.kernel == 7   ? dph::tc_unfold_ws_bytes(g, false)
+                       : pl.kernel == 5 ? dph::t1_sum_ws_bytes(g)
                        : pl.kernel == 4 ? dph::tc_sum_conv_ws_bytes(g)
                        : pl.kernel == 3 ? dph::tc_conv_ws_bytes(g, false)
                        : pl.kernel == 2 ? dph::tc_sumx_ws_bytes(lg)
@@ -288,6 +297,7 @@ size_t norm_ws_bytes(const Geom& g, const Plan& pl) {
     case NK_TC_INST: inner = dph::tc_inst_ws_bytes(pl.lg); break;
     case NK_TC_CONV: inner = dph::tc_conv_ws_bytes(g, true); break;
     case NK_TC_GHOST_CONV: inner = dph::tc_ghost_conv_ws_bytes(g); break;
+    case NK_TC_UNFOLD: inner = dph::tc_unfold_ws_bytes(g, true); break;
   }
   return (pl.rows ? rows_bytes(g) : 0) + inner;
 }
@@ -300,13 +310,16 @@ static const char kAlignedProbe[16] __attribute__((aligned(16))) = {};
 bool keep_plan(int dtype, const Geom& g, const void* A, const void* G, const void* ws, Plan* pl) {
   if (dtype != DP_BF16 || g.T == 1) return false;
   *pl = norm_plan(g, DP_NORM_INSTANTIATE, dtype, A, G, ws);
-  return pl->kernel == NK_TC_CONV || pl->kernel == NK_TC_INST;
+  return pl->kernel == NK_TC_CONV || pl->kernel == NK_TC_INST || pl->kernel == NK_TC_UNFOLD;
 }
 bool keep_plan(int dtype, const Geom& g, Plan* pl) {
   return keep_plan(dtype, g, kAlignedProbe, kAlignedProbe, kAlignedProbe, pl);
 }
-// Columns of each kept gradient (conv tile columns = D; rows of a padded conv layer = Dp).
-int kept_width(const Geom& g, const Plan& pl) { return pl.kernel == NK_TC_CONV ? g.D : pl.lg.D; }
+// Columns of each kept gradient (conv tile columns or the on-chip unfold's weight layout = D;
+// rows of a padded conv layer = Dp).
+int kept_width(const Geom& g, const Plan& pl) {
+  return pl.kernel == NK_TC_CONV || pl.kernel == NK_TC_UNFOLD ? g.D : pl.lg.D;
+}
 size_t kept_sum_need(const Geom& g, const Plan& pl) {
   return dph::kept_sum_ws_bytes(g.B, g.p, kept_width(g, pl)) + (pl.rows ? padded_out_bytes(g) : 0);
 }
@@ -437,6 +450,7 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
       break;
     case NK_TC_CONV: e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_TC_GHOST_CONV: e = dph::launch_tc_ghost_conv(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
+    case NK_TC_UNFOLD: e = dph::launch_tc_unfold_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_SIMT_GHOST: e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
     case NK_SIMT_INST: e = dph::launch_simt_inst(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
   }
@@ -544,7 +558,9 @@ static dp_status clipped_sum_impl(const dp_layer_desc* desc, const void* A, cons
     kacc = 0;
     wsp = static_cast<uint8_t*>(wsp) + padded_out_bytes(g);
   }
-  if (pl.kernel == 5)
+  if (pl.kernel == 7)
+    e = dph::launch_tc_unfold_sum(g, A, G, factors, dW, db, accumulate, wsp, status_ptr(), stream, nz);
+  else if (pl.kernel == 5)
     e = dph::launch_t1_sum(g, desc->dtype, A, G, factors, dW, db, accumulate, static_cast<float*>(wsp), stream, nz);
   else if (pl.kernel == 4 || pl.kernel == 3) {
     const bool xh = reuse_norm_mode >= 0 && norm_leaves_nhwc(g, reuse_norm_mode, desc->dtype, A, G, workspace);
@@ -607,6 +623,8 @@ dp_status dp_layer_sqnorms_keep(const dp_layer_desc* desc, const void* A, const 
   float* keep_b = g.has_bias ? grads + (size_t)g.B * g.p * kept_width(g, pl) : nullptr;
   if (pl.kernel == NK_TC_CONV)
     e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, wsp, status_ptr(), stream, grads, keep_b);
+  else if (pl.kernel == NK_TC_UNFOLD)
+    e = dph::launch_tc_unfold_norm(g, A, G, sqnorm_out, wsp, status_ptr(), stream, grads, keep_b);
   else
     e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, static_cast<float*>(wsp), status_ptr(), stream, grads, keep_b,
                             !pl.rows);

@@ -440,11 +440,17 @@ cudaError_t launch_reduce_splits2(SplitSeg a, SplitSeg b, int splits, int accumu
                                   NoiseArgs* nz) {
   if (!b.out) b.n = 0;
   const bool noise = nz && nz->on;
-  if (!noise && splits >= 16 && std::max(a.n, b.n) <= ((size_t)1 << 16)) {
-    // many splits of short vectors: the warp- and block-per-element kernels (packed layouts)
-    cudaError_t e = launch_reduce_splits(a.ws, splits, a.n, a.out, accumulate, s);
+  if (splits >= 16 && std::max(a.n, b.n) <= ((size_t)1 << 16)) {
+    // many splits of short vectors: the warp- and block-per-element kernels (packed layouts),
+    // with or without the noise, so that a noised call sums in the same order as a plain one
+    cudaError_t e = launch_reduce_splits(a.ws, splits, a.n, a.out, accumulate, s, nz, noise ? nz->off_a : 0);
+    if (noise) nz->applied_a = 1;
     if (e != cudaSuccess || !b.n) return e;
-    if (b.stride == b.n) return launch_reduce_splits(b.ws, splits, b.n, b.out, accumulate, s);
+    if (b.stride == b.n) {
+      e = launch_reduce_splits(b.ws, splits, b.n, b.out, accumulate, s, nz, noise ? nz->off_b : 0);
+      if (noise) nz->applied_b = 1;
+      return e;
+    }
     a.n = 0;   // a strided bias segment: the kernel below takes it alone
   }
   auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15) == 0; };

@@ -38,6 +38,17 @@ cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep,
                             dpk::NoiseArgs* nz = nullptr);
 // Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
+// Conv layers whose unfolded width plus bias is at most 64 (first layers over a few input
+// channels): the unfold formed on chip from the example's input, G read as it lies.
+bool tc_unfold_supported(const Geom& g);
+size_t tc_unfold_ws_bytes(const Geom& g, bool norm);
+// ||g_i||^2 -> out [B]; with `keep`, g_i [B, p, D] (weight layout) and b_i [B, p] as well.
+cudaError_t launch_tc_unfold_norm(const Geom& g, const void* A, const void* G, float* out, void* ws,
+                                  unsigned* status, cudaStream_t s, float* keep = nullptr, float* keep_b = nullptr);
+// dW (+)= sum_i c_i g_i, db (+)= sum_i c_i b_i (example splits summed in a fixed order).
+cudaError_t launch_tc_unfold_sum(const Geom& g, const void* A, const void* G, const float* factors, float* dW,
+                                 float* db, int accumulate, void* ws, unsigned* status, cudaStream_t s,
+                                 dpk::NoiseArgs* nz = nullptr);
 // Ghost norm from per-example Gram tiles (bf16 in, fp32 accumulate).
 bool tc_ghost_supported(const Geom& g);
 size_t tc_ghost_ws_bytes(const Geom& g);
@@ -97,7 +108,8 @@ cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, fl
                                  unsigned* status, cudaStream_t s);
 // dW[j, m] (+)= Wp[j, m] for j < p, m < D (Wp rows of Dp floats).
 cudaError_t launch_compact_cols(const float* Wp, int p, int D, int Dp, float* dW, int accumulate, cudaStream_t s);
-// 2D/3D bf16 tensor map with 128-byte swizzle (dims innermost first, strides in bytes).
+// 2D/3D bf16 tensor map (dims innermost first, strides in bytes), 128-byte swizzle unless
+// `swizzle` is false; elements outside the tensor read as zero.
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box);
+                      const uint64_t* strides_bytes, const uint32_t* box, bool swizzle = true);
 }  // namespace dph

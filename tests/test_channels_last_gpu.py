@@ -24,7 +24,8 @@ CASES = [
     ("im2col_s2_dil2_nobias", LayerSpec("e", "conv2d", p=136, Cin=128, H=23, W=23, k=3, stride=2, pad=2, dil=2,
                                         has_bias=False), 2, "bf16"),
     ("rows_smem", LayerSpec("e", "conv2d", p=64, Cin=16, H=12, W=12, k=3, pad=1), 4, "bf16"),
-    ("rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16"),
+    ("rows_padD", LayerSpec("e", "conv2d", p=64, Cin=9, H=12, W=12, k=3, pad=1), 4, "bf16"),
+    ("unfold_on_chip", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16"),
     ("rows_global_unfold", LayerSpec("e", "conv2d", p=16, Cin=48, H=48, W=48, k=3, pad=1), 2, "bf16"),
     ("ffma_bf16", LayerSpec("e", "conv2d", p=6, Cin=5, H=9, W=8, k=3, stride=2, pad=1), 3, "bf16"),
     ("ffma_fp32", LayerSpec("e", "conv2d", p=4, Cin=3, H=10, W=10, k=3, pad=2, dil=2), 2, "fp32"),
@@ -69,7 +70,8 @@ def test_channels_last_norms_and_sums(lib, tag, spec, B, dtype):
 
 @pytest.mark.parametrize("tag,spec,B", [
     ("im2col_T144", LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 3),
-    ("rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4)])
+    ("rows_padD", LayerSpec("e", "conv2d", p=64, Cin=9, H=12, W=12, k=3, pad=1), 4),
+    ("unfold_on_chip", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4)])
 def test_channels_last_kept_gradients(lib, tag, spec, B):
     import torch
     dp = lib

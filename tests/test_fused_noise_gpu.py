@@ -29,7 +29,11 @@ CASES = [
     ("conv_im2col_rowscaled_cl", LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=3, pad=1), 4, "bf16", True,
      False),
     # padded unfolded width: the weights get their noise after the compaction
-    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16", False, False),
+    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=9, H=12, W=12, k=3, pad=1), 4, "bf16", False, False),
+    # on-chip unfold of a narrow conv layer: fused with example splits, a noise pass with one
+    ("conv_unfold", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16", False, True),
+    ("conv_unfold_one_split", LayerSpec("e", "conv2d", p=64, Cin=3, H=16, W=16, k=3, pad=1), 1, "bf16", False,
+     False),
     ("ffma_small", LayerSpec("e", "linear", p=6, d=10, T=5), 4, "fp32", False, False),
 ]
 

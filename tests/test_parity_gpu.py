@@ -189,7 +189,9 @@ EDGE = [
     ("conv_rows_k1_nobias", LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=1, has_bias=False), 4, "bf16"),
     ("conv_rows_p8", LayerSpec("e", "conv2d", p=8, Cin=8, H=5, W=7, k=3, pad=1), 3, "bf16"),
     # D = 27 padded to 32 columns in the row layout (the first VGG-11 layer's shape)
-    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16"),
+    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=9, H=12, W=12, k=3, pad=1), 4, "bf16"),
+    # narrow conv layers: the unfold formed on chip (per-element gathers: Wout % 8 != 0)
+    ("conv_unfold_12x12", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4, "bf16"),
     ("conv_rows_padD_s2", LayerSpec("e", "conv2d", p=24, Cin=5, H=13, W=11, k=3, stride=2, pad=1), 3, "bf16"),
     # conv layers whose unfold is done by TMA im2col loads (Cin % 64 == 0, T % 8 == 0, T >= 64)
     ("conv_im2col_3x3", LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 3, "bf16"),
@@ -303,7 +305,8 @@ ACC = [(LayerSpec("e", "linear", p=42, d=72, T=9), 6),          # SIMT (p not a 
        (LayerSpec("e", "linear", p=128, d=64, T=40), 5),         # row-scaled tensor-core GEMM
        (LayerSpec("e", "linear", p=128, d=128, T=64), 4),        # per-example, several splits
        (LayerSpec("e", "linear", p=64, d=256, T=80), 1),         # per-example, one split
-       (LayerSpec("e", "conv2d", p=16, Cin=3, H=8, W=8, k=3, pad=1), 3),   # conv, padded columns
+       (LayerSpec("e", "conv2d", p=16, Cin=9, H=8, W=8, k=3, pad=1), 3),   # conv, padded columns
+       (LayerSpec("e", "conv2d", p=64, Cin=3, H=8, W=8, k=3, pad=1), 1),   # conv, on-chip unfold, one split
        (LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=3, pad=1), 3),  # conv, im2col row-scaled
        (LayerSpec("e", "conv2d", p=72, Cin=64, H=12, W=12, k=3, pad=1), 2),  # conv, im2col per example
        (LayerSpec("e", "linear", p=10, d=13, T=1), 300),                   # one row, 3 example splits
@@ -312,11 +315,11 @@ ACC = [(LayerSpec("e", "linear", p=42, d=72, T=9), 6),          # SIMT (p not a 
        (LayerSpec("e", "linear", p=512, d=256, T=70), 11)]                 # per-example, bias, splits
 
 
-ACC_PIN = ["", "rows", "example", "example", "", "", "", "", "example", "example", "example"]
+ACC_PIN = ["", "rows", "example", "example", "", "", "", "", "", "example", "example", "example"]
 
 
 @pytest.mark.parametrize("spec,B,pin", [(s, b, p) for (s, b), p in zip(ACC, ACC_PIN)],
-                         ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single", "conv_padded",
+                         ids=["simt", "tc_rows", "tc_ex_splits", "tc_ex_single", "conv_padded", "conv_unfold_direct",
                               "conv_im2col_rows", "conv_im2col_example", "t1_splits", "tc_ex_grid",
                               "tc_ex_256_single", "tc_ex_tail_splits"])
 def test_accumulate_adds_to_existing_sum(lib, spec, B, pin, monkeypatch):
@@ -401,7 +404,7 @@ KEPT = [
     ("conv_im2col_s2_dil2_nobias", LayerSpec("e", "conv2d", p=136, Cin=128, H=23, W=23, k=3, stride=2, pad=2, dil=2,
                                              has_bias=False), 2),
     ("linear", LayerSpec("e", "linear", p=136, d=200, T=70), 5),
-    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=3, H=12, W=12, k=3, pad=1), 4),
+    ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=9, H=12, W=12, k=3, pad=1), 4),
 ]
 
 
@@ -414,7 +417,7 @@ def test_kept_gradients_norm_and_sum(lib, tag, spec, B):
     fac = workloads.factor_inputs(wl, B)
     desc = desc_for(dp, spec, B, "bf16")
     nbytes = dp.dp_grads_size(desc)
-    width = 32 if tag == "conv_rows_padD" else spec.D      # the padded row layout keeps 27 -> 32 columns
+    width = 88 if tag == "conv_rows_padD" else spec.D      # the padded row layout keeps 81 -> 88 columns
     assert nbytes == 4 * B * spec.p * width + (4 * B * spec.p if spec.has_bias else 0)
     grads = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
     ws = torch.empty(dp.dp_workspace_size(desc, dp.DP_NORM_INSTANTIATE), dtype=torch.uint8, device="cuda")
