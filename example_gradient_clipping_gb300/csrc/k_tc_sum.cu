@@ -16,6 +16,10 @@
 //              clip factor (zero outside the CTA's rows) and accumulate the bias sums;
 //              then the epilogue: TMEM -> registers -> fp32 partial tile.
 // Partials [split, p, d] are reduced in a fixed order (deterministic) by a second kernel.
+// Wide tiles (rows already scaled, p >= 256): 256 x 256 per CTA as two M = 128 accumulators
+// in TMEM sharing each stage's A boxes, so a CTA reads 64 KB per 64 rows for twice the MMA
+// work of a 48 KB narrow stage (the TMA delivery into an SM, not the tensor core, bounds
+// the narrow tile).
 #include <algorithm>
 #include <cudaTypedefs.h>
 
@@ -25,15 +29,19 @@
 namespace dpk {
 namespace tcsum {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int G_TILE = BM * BK * 2;            // 16 KB: two 64-column boxes
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_TILE = BN * BK * 2;            // 32 KB: four 64-column boxes
 constexpr int BOX = 64 * BK * 2;               // 8 KB
-constexpr int STAGE = G_TILE + A_TILE;
 constexpr int kThreads = 224;
 constexpr int PSTR = BN + 4;                   // staged output row stride (floats)
-static_assert(BM * PSTR * 4 <= STAGES * (BM * BK * 2 + BN * BK * 2), "staging fits in the stage buffers");
-constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+template <bool kWide> struct Cfg {
+  static constexpr int TM = kWide ? 2 * BM : BM;          // output rows per CTA
+  static constexpr int STAGES = kWide ? 3 : 4;
+  static constexpr int G_TILE = TM * BK * 2;              // 16 KB (two boxes) or 32 KB (four)
+  static constexpr int STAGE = G_TILE + A_TILE;
+  static constexpr int SMEM = STAGES * STAGE + 1024 + 256;
+  static_assert(BM * PSTR * 4 <= STAGES * STAGE, "staging fits in the stage buffers");
+};
 
 struct Params {
   const float* factors;
@@ -65,9 +73,12 @@ __device__ __forceinline__ void load_a_block(const Params& P, const CUtensorMap*
                           (uint16_t)(kw * P.dil), (uint16_t)(kh * P.dil));
 }
 
+template <bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapA,
               Params P) {
+  using C = Cfg<kWide>;
+  constexpr int STAGES = C::STAGES, STAGE = C::STAGE, G_TILE = C::G_TILE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
@@ -78,7 +89,7 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN, split = blockIdx.z;
+  const int m0 = blockIdx.x * C::TM, n0 = blockIdx.y * BN, split = blockIdx.z;
   const long r0 = (long)split * P.rows_per_split;
   const long r1 = min(P.R, r0 + P.rows_per_split);
   const int nk = (int)((r1 - r0 + BK - 1) / BK);
@@ -95,7 +106,7 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
     ptx::prefetch_tensormap(&mapG);
     ptx::prefetch_tensormap(&mapA);
   }
-  if (warp == 1) ptx::tmem_alloc(tmem_slot, 256);
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, kWide ? 512 : 256);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -104,7 +115,8 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
   pdl_wait();      // the previous kernel has completed; its writes are visible
 
   // boxes inside the layer: G boxes along p, A boxes along D; MMA width N along D
-  const int ng = min(2, (P.p - m0 + 63) / 64), na = min(4, (P.d - n0 + 63) / 64);
+  const int ng = min(C::TM / 64, (P.p - m0 + 63) / 64), na = min(4, (P.d - n0 + 63) / 64);
+  const int nacc = (ng + 1) / 2;   // accumulators with rows inside p (1, or 2 for wide tiles)
   const int n_mma = min(BN, (P.d - n0 + 15) / 16 * 16);
   if (warp == 0 || warp == 6) {
     // TMA producers (whole warp; the elected lane issues); producer pr loads stages k % 2 == pr
@@ -142,8 +154,13 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
       const uint32_t idesc = ptx::idesc_bf16_f32(BM, n_mma, 1, 1);
       if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
+        for (int kk = 0; kk < BK / 16; ++kk) {
           ptx::umma_bf16(tmem, ptx::sdesc_add(da, kk * 2048), ptx::sdesc_add(db, kk * 2048), idesc, (k | kk) != 0);
+          // the second accumulator: G boxes 2 and 3 (outputs m0+128 ..), the same A boxes
+          if (kWide && nacc > 1)
+            ptx::umma_bf16(tmem + 256, ptx::sdesc_add(da, 2 * BOX + kk * 2048),
+                           ptx::sdesc_add(db, kk * 2048), idesc, (k | kk) != 0);
+        }
         ptx::umma_commit(&empty[s]);
       }
       __syncwarp();
@@ -215,35 +232,39 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     float* stg = reinterpret_cast<float*>(smem);
-    if (__all_sync(0xffffffffu, w)) {
-      ptx::tc_fence_after();
+    const bool got = __all_sync(0xffffffffu, w);
+    for (int h = 0; h < nacc; ++h) {
+      if (h > 0) asm volatile("bar.sync 1, 128;" ::: "memory");   // the staging tile is free again
+      if (got) {
+        ptx::tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < (n_mma + 31) / 32; ++c) {
-        float v[32];
-        ptx::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
-        ptx::tmem_wait_ld();
+        for (int c = 0; c < (n_mma + 31) / 32; ++c) {
+          float v[32];
+          ptx::tmem_ld32(tmem + h * 256 + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(stg + row * PSTR + c * 32 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(stg + row * PSTR + c * 32 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
       }
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-    if (!*abort) {
-      const int t = threadIdx.x - 64, nc4 = (n_mma + 3) / 4;
-      const bool vec = (P.d & 3) == 0;
-      for (int item = t; item < BM * nc4; item += 128) {
-        const int r = item / nc4, c4 = item - r * nc4;
-        const int m = m0 + r, n = n0 + c4 * 4;
-        if (m >= P.p) continue;
-        const float4 o = *reinterpret_cast<const float4*>(stg + r * PSTR + c4 * 4);
-        float* out = P.ws + ((size_t)split * P.p + m) * P.d + n;
-        if (vec && n + 4 <= P.d) {
-          *reinterpret_cast<float4*>(out) = o;
-        } else {
-          const float ov[4] = {o.x, o.y, o.z, o.w};
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+      if (!*abort) {
+        const int t = threadIdx.x - 64, nc4 = (n_mma + 3) / 4;
+        const bool vec = (P.d & 3) == 0;
+        for (int item = t; item < BM * nc4; item += 128) {
+          const int r = item / nc4, c4 = item - r * nc4;
+          const int m = m0 + h * BM + r, n = n0 + c4 * 4;
+          if (m >= P.p) continue;
+          const float4 o = *reinterpret_cast<const float4*>(stg + r * PSTR + c4 * 4);
+          float* out = P.ws + ((size_t)split * P.p + m) * P.d + n;
+          if (vec && n + 4 <= P.d) {
+            *reinterpret_cast<float4*>(out) = o;
+          } else {
+            const float ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (n + q < P.d) out[q] = ov[q];
+            for (int q = 0; q < 4; ++q)
+              if (n + q < P.d) out[q] = ov[q];
+          }
         }
       }
     }
@@ -255,7 +276,7 @@ tc_sum_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ 
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 256);
+    ptx::tmem_dealloc(tmem, kWide ? 512 : 256);
   }
 }
 
@@ -301,8 +322,21 @@ static int cdiv_i(long a, long b) { return (int)((a + b - 1) / b); }
 
 // Split of the batch rows over CTAs: enough splits to cover the SMs with output
 // tiles, each split a whole number of 64-row stages and every split non-empty.
-static void tc_sum_split(const Geom& g, int* splits_out, long* rows_per_split) {
-  const long tiles = (long)cdiv_i(g.p, tcsum::BM) * cdiv_i(g.D, tcsum::BN);
+static void tc_sum_split(const Geom& g, int* splits_out, long* rows_per_split, bool wide = false);
+
+// Wide tiles for rows that arrive scaled (the conv row layout) when p fills them and each
+// CTA still runs at least 24 stages (with fewer, the two accumulators' drains outweigh the
+// saved loads: VGG-11's 2x2 layers ran 10% slower wide, its 8x8 and 4x4 layers 6-19% faster).
+static bool tc_sum_wide(const Geom& g, bool prescaled) {
+  if (!prescaled || g.p < 256) return false;
+  int splits;
+  long rps;
+  tc_sum_split(g, &splits, &rps, true);
+  return rps >= 24 * tcsum::BK;
+}
+
+static void tc_sum_split(const Geom& g, int* splits_out, long* rows_per_split, bool wide) {
+  const long tiles = (long)cdiv_i(g.p, wide ? 2 * tcsum::BM : tcsum::BM) * cdiv_i(g.D, tcsum::BN);
   const long R = (long)g.B * g.T;
   long splits = std::max<long>(1, 152 / tiles);
   splits = std::min<long>(splits, std::max<long>(1, R / (4 * tcsum::BK)));
@@ -312,11 +346,13 @@ static void tc_sum_split(const Geom& g, int* splits_out, long* rows_per_split) {
   *rows_per_split = rps;
 }
 
+// Splits of either tile width (the workspace covers both).
 static int tc_sum_splits(const Geom& g) {
-  int s;
+  int s, sw;
   long rps;
-  tc_sum_split(g, &s, &rps);
-  return s;
+  tc_sum_split(g, &s, &rps, false);
+  tc_sum_split(g, &sw, &rps, true);
+  return std::max(s, sw);
 }
 
 bool tc_sum_supported(const Geom& g) {
@@ -408,9 +444,10 @@ static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtens
                               float* dW, float* db, int accumulate, float* ws, unsigned* status, cudaStream_t s,
                               bool prescaled, NoiseArgs* nz) {
   const long R = (long)g.B * g.T;
+  const bool wide = tc_sum_wide(g, prescaled);
   int splits;
   long rps;
-  tc_sum_split(g, &splits, &rps);
+  tc_sum_split(g, &splits, &rps, wide);
   tcsum::Params P;
   P.factors = factors;
   P.ws = ws;
@@ -430,15 +467,18 @@ static cudaError_t run_tc_sum(const Geom& g, const CUtensorMap& mg, const CUtens
   P.dil = g.dil;
   int dev = 0;
   cudaGetDevice(&dev);
-  static bool attr_set[64] = {};
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tcsum::tc_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tcsum::SMEM);
+  static bool attr_set[64][2] = {};
+  if (dev >= 0 && dev < 64 && !attr_set[dev][wide]) {
+    cudaError_t e = wide ? cudaFuncSetAttribute(tcsum::tc_sum_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                tcsum::Cfg<true>::SMEM)
+                         : cudaFuncSetAttribute(tcsum::tc_sum_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                tcsum::Cfg<false>::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev][wide] = true;
   }
-  dim3 grid(cdiv_i(g.p, tcsum::BM), cdiv_i(g.D, tcsum::BN), splits);
-  launch_pdl(tcsum::tc_sum_kernel, grid, tcsum::kThreads, tcsum::SMEM, s, mg, ma, P);
+  dim3 grid(cdiv_i(g.p, wide ? 2 * tcsum::BM : tcsum::BM), cdiv_i(g.D, tcsum::BN), splits);
+  if (wide) launch_pdl(tcsum::tc_sum_kernel<true>, grid, tcsum::kThreads, tcsum::Cfg<true>::SMEM, s, mg, ma, P);
+  else launch_pdl(tcsum::tc_sum_kernel<false>, grid, tcsum::kThreads, tcsum::Cfg<false>::SMEM, s, mg, ma, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (!g.conv) {

@@ -301,6 +301,31 @@ def test_conv_rows_sum_kernels(lib, pin, monkeypatch):
     _check_layer(lib, spec, wl)
 
 
+@pytest.mark.parametrize("p,has_bias", [(320, True), (448, False)], ids=["p320_one_acc_tail", "p448_three_boxes"])
+def test_conv_rowscaled_wide_tiles(lib, p, has_bias):
+    """The row-scaled conv GEMM with 256-output tiles (two TMEM accumulators sharing each
+    stage's unfolded columns): enough batch rows per CTA to take them, a last output tile
+    with one accumulator (320 = 256 + 64) or with three of its four G boxes (448)."""
+    import torch
+    dp = lib
+    spec = LayerSpec("e", "conv2d", p=p, Cin=64, H=8, W=8, k=3, pad=1, has_bias=has_bias, a_dist="abs_normal")
+    B = 640
+    wl = Workload(name="wide", B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=41)
+    A, G = workloads.layer_inputs(wl, 0)
+    fac = workloads.factor_inputs(wl, B, 0.1, 1.0)
+    desc = desc_for(dp, spec, B, "bf16")
+    ws = torch.empty(dp.dp_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    Ad, Gd = to_dev(A, "bf16"), to_dev(G, "bf16")
+    dW = torch.full((spec.p * spec.D,), float("nan"), device="cuda")
+    db = torch.full((spec.p,), float("nan"), device="cuda") if has_bias else None
+    dp.dp_clipped_sum(desc, Ad, Gd, torch.tensor(fac, device="cuda"), dW, db, ws)
+    torch.cuda.synchronize()
+    S, Sb = oracle.clipped_sum(spec, A, G, fac.astype(np.float64))
+    assert rel_rows(dW.cpu().numpy(), S, spec.D) <= TOL["bf16"]
+    if has_bias:
+        assert rel_rows(db.cpu().numpy(), Sb) <= TOL["bf16"]
+
+
 ACC = [(LayerSpec("e", "linear", p=42, d=72, T=9), 6),          # SIMT (p not a multiple of 8)
        (LayerSpec("e", "linear", p=128, d=64, T=40), 5),         # row-scaled tensor-core GEMM
        (LayerSpec("e", "linear", p=128, d=128, T=64), 4),        # per-example, several splits
