@@ -22,6 +22,10 @@
 // consecutive in memory (2D boxes over the flattened rows), so one Gram tile holds
 // every example's Gram as a diagonal block; the epilogue adds only entries (r, s) of
 // the same example, row by row, then sums each example's T rows in a fixed order.
+// K splits (single row block or packed, fewer CTAs than SMs): the A-Gram is linear in its
+// K chunks, so split z of the grid forms the A-Gram over its share of the unfolded columns,
+// the whole G-Gram, and writes its part of the Hadamard sum (split 0 adds the bias term);
+// a fixed-order sum over the splits gives s_i.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -46,6 +50,7 @@ struct Params {
   // chunk q of the unfolded rows is channel block q / (k*k), filter tap q % (k*k)
   int conv, Wout, k, stride, pad, dil;
   int early;           // A and G are the caller's inputs: loads may start before pdl_wait
+  int ksplit;          // splits of the A-Gram's K chunks (grid y); > 1: out is [ksplit, B]
 };
 
 // Load K chunk kk (64 unfolded columns) of the 128 rows that start at row t0 of
@@ -97,6 +102,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   const bool dual = !packed && nb == 2;
   const bool x_is_g = kG >= kA;                 // dual: the wider operand goes first
   const int kX = x_is_g ? kG : kA, kY = x_is_g ? kA : kG;
+  // this split's A chunks [ka0, ka1) (all of them without K splits)
+  const int split = blockIdx.y;
+  const int ka0 = (int)((long)kA * split / P.ksplit), ka1 = (int)((long)kA * (split + 1) / P.ksplit);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -170,8 +178,8 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       const bool diag = tb == sb;
       for (int ph = 0; ph < 2 && live; ++ph) {
         const CUtensorMap* map = ph == 0 ? &mapA : &mapG;
-        const int nk = ph == 0 ? kA : kG;
-        for (int kk = 0; kk < nk; ++kk) {
+        const int k_lo = ph == 0 ? ka0 : 0, k_hi = ph == 0 ? ka1 : kG;
+        for (int kk = k_lo; kk < k_hi; ++kk) {
           for (int h = 0; h < (diag ? 1 : 2); ++h, ++k) {
             if ((k & 1) != pr) continue;
             const int s = k % STAGES;
@@ -270,9 +278,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       }
       ptx::tc_fence_after();
       for (int ph = 0; ph < 2 && live; ++ph) {
-        const int nk = ph == 0 ? kA : kG;
+        const int k_lo = ph == 0 ? ka0 : 0, k_hi = ph == 0 ? ka1 : kG;
         const uint32_t d_tmem = tmem + b * 256 + ph * 128;
-        for (int kk = 0; kk < nk; ++kk) {
+        for (int kk = k_lo; kk < k_hi; ++kk) {
           const int s0 = k % STAGES, s1 = (k + 1) % STAGES;
           bool w = ptx::mbar_wait(&full[s0], (k / STAGES) & 1, abort, P.status);
           if (!diag) w = w && ptx::mbar_wait(&full[s1], ((k + 1) / STAGES) & 1, abort, P.status);
@@ -284,7 +292,8 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           if (ptx::elect_one()) {
 #pragma unroll
             for (int u = 0; u < BK / 16; ++u)
-              ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, u * 32), ptx::sdesc_add(db, u * 32), kIdesc, (kk | u) != 0);
+              ptx::umma_bf16(d_tmem, ptx::sdesc_add(da, u * 32), ptx::sdesc_add(db, u * 32), kIdesc,
+                             (kk != k_lo) || u != 0);
             ptx::umma_commit(&empty[s0]);
             if (!diag) ptx::umma_commit(&empty[s1]);
           }
@@ -380,7 +389,7 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (e < P.ept && ex < P.B && ok && !*abort) {
         float h = 0.f, sg = 0.f;
         for (int r = e * P.T; r < (e + 1) * P.T; ++r) { h += rowbuf[r]; sg += rowbuf[BT + r]; }
-        P.out[ex] = h + (P.has_bias ? sg : 0.f);
+        P.out[(size_t)split * P.B + ex] = h + (P.has_bias && split == 0 ? sg : 0.f);
       }
     } else {
       H = warp_sum(H);
@@ -393,7 +402,7 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (threadIdx.x == 64 && ok && !*abort) {
         float h = 0.f, s = 0.f;
         for (int q = 0; q < 4; ++q) { h += red[2 * q]; s += red[2 * q + 1]; }
-        P.out[i] = h + (P.has_bias ? s : 0.f);
+        P.out[(size_t)split * P.B + i] = h + (P.has_bias && split == 0 ? s : 0.f);
       }
     }
   }
@@ -421,10 +430,25 @@ bool tc_ghost_supported(const Geom& g) {
   return !g.conv && (g.d % 8 == 0) && (g.p % 8 == 0) && g.T >= 2 && g.T <= 512;
 }
 
-size_t tc_ghost_ws_bytes(const Geom&) { return 0; }
+static int ghost_ept(const Geom& g) { return 2 * g.T <= tcghost::BT ? tcghost::BT / g.T : 0; }
+
+// K splits of the A-Gram when the examples give fewer CTAs than SMs (not in dual mode).
+static int ghost_ksplit(const Geom& g) {
+  const int ept = ghost_ept(g);
+  const int nb = (g.T + tcghost::BT - 1) / tcghost::BT;
+  if (!ept && nb == 2) return 1;
+  const long ctas = ept ? (g.B + ept - 1) / ept : g.B;
+  const int kA = (g.D + tcghost::BK - 1) / tcghost::BK;
+  return (int)std::max<long>(1, std::min<long>(kA, 152 / std::max<long>(1, ctas)));
+}
+
+size_t tc_ghost_ws_bytes(const Geom& g) {
+  const int ks = ghost_ksplit(g);
+  return ks > 1 ? ((size_t)ks * g.B * sizeof(float) + 255) / 256 * 256 : 0;
+}
 
 static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtensorMap& mg, tcghost::Params P,
-                             cudaStream_t s) {
+                             cudaStream_t s, float* part) {
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
@@ -434,12 +458,18 @@ static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtenso
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const int grid = P.ept ? (g.B + P.ept - 1) / P.ept : g.B;
+  P.ksplit = ghost_ksplit(g);
+  float* out = P.out;
+  if (P.ksplit > 1) {
+    if (!part) return cudaErrorInvalidValue;
+    P.out = part;
+  }
+  const dim3 grid(P.ept ? (g.B + P.ept - 1) / P.ept : g.B, P.ksplit);
   launch_pdl(tcghost::tc_ghost_kernel, grid, tcghost::kThreads, tcghost::SMEM, s, ma, mg, P);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || P.ksplit == 1) return e;
+  return launch_reduce_splits(part, P.ksplit, (size_t)g.B, out, 0, s);
 }
-
-static int ghost_ept(const Geom& g) { return 2 * g.T <= tcghost::BT ? tcghost::BT / g.T : 0; }
 
 // Conv layers with Cin % 64 == 0: the A-Gram reads the unfolded rows through TMA im2col
 // loads (128 pixels x 64 channels per filter tap) from an NHWC copy of the input; the
@@ -454,7 +484,7 @@ bool tc_ghost_conv_supported(const Geom& g) {
 static size_t al256g(size_t n) { return (n + 255) & ~size_t(255); }
 
 size_t tc_ghost_conv_ws_bytes(const Geom& g) {
-  return al256g((size_t)g.B * g.H * g.W * g.Cin * 2) + al256g((size_t)g.B * g.T * g.p * 2);
+  return al256g((size_t)g.B * g.H * g.W * g.Cin * 2) + al256g((size_t)g.B * g.T * g.p * 2) + tc_ghost_ws_bytes(g);
 }
 
 cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, float* out, void* ws,
@@ -484,11 +514,14 @@ cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, fl
     const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
     if (!encode_tmap_bf16(&mg, Gt, 3, dg, sg, box)) return cudaErrorInvalidValue;
   }
-  tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil, 0};
-  return run_ghost(g, ma, mg, P, s);
+  tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil, 0, 1};
+  // the split partials follow the NHWC copy and the rows in the workspace (in either layout)
+  float* part = reinterpret_cast<float*>(w + al256g((size_t)g.B * g.H * g.W * g.Cin * 2) +
+                                         al256g((size_t)g.B * g.T * g.p * 2));
+  return run_ghost(g, ma, mg, P, s, part);
 }
 
-cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* /*ws*/,
+cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* ws,
                             unsigned* status, cudaStream_t s, bool early) {
   CUtensorMap ma, mg;
   const int ept = ghost_ept(g);
@@ -507,8 +540,8 @@ cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* 
     if (!encode_tmap_bf16(&ma, A, 3, da, sa, box) || !encode_tmap_bf16(&mg, G, 3, dg, sg, box))
       return cudaErrorInvalidValue;
   }
-  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0, early ? 1 : 0};
-  return run_ghost(g, ma, mg, P, s);
+  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0, early ? 1 : 0, 1};
+  return run_ghost(g, ma, mg, P, s, ws);
 }
 
 }  // namespace dph
