@@ -23,9 +23,10 @@
 // every example's Gram as a diagonal block; the epilogue adds only entries (r, s) of
 // the same example, row by row, then sums each example's T rows in a fixed order.
 // K splits (single row block or packed, fewer CTAs than SMs): the A-Gram is linear in its
-// K chunks, so split z of the grid forms the A-Gram over its share of the unfolded columns,
-// the whole G-Gram, and writes its part of the Hadamard sum (split 0 adds the bias term);
-// a fixed-order sum over the splits gives s_i.
+// K chunks, so CTA y of a cluster of ksplit forms the A-Gram over its share of the unfolded
+// columns, the whole G-Gram, and its part of the Hadamard sum (rank 0 adds the bias term);
+// the parts go to rank 0's shared memory and rank 0 sums them in rank order after a
+// cluster barrier (no second kernel).
 #include <algorithm>
 
 #include "tc.cuh"
@@ -38,7 +39,8 @@ constexpr int BT = 128, BK = 64, STAGES = 8;
 constexpr int TILE = BT * BK * 2;   // 16 KB
 constexpr int STAGE = TILE;         // one tile per slot
 constexpr int kThreads = 224;
-constexpr int SMEM = STAGES * STAGE + 1024 + 2048;
+constexpr int MAXSPLIT = 8;         // K splits: one cluster (portable size)
+constexpr int SMEM = STAGES * STAGE + 1024 + 2048 + MAXSPLIT * BT * 4 + 64;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(BT, BT, 0, 0);
 
 struct Params {
@@ -50,8 +52,15 @@ struct Params {
   // chunk q of the unfolded rows is channel block q / (k*k), filter tap q % (k*k)
   int conv, Wout, k, stride, pad, dil;
   int early;           // A and G are the caller's inputs: loads may start before pdl_wait
-  int ksplit;          // splits of the A-Gram's K chunks (grid y); > 1: out is [ksplit, B]
+  int ksplit;          // splits of the A-Gram's K chunks (grid y, one cluster of ksplit CTAs)
 };
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 // Load K chunk kk (64 unfolded columns) of the 128 rows that start at row t0 of
 // example e: a tiled box, or for conv layers an im2col block of one filter tap.
@@ -92,6 +101,8 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 2);   // [8]
   float* rowbuf = red + 8;                                 // packed mode: [2][BT] per-row sums
+  float* csum = rowbuf + 2 * BT;                           // K splits (rank 0): [split][example]
+  uint32_t* cabort = reinterpret_cast<uint32_t*>(csum + MAXSPLIT * BT);   // [split] aborted
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i = blockIdx.x;
@@ -103,7 +114,7 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   const bool x_is_g = kG >= kA;                 // dual: the wider operand goes first
   const int kX = x_is_g ? kG : kA, kY = x_is_g ? kA : kG;
   // this split's A chunks [ka0, ka1) (all of them without K splits)
-  const int split = blockIdx.y;
+  const int split = blockIdx.y;   // = the cluster rank with K splits
   const int ka0 = (int)((long)kA * split / P.ksplit), ka1 = (int)((long)kA * (split + 1) / P.ksplit);
 
   if (threadIdx.x == 0) {
@@ -389,7 +400,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (e < P.ept && ex < P.B && ok && !*abort) {
         float h = 0.f, sg = 0.f;
         for (int r = e * P.T; r < (e + 1) * P.T; ++r) { h += rowbuf[r]; sg += rowbuf[BT + r]; }
-        P.out[(size_t)split * P.B + ex] = h + (P.has_bias && split == 0 ? sg : 0.f);
+        const float v = h + (P.has_bias && split == 0 ? sg : 0.f);
+        if (P.ksplit > 1) st_cluster_f32(ptx::map_rank(ptx::smem_u32(csum + split * BT + e), 0), v);
+        else P.out[ex] = v;
       }
     } else {
       H = warp_sum(H);
@@ -402,7 +415,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
       if (threadIdx.x == 64 && ok && !*abort) {
         float h = 0.f, s = 0.f;
         for (int q = 0; q < 4; ++q) { h += red[2 * q]; s += red[2 * q + 1]; }
-        P.out[(size_t)split * P.B + i] = h + (P.has_bias && split == 0 ? s : 0.f);
+        const float v = h + (P.has_bias && split == 0 ? s : 0.f);
+        if (P.ksplit > 1) st_cluster_f32(ptx::map_rank(ptx::smem_u32(csum + split * BT), 0), v);
+        else P.out[i] = v;
       }
     }
   }
@@ -412,6 +427,26 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   if (*abort && threadIdx.x == 32) {
     ptx::umma_commit(drainb);   // arrives once every MMA issued so far has completed
     ptx::mbar_wait_drain(drainb, 0);
+  }
+  if (P.ksplit > 1) {
+    // every CTA's parts (and abort flag) are in rank 0's shared memory after the barrier;
+    // rank 0 adds them in rank order
+    if (threadIdx.x == 0) st_cluster_u32(ptx::map_rank(ptx::smem_u32(cabort + split), 0), *abort ? 1u : 0u);
+    ptx::cluster_sync();
+    if (split == 0) {
+      bool bad = false;
+      for (int r = 0; r < P.ksplit; ++r) bad |= cabort[r] != 0;
+      const int ne = packed ? P.ept : 1;
+      const int e = threadIdx.x - 64;
+      if (!bad && e >= 0 && e < ne) {
+        const int ex = packed ? i * P.ept + e : i;
+        if (ex < P.B) {
+          float v = 0.f;
+          for (int r = 0; r < P.ksplit; ++r) v += csum[r * BT + e];
+          P.out[ex] = v;
+        }
+      }
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -439,16 +474,13 @@ static int ghost_ksplit(const Geom& g) {
   if (!ept && nb == 2) return 1;
   const long ctas = ept ? (g.B + ept - 1) / ept : g.B;
   const int kA = (g.D + tcghost::BK - 1) / tcghost::BK;
-  return (int)std::max<long>(1, std::min<long>(kA, 152 / std::max<long>(1, ctas)));
+  return (int)std::max<long>(1, std::min<long>(std::min(kA, tcghost::MAXSPLIT), 152 / std::max<long>(1, ctas)));
 }
 
-size_t tc_ghost_ws_bytes(const Geom& g) {
-  const int ks = ghost_ksplit(g);
-  return ks > 1 ? ((size_t)ks * g.B * sizeof(float) + 255) / 256 * 256 : 0;
-}
+size_t tc_ghost_ws_bytes(const Geom&) { return 0; }
 
 static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtensorMap& mg, tcghost::Params P,
-                             cudaStream_t s, float* part) {
+                             cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
@@ -459,16 +491,28 @@ static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtenso
     attr_set[dev] = true;
   }
   P.ksplit = ghost_ksplit(g);
-  float* out = P.out;
-  if (P.ksplit > 1) {
-    if (!part) return cudaErrorInvalidValue;
-    P.out = part;
-  }
   const dim3 grid(P.ept ? (g.B + P.ept - 1) / P.ept : g.B, P.ksplit);
-  launch_pdl(tcghost::tc_ghost_kernel, grid, tcghost::kThreads, tcghost::SMEM, s, ma, mg, P);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || P.ksplit == 1) return e;
-  return launch_reduce_splits(part, P.ksplit, (size_t)g.B, out, 0, s);
+  if (P.ksplit == 1) {
+    launch_pdl(tcghost::tc_ghost_kernel, grid, tcghost::kThreads, tcghost::SMEM, s, ma, mg, P);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(tcghost::kThreads);
+  cfg.dynamicSmemBytes = tcghost::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = P.ksplit;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tcghost::tc_ghost_kernel, ma, mg, P);
+  count_launch();
+  return e;
 }
 
 // Conv layers with Cin % 64 == 0: the A-Gram reads the unfolded rows through TMA im2col
@@ -484,7 +528,7 @@ bool tc_ghost_conv_supported(const Geom& g) {
 static size_t al256g(size_t n) { return (n + 255) & ~size_t(255); }
 
 size_t tc_ghost_conv_ws_bytes(const Geom& g) {
-  return al256g((size_t)g.B * g.H * g.W * g.Cin * 2) + al256g((size_t)g.B * g.T * g.p * 2) + tc_ghost_ws_bytes(g);
+  return al256g((size_t)g.B * g.H * g.W * g.Cin * 2) + al256g((size_t)g.B * g.T * g.p * 2);
 }
 
 cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, float* out, void* ws,
@@ -515,13 +559,10 @@ cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, fl
     if (!encode_tmap_bf16(&mg, Gt, 3, dg, sg, box)) return cudaErrorInvalidValue;
   }
   tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil, 0, 1};
-  // the split partials follow the NHWC copy and the rows in the workspace (in either layout)
-  float* part = reinterpret_cast<float*>(w + al256g((size_t)g.B * g.H * g.W * g.Cin * 2) +
-                                         al256g((size_t)g.B * g.T * g.p * 2));
-  return run_ghost(g, ma, mg, P, s, part);
+  return run_ghost(g, ma, mg, P, s);
 }
 
-cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* ws,
+cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* /*ws*/,
                             unsigned* status, cudaStream_t s, bool early) {
   CUtensorMap ma, mg;
   const int ept = ghost_ept(g);
@@ -541,7 +582,7 @@ cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* 
       return cudaErrorInvalidValue;
   }
   tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0, early ? 1 : 0, 1};
-  return run_ghost(g, ma, mg, P, s, ws);
+  return run_ghost(g, ma, mg, P, s);
 }
 
 }  // namespace dph
