@@ -68,7 +68,8 @@ struct Params {
   unsigned* status;
   int B, T, p, D, Np, bias;
   int Cin, H, W, Hout, Wout, k, kh, stride, pad, padh, dil;
-  int nhwc;                 // input and output gradient channels last
+  int nhwc;                 // input and output gradient channels last (the input is staged
+                            // channels first on chip all the same)
   int XP;                   // channels first: padded row pitch of the input on chip (elements)
   int xelems;               // Cin * H * W
   int xvec;                 // the builders move the input in 16-byte vectors
@@ -134,10 +135,15 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
   }
 }
 
-// On-chip input position of element (column coff, row h, column w): channels first in
-// padded rows (8 zeros either side), channels last dense.
-__device__ __forceinline__ int xpos(const Params& P, int coff, int h, int w) {
-  return P.nhwc ? (h * P.W + w) * P.Cin + coff : coff + h * P.XP + 8 + w;
+// On-chip input position of element (channel offset coff = c*H*XP, row h, column w): channels
+// first in padded rows (8 zeros either side), whatever the input's layout in memory.
+__device__ __forceinline__ int xpos(const Params& P, int coff, int h, int w) { return coff + h * P.XP + 8 + w; }
+
+// On-chip position of element q of one example's input as it lies in memory.
+__device__ __forceinline__ int xdst(const Params& P, int q) {
+  if (!P.nhwc) return (q / P.W) * P.XP + 8 + q % P.W;
+  const int px = q / P.Cin, c = q - px * P.Cin;   // channels last: [H, W, Cin]
+  return (c * P.H + px / P.W) * P.XP + 8 + px % P.W;
 }
 
 // The example's input into an on-chip buffer (interior only: the pads stay zero).
@@ -156,17 +162,19 @@ __device__ __forceinline__ void store_x_regs(const Params& P, __nv_bfloat16* xs,
   for (int j = 0; j < XV; ++j) {
     const int q = bt + j * kBT;
     if (q < nv) {
-      const int o = P.nhwc ? q * 8 : (q / wv) * P.XP + 8 + (q % wv) * 8;
-      *reinterpret_cast<uint4*>(xs + o) = v[j];
+      if (!P.nhwc) {
+        *reinterpret_cast<uint4*>(xs + (q / wv) * P.XP + 8 + (q % wv) * 8) = v[j];
+      } else {            // channels last: the 8 elements go to their channels' rows
+        const __nv_bfloat16* e8 = reinterpret_cast<const __nv_bfloat16*>(&v[j]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xs[xdst(P, q * 8 + k)] = e8[k];
+      }
     }
   }
 }
 __device__ __forceinline__ void load_x_scalar(const Params& P, int e, int bt, __nv_bfloat16* xs) {
   const __nv_bfloat16* src = P.X + (size_t)e * P.xelems;
-  for (int q = bt; q < P.xelems; q += kBT) {
-    const int o = P.nhwc ? q : (q / P.W) * P.XP + 8 + q % P.W;
-    xs[o] = src[q];
-  }
+  for (int q = bt; q < P.xelems; q += kBT) xs[xdst(P, q)] = src[q];
 }
 
 // 8 consecutive bf16 of an on-chip row starting at element `pos` (any alignment): two aligned
@@ -545,7 +553,7 @@ tc_unfold_kernel(const __grid_constant__ CUtensorMap mapX, Params P) {
     const int n = threadIdx.x, kk = P.kh * P.k;
     if (n < P.D) {
       const int ch = n / kk, r = n - ch * kk, ih = r / P.k, iw = r - ih * P.k;
-      c->coff[n] = P.nhwc ? ch : ch * P.H * P.XP;
+      c->coff[n] = ch * P.H * P.XP;
       c->dh[n] = ih * P.dil - P.padh;
       c->dw[n] = iw * P.dil - P.pad;
     } else {
@@ -609,7 +617,7 @@ bool tc_unfold_supported(const Geom& g) {
   if (!g.conv || g.Z != 1 || g.kz != 1 || g.B < 1 || g.p < 1 || g.T < 1) return false;
   if (unfold_np(g) > tcunf::NMAX) return false;
   if (g.nhwc ? g.p % 8 != 0 : g.T % 8 != 0) return false;   // 16-byte TMA row strides of G
-  const long xe = g.nhwc ? (long)g.Cin * g.H * g.W : (long)g.Cin * g.H * unfold_xp(g);
+  const long xe = (long)g.Cin * g.H * unfold_xp(g);   // the input on chip, channels first, padded rows
   return xe <= tcunf::XMAXE;
 }
 
@@ -663,7 +671,7 @@ static tcunf::Params unfold_params(const Geom& g, const void* A, unsigned* statu
   P.xelems = g.Cin * g.H * g.W;
   const bool al = (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
   P.xvec = al && P.xelems % 8 == 0 && (g.nhwc || g.W % 8 == 0);
-  P.fast = !g.nhwc && g.stride == 1 && g.Wout % 8 == 0 && g.pad <= 8 && g.padh <= 8;
+  P.fast = g.stride == 1 && g.Wout % 8 == 0 && g.pad <= 8 && g.padh <= 8;
   P.xrows = g.Cin * g.H;
   P.xtma = al && !g.nhwc && g.W % 8 == 0 && P.XP <= 256 && P.xrows <= 256;
   P.nk = cdiv_u(g.T, 64);

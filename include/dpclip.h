@@ -166,9 +166,11 @@ dp_status dp_clip_factors(const float* sqnorms, int B, int L, int per_layer, con
  * factors: device fp32 [B] (a row of dp_clip_factors' output).  accumulate = 0 writes,
  * 1 adds to the existing dW/db (gradient accumulation over micro-batches).
  * An example whose norm overflowed but whose inputs are finite gets factor 0 from
- * dp_clip_factors and adds nothing; an example whose A or G hold inf or NaN can still
- * turn entries of the sum into NaN (0 * inf), and dp_clip_factors has raised
- * DP_ERR_NONFINITE for it: a caller that sees that status discards the step.
+ * dp_clip_factors and adds nothing.  An example whose A or G hold inf or NaN (factor 0,
+ * DP_ERR_NONFINITE raised by dp_clip_factors) still meets the contraction: exactly the
+ * outputs it reaches through a non-finite value become NaN (0 * inf: row j of dW and db[j]
+ * for a non-finite G_i[t, j], column m of dW for a non-finite A_i[t, m]); every other entry
+ * is the sum over the remaining examples.  A caller that sees the status discards the step.
  * workspace: device, >= dp_workspace_size(desc, 0) bytes. */
 dp_status dp_clipped_sum(const dp_layer_desc* desc, const void* A, const void* G,
                          const float* factors, float* dW, float* db, int accumulate,

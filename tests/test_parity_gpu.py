@@ -564,6 +564,38 @@ def test_nonfinite_norm_zeroes_factor_and_raises_status(lib):
     assert f[2] == 0.0 and np.all(np.isfinite(f))
 
 
+@pytest.mark.parametrize("pin", ["", "rows", "example"], ids=["auto", "rows_gemm", "per_example"])
+def test_nonfinite_example_with_factor_zero_in_the_sum(lib, pin, monkeypatch):
+    """An example whose G holds inf gets factor 0; in the clipped sum it still meets the
+    contraction, so exactly the outputs it touches through the inf become NaN (0 * inf): row
+    j of dW and db[j] for G_i[t, j] = inf.  Every other entry equals the sum over the finite
+    examples."""
+    import torch
+    if pin:
+        monkeypatch.setenv("DPCLIP_SUM_KERNEL", pin)
+    dp = lib
+    spec = LayerSpec("e", "linear", p=64, d=128, T=64)
+    B = 4
+    wl = Workload(name="nf_sum", B=B, layers=(spec,), dtype="bf16", C=1.0, sigma=1.0, seed=3)
+    A, G = workloads.layer_inputs(wl, 0)
+    G[2, 1, 3] = np.inf
+    fac = np.array([0.5, 0.8, 0.0, 1.0], dtype=np.float32)
+    desc = desc_for(dp, spec, B, "bf16")
+    ws = torch.empty(max(dp.dp_workspace_size(desc), 16), dtype=torch.uint8, device="cuda")
+    dW = torch.empty(spec.p * spec.D, device="cuda")
+    db = torch.empty(spec.p, device="cuda")
+    dp.dp_clipped_sum(desc, to_dev(A, "bf16"), to_dev(G, "bf16"), torch.tensor(fac, device="cuda"), dW, db, ws)
+    torch.cuda.synchronize()
+    W = dW.cpu().numpy().reshape(spec.p, spec.D)
+    b = db.cpu().numpy()
+    assert np.all(np.isnan(W[3])) and np.isnan(b[3])
+    keep = [i for i in range(B) if i != 2]
+    S, Sb = oracle.clipped_sum(spec, A[keep], G[keep], fac[keep].astype(np.float64))
+    rows = [j for j in range(spec.p) if j != 3]
+    assert rel_rows(W[rows], S.reshape(spec.p, spec.D)[rows], spec.D) <= TOL["bf16"]
+    assert rel_rows(b[rows], Sb[rows]) <= TOL["bf16"]
+
+
 # ----------------------------------------------------------------- noise and adaptive bound
 
 @pytest.mark.parametrize("n,offset", [(1, 0), (3, 5), (7, 2), (1000, 0), (1001, 13), (1 << 20, 3), (1002, 8),
