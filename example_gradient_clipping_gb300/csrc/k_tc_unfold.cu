@@ -177,26 +177,8 @@ __device__ __forceinline__ void load_x_scalar(const Params& P, int e, int bt, __
   for (int q = bt; q < P.xelems; q += kBT) xs[xdst(P, q)] = src[q];
 }
 
-// 8 consecutive bf16 of an on-chip row starting at element `pos` (any alignment): two aligned
-// 16-byte loads and a funnel shift by the (warp-uniform) misalignment.
-__device__ __forceinline__ uint4 window8(const __nv_bfloat16* xs, int pos) {
-  const int a = pos & ~7, r = pos & 7;
-  const uint4 w0 = *reinterpret_cast<const uint4*>(xs + a);
-  const uint4 w1 = *reinterpret_cast<const uint4*>(xs + a + 8);
-  uint32_t s0, s1, s2, s3, s4;
-  switch (r >> 1) {
-    case 0: s0 = w0.x; s1 = w0.y; s2 = w0.z; s3 = w0.w; s4 = w1.x; break;
-    case 1: s0 = w0.y; s1 = w0.z; s2 = w0.w; s3 = w1.x; s4 = w1.y; break;
-    case 2: s0 = w0.z; s1 = w0.w; s2 = w1.x; s3 = w1.y; s4 = w1.z; break;
-    default: s0 = w0.w; s1 = w1.x; s2 = w1.y; s3 = w1.z; s4 = w1.w; break;
-  }
-  if (r & 1)
-    return make_uint4(__funnelshift_r(s0, s1, 16), __funnelshift_r(s1, s2, 16), __funnelshift_r(s2, s3, 16),
-                      __funnelshift_r(s3, s4, 16));
-  return make_uint4(s0, s1, s2, s3);
-}
-
-// One 16-byte unit of U^T: column n, pixels t0 .. t0+7 of the example.
+// One 16-byte unit of U^T, element by element: column n, pixels t0 .. t0+7 of the example
+// (any stride, dilation or width; the window path of build_chunk covers stride 1).
 __device__ __forceinline__ uint4 build_unit(const Params& P, const Ctl* c, const __nv_bfloat16* xs, int n, int t0) {
   const int coff = c->coff[n];
   if (coff == -2 || t0 >= P.T) return make_uint4(0u, 0u, 0u, 0u);       // padding column / past T
@@ -206,12 +188,6 @@ __device__ __forceinline__ uint4 build_unit(const Params& P, const Ctl* c, const
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j] = __float2bfloat16_rn(t0 + j < P.T ? 1.f : 0.f);
     return *reinterpret_cast<const uint4*>(o);
-  }
-  if (P.fast) {   // 8 pixels of one output row; the row's pads hold the horizontal zeros
-    const int ho = t0 / P.Wout, wo = t0 - ho * P.Wout;
-    const int h = ho + c->dh[n];
-    if (h < 0 || h >= P.H) return make_uint4(0u, 0u, 0u, 0u);
-    return window8(xs, coff + h * P.XP + 8 + wo + c->dw[n]);
   }
   __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
