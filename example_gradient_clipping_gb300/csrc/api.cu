@@ -211,11 +211,16 @@ int sum_kernel_for(const Geom& lg) {
   return 0;
 }
 
-// DPCLIP_CONV=rows keeps conv layers on their written-out row layout (tests, tuning);
-// otherwise conv layers the im2col kernels take use them.
+// DPCLIP_CONV=rows keeps conv layers on their written-out row layout, DPCLIP_CONV=im2col on
+// the im2col kernels where the shifted-tile kernel would take them (tests, tuning);
+// otherwise conv layers the TMA kernels take use them.
 bool conv_rows_pinned() {
   const char* v = std::getenv("DPCLIP_CONV");
   return v && !std::strcmp(v, "rows");
+}
+bool conv_im2col_pinned() {
+  const char* v = std::getenv("DPCLIP_CONV");
+  return v && !std::strcmp(v, "im2col");
 }
 
 bool im2col_inputs(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
@@ -223,6 +228,11 @@ bool im2col_inputs(const Geom& g, int dtype, const void* A, const void* G, const
 }
 bool use_tc_conv(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
   return im2col_inputs(g, dtype, A, G, ws) && dph::tc_conv_supported(g);
+}
+// Stride-1 "same" 1x1 / 3x3 conv layers, 64 input channels, at most 64 outputs: the filter
+// rows and columns as shifted views of one output-gradient tile and one input tile.
+bool use_tc_halo(const Geom& g, int dtype, const void* A, const void* G, const void* ws) {
+  return im2col_inputs(g, dtype, A, G, ws) && !conv_im2col_pinned() && dph::tc_halo_supported(g);
 }
 // Conv layers with at most 64 unfolded columns (plus bias) form their unfold on chip and
 // read G as it lies (DPCLIP_CONV=rows keeps them on the written-out row layout).
@@ -252,11 +262,13 @@ Plan sum_plan(const Geom& g, int dtype, const void* A, const void* G, const void
   return pl;
 }
 
-enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST, NK_TC_CONV, NK_TC_GHOST_CONV, NK_TC_UNFOLD };
+enum { NK_T1, NK_SIMT_GHOST, NK_SIMT_INST, NK_TC_GHOST, NK_TC_INST, NK_TC_CONV, NK_TC_GHOST_CONV, NK_TC_UNFOLD,
+       NK_TC_HALO };
 
 Plan norm_plan(const Geom& g, int mode, int dtype, const void* A, const void* G, const void* ws) {
   if (mode == DP_NORM_T1) return Plan{NK_T1, false, g};
   if (mode == DP_NORM_INSTANTIATE && use_tc_unfold(g, dtype, G)) return Plan{NK_TC_UNFOLD, false, g};
+  if (mode == DP_NORM_INSTANTIATE && use_tc_halo(g, dtype, A, G, ws)) return Plan{NK_TC_HALO, false, g};
   if (mode == DP_NORM_INSTANTIATE && use_tc_conv(g, dtype, A, G, ws)) return Plan{NK_TC_CONV, false, g};
   if (mode == DP_NORM_GHOST && im2col_inputs(g, dtype, A, G, ws) && dph::tc_ghost_conv_supported(g))
     return Plan{NK_TC_GHOST_CONV, false, g};
@@ -298,6 +310,7 @@ size_t norm_ws_bytes(const Geom& g, const Plan& pl) {
     case NK_TC_CONV: inner = dph::tc_conv_ws_bytes(g, true); break;
     case NK_TC_GHOST_CONV: inner = dph::tc_ghost_conv_ws_bytes(g); break;
     case NK_TC_UNFOLD: inner = dph::tc_unfold_ws_bytes(g, true); break;
+    case NK_TC_HALO: inner = dph::tc_halo_ws_bytes(g); break;
   }
   return (pl.rows ? rows_bytes(g) : 0) + inner;
 }
@@ -310,7 +323,8 @@ static const char kAlignedProbe[16] __attribute__((aligned(16))) = {};
 bool keep_plan(int dtype, const Geom& g, const void* A, const void* G, const void* ws, Plan* pl) {
   if (dtype != DP_BF16 || g.T == 1) return false;
   *pl = norm_plan(g, DP_NORM_INSTANTIATE, dtype, A, G, ws);
-  return pl->kernel == NK_TC_CONV || pl->kernel == NK_TC_INST || pl->kernel == NK_TC_UNFOLD;
+  return pl->kernel == NK_TC_CONV || pl->kernel == NK_TC_INST || pl->kernel == NK_TC_UNFOLD ||
+         pl->kernel == NK_TC_HALO;
 }
 bool keep_plan(int dtype, const Geom& g, Plan* pl) {
   return keep_plan(dtype, g, kAlignedProbe, kAlignedProbe, kAlignedProbe, pl);
@@ -318,7 +332,7 @@ bool keep_plan(int dtype, const Geom& g, Plan* pl) {
 // Columns of each kept gradient (conv tile columns or the on-chip unfold's weight layout = D;
 // rows of a padded conv layer = Dp).
 int kept_width(const Geom& g, const Plan& pl) {
-  return pl.kernel == NK_TC_CONV || pl.kernel == NK_TC_UNFOLD ? g.D : pl.lg.D;
+  return pl.kernel == NK_TC_CONV || pl.kernel == NK_TC_UNFOLD || pl.kernel == NK_TC_HALO ? g.D : pl.lg.D;
 }
 size_t kept_sum_need(const Geom& g, const Plan& pl) {
   return dph::kept_sum_ws_bytes(g.B, g.p, kept_width(g, pl)) + (pl.rows ? padded_out_bytes(g) : 0);
@@ -451,6 +465,7 @@ dp_status dp_layer_sqnorms(const dp_layer_desc* desc, const void* A, const void*
     case NK_TC_CONV: e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_TC_GHOST_CONV: e = dph::launch_tc_ghost_conv(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_TC_UNFOLD: e = dph::launch_tc_unfold_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
+    case NK_TC_HALO: e = dph::launch_tc_halo_norm(g, A, G, sqnorm_out, ws, status_ptr(), stream); break;
     case NK_SIMT_GHOST: e = dph::launch_simt_ghost(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
     case NK_SIMT_INST: e = dph::launch_simt_inst(g, desc->dtype, A, G, sqnorm_out, ws, stream); break;
   }
@@ -482,7 +497,7 @@ static bool norm_leaves_nhwc(const Geom& g, int norm_mode, int dtype, const void
   if (!g.conv || g.nhwc || norm_mode < DP_NORM_AUTO || norm_mode > DP_NORM_AUTO_TIME || norm_mode == DP_NORM_T1)
     return false;   // (channels-last inputs need no copy to share)
   const Plan npl = norm_plan(g, resolve_mode(g, norm_mode), dtype, A, G, ws);
-  return npl.kernel == NK_TC_GHOST_CONV || npl.kernel == NK_TC_CONV;
+  return npl.kernel == NK_TC_GHOST_CONV || npl.kernel == NK_TC_CONV || npl.kernel == NK_TC_HALO;
 }
 
 // The noise of a fused call: the scale and divisor as dp_add_noise forms them.
@@ -625,6 +640,8 @@ dp_status dp_layer_sqnorms_keep(const dp_layer_desc* desc, const void* A, const 
     e = dph::launch_tc_conv_norm(g, A, G, sqnorm_out, wsp, status_ptr(), stream, grads, keep_b);
   else if (pl.kernel == NK_TC_UNFOLD)
     e = dph::launch_tc_unfold_norm(g, A, G, sqnorm_out, wsp, status_ptr(), stream, grads, keep_b);
+  else if (pl.kernel == NK_TC_HALO)
+    e = dph::launch_tc_halo_norm(g, A, G, sqnorm_out, wsp, status_ptr(), stream, grads, keep_b);
   else
     e = dph::launch_tc_inst(pl.lg, A, G, sqnorm_out, static_cast<float*>(wsp), status_ptr(), stream, grads, keep_b,
                             !pl.rows);
@@ -655,7 +672,7 @@ static dp_status kept_sum_impl(const dp_layer_desc* desc, const float* grads, co
                 workspace ? ws_bytes : (size_t)0);
   const int width = kept_width(g, pl);
   const float* keep_b = g.has_bias ? grads + (size_t)g.B * g.p * width : nullptr;
-  const int conv_kk = pl.kernel == NK_TC_CONV ? g.k * g.k : 0;
+  const int conv_kk = pl.kernel == NK_TC_CONV || pl.kernel == NK_TC_HALO ? g.k * g.k : 0;
   const bool padded = pl.rows && padded_out_bytes(g) != 0;
   float* kdW = dW;
   float* kdb = db;
@@ -667,7 +684,7 @@ static dp_status kept_sum_impl(const dp_layer_desc* desc, const float* grads, co
   }
   cudaError_t e = dph::launch_kept_sum(g.B, g.p, width, conv_kk, grads, keep_b, factors, kdW, kdb,
                                        padded ? 0 : accumulate, static_cast<float*>(wsp), stream,
-                                       padded ? nullptr : nz);
+                                       padded ? nullptr : nz, pl.kernel == NK_TC_HALO);
   if (e == cudaSuccess && padded) {
     e = dph::launch_compact_cols(kdW, g.p, g.D, width, dW, accumulate, stream);
     if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);

@@ -80,7 +80,7 @@ size_t kept_sum_ws_bytes(int B, int p, int D) {
 
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
                             const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s,
-                            NoiseArgs* nz) {
+                            NoiseArgs* nz, bool quad) {
   if (((size_t)p * D) % 4 || p % 4) return cudaErrorInvalidValue;
   const int splits = kept_splits(B, p, D);
   const int eps = (B + splits - 1) / splits;
@@ -95,7 +95,7 @@ cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (conv_kk > 0) {
-    e = launch_conv_reduce(part, splits, p, D, conv_kk, dW, accumulate, s);
+    e = launch_conv_reduce(part, splits, p, D, conv_kk, dW, accumulate, s, quad);
     if (e != cudaSuccess || !bias) return e;
     return conv_bias_reduce(part_b, splits, p, db, accumulate, s, nz);
   }

@@ -340,12 +340,13 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
 }
 
 // dW[j, m] (+)= sum_s part[s, j, n(m)] in split order; n(m) maps the weight column
-// m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64).  (The noise of a fused
+// m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64); with `quad` a split's
+// [p, ncols] block is stored column-quad major ([ncols / 4][p][4]).  (The noise of a fused
 // call is not drawn here: one output per thread would draw a whole Philox block per output,
 // which measured slower than the separate four-outputs-per-block noise pass on the large
 // layers; grouping four outputs per thread instead starved the small layers of threads.)
 __global__ void conv_reduce_kernel(const float* __restrict__ part, int splits, int p, int ncols, int kk,
-                                   float* __restrict__ dW, int accumulate) {
+                                   float* __restrict__ dW, int accumulate, int quad) {
   pdl_trigger();
   pdl_wait();
   const size_t n = (size_t)p * ncols;
@@ -353,8 +354,9 @@ __global__ void conv_reduce_kernel(const float* __restrict__ part, int splits, i
     const int j = (int)(q / ncols), m = (int)(q - (size_t)j * ncols);
     const int cch = m / kk, tap = m - cch * kk;
     const int col = ((cch >> 6) * kk + tap) * 64 + (cch & 63);
+    const size_t at = quad ? ((size_t)(col >> 2) * p + j) * 4 + (col & 3) : (size_t)j * ncols + col;
     float s = 0.f;
-    for (int sp = 0; sp < splits; ++sp) s += part[((size_t)sp * p + j) * ncols + col];
+    for (int sp = 0; sp < splits; ++sp) s += part[(size_t)sp * p * ncols + at];
     dW[q] = accumulate ? dW[q] + s : s;
   }
 }
@@ -464,10 +466,11 @@ static bool encode_maps(const Geom& g, const void* Xh, const void* G, CUtensorMa
 }
 
 cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
-                               cudaStream_t s) {
+                               cudaStream_t s, bool quad) {
   const size_t n = (size_t)p * ncols;
   const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
-  launch_plain(tcconv::conv_reduce_kernel, blocks ? blocks : 1, 256, 0, s, part, splits, p, ncols, kk, dW, accumulate);
+  launch_plain(tcconv::conv_reduce_kernel, blocks ? blocks : 1, 256, 0, s, part, splits, p, ncols, kk, dW, accumulate,
+               quad ? 1 : 0);
   return cudaGetLastError();
 }
 

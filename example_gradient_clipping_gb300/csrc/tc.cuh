@@ -31,13 +31,21 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
                            bool early = false);
 // Clipped sum from kept per-example gradients: dW (+)= sum_i c_i g_i, db (+)= sum_i c_i b_i
 // (2pD flop per example, one read of the kept gradients).  conv_kk > 0: g_i in the conv
-// kernel's tile column order with that many filter taps (mapped back to [p, Cin, k, k]).
+// kernel's tile column order with that many filter taps (mapped back to [p, Cin, k, k]);
+// `quad`: g_i stored column-quad major, [D / 4][p][4] (the shifted-tile kernel's stores).
 size_t kept_sum_ws_bytes(int B, int p, int D);
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
                             const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s,
-                            dpk::NoiseArgs* nz = nullptr);
+                            dpk::NoiseArgs* nz = nullptr, bool quad = false);
 // Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
+// Stride-1 "same" conv layers over 64 input channels: every filter tap a shifted view of one
+// input tile (NHWC copy of a channels-first input and channels-last rows of G in the workspace).
+bool tc_halo_supported(const Geom& g);
+size_t tc_halo_ws_bytes(const Geom& g);
+// ||g_i||^2 -> out [B]; with `keep`, g_i [B, p, D] in the conv tile column order and b_i [B, p].
+cudaError_t launch_tc_halo_norm(const Geom& g, const void* A, const void* G, float* out, void* ws, unsigned* status,
+                                cudaStream_t s, float* keep = nullptr, float* keep_b = nullptr);
 // Conv layers whose unfolded width plus bias is at most 64 (first layers over a few input
 // channels): the unfold formed on chip from the example's input, G read as it lies.
 bool tc_unfold_supported(const Geom& g);
@@ -87,9 +95,10 @@ cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, cons
 // im2col map (bf16, 128-byte swizzle, 64 channels per pixel) over an NHWC copy of a conv input.
 bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pixels);
 // dW[j, m] (+)= sum over splits of part[s, j, col(m)], col mapping the weight column
-// m = c*kk + tap to the im2col tile column (c/64 * kk + tap) * 64 + c % 64.
+// m = c*kk + tap to the im2col tile column (c/64 * kk + tap) * 64 + c % 64; `quad`: part's
+// rows stored column-quad major, [ncols / 4][p][4].
 cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
-                               cudaStream_t s);
+                               cudaStream_t s, bool quad = false);
 // A conv sum's bias: db (+)= the splits of part_db [splits, p] in order, with nz's noise
 // (nz->applied_b is then set).
 cudaError_t conv_bias_reduce(const float* part_db, int splits, int p, float* db, int accumulate, cudaStream_t s,
