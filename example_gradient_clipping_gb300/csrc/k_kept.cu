@@ -7,10 +7,15 @@
 // [MixGhost] section 2 ("Previous arts") does -- fast but memory-costly -- at the 2BpD
 // time of its Appendix C.5, instead of a second contraction over the T rows (2BTpD).
 //
-// kept_wsum_kernel: examples split over blockIdx.y; thread = 4 consecutive elements of the
-// weight part (then of the bias part), summing c_i g_i over the split's examples in order;
-// the fixed-order reduction over the splits follows (conv: mapping the kernel's tile
-// column order back to the weight layout).
+// kept_wsum_direct_kernel (the sums without fused noise): a block per chunk of kPer 4-element
+// items of the per-example layout, over all B examples: its kGroups thread groups sum
+// c_i g_i over consecutive example ranges in order, sixteen examples' loads in flight, then
+// the groups' sums are added in group order and written straight to their weight (or bias)
+// positions -- one launch and one read of the kept gradients, no partial sums.
+// kept_wsum_kernel (the noised sums): examples split over blockIdx.y; thread = 4 consecutive
+// elements of the weight part (then of the bias part), summing c_i g_i over the split's
+// examples in order; the fixed-order reduction over the splits follows, drawing the noise
+// (conv: mapping the kernel's tile column order back to the weight layout).
 #include <algorithm>
 
 #include "tc.cuh"
@@ -59,6 +64,89 @@ __global__ void __launch_bounds__(256) kept_wsum_kernel(const float* __restrict_
   }
 }
 
+constexpr int kPer = 64, kGroups = 8;   // items per block, example groups (512 threads)
+
+// Weight position of element f of a kept gradient's per-example layout: conv_kk == 0 the
+// weight layout itself; else tile columns col = (c / 64 * kk + tap) * 64 + c % 64 of rows n,
+// stored [n][col] (width D) or column-quad major ([col / 4][n][4]), mapped to n * D + c * kk + tap.
+__device__ __forceinline__ long kept_pos(size_t f, int p, int D, int kk, int quad) {
+  if (kk == 0) return (long)f;
+  int n, col;
+  if (quad) {
+    const size_t qd = f / (4 * (size_t)p), r = f - qd * 4 * (size_t)p;
+    n = (int)(r >> 2);
+    col = (int)(qd * 4 + (r & 3));
+  } else {
+    n = (int)(f / D);
+    col = (int)(f - (size_t)n * D);
+  }
+  const int blk = col >> 6, tap = blk % kk, c = (blk / kk) * 64 + (col & 63);
+  if (c * kk >= D) return -1;   // (no such channel)
+  return (long)n * D + (long)c * kk + tap;
+}
+
+__global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
+    const float* __restrict__ keep, const float* __restrict__ keep_b, const float* __restrict__ factors, int B,
+    size_t nw, int p, int D, int kk, int quad, float* __restrict__ dW, float* __restrict__ db, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float4 red[kGroups][kPer];
+  const size_t iw = nw / 4, items = iw + (keep_b ? (size_t)p / 4 : 0);
+  const int lane_item = threadIdx.x % kPer, grp = threadIdx.x / kPer;
+  const size_t it = (size_t)blockIdx.x * kPer + lane_item;
+  const int eg = (B + kGroups - 1) / kGroups, e0 = grp * eg, e1 = min(B, e0 + eg);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (it < items) {
+    const bool w = it < iw;
+    const float* src = w ? keep + it * 4 : keep_b + (it - iw) * 4;
+    const size_t stride = w ? nw : (size_t)p;
+    for (int e = e0; e < e1; e += 16) {   // sixteen examples' loads in flight, summed in order
+      float4 v[16];
+      float c[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (e + q < e1) {
+          v[q] = __ldcs(reinterpret_cast<const float4*>(src + (size_t)(e + q) * stride));
+          c[q] = __ldg(factors + e + q);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (e + q < e1) {
+          acc.x = fmaf(c[q], v[q].x, acc.x);
+          acc.y = fmaf(c[q], v[q].y, acc.y);
+          acc.z = fmaf(c[q], v[q].z, acc.z);
+          acc.w = fmaf(c[q], v[q].w, acc.w);
+        }
+      }
+    }
+  }
+  red[grp][lane_item] = acc;
+  __syncthreads();
+  if (grp == 0 && it < items) {
+    float4 s = red[0][lane_item];
+#pragma unroll
+    for (int g = 1; g < kGroups; ++g) {
+      const float4 t = red[g][lane_item];
+      s.x += t.x;
+      s.y += t.y;
+      s.z += t.z;
+      s.w += t.w;
+    }
+    const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (it < iw) {
+        const long m = kept_pos(it * 4 + i, p, D, kk, quad);
+        if (m >= 0) dW[m] = accumulate ? dW[m] + sv[i] : sv[i];
+      } else {
+        const size_t j = (it - iw) * 4 + i;
+        db[j] = accumulate ? db[j] + sv[i] : sv[i];
+      }
+    }
+  }
+}
+
 }  // namespace dpk
 
 namespace dph {
@@ -82,12 +170,18 @@ cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep,
                             const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s,
                             NoiseArgs* nz, bool quad) {
   if (((size_t)p * D) % 4 || p % 4) return cudaErrorInvalidValue;
+  const bool bias = db && keep_b;
+  const size_t nw = (size_t)p * D;
+  if (!(nz && nz->on)) {   // one launch, straight to dW and db
+    const size_t items = nw / 4 + (bias ? (size_t)p / 4 : 0);
+    launch_pdl(kept_wsum_direct_kernel, (unsigned)((items + kPer - 1) / kPer), kPer * kGroups, 0, s, keep,
+               bias ? keep_b : nullptr, factors, B, nw, p, D, conv_kk, quad ? 1 : 0, dW, db, accumulate);
+    return cudaGetLastError();
+  }
   const int splits = kept_splits(B, p, D);
   const int eps = (B + splits - 1) / splits;
-  const size_t nw = (size_t)p * D;
   float* part = ws;
   float* part_b = ws + (size_t)splits * nw;
-  const bool bias = db && keep_b;
   const size_t items = nw / 4 + (bias ? (size_t)p / 4 : 0);
   const unsigned bx = (unsigned)std::min<size_t>((items + 255) / 256, 152 * 8);
   launch_pdl(kept_wsum_kernel, dim3(bx, (unsigned)splits), 256, 0, s, keep, bias ? keep_b : nullptr, factors, B, nw,
@@ -95,8 +189,10 @@ cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep,
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (conv_kk > 0) {
-    e = launch_conv_reduce(part, splits, p, D, conv_kk, dW, accumulate, s, quad);
-    if (e != cudaSuccess || !bias) return e;
+    const bool nb = nz && nz->on;   // a noised bias keeps its own reduction (which draws it)
+    e = launch_conv_reduce(part, splits, p, D, conv_kk, dW, accumulate, s, quad, bias && !nb ? part_b : nullptr,
+                           db);
+    if (e != cudaSuccess || !bias || !nb) return e;
     return conv_bias_reduce(part_b, splits, p, db, accumulate, s, nz);
   }
   return launch_reduce_splits2(SplitSeg{part, nw, nw, dW}, SplitSeg{part_b, (size_t)p, bias ? (size_t)p : 0, db},

@@ -446,8 +446,8 @@ cudaError_t launch_tc_halo_norm(const Geom& g, const void* A, const void* G, flo
   if (!g.nhwc) {
     Xh = w;
     Gr = w + halo_xbytes(g);
-    e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, w, s);                        // NCHW -> NHWC
-    if (e == cudaSuccess) e = launch_transpose_rows(g.B, g.T, g.p, G, w + halo_xbytes(g), s);   // [p, T] -> [T, p]
+    // NCHW -> NHWC, [p, T] -> [T, p]: one launch
+    e = launch_transpose_rows2(g.B, g.H * g.W, g.Cin, A, w, g.T, g.p, G, w + halo_xbytes(g), s);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mX, mG;

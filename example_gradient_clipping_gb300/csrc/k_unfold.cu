@@ -162,6 +162,52 @@ __global__ void transpose_rows_vec_kernel(int B, int T, int p, int tt, const __n
   }
 }
 
+// Two unscaled transposes in one launch (the conv kernels' input and output-gradient copies):
+// units of the first, then of the second, through the same 64 x 64 tile as above.
+struct TransposeJob {
+  int T, p, tt;
+  const __nv_bfloat16* src;
+  __nv_bfloat16* dst;
+  long units;
+};
+__global__ void transpose_rows_vec2_kernel(int B, TransposeJob j0, TransposeJob j1) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ __align__(16) __nv_bfloat16 s[kTT][kTT];
+  for (long uu = blockIdx.x; uu < j0.units + j1.units; uu += gridDim.x) {
+    const bool second = uu >= j0.units;
+    const TransposeJob& J = second ? j1 : j0;
+    const long u = second ? uu - j0.units : uu;
+    const int nt = (J.T + J.tt - 1) / J.tt, tp = (J.p + kTT - 1) / kTT;
+    const int tch = J.tt / 8;
+    const int i = (int)(u / ((long)nt * tp));
+    const int rem = (int)(u - (long)i * nt * tp);
+    const int t0 = (rem / tp) * J.tt, jj0 = (rem % tp) * kTT;
+    const __nv_bfloat16* gi = J.src + (size_t)i * J.T * J.p;
+    for (int q = threadIdx.x; q < kTT * tch; q += blockDim.x) {
+      const int jr = q / tch, tc = q - jr * tch;
+      const int j = jj0 + jr, t = t0 + tc * 8;
+      if (j < J.p && t < J.T)
+        *reinterpret_cast<uint4*>(&s[jr][(tc ^ ((jr >> 3) & 7)) * 8]) =
+            __ldcs(reinterpret_cast<const uint4*>(gi + (size_t)j * J.T + t));
+    }
+    __syncthreads();
+    __nv_bfloat16* go = J.dst + (size_t)i * J.T * J.p;
+    for (int q = threadIdx.x; q < J.tt * (kTT / 8); q += blockDim.x) {
+      const int tr = q >> 3, jc = q & 7;
+      const int t = t0 + tr, j = jj0 + jc * 8;
+      if (t < J.T && j < J.p) {
+        __align__(16) __nv_bfloat16 v[8];
+        const int col = ((tr >> 3) ^ jc) * 8 + (tr & 7);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) v[r] = s[jc * 8 + r][col];
+        *reinterpret_cast<uint4*>(go + (size_t)t * J.p + j) = *reinterpret_cast<const uint4*>(v);
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // Rows with T % 8 != 0 (p % 8 == 0): one thread per (example, 8 outputs j0 .. j0+7),
 // over all T pixels: gathers eight rows of G_i per pixel, one 16-byte store each.
 __global__ void transpose_rows_short_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
@@ -338,6 +384,28 @@ cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* ds
     dim3 grid((T + 31) / 32, (p + 31) / 32, std::min(B, 65535));
     launch_plain(transpose_rows_kernel, grid, dim3(32, 8), 0, s, B, T, p, Gb, Gtb);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_rows2(int B, int T0, int p0, const void* src0, void* dst0, int T1, int p1, const void* src1,
+                                   void* dst1, cudaStream_t s) {
+  if (T0 % 8 || p0 % 8 || T1 % 8 || p1 % 8) {
+    const cudaError_t e = launch_transpose_rows(B, T0, p0, src0, dst0, s);
+    return e != cudaSuccess ? e : launch_transpose_rows(B, T1, p1, src1, dst1, s);
+  }
+  auto job = [&](int T, int p, const void* src, void* dst) {
+    TransposeJob J;
+    J.T = T;
+    J.p = p;
+    J.tt = std::min(kTT, T);
+    J.src = static_cast<const __nv_bfloat16*>(src);
+    J.dst = static_cast<__nv_bfloat16*>(dst);
+    J.units = (long)B * ((T + J.tt - 1) / J.tt) * ((p + kTT - 1) / kTT);
+    return J;
+  };
+  const TransposeJob a = job(T0, p0, src0, dst0), b = job(T1, p1, src1, dst1);
+  const unsigned blocks = (unsigned)std::min<long>(a.units + b.units, 152L * 16);
+  launch_plain(transpose_rows_vec2_kernel, blocks, 256, 0, s, B, a, b);
   return cudaGetLastError();
 }
 

@@ -74,6 +74,9 @@ cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* 
 // Per example [p, T] -> [T, p] (bf16): the output gradient's row layout, and NCHW -> NHWC.
 cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s,
                                   const float* scale = nullptr, float* bias_part = nullptr);
+// Two such transposes (same B) in one launch.
+cudaError_t launch_transpose_rows2(int B, int T0, int p0, const void* src0, void* dst0, int T1, int p1, const void* src1,
+                                   void* dst1, cudaStream_t s);
 // Gt = bf16(c_i G_i^T) for the row-scaled clipped sum, and db (+)= sum_i c_i sum_t G[i, :, t]
 // from fp32 partial sums taken on the way (bias_part: scaled_rows_bias_bytes).
 cudaError_t launch_scaled_rows(int B, int T, int p, const void* G, void* Gt, const float* factors, float* db,
@@ -96,9 +99,11 @@ cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, cons
 bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pixels);
 // dW[j, m] (+)= sum over splits of part[s, j, col(m)], col mapping the weight column
 // m = c*kk + tap to the im2col tile column (c/64 * kk + tap) * 64 + c % 64; `quad`: part's
-// rows stored column-quad major, [ncols / 4][p][4].
+// rows stored column-quad major, [ncols / 4][p][4].  With part_b, also db (+)= the splits of
+// part_b [splits, p] in order, in the same launch.
 cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
-                               cudaStream_t s, bool quad = false);
+                               cudaStream_t s, bool quad = false, const float* part_b = nullptr,
+                               float* db = nullptr);
 // A conv sum's bias: db (+)= the splits of part_db [splits, p] in order, with nz's noise
 // (nz->applied_b is then set).
 cudaError_t conv_bias_reduce(const float* part_db, int splits, int p, float* db, int accumulate, cudaStream_t s,
