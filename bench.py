@@ -147,8 +147,7 @@ class ClockSampler:
 
 
 # Kernels that serve each call on the tensor-core paths (for the DRAM traffic record).
-_DOMINANT_KERNELS = {"sums": ["tc_sumx_kernel", "tc_sum_kernel", "tc_conv_kernel", "kept_wsum_direct_kernel",
-                              "kept_wsum_kernel"],
+_DOMINANT_KERNELS = {"sums": ["tc_sumx_kernel", "tc_sum_kernel", "tc_conv_kernel", "kept_wsum_direct_kernel"],
                      "norms": ["tc_ghost_kernel", "tc_conv_kernel", "tc_halo_kernel", "tc_unfold_kernel",
                                "tc_sumx_kernel"],
                      "noise": ["add_noise_kernel"], "factors": ["clip_factors_kernel"]}

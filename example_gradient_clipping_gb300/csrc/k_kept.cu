@@ -7,62 +7,17 @@
 // [MixGhost] section 2 ("Previous arts") does -- fast but memory-costly -- at the 2BpD
 // time of its Appendix C.5, instead of a second contraction over the T rows (2BTpD).
 //
-// kept_wsum_direct_kernel (the sums without fused noise): a block per chunk of kPer 4-element
-// items of the per-example layout, over all B examples: its kGroups thread groups sum
-// c_i g_i over consecutive example ranges in order, sixteen examples' loads in flight, then
-// the groups' sums are added in group order and written straight to their weight (or bias)
-// positions -- one launch and one read of the kept gradients, no partial sums.
-// kept_wsum_kernel (the noised sums): examples split over blockIdx.y; thread = 4 consecutive
-// elements of the weight part (then of the bias part), summing c_i g_i over the split's
-// examples in order; the fixed-order reduction over the splits follows, drawing the noise
-// (conv: mapping the kernel's tile column order back to the weight layout).
+// kept_wsum_direct_kernel: a block per chunk of kPer 4-element items of the per-example
+// layout, over all B examples: its kGroups thread groups sum c_i g_i over consecutive
+// example ranges in order, sixteen examples' loads in flight, then the groups' sums are added
+// in group order and written straight to their weight (or bias) positions (conv: mapping the
+// kernel's tile column order back to the weight layout) -- one launch and one read of the
+// kept gradients, no partial sums.  A noised call's noise pass follows (the caller's).
 #include <algorithm>
 
 #include "tc.cuh"
 
 namespace dpk {
-
-__global__ void __launch_bounds__(256) kept_wsum_kernel(const float* __restrict__ keep, const float* __restrict__ keep_b,
-                                                        const float* __restrict__ factors, int B, size_t nw, int p,
-                                                        int eps, float* __restrict__ part, float* __restrict__ part_b) {
-  pdl_trigger();
-  pdl_wait();
-  const int e0 = blockIdx.y * eps, e1 = min(B, e0 + eps);
-  const size_t iw = nw / 4, items = iw + (keep_b ? (size_t)p / 4 : 0);
-  for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (size_t)gridDim.x * blockDim.x) {
-    const bool w = it < iw;
-    const float* src = w ? keep + it * 4 : keep_b + (it - iw) * 4;
-    const size_t stride = w ? nw : (size_t)p;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int e = e0;
-    for (; e + 4 <= e1; e += 4) {          // four examples' loads in flight, summed in order
-      float4 v[4];
-      float c[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        v[q] = __ldcs(reinterpret_cast<const float4*>(src + (size_t)(e + q) * stride));
-        c[q] = __ldg(factors + e + q);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc.x = fmaf(c[q], v[q].x, acc.x);
-        acc.y = fmaf(c[q], v[q].y, acc.y);
-        acc.z = fmaf(c[q], v[q].z, acc.z);
-        acc.w = fmaf(c[q], v[q].w, acc.w);
-      }
-    }
-    for (; e < e1; ++e) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(src + (size_t)e * stride));
-      const float c = __ldg(factors + e);
-      acc.x = fmaf(c, v.x, acc.x);
-      acc.y = fmaf(c, v.y, acc.y);
-      acc.z = fmaf(c, v.z, acc.z);
-      acc.w = fmaf(c, v.w, acc.w);
-    }
-    float* dst = w ? part + (size_t)blockIdx.y * nw + it * 4 : part_b + (size_t)blockIdx.y * p + (it - iw) * 4;
-    *reinterpret_cast<float4*>(dst) = acc;
-  }
-}
 
 constexpr int kPer = 64, kGroups = 8;   // items per block, example groups (512 threads)
 
@@ -152,51 +107,17 @@ __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
 namespace dph {
 using namespace dpk;
 
-// Example splits: enough blocks to cover the SMs a few times over.
-static int kept_splits(int B, int p, int D) {
-  const size_t items = ((size_t)p * D + p) / 4;
-  const long per_split = (long)std::max<size_t>(1, (items + 255) / 256);
-  long s = std::max<long>(1, std::min<long>(B, (152L * 4 + per_split - 1) / per_split));
-  const int eps = (int)((B + s - 1) / s);
-  return (B + eps - 1) / eps;
-}
-
-size_t kept_sum_ws_bytes(int B, int p, int D) {
-  const int s = kept_splits(B, p, D);
-  return (size_t)s * ((size_t)p * D + p) * sizeof(float);
-}
+size_t kept_sum_ws_bytes(int, int, int) { return 256; }
 
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
-                            const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s,
-                            NoiseArgs* nz, bool quad) {
+                            const float* factors, float* dW, float* db, int accumulate, cudaStream_t s, bool quad) {
   if (((size_t)p * D) % 4 || p % 4) return cudaErrorInvalidValue;
   const bool bias = db && keep_b;
   const size_t nw = (size_t)p * D;
-  if (!(nz && nz->on)) {   // one launch, straight to dW and db
-    const size_t items = nw / 4 + (bias ? (size_t)p / 4 : 0);
-    launch_pdl(kept_wsum_direct_kernel, (unsigned)((items + kPer - 1) / kPer), kPer * kGroups, 0, s, keep,
-               bias ? keep_b : nullptr, factors, B, nw, p, D, conv_kk, quad ? 1 : 0, dW, db, accumulate);
-    return cudaGetLastError();
-  }
-  const int splits = kept_splits(B, p, D);
-  const int eps = (B + splits - 1) / splits;
-  float* part = ws;
-  float* part_b = ws + (size_t)splits * nw;
   const size_t items = nw / 4 + (bias ? (size_t)p / 4 : 0);
-  const unsigned bx = (unsigned)std::min<size_t>((items + 255) / 256, 152 * 8);
-  launch_pdl(kept_wsum_kernel, dim3(bx, (unsigned)splits), 256, 0, s, keep, bias ? keep_b : nullptr, factors, B, nw,
-             p, eps, part, part_b);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (conv_kk > 0) {
-    const bool nb = nz && nz->on;   // a noised bias keeps its own reduction (which draws it)
-    e = launch_conv_reduce(part, splits, p, D, conv_kk, dW, accumulate, s, quad, bias && !nb ? part_b : nullptr,
-                           db);
-    if (e != cudaSuccess || !bias || !nb) return e;
-    return conv_bias_reduce(part_b, splits, p, db, accumulate, s, nz);
-  }
-  return launch_reduce_splits2(SplitSeg{part, nw, nw, dW}, SplitSeg{part_b, (size_t)p, bias ? (size_t)p : 0, db},
-                               splits, accumulate, s, nz);
+  launch_pdl(kept_wsum_direct_kernel, (unsigned)((items + kPer - 1) / kPer), kPer * kGroups, 0, s, keep,
+             bias ? keep_b : nullptr, factors, B, nw, p, D, conv_kk, quad ? 1 : 0, dW, db, accumulate);
+  return cudaGetLastError();
 }
 
 }  // namespace dph

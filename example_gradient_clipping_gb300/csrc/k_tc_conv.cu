@@ -340,33 +340,21 @@ tc_conv_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__
 }
 
 // dW[j, m] (+)= sum_s part[s, j, n(m)] in split order; n(m) maps the weight column
-// m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64); with `quad` a split's
-// [p, ncols] block is stored column-quad major ([ncols / 4][p][4]).  Threads past the weight
-// outputs form db[j] (+)= sum_s part_b[s, j] when part_b is given.  (The noise of a fused
+// m = c*k*k + tap to the tile column (64*(c/64)*k*k + 64*tap + c%64).  (The noise of a fused
 // call is not drawn here: one output per thread would draw a whole Philox block per output,
 // which measured slower than the separate four-outputs-per-block noise pass on the large
 // layers; grouping four outputs per thread instead starved the small layers of threads.)
 __global__ void conv_reduce_kernel(const float* __restrict__ part, int splits, int p, int ncols, int kk,
-                                   float* __restrict__ dW, int accumulate, int quad,
-                                   const float* __restrict__ part_b, float* __restrict__ db) {
+                                   float* __restrict__ dW, int accumulate) {
   pdl_trigger();
   pdl_wait();
   const size_t n = (size_t)p * ncols;
-  const size_t nt = n + (part_b ? (size_t)p : 0);
-  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < nt; q += (size_t)gridDim.x * blockDim.x) {
-    if (q >= n) {
-      const int j = (int)(q - n);
-      float s = 0.f;
-      for (int sp = 0; sp < splits; ++sp) s += part_b[(size_t)sp * p + j];
-      db[j] = accumulate ? db[j] + s : s;
-      continue;
-    }
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
     const int j = (int)(q / ncols), m = (int)(q - (size_t)j * ncols);
     const int cch = m / kk, tap = m - cch * kk;
     const int col = ((cch >> 6) * kk + tap) * 64 + (cch & 63);
-    const size_t at = quad ? ((size_t)(col >> 2) * p + j) * 4 + (col & 3) : (size_t)j * ncols + col;
     float s = 0.f;
-    for (int sp = 0; sp < splits; ++sp) s += part[(size_t)sp * p * ncols + at];
+    for (int sp = 0; sp < splits; ++sp) s += part[((size_t)sp * p + j) * ncols + col];
     dW[q] = accumulate ? dW[q] + s : s;
   }
 }
@@ -476,11 +464,10 @@ static bool encode_maps(const Geom& g, const void* Xh, const void* G, CUtensorMa
 }
 
 cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
-                               cudaStream_t s, bool quad, const float* part_b, float* db) {
-  const size_t n = (size_t)p * ncols + (part_b ? (size_t)p : 0);
+                               cudaStream_t s) {
+  const size_t n = (size_t)p * ncols;
   const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 8);
-  launch_plain(tcconv::conv_reduce_kernel, blocks ? blocks : 1, 256, 0, s, part, splits, p, ncols, kk, dW, accumulate,
-               quad ? 1 : 0, part_b, db);
+  launch_plain(tcconv::conv_reduce_kernel, blocks ? blocks : 1, 256, 0, s, part, splits, p, ncols, kk, dW, accumulate);
   return cudaGetLastError();
 }
 

@@ -33,10 +33,11 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
 // (2pD flop per example, one read of the kept gradients).  conv_kk > 0: g_i in the conv
 // kernel's tile column order with that many filter taps (mapped back to [p, Cin, k, k]);
 // `quad`: g_i stored column-quad major, [D / 4][p][4] (the shifted-tile kernel's stores).
+// No noise: a noised call adds its noise pass afterwards.
 size_t kept_sum_ws_bytes(int B, int p, int D);
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
-                            const float* factors, float* dW, float* db, int accumulate, float* ws, cudaStream_t s,
-                            dpk::NoiseArgs* nz = nullptr, bool quad = false);
+                            const float* factors, float* dW, float* db, int accumulate, cudaStream_t s,
+                            bool quad = false);
 // Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
 // Stride-1 "same" conv layers over 64 input channels: every filter tap a shifted view of one
@@ -99,11 +100,8 @@ cudaError_t launch_tc_conv_sum(const Geom& g, const void* A, const void* G, cons
 bool encode_im2col_bf16(CUtensorMap* map, const void* Xh, const Geom& g, int pixels);
 // dW[j, m] (+)= sum over splits of part[s, j, col(m)], col mapping the weight column
 // m = c*kk + tap to the im2col tile column (c/64 * kk + tap) * 64 + c % 64; `quad`: part's
-// rows stored column-quad major, [ncols / 4][p][4].  With part_b, also db (+)= the splits of
-// part_b [splits, p] in order, in the same launch.
 cudaError_t launch_conv_reduce(const float* part, int splits, int p, int ncols, int kk, float* dW, int accumulate,
-                               cudaStream_t s, bool quad = false, const float* part_b = nullptr,
-                               float* db = nullptr);
+                               cudaStream_t s);
 // A conv sum's bias: db (+)= the splits of part_db [splits, p] in order, with nz's noise
 // (nz->applied_b is then set).
 cudaError_t conv_bias_reduce(const float* part_db, int splits, int p, float* db, int accumulate, cudaStream_t s,
