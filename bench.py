@@ -303,6 +303,9 @@ FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 def roofline(wl, work, means, pk, peak_kind="burst"):
     """Roofline object of the step's dominant call (largest per-call mean)."""
     dom = max(("norms", "factors", "sums", "noise"), key=means.get)   # sums_noised: the step's fused form
+    if not means[dom] > 0:   # the per-call timing gave nothing (e.g. under a profiler): no figure
+        return dict(bound=None, achieved=None, peak=None, unit=None, frac=None, traffic=None, kernel=None,
+                    peak_source=None)
     tc_peak = pk["bf16"] if peak_kind == "burst" else pk["bf16_sus"]
     sum_bytes = work["kept_bytes"] + 4 * work["n_params"]     # kept gradients read, sums written
     if dom in ("sums", "norms") and wl.dtype == "fp32":
