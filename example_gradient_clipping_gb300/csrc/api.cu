@@ -681,7 +681,8 @@ static dp_status kept_sum_impl(const dp_layer_desc* desc, const float* grads, co
     kdb = db ? kdW + align256((size_t)g.p * width * 4) / 4 : nullptr;
   }
   cudaError_t e = dph::launch_kept_sum(g.B, g.p, width, conv_kk, grads, keep_b, factors, kdW, kdb,
-                                       padded ? 0 : accumulate, stream, pl.kernel == NK_TC_HALO);
+                                       padded ? 0 : accumulate, stream, pl.kernel == NK_TC_HALO,
+                                       padded ? nullptr : nz);   // (a padded sum gets its noise after compaction)
   if (e == cudaSuccess && padded) {
     e = dph::launch_compact_cols(kdW, g.p, g.D, width, dW, accumulate, stream);
     if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);

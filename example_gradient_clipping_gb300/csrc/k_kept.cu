@@ -12,7 +12,9 @@
 // example ranges in order, sixteen examples' loads in flight, then the groups' sums are added
 // in group order and written straight to their weight (or bias) positions (conv: mapping the
 // kernel's tile column order back to the weight layout) -- one launch and one read of the
-// kept gradients, no partial sums.  A noised call's noise pass follows (the caller's).
+// kept gradients, no partial sums.  With nz on, each output also gets its noise and the 1/B
+// scale on the way out, z drawn at its flat index with the noise pass's arithmetic (so the
+// result is the same as the sum followed by that pass).
 #include <algorithm>
 
 #include "tc.cuh"
@@ -42,9 +44,11 @@ __device__ __forceinline__ long kept_pos(size_t f, int p, int D, int kk, int qua
 
 __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
     const float* __restrict__ keep, const float* __restrict__ keep_b, const float* __restrict__ factors, int B,
-    size_t nw, int p, int D, int kk, int quad, float* __restrict__ dW, float* __restrict__ db, int accumulate) {
+    size_t nw, int p, int D, int kk, int quad, float* __restrict__ dW, float* __restrict__ db, int accumulate,
+    NoiseArgs nz) {
   pdl_trigger();
   pdl_wait();
+  const uint64_t seed = nz.on && nz.seed_dev ? (uint64_t)*nz.seed_dev : nz.seed;
   __shared__ float4 red[kGroups][kPer];
   const size_t iw = nw / 4, items = iw + (keep_b ? (size_t)p / 4 : 0);
   const int lane_item = threadIdx.x % kPer, grp = threadIdx.x / kPer;
@@ -93,10 +97,16 @@ __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
     for (int i = 0; i < 4; ++i) {
       if (it < iw) {
         const long m = kept_pos(it * 4 + i, p, D, kk, quad);
-        if (m >= 0) dW[m] = accumulate ? dW[m] + sv[i] : sv[i];
+        if (m >= 0) {
+          float v = accumulate ? dW[m] + sv[i] : sv[i];
+          if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_a + (uint64_t)m, seed), v) * nz.invB;
+          dW[m] = v;
+        }
       } else {
         const size_t j = (it - iw) * 4 + i;
-        db[j] = accumulate ? db[j] + sv[i] : sv[i];
+        float v = accumulate ? db[j] + sv[i] : sv[i];
+        if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_b + j, seed), v) * nz.invB;
+        db[j] = v;
       }
     }
   }
@@ -110,14 +120,22 @@ using namespace dpk;
 size_t kept_sum_ws_bytes(int, int, int) { return 256; }
 
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
-                            const float* factors, float* dW, float* db, int accumulate, cudaStream_t s, bool quad) {
+                            const float* factors, float* dW, float* db, int accumulate, cudaStream_t s, bool quad,
+                            NoiseArgs* nz) {
   if (((size_t)p * D) % 4 || p % 4) return cudaErrorInvalidValue;
   const bool bias = db && keep_b;
   const size_t nw = (size_t)p * D;
   const size_t items = nw / 4 + (bias ? (size_t)p / 4 : 0);
+  NoiseArgs none = {};
+  const NoiseArgs& na = nz && nz->on ? *nz : none;
   launch_pdl(kept_wsum_direct_kernel, (unsigned)((items + kPer - 1) / kPer), kPer * kGroups, 0, s, keep,
-             bias ? keep_b : nullptr, factors, B, nw, p, D, conv_kk, quad ? 1 : 0, dW, db, accumulate);
-  return cudaGetLastError();
+             bias ? keep_b : nullptr, factors, B, nw, p, D, conv_kk, quad ? 1 : 0, dW, db, accumulate, na);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && nz && nz->on) {
+    nz->applied_a = 1;
+    nz->applied_b = bias ? 1 : nz->applied_b;
+  }
+  return e;
 }
 
 }  // namespace dph

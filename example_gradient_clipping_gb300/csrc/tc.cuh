@@ -33,11 +33,11 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
 // (2pD flop per example, one read of the kept gradients).  conv_kk > 0: g_i in the conv
 // kernel's tile column order with that many filter taps (mapped back to [p, Cin, k, k]);
 // `quad`: g_i stored column-quad major, [D / 4][p][4] (the shifted-tile kernel's stores).
-// No noise: a noised call adds its noise pass afterwards.
+// With nz on, the noise and the 1/B scale in the same pass (nz->applied_* set).
 size_t kept_sum_ws_bytes(int B, int p, int D);
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
                             const float* factors, float* dW, float* db, int accumulate, cudaStream_t s,
-                            bool quad = false);
+                            bool quad = false, dpk::NoiseArgs* nz = nullptr);
 // Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
 // Stride-1 "same" conv layers over 64 input channels: every filter tap a shifted view of one

@@ -130,22 +130,21 @@ class ClipStep:
                 dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
 
     def sums_noised(self, inputs, seed: int = 0, seed_dev=None, stream=None) -> None:
-        """sums() and noise() together.  Linear layers' clipped sum calls add their blocks'
-        noise and the 1/B scale in the sum's final reduction (dp_clipped_sum_noised); the
-        conv layers' weight sums end in a column-mapping pass that does not draw noise, so
-        their blocks get theirs from one multi-block noise launch after the sums
-        (dp_add_noise_blocks) instead of one noise pass per layer."""
+        """sums() and noise() together.  Linear layers' clipped sum calls and every layer's
+        sum from kept gradients add their blocks' noise and the 1/B scale in the sum's final
+        pass (dp_clipped_sum_noised, dp_clipped_sum_kept_noised); the other conv layers'
+        weight sums end in a column-mapping pass that does not draw noise, so their blocks get
+        theirs from one multi-block noise launch after the sums (dp_add_noise_blocks) instead
+        of one noise pass per layer."""
         blocks = []
         for l, (d, (A, G)) in enumerate(zip(self.descs, inputs)):
             dW, db = self.layer_views(l)
             fac = self.factors[l] if self.per_layer else self.factors[0]
             C = self.C[l] if self.per_layer else self.C[0]
-            if d.kind != DP_LINEAR:
+            if d.kind != DP_LINEAR and self.kept[l] is None:
                 p, D = self.shapes[l]
                 blocks.append((self.offsets[l], p * D + (p if d.has_bias else 0), C))
-                if self.kept[l] is not None:
-                    dp_clipped_sum_kept(d, self.kept[l], fac, dW, db, self.workspace, stream=stream)
-                elif self.own_ws[l] is not None:
+                if self.own_ws[l] is not None:
                     dp_clipped_sum_reuse(d, self.modes[l], A, G, fac, dW, db, self.own_ws[l], stream=stream)
                 else:
                     dp_clipped_sum(d, A, G, fac, dW, db, self.workspace, stream=stream)
