@@ -64,7 +64,7 @@ struct Params {
 };
 
 struct Ctl {
-  uint64_t full[MAXST], empty[MAXST], accum[2], tfree[2], drain;
+  uint64_t full[MAXST], empty[MAXST], accum[2], tfree[2][MAXG], drain;
   uint32_t tmem;
   int abort;
   float red[kEpiWarps];
@@ -127,8 +127,11 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mX,
 }
 
 // Warp 1: per example, every stage's K steps: B = the input views (all kw), one MMA per
-// filter-row pair.  The stage's tile offsets advance without divisions and the descriptors by
-// one K step (2048 bytes) at a time: the issuing thread's work between MMAs is a few adds.
+// filter-row pair, a stage's K steps group by group.  Each group's TMEM is released on its own
+// (tfree[b][g]), so the next example's first MMAs into group 0 start while the epilogue still
+// drains group 1 (with one 384-column buffer the whole drain would otherwise idle the tensor
+// pipe).  The stage's tile offsets advance without divisions and the descriptors by one K step
+// (2048 bytes) at a time: the issuing thread's work between MMAs is a few adds.
 __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* c, uint32_t tmem, int e0, int e1) {
   volatile int* abort = &c->abort;
   const uint32_t idesc = ptx::idesc_bf16_f32(128, P.N, 1, 1);
@@ -148,11 +151,6 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
   bool live = true;
   for (int x = 0; x < e1 - e0 && live; ++x) {
     const int b = x % P.nbuf;
-    if (x >= P.nbuf) {
-      const bool w = ptx::mbar_wait(&c->tfree[b], ((x / P.nbuf) & 1) ^ 1, abort, P.status);
-      if (!__all_sync(0xffffffffu, w)) break;
-    }
-    ptx::tc_fence_after();
     const uint32_t dbase = tmem + b * P.ncols;
     // pixel offsets of the stage's first K pixel in its input tile (view b(0)) and in its
     // output-gradient tile (view a_lo): the remainders of x_row and g_row
@@ -163,22 +161,30 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
       if (!__all_sync(0xffffffffu, w)) { live = false; break; }
       const uint32_t st = ptx::smem_u32(smem + s * P.sbytes);
       const int nkq = (min(P.spx, P.nK - u * P.spx) + 15) >> 4;
-      if (ptx::elect_one()) {
-        uint64_t db = bbits | (uint64_t)(((st + (uint32_t)rx * 128) >> 4) & 0x3FFFu);
-        uint64_t da[MAXG];
+      const uint64_t db0 = bbits | (uint64_t)(((st + (uint32_t)rx * 128) >> 4) & 0x3FFFu);
 #pragma unroll
-        for (int g = 0; g < MAXG; ++g)
-          da[g] = dhi | lbo_bits[g] | (uint64_t)(((st + P.goff + (uint32_t)(rg + adelta[g]) * 128) >> 4) & 0x3FFFu);
-        for (int kq = 0; kq < nkq; ++kq) {
-#pragma unroll
-          for (int g = 0; g < MAXG; ++g) {
-            if (g < P.ngu) ptx::umma_bf16(dbase + g * P.N, da[g], db, idesc, (u | kq) != 0);
-            da[g] += 2048 >> 4;
+      for (int g = 0; g < MAXG; ++g) {
+        if (g >= P.ngu) break;
+        if (u == 0) {   // the group's TMEM columns, free once the epilogue has read example x - nbuf's
+          if (x >= P.nbuf) {
+            const bool w2 = ptx::mbar_wait(&c->tfree[b][g], ((x / P.nbuf) & 1) ^ 1, abort, P.status);
+            if (!__all_sync(0xffffffffu, w2)) { live = false; break; }
           }
-          db += 2048 >> 4;
+          ptx::tc_fence_after();
         }
-        ptx::umma_commit(&c->empty[s]);
+        if (ptx::elect_one()) {
+          uint64_t da = dhi | lbo_bits[g] | (uint64_t)(((st + P.goff + (uint32_t)(rg + adelta[g]) * 128) >> 4) & 0x3FFFu);
+          uint64_t db = db0;
+          for (int kq = 0; kq < nkq; ++kq) {
+            ptx::umma_bf16(dbase + g * P.N, da, db, idesc, (u | kq) != 0);
+            da += 2048 >> 4;
+            db += 2048 >> 4;
+          }
+        }
+        __syncwarp();
       }
+      if (!live) break;
+      if (ptx::elect_one()) ptx::umma_commit(&c->empty[s]);
       __syncwarp();
       rx += sr;
       if (rx >= P.Wp) rx -= P.Wp;
@@ -197,9 +203,10 @@ __device__ __forceinline__ void mma_issuer(const Params& P, uint8_t* smem, Ctl* 
 }
 
 // Warps 4-11, per example: first the bias sums from the output gradient in global memory, then
-// the example's TMEM: lane m of group g is half m / 64 (filter row kh0 or kh1), output m % 64;
-// its columns kw * 64 + c, the two warps of a lane quarter taking one half of them each, all
-// their loads in flight before one wait.
+// the example's TMEM group by group: lane m of group g is half m / 64 (filter row kh0 or kh1),
+// output m % 64; its columns kw * 64 + c, the two warps of a lane quarter taking one half of
+// them each, all their loads in flight before one wait, the group released before its squares
+// and stores.
 __device__ __forceinline__ void epilogue(const Params& P, Ctl* c, uint32_t tmem, int e0, int e1) {
   volatile int* abort = &c->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,6 +257,9 @@ __device__ __forceinline__ void epilogue(const Params& P, Ctl* c, uint32_t tmem,
         for (int i = 0; i < 3; ++i)
           if (i < nl) ptx::tmem_ld32(base + 32 * i, v[i]);
         ptx::tmem_wait_ld();
+        ptx::tc_fence_before();   // the group's columns are read: the next example's MMAs may start
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c->tfree[b][g]);
         if (valid) {
 #pragma unroll
           for (int i = 0; i < 3; ++i) {
@@ -268,9 +278,6 @@ __device__ __forceinline__ void epilogue(const Params& P, Ctl* c, uint32_t tmem,
           }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&c->tfree[b]);
     }
     if (duty) {   // b_i: the phases' sums (lanes chunk, chunk + ncp, ... of a warp, then the warps)
       for (int o = ncp; o < 32; o <<= 1)
@@ -318,7 +325,7 @@ tc_halo_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&c->accum[b], 1);
-      ptx::mbar_init(&c->tfree[b], kEpiWarps);
+      for (int g = 0; g < MAXG; ++g) ptx::mbar_init(&c->tfree[b][g], kEpiWarps);
     }
     ptx::mbar_init(&c->drain, 1);
     c->abort = 0;
