@@ -295,6 +295,9 @@ def max_over_ranks(v: float, device) -> float:
 # the adaptive bound) and flat.
 PER_CONFIG = ("t1_linear_b32", "seq_linear_b64_t128", "conv3x3_b256", "vgg11_cifar_b1024",
               "vgg11_cifar_b1024_flat")
+# ... and the conv workloads once more with channels-last conv inputs (DP_NHWC: no layout
+# copies), under "<name>/channels_last".
+PER_CONFIG_CHANNELS_LAST = ("conv3x3_b256", "vgg11_cifar_b1024")
 # FP32 FFMA peak for the fp32 one-row layer's FFMA kernels: 152 SMs x 128 FP32 lanes x
 # 2 flop x 2.07 GHz.
 FP32_FFMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
@@ -515,22 +518,23 @@ def run_ours(args, wl):
     per_config = {}
     if not args.no_per_config and wl.name == DEFAULT_WORKLOAD:
         k_steps = max(3, min(args.steps, 20))
-        for name in PER_CONFIG:
+        runs = [(n, False) for n in PER_CONFIG] + [(n, True) for n in PER_CONFIG_CHANNELS_LAST]
+        for name, cl2 in runs:
             import workloads
             w2 = workloads.get_workload(name)
-            b2 = StepBench(dp, w2, dev)
+            b2 = StepBench(dp, w2, dev, channels_last=cl2)
             b2.timed(b2.step.graph.replay, W, seed0, flush, stream)
             ms = b2.timed(b2.step.graph.replay, k_steps, seed0, flush, stream)
             m2 = b2.per_call_means(5, seed0, flush, stream)
             r2 = roofline(w2, b2.work, m2, pk, "burst")
             tot = max_over_ranks(sum(ms), dev)
-            per_config[name] = dict(
+            per_config[name + ("/channels_last" if cl2 else "")] = dict(
                 value=world * w2.B * k_steps / (tot / 1e3), unit="examples/s", ms_per_step=tot / k_steps,
                 steps=k_steps, dtype=w2.dtype, norm_modes=b2.modes, kernels_per_step=b2.step.graph_kernels,
                 step_flop=b2.work["flop_norm"] + b2.work["flop_sum"], step_bytes=b2.work["bytes_total"],
                 calls_ms={n: round(v, 5) for n, v in m2.items()},
                 roofline={k: r2[k] for k in ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic")},
-                description=w2.description)
+                conv_layout="channels last" if cl2 else "channels first", description=w2.description)
             b2.free()
             del b2
 

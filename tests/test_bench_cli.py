@@ -56,9 +56,10 @@ def test_bench_line_keys():
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     pc = d["per_config"]
     assert set(pc) == {"t1_linear_b32", "seq_linear_b64_t128", "conv3x3_b256", "vgg11_cifar_b1024",
-                       "vgg11_cifar_b1024_flat"}
+                       "vgg11_cifar_b1024_flat", "conv3x3_b256/channels_last", "vgg11_cifar_b1024/channels_last"}
     for name, c in pc.items():
         assert c["value"] > 0 and c["ms_per_step"] > 0 and c["roofline"]["frac"] > 0, name
+        assert c["conv_layout"] == ("channels last" if name.endswith("/channels_last") else "channels first"), name
     assert pc["vgg11_cifar_b1024"]["kernels_per_step"] > pc["vgg11_cifar_b1024_flat"]["kernels_per_step"]
 
 
