@@ -676,13 +676,15 @@ static dp_status kept_sum_impl(const dp_layer_desc* desc, const float* grads, co
   const bool padded = pl.rows && padded_out_bytes(g) != 0;
   float* kdW = dW;
   float* kdb = db;
+  void* wsp = workspace;
   if (padded) {     // rows of a conv layer whose unfolded width was padded: compact afterwards
-    kdW = static_cast<float*>(workspace);
+    kdW = static_cast<float*>(wsp);
     kdb = db ? kdW + align256((size_t)g.p * width * 4) / 4 : nullptr;
+    wsp = static_cast<uint8_t*>(wsp) + padded_out_bytes(g);
   }
   cudaError_t e = dph::launch_kept_sum(g.B, g.p, width, conv_kk, grads, keep_b, factors, kdW, kdb,
                                        padded ? 0 : accumulate, stream, pl.kernel == NK_TC_HALO,
-                                       padded ? nullptr : nz);   // (a padded sum gets its noise after compaction)
+                                       padded ? nullptr : nz, wsp);   // (a padded sum: its noise after compaction)
   if (e == cudaSuccess && padded) {
     e = dph::launch_compact_cols(kdW, g.p, g.D, width, dW, accumulate, stream);
     if (e == cudaSuccess && kdb) e = dph::launch_compact_cols(kdb, 1, g.p, g.p, db, accumulate, stream);

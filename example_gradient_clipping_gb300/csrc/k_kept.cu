@@ -14,7 +14,10 @@
 // kernel's tile column order back to the weight layout) -- one launch and one read of the
 // kept gradients, no partial sums.  With nz on, each output also gets its noise and the 1/B
 // scale on the way out, z drawn at its flat index with the noise pass's arithmetic (so the
-// result is the same as the sum followed by that pass).
+// result is the same as the sum followed by that pass).  Small layers (fewer item blocks than
+// half the SMs: VGG-11's first conv layer has 7) split the examples over blockIdx.y as well;
+// each split's group-ordered sums go to a partial row, and kept_wsum_finish_kernel adds the
+// splits in order and writes as above.
 #include <algorithm>
 
 #include "tc.cuh"
@@ -42,10 +45,34 @@ __device__ __forceinline__ long kept_pos(size_t f, int p, int D, int kk, int qua
   return (long)n * D + (long)c * kk + tap;
 }
 
+// Item it's four sums (s) to their weight or bias positions, with the accumulate flag and the
+// fused noise.
+__device__ __forceinline__ void kept_write(size_t it, size_t iw, float4 s, int p, int D, int kk, int quad,
+                                           float* __restrict__ dW, float* __restrict__ db, int accumulate,
+                                           const NoiseArgs& nz, uint64_t seed) {
+  const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (it < iw) {
+      const long m = kept_pos(it * 4 + i, p, D, kk, quad);
+      if (m >= 0) {
+        float v = accumulate ? dW[m] + sv[i] : sv[i];
+        if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_a + (uint64_t)m, seed), v) * nz.invB;
+        dW[m] = v;
+      }
+    } else {
+      const size_t j = (it - iw) * 4 + i;
+      float v = accumulate ? db[j] + sv[i] : sv[i];
+      if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_b + j, seed), v) * nz.invB;
+      db[j] = v;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
     const float* __restrict__ keep, const float* __restrict__ keep_b, const float* __restrict__ factors, int B,
     size_t nw, int p, int D, int kk, int quad, float* __restrict__ dW, float* __restrict__ db, int accumulate,
-    NoiseArgs nz) {
+    NoiseArgs nz, float4* __restrict__ part) {
   pdl_trigger();
   pdl_wait();
   const uint64_t seed = nz.on && nz.seed_dev ? (uint64_t)*nz.seed_dev : nz.seed;
@@ -53,7 +80,9 @@ __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
   const size_t iw = nw / 4, items = iw + (keep_b ? (size_t)p / 4 : 0);
   const int lane_item = threadIdx.x % kPer, grp = threadIdx.x / kPer;
   const size_t it = (size_t)blockIdx.x * kPer + lane_item;
-  const int eg = (B + kGroups - 1) / kGroups, e0 = grp * eg, e1 = min(B, e0 + eg);
+  // this block's examples: split blockIdx.y of gridDim.y, then group grp of kGroups
+  const int es = (B + gridDim.y - 1) / gridDim.y, sb = blockIdx.y * es, se = min(B, sb + es);
+  const int eg = (es + kGroups - 1) / kGroups, e0 = sb + grp * eg, e1 = min(se, e0 + eg);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (it < items) {
     const bool w = it < iw;
@@ -92,23 +121,29 @@ __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
       s.z += t.z;
       s.w += t.w;
     }
-    const float sv[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (it < iw) {
-        const long m = kept_pos(it * 4 + i, p, D, kk, quad);
-        if (m >= 0) {
-          float v = accumulate ? dW[m] + sv[i] : sv[i];
-          if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_a + (uint64_t)m, seed), v) * nz.invB;
-          dW[m] = v;
-        }
-      } else {
-        const size_t j = (it - iw) * 4 + i;
-        float v = accumulate ? db[j] + sv[i] : sv[i];
-        if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_b + j, seed), v) * nz.invB;
-        db[j] = v;
-      }
+    if (part) part[(size_t)blockIdx.y * items + it] = s;
+    else kept_write(it, iw, s, p, D, kk, quad, dW, db, accumulate, nz, seed);
+  }
+}
+
+// The splits' partial rows added in split order, then written as the one-launch kernel does.
+__global__ void __launch_bounds__(256) kept_wsum_finish_kernel(const float4* __restrict__ part, int splits, size_t iw,
+                                                               size_t items, int p, int D, int kk, int quad,
+                                                               float* __restrict__ dW, float* __restrict__ db,
+                                                               int accumulate, NoiseArgs nz) {
+  pdl_trigger();
+  pdl_wait();
+  const uint64_t seed = nz.on && nz.seed_dev ? (uint64_t)*nz.seed_dev : nz.seed;
+  for (size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (size_t)gridDim.x * blockDim.x) {
+    float4 s = part[it];
+    for (int k = 1; k < splits; ++k) {
+      const float4 t = part[(size_t)k * items + it];
+      s.x += t.x;
+      s.y += t.y;
+      s.z += t.z;
+      s.w += t.w;
     }
+    kept_write(it, iw, s, p, D, kk, quad, dW, db, accumulate, nz, seed);
   }
 }
 
@@ -117,20 +152,41 @@ __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
 namespace dph {
 using namespace dpk;
 
-size_t kept_sum_ws_bytes(int, int, int) { return 256; }
+// Example splits: one unless the item blocks fill less than half the SMs; then enough to
+// give about two blocks per SM, each split at least 64 examples.
+static int kept_splits(int B, int p, int D) {
+  const long blocks = (long)(((size_t)p * D / 4 + p / 4 + kPer - 1) / kPer);
+  if (blocks * 2 >= 152) return 1;
+  return (int)std::max<long>(1, std::min<long>((304 + blocks - 1) / blocks, B / 64));
+}
+
+size_t kept_sum_ws_bytes(int B, int p, int D) {
+  const int s = kept_splits(B, p, D);
+  return s > 1 ? (size_t)s * ((size_t)p * D / 4 + p / 4) * 16 : 256;
+}
 
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
                             const float* factors, float* dW, float* db, int accumulate, cudaStream_t s, bool quad,
-                            NoiseArgs* nz) {
+                            NoiseArgs* nz, void* ws) {
   if (((size_t)p * D) % 4 || p % 4) return cudaErrorInvalidValue;
   const bool bias = db && keep_b;
   const size_t nw = (size_t)p * D;
   const size_t items = nw / 4 + (bias ? (size_t)p / 4 : 0);
   NoiseArgs none = {};
   const NoiseArgs& na = nz && nz->on ? *nz : none;
-  launch_pdl(kept_wsum_direct_kernel, (unsigned)((items + kPer - 1) / kPer), kPer * kGroups, 0, s, keep,
-             bias ? keep_b : nullptr, factors, B, nw, p, D, conv_kk, quad ? 1 : 0, dW, db, accumulate, na);
-  const cudaError_t e = cudaGetLastError();
+  const int splits = kept_splits(B, p, D);
+  float4* part = splits > 1 ? static_cast<float4*>(ws) : nullptr;
+  if (splits > 1 && !ws) return cudaErrorInvalidValue;
+  launch_pdl(kept_wsum_direct_kernel, dim3((unsigned)((items + kPer - 1) / kPer), (unsigned)splits), kPer * kGroups,
+             0, s, keep, bias ? keep_b : nullptr, factors, B, nw, p, D, conv_kk, quad ? 1 : 0, dW, db, accumulate, na,
+             part);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess && splits > 1) {
+    const unsigned blocks = (unsigned)std::min<size_t>((items + 255) / 256, 152 * 4);
+    launch_pdl(kept_wsum_finish_kernel, blocks, 256, 0, s, (const float4*)part, splits, nw / 4, items, p, D, conv_kk,
+               quad ? 1 : 0, dW, db, accumulate, na);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess && nz && nz->on) {
     nz->applied_a = 1;
     nz->applied_b = bias ? 1 : nz->applied_b;

@@ -37,7 +37,7 @@ cudaError_t launch_tc_inst(const Geom& g, const void* A, const void* G, float* o
 size_t kept_sum_ws_bytes(int B, int p, int D);
 cudaError_t launch_kept_sum(int B, int p, int D, int conv_kk, const float* keep, const float* keep_b,
                             const float* factors, float* dW, float* db, int accumulate, cudaStream_t s,
-                            bool quad = false, dpk::NoiseArgs* nz = nullptr);
+                            bool quad = false, dpk::NoiseArgs* nz = nullptr, void* ws = nullptr);
 // Diagnostic: one kernel whose bounded wait runs out (timeout status, TMEM released).
 cudaError_t launch_selftest_wait(unsigned* status, unsigned long long* waited_ns, cudaStream_t s);
 // Stride-1 "same" conv layers over 64 input channels: every filter tap a shifted view of one
