@@ -21,7 +21,8 @@
 // One CTA per (128-output tile, example split); per example one MMA chain of M = 128 (the
 // outputs; rows past p read zeros), N = D + bias rounded up to 16, K = the example's pixels,
 // into one of four TMEM buffers.
-// Roles (384 threads): warp 0 loads the examples' inputs (TMA, one box per example), warp 1
+// Roles (384 threads): warp 0 loads the examples' inputs (TMA, one box per example, or 16-byte
+// vectors scattered to channels-first rows), warp 1
 // issues the MMAs, warps 2, 3, 8-11 (the builders) take the 64-pixel chunks in turn: each
 // copies its chunk's G block into the ring with cp.async and forms U^T next to it while the
 // copies land (a stream of 128-byte rows through the SM's one TMA queue was measured to move
@@ -50,7 +51,6 @@ constexpr int NBUF = 4;                       // TMEM buffers, 64 columns apart
 constexpr int kThreads = 384;
 constexpr int kBuilders = 6;                  // warps 2, 3, 8, 9, 10, 11
 constexpr int kBT = 32 * kBuilders;
-constexpr int XV = (XMAXE / 8 + kBT - 1) / kBT;   // 16-byte input vectors per builder thread
 constexpr int kEpiFirst = 4, kEpiWarps = 4;
 constexpr int CTL = 2048;
 constexpr int SMEM = 1024 + RING + 2 * XBUF + CTL;
@@ -146,32 +146,8 @@ __device__ __forceinline__ int xdst(const Params& P, int q) {
   return (c * P.H + px / P.W) * P.XP + 8 + px % P.W;
 }
 
-// The example's input into an on-chip buffer (interior only: the pads stay zero).
-__device__ __forceinline__ void load_x_regs(const Params& P, int e, int bt, uint4 (&v)[XV]) {
-  const uint4* src = reinterpret_cast<const uint4*>(P.X + (size_t)e * P.xelems);
-  const int nv = P.xelems >> 3;
-#pragma unroll
-  for (int j = 0; j < XV; ++j) {
-    const int q = bt + j * kBT;
-    if (q < nv) v[j] = __ldg(src + q);
-  }
-}
-__device__ __forceinline__ void store_x_regs(const Params& P, __nv_bfloat16* xs, int bt, const uint4 (&v)[XV]) {
-  const int nv = P.xelems >> 3, wv = P.W >> 3;
-#pragma unroll
-  for (int j = 0; j < XV; ++j) {
-    const int q = bt + j * kBT;
-    if (q < nv) {
-      if (!P.nhwc) {
-        *reinterpret_cast<uint4*>(xs + (q / wv) * P.XP + 8 + (q % wv) * 8) = v[j];
-      } else {            // channels last: the 8 elements go to their channels' rows
-        const __nv_bfloat16* e8 = reinterpret_cast<const __nv_bfloat16*>(&v[j]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) xs[xdst(P, q * 8 + k)] = e8[k];
-      }
-    }
-  }
-}
+// The example's input into an on-chip buffer element by element (interior only: the pads
+// stay zero), when it does not come in 16-byte vectors.
 __device__ __forceinline__ void load_x_scalar(const Params& P, int e, int bt, __nv_bfloat16* xs) {
   const __nv_bfloat16* src = P.X + (size_t)e * P.xelems;
   for (int q = bt; q < P.xelems; q += kBT) xs[xdst(P, q)] = src[q];
@@ -284,6 +260,48 @@ __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mX,
     for (int q = max(0, x - 2); q < x; ++q) ptx::mbar_wait_drain(&c->xfull[q & 1], (q >> 1) & 1);
 }
 
+// Warp 0 when the input arrives in 16-byte vectors but not by TMA (channels last, or rows not
+// a multiple of 8 wide): example x's input into buffer x & 1, each vector's elements to their
+// channels' padded rows, as soon as the builders have released example x - 2; one arrival on
+// xfull once the warp's stores are done.  (The builders meeting at a barrier per example to
+// copy it themselves left most of them waiting on the slowest: VGG-11's first layer with
+// channels-last inputs ran 84 us against 56 channels first.)
+__device__ __forceinline__ void stager(const Params& P, __nv_bfloat16* xbuf0, __nv_bfloat16* xbuf1, Ctl* c, int e0,
+                                       int e1) {
+  volatile int* abort = &c->abort;
+  const int lane = threadIdx.x & 31;
+  const int nv = P.xelems >> 3, wv = P.W >> 3;
+  for (int x = 0; x < e1 - e0; ++x) {
+    const int b = x & 1;
+    const bool w = x < 2 || ptx::mbar_wait(&c->xempty[b], ((x >> 1) & 1) ^ 1, abort, P.status);
+    if (!__all_sync(0xffffffffu, w)) break;
+    __nv_bfloat16* xs = b ? xbuf1 : xbuf0;
+    const uint4* src = reinterpret_cast<const uint4*>(P.X + (size_t)(e0 + x) * P.xelems);
+    for (int q0 = 0; q0 < nv; q0 += 128) {   // four vectors in flight per lane
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = q0 + j * 32 + lane;
+        if (q < nv) v[j] = __ldg(src + q);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = q0 + j * 32 + lane;
+        if (q >= nv) continue;
+        if (!P.nhwc) {
+          *reinterpret_cast<uint4*>(xs + (q / wv) * P.XP + 8 + (q % wv) * 8) = v[j];
+        } else {
+          const __nv_bfloat16* e8 = reinterpret_cast<const __nv_bfloat16*>(&v[j]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) xs[xdst(P, q * 8 + k)] = e8[k];
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&c->xfull[b]);
+  }
+}
+
 // Per-lane unfold metadata for the fast path: this lane's column n = 4 i + lane / 8 (i < Np/4)
 // reads input position ubase[i] + h * XP + wo with h = ho + udh[i] (ubase = -1: the bias
 // column's ones, -2: a zero column).
@@ -362,9 +380,9 @@ __device__ __forceinline__ void build_chunk(const Params& P, const Ctl* c, const
 // made visible to the tensor core before the builder's one arrival on the chunk's full
 // barrier.  (Issuing a chunk's copies one chunk of the builder ahead measured slower: the
 // builder then waits for a ring slot six chunks earlier.)  The input of example x sits in
-// buffer x & 1: TMA inputs are waited for (xfull) and released per builder (xempty); otherwise
-// the builders copy it themselves, prefetched into registers one example ahead, and meet at a
-// barrier before using it.  Every builder walks every example (also after an abort, when it
+// buffer x & 1: inputs that warp 0 lands (by TMA or vector copies) are waited for (xfull) and
+// released per builder (xempty); otherwise the builders copy it element by element and meet at
+// a barrier before using it.  Every builder walks every example (also after an abort, when it
 // skips the work) so that the barrier and the release counts stay complete.
 __device__ __forceinline__ void builders(const Params& P, uint8_t* smem, __nv_bfloat16* xbuf0,
                                          __nv_bfloat16* xbuf1, Ctl* c, int e0, int e1, int m0, int bw) {
@@ -372,20 +390,17 @@ __device__ __forceinline__ void builders(const Params& P, uint8_t* smem, __nv_bf
   const int lane = threadIdx.x & 31, bt = bw * 32 + lane;
   UnitMeta um;
   unit_meta(P, c, lane, um);
-  uint4 pre[XV];
-  if (!P.xtma && P.xvec && e0 < e1) load_x_regs(P, e0, bt, pre);
+  const bool xbar = P.xtma || P.xvec;   // the input arrives through xfull / xempty (TMA or warp 0)
   for (int e = e0; e < e1; ++e) {
     const int x = e - e0;
     __nv_bfloat16* xs = (x & 1) ? xbuf1 : xbuf0;
     bool live = true;
-    if (P.xtma) {
+    if (xbar) {
       const bool w = ptx::mbar_wait(&c->xfull[x & 1], (x >> 1) & 1, abort, P.status);
       live = __all_sync(0xffffffffu, w);
     } else {
-      if (P.xvec) store_x_regs(P, xs, bt, pre);
-      else load_x_scalar(P, e, bt, xs);
+      load_x_scalar(P, e, bt, xs);
       asm volatile("bar.sync 3, %0;" ::"r"(kBT) : "memory");
-      if (P.xvec && e + 1 < e1) load_x_regs(P, e + 1, bt, pre);   // lands while this example is built
     }
     for (int u = 0; u < P.nk && live; ++u) {
       const int k = x * P.nk + u;
@@ -401,7 +416,7 @@ __device__ __forceinline__ void builders(const Params& P, uint8_t* smem, __nv_bf
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&c->full[s]);
     }
-    if (P.xtma) {
+    if (xbar) {
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&c->xempty[x & 1]);
     }
@@ -568,6 +583,7 @@ tc_unfold_kernel(const __grid_constant__ CUtensorMap mapX, Params P) {
     epilogue<kNorm>(P, c, tmem, e0, e1, m0);
   } else if (warp == 0) {
     if (P.xtma) producer(P, &mapX, smem + RING, c, e0, e1);
+    else if (P.xvec) stager(P, xbuf0, xbuf1, c, e0, e1);
   } else if (warp == 1) {
     mma_issuer(P, smem, c, tmem, e0, e1);
   } else {
