@@ -540,9 +540,8 @@ cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, fl
     Xh = const_cast<void*>(A);
     Gt = const_cast<void*>(G);
   } else {
-    cudaError_t e = launch_transpose_rows(g.B, g.H * g.W, g.Cin, A, Xh, s);   // NCHW -> NHWC
-    if (e != cudaSuccess) return e;
-    e = launch_transpose_rows(g.B, g.T, g.p, G, Gt, s);                        // [p, T] -> [T, p]
+    // NCHW -> NHWC and [p, T] -> [T, p], in one launch where both take the tiled kernel
+    const cudaError_t e = launch_transpose_rows2(g.B, g.H * g.W, g.Cin, A, Xh, g.T, g.p, G, Gt, s);
     if (e != cudaSuccess) return e;
   }
   const int ept = ghost_ept(g);
