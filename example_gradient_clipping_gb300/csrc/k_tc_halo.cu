@@ -40,7 +40,7 @@ constexpr int kEpiFirst = 4, kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kProducers = 3;                 // warps 0, 2, 3
 constexpr int MAXST = 8;
-constexpr int MAXG = 2;                       // MMAs per K step (filter-row groups of a unit)
+constexpr int MAXG = 2;                       // MMAs per K step (filter-row groups of an example)
 constexpr int CTL = 8192;
 constexpr int SMEM_MAX = 232448 - 1024;       // dynamic shared memory (+ alignment slack)
 
@@ -101,7 +101,10 @@ __device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* ba
 // Warps 0, 2 and 3 (pr = 0, 1, 2): stage k of the CTA's sequence (example k / nk, stage k % nk)
 // when k % 3 == pr: the input box (xrows padded rows from column -pad) and the G box (grows
 // output rows).  Boxes of this shape streamed at about 42 GB/s per SM from one issuing warp, 71
-// from two and near 100 from three or more, hence the three.
+// from two and near 100 from three or more, hence the three.  The slot waits go by phase
+// parity, sound while a slot's barrier is at most one phase behind: a producer's previous stage
+// k - 3 was loaded after stage k - 3 - nst was consumed, which keeps it so for nst >= 3 (the
+// planner's minimum).
 __device__ __forceinline__ void producer(const Params& P, const CUtensorMap* mX, const CUtensorMap* mG,
                                          uint8_t* smem, Ctl* c, int e0, int e1, int pr) {
   volatile int* abort = &c->abort;
