@@ -103,112 +103,145 @@ __global__ void unfold_rows_kernel(Geom g, int Dp, const __nv_bfloat16* __restri
   }
 }
 
-// Per example [p, T] -> [T, p] with 16-byte loads and stores (T % 8 == 0, p % 8 == 0),
-// through a tile of 64 rows j by tt <= 64 pixels t (tt = T rounded up to 8 when T < 64).
-// Shared tile [j][t] in 8-element chunks, chunk index XORed with (j / 8) % 8 so that both
-// the row stores and the column gathers spread over the banks.  With `scale`, every
-// value of example i is multiplied by scale[i] in fp32 and rounded to bf16 once.
-constexpr int kTT = 64;
-__global__ void transpose_rows_vec_kernel(int B, int T, int p, int tt, const __nv_bfloat16* __restrict__ G,
+// Per example [p, T] -> [T, p] (T % 8 == 0, p % 8 == 0) through registers, no shared memory.
+// A warp takes a tile of 8 * JC rows j by 8 * TQ pixels t (TQ = 4, 2 or 1 as T allows, JC =
+// 32 / TQ); each lane loads one 8 x 8 block (eight 16-byte pieces of consecutive rows),
+// transposes it with byte permutes and stores eight 16-byte pieces of consecutive pixel rows.
+// One load instruction of the warp covers 16 * TQ contiguous bytes of each of JC rows, one
+// store instruction 16 * JC contiguous bytes of each of TQ pixel rows.  With kScale, every
+// value of example i is multiplied by scale[i] in fp32 and rounded to bf16 once, and with
+// `bias_part` each tile writes the partial scale[i] * sum_t G[i, j, t] over its pixels to
+// bias_part[(i * nt + tile) * p + j] (nt pixel tiles per example).
+struct RowsJob {
+  int T, p, tq, nt, njb;                 // pixel chunks per tile, pixel tiles, row tiles
+  const __nv_bfloat16* src;
+  __nv_bfloat16* dst;
+  long units;                            // B * nt * njb warp tiles
+};
+
+__host__ __device__ __forceinline__ int rows_tile_tq(int T) { return T >= 32 ? 4 : T >= 16 ? 2 : 1; }
+
+__device__ __forceinline__ uint32_t u4_word(const uint4& q, int k) {
+  return k == 0 ? q.x : k == 1 ? q.y : k == 2 ? q.z : q.w;
+}
+
+template <bool kScale>
+__global__ void __launch_bounds__(256, kScale ? 3 : 4) transpose_rows_reg_kernel(RowsJob j0, RowsJob j1,
+                                                                    const float* __restrict__ scale,
+                                                                    float* __restrict__ bias_part) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+  for (long uu = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5; uu < j0.units + j1.units; uu += nwarps) {
+    const bool second = uu >= j0.units;
+    const RowsJob J = second ? j1 : j0;
+    const long u = second ? uu - j0.units : uu;
+    const long per = (long)J.nt * J.njb;
+    const int i = (int)(u / per);
+    const int rem = (int)(u - (long)i * per);
+    const int tb = rem / J.njb, jb = rem - tb * J.njb;     // pixel tile, row tile
+    const int tq = lane % J.tq, jc = lane / J.tq;
+    const int t = (tb * J.tq + tq) * 8, j = (jb * (32 / J.tq) + jc) * 8;
+    const bool ok = t < J.T && j < J.p;
+    const size_t base = (size_t)i * J.T * J.p;
+    uint4 a[8];
+    if (ok) {
+      const __nv_bfloat16* src = J.src + base + (size_t)j * J.T + t;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) a[r] = __ldcs(reinterpret_cast<const uint4*>(src + (size_t)r * J.T));
+    } else {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) a[r] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float sc = kScale ? __ldg(scale + i) : 1.f;
+    float bs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    __nv_bfloat16* dst = J.dst + base + (size_t)t * J.p + j;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      // pixel s of the block: channel pair (2v, 2v + 1) from rows 2v and 2v + 1, the value in
+      // the low (s even) or high half of their word s / 2
+      const uint32_t sel = (s & 1) ? 0x7632u : 0x5410u;
+      uint32_t w[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) w[v] = __byte_perm(u4_word(a[2 * v], s >> 1), u4_word(a[2 * v + 1], s >> 1), sel);
+      if (kScale) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float lo = __uint_as_float(w[v] << 16), hi = __uint_as_float(w[v] & 0xffff0000u);
+          bs[2 * v] += lo;
+          bs[2 * v + 1] += hi;
+          const __nv_bfloat162 h = __floats2bfloat162_rn(sc * lo, sc * hi);
+          w[v] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
+      if (ok) *reinterpret_cast<uint4*>(dst + (size_t)s * J.p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    if (kScale && bias_part) {
+      // the TQ lanes of one row chunk hold consecutive pixel chunks: add across them
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        for (int o = 1; o < J.tq; o <<= 1) bs[r] += __shfl_xor_sync(0xffffffffu, bs[r], o);
+      if (tq == 0 && j < J.p) {
+        float* bp = bias_part + ((size_t)i * J.nt + tb) * J.p + j;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) bp[r] = sc * bs[r];
+      }
+    }
+  }
+}
+
+// Per example [p, T] -> [T, p] for T < 8 (p % 8 == 0): one thread per (example, 8 rows
+// j0 .. j0+7), whose 8 x T values are contiguous (T 16-byte loads); each pixel's eight values
+// are picked out in registers and stored as one 16-byte piece.  Scale and bias partial (one
+// per example: bias_part[i * p + j]) as above.
+template <int T>
+__global__ void transpose_rows_few_kernel(int B, int p, const __nv_bfloat16* __restrict__ G,
                                           __nv_bfloat16* __restrict__ Gt, const float* __restrict__ scale,
                                           float* __restrict__ bias_part) {
   pdl_trigger();
   pdl_wait();
-  __shared__ __align__(16) __nv_bfloat16 s[kTT][kTT];
-  const int nt = (T + tt - 1) / tt, tp = (p + kTT - 1) / kTT;
-  const int tch = tt / 8;                                 // t chunks per tile row
-  const long units = (long)B * nt * tp;
-  for (long u = blockIdx.x; u < units; u += gridDim.x) {
-    const int i = (int)(u / ((long)nt * tp));
-    const int rem = (int)(u - (long)i * nt * tp);
-    const int t0 = (rem / tp) * tt, j0 = (rem % tp) * kTT;
-    const __nv_bfloat16* gi = G + (size_t)i * T * p;
-    for (int q = threadIdx.x; q < kTT * tch; q += blockDim.x) {
-      const int jr = q / tch, tc = q - jr * tch;          // tile row (output j), t chunk
-      const int j = j0 + jr, t = t0 + tc * 8;
-      if (j < p && t < T)
-        *reinterpret_cast<uint4*>(&s[jr][(tc ^ ((jr >> 3) & 7)) * 8]) =
-            *reinterpret_cast<const uint4*>(gi + (size_t)j * T + t);
-    }
-    __syncthreads();
-    __nv_bfloat16* go = Gt + (size_t)i * T * p;
+  const int cp = p >> 3;
+  const size_t n = (size_t)B * cp;
+  for (size_t q = blockIdx.x * (size_t)blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
+    const size_t i = q / cp;
+    const int j0 = (int)(q - i * cp) * 8;
+    const uint4* src = reinterpret_cast<const uint4*>(G + (i * p + j0) * T);
+    uint4 a[T];
+#pragma unroll
+    for (int k = 0; k < T; ++k) a[k] = __ldcs(src + k);
     const float sc = scale ? __ldg(scale + i) : 1.f;
-    for (int q = threadIdx.x; q < tt * (kTT / 8); q += blockDim.x) {
-      const int tr = q >> 3, jc = q & 7;                 // tile t, j chunk
-      const int t = t0 + tr, j = j0 + jc * 8;
-      if (t < T && j < p) {
-        __align__(16) __nv_bfloat16 v[8];
-        const int col = ((tr >> 3) ^ jc) * 8 + (tr & 7);
+    float bs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
-          v[r] = scale ? __float2bfloat16_rn(sc * __bfloat162float(s[jc * 8 + r][col])) : s[jc * 8 + r][col];
-        *reinterpret_cast<uint4*>(go + (size_t)t * p + j) = *reinterpret_cast<const uint4*>(v);
+    for (int t = 0; t < T; ++t) {
+      uint32_t w[4];
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        // value (row r, pixel t) is element r * T + t of the block: 16-byte piece / 8, word / 2, half
+        const int e0 = 2 * v * T + t, e1 = (2 * v + 1) * T + t;
+        const uint32_t x = u4_word(a[e0 >> 3], (e0 & 7) >> 1), y = u4_word(a[e1 >> 3], (e1 & 7) >> 1);
+        w[v] = __byte_perm(x, y, ((e0 & 1) ? 0x32u : 0x10u) | ((e1 & 1) ? 0x7600u : 0x5400u));
       }
-    }
-    if (bias_part && threadIdx.x < kTT) {
-      // bias partial of this (example, pixel tile): scale[i] * sum_t G[i, j, t] in fp32
-      const int jr = threadIdx.x, j = j0 + jr;
-      if (j < p) {
-        float acc = 0.f;
-        for (int tc = 0; tc < tch && t0 + tc * 8 < T; ++tc) {
-          const __nv_bfloat16* c8 = &s[jr][(tc ^ ((jr >> 3) & 7)) * 8];
+      if (scale) {
 #pragma unroll
-          for (int r = 0; r < 8; ++r) acc += __bfloat162float(c8[r]);
+        for (int v = 0; v < 4; ++v) {
+          const float lo = __uint_as_float(w[v] << 16), hi = __uint_as_float(w[v] & 0xffff0000u);
+          bs[2 * v] += lo;
+          bs[2 * v + 1] += hi;
+          const __nv_bfloat162 h = __floats2bfloat162_rn(sc * lo, sc * hi);
+          w[v] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        bias_part[((size_t)i * nt + rem / tp) * p + j] = sc * acc;
       }
+      *reinterpret_cast<uint4*>(Gt + (i * T + t) * p + j0) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    __syncthreads();
-  }
-}
-
-// Two unscaled transposes in one launch (the conv kernels' input and output-gradient copies):
-// units of the first, then of the second, through the same 64 x 64 tile as above.
-struct TransposeJob {
-  int T, p, tt;
-  const __nv_bfloat16* src;
-  __nv_bfloat16* dst;
-  long units;
-};
-__global__ void transpose_rows_vec2_kernel(int B, TransposeJob j0, TransposeJob j1) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ __align__(16) __nv_bfloat16 s[kTT][kTT];
-  for (long uu = blockIdx.x; uu < j0.units + j1.units; uu += gridDim.x) {
-    const bool second = uu >= j0.units;
-    const TransposeJob& J = second ? j1 : j0;
-    const long u = second ? uu - j0.units : uu;
-    const int nt = (J.T + J.tt - 1) / J.tt, tp = (J.p + kTT - 1) / kTT;
-    const int tch = J.tt / 8;
-    const int i = (int)(u / ((long)nt * tp));
-    const int rem = (int)(u - (long)i * nt * tp);
-    const int t0 = (rem / tp) * J.tt, jj0 = (rem % tp) * kTT;
-    const __nv_bfloat16* gi = J.src + (size_t)i * J.T * J.p;
-    for (int q = threadIdx.x; q < kTT * tch; q += blockDim.x) {
-      const int jr = q / tch, tc = q - jr * tch;
-      const int j = jj0 + jr, t = t0 + tc * 8;
-      if (j < J.p && t < J.T)
-        *reinterpret_cast<uint4*>(&s[jr][(tc ^ ((jr >> 3) & 7)) * 8]) =
-            __ldcs(reinterpret_cast<const uint4*>(gi + (size_t)j * J.T + t));
-    }
-    __syncthreads();
-    __nv_bfloat16* go = J.dst + (size_t)i * J.T * J.p;
-    for (int q = threadIdx.x; q < J.tt * (kTT / 8); q += blockDim.x) {
-      const int tr = q >> 3, jc = q & 7;
-      const int t = t0 + tr, j = jj0 + jc * 8;
-      if (t < J.T && j < J.p) {
-        __align__(16) __nv_bfloat16 v[8];
-        const int col = ((tr >> 3) ^ jc) * 8 + (tr & 7);
+    if (bias_part) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) v[r] = s[jc * 8 + r][col];
-        *reinterpret_cast<uint4*>(go + (size_t)t * J.p + j) = *reinterpret_cast<const uint4*>(v);
-      }
+      for (int r = 0; r < 8; ++r) bias_part[i * p + j0 + r] = sc * bs[r];
     }
-    __syncthreads();
   }
 }
 
-// Rows with T % 8 != 0 (p % 8 == 0): one thread per (example, 8 outputs j0 .. j0+7),
+// Rows with T % 8 != 0, T > 8 (p % 8 == 0): one thread per (example, 8 outputs j0 .. j0+7),
 // over all T pixels: gathers eight rows of G_i per pixel, one 16-byte store each.
 __global__ void transpose_rows_short_kernel(int B, int T, int p, const __nv_bfloat16* __restrict__ G,
                                             __nv_bfloat16* __restrict__ Gt, const float* __restrict__ scale,
@@ -359,11 +392,38 @@ cudaError_t launch_conv_rows(const Geom& g, const void* x, const void* G, void* 
 }
 
 int transpose_bias_parts(int B, int T) {
-  if (T % 8 == 0) {
-    const int tt = std::min(kTT, T);
-    return B * ((T + tt - 1) / tt);
-  }
+  if (T % 8 == 0) return B * ((T + 8 * rows_tile_tq(T) - 1) / (8 * rows_tile_tq(T)));
   return B;
+}
+
+static RowsJob rows_job(int B, int T, int p, const void* src, void* dst) {
+  RowsJob J;
+  J.T = T;
+  J.p = p;
+  J.tq = rows_tile_tq(T);
+  J.nt = (T + 8 * J.tq - 1) / (8 * J.tq);
+  J.njb = (p + 8 * (32 / J.tq) - 1) / (8 * (32 / J.tq));
+  J.src = static_cast<const __nv_bfloat16*>(src);
+  J.dst = static_cast<__nv_bfloat16*>(dst);
+  J.units = (long)B * J.nt * J.njb;
+  return J;
+}
+
+static void launch_rows_reg(const RowsJob& a, const RowsJob& b, const float* scale, float* bias_part, cudaStream_t s) {
+  const long warps = a.units + b.units;
+  const unsigned blocks = (unsigned)std::max<long>(1, std::min<long>((warps + 7) / 8, 152L * 16));
+  if (scale)
+    launch_plain(transpose_rows_reg_kernel<true>, blocks, 256, 0, s, a, b, scale, bias_part);
+  else
+    launch_plain(transpose_rows_reg_kernel<false>, blocks, 256, 0, s, a, b, scale, bias_part);
+}
+
+template <int T>
+static void launch_rows_few(int B, int p, const __nv_bfloat16* G, __nv_bfloat16* Gt, const float* scale,
+                            float* bias_part, cudaStream_t s) {
+  const size_t n = (size_t)B * (p / 8);
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 16);
+  launch_plain(transpose_rows_few_kernel<T>, blocks ? blocks : 1, 256, 0, s, B, p, G, Gt, scale, bias_part);
 }
 
 cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* dst, cudaStream_t s,
@@ -371,10 +431,19 @@ cudaError_t launch_transpose_rows(int B, int T, int p, const void* src, void* ds
   const auto* Gb = static_cast<const __nv_bfloat16*>(src);
   auto* Gtb = static_cast<__nv_bfloat16*>(dst);
   if (T % 8 == 0 && p % 8 == 0) {
-    const int tt = std::min(kTT, T);
-    const long units = (long)B * ((T + tt - 1) / tt) * ((p + kTT - 1) / kTT);
-    const unsigned blocks = (unsigned)std::min<long>(units, 152L * 16);
-    launch_plain(transpose_rows_vec_kernel, blocks, 256, 0, s, B, T, p, tt, Gb, Gtb, scale, bias_part);
+    RowsJob none = rows_job(B, T, p, src, dst);
+    none.units = 0;
+    launch_rows_reg(rows_job(B, T, p, src, dst), none, scale, bias_part, s);
+  } else if (p % 8 == 0 && T < 8) {
+    switch (T) {
+      case 1: launch_rows_few<1>(B, p, Gb, Gtb, scale, bias_part, s); break;
+      case 2: launch_rows_few<2>(B, p, Gb, Gtb, scale, bias_part, s); break;
+      case 3: launch_rows_few<3>(B, p, Gb, Gtb, scale, bias_part, s); break;
+      case 4: launch_rows_few<4>(B, p, Gb, Gtb, scale, bias_part, s); break;
+      case 5: launch_rows_few<5>(B, p, Gb, Gtb, scale, bias_part, s); break;
+      case 6: launch_rows_few<6>(B, p, Gb, Gtb, scale, bias_part, s); break;
+      default: launch_rows_few<7>(B, p, Gb, Gtb, scale, bias_part, s); break;
+    }
   } else if (p % 8 == 0) {
     const size_t n = (size_t)B * (p / 8);
     const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)152 * 16);
@@ -393,19 +462,7 @@ cudaError_t launch_transpose_rows2(int B, int T0, int p0, const void* src0, void
     const cudaError_t e = launch_transpose_rows(B, T0, p0, src0, dst0, s);
     return e != cudaSuccess ? e : launch_transpose_rows(B, T1, p1, src1, dst1, s);
   }
-  auto job = [&](int T, int p, const void* src, void* dst) {
-    TransposeJob J;
-    J.T = T;
-    J.p = p;
-    J.tt = std::min(kTT, T);
-    J.src = static_cast<const __nv_bfloat16*>(src);
-    J.dst = static_cast<__nv_bfloat16*>(dst);
-    J.units = (long)B * ((T + J.tt - 1) / J.tt) * ((p + kTT - 1) / kTT);
-    return J;
-  };
-  const TransposeJob a = job(T0, p0, src0, dst0), b = job(T1, p1, src1, dst1);
-  const unsigned blocks = (unsigned)std::min<long>(a.units + b.units, 152L * 16);
-  launch_plain(transpose_rows_vec2_kernel, blocks, 256, 0, s, B, a, b);
+  launch_rows_reg(rows_job(B, T0, p0, src0, dst0), rows_job(B, T1, p1, src1, dst1), nullptr, nullptr, s);
   return cudaGetLastError();
 }
 
