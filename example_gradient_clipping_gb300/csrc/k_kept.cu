@@ -9,10 +9,11 @@
 //
 // kept_wsum_direct_kernel: a block per chunk of kPer 4-element items of the per-example
 // layout, over all B examples: its kGroups thread groups sum c_i g_i over consecutive
-// example ranges in order, sixteen examples' loads in flight, then the groups' sums are added
-// in group order and written straight to their weight (or bias) positions (conv: mapping the
-// kernel's tile column order back to the weight layout) -- one launch and one read of the
-// kept gradients, no partial sums.  With nz on, each output also gets its noise and the 1/B
+// example ranges in order, eight to sixteen examples' loads in flight (two batches of eight,
+// the next issued before the current is summed), then the groups' sums are added in group
+// order, one thread per element, and written straight to their weight (or bias) positions
+// (conv: mapping the kernel's tile column order back to the weight layout) -- one launch and
+// one read of the kept gradients, no partial sums.  With nz on, each output also gets its noise and the 1/B
 // scale on the way out, z drawn at its flat index with the noise pass's arithmetic (so the
 // result is the same as the sum followed by that pass).  Small layers (fewer item blocks than
 // half the SMs: VGG-11's first conv layer has 7) split the examples over blockIdx.y as well;
@@ -45,27 +46,23 @@ __device__ __forceinline__ long kept_pos(size_t f, int p, int D, int kk, int qua
   return (long)n * D + (long)c * kk + tap;
 }
 
-// Item it's four sums (s) to their weight or bias positions, with the accumulate flag and the
-// fused noise.
-__device__ __forceinline__ void kept_write(size_t it, size_t iw, float4 s, int p, int D, int kk, int quad,
-                                           float* __restrict__ dW, float* __restrict__ db, int accumulate,
-                                           const NoiseArgs& nz, uint64_t seed) {
-  const float sv[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (it < iw) {
-      const long m = kept_pos(it * 4 + i, p, D, kk, quad);
-      if (m >= 0) {
-        float v = accumulate ? dW[m] + sv[i] : sv[i];
-        if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_a + (uint64_t)m, seed), v) * nz.invB;
-        dW[m] = v;
-      }
-    } else {
-      const size_t j = (it - iw) * 4 + i;
-      float v = accumulate ? db[j] + sv[i] : sv[i];
-      if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_b + j, seed), v) * nz.invB;
-      db[j] = v;
+// Sum v of element i (0..3) of item it to its weight or bias position, with the accumulate
+// flag and the fused noise.
+__device__ __forceinline__ void kept_write1(size_t it, int i, size_t iw, float v, int p, int D, int kk, int quad,
+                                            float* __restrict__ dW, float* __restrict__ db, int accumulate,
+                                            const NoiseArgs& nz, uint64_t seed) {
+  if (it < iw) {
+    const long m = kept_pos(it * 4 + i, p, D, kk, quad);
+    if (m >= 0) {
+      if (accumulate) v += dW[m];
+      if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_a + (uint64_t)m, seed), v) * nz.invB;
+      dW[m] = v;
     }
+  } else {
+    const size_t j = (it - iw) * 4 + i;
+    if (accumulate) v += db[j];
+    if (nz.on) v = fmaf(nz.sc, noise_z1(nz.off_b + j, seed), v) * nz.invB;
+    db[j] = v;
   }
 }
 
@@ -88,18 +85,22 @@ __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
     const bool w = it < iw;
     const float* src = w ? keep + it * 4 : keep_b + (it - iw) * 4;
     const size_t stride = w ? nw : (size_t)p;
-    for (int e = e0; e < e1; e += 16) {   // sixteen examples' loads in flight, summed in order
-      float4 v[16];
-      float c[16];
+    // examples e0 .. e1 - 1 in batches of eight, summed in example order; the next batch's
+    // loads are issued before the current batch is summed, so eight to sixteen are in flight
+    float4 va[8], vb[8];
+    float ca[8], cb[8];
+    auto load = [&](float4 (&v)[8], float (&c)[8], int e) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < 8; ++q) {
         if (e + q < e1) {
           v[q] = __ldcs(reinterpret_cast<const float4*>(src + (size_t)(e + q) * stride));
           c[q] = __ldg(factors + e + q);
         }
       }
+    };
+    auto add = [&](const float4 (&v)[8], const float (&c)[8], int e) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < 8; ++q) {
         if (e + q < e1) {
           acc.x = fmaf(c[q], v[q].x, acc.x);
           acc.y = fmaf(c[q], v[q].y, acc.y);
@@ -107,22 +108,29 @@ __global__ void __launch_bounds__(kPer * kGroups) kept_wsum_direct_kernel(
           acc.w = fmaf(c[q], v[q].w, acc.w);
         }
       }
+    };
+    if (e0 < e1) load(va, ca, e0);
+    for (int e = e0; e < e1; e += 16) {
+      if (e + 8 < e1) load(vb, cb, e + 8);
+      add(va, ca, e);
+      if (e + 16 < e1) load(va, ca, e + 16);
+      if (e + 8 < e1) add(vb, cb, e + 8);
     }
   }
   red[grp][lane_item] = acc;
   __syncthreads();
-  if (grp == 0 && it < items) {
-    float4 s = red[0][lane_item];
+  // one thread per element of the block's items: the groups' sums added in group order
+  if (threadIdx.x < 4 * kPer) {
+    const int li = threadIdx.x >> 2, i = threadIdx.x & 3;
+    const size_t iti = (size_t)blockIdx.x * kPer + li;
+    if (iti < items) {
+      const float* r = reinterpret_cast<const float*>(&red[0][0]);
+      float v = r[li * 4 + i];
 #pragma unroll
-    for (int g = 1; g < kGroups; ++g) {
-      const float4 t = red[g][lane_item];
-      s.x += t.x;
-      s.y += t.y;
-      s.z += t.z;
-      s.w += t.w;
+      for (int g = 1; g < kGroups; ++g) v += r[(g * kPer + li) * 4 + i];
+      if (part) reinterpret_cast<float*>(part + (size_t)blockIdx.y * items + iti)[i] = v;
+      else kept_write1(iti, i, iw, v, p, D, kk, quad, dW, db, accumulate, nz, seed);
     }
-    if (part) part[(size_t)blockIdx.y * items + it] = s;
-    else kept_write(it, iw, s, p, D, kk, quad, dW, db, accumulate, nz, seed);
   }
 }
 
@@ -143,7 +151,10 @@ __global__ void __launch_bounds__(256) kept_wsum_finish_kernel(const float4* __r
       s.z += t.z;
       s.w += t.w;
     }
-    kept_write(it, iw, s, p, D, kk, quad, dW, db, accumulate, nz, seed);
+    kept_write1(it, 0, iw, s.x, p, D, kk, quad, dW, db, accumulate, nz, seed);
+    kept_write1(it, 1, iw, s.y, p, D, kk, quad, dW, db, accumulate, nz, seed);
+    kept_write1(it, 2, iw, s.z, p, D, kk, quad, dW, db, accumulate, nz, seed);
+    kept_write1(it, 3, iw, s.w, p, D, kk, quad, dW, db, accumulate, nz, seed);
   }
 }
 
