@@ -74,6 +74,8 @@ def _load():
         "dp_add_noise": (c_int, [c_void, c_size, c_f, c_f, c_int, c_u64, c_u64, c_void]),
         "dp_add_noise_devseed": (c_int, [c_void, c_size, c_f, c_f, c_int, c_void, c_u64, c_void]),
         "dp_adaptive_bound": (c_int, [c_void, c_int, c_f, c_f, c_f, c_f, c_u64, c_int, c_void, c_void]),
+        "dp_adaptive_bounds": (c_int, [c_void, c_int, c_int, c_int, ctypes.POINTER(c_f), c_f, c_f, c_f, c_u64,
+                                       c_void, c_void, c_void]),
         "dp_check_status": (c_int, [c_void]),
         "dp_selftest_wait_timeout": (c_int, [c_void, c_void]),
         "dp_grads_size": (c_size, [PD]),
@@ -194,6 +196,16 @@ def dp_adaptive_bound(sqnorms, B: int, C_l2: float, alpha: float, beta: float, s
                       seed: int, layer: int, out, stream=None) -> None:
     _check(_lib.dp_adaptive_bound(_ptr(sqnorms), B, C_l2, alpha, beta, sigma_l2, seed, layer, _ptr(out),
                                   _stream(stream)))
+
+
+def dp_adaptive_bounds(sqnorms, B: int, C_l2: Sequence[float], alpha: float, beta: float, sigma_l2: float,
+                       seed: int, out, layer0: int = 0, seed_dev=None, stream=None) -> None:
+    """dp_adaptive_bound of layers layer0 .. layer0 + len(C_l2) - 1 in one launch: sqnorms
+    [L, B], out [L, 2]; with seed_dev the seed is read from that device buffer."""
+    Cs = [float(c) for c in C_l2]
+    arr = (ctypes.c_float * max(1, len(Cs)))(*Cs)
+    _check(_lib.dp_adaptive_bounds(_ptr(sqnorms), B, layer0, len(Cs), arr, alpha, beta, sigma_l2, seed,
+                                   _ptr(seed_dev), _ptr(out), _stream(stream)))
 
 
 def dp_clipped_sum_reuse(desc: LayerDesc, norm_mode: int, A, G, factors, dW, db=None, workspace=None,

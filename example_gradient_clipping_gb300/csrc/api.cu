@@ -800,9 +800,28 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
     return fail(DP_ERR_INVALID_ARG, "C_l2 > 0, finite alpha and beta, sigma_l2 >= 0 required");
   unsigned* st = status_ptr();
   if (!st) return fail(DP_ERR_CUDA, "dp_adaptive_bound: no device status word on the current device");
-  cudaError_t e = dph::launch_adaptive_bound(sqnorms, B, C_l2, alpha, beta, sigma_l2, seed, layer,
+  cudaError_t e = dph::launch_adaptive_bound(sqnorms, B, 1, &C_l2, alpha, beta, sigma_l2, seed, nullptr, layer,
                                              out, st, stream);
   if (e != cudaSuccess) return cuda_fail(e, "dp_adaptive_bound launch");
+  return ok();
+}
+
+dp_status dp_adaptive_bounds(const float* sqnorms, int B, int layer0, int L, const float* C_l2, float alpha,
+                             float beta, float sigma_l2, uint64_t seed, const unsigned long long* seed_dev,
+                             float* out, cudaStream_t stream) {
+  if (!sqnorms || !out || !C_l2) return fail(DP_ERR_INVALID_ARG, "sqnorms, C_l2 and out must be non-NULL");
+  if (B <= 0 || layer0 < 0 || L < 1 || L > 64)
+    return fail(DP_ERR_INVALID_ARG, "B=%d must be > 0, layer0=%d >= 0 and 1 <= L=%d <= 64", B, layer0, L);
+  for (int l = 0; l < L; ++l)
+    if (!(C_l2[l] > 0.f) || !std::isfinite(C_l2[l]))
+      return fail(DP_ERR_INVALID_ARG, "C_l2[%d] must be finite and > 0", l);
+  if (!std::isfinite(alpha) || !std::isfinite(beta) || !(sigma_l2 >= 0.f))
+    return fail(DP_ERR_INVALID_ARG, "finite alpha and beta, sigma_l2 >= 0 required");
+  unsigned* st = status_ptr();
+  if (!st) return fail(DP_ERR_CUDA, "dp_adaptive_bounds: no device status word on the current device");
+  cudaError_t e = dph::launch_adaptive_bound(sqnorms, B, L, C_l2, alpha, beta, sigma_l2, seed, seed_dev, layer0, out,
+                                             st, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dp_adaptive_bounds launch");
   return ok();
 }
 

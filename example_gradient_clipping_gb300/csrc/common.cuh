@@ -256,9 +256,11 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
                              uint64_t offset, const unsigned long long* seed_dev, cudaStream_t s);
 cudaError_t launch_add_noise_blocks(float* grad, const dpk::NoiseBlocks& nb, float invB, uint64_t seed,
                                     const unsigned long long* seed_dev, cudaStream_t s);
-cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
-                                  float sigma_l2, uint64_t seed, int layer, float* out, unsigned* status,
-                                  cudaStream_t s);
+// Adaptive bounds of layers layer0 .. layer0 + L - 1 (1 <= L <= 64) in one launch: norms
+// sq [L, B], bounds C_l2 (host, L), out [L, 2]; with seed_dev the seed is read on the device.
+cudaError_t launch_adaptive_bound(const float* sq, int B, int L, const float* C_l2, float alpha, float beta,
+                                  float sigma_l2, uint64_t seed, const unsigned long long* seed_dev, int layer0,
+                                  float* out, unsigned* status, cudaStream_t s);
 // out[e] (+)= sum_k ws[k*n + e], fixed order; with nz->on also the noise of flat index
 // noff + e and the 1/B scale.
 cudaError_t launch_reduce_splits(const float* ws, int splits, size_t n, float* out, int accumulate,

@@ -267,17 +267,23 @@ __global__ void __launch_bounds__(256) add_noise_kernel(float* __restrict__ grad
 
 // ---------------------------------------------------------------------------
 // Adaptive bound ([ThreeTools] section 3): C_next = alpha/B (sum_i min(n_i, C_l2)
-// + sigma_l2 C_l2 z), C_l2_next = beta C_next.  One block; fp64 accumulation.
-__global__ void __launch_bounds__(256) adaptive_bound_kernel(const float* __restrict__ sq, int B,
-                                                             float C_l2, float alpha, float beta,
-                                                             float sigma_l2, uint64_t seed, int layer,
-                                                             float* __restrict__ out, unsigned* status) {
+// + sigma_l2 C_l2 z), C_l2_next = beta C_next.  One block per layer (layer0 + blockIdx.x,
+// norms sq[blockIdx.x * B ..], bound Cl2.C[blockIdx.x], out[2 * blockIdx.x ..]); fp64
+// accumulation; with seed_dev the seed is read from device memory.
+__global__ void __launch_bounds__(256) adaptive_bound_kernel(const float* __restrict__ sq, int B, Bounds Cl2,
+                                                             float alpha, float beta, float sigma_l2,
+                                                             uint64_t seed,
+                                                             const unsigned long long* __restrict__ seed_dev,
+                                                             int layer0, float* __restrict__ out,
+                                                             unsigned* status) {
   pdl_trigger();
   pdl_wait();
   __shared__ double part[8];
+  const float C_l2 = Cl2.C[blockIdx.x];
+  const float* sql = sq + (size_t)blockIdx.x * B;
   double acc = 0.0;
   for (int i = threadIdx.x; i < B; i += blockDim.x) {
-    const float n = sqrtf(sq[i]);
+    const float n = sqrtf(sql[i]);
     // a non-finite norm raises the status (as the clip factors do) and counts as a norm
     // at the bound, min(inf, C_l2) = C_l2
     if (!isfinite(n)) atomicOr(status, kStatusNonfinite);
@@ -290,11 +296,11 @@ __global__ void __launch_bounds__(256) adaptive_bound_kernel(const float* __rest
     double tot = 0.0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += part[w];
     float z[4];
-    const uint64_t e = (uint64_t)layer;
-    normal4(e >> 2, seed, 1u, z);
+    const uint64_t e = (uint64_t)(layer0 + (int)blockIdx.x);
+    normal4(e >> 2, seed_dev ? (uint64_t)*seed_dev : seed, 1u, z);
     const double cn = (double)alpha / (double)B * (tot + (double)sigma_l2 * (double)C_l2 * (double)z[e & 3]);
-    out[0] = (float)cn;
-    out[1] = (float)((double)beta * cn);
+    out[2 * blockIdx.x] = (float)cn;
+    out[2 * blockIdx.x + 1] = (float)((double)beta * cn);
   }
 }
 
@@ -359,10 +365,14 @@ cudaError_t launch_add_noise(float* grad, size_t n, float sc, float invB, uint64
   return cudaGetLastError();
 }
 
-cudaError_t launch_adaptive_bound(const float* sq, int B, float C_l2, float alpha, float beta,
-                                  float sigma_l2, uint64_t seed, int layer, float* out, unsigned* status,
-                                  cudaStream_t s) {
-  launch_pdl(adaptive_bound_kernel, 1, 256, 0, s, sq, B, C_l2, alpha, beta, sigma_l2, seed, layer, out, status);
+cudaError_t launch_adaptive_bound(const float* sq, int B, int L, const float* C_l2, float alpha, float beta,
+                                  float sigma_l2, uint64_t seed, const unsigned long long* seed_dev, int layer0,
+                                  float* out, unsigned* status, cudaStream_t s) {
+  if (L < 1 || L > 64) return cudaErrorInvalidValue;
+  Bounds b{};
+  for (int l = 0; l < L; ++l) b.C[l] = C_l2[l];
+  launch_pdl(adaptive_bound_kernel, (unsigned)L, 256, 0, s, sq, B, b, alpha, beta, sigma_l2, seed, seed_dev, layer0,
+             out, status);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,7 @@ from __future__ import annotations
 
 from typing import List, Optional, Sequence, Tuple
 
-from . import (DP_LINEAR, DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_adaptive_bound, dp_add_noise,
+from . import (DP_LINEAR, DP_NORM_AUTO, DP_NORM_INSTANTIATE, LayerDesc, dp_adaptive_bounds, dp_add_noise,
                dp_add_noise_blocks, dp_add_noise_devseed, dp_clip_factors,
                dp_clipped_sum, dp_clipped_sum_kept, dp_clipped_sum_kept_noised, dp_clipped_sum_noised,
                dp_clipped_sum_reuse, dp_grads_size, dp_launch_count, dp_layer_sqnorms, dp_layer_sqnorms_keep,
@@ -32,9 +32,10 @@ class ClipStep:
 
     adaptive: None, or dict(alpha, beta, sigma_l2, C_l2) -- the noisy-mean adaptive bound
     of [ThreeTools] section 3, run per layer on the step's norms right after they are
-    formed (dp_adaptive_bound; C_l2 one value or one per layer).  Layer l's next bound
-    and next norm bound land in bounds_next[l] = (C_next, C_l2_next) on the device; the
-    step's own factors use the bounds it was built with."""
+    formed (dp_adaptive_bounds: every layer in one launch; C_l2 one value or one per layer;
+    a captured step reads the noise seed from the same device buffer as the gradient noise).
+    Layer l's next bound and next norm bound land in bounds_next[l] = (C_next, C_l2_next) on
+    the device; the step's own factors use the bounds it was built with."""
 
     def __init__(self, descs: Sequence[LayerDesc], C, sigma: float, per_layer: bool = False,
                  norm_modes: Optional[Sequence[int]] = None, device: str = "cuda", keep_grads="auto",
@@ -104,14 +105,16 @@ class ClipStep:
                 ws = self.own_ws[l] if self.own_ws[l] is not None else self.workspace
                 self.chosen[l] = dp_layer_sqnorms(d, A, G, self.sqnorms[l], ws, mode=self.modes[l], stream=stream)
 
-    def adaptive_(self, seed: int = 0, stream=None) -> None:
-        """The adaptive bound of every layer from the norms just formed (no-op without one)."""
+    def adaptive_(self, seed: int = 0, seed_dev=None, stream=None) -> None:
+        """The adaptive bound of every layer from the norms just formed, all layers in one
+        launch (no-op without one); with seed_dev the seed is read from that device buffer."""
         a = self.adaptive
         if a is None:
             return
-        for l in range(len(self.descs)):
-            dp_adaptive_bound(self.sqnorms[l], self.B, a["C_l2"][l], a["alpha"], a["beta"], a["sigma_l2"], seed, l,
-                              self.bounds_next[l], stream=stream)
+        for l0 in range(0, len(self.descs), 64):
+            l1 = min(len(self.descs), l0 + 64)
+            dp_adaptive_bounds(self.sqnorms[l0:l1], self.B, a["C_l2"][l0:l1], a["alpha"], a["beta"], a["sigma_l2"],
+                               seed, self.bounds_next[l0:l1], layer0=l0, seed_dev=seed_dev, stream=stream)
 
     def factors_(self, stream=None) -> None:
         L = len(self.descs)
@@ -201,7 +204,7 @@ class ClipStep:
         n0 = dp_launch_count()
         with torch.cuda.graph(g):
             self.norms(inputs)
-            self.adaptive_()
+            self.adaptive_(seed_dev=self.seed_buf)
             self.factors_()
             self.sums_and_noise_devseed(inputs)
         self.graph_kernels = dp_launch_count() - n0

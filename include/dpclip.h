@@ -223,6 +223,19 @@ dp_status dp_adaptive_bound(const float* sqnorms, int B, float C_l2, float alpha
                             float sigma_l2, uint64_t seed, int layer, float* out,
                             cudaStream_t stream);
 
+/* dp_adaptive_bound of layers layer0 .. layer0 + L - 1 in one launch (1 <= L <= 64,
+ * [ThreeTools] section 3): the k-th of them reads sqnorms[k*B .. k*B + B - 1] (device fp32
+ * [L, B]) and its bound C_l2[k] (host array of L, each finite and > 0) and writes
+ * out[2k] = C_next, out[2k + 1] = C_l2_next (device fp32 [L, 2]); its z is element
+ * layer0 + k of noise stream 1 under the seed.  Equal, bit for bit, to L dp_adaptive_bound
+ * calls with layer = layer0 + k.  seed_dev non-NULL: the seed is read from device memory (a
+ * 64-bit value) when the kernel runs, seed is then ignored (for a captured step replayed
+ * with a new seed).  DP_ERR_INVALID_ARG for NULL pointers, B <= 0, layer0 < 0, L out of
+ * range or bad bounds; a non-finite norm as in dp_adaptive_bound. */
+dp_status dp_adaptive_bounds(const float* sqnorms, int B, int layer0, int L, const float* C_l2, float alpha,
+                             float beta, float sigma_l2, uint64_t seed, const unsigned long long* seed_dev,
+                             float* out, cudaStream_t stream);
+
 /* ---- A layout shared by a layer's norm and sum calls ---------------------------------
  * Conv layers on the im2col kernels work on an NHWC copy of the input, which both the norm
  * and the sum call write at the front of the workspace.  dp_clipped_sum_reuse is

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol(dp):
     lib = ctypes.CDLL(dp.LIB_PATH)
     names = _declared_symbols()
     assert {"dp_layer_sqnorms", "dp_clip_factors", "dp_clipped_sum", "dp_add_noise",
-            "dp_adaptive_bound"} <= names
+            "dp_adaptive_bound", "dp_adaptive_bounds"} <= names
     for n in sorted(names):
         assert hasattr(lib, n), n
     assert dp.dp_abi_version() == 3
@@ -140,6 +140,11 @@ def test_invalid_calls_launch_nothing(dp):
     dp.dp_add_noise(0, 1.0, 1.0, 4, 0, 0, n=0, stream=0)   # empty: no-op
     with pytest.raises(dp.DPError):
         dp.dp_adaptive_bound(16, 4, 0.0, 1.1, 2.0, 2.5, 0, 0, 16, stream=0)
+    for kw in (dict(C_l2=[]), dict(C_l2=[1.0] * 65), dict(C_l2=[1.0, 0.0]), dict(C_l2=[float("nan")]),
+               dict(C_l2=[1.0], layer0=-1)):
+        with pytest.raises(dp.DPError) as e:
+            dp.dp_adaptive_bounds(16, 4, kw.pop("C_l2"), 1.1, 2.0, 2.5, 0, 16, stream=0, **kw)
+        assert e.value.status == dp.DP_ERR_INVALID_ARG
 
 
 def test_invalid_noise_of_fused_sums_launches_nothing(dp):

@@ -152,6 +152,38 @@ def test_clip_step_fused_matches_unfused_and_oracle(lib, per_layer):
     assert rel_flat(got[1].numpy(), ref["noisy"], specs) <= TOL["bf16"]
 
 
+def test_captured_step_draws_adaptive_bound_noise_from_replay_seed(lib):
+    """A per-layer step with the adaptive bound: a graph replay with seed s gives the bounds
+    (and the gradient) of an eager run with seed s, for two seeds, and the bounds are the
+    oracle's for that seed."""
+    import torch
+    dp = lib
+    specs = (LayerSpec("a", "linear", p=40, d=72, T=30),
+             LayerSpec("b", "conv2d", p=16, Cin=8, H=6, W=6, k=3, pad=1))
+    wl = Workload(name="adaptive", B=20, layers=specs, dtype="bf16", C=1.0, sigma=0.6, seed=3, per_layer=True)
+    inputs = [workloads.layer_inputs(wl, l) for l in range(2)]
+    dev = [(to_dev(A, "bf16"), to_dev(G, "bf16")) for A, G in inputs]
+    descs = [desc_for(dp, s, wl.B, "bf16") for s in specs]
+    ad = dict(alpha=1.1, beta=2.0, sigma_l2=2.5, C_l2=[0.7, 1.3])
+    st = dp.ClipStep(descs, C=[0.5, 0.8], sigma=wl.sigma, per_layer=True, adaptive=ad)
+    eager = {}
+    for seed in (99, 7):
+        g = st.run(dev, seed=seed).clone()
+        eager[seed] = (g, st.bounds_next.clone())
+    st.capture(dev)
+    sq = st.sqnorms.cpu().numpy().astype(np.float64)
+    for seed in (99, 7):
+        g = st.replay(seed).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(g, eager[seed][0])
+        assert torch.equal(st.bounds_next, eager[seed][1])
+        for l in range(2):
+            rc, rcl2 = oracle.adaptive_bound(sq[l], ad["C_l2"][l], 1.1, 2.0, 2.5, seed, l)
+            c, cl2 = st.bounds_next[l].cpu().numpy()
+            assert c == pytest.approx(rc, rel=1e-5, abs=1e-6) and cl2 == pytest.approx(rcl2, rel=1e-5, abs=1e-6)
+    assert not torch.equal(eager[99][1], eager[7][1])
+
+
 def test_noise_blocks_equal_one_pass_per_block(lib):
     """dp_add_noise_blocks over blocks with their own bounds (misaligned offsets, neighbours
     sharing a Philox block, an empty block, a gap) equals one dp_add_noise per block, bit for

@@ -639,6 +639,33 @@ def test_adaptive_bound_matches_oracle(lib):
         assert cl2 == pytest.approx(rcl2, rel=1e-5, abs=1e-6)
 
 
+def test_adaptive_bounds_of_all_layers_in_one_launch(lib):
+    """dp_adaptive_bounds over nine layers (and over layers 64 .. 66) equals one
+    dp_adaptive_bound call per layer bit for bit and the oracle per layer; the seed read from
+    device memory gives the same values as the seed passed by value."""
+    import torch
+    rng = np.random.default_rng(5)
+    L, B = 9, 1000
+    s = (rng.random((L, B)) * rng.uniform(0.5, 20.0, (L, 1))).astype(np.float32)
+    C_l2 = [float(c) for c in rng.uniform(0.5, 4.0, L)]
+    sd = torch.tensor(s, device="cuda")
+    for layer0 in (0, 64):
+        n = L if layer0 == 0 else 3
+        out = torch.full((n, 2), float("nan"), device="cuda")
+        lib.dp_adaptive_bounds(sd[:n], B, C_l2[:n], 1.1, 2.0, 2.5, 11, out, layer0=layer0)
+        seed_dev = torch.tensor([11], dtype=torch.int64, device="cuda")
+        out_dev = torch.full((n, 2), float("nan"), device="cuda")
+        lib.dp_adaptive_bounds(sd[:n], B, C_l2[:n], 1.1, 2.0, 2.5, 999, out_dev, layer0=layer0, seed_dev=seed_dev)
+        one = torch.full((2,), float("nan"), device="cuda")
+        for k in range(n):
+            lib.dp_adaptive_bound(sd[k], B, C_l2[k], 1.1, 2.0, 2.5, 11, layer0 + k, one)
+            assert torch.equal(out[k], one), k
+            assert torch.equal(out_dev[k], one), k
+            rc, rcl2 = oracle.adaptive_bound(s[k].astype(np.float64), C_l2[k], 1.1, 2.0, 2.5, 11, layer0 + k)
+            c, cl2 = one.cpu().numpy()
+            assert c == pytest.approx(rc, rel=1e-5, abs=1e-6) and cl2 == pytest.approx(rcl2, rel=1e-5, abs=1e-6)
+
+
 def test_adaptive_bound_nonfinite_norm_raises_status(lib):
     """A non-finite norm raises DP_ERR_NONFINITE and enters the noisy mean at the bound
     (min(inf, C_l2) = C_l2): the oracle's value with that norm set to the bound."""
