@@ -291,11 +291,14 @@ class VirtualStep:
         if not b.per_layer:
             dp_add_noise(self.grad, b.sigma, b.C[0], self.examples, seed, 0, stream=stream)
         else:
+            # every layer's block with its own bound, up to 64 blocks a launch (bit-identical to
+            # one dp_add_noise per layer)
+            blocks = []
             for l, d in enumerate(b.descs):
                 p, D = b.shapes[l]
-                n = p * D + (p if d.has_bias else 0)
-                o = b.offsets[l]
-                dp_add_noise(self.grad[o:o + n], b.sigma, b.C[l], self.examples, seed, o, stream=stream)
+                blocks.append((b.offsets[l], p * D + (p if d.has_bias else 0), b.C[l]))
+            for k in range(0, len(blocks), 64):
+                dp_add_noise_blocks(self.grad, blocks[k:k + 64], b.sigma, self.examples, seed=seed, stream=stream)
         return self.grad
 
 

@@ -188,6 +188,15 @@ EDGE = [
      "bf16"),
     ("conv_rows_k1_nobias", LayerSpec("e", "conv2d", p=64, Cin=64, H=8, W=8, k=1, has_bias=False), 4, "bf16"),
     ("conv_rows_p8", LayerSpec("e", "conv2d", p=8, Cin=8, H=5, W=7, k=3, pad=1), 3, "bf16"),
+    # output-gradient row copies of every pixel count class: T = 4 and 6 (one thread per
+    # 8 x T block), 8 (a warp tile of 256 rows x 8 pixels), 24 (128 x 16, ragged), 12 (T % 8 != 0)
+    ("conv_rows_T4", LayerSpec("e", "conv2d", p=16, Cin=8, H=2, W=2, k=3, pad=1), 5, "bf16"),
+    ("conv_rows_T6_p136", LayerSpec("e", "conv2d", p=136, Cin=8, H=2, W=3, k=3, pad=1), 3, "bf16"),
+    ("conv_rows_T8_p40", LayerSpec("e", "conv2d", p=40, Cin=8, H=2, W=4, k=3, pad=1), 4, "bf16"),
+    ("conv_rows_T24", LayerSpec("e", "conv2d", p=24, Cin=8, H=4, W=6, k=3, pad=1), 3, "bf16"),
+    ("conv_rows_T12", LayerSpec("e", "conv2d", p=24, Cin=8, H=3, W=4, k=3, pad=1), 3, "bf16"),
+    ("conv_c64_2x2", LayerSpec("e", "conv2d", p=64, Cin=64, H=2, W=2, k=3, pad=1), 5, "bf16"),
+    ("conv_c128_4x4_p72", LayerSpec("e", "conv2d", p=72, Cin=128, H=4, W=4, k=3, pad=1), 3, "bf16"),
     # D = 27 padded to 32 columns in the row layout (the first VGG-11 layer's shape)
     ("conv_rows_padD", LayerSpec("e", "conv2d", p=64, Cin=9, H=12, W=12, k=3, pad=1), 4, "bf16"),
     # narrow conv layers: the unfold formed on chip (per-element gathers: Wout % 8 != 0)
