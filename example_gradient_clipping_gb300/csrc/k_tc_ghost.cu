@@ -17,7 +17,11 @@
 // are formed first, all three block pairs at once from the two row blocks loaded per K
 // step (TMEM columns 0..383), then the narrower operand Y pair by pair into columns
 // 384..511; after each Y pair the epilogue forms that pair's Hadamard sum.  The wider
-// operand's rows are loaded once instead of once per pair.
+// operand's rows are loaded once instead of once per pair.  The second row block holds
+// T - 128 rows: (linear layers) its loads cover only r1 = T - 128 rounded up to 16 rows and
+// the MMAs that take it as B run at N = r1, so the Gram tiles with block 1 on the B side have
+// r1 written columns and the (1, 1) tiles r1 rows with data (the rest of block 1's slot is
+// stale); the epilogue reads only those (the entries it skips are zero in the full tiles).
 // Packed mode (2T <= 128): one CTA takes ept = 128 / T examples whose rows are
 // consecutive in memory (2D boxes over the flattened rows), so one Gram tile holds
 // every example's Gram as a diagonal block; the epilogue adds only entries (r, s) of
@@ -53,6 +57,7 @@ struct Params {
   int conv, Wout, k, stride, pad, dil;
   int early;           // A and G are the caller's inputs: loads may start before pdl_wait
   int ksplit;          // splits of the A-Gram's K chunks (grid y, one cluster of ksplit CTAs)
+  int r1;              // dual mode: rows loaded for the second row block (16 .. 128, a multiple of 16)
 };
 
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
@@ -87,7 +92,7 @@ __device__ __forceinline__ void pair_of(int j, int nb, int& tb, int& sb) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapG,
-                Params P) {
+                const __grid_constant__ CUtensorMap mapA1, const __grid_constant__ CUtensorMap mapG1, Params P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
@@ -133,6 +138,10 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     ptx::fence_mbar_init();
     ptx::prefetch_tensormap(&mapA);
     ptx::prefetch_tensormap(&mapG);
+    if (P.r1 < BT) {
+      ptx::prefetch_tensormap(&mapA1);
+      ptx::prefetch_tensormap(&mapG1);
+    }
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
   ptx::tc_fence_before();
@@ -172,11 +181,13 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           is_a = x_is_g;
         }
         if (ptx::elect_one()) {
-          ptx::mbar_arrive_expect_tx(&full[s], TILE);
+          // block 1: its r1 rows (maps with r1-row boxes) unless it takes whole tiles
+          const bool cut = blk == 1 && P.r1 < BT;
+          ptx::mbar_arrive_expect_tx(&full[s], cut ? (uint32_t)P.r1 * BK * 2 : (uint32_t)TILE);
           if (is_a)
-            load_a_rows(P, &mapA, &full[s], smem + s * STAGE, kk, blk * BT, i, false);
+            load_a_rows(P, cut ? &mapA1 : &mapA, &full[s], smem + s * STAGE, kk, blk * BT, i, false);
           else
-            ptx::tma_load_3d(&mapG, &full[s], smem + s * STAGE, kk * BK, blk * BT, i);
+            ptx::tma_load_3d(cut ? &mapG1 : &mapG, &full[s], smem + s * STAGE, kk * BK, blk * BT, i);
         }
         __syncwarp();
         ++issued;
@@ -225,6 +236,7 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     bool live = true;
     if (dual) {
       ptx::tc_fence_after();
+      const uint32_t idesc1 = ptx::idesc_bf16_f32(BT, P.r1, 0, 0);   // B = row block 1: N = r1
       // X Grams: (X0,X0) -> cols 0, (X0,X1) -> 128, (X1,X1) -> 256
       for (int kk = 0; kk < kX && live; ++kk, k += 2) {
         const int s0 = k % STAGES, s1 = (k + 1) % STAGES;
@@ -238,8 +250,8 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           for (int u = 0; u < BK / 16; ++u) {
             const uint64_t a0 = ptx::sdesc_add(d0, u * 32), a1 = ptx::sdesc_add(d1, u * 32);
             ptx::umma_bf16(tmem, a0, a0, kIdesc, (kk | u) != 0);
-            ptx::umma_bf16(tmem + 128, a0, a1, kIdesc, (kk | u) != 0);
-            ptx::umma_bf16(tmem + 256, a1, a1, kIdesc, (kk | u) != 0);
+            ptx::umma_bf16(tmem + 128, a0, a1, idesc1, (kk | u) != 0);
+            ptx::umma_bf16(tmem + 256, a1, a1, idesc1, (kk | u) != 0);
           }
           ptx::umma_commit(&empty[s0]);
           ptx::umma_commit(&empty[s1]);
@@ -264,8 +276,8 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           if (ptx::elect_one()) {
 #pragma unroll
             for (int u = 0; u < BK / 16; ++u)
-              ptx::umma_bf16(tmem + 384, ptx::sdesc_add(da, u * 32), ptx::sdesc_add(db, u * 32), kIdesc,
-                             (kk | u) != 0);
+              ptx::umma_bf16(tmem + 384, ptx::sdesc_add(da, u * 32), ptx::sdesc_add(db, u * 32),
+                             q == 0 ? kIdesc : idesc1, (kk | u) != 0);
             ptx::umma_commit(&empty[s0]);
             if (!diag) ptx::umma_commit(&empty[s1]);
           }
@@ -334,16 +346,21 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         float h = 0.f, sg = 0.f;
         const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
         const uint32_t bx = tmem + q * 128 + lanes, by = tmem + 384 + lanes;
+        // columns the pair's MMAs wrote; rows of block 1 past r1 hold no data
+        const int cmax = q == 0 ? BT : P.r1;
+        const bool rok = q != 2 || row < P.r1;
 #pragma unroll 1
-        for (int c = 0; c < BT / 32; ++c) {
+        for (int c = 0; c < BT / 32 && c * 32 < cmax; ++c) {
           float vx[32], vy[32];
           ptx::tmem_ld32(bx + c * 32, vx);
           ptx::tmem_ld32(by + c * 32, vy);
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            h = fmaf(vx[e], vy[e], h);
-            sg += x_is_g ? vx[e] : vy[e];
+            if (rok && c * 32 + e < cmax) {
+              h = fmaf(vx[e], vy[e], h);
+              sg += x_is_g ? vx[e] : vy[e];
+            }
           }
         }
         const float wgt = q == 1 ? 2.f : 1.f;
@@ -479,8 +496,8 @@ static int ghost_ksplit(const Geom& g) {
 
 size_t tc_ghost_ws_bytes(const Geom&) { return 0; }
 
-static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtensorMap& mg, tcghost::Params P,
-                             cudaStream_t s) {
+static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtensorMap& mg, const CUtensorMap& ma1,
+                             const CUtensorMap& mg1, tcghost::Params P, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
@@ -493,7 +510,7 @@ static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtenso
   P.ksplit = ghost_ksplit(g);
   const dim3 grid(P.ept ? (g.B + P.ept - 1) / P.ept : g.B, P.ksplit);
   if (P.ksplit == 1) {
-    launch_pdl(tcghost::tc_ghost_kernel, grid, tcghost::kThreads, tcghost::SMEM, s, ma, mg, P);
+    launch_pdl(tcghost::tc_ghost_kernel, grid, tcghost::kThreads, tcghost::SMEM, s, ma, mg, ma1, mg1, P);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -510,7 +527,7 @@ static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtenso
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, tcghost::tc_ghost_kernel, ma, mg, P);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tcghost::tc_ghost_kernel, ma, mg, ma1, mg1, P);
   count_launch();
   return e;
 }
@@ -557,13 +574,15 @@ cudaError_t launch_tc_ghost_conv(const Geom& g, const void* A, const void* G, fl
     const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
     if (!encode_tmap_bf16(&mg, Gt, 3, dg, sg, box)) return cudaErrorInvalidValue;
   }
-  tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil, 0, 1};
-  return run_ghost(g, ma, mg, P, s);
+  tcghost::Params P{out, status, g.T, g.D, g.p, g.has_bias, g.B, ept, 1, g.Wout, g.k, g.stride, g.pad, g.dil, 0, 1,
+                    tcghost::BT};
+  return run_ghost(g, ma, mg, ma, mg, P, s);
 }
 
 cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* out, float* /*ws*/,
                             unsigned* status, cudaStream_t s, bool early) {
-  CUtensorMap ma, mg;
+  CUtensorMap ma, mg, ma1, mg1;
+  int r1 = tcghost::BT;
   const int ept = ghost_ept(g);
   if (ept) {   // flattened rows [B*T, width]
     const uint64_t da[2] = {(uint64_t)g.d, (uint64_t)g.B * g.T}, sa[1] = {(uint64_t)g.d * 2};
@@ -579,9 +598,16 @@ cudaError_t launch_tc_ghost(const Geom& g, const void* A, const void* G, float* 
     const uint32_t box[3] = {tcghost::BK, tcghost::BT, 1};
     if (!encode_tmap_bf16(&ma, A, 3, da, sa, box) || !encode_tmap_bf16(&mg, G, 3, dg, sg, box))
       return cudaErrorInvalidValue;
+    // two row blocks: the second one's T - 128 rows, rounded up to 16, in boxes of their own
+    if (g.T > tcghost::BT && g.T <= 2 * tcghost::BT) r1 = std::min(tcghost::BT, (g.T - tcghost::BT + 15) / 16 * 16);
+    if (r1 < tcghost::BT) {
+      const uint32_t box1[3] = {tcghost::BK, (uint32_t)r1, 1};
+      if (!encode_tmap_bf16(&ma1, A, 3, da, sa, box1) || !encode_tmap_bf16(&mg1, G, 3, dg, sg, box1))
+        return cudaErrorInvalidValue;
+    }
   }
-  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0, early ? 1 : 0, 1};
-  return run_ghost(g, ma, mg, P, s);
+  tcghost::Params P{out, status, g.T, g.d, g.p, g.has_bias, g.B, ept, 0, 0, 0, 0, 0, 0, early ? 1 : 0, 1, r1};
+  return r1 < tcghost::BT ? run_ghost(g, ma, mg, ma1, mg1, P, s) : run_ghost(g, ma, mg, ma, mg, P, s);
 }
 
 }  // namespace dph

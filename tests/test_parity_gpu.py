@@ -227,10 +227,12 @@ EDGE = [
     ("conv3d_k1_c64", LayerSpec("e", "conv3d", p=64, Cin=64, Z=3, H=8, W=8, k=1), 3, "bf16"),
     ("conv3d_c64_pad", LayerSpec("e", "conv3d", p=64, Cin=64, Z=2, H=8, W=8, k=3, pad=1), 2, "bf16"),
     ("conv3d_fp32", LayerSpec("e", "conv3d", p=6, Cin=3, Z=5, H=5, W=5, k=3, pad=1), 3, "fp32"),
-    # two row blocks (128 < T <= 256): block 1 multiplied only to its valid rows rounded to 16
+    # two row blocks (128 < T <= 256): block 1 loaded as its valid rows rounded to 16 (N = r1 on the B side)
     ("lin_ghost_dual_T129", LayerSpec("e", "linear", p=64, d=64, T=129), 2, "bf16"),
     ("lin_ghost_dual_T150", LayerSpec("e", "linear", p=72, d=200, T=150), 3, "bf16"),
     ("lin_ghost_dual_T241_wide_p", LayerSpec("e", "linear", p=264, d=96, T=241, has_bias=False), 2, "bf16"),
+    # the second row block loaded as 64 rows (T - 128 = 52): its Gram columns end at a 32-column chunk
+    ("lin_ghost_dual_T180_r64", LayerSpec("e", "linear", p=96, d=64, T=180), 3, "bf16"),
     # one row block: T just above the packed limit, batches of about half the SM count
     ("lin_ghost_slab_T65", LayerSpec("e", "linear", p=40, d=48, T=65), 5, "bf16"),
     ("lin_ghost_slab_B76", LayerSpec("e", "linear", p=64, d=72, T=128), 76, "bf16"),
