@@ -22,6 +22,9 @@
 // the MMAs that take it as B run at N = r1, so the Gram tiles with block 1 on the B side have
 // r1 written columns and the (1, 1) tiles r1 rows with data (the rest of block 1's slot is
 // stale); the epilogue reads only those (the entries it skips are zero in the full tiles).
+// Dual-mode CTAs are persistent (at most one per SM, examples blockIdx.x + n * gridDim.x): the
+// producers stream the next example's tiles while the current one's last pairs are reduced,
+// and its X Grams start once the epilogue has read the previous example's last Y pair.
 // Packed mode (2T <= 128): one CTA takes ept = 128 / T examples whose rows are
 // consecutive in memory (2D boxes over the flattened rows), so one Gram tile holds
 // every example's Gram as a diagonal block; the epilogue adds only entries (r, s) of
@@ -104,7 +107,7 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
   uint64_t* yfree = ydone + 1;            // dual mode: the epilogue has read the Y Gram
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(yfree + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(tmem_slot + 2);   // [8]
+  float* red = reinterpret_cast<float*>(tmem_slot + 2);   // [8] (dual mode: [2][8])
   float* rowbuf = red + 8;                                 // packed mode: [2][BT] per-row sums
   float* csum = rowbuf + 2 * BT;                           // K splits (rank 0): [split][example]
   uint32_t* cabort = reinterpret_cast<uint32_t*>(csum + MAXSPLIT * BT);   // [split] aborted
@@ -159,7 +162,8 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     const int pr = warp == 6 ? 1 : 0;
     int k = 0, issued = 0, last = -1;
     bool live = true;
-    if (dual) {
+    // dual mode: the CTA's examples one after another (ex = blockIdx.x, += gridDim.x)
+    for (int ex = i; dual && ex < P.B && live; ex += gridDim.x) {
       // X: both row blocks per K step; then Y: pairs (0,0), (0,1), (1,1)
       const int nunits = 2 * kX + 4 * kY;
       for (int u = 0; u < nunits && live; ++u, ++k) {
@@ -185,9 +189,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
           const bool cut = blk == 1 && P.r1 < BT;
           ptx::mbar_arrive_expect_tx(&full[s], cut ? (uint32_t)P.r1 * BK * 2 : (uint32_t)TILE);
           if (is_a)
-            load_a_rows(P, cut ? &mapA1 : &mapA, &full[s], smem + s * STAGE, kk, blk * BT, i, false);
+            load_a_rows(P, cut ? &mapA1 : &mapA, &full[s], smem + s * STAGE, kk, blk * BT, ex, false);
           else
-            ptx::tma_load_3d(cut ? &mapG1 : &mapG, &full[s], smem + s * STAGE, kk * BK, blk * BT, i);
+            ptx::tma_load_3d(cut ? &mapG1 : &mapG, &full[s], smem + s * STAGE, kk * BK, blk * BT, ex);
         }
         __syncwarp();
         ++issued;
@@ -234,9 +238,15 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     // MMA issuer (whole warp; the elected lane issues)
     int k = 0;
     bool live = true;
-    if (dual) {
+    const uint32_t idesc1 = ptx::idesc_bf16_f32(BT, P.r1, 0, 0);   // B = row block 1: N = r1
+    int qq = 0;                                                     // Y pairs issued so far
+    for (int ex = i; dual && ex < P.B && live; ex += gridDim.x) {
+      // a later example's Grams overwrite TMEM once the epilogue has read the last Y pair
+      if (qq > 0) {
+        const bool w = ptx::mbar_wait(yfree, (qq - 1) & 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) { live = false; break; }
+      }
       ptx::tc_fence_after();
-      const uint32_t idesc1 = ptx::idesc_bf16_f32(BT, P.r1, 0, 0);   // B = row block 1: N = r1
       // X Grams: (X0,X0) -> cols 0, (X0,X1) -> 128, (X1,X1) -> 256
       for (int kk = 0; kk < kX && live; ++kk, k += 2) {
         const int s0 = k % STAGES, s1 = (k + 1) % STAGES;
@@ -259,9 +269,9 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         __syncwarp();
       }
       // Y Gram of each pair into cols 384, after the epilogue read the previous one
-      for (int q = 0; q < 3 && live; ++q) {
+      for (int q = 0; q < 3 && live; ++q, ++qq) {
         if (q > 0) {
-          const bool w = ptx::mbar_wait(yfree, (q - 1) & 1, abort, P.status);
+          const bool w = ptx::mbar_wait(yfree, (qq - 1) & 1, abort, P.status);
           if (!__all_sync(0xffffffffu, w)) { live = false; break; }
           ptx::tc_fence_after();
         }
@@ -338,10 +348,16 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
     const int c_lo = packed ? row / P.T * P.T : 0, c_hi = packed ? c_lo + P.T : BT;
     float H = 0.f, S = 0.f;
     bool ok = true;
-    if (dual) {
-      for (int q = 0; q < 3; ++q) {
-        const bool w = ptx::mbar_wait(ydone, q & 1, abort, P.status);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+    // dual mode: the CTA's examples one after another; every epilogue warp passes the
+    // per-example barrier once per example, so after a failed wait it only skips the work
+    int qq = 0, el = 0;                                  // Y pairs read, examples done
+    for (int ex = i; dual && ex < P.B; ex += gridDim.x, ++el) {
+      H = 0.f;
+      S = 0.f;
+      for (int q = 0; q < 3; ++q, ++qq) {
+        if (!ok) continue;
+        const bool w = ptx::mbar_wait(ydone, qq & 1, abort, P.status);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; continue; }
         ptx::tc_fence_after();
         float h = 0.f, sg = 0.f;
         const uint32_t lanes = (uint32_t)(quarter * 32) << 16;
@@ -369,6 +385,21 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(yfree);
+      }
+      // the example's norm: the four warps' sums (two buffers: a warp may reach the next
+      // example's writes while thread 64 still reads this one's)
+      H = warp_sum(H);
+      S = warp_sum(S);
+      float* rb = red + (el & 1) * 8;
+      if (lane == 0) {
+        rb[(warp - 2) * 2] = H;
+        rb[(warp - 2) * 2 + 1] = S;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps only
+      if (threadIdx.x == 64 && ok && !*abort) {
+        float h = 0.f, sv = 0.f;
+        for (int q = 0; q < 4; ++q) { h += rb[2 * q]; sv += rb[2 * q + 1]; }
+        P.out[ex] = h + (P.has_bias ? sv : 0.f);
       }
     }
     for (int j = 0; j < npairs && !dual; ++j) {
@@ -421,7 +452,7 @@ tc_ghost_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant_
         if (P.ksplit > 1) st_cluster_f32(ptx::map_rank(ptx::smem_u32(csum + split * BT + e), 0), v);
         else P.out[ex] = v;
       }
-    } else {
+    } else if (!dual) {
       H = warp_sum(H);
       S = warp_sum(S);
       if (lane == 0) {
@@ -508,7 +539,9 @@ static cudaError_t run_ghost(const Geom& g, const CUtensorMap& ma, const CUtenso
     attr_set[dev] = true;
   }
   P.ksplit = ghost_ksplit(g);
-  const dim3 grid(P.ept ? (g.B + P.ept - 1) / P.ept : g.B, P.ksplit);
+  // two row blocks: persistent CTAs, one per SM at most (the kernel loops over examples)
+  const bool dual = !P.ept && (g.T + tcghost::BT - 1) / tcghost::BT == 2;
+  const dim3 grid(P.ept ? (g.B + P.ept - 1) / P.ept : dual ? std::min(g.B, 152) : g.B, P.ksplit);
   if (P.ksplit == 1) {
     launch_pdl(tcghost::tc_ghost_kernel, grid, tcghost::kThreads, tcghost::SMEM, s, ma, mg, ma1, mg1, P);
     return cudaGetLastError();

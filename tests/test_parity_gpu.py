@@ -233,6 +233,8 @@ EDGE = [
     ("lin_ghost_dual_T241_wide_p", LayerSpec("e", "linear", p=264, d=96, T=241, has_bias=False), 2, "bf16"),
     # the second row block loaded as 64 rows (T - 128 = 52): its Gram columns end at a 32-column chunk
     ("lin_ghost_dual_T180_r64", LayerSpec("e", "linear", p=96, d=64, T=180), 3, "bf16"),
+    # more examples than SMs: each two-block CTA takes two or three examples in turn
+    ("lin_ghost_dual_B400", LayerSpec("e", "linear", p=64, d=72, T=150), 400, "bf16"),
     # one row block: T just above the packed limit, batches of about half the SM count
     ("lin_ghost_slab_T65", LayerSpec("e", "linear", p=40, d=48, T=65), 5, "bf16"),
     ("lin_ghost_slab_B76", LayerSpec("e", "linear", p=64, d=72, T=128), 76, "bf16"),
