@@ -154,11 +154,11 @@ _DOMINANT_KERNELS = {"sums": ["tc_sumx_kernel", "tc_sum_kernel", "tc_conv_kernel
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
-def _profiled_traffic(workload, kernels, B):
-    """DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture,
-    recorded in profiles/dram_traffic.json with the hash of the kernel's source file at
-    capture time and the batch the bytes are stated for; None when there is no record, the
-    source has changed since or the batch differs."""
+def _profiled_traffic(workload, call, kernels, B):
+    """DRAM bytes (read + write) per launch of the dominant call's kernel from one ncu
+    capture, recorded in profiles/dram_traffic.json with the call, the hash of the kernel's
+    source file at capture time and the batch the bytes are stated for; None when there is no
+    record, the source has changed since or the batch differs."""
     import hashlib
     try:
         with open(TRAFFIC_FILE) as f:
@@ -166,7 +166,8 @@ def _profiled_traffic(workload, kernels, B):
     except (OSError, ValueError, KeyError):
         return None
     for r in recs:
-        if r.get("workload") != workload or r.get("kernel") not in kernels or r.get("B") != B:
+        if (r.get("workload") != workload or r.get("call") != call or r.get("kernel") not in kernels
+                or r.get("B") != B):
             continue
         src = os.path.join(ROOT, "example_gradient_clipping_gb300", "csrc", r["source"])
         try:
@@ -329,7 +330,7 @@ def roofline(wl, work, means, pk, peak_kind="burst"):
         nb = 8 * work["n_params"]
         roof = dict(bound="hbm", achieved=nb / (means[dom] * 1e-3) / 1e9, peak=pk["hbm"], unit="GB/s")
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = _profiled_traffic(wl.name, _DOMINANT_KERNELS[dom], wl.B)
+    roof["traffic"] = _profiled_traffic(wl.name, dom, _DOMINANT_KERNELS[dom], wl.B)
     roof["kernel"] = {"sums": "dp_clipped_sum", "norms": "dp_layer_sqnorms", "noise": "dp_add_noise",
                       "factors": "dp_clip_factors"}[dom]
     roof["peak_source"] = (f"{pk['src']} ({peak_kind})" if roof["bound"] == "tensor" else
