@@ -68,3 +68,27 @@ def test_bench_line_small_workload():
     d = _run(["--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--workload", "seq_linear_b64_t128"], 600)
     assert d["config"]["workload"] == "seq_linear_b64_t128" and "per_config" not in d
     assert d["e2e"]["h2d_bytes_per_step"] == 2 * 64 * 128 * 768 * 2
+
+
+def test_traffic_records_match_call_kernel_batch_and_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from a record only for the dominant call's kernel at the batch
+    the record states, while the kernel's source is the one captured; else it is null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src_dir = tmp_path / "example_gradient_clipping_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (src_dir / "k.cu").write_bytes(b"kernel source")
+    import hashlib
+    h = hashlib.sha256(b"kernel source").hexdigest()[:16]
+    rec = dict(workload="w", call="sums", kernel="kern", source="k.cu", source_sha256_16=h, B=64,
+               dram_bytes_per_launch=1234)
+    (tmp_path / "traffic.json").write_text(json.dumps({"records": [rec]}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(tmp_path / "traffic.json"))
+    assert bench._profiled_traffic("w", "sums", ["kern"], 64) == 1234
+    assert bench._profiled_traffic("w", "norms", ["kern"], 64) is None      # another call
+    assert bench._profiled_traffic("w", "sums", ["other"], 64) is None      # another kernel
+    assert bench._profiled_traffic("w", "sums", ["kern"], 128) is None      # another batch
+    assert bench._profiled_traffic("v", "sums", ["kern"], 64) is None       # another workload
+    (src_dir / "k.cu").write_bytes(b"kernel source, edited")
+    assert bench._profiled_traffic("w", "sums", ["kern"], 64) is None      # the source changed
